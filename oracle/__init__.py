@@ -1,0 +1,185 @@
+"""Python face of the oracle (oracle.c): build it with gcc and call it via ctypes.
+
+Test infrastructure only: the tests, the smoke check and the bench's CPU
+baseline use it; the product path never imports it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+
+RESIDUAL = 1
+PRENORM = 2
+
+
+class OQ(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_uint64), ("s", ctypes.c_uint64), ("b", ctypes.c_uint64),
+                ("out", ctypes.c_uint32), ("inp", ctypes.c_uint32)]
+
+
+class OLayer(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("inter", ctypes.c_int32), ("bits", ctypes.c_int32), ("flags", ctypes.c_int32),
+                ("router", ctypes.c_void_p), ("shared_gate", ctypes.c_void_p),
+                ("shared_record", ctypes.c_void_p), ("sh_gate_up", OQ), ("sh_down", OQ),
+                ("experts", ctypes.c_void_p), ("stride", ctypes.c_uint64),
+                ("gate_up", OQ), ("down", OQ)]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (OpenMP when the compiler has it)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", _SRC, "-o", _LIB + ".tmp", "-lm"]
+    try:
+        subprocess.run(base[:5] + ["-fopenmp"] + base[5:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        _lib = ctypes.CDLL(build())
+        d, i32, p = ctypes.c_double, ctypes.c_int, ctypes.c_void_p
+        _lib.oracle_bf16.restype = d
+        _lib.oracle_bf16.argtypes = [ctypes.c_uint16]
+        _lib.oracle_code_at.restype = ctypes.c_uint32
+        _lib.oracle_code_at.argtypes = [p, ctypes.c_int64, i32]
+        _lib.oracle_dequant.argtypes = [p, ctypes.POINTER(OQ), i32, p]
+        _lib.oracle_topk_softmax.argtypes = [p, i32, i32, p, p]
+        _lib.oracle_union.restype = i32
+        _lib.oracle_union.argtypes = [p, i32, p]
+        _lib.oracle_expert.argtypes = [ctypes.POINTER(OLayer), i32, p, p]
+        _lib.oracle_shared_expert.argtypes = [ctypes.POINTER(OLayer), p, p]
+        _lib.oracle_moe_layer.restype = i32
+        _lib.oracle_moe_layer.argtypes = [ctypes.POINTER(OLayer), i32, p, p, p, p, p, p, p, p, p]
+        _lib.oracle_moe_forward.argtypes = [ctypes.POINTER(OLayer), i32, i32, p, p, p, p]
+        _lib.oracle_prefill_rows.argtypes = [ctypes.POINTER(OLayer), p, p, i32, i32, p, p, p]
+        _lib.oracle_threads.restype = i32
+    return _lib
+
+
+def _ptr(a: np.ndarray | None) -> int | None:
+    return None if a is None else a.ctypes.data
+
+
+def _oq(q) -> OQ:
+    return OQ(q.w, q.s, q.b, q.out, q.inp)
+
+
+class Layer:
+    """Oracle view of a synth.Layer (keeps the numpy buffers alive)."""
+
+    def __init__(self, layer):
+        self.src = layer
+        self._keep = [layer.router, layer.records, layer.shared_gate, layer.shared_record]
+        sl = layer.shared_layout
+        self.c = OLayer(layer.hidden, layer.n_experts, layer.top_k, layer.inter, layer.bits, layer.flags,
+                        _ptr(layer.router), _ptr(layer.shared_gate), _ptr(layer.shared_record),
+                        _oq(sl.gate_up) if sl else OQ(), _oq(sl.down) if sl else OQ(),
+                        _ptr(layer.records), layer.layout.stride,
+                        _oq(layer.layout.gate_up), _oq(layer.layout.down))
+
+
+def code_at(words: np.ndarray, i: int, bits: int) -> int:
+    words = np.ascontiguousarray(words, dtype=np.uint32)
+    return int(lib().oracle_code_at(_ptr(words), i, bits))
+
+
+def bf16(bits_value: int) -> float:
+    return float(lib().oracle_bf16(bits_value))
+
+
+def dequant(record: np.ndarray, q, bits: int) -> np.ndarray:
+    record = np.ascontiguousarray(record, dtype=np.uint8)
+    W = np.empty((q.out, q.inp), dtype=np.float64)
+    lib().oracle_dequant(_ptr(record), ctypes.byref(_oq(q)), bits, _ptr(W))
+    return W
+
+
+def topk_softmax(logits: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
+    logits = np.ascontiguousarray(logits, dtype=np.float64)
+    idx = np.empty(k, dtype=np.int32)
+    w = np.empty(k, dtype=np.float64)
+    lib().oracle_topk_softmax(_ptr(logits), logits.shape[0], k, _ptr(idx), _ptr(w))
+    return idx, w
+
+
+def union(ids: np.ndarray) -> np.ndarray:
+    ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
+    u = np.empty(ids.shape[0], dtype=np.int32)
+    n = lib().oracle_union(_ptr(ids), ids.shape[0], _ptr(u))
+    return u[:n].copy()
+
+
+def expert(layer: Layer, e: int, x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty(layer.src.hidden, dtype=np.float64)
+    lib().oracle_expert(ctypes.byref(layer.c), e, _ptr(x), _ptr(y))
+    return y
+
+
+def shared_expert(layer: Layer, x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty(layer.src.hidden, dtype=np.float64)
+    lib().oracle_shared_expert(ctypes.byref(layer.c), _ptr(x), _ptr(y))
+    return y
+
+
+def moe_layer(layer: Layer, x: np.ndarray) -> dict:
+    """One layer over nb rows; returns out, moe, logits, idx, w, gamma, union, wmap."""
+    src = layer.src
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    nb = x.shape[0]
+    H, E, k = src.hidden, src.n_experts, src.top_k
+    r = dict(out=np.empty((nb, H)), moe=np.empty((nb, H)), logits=np.empty((nb, E)),
+             idx=np.empty((nb, k), dtype=np.int32), w=np.empty((nb, k)), gamma=np.empty(nb),
+             union=np.empty(64, dtype=np.int32), wmap=np.empty((4, 64)))
+    U = lib().oracle_moe_layer(ctypes.byref(layer.c), nb, _ptr(x), _ptr(r["out"]), _ptr(r["moe"]),
+                               _ptr(r["logits"]), _ptr(r["idx"]), _ptr(r["w"]), _ptr(r["gamma"]),
+                               _ptr(r["union"]), _ptr(r["wmap"]))
+    r["union"] = r["union"][:U].copy()
+    return r
+
+
+def moe_forward(layers: list[Layer], x: np.ndarray) -> dict:
+    """Stacked layers; returns out [nb][H], inputs [L][nb][H], idx [L][nb][k]."""
+    arr = (OLayer * len(layers))(*[l.c for l in layers])
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    nb, H = x.shape
+    k = layers[0].src.top_k
+    out = np.empty((nb, H))
+    inputs = np.empty((len(layers), nb, H))
+    idx = np.empty((len(layers), nb, k), dtype=np.int32)
+    lib().oracle_moe_forward(arr, len(layers), nb, _ptr(x), _ptr(out), _ptr(inputs), _ptr(idx))
+    return dict(out=out, inputs=inputs, idx=idx)
+
+
+def prefill_rows(layer: Layer, x: np.ndarray, rows, mirror: bool) -> dict:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    n = rows.shape[0]
+    H, k = layer.src.hidden, layer.src.top_k
+    out = np.empty((n, H))
+    idx = np.empty((n, k), dtype=np.int32)
+    w = np.empty((n, k))
+    lib().oracle_prefill_rows(ctypes.byref(layer.c), _ptr(x), _ptr(rows), n, int(mirror),
+                              _ptr(out), _ptr(idx), _ptr(w))
+    return dict(out=out, idx=idx, w=w)
+
+
+def threads() -> int:
+    return int(lib().oracle_threads())

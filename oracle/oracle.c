@@ -1,0 +1,384 @@
+/*
+ * oracle.c -- the oracle: a plain, slow, obviously correct CPU statement of the
+ * routed quantized mixture-of-experts step, in double precision.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path calls, links or loads
+ * this file; only the tests, the smoke check and the bench's CPU baseline do.
+ * It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it follows (pages of the qwen4_exp::gpu rustdoc and source):
+ *  - `Gpu::router_b` (struct Gpu page): router over nb rows of x, softmax over
+ *    experts, top-k.  Read here as: logits L = R x (R bf16), the k largest
+ *    logits (ties to the lower expert id, ranked in float32, the precision the
+ *    kernel decides in), weights = softmax over those k logits.
+ *  - `union_of` (gpu.rs source page): the union of the rows' experts, unique
+ *    ids in first-seen order over the row-major [nb][k] id table.
+ *  - `slot_tab` / `wmap` fields (struct Gpu page): per union slot a record
+ *    address; per row and slot the routing weight (0 when the row did not
+ *    route to that expert).
+ *  - `struct Q` and `Q::at_offset` (gpu.rs source page): an affine-quantized
+ *    projection is byte offsets of codes / scales / biases relative to its
+ *    record; 8 codes per uint32 word at 4 bits; groups of 64 codes (the
+ *    "expert width must be a multiple of the 64-code quantization group"
+ *    check in load.rs).  Weight = scale * code + bias, per 64-code group.
+ *    Codes are a little-endian bitstream per row, LSB first (3-bit codes
+ *    straddle words).
+ *  - `Gpu::experts_b` (struct Gpu page): routed experts plus the shared
+ *    expert summed per row; each expert is gate_up -> silu(gate)*up -> down.
+ *    The shared expert's scalar gate is sigmoid(shared_gate . x) -- the pages
+ *    name the gate but not its activation; sigmoid is the reading taken.
+ *  - `expert_qmm_from` (struct Gpu page): low-bit (3/2-bit) records only for
+ *    routed experts; "dense projections stay Q4", so the shared expert is 4-bit.
+ *  - `encode_block` (struct Gpu page): the block output feeds the next block
+ *    through a fused norm; stacked layers here use x_{l+1} = x_l + MoE(x^_l)
+ *    with x^ the unit-weight RMSNorm (eps 1e-6) when the layer's flags ask.
+ *
+ * Every dot product accumulates in double; results are returned as double.
+ * The bf16 "mirror" mode rounds the expert input, the dequantized weights,
+ * the activation h and the output to bf16 (nearest-even) at the points where
+ * the prefill tensor-core path stores bf16, so that path can be graded
+ * against the same rounding.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+typedef struct {
+  uint64_t w, s, b; /* byte offsets inside the record */
+  uint32_t out, inp;
+} oq_t;
+
+typedef struct {
+  int32_t hidden, n_experts, top_k, inter, bits, flags;
+  const uint16_t *router;        /* [E][H] bf16 bits */
+  const uint16_t *shared_gate;   /* [H] bf16 bits; NULL = no shared expert */
+  const uint8_t *shared_record;  /* 4-bit record of the shared expert */
+  oq_t sh_gate_up, sh_down;
+  const uint8_t *experts;        /* E records, `stride` bytes apart */
+  uint64_t stride;
+  oq_t gate_up, down;
+} oracle_layer_t;
+
+enum { ORACLE_RESIDUAL = 1, ORACLE_PRENORM = 2 };
+
+/* ------------------------------------------------------------ scalars */
+
+/* The value a bf16 bit pattern denotes (exact in double). */
+double oracle_bf16(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* Round a double to the nearest bf16 value, ties to even (via the exact
+ * float-rounding of the bit pattern; doubles here are within float range). */
+static double round_bf16(double v) {
+  float f = (float)v; /* values reaching here are exact floats or close */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u) return v;
+  uint32_t lsb = (u >> 16) & 1u;
+  u = (u + 0x7fffu + lsb) & 0xffff0000u;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
+
+/* ------------------------------------------------------------ codes */
+
+/* Code `i` of one row: bits [i*bits, i*bits+bits) of the row's bitstream,
+ * taken one bit at a time, LSB first. */
+uint32_t oracle_code_at(const uint32_t *row, int64_t i, int bits) {
+  uint32_t v = 0;
+  for (int j = 0; j < bits; j++) {
+    int64_t p = i * bits + j;
+    v |= ((row[p >> 5] >> (p & 31)) & 1u) << j;
+  }
+  return v;
+}
+
+/* Dequantize one projection into W[out][inp]: W = scale(group) * code + bias(group). */
+void oracle_dequant(const uint8_t *rec, const oq_t *q, int bits, double *W) {
+  const int64_t words_per_row = (int64_t)q->inp * bits / 32;
+  const int64_t groups = q->inp / 64;
+  const uint32_t *codes = (const uint32_t *)(rec + q->w);
+  const uint16_t *sc = (const uint16_t *)(rec + q->s);
+  const uint16_t *bi = (const uint16_t *)(rec + q->b);
+  for (int64_t o = 0; o < q->out; o++) {
+    const uint32_t *row = codes + o * words_per_row;
+    for (int64_t i = 0; i < q->inp; i++) {
+      int64_t g = i / 64;
+      double s = oracle_bf16(sc[o * groups + g]);
+      double b = oracle_bf16(bi[o * groups + g]);
+      W[o * q->inp + i] = s * (double)oracle_code_at(row, i, bits) + b;
+    }
+  }
+}
+
+/* y[out] = W x for one projection (dequantized row by row), optionally
+ * rounding each weight to bf16 first (mirror mode). */
+static void qmatvec(const uint8_t *rec, const oq_t *q, int bits, const double *x, double *y,
+                    int mirror) {
+  const int64_t words_per_row = (int64_t)q->inp * bits / 32;
+  const int64_t groups = q->inp / 64;
+  const uint32_t *codes = (const uint32_t *)(rec + q->w);
+  const uint16_t *sc = (const uint16_t *)(rec + q->s);
+  const uint16_t *bi = (const uint16_t *)(rec + q->b);
+  for (int64_t o = 0; o < q->out; o++) {
+    const uint32_t *row = codes + o * words_per_row;
+    double acc = 0.0;
+    for (int64_t i = 0; i < q->inp; i++) {
+      int64_t g = i / 64;
+      double w = oracle_bf16(sc[o * groups + g]) * (double)oracle_code_at(row, i, bits) +
+                 oracle_bf16(bi[o * groups + g]);
+      if (mirror) w = round_bf16(w);
+      acc += w * x[i];
+    }
+    y[o] = acc;
+  }
+}
+
+/* One expert on one row: gu = W_gu x (2*inter outputs: gate then up),
+ * h = silu(gate) * up, y = W_d h.  `y` has `hidden` entries. */
+static void expert_row(const uint8_t *rec, const oq_t *gu, const oq_t *dn, int bits, int inter,
+                       const double *x, double *y, int mirror) {
+  double *g = (double *)malloc(sizeof(double) * 2 * (size_t)inter);
+  double *h = (double *)malloc(sizeof(double) * (size_t)inter);
+  qmatvec(rec, gu, bits, x, g, mirror);
+  for (int i = 0; i < inter; i++) {
+    h[i] = silu(g[i]) * g[inter + i];
+    if (mirror) h[i] = round_bf16(h[i]);
+  }
+  qmatvec(rec, dn, bits, h, y, mirror);
+  free(g);
+  free(h);
+}
+
+/* Exported for the brute-force pin: expert `e` of a layer on one row. */
+void oracle_expert(const oracle_layer_t *L, int e, const double *x, double *y) {
+  expert_row(L->experts + (uint64_t)e * L->stride, &L->gate_up, &L->down, L->bits, L->inter, x, y,
+             0);
+}
+
+/* Exported for the brute-force pin: the shared expert on one row (4-bit). */
+void oracle_shared_expert(const oracle_layer_t *L, const double *x, double *y) {
+  expert_row(L->shared_record, &L->sh_gate_up, &L->sh_down, 4, L->inter, x, y, 0);
+}
+
+/* ------------------------------------------------------------ routing */
+
+/* x^ = x / sqrt(mean(x^2) + 1e-6) (unit weight). */
+static void rmsnorm(const double *x, int H, double *xn) {
+  double ss = 0.0;
+  for (int i = 0; i < H; i++) ss += x[i] * x[i];
+  double r = 1.0 / sqrt(ss / H + 1e-6);
+  for (int i = 0; i < H; i++) xn[i] = x[i] * r;
+}
+
+/* Router logits of one row: L[e] = sum_i R[e][i] x[i]. */
+static void router_row(const oracle_layer_t *L, const double *x, double *logit) {
+  for (int e = 0; e < L->n_experts; e++) {
+    double acc = 0.0;
+    const uint16_t *r = L->router + (int64_t)e * L->hidden;
+    for (int i = 0; i < L->hidden; i++) acc += oracle_bf16(r[i]) * x[i];
+    logit[e] = acc;
+  }
+}
+
+/* Top-k of one row by repeated selection of the largest remaining logit,
+ * compared as float32 (the kernel's precision), ties to the lower id; then
+ * the softmax over the k chosen logits (in double). */
+void oracle_topk_softmax(const double *logit, int E, int k, int32_t *idx, double *w) {
+  char *taken = (char *)calloc((size_t)E, 1);
+  for (int r = 0; r < k; r++) {
+    int best = -1;
+    float bv = 0.0f;
+    for (int e = 0; e < E; e++) {
+      if (taken[e]) continue;
+      float v = (float)logit[e];
+      if (best < 0 || v > bv) { /* strict: an equal later id never wins */
+        best = e;
+        bv = v;
+      }
+    }
+    taken[best] = 1;
+    idx[r] = best;
+  }
+  double m = logit[idx[0]];
+  for (int r = 1; r < k; r++)
+    if (logit[idx[r]] > m) m = logit[idx[r]];
+  double z = 0.0;
+  for (int r = 0; r < k; r++) z += exp(logit[idx[r]] - m);
+  for (int r = 0; r < k; r++) w[r] = exp(logit[idx[r]] - m) / z;
+  free(taken);
+}
+
+/* Union of ids in first-seen order (row-major over [nb][k]); returns its size. */
+int oracle_union(const int32_t *idx, int n, int32_t *uni) {
+  int u = 0;
+  for (int i = 0; i < n; i++) {
+    int seen = 0;
+    for (int j = 0; j < u; j++)
+      if (uni[j] == idx[i]) seen = 1;
+    if (!seen) uni[u++] = idx[i];
+  }
+  return u;
+}
+
+/* ------------------------------------------------------------ one layer */
+
+/* One MoE layer over nb rows.
+ *   x      [nb][H]   layer input
+ *   out    [nb][H]   layer output (MoE, plus x when the layer is RESIDUAL)
+ *   moe    [nb][H]   MoE part alone (before the residual), may be NULL
+ *   logits [nb][E], idx [nb][k], w [nb][k], gamma [nb], uni [64], wmap [4][64]:
+ *          routing results, each may be NULL.
+ * Returns the union size. */
+int oracle_moe_layer(const oracle_layer_t *L, int nb, const double *x, double *out, double *moe,
+                     double *logits, int32_t *idx, double *w, double *gamma, int32_t *uni,
+                     double *wmap) {
+  const int H = L->hidden, E = L->n_experts, k = L->top_k;
+  double *xn = (double *)malloc(sizeof(double) * (size_t)nb * H);
+  double *lg = (double *)malloc(sizeof(double) * (size_t)nb * E);
+  int32_t *id = (int32_t *)malloc(sizeof(int32_t) * (size_t)nb * k);
+  double *wt = (double *)malloc(sizeof(double) * (size_t)nb * k);
+  double *y = (double *)malloc(sizeof(double) * (size_t)H);
+  int32_t un[64];
+
+  for (int b = 0; b < nb; b++) {
+    if (L->flags & ORACLE_PRENORM)
+      rmsnorm(x + (int64_t)b * H, H, xn + (int64_t)b * H);
+    else
+      memcpy(xn + (int64_t)b * H, x + (int64_t)b * H, sizeof(double) * H);
+    router_row(L, xn + (int64_t)b * H, lg + (int64_t)b * E);
+    oracle_topk_softmax(lg + (int64_t)b * E, E, k, id + b * k, wt + b * k);
+  }
+  int U = oracle_union(id, nb * k, un);
+
+  for (int b = 0; b < nb; b++) {
+    const double *xb = xn + (int64_t)b * H;
+    double *ob = out + (int64_t)b * H;
+    for (int i = 0; i < H; i++) ob[i] = 0.0;
+    for (int r = 0; r < k; r++) {
+      oracle_expert(L, id[b * k + r], xb, y);
+      for (int i = 0; i < H; i++) ob[i] += wt[b * k + r] * y[i];
+    }
+    double gm = 0.0;
+    if (L->shared_gate) {
+      double acc = 0.0;
+      for (int i = 0; i < H; i++) acc += oracle_bf16(L->shared_gate[i]) * xb[i];
+      gm = sigmoid(acc);
+      oracle_shared_expert(L, xb, y);
+      for (int i = 0; i < H; i++) ob[i] += gm * y[i];
+    }
+    if (gamma) gamma[b] = gm;
+    if (moe) memcpy(moe + (int64_t)b * H, ob, sizeof(double) * H);
+    if (L->flags & ORACLE_RESIDUAL)
+      for (int i = 0; i < H; i++) ob[i] += x[(int64_t)b * H + i];
+  }
+
+  if (logits) memcpy(logits, lg, sizeof(double) * (size_t)nb * E);
+  if (idx) memcpy(idx, id, sizeof(int32_t) * (size_t)nb * k);
+  if (w) memcpy(w, wt, sizeof(double) * (size_t)nb * k);
+  if (uni) memcpy(uni, un, sizeof(int32_t) * (size_t)U);
+  if (wmap) {
+    for (int i = 0; i < 4 * 64; i++) wmap[i] = 0.0;
+    for (int b = 0; b < nb; b++)
+      for (int r = 0; r < k; r++)
+        for (int j = 0; j < U; j++)
+          if (un[j] == id[b * k + r]) wmap[b * 64 + j] = wt[b * k + r];
+  }
+  free(xn);
+  free(lg);
+  free(id);
+  free(wt);
+  free(y);
+  return U;
+}
+
+/* Stacked layers: x_{l+1} = layer_l(x_l).  `inputs` (may be NULL) receives
+ * each layer's input [n_layers][nb][H]; `idx` (may be NULL) receives
+ * [n_layers][nb][k]. */
+void oracle_moe_forward(const oracle_layer_t *layers, int n_layers, int nb, const double *x,
+                        double *out, double *inputs, int32_t *idx) {
+  const int H = layers[0].hidden;
+  double *cur = (double *)malloc(sizeof(double) * (size_t)nb * H);
+  double *nxt = (double *)malloc(sizeof(double) * (size_t)nb * H);
+  memcpy(cur, x, sizeof(double) * (size_t)nb * H);
+  for (int l = 0; l < n_layers; l++) {
+    if (inputs) memcpy(inputs + (int64_t)l * nb * H, cur, sizeof(double) * (size_t)nb * H);
+    oracle_moe_layer(&layers[l], nb, cur, nxt, NULL, NULL,
+                     idx ? idx + (int64_t)l * nb * layers[l].top_k : NULL, NULL, NULL, NULL, NULL);
+    double *t = cur;
+    cur = nxt;
+    nxt = t;
+  }
+  memcpy(out, cur, sizeof(double) * (size_t)nb * H);
+  free(cur);
+  free(nxt);
+}
+
+/* ------------------------------------------------------------ prefill rows */
+
+/* Independent rows of a prefill chunk (one layer).  For each listed row:
+ * route in double, then evaluate the experts either exactly (mirror = 0) or
+ * with bf16 rounding of x^, W, h and the output (mirror = 1).  Rows are
+ * independent, so they are spread over host threads.
+ *   x [t][H] float32; rows [n]; out [n][H]; idx [n][k]; w [n][k]. */
+void oracle_prefill_rows(const oracle_layer_t *L, const float *x, const int64_t *rows, int n,
+                         int mirror, double *out, int32_t *idx, double *w) {
+  const int H = L->hidden, E = L->n_experts, k = L->top_k;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int n_i = 0; n_i < n; n_i++) {
+    double *xb = (double *)malloc(sizeof(double) * H);
+    double *xe = (double *)malloc(sizeof(double) * H);
+    double *lg = (double *)malloc(sizeof(double) * E);
+    double *y = (double *)malloc(sizeof(double) * H);
+    int32_t *id = idx + (int64_t)n_i * k;
+    double *wt = w + (int64_t)n_i * k;
+    double *ob = out + (int64_t)n_i * H;
+    const float *xr = x + rows[n_i] * H;
+    for (int i = 0; i < H; i++) xb[i] = xr[i];
+    if (L->flags & ORACLE_PRENORM) rmsnorm(xb, H, xb);
+    router_row(L, xb, lg);
+    oracle_topk_softmax(lg, E, k, id, wt);
+    for (int i = 0; i < H; i++) xe[i] = mirror ? round_bf16(xb[i]) : xb[i];
+    for (int i = 0; i < H; i++) ob[i] = 0.0;
+    for (int r = 0; r < k; r++) {
+      expert_row(L->experts + (uint64_t)id[r] * L->stride, &L->gate_up, &L->down, L->bits,
+                 L->inter, xe, y, mirror);
+      for (int i = 0; i < H; i++) ob[i] += wt[r] * y[i];
+    }
+    if (L->shared_gate) {
+      double acc = 0.0;
+      for (int i = 0; i < H; i++) acc += oracle_bf16(L->shared_gate[i]) * xb[i];
+      double gm = sigmoid(acc);
+      expert_row(L->shared_record, &L->sh_gate_up, &L->sh_down, 4, L->inter, xe, y, mirror);
+      for (int i = 0; i < H; i++) ob[i] += gm * y[i];
+    }
+    if (L->flags & ORACLE_RESIDUAL)
+      for (int i = 0; i < H; i++) ob[i] += xr[i];
+    if (mirror)
+      for (int i = 0; i < H; i++) ob[i] = round_bf16(ob[i]);
+    free(xb);
+    free(xe);
+    free(lg);
+    free(y);
+  }
+}
+
+/* Threads an OpenMP region here would use (1 without OpenMP). */
+int oracle_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

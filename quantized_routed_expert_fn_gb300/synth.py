@@ -1,0 +1,245 @@
+"""Seeded synthetic inputs for the routed quantized mixture-of-experts step.
+
+This module draws the workloads' random inputs and stores them in the record
+format; it holds none of the step's arithmetic (no dequantisation, no dot
+products, no routing).  Both the CUDA path's tests and the CPU oracle are fed
+from here, so it is the one module the two share.
+
+Record format (the `Q` projection of the gpu.rs source page, `struct Q`: byte
+offsets `w`/`s`/`b` of codes, scales and biases inside one buffer, plus `out`
+and `inp`):
+
+* codes: uint32 words, row-major `[out][inp*bits/32]`; each row is one
+  little-endian bitstream, code `i` in bits `[i*bits, i*bits+bits)`, LSB first
+  (8 codes per word at 4 bits, 16 at 2 bits; 3-bit codes straddle words);
+* scales and biases: bf16, row-major `[out][inp/64]`, one per 64-code group;
+* a routed expert record holds `gate_up` (`out = 2*inter`, rows `0..inter-1`
+  the gate, `inter..2*inter-1` the up projection, `inp = hidden`) and then
+  `down` (`out = hidden`, `inp = inter`); every tensor starts on a 256-byte
+  boundary.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+
+GROUP = 64
+ALIGN = 256
+SLOT_STRIDE = 64
+MAX_NB = 4
+
+
+def _align(n: int, a: int = ALIGN) -> int:
+    return (n + a - 1) // a * a
+
+
+def f32_to_bf16_bits(a) -> np.ndarray:
+    """Round float32 values to bf16 (nearest, ties to even); returns uint16 bits."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return u.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b) -> np.ndarray:
+    """Widen bf16 bits to the float32 values they denote."""
+    b = np.ascontiguousarray(b, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Pack integer codes `[rows][n]` (each < 2**bits) into uint32 words, LSB first."""
+    codes = np.asarray(codes)
+    rows, n = codes.shape
+    if (n * bits) % 32:
+        raise ValueError("row bit length must be a multiple of 32")
+    bitplanes = ((codes[..., None].astype(np.uint32) >> np.arange(bits, dtype=np.uint32)) & 1)
+    stream = bitplanes.reshape(rows, n * bits).astype(np.uint8)
+    packed = np.packbits(stream, axis=1, bitorder="little")
+    return packed.view("<u4").reshape(rows, n * bits // 32).astype(np.uint32)
+
+
+@dataclasses.dataclass(frozen=True)
+class QDesc:
+    """Byte offsets of one quantized projection inside its record."""
+    w: int
+    s: int
+    b: int
+    out: int
+    inp: int
+
+
+@dataclasses.dataclass(frozen=True)
+class RecordLayout:
+    bits: int
+    hidden: int
+    inter: int
+    gate_up: QDesc
+    down: QDesc
+    stride: int
+
+
+def q_bytes(out: int, inp: int, bits: int) -> tuple[int, int, int]:
+    """(code bytes, scale bytes, bias bytes) of one projection."""
+    return out * inp * bits // 8, out * (inp // GROUP) * 2, out * (inp // GROUP) * 2
+
+
+def record_layout(hidden: int, inter: int, bits: int) -> RecordLayout:
+    off = 0
+    descs = []
+    for out, inp in ((2 * inter, hidden), (hidden, inter)):
+        cw, cs, cb = q_bytes(out, inp, bits)
+        w = off
+        off = _align(off + cw)
+        s = off
+        off = _align(off + cs)
+        b = off
+        off = _align(off + cb)
+        descs.append(QDesc(w, s, b, out, inp))
+    return RecordLayout(bits, hidden, inter, descs[0], descs[1], _align(off, 4096))
+
+
+def _fill_q(rng, rec: np.ndarray, q: QDesc, bits: int, scale_lo: float, scale_hi: float,
+            bias_noise: float, codes=None) -> None:
+    n_rec = rec.shape[0]
+    cw, cs, _ = q_bytes(q.out, q.inp, bits)
+    if codes is None:
+        # i.i.d. uniform codes packed LSB first form i.i.d. uniform bits, so
+        # uniform random words are exactly such a packing.
+        words = rng.integers(0, 2**32, size=(n_rec, cw // 4), dtype=np.uint64).astype(np.uint32)
+    else:
+        words = np.stack([pack_codes(c, bits).reshape(-1) for c in codes])
+    rec[:, q.w:q.w + cw] = words.view(np.uint8).reshape(n_rec, cw)
+    ng = q.out * (q.inp // GROUP)
+    scale = rng.uniform(scale_lo, scale_hi, size=(n_rec, ng)).astype(np.float32)
+    s_bits = f32_to_bf16_bits(scale)
+    s_val = bf16_bits_to_f32(s_bits).reshape(n_rec, ng)
+    bias = -float(2 ** (bits - 1)) * s_val
+    if bias_noise:
+        bias = bias + rng.normal(0.0, bias_noise, size=bias.shape).astype(np.float32)
+    b_bits = f32_to_bf16_bits(bias)
+    rec[:, q.s:q.s + cs] = s_bits.reshape(n_rec, ng).view(np.uint8)
+    rec[:, q.b:q.b + cs] = b_bits.reshape(n_rec, ng).view(np.uint8)
+
+
+def make_records(rng, n: int, layout: RecordLayout, scale_lo: float, scale_hi: float,
+                 bias_noise: float) -> np.ndarray:
+    """`n` records `[n][stride]` (uint8) with uniform codes and affine scale/bias."""
+    rec = np.zeros((n, layout.stride), dtype=np.uint8)
+    for q in (layout.gate_up, layout.down):
+        _fill_q(rng, rec, q, layout.bits, scale_lo, scale_hi, bias_noise)
+    return rec
+
+
+def make_uniform_record(layout: RecordLayout, code: int, scale_bits: int, bias_bits: int) -> np.ndarray:
+    """One record whose every code, scale and bias take the given values (hand-worked cases)."""
+    rec = np.zeros((1, layout.stride), dtype=np.uint8)
+    for q in (layout.gate_up, layout.down):
+        cw, cs, _ = q_bytes(q.out, q.inp, layout.bits)
+        words = pack_codes(np.full((q.out, q.inp), code, dtype=np.uint32), layout.bits)
+        rec[0, q.w:q.w + cw] = words.reshape(-1).view(np.uint8)
+        ng = q.out * (q.inp // GROUP)
+        rec[0, q.s:q.s + cs] = np.full(ng, scale_bits, dtype=np.uint16).view(np.uint8)
+        rec[0, q.b:q.b + cs] = np.full(ng, bias_bits, dtype=np.uint16).view(np.uint8)
+    return rec
+
+
+@dataclasses.dataclass
+class Layer:
+    """Host copy of one MoE layer's weights (all experts resident)."""
+    hidden: int
+    n_experts: int
+    top_k: int
+    inter: int
+    bits: int
+    flags: int
+    router: np.ndarray            # uint16 [E][H] bf16 bits
+    shared_gate: np.ndarray | None  # uint16 [H] bf16 bits
+    shared_record: np.ndarray | None  # uint8 [stride4] (4-bit record)
+    shared_layout: RecordLayout | None
+    records: np.ndarray           # uint8 [E][stride]
+    layout: RecordLayout
+
+
+# per-layer flags (same values as the C ABI)
+RESIDUAL = 1
+PRENORM = 2
+
+
+def make_layer(rng, hidden: int, n_experts: int, top_k: int, inter: int, bits: int = 4,
+               shared: bool = True, flags: int = 0, scale=(0.005, 0.02), bias_noise=1e-3,
+               router_std: float = 0.05, gate_std: float = 0.05,
+               shared_scale=(0.005, 0.02), shared_bias_noise=1e-3) -> Layer:
+    lay = record_layout(hidden, inter, bits)
+    router = f32_to_bf16_bits(rng.normal(0.0, router_std, size=(n_experts, hidden)).astype(np.float32))
+    records = make_records(rng, n_experts, lay, scale[0], scale[1], bias_noise)
+    sg = srec = slay = None
+    if shared:
+        slay = record_layout(hidden, inter, 4)
+        sg = f32_to_bf16_bits(rng.normal(0.0, gate_std, size=hidden).astype(np.float32))
+        srec = make_records(rng, 1, slay, shared_scale[0], shared_scale[1], shared_bias_noise)[0]
+    return Layer(hidden, n_experts, top_k, inter, bits, flags, router, sg, srec, slay, records, lay)
+
+
+def make_x(rng, nb: int, hidden: int, rho: float = 0.0) -> np.ndarray:
+    """Rows `x_b = sqrt(rho)*c + sqrt(1-rho)*z_b`, each marginally N(0,1), float32."""
+    z = rng.normal(0.0, 1.0, size=(nb, hidden))
+    if rho:
+        c = rng.normal(0.0, 1.0, size=(1, hidden))
+        z = math.sqrt(rho) * c + math.sqrt(1.0 - rho) * z
+    return z.astype(np.float32)
+
+
+# ---------------------------------------------------------------- workloads
+# The five workloads of the step, with the sizes, distributions and seeds
+# that parity tests and the bench use.
+
+CONFIGS = {
+    # one layer, nb=1, no shared expert
+    "c0": dict(hidden=256, n_experts=8, top_k=2, inter=128, bits=4, shared=False, n_layers=1, nb=1),
+    # 48 stacked layers with residual add (and unit RMSNorm before each), decode nb=1
+    "c1": dict(hidden=2048, n_experts=128, top_k=8, inter=768, bits=4, shared=True, n_layers=48, nb=1,
+               flags=RESIDUAL | PRENORM),
+    # speculative-verify batch nb=4, union of 20-40 experts
+    "c2": dict(hidden=2048, n_experts=512, top_k=10, inter=512, bits=4, shared=True, n_layers=1, nb=4),
+    # low-bit records, shape of c2
+    "c3b3": dict(hidden=2048, n_experts=512, top_k=10, inter=512, bits=3, shared=True, n_layers=1, nb=4,
+                 scale=(0.01, 0.04), bias_noise=0.0),
+    "c3b2": dict(hidden=2048, n_experts=512, top_k=10, inter=512, bits=2, shared=True, n_layers=1, nb=4,
+                 scale=(0.01, 0.04), bias_noise=0.0),
+    # prefill chunk of 4096 tokens
+    "c4": dict(hidden=2048, n_experts=512, top_k=10, inter=512, bits=4, shared=True, n_layers=1, nb=4096),
+}
+
+
+def make_config_layers(name: str, seed: int = 0, n_layers: int | None = None, **over) -> list[Layer]:
+    cfg = dict(CONFIGS[name])
+    cfg.update(over)
+    nl = n_layers if n_layers is not None else cfg["n_layers"]
+    rng = np.random.default_rng(seed)
+    layers = []
+    for _ in range(nl):
+        layers.append(make_layer(rng, cfg["hidden"], cfg["n_experts"], cfg["top_k"], cfg["inter"],
+                                 cfg["bits"], cfg["shared"], cfg.get("flags", 0),
+                                 scale=cfg.get("scale", (0.005, 0.02)),
+                                 bias_noise=cfg.get("bias_noise", 1e-3)))
+    return layers
+
+
+def zipf_router(rng, layer: Layer, s: float = 1.1, noise_std: float = 0.028) -> None:
+    """Prefill popularity: channel 0 of x is held at 1 and router column 0 carries
+    `-s*ln(rank)` for a seeded permutation of expert ranks, the rest N(0, noise_std);
+    top-k then draws experts roughly as Zipf(s) without replacement."""
+    E, H = layer.n_experts, layer.hidden
+    rank = rng.permutation(E) + 1
+    r = rng.normal(0.0, noise_std, size=(E, H)).astype(np.float32)
+    r[:, 0] = (-s * np.log(rank)).astype(np.float32)
+    layer.router = f32_to_bf16_bits(r)
+
+
+def make_prefill_x(rng, t: int, hidden: int) -> np.ndarray:
+    x = rng.normal(0.0, 1.0, size=(t, hidden)).astype(np.float32)
+    x[:, 0] = 1.0
+    return x

@@ -1,0 +1,313 @@
+"""Pins of the oracle against facts fixed outside it: hand-written fixtures,
+closed forms, invariants, textbook routines and a dense brute force."""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+import oracle
+from quantized_routed_expert_fn_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                yield line
+
+
+# ------------------------------------------------------------------ codes
+
+def test_code_fixtures():
+    n = 0
+    for line in _golden_lines("codes.txt"):
+        bits, words, codes = (p.strip() for p in line.split(";"))
+        bits = int(bits)
+        words = np.array([int(w, 16) for w in words.split()], dtype=np.uint32)
+        codes = [int(c) for c in codes.split()]
+        got = [oracle.code_at(words, i, bits) for i in range(len(codes))]
+        assert got == codes, line
+        n += 1
+    assert n >= 6
+
+
+def test_bf16_fixtures():
+    for line in _golden_lines("bf16.txt"):
+        b, v = line.split()
+        assert oracle.bf16(int(b, 16)) == float(v)
+
+
+@pytest.mark.parametrize("bits", [4, 3, 2])
+def test_pack_unpack_every_code_every_position(bits):
+    """Every code value at every position of a 64-code group survives the
+    generator's packing and the oracle's unpacking."""
+    n = 64
+    vals = 1 << bits
+    codes = np.array([[(i + r) % vals for i in range(n)] for r in range(vals)], dtype=np.uint32)
+    words = synth.pack_codes(codes, bits)
+    assert words.shape == (vals, n * bits // 32)
+    for r in range(vals):
+        got = [oracle.code_at(words[r], i, bits) for i in range(n)]
+        assert got == list(codes[r])
+
+
+@pytest.mark.parametrize("bits", [4, 3, 2])
+def test_dequant_endpoints(bits):
+    """Code 0 maps to the bias; the largest code to scale*(2^b-1) + bias."""
+    lay = synth.record_layout(256, 64, bits)
+    s_bits, b_bits = 0x3C00, 0xBD80  # 0.0078125, -0.0625
+    s, b = 0.0078125, -0.0625
+    for code, want in ((0, b), ((1 << bits) - 1, s * ((1 << bits) - 1) + b)):
+        rec = synth.make_uniform_record(lay, code, s_bits, b_bits)[0]
+        for q in (lay.gate_up, lay.down):
+            W = oracle.dequant(rec, q, bits)
+            assert W.shape == (q.out, q.inp)
+            assert np.all(W == want)
+
+
+def test_dequant_groups_are_64_wide():
+    """A scale change at code 64 affects exactly codes 64..127 of a row."""
+    lay = synth.record_layout(256, 64, 4)
+    rec = synth.make_uniform_record(lay, 1, 0x3F80, 0x0000)[0].copy()
+    q = lay.gate_up
+    scales = rec[q.s:q.s + q.out * (q.inp // 64) * 2].view(np.uint16)
+    scales[1] = 0x4000  # row 0, group 1 -> scale 2.0
+    W = oracle.dequant(rec, q, 4)
+    assert np.all(W[0, :64] == 1.0) and np.all(W[0, 64:128] == 2.0) and np.all(W[0, 128:] == 1.0)
+    assert np.all(W[1:] == 1.0)
+
+
+# ------------------------------------------------------------------ routing
+
+def _sorted_topk(logits, k):
+    order = sorted(range(len(logits)), key=lambda e: (-np.float32(logits[e]), e))
+    return order[:k]
+
+
+@pytest.mark.parametrize("E,k", [(8, 2), (128, 8), (512, 10), (16, 16), (5, 1)])
+def test_topk_matches_full_sort(E, k):
+    rng = np.random.default_rng(E * 31 + k)
+    for _ in range(20):
+        logits = rng.normal(0, 2, size=E)
+        idx, w = oracle.topk_softmax(logits, k)
+        assert list(idx) == _sorted_topk(logits, k)
+        assert abs(w.sum() - 1.0) < 1e-12
+        assert np.all(np.diff(w) <= 1e-15)
+
+
+def test_topk_ties_lower_id_wins():
+    logits = np.array([1.0, 3.0, 3.0, 2.0, 3.0, 0.5])
+    idx, w = oracle.topk_softmax(logits, 3)
+    assert list(idx) == [1, 2, 4]
+    assert np.allclose(w, 1.0 / 3.0, atol=0, rtol=1e-15)
+
+
+def test_softmax_reduces_to_textbook_when_k_is_e():
+    rng = np.random.default_rng(3)
+    logits = rng.normal(0, 3, size=40)
+    idx, w = oracle.topk_softmax(logits, 40)
+    ref = scipy.special.softmax(logits)
+    assert np.allclose(w, ref[idx], rtol=1e-13, atol=0)
+
+
+def test_softmax_shift_invariant_and_k1():
+    rng = np.random.default_rng(4)
+    logits = rng.normal(0, 1, size=64)
+    i1, w1 = oracle.topk_softmax(logits, 6)
+    i2, w2 = oracle.topk_softmax(logits + 17.0, 6)
+    assert list(i1) == list(i2)
+    assert np.allclose(w1, w2, rtol=1e-12, atol=0)
+    i, w = oracle.topk_softmax(logits, 1)
+    assert w[0] == 1.0 and i[0] == int(np.argmax(logits))
+
+
+def test_union_first_seen_order():
+    assert list(oracle.union(np.array([3, 1, 3, 2, 1, 7]))) == [3, 1, 2, 7]
+    assert list(oracle.union(np.array([5, 5, 5]))) == [5]
+
+
+# ------------------------------------------------------------------ expert math
+
+def _uniform_layer(H, I, E, k, code, s_bits, b_bits, shared=False):
+    lay = synth.record_layout(H, I, 4)
+    rec = synth.make_uniform_record(lay, code, s_bits, b_bits)
+    layer = synth.make_layer(np.random.default_rng(0), H, E, k, I, 4, shared=shared)
+    layer.records = np.repeat(rec, E, axis=0)
+    if shared:
+        layer.shared_record = rec[0].copy()
+    return layer
+
+
+@pytest.mark.parametrize("H,I,E,k", [(64, 64, 2, 1), (256, 128, 8, 2)])
+def test_closed_form_uniform_records(H, I, E, k):
+    """All codes q, scale sigma, bias -8 sigma: every weight is c = sigma (q-8),
+    so gate = up = c*S with S = sum(x), h = silu(cS)*cS and y = c*I*h for
+    every output; routing weights sum to 1, so out = y."""
+    sigma, q = 2.0 ** -6, 11
+    layer = _uniform_layer(H, I, E, k, q, 0x3C80, 0xBE00)  # 0.015625, -0.125
+    assert synth.bf16_bits_to_f32(np.array([0x3C80, 0xBE00], dtype=np.uint16)).tolist() == [sigma, -8 * sigma]
+    c = sigma * (q - 8)
+    x = np.random.default_rng(1).normal(size=(2, H))
+    r = oracle.moe_layer(oracle.Layer(layer), x)
+    for b in range(2):
+        S = x[b].sum()
+        g = c * S
+        want = c * I * (g / (1 + math.exp(-g))) * g
+        assert np.allclose(r["out"][b], want, rtol=1e-12, atol=1e-15)
+
+
+def test_code_eight_with_bias_minus_eight_scale_gives_zero():
+    layer = _uniform_layer(64, 64, 2, 1, 8, 0x3C80, 0xBE00)
+    x = np.random.default_rng(2).normal(size=(1, 64))
+    assert np.all(oracle.moe_layer(oracle.Layer(layer), x)["out"] == 0.0)
+
+
+def test_zero_shared_gate_weights_half():
+    """sigmoid(0) = 1/2: a zero shared-gate vector scales the shared expert by 0.5."""
+    layer = synth.make_layer(np.random.default_rng(5), 128, 4, 1, 64, 4, shared=True)
+    layer.shared_gate = np.zeros(128, dtype=np.uint16)
+    ol = oracle.Layer(layer)
+    x = np.random.default_rng(6).normal(size=(1, 128))
+    r = oracle.moe_layer(ol, x)
+    assert r["gamma"][0] == 0.5
+    y_r = oracle.expert(ol, int(r["idx"][0, 0]), x[0])
+    y_s = oracle.shared_expert(ol, x[0])
+    assert np.allclose(r["out"][0], y_r + 0.5 * y_s, rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------------------ dense brute force
+
+def _np_dequant(rec, q, bits):
+    """Independent numpy decoding: expand each row's words to a bit array, then
+    read `bits` consecutive bits per code, LSB first."""
+    words = rec[q.w:q.w + q.out * q.inp * bits // 8].view("<u4").reshape(q.out, -1)
+    shifts = np.arange(32, dtype=np.uint32)
+    bitarr = ((words[:, :, None] >> shifts) & 1).reshape(q.out, -1)
+    codes = bitarr.reshape(q.out, q.inp, bits) @ (1 << np.arange(bits))
+    ng = q.inp // 64
+    s = synth.bf16_bits_to_f32(rec[q.s:q.s + q.out * ng * 2].view(np.uint16)).astype(np.float64).reshape(q.out, ng)
+    b = synth.bf16_bits_to_f32(rec[q.b:q.b + q.out * ng * 2].view(np.uint16)).astype(np.float64).reshape(q.out, ng)
+    return np.repeat(s, 64, axis=1) * codes + np.repeat(b, 64, axis=1)
+
+
+def _np_expert(rec, lay, bits, x):
+    Wgu = _np_dequant(rec, lay.gate_up, bits)
+    Wd = _np_dequant(rec, lay.down, bits)
+    gu = Wgu @ x
+    I = lay.inter
+    h = gu[:I] * scipy.special.expit(gu[:I]) * gu[I:]
+    return Wd @ h
+
+
+@pytest.mark.parametrize("bits,shared,flags", [(4, False, 0), (4, True, 0), (3, True, 0), (2, True, 0),
+                                               (4, True, synth.RESIDUAL | synth.PRENORM)])
+def test_dense_bruteforce_all_experts_masked(bits, shared, flags):
+    """Evaluate every expert densely, weight by the full softmax masked to the
+    top-k and renormalised; must equal the oracle's routed evaluation."""
+    H, E, k, I, nb = 128, 8, 3, 64, 3
+    rng = np.random.default_rng(10 + bits)
+    layer = synth.make_layer(rng, H, E, k, I, bits, shared=shared, flags=flags)
+    x = rng.normal(size=(nb, H))
+    r = oracle.moe_layer(oracle.Layer(layer), x)
+    R = synth.bf16_bits_to_f32(layer.router).astype(np.float64)
+    for b in range(nb):
+        xb = x[b]
+        if flags & synth.PRENORM:
+            xb = xb / np.sqrt(np.mean(xb * xb) + 1e-6)
+        logits = R @ xb
+        p = scipy.special.softmax(logits)
+        top = np.argsort(-logits, kind="stable")[:k]
+        mask = np.zeros(E)
+        mask[top] = 1
+        wts = p * mask / (p * mask).sum()
+        dense = sum(wts[e] * _np_expert(layer.records[e], layer.layout, bits, xb) for e in range(E))
+        if shared:
+            sg = synth.bf16_bits_to_f32(layer.shared_gate).astype(np.float64)
+            dense = dense + scipy.special.expit(sg @ xb) * _np_expert(layer.shared_record, layer.shared_layout, 4, xb)
+        if flags & synth.RESIDUAL:
+            dense = dense + x[b]
+        assert sorted(r["idx"][b]) == sorted(top)
+        assert np.allclose(r["out"][b], dense, rtol=1e-9, atol=1e-12)
+
+
+def test_batch_rows_are_independent():
+    rng = np.random.default_rng(20)
+    layer = oracle.Layer(synth.make_layer(rng, 128, 8, 2, 64, 4))
+    x = rng.normal(size=(4, 128))
+    r4 = oracle.moe_layer(layer, x)
+    for b in range(4):
+        r1 = oracle.moe_layer(layer, x[b:b + 1])
+        assert np.array_equal(r1["out"][0], r4["out"][b])
+        assert list(r1["idx"][0]) == list(r4["idx"][b])
+
+
+def test_expert_relabeling_leaves_output_unchanged():
+    rng = np.random.default_rng(21)
+    src = synth.make_layer(rng, 128, 8, 2, 64, 4)
+    x = rng.normal(size=(2, 128))
+    r = oracle.moe_layer(oracle.Layer(src), x)
+    perm = rng.permutation(8)
+    src.router = src.router[perm].copy()
+    src.records = src.records[perm].copy()
+    rp = oracle.moe_layer(oracle.Layer(src), x)
+    assert np.allclose(r["out"], rp["out"], rtol=1e-12, atol=1e-15)
+    assert sorted(perm[rp["idx"][0]]) == sorted(r["idx"][0])
+
+
+def test_union_and_wmap_consistent():
+    rng = np.random.default_rng(22)
+    layer = oracle.Layer(synth.make_layer(rng, 128, 16, 4, 64, 4))
+    x = rng.normal(size=(4, 128))
+    r = oracle.moe_layer(layer, x)
+    U = r["union"]
+    assert len(set(U.tolist())) == len(U) == len(set(r["idx"].reshape(-1).tolist()))
+    for b in range(4):
+        assert abs(r["wmap"][b, :len(U)].sum() - 1.0) < 1e-12
+        for j, e in enumerate(U):
+            want = r["w"][b][list(r["idx"][b]).index(e)] if e in r["idx"][b] else 0.0
+            assert r["wmap"][b, j] == want
+
+
+def test_stacked_layers_compose():
+    rng = np.random.default_rng(23)
+    layers = [synth.make_layer(rng, 128, 8, 2, 64, 4, flags=synth.RESIDUAL | synth.PRENORM) for _ in range(3)]
+    ol = [oracle.Layer(l) for l in layers]
+    x = rng.normal(size=(2, 128))
+    f = oracle.moe_forward(ol, x)
+    cur = x
+    for l in range(3):
+        assert np.array_equal(f["inputs"][l], cur)
+        cur = oracle.moe_layer(ol[l], cur)["out"]
+    assert np.array_equal(f["out"], cur)
+
+
+def test_prenorm_is_scale_invariant():
+    rng = np.random.default_rng(24)
+    layer = oracle.Layer(synth.make_layer(rng, 128, 8, 2, 64, 4, flags=synth.PRENORM))
+    x = rng.normal(size=(1, 128))
+    a = oracle.moe_layer(layer, x)["out"]
+    b = oracle.moe_layer(layer, 4.0 * x)["out"]
+    # rmsnorm(4x) differs from rmsnorm(x) only through eps = 1e-6 (relative ~1e-6)
+    assert np.abs(a - b).max() <= 1e-5 * np.abs(a).max()
+
+
+def test_prefill_rows_match_layer_and_mirror_is_bf16():
+    rng = np.random.default_rng(25)
+    layer = synth.make_layer(rng, 128, 16, 4, 64, 4)
+    ol = oracle.Layer(layer)
+    x = rng.normal(size=(6, 128)).astype(np.float32)
+    rows = np.array([0, 3, 5])
+    exact = oracle.prefill_rows(ol, x, rows, mirror=False)
+    mir = oracle.prefill_rows(ol, x, rows, mirror=True)
+    ref = oracle.moe_layer(ol, x[rows].astype(np.float64))
+    assert np.allclose(exact["out"], ref["out"], rtol=1e-13, atol=1e-15)
+    assert np.array_equal(exact["idx"], ref["idx"])
+    rms = np.sqrt((exact["out"] ** 2).mean(axis=1, keepdims=True))
+    assert np.all(np.abs(mir["out"] - exact["out"]) < 3e-2 * rms)
+    m32 = mir["out"].astype(np.float32)
+    assert np.array_equal(m32.view(np.uint32) & 0xFFFF, np.zeros_like(m32, dtype=np.uint32))
