@@ -1,0 +1,296 @@
+"""Throughput of the routed quantized MoE step on GB300.
+
+Workload (default): 48 stacked MoE layers, decode nb=1 -- hidden 2048, 128
+experts, top-8, expert width 768, 4-bit g64 records, shared expert of width
+768 with a sigmoid gate, unit RMSNorm before each layer and a residual add.
+One step = one moe_forward call over all 48 layers (one persistent kernel).
+Metric: MoE-layer rows per second = nb * layers / step time; the HBM roofline
+fraction of the kernel is reported beside it.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload c1|c2|c3b3|c3b2] [--nb NB]
+
+Under torchrun each rank runs an independent replica on its own GPU (the path
+has no exchange step); value = rows of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "c1": "48 stacked MoE layers, nb=1 decode: hidden 2048, 128 experts, top-8, inter 768, shared expert "
+          "(inter 768, sigmoid gate), 4-bit g64 records, RMSNorm + residual",
+    "c2": "one MoE layer, verify batch nb=4: hidden 2048, 512 experts, top-10, inter 512, shared expert, 4-bit g64",
+    "c3b3": "one MoE layer, nb=4: hidden 2048, 512 experts, top-10, inter 512, 3-bit routed records",
+    "c3b2": "one MoE layer, nb=4: hidden 2048, 512 experts, top-10, inter 512, 2-bit routed records",
+}
+METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 1 GB300"
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"moe_clocks_{os.getpid()}.csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def layer_bytes(L, union_size: int, nb: int) -> int:
+    """Algorithmic bytes of one layer: router + shared gate + union records +
+    shared record + layer input and output."""
+    b = L.n_experts * L.hidden * 2
+    b += union_size * record_bytes(L.layout)
+    if L.shared_layout is not None:
+        b += L.hidden * 2 + record_bytes(L.shared_layout)
+    b += 2 * nb * L.hidden * 4
+    return b
+
+
+def record_bytes(lay) -> int:
+    from quantized_routed_expert_fn_gb300.synth import q_bytes
+    tot = 0
+    for q in (lay.gate_up, lay.down):
+        tot += sum(q_bytes(q.out, q.inp, lay.bits))
+    return tot
+
+
+def run_ours(args, rank, world, device):
+    import torch
+    from quantized_routed_expert_fn_gb300 import build, moe, synth
+
+    build.build()
+    moe.lib()
+    torch.cuda.set_device(device)
+    name = args.workload
+    cfg = synth.CONFIGS[name]
+    nb = args.nb or cfg["nb"]
+    layers = synth.make_device_layers(name, seed=1 + rank, device=device)
+    dl = moe.DeviceLayers(layers, device=device)
+    nl = dl.n
+    H = cfg["hidden"]
+    gen = torch.Generator(device="cpu").manual_seed(100 + rank)
+    x_host = torch.randn((nb, H), generator=gen, dtype=torch.float32)
+    if nb > 1:  # correlated rows: union of about 30 of 40 possible experts
+        c = torch.randn((1, H), generator=gen)
+        x_host = (0.55 ** 0.5) * c + (0.45 ** 0.5) * x_host
+    x = x_host.to(device)
+    out = torch.empty_like(x)
+    ws = moe.alloc_workspace(moe.forward_workspace(dl, nb), device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    slot = torch.zeros((nl, 64), dtype=torch.int64, device=device)
+    wmap = torch.zeros((nl, 4, 64), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        moe.forward(dl, x, out, ws, status, slot, wmap, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
+    unions = [int(v) for v in slot[:, 63].cpu().tolist()]
+    bytes_per_step = sum(layer_bytes(L, u, nb) for L, u in zip(layers, unions))
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as td
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3)
+    # device-timed region: inputs resident in HBM
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        td.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        td.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clocks = sampler.stop() if sampler else None
+    if status.item() != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
+
+    # end to end through the same call with host buffers: H2D of x, D2H of out
+    x_pin = x_host.pin_memory()
+    o_pin = torch.empty((nb, H), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        x.copy_(x_pin, non_blocking=True)
+        moe.forward(dl, x, out, ws, status, slot, wmap, stream=stream)
+        o_pin.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        td.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if dist:
+        td.barrier()
+
+    if dist:
+        t = torch.tensor([ms, e2e_ms], device=device)
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    rows = nb * nl * world
+    peak, peak_kind = load_peaks()
+    achieved = bytes_per_step / (ms * 1e-3) / 1e9
+    return dict(ms=ms, e2e_ms=e2e_ms, rows=rows, nb=nb, nl=nl, bytes=bytes_per_step, achieved=achieved,
+                peak=peak, peak_kind=peak_kind, clocks=clocks, unions=unions)
+
+
+def oracle_sample(name, nb, budget_s):
+    """Time the oracle (as it stands) on host cores on the first layers of the
+    same workload, drawn on the host with the same distributions."""
+    import oracle
+    from quantized_routed_expert_fn_gb300 import synth
+    cfg = synth.CONFIGS[name]
+    rng = np.random.default_rng(5)
+    x = synth.make_x(rng, nb, cfg["hidden"])
+    layers_done, t_total = 0, 0.0
+    layer_iter = 0
+    while t_total < budget_s and layer_iter < cfg["n_layers"]:
+        L = synth.make_config_layers(name, seed=1000 + layer_iter, n_layers=1)[0]
+        ol = oracle.Layer(L)
+        t0 = time.perf_counter()
+        r = oracle.moe_layer(ol, x)
+        t_total += time.perf_counter() - t0
+        x = r["out"]
+        layers_done += 1
+        layer_iter += 1
+    # the oracle's layer path is serial C: one host core
+    return dict(value=nb * layers_done / t_total, layers=layers_done, seconds=t_total, cores=1)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="c1", choices=sorted(WORKLOADS))
+    ap.add_argument("--nb", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    from quantized_routed_expert_fn_gb300 import synth
+    cfg = synth.CONFIGS[args.workload]
+    nb = args.nb or cfg["nb"]
+    config = {"workload": WORKLOADS[args.workload], "nb": nb, "layers": cfg["n_layers"],
+              "l2": "inputs larger than L2 (each step streams every layer's union records once)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        s = oracle_sample(args.workload, nb, budget_s=min(args.cpu_budget, 20.0))
+        ms = 1000.0 * nb * cfg["n_layers"] / s["value"]
+        line = {"metric": METRIC, "value": s["value"], "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config, "impl": "reference",
+                "cpu_baseline": {"value": s["value"], "unit": "rows/s", "cores": s["cores"], "kind": "oracle",
+                                 "sample": f"first {s['layers']} layers of the workload, {s['seconds']:.1f} s"},
+                "e2e": {"value": s["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+    if world > 1:
+        import torch.distributed as td
+        td.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
+    device = torch.device(f"cuda:{local}")
+    r = run_ours(args, rank, world, device)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = oracle_sample(args.workload, nb, budget_s=args.cpu_budget) if world == 1 or rank == 0 else None
+    value = r["rows"] / (r["ms"] * 1e-3)
+    e2e_value = r["rows"] / (r["e2e_ms"] * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": nb * cfg["hidden"] * 4,
+                "d2h_bytes_per_step": nb * cfg["hidden"] * 4},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
+                     "frac": r["achieved"] / r["peak"], "traffic": None,
+                     "peak_source": r["peak_kind"], "algorithmic_bytes_per_launch": r["bytes"]},
+        "cpu_baseline": {"value": cpu["value"], "unit": "rows/s", "cores": cpu["cores"], "kind": "oracle",
+                         "sample": f"first {cpu['layers']} layers of the workload, {cpu['seconds']:.1f} s"},
+        "clocks": r["clocks"],
+        "union_sizes": sorted(set(r["unions"])),
+    }
+    print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

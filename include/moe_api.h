@@ -1,0 +1,140 @@
+/*
+ * moe_api.h -- C ABI of the GB300 routed quantized mixture-of-experts step.
+ *
+ * The step, for nb consecutive rows of activations x[nb][hidden] (row-major,
+ * float32, device memory):
+ *   1. router logits L[b][e] = sum_i R[e][i] * x^[b][i], R bf16 [E][hidden]
+ *      (x^ = x, or the unit-weight RMSNorm of x with eps 1e-6 when the layer
+ *      has MOE_PRENORM);
+ *   2. per row the top_k experts by logit (ties to the lower id) and routing
+ *      weights = softmax over those k logits;
+ *   3. the union of the rows' experts in first-seen order (row-major over the
+ *      [nb][top_k] table), published as a slot table of record addresses and a
+ *      per-row weight map;
+ *   4. each union expert's affine-quantized record evaluated as
+ *      gate_up -> silu(gate) * up -> down;
+ *   5. out[b] = sum_j wmap[b][j] * y_j[b] + sigmoid(shared_gate . x^[b]) *
+ *      y_shared[b]  (+ x[b] when the layer has MOE_RESIDUAL).
+ *
+ * Sources (qwen4_exp::gpu pages): `Gpu::router_b` (router over nb rows,
+ * softmax over experts, top-k) and `Gpu::experts_b` (routed experts of the
+ * union published in the slot table, plus the shared expert, summed per row)
+ * on the struct Gpu page; the `slot_tab` and `wmap` fields there (per layer
+ * SLOT_STRIDE = 64 u64 record addresses, entry 62 the resident count, entry 63
+ * the union size; per layer [MAX_NB][64] routing weights); `struct Q`,
+ * `Q::at_offset`, `union_of`, `MAX_NB = 4` and `SLOT_STRIDE` on the gpu.rs
+ * source page; the load-time checks of load.rs (hidden % 256, expert width a
+ * multiple of the 64-code group, top_k * MAX_NB < SLOT_STRIDE, shared width ==
+ * expert width, 16-byte aligned code offsets).  The pages do not name the
+ * shared gate's activation: sigmoid is the reading taken here.
+ *
+ * Ownership: the caller allocates every buffer (device memory unless stated);
+ * the library allocates nothing and keeps no state between calls.  Calls are
+ * asynchronous on the given stream; device-side failures are written to
+ * *dev_status (a device int the call zeroes first), readable after a sync.
+ * Host-side checks run before any launch; a failing call returns a negative
+ * status, launches nothing, and moe_last_error() describes it.
+ */
+#ifndef MOE_API_H
+#define MOE_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *moe_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+/* One affine-quantized projection (`struct Q`): byte offsets, relative to the
+ * record base, of the codes (uint32 words, row-major [out][inp*bits/32], each
+ * row one LSB-first bitstream), the scales and the biases (bf16, row-major
+ * [out][inp/64]).  Every offset must be 256-byte aligned. */
+typedef struct {
+  uint64_t w, s, b;
+  uint32_t out, inp;
+} moe_q;
+
+/* One MoE layer.  A routed record holds gate_up (out = 2*inter: rows
+ * 0..inter-1 the gate, inter..2*inter-1 the up projection; inp = hidden) and
+ * down (out = hidden, inp = inter).  All layers of one call share hidden,
+ * n_experts, top_k, inter and bits. */
+typedef struct {
+  uint32_t hidden, n_experts, top_k, inter;
+  uint32_t bits;  /* routed records: 4, 3 or 2 */
+  uint32_t group; /* must be 64 */
+  uint32_t flags; /* MOE_RESIDUAL | MOE_PRENORM */
+  const uint16_t *router;      /* bf16 [n_experts][hidden] */
+  const uint16_t *shared_gate; /* bf16 [hidden]; NULL = no shared expert */
+  const void *shared_record;   /* 4-bit record of the shared expert (NULL iff shared_gate is) */
+  moe_q sh_gate_up, sh_down;   /* relative to shared_record */
+  const uint64_t *expert_addr; /* device array [n_experts] of record base addresses */
+  moe_q gate_up, down;         /* relative to each routed record */
+} moe_layer;
+
+enum {
+  MOE_RESIDUAL = 1, /* out = x + MoE(x^) */
+  MOE_PRENORM = 2,  /* x^ = x / sqrt(mean(x^2) + 1e-6) feeds router, gate and experts */
+  MOE_TEST_WITHHOLD = 0x100 /* failure-detection test only: the router's completion is
+                               never released, so the kernel's bounded wait must give up
+                               and report MOE_ETIMEOUT */
+};
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_EINVAL = -1,   /* NULL pointer, bad nb / n_layers, flags, aliasing */
+  MOE_ESHAPE = -2,   /* unsupported or inconsistent dimensions */
+  MOE_EALIGN = -3,   /* misaligned pointer or offset */
+  MOE_ECUDA = -4,    /* a CUDA runtime call failed */
+  MOE_ETIMEOUT = -5, /* (device) a bounded wait gave up */
+  MOE_EDEVICE = -6,  /* (device) bad data met on the device, e.g. a null record address */
+  MOE_ENOSPACE = -7  /* workspace too small */
+};
+
+#define MOE_SLOT_STRIDE 64
+#define MOE_MAX_NB 4
+#define MOE_MAX_LAYERS 64
+
+/* Route one layer: router logits, top-k softmax and the union / slot table.
+ *   x        [nb][hidden] float32; nb in 1..4
+ *   logits   [nb][n_experts] float32, or NULL
+ *   topk_idx [nb][top_k] uint32 (descending logit)
+ *   topk_w   [nb][top_k] float32 (sum to 1 per row)
+ *   slot_row [64] uint64: record addresses of the union in first-seen order,
+ *            [62] = [63] = union size (every record is resident)
+ *   wmap_row [4][64] float32: row b's weight for union slot j, else 0
+ *   work     device workspace of at least moe_forward_workspace(L, 1, nb) bytes
+ * Returns MOE_OK or a negative moe_status. */
+int moe_route(const moe_layer *L, const float *x, int nb, float *logits, uint32_t *topk_idx,
+              float *topk_w, uint64_t *slot_row, float *wmap_row, void *work, size_t work_bytes,
+              int *dev_status, moe_stream_t stream);
+
+/* n_layers stacked MoE layers over nb rows (decode / speculative verify):
+ * x_{l+1} = layer_l(x_l), out = x_{n_layers}.  One persistent kernel runs the
+ * whole stack; no host round trip between layers.
+ *   layers   host array [n_layers] (read during the call only); n_layers in 1..64
+ *   x        [nb][hidden] float32; out [nb][hidden] float32, must not overlap x
+ *   work     device workspace, at least moe_forward_workspace(layers, n_layers, nb)
+ *            bytes, 256-byte aligned; its contents need no initialisation
+ *   slot_tab [n_layers][64] uint64, wmap [n_layers][4][64] float32 (see moe_route)
+ *   topk_idx [n_layers][nb][top_k] uint32, or NULL
+ * Supported shapes: hidden % 256 == 0 and <= 4096, inter % 128 == 0 and <= 1024,
+ * n_experts <= 1024, top_k <= 32, top_k * nb < 64, group == 64.
+ * Returns MOE_OK or a negative moe_status. */
+int moe_forward(const moe_layer *layers, int n_layers, const float *x, int nb, float *out,
+                void *work, size_t work_bytes, uint64_t *slot_tab, float *wmap,
+                uint32_t *topk_idx, int *dev_status, moe_stream_t stream);
+
+/* Workspace bytes moe_forward needs for these layers and nb rows (0 if the
+ * arguments are invalid). */
+size_t moe_forward_workspace(const moe_layer *layers, int n_layers, int nb);
+
+/* Thread-local description of the last failing host-side check or CUDA call. */
+const char *moe_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_API_H */

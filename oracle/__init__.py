@@ -66,6 +66,8 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_shared_expert.argtypes = [ctypes.POINTER(OLayer), p, p]
         _lib.oracle_moe_layer.restype = i32
         _lib.oracle_moe_layer.argtypes = [ctypes.POINTER(OLayer), i32, p, p, p, p, p, p, p, p, p]
+        _lib.oracle_route.restype = i32
+        _lib.oracle_route.argtypes = [ctypes.POINTER(OLayer), i32, p, p, p, p, p]
         _lib.oracle_moe_forward.argtypes = [ctypes.POINTER(OLayer), i32, i32, p, p, p, p]
         _lib.oracle_prefill_rows.argtypes = [ctypes.POINTER(OLayer), p, p, i32, i32, p, p, p]
         _lib.oracle_threads.restype = i32
@@ -151,6 +153,19 @@ def moe_layer(layer: Layer, x: np.ndarray) -> dict:
     U = lib().oracle_moe_layer(ctypes.byref(layer.c), nb, _ptr(x), _ptr(r["out"]), _ptr(r["moe"]),
                                _ptr(r["logits"]), _ptr(r["idx"]), _ptr(r["w"]), _ptr(r["gamma"]),
                                _ptr(r["union"]), _ptr(r["wmap"]))
+    r["union"] = r["union"][:U].copy()
+    return r
+
+
+def route(layer: Layer, x: np.ndarray) -> dict:
+    """Routing alone: logits, idx, w, union."""
+    src = layer.src
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    nb = x.shape[0]
+    r = dict(logits=np.empty((nb, src.n_experts)), idx=np.empty((nb, src.top_k), dtype=np.int32),
+             w=np.empty((nb, src.top_k)), union=np.empty(256, dtype=np.int32))
+    U = lib().oracle_route(ctypes.byref(layer.c), nb, _ptr(x), _ptr(r["logits"]), _ptr(r["idx"]), _ptr(r["w"]),
+                           _ptr(r["union"]))
     r["union"] = r["union"][:U].copy()
     return r
 

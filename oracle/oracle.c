@@ -232,6 +232,28 @@ int oracle_union(const int32_t *idx, int n, int32_t *uni) {
   return u;
 }
 
+/* Routing alone for nb rows (norm when the layer asks, router, top-k,
+ * softmax): logits [nb][E], idx [nb][k], w [nb][k].  Returns the union size;
+ * uni [64] (may be NULL) receives the union. */
+int oracle_route(const oracle_layer_t *L, int nb, const double *x, double *logits, int32_t *idx,
+                 double *w, int32_t *uni) {
+  const int H = L->hidden, E = L->n_experts, k = L->top_k;
+  double *xn = (double *)malloc(sizeof(double) * (size_t)H);
+  int32_t un[64 * 4];
+  for (int b = 0; b < nb; b++) {
+    if (L->flags & ORACLE_PRENORM)
+      rmsnorm(x + (int64_t)b * H, H, xn);
+    else
+      memcpy(xn, x + (int64_t)b * H, sizeof(double) * H);
+    router_row(L, xn, logits + (int64_t)b * E);
+    oracle_topk_softmax(logits + (int64_t)b * E, E, k, idx + b * k, w + b * k);
+  }
+  int U = oracle_union(idx, nb * k, un);
+  if (uni) memcpy(uni, un, sizeof(int32_t) * (size_t)U);
+  free(xn);
+  return U;
+}
+
 /* ------------------------------------------------------------ one layer */
 
 /* One MoE layer over nb rows.

@@ -1,0 +1,215 @@
+// api.cu -- C ABI: argument checks, workspace layout and launches.
+//
+// The checks restate the load-time checks of the load.rs source page
+// (hidden % 256 == 0; expert width a multiple of the 64-code group;
+// top_k * rows < SLOT_STRIDE; shared expert width == expert width; Q4 code
+// offsets 16-byte aligned, kept here as 256-byte alignment of every tensor)
+// plus the limits of these kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "decode.cuh"
+#include "moe_api.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+struct WsLayout {
+  size_t cnt, logits, xbuf, hfrag, ypart, total;
+};
+
+WsLayout ws_layout(int H, int E, int I, int nl) {
+  WsLayout w{};
+  size_t off = 0;
+  w.cnt = off;
+  off += align256((size_t)nl * moe::kCntPerLayer * 4);
+  w.logits = off;
+  off += align256((size_t)nl * 4 * (E + 1) * 4);
+  w.xbuf = off;
+  off += align256((size_t)nl * 4 * H * 4);
+  w.hfrag = off;
+  off += align256((size_t)64 * I * 16);
+  w.ypart = off;
+  off += align256((size_t)64 * 4 * H * 4);
+  w.total = off;
+  return w;
+}
+
+int check_q(const moe_q &q, uint32_t out, uint32_t inp, const char *what, int l) {
+  if (q.out != out || q.inp != inp)
+    return fail(MOE_ESHAPE, "layer %d %s: shape [%u][%u], expected [%u][%u]", l, what, q.out, q.inp, out, inp);
+  if ((q.w | q.s | q.b) & 255u) return fail(MOE_EALIGN, "layer %d %s: offsets must be 256-byte aligned", l, what);
+  return MOE_OK;
+}
+
+int check_layers(const moe_layer *layers, int nl, int nb) {
+  if (!layers) return fail(MOE_EINVAL, "layers is NULL");
+  if (nl < 1 || nl > MOE_MAX_LAYERS) return fail(MOE_EINVAL, "n_layers %d outside 1..%d", nl, MOE_MAX_LAYERS);
+  if (nb < 1 || nb > MOE_MAX_NB) return fail(MOE_EINVAL, "nb %d outside 1..%d", nb, MOE_MAX_NB);
+  const moe_layer &L0 = layers[0];
+  const uint32_t H = L0.hidden, E = L0.n_experts, K = L0.top_k, I = L0.inter, bits = L0.bits;
+  if (H == 0 || H % 256) return fail(MOE_ESHAPE, "hidden %u must be a positive multiple of 256", H);
+  if (H > 2048) return fail(MOE_ESHAPE, "hidden %u above the decode kernel's limit 2048", H);
+  if (I == 0 || I % 128) return fail(MOE_ESHAPE, "inter %u must be a positive multiple of 128", I);
+  if (I > 1024) return fail(MOE_ESHAPE, "inter %u above the decode kernel's limit 1024", I);
+  if (E < 1 || E > 1024) return fail(MOE_ESHAPE, "n_experts %u outside 1..1024", E);
+  if (K < 1 || K > E || K > 32) return fail(MOE_ESHAPE, "top_k %u outside 1..min(n_experts, 32)", K);
+  if (K * (uint32_t)nb >= MOE_SLOT_STRIDE) return fail(MOE_ESHAPE, "top_k * nb = %u must be < 64", K * nb);
+  if (bits != 2 && bits != 3 && bits != 4) return fail(MOE_ESHAPE, "bits %u not in {2,3,4}", bits);
+  for (int l = 0; l < nl; l++) {
+    const moe_layer &L = layers[l];
+    if (L.hidden != H || L.n_experts != E || L.top_k != K || L.inter != I || L.bits != bits)
+      return fail(MOE_ESHAPE, "layer %d: dimensions or bits differ from layer 0", l);
+    if (L.group != 64) return fail(MOE_ESHAPE, "layer %d: group %u, only 64 is supported", l, L.group);
+    if (L.flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM | MOE_TEST_WITHHOLD))
+      return fail(MOE_EINVAL, "layer %d: unknown flags 0x%x", l, L.flags);
+    if (!L.router || !L.expert_addr) return fail(MOE_EINVAL, "layer %d: router / expert_addr NULL", l);
+    if ((uintptr_t)L.router & 15u) return fail(MOE_EALIGN, "layer %d: router not 16-byte aligned", l);
+    if (!L.shared_gate != !L.shared_record)
+      return fail(MOE_EINVAL, "layer %d: shared_gate and shared_record must both be set or both NULL", l);
+    if (L.shared_gate) {
+      if (((uintptr_t)L.shared_gate | (uintptr_t)L.shared_record) & 15u)
+        return fail(MOE_EALIGN, "layer %d: shared gate / record not 16-byte aligned", l);
+      int r;
+      if ((r = check_q(L.sh_gate_up, 2 * I, H, "sh_gate_up", l))) return r;
+      if ((r = check_q(L.sh_down, H, I, "sh_down", l))) return r;
+    }
+    int r;
+    if ((r = check_q(L.gate_up, 2 * I, H, "gate_up", l))) return r;
+    if ((r = check_q(L.down, H, I, "down", l))) return r;
+  }
+  return MOE_OK;
+}
+
+unsigned long long timeout_ns() {
+  const char *s = getenv("MOE_TIMEOUT_MS");
+  double ms = s ? atof(s) : 1000.0;
+  if (!(ms > 0)) ms = 1000.0;
+  return (unsigned long long)(ms * 1e6);
+}
+
+bool overlap(const void *a, size_t na, const void *b, size_t nb) {
+  const char *pa = (const char *)a, *pb = (const char *)b;
+  return pa < pb + nb && pb < pa + na;
+}
+
+int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, void *work, size_t work_bytes,
+        uint64_t *slot_tab, float *wmap, uint32_t *topk_idx, float *topk_w, float *logits, int *status,
+        moe_stream_t stream, int route_only) {
+  const moe_layer &L0 = layers[0];
+  const int H = (int)L0.hidden, E = (int)L0.n_experts, I = (int)L0.inter;
+  if (!x) return fail(MOE_EINVAL, "x is NULL");
+  if (!route_only && !out) return fail(MOE_EINVAL, "out is NULL");
+  if (!status) return fail(MOE_EINVAL, "dev_status is NULL");
+  if (!work) return fail(MOE_EINVAL, "work is NULL");
+  if ((uintptr_t)work & 255u) return fail(MOE_EALIGN, "work must be 256-byte aligned");
+  if (!route_only && overlap(x, (size_t)nb * H * 4, out, (size_t)nb * H * 4))
+    return fail(MOE_EINVAL, "out overlaps x");
+  const WsLayout w = ws_layout(H, E, I, nl);
+  if (work_bytes < w.total) return fail(MOE_ENOSPACE, "work holds %zu bytes, %zu needed", work_bytes, w.total);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MOE_ECUDA, "cudaGetDevice failed");
+  int grid = 0;
+  if (moe::decode_grid(dev, H, E, (int)L0.bits, &grid) != 0)
+    return fail(MOE_ECUDA, "decode kernel cannot be resident (shared memory %d bytes)",
+                moe::decode_smem_bytes(H, E, (int)L0.bits));
+
+  static_assert(sizeof(moe::FwdParams) < 32000, "kernel parameters too large");
+  moe::FwdParams p;
+  memset(&p, 0, sizeof p);
+  p.H = H, p.E = E, p.K = (int)L0.top_k, p.I = I, p.nb = nb, p.nl = nl, p.bits = (int)L0.bits;
+  p.route_only = route_only;
+  p.x = x, p.out = out;
+  p.slot_tab = slot_tab, p.wmap = wmap, p.topk_idx = topk_idx, p.topk_w = topk_w, p.logits_out = logits;
+  p.status = status;
+  char *base = (char *)work;
+  p.cnt = (unsigned *)(base + w.cnt);
+  p.logits = (float *)(base + w.logits);
+  p.xbuf = (float *)(base + w.xbuf);
+  p.hfrag = (uint16_t *)(base + w.hfrag);
+  p.ypart = (float *)(base + w.ypart);
+  p.timeout_ns = timeout_ns();
+  for (int l = 0; l < nl; l++) {
+    const moe_layer &L = layers[l];
+    moe::LayerP &q = p.L[l];
+    q.router = L.router;
+    q.sgate = L.shared_gate;
+    q.srec = (const uint8_t *)L.shared_record;
+    q.eaddr = L.expert_addr;
+    q.gu = {(uint32_t)L.gate_up.w, (uint32_t)L.gate_up.s, (uint32_t)L.gate_up.b};
+    q.dn = {(uint32_t)L.down.w, (uint32_t)L.down.s, (uint32_t)L.down.b};
+    q.sgu = {(uint32_t)L.sh_gate_up.w, (uint32_t)L.sh_gate_up.s, (uint32_t)L.sh_gate_up.b};
+    q.sdn = {(uint32_t)L.sh_down.w, (uint32_t)L.sh_down.s, (uint32_t)L.sh_down.b};
+    q.flags = L.flags & (MOE_RESIDUAL | MOE_PRENORM);
+    if (L.flags & MOE_TEST_WITHHOLD) p.withhold = 1;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)nl * moe::kCntPerLayer * 4, st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = moe::launch_decode(p, grid, st);
+  if (e != cudaSuccess) return fail(MOE_ECUDA, "launch failed: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+int check_offsets_fit(const moe_layer *layers, int nl) {
+  for (int l = 0; l < nl; l++) {
+    const moe_layer &L = layers[l];
+    const moe_q *qs[4] = {&L.gate_up, &L.down, &L.sh_gate_up, &L.sh_down};
+    for (const moe_q *q : qs)
+      if ((q->w | q->s | q->b) >> 32) return fail(MOE_ESHAPE, "layer %d: record offsets must be < 4 GiB", l);
+  }
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_last_error(void) { return g_err.c_str(); }
+
+size_t moe_forward_workspace(const moe_layer *layers, int n_layers, int nb) {
+  if (check_layers(layers, n_layers, nb) != MOE_OK) return 0;
+  const moe_layer &L0 = layers[0];
+  return ws_layout((int)L0.hidden, (int)L0.n_experts, (int)L0.inter, n_layers).total;
+}
+
+int moe_forward(const moe_layer *layers, int n_layers, const float *x, int nb, float *out, void *work,
+                size_t work_bytes, uint64_t *slot_tab, float *wmap, uint32_t *topk_idx, int *dev_status,
+                moe_stream_t stream) {
+  int r = check_layers(layers, n_layers, nb);
+  if (r == MOE_OK) r = check_offsets_fit(layers, n_layers);
+  if (r != MOE_OK) return r;
+  return run(layers, n_layers, x, nb, out, work, work_bytes, slot_tab, wmap, topk_idx, nullptr, nullptr,
+             dev_status, stream, 0);
+}
+
+int moe_route(const moe_layer *L, const float *x, int nb, float *logits, uint32_t *topk_idx, float *topk_w,
+              uint64_t *slot_row, float *wmap_row, void *work, size_t work_bytes, int *dev_status,
+              moe_stream_t stream) {
+  int r = check_layers(L, 1, nb);
+  if (r == MOE_OK) r = check_offsets_fit(L, 1);
+  if (r != MOE_OK) return r;
+  if (!topk_idx || !topk_w || !slot_row || !wmap_row)
+    return fail(MOE_EINVAL, "topk_idx, topk_w, slot_row and wmap_row are required");
+  return run(L, 1, x, nb, nullptr, work, work_bytes, slot_row, wmap_row, topk_idx, topk_w, logits, dev_status,
+             stream, 1);
+}
+
+}  // extern "C"

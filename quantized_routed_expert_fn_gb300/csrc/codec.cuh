@@ -1,0 +1,133 @@
+// codec.cuh -- b-bit affine codes -> exact bf16 integers for tensor-core fragments.
+//
+// Record format (gpu.rs source page, `struct Q`): codes are uint32 words,
+// each weight row one little-endian bitstream, code i in bits [i*b, i*b+b).
+// Groups of 64 codes share one bf16 scale and one bf16 bias (the "64-code
+// quantization group" of the load.rs checks); weight = scale * code + bias.
+//
+// The matvec kernels feed the raw code q (an exact small integer) to a bf16
+// tensor-core MMA and apply scale and bias per group in fp32 afterwards:
+//   sum_i (s*q_i + beta) x_i = s * sum_i q_i x_i + beta * sum_i x_i.
+//
+// Work split: within a block of 128 input positions, lane quad position t
+// (0..3) owns the 32 codes at positions 32t..32t+31, i.e. 4*b bytes of a row
+// (codes of group t/2 of the block).  Those 32 codes are consumed as 16
+// pairs; pair p supplies one bf16x2 B-fragment register (first code in the
+// low half).  MMA step m (0..7) of the block uses pairs 2m and 2m+1 as the
+// k-slots (2t, 2t+1) and (2t+8, 2t+9).  Which code goes to which pair is a
+// free permutation (the dot product does not care) chosen so that one mask
+// places both codes of a pair in the mantissas of 128.0 (bf16 0x4300):
+// 128 + q*2^s is exact for q*2^s < 128; one bf16 FMA by 2^-s then removes
+// the offset exactly.  The activation fragments use the same permutation.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr uint32_t kMagic = 0x43004300u;  // bf16x2 (128, 128)
+
+// bf16 of 2^-s, and of -128 * 2^-s
+__host__ __device__ constexpr uint32_t bf_pow2neg(int s) { return 0x3f80u - 0x80u * (uint32_t)s; }
+__host__ __device__ constexpr uint32_t bf_off(int s) { return 0xc300u - 0x80u * (uint32_t)s; }
+__host__ __device__ constexpr uint32_t pk(uint32_t lo, uint32_t hi) { return lo | (hi << 16); }
+
+template <int BITS>
+struct Codec;
+
+// 4-bit: 4 words; pair 4w+j = nibbles (j, j+4) of word w, both at shift 4j.
+template <>
+struct Codec<4> {
+  static constexpr int kWords = 4;
+  __host__ __device__ static constexpr int lo(int p) { return 8 * (p / 4) + p % 4; }
+  __host__ __device__ static constexpr int hi(int p) { return lo(p) + 4; }
+  __device__ static __forceinline__ void unpack(const uint32_t (&w)[kWords], uint32_t (&bf)[16]) {
+#pragma unroll
+    for (int p = 0; p < 4; p++) {
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        uint32_t v = ((w[p] >> (4 * j)) & 0x000f000fu) | kMagic;
+        bf[4 * p + j] = bfma2(v, 0x3f803f80u, 0xc300c300u);
+      }
+    }
+  }
+};
+
+// 2-bit: 2 words; pair 8w+j = codes (j, j+8) of word w (bits 2j and 16+2j),
+// read from w, w>>6 or w>>12 so that both sit at shift s <= 4.
+template <>
+struct Codec<2> {
+  static constexpr int kWords = 2;
+  __host__ __device__ static constexpr int lo(int p) { return 16 * (p / 8) + p % 8; }
+  __host__ __device__ static constexpr int hi(int p) { return lo(p) + 8; }
+  __device__ static __forceinline__ void unpack(const uint32_t (&w)[kWords], uint32_t (&bf)[16]) {
+#pragma unroll
+    for (int p = 0; p < 2; p++) {
+      const uint32_t src[3] = {w[p], w[p] >> 6, w[p] >> 12};
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        const int k = j < 3 ? 0 : (j < 6 ? 1 : 2);
+        const int s = 2 * (j - 3 * k);
+        const uint32_t mask = (3u << s) | (3u << (16 + s));
+        uint32_t v = (src[k] & mask) | kMagic;
+        bf[8 * p + j] = bfma2(v, pk(bf_pow2neg(s), bf_pow2neg(s)), pk(bf_off(s), bf_off(s)));
+      }
+    }
+  }
+};
+
+// 3-bit: 3 words = one 96-bit stream of 32 codes (codes straddle words).
+// Each pair is read from a 32-bit window of the stream starting at bit o;
+// the low code sits at window bit s_lo <= 4, the high code at 16 + s_hi.
+// Ten windows cover all 32 codes (found by a small integer program over
+// window offsets; any exact cover works).
+struct Pair3 {
+  int o, lo, hi, slo, shi;
+};
+__host__ __device__ constexpr Pair3 pair3(int p) {
+  constexpr Pair3 t[16] = {{-1, 0, 5, 1, 0},   {-1, 1, 6, 4, 3},   {5, 2, 8, 1, 3},
+                           {5, 3, 7, 4, 0},    {11, 4, 10, 1, 3},  {23, 9, 13, 4, 0},
+                           {32, 11, 16, 1, 0}, {32, 12, 17, 4, 3}, {41, 14, 20, 1, 3},
+                           {41, 15, 19, 4, 0}, {50, 18, 22, 4, 0}, {61, 21, 27, 2, 4},
+                           {68, 23, 29, 1, 3}, {68, 24, 28, 4, 0}, {74, 25, 30, 1, 0},
+                           {74, 26, 31, 4, 3}};
+  return t[p];
+}
+
+template <>
+struct Codec<3> {
+  static constexpr int kWords = 3;
+  __host__ __device__ static constexpr int lo(int p) { return pair3(p).lo; }
+  __host__ __device__ static constexpr int hi(int p) { return pair3(p).hi; }
+  __device__ static __forceinline__ uint32_t window(const uint32_t (&w)[kWords], int o) {
+    if (o < 0) return w[0] << (-o);
+    if (o == 0) return w[0];
+    if (o < 32) return __funnelshift_r(w[0], w[1], o);
+    if (o == 32) return w[1];
+    if (o < 64) return __funnelshift_r(w[1], w[2], o - 32);
+    if (o == 64) return w[2];
+    return w[2] >> (o - 64);
+  }
+  __device__ static __forceinline__ void unpack(const uint32_t (&w)[kWords], uint32_t (&bf)[16]) {
+#pragma unroll
+    for (int p = 0; p < 16; p++) {
+      const Pair3 q = pair3(p);
+      const uint32_t win = window(w, q.o);
+      const uint32_t mask = (7u << q.slo) | (7u << (16 + q.shi));
+      uint32_t v = (win & mask) | kMagic;
+      bf[p] = bfma2(v, pk(bf_pow2neg(q.slo), bf_pow2neg(q.shi)), pk(bf_off(q.slo), bf_off(q.shi)));
+    }
+  }
+};
+
+// Runtime lookup of the pair tables (activation staging and h scatter).
+__host__ __device__ inline int pair_lo(int bits, int p) {
+  return bits == 4 ? Codec<4>::lo(p) : (bits == 2 ? Codec<2>::lo(p) : Codec<3>::lo(p));
+}
+__host__ __device__ inline int pair_hi(int bits, int p) {
+  return bits == 4 ? Codec<4>::hi(p) : (bits == 2 ? Codec<2>::hi(p) : Codec<3>::hi(p));
+}
+
+}  // namespace moe

@@ -1,0 +1,56 @@
+// decode.cuh -- parameters of the persistent decode / verify kernel (nb <= 4 rows).
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct QOff {
+  uint32_t w, s, b;  // byte offsets inside a record
+};
+
+struct LayerP {
+  const uint16_t *router;  // bf16 [E][H]
+  const uint16_t *sgate;   // bf16 [H] or nullptr
+  const uint8_t *srec;     // shared expert record (4-bit) or nullptr
+  const uint64_t *eaddr;   // [E] record base addresses
+  QOff gu, dn, sgu, sdn;
+  uint32_t flags;
+};
+
+// per-layer counters in the workspace (uint32 each)
+constexpr int kCntRouter = 0;  // router rows finished
+constexpr int kCntRows = 1;    // 64-row output ranges finalised
+constexpr int kCntGu = 8;      // [64] gate_up units finished per internal slot
+constexpr int kCntDn = 72;     // [H/64] down units finished per output range
+constexpr int kCntPerLayer = 256;
+
+struct FwdParams {
+  int H, E, K, I, nb, nl, bits;
+  int route_only;
+  int withhold;  // failure-detection test: never release the router count
+  const float *x;
+  float *out;
+  uint64_t *slot_tab;     // [nl][64] or nullptr
+  float *wmap;            // [nl][4][64] or nullptr
+  uint32_t *topk_idx;     // [nl][nb][K] or nullptr
+  float *topk_w;          // [nl][nb][K] or nullptr
+  float *logits_out;      // [nb][E] (route only) or nullptr
+  int *status;
+  unsigned *cnt;          // [nl][kCntPerLayer]
+  float *logits;          // [nl][4][E+1]
+  float *xbuf;            // [nl][4][H]   input of layer l (l >= 1)
+  uint16_t *hfrag;        // [64][I/128][8][32][2][2] bf16 activation fragments of h
+  float *ypart;           // [64][4][H]   per-slot weighted down outputs
+  unsigned long long timeout_ns;
+  LayerP L[kMaxLayers];
+};
+
+// Launch helpers (decode.cu)
+int decode_smem_bytes(int H, int E, int bits);
+cudaError_t launch_decode(const FwdParams &p, int grid, cudaStream_t st);
+int decode_grid(int device, int H, int E, int bits, int *grid);
+
+}  // namespace moe

@@ -1,0 +1,166 @@
+"""Python binding of the C ABI in include/moe_api.h (argument marshalling only).
+
+Every step of the path runs in libmoe_gb300.so; this module only turns torch
+tensors into pointers, fills the ABI structs and checks return codes.  There
+is no fallback: if the library is missing the import of `lib()` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+from . import synth
+
+RESIDUAL = 1
+PRENORM = 2
+TEST_WITHHOLD = 0x100
+
+OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EDEVICE, ENOSPACE = 0, -1, -2, -3, -4, -5, -6, -7
+STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_EALIGN", -4: "MOE_ECUDA",
+                -5: "MOE_ETIMEOUT", -6: "MOE_EDEVICE", -7: "MOE_ENOSPACE"}
+
+EXPORTS = ["moe_route", "moe_forward", "moe_forward_workspace", "moe_last_error"]
+
+
+class MoeQ(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_uint64), ("s", ctypes.c_uint64), ("b", ctypes.c_uint64),
+                ("out", ctypes.c_uint32), ("inp", ctypes.c_uint32)]
+
+
+class MoeLayer(ctypes.Structure):
+    _fields_ = [("hidden", ctypes.c_uint32), ("n_experts", ctypes.c_uint32), ("top_k", ctypes.c_uint32),
+                ("inter", ctypes.c_uint32), ("bits", ctypes.c_uint32), ("group", ctypes.c_uint32),
+                ("flags", ctypes.c_uint32),
+                ("router", ctypes.c_void_p), ("shared_gate", ctypes.c_void_p), ("shared_record", ctypes.c_void_p),
+                ("sh_gate_up", MoeQ), ("sh_down", MoeQ),
+                ("expert_addr", ctypes.c_void_p),
+                ("gate_up", MoeQ), ("down", MoeQ)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """Load libmoe_gb300.so (built by build.build()); raise if it is absent."""
+    global _lib
+    if _lib is None:
+        path = path or _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it with quantized_routed_expert_fn_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        L.moe_last_error.restype = ctypes.c_char_p
+        L.moe_forward_workspace.restype = sz
+        L.moe_forward_workspace.argtypes = [ctypes.POINTER(MoeLayer), i32, i32]
+        L.moe_forward.restype = i32
+        L.moe_forward.argtypes = [ctypes.POINTER(MoeLayer), i32, vp, i32, vp, vp, sz, vp, vp, vp, vp, vp]
+        L.moe_route.restype = i32
+        L.moe_route.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().moe_last_error().decode()
+
+
+def _check(code: int) -> None:
+    if code != OK:
+        raise MoeError(code, last_error())
+
+
+def _p(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _q(q) -> MoeQ:
+    return MoeQ(q.w, q.s, q.b, q.out, q.inp)
+
+
+class DeviceLayers:
+    """Device copies of synth.Layer weights plus the ABI structs that point at them."""
+
+    def __init__(self, layers, device="cuda"):
+        self.tensors = []
+        arr = (MoeLayer * len(layers))()
+        for i, L in enumerate(layers):
+            if isinstance(L, synth.DeviceLayer):
+                router, recs, sg, srec = L.router, L.records, L.shared_gate, L.shared_record
+            else:
+                router = torch.from_numpy(L.router.view(np.int16)).to(device)
+                recs = torch.from_numpy(L.records).to(device)
+                sg = srec = None
+                if L.shared_gate is not None:
+                    sg = torch.from_numpy(L.shared_gate.view(np.int16)).to(device)
+                    srec = torch.from_numpy(L.shared_record).to(device)
+            stride = L.layout.stride
+            base = recs.data_ptr()
+            eaddr = torch.arange(L.n_experts, dtype=torch.int64, device=recs.device) * stride + base
+            self.tensors += [router, recs, eaddr, sg, srec]
+            c = arr[i]
+            c.hidden, c.n_experts, c.top_k, c.inter = L.hidden, L.n_experts, L.top_k, L.inter
+            c.bits, c.group, c.flags = L.bits, 64, L.flags
+            c.router = router.data_ptr()
+            c.shared_gate = _p(sg)
+            c.shared_record = _p(srec)
+            if L.shared_layout is not None:
+                c.sh_gate_up, c.sh_down = _q(L.shared_layout.gate_up), _q(L.shared_layout.down)
+            c.expert_addr = eaddr.data_ptr()
+            c.gate_up, c.down = _q(L.layout.gate_up), _q(L.layout.down)
+        self.c = arr
+        self.n = len(layers)
+        self.src = layers
+
+    def set_flags(self, flags: int) -> None:
+        for i in range(self.n):
+            self.c[i].flags = flags
+
+
+def forward_workspace(layers: DeviceLayers | ctypes.Array, nb: int, n_layers: int | None = None) -> int:
+    arr = layers.c if isinstance(layers, DeviceLayers) else layers
+    n = n_layers if n_layers is not None else len(arr)
+    return int(lib().moe_forward_workspace(arr, n, nb))
+
+
+def alloc_workspace(nbytes: int, device="cuda") -> torch.Tensor:
+    return torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+
+
+def _aligned(ws: torch.Tensor) -> tuple[int, int]:
+    p = ws.data_ptr()
+    a = (p + 255) // 256 * 256
+    return a, ws.numel() - (a - p)
+
+
+def forward(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, work: torch.Tensor, status: torch.Tensor,
+            slot_tab=None, wmap=None, topk_idx=None, n_layers: int | None = None, stream=None,
+            layer_offset: int = 0) -> None:
+    """moe_forward over layers[layer_offset : layer_offset + n_layers]."""
+    n = n_layers if n_layers is not None else layers.n - layer_offset
+    arr = ctypes.cast(ctypes.byref(layers.c, layer_offset * ctypes.sizeof(MoeLayer)), ctypes.POINTER(MoeLayer))
+    wp, wb = _aligned(work)
+    _check(lib().moe_forward(arr, n, _p(x), x.shape[0], _p(out), wp, wb, _p(slot_tab), _p(wmap), _p(topk_idx),
+                             _p(status), _stream(stream)))
+
+
+def route(layers: DeviceLayers, x: torch.Tensor, topk_idx, topk_w, slot_row, wmap_row, work, status,
+          logits=None, layer: int = 0, stream=None) -> None:
+    arr = ctypes.cast(ctypes.byref(layers.c, layer * ctypes.sizeof(MoeLayer)), ctypes.POINTER(MoeLayer))
+    wp, wb = _aligned(work)
+    _check(lib().moe_route(arr, _p(x), x.shape[0], _p(logits), _p(topk_idx), _p(topk_w), _p(slot_row),
+                           _p(wmap_row), wp, wb, _p(status), _stream(stream)))

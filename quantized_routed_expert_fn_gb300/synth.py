@@ -108,7 +108,7 @@ def _fill_q(rng, rec: np.ndarray, q: QDesc, bits: int, scale_lo: float, scale_hi
     if codes is None:
         # i.i.d. uniform codes packed LSB first form i.i.d. uniform bits, so
         # uniform random words are exactly such a packing.
-        words = rng.integers(0, 2**32, size=(n_rec, cw // 4), dtype=np.uint64).astype(np.uint32)
+        words = np.frombuffer(rng.bytes(n_rec * cw), dtype=np.uint32).reshape(n_rec, cw // 4)
     else:
         words = np.stack([pack_codes(c, bits).reshape(-1) for c in codes])
     rec[:, q.w:q.w + cw] = words.view(np.uint8).reshape(n_rec, cw)
@@ -243,3 +243,66 @@ def make_prefill_x(rng, t: int, hidden: int) -> np.ndarray:
     x = rng.normal(0.0, 1.0, size=(t, hidden)).astype(np.float32)
     x[:, 0] = 1.0
     return x
+
+
+# ------------------------------------------------------------- device-side draws
+# Same distributions as above, drawn with torch directly on the GPU (used where
+# the host draw would take minutes, e.g. the 48-layer stack's 16 GB of records).
+
+@dataclasses.dataclass
+class DeviceLayer:
+    hidden: int
+    n_experts: int
+    top_k: int
+    inter: int
+    bits: int
+    flags: int
+    router: "object"          # torch.int16 [E][H] (bf16 bits)
+    shared_gate: "object"     # torch.int16 [H] or None
+    shared_record: "object"   # torch.uint8 [stride4] or None
+    shared_layout: RecordLayout | None
+    records: "object"         # torch.uint8 [E][stride]
+    layout: RecordLayout
+
+
+def _dev_fill_q(torch, gen, rec, q: QDesc, bits: int, scale_lo: float, scale_hi: float, bias_noise: float):
+    n = rec.shape[0]
+    cw, cs, _ = q_bytes(q.out, q.inp, bits)
+    words = torch.randint(-2**31, 2**31 - 1, (n, cw // 4), dtype=torch.int32, device=rec.device, generator=gen)
+    rec[:, q.w:q.w + cw] = words.view(torch.uint8)
+    ng = q.out * (q.inp // GROUP)
+    s = (torch.rand((n, ng), device=rec.device, generator=gen) * (scale_hi - scale_lo) + scale_lo).to(torch.bfloat16)
+    b = -float(2 ** (bits - 1)) * s.float()
+    if bias_noise:
+        b = b + torch.randn((n, ng), device=rec.device, generator=gen) * bias_noise
+    rec[:, q.s:q.s + cs] = s.view(torch.int16).view(torch.uint8)
+    rec[:, q.b:q.b + cs] = b.to(torch.bfloat16).view(torch.int16).view(torch.uint8)
+
+
+def make_device_layers(name: str, seed: int = 0, device="cuda", n_layers: int | None = None, **over):
+    import torch
+    cfg = dict(CONFIGS[name])
+    cfg.update(over)
+    nl = n_layers if n_layers is not None else cfg["n_layers"]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed)
+    H, E, k, I, bits = cfg["hidden"], cfg["n_experts"], cfg["top_k"], cfg["inter"], cfg["bits"]
+    scale = cfg.get("scale", (0.005, 0.02))
+    noise = cfg.get("bias_noise", 1e-3)
+    lay = record_layout(H, I, bits)
+    out = []
+    for _ in range(nl):
+        router = (torch.randn((E, H), device=device, generator=gen) * 0.05).to(torch.bfloat16).view(torch.int16)
+        recs = torch.zeros((E, lay.stride), dtype=torch.uint8, device=device)
+        for q in (lay.gate_up, lay.down):
+            _dev_fill_q(torch, gen, recs, q, bits, scale[0], scale[1], noise)
+        sg = srec = slay = None
+        if cfg["shared"]:
+            slay = record_layout(H, I, 4)
+            sg = (torch.randn(H, device=device, generator=gen) * 0.05).to(torch.bfloat16).view(torch.int16)
+            srec = torch.zeros((1, slay.stride), dtype=torch.uint8, device=device)
+            for q in (slay.gate_up, slay.down):
+                _dev_fill_q(torch, gen, srec, q, 4, 0.005, 0.02, 1e-3)
+            srec = srec[0]
+        out.append(DeviceLayer(H, E, k, I, bits, cfg.get("flags", 0), router, sg, srec, slay, recs, lay))
+    return out

@@ -1,0 +1,219 @@
+"""GPU parity of the decode / verify path (moe_forward, moe_route) against the oracle."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from helpers import (GAP, assert_close_rows, assert_gaps, check_routing, check_union, find_x, find_x_union,
+                     topk_gap)
+from quantized_routed_expert_fn_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_routed_expert_fn_gb300 import build, moe as m
+    build.build()
+    m.lib()
+    return m
+
+
+def run_forward(m, dl, x, n_layers=None, offset=0):
+    nb, H = x.shape
+    n = n_layers if n_layers is not None else dl.n - offset
+    k = dl.src[offset].top_k
+    xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+    out = torch.empty_like(xt)
+    ws = m.alloc_workspace(m.forward_workspace(dl.c, nb, n))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    slot = torch.zeros((n, 64), dtype=torch.int64, device="cuda")
+    wmap = torch.zeros((n, 4, 64), dtype=torch.float32, device="cuda")
+    idx = torch.zeros((n, nb, k), dtype=torch.int32, device="cuda")
+    m.forward(dl, xt, out, ws, status, slot, wmap, idx, n_layers=n, layer_offset=offset)
+    torch.cuda.synchronize()
+    assert status.item() == 0, m.STATUS_NAMES.get(status.item())
+    return dict(out=out.cpu().numpy(), slot=slot.cpu().numpy(), wmap=wmap.cpu().numpy(), idx=idx.cpu().numpy())
+
+
+def eaddr_of(dl, layer):
+    return dl.tensors[5 * layer + 2].cpu().numpy()
+
+
+def check_layer(m, layers, x, what, dl=None):
+    dl = dl or m.DeviceLayers(layers)
+    ol = oracle.Layer(layers[0])
+    ref = oracle.moe_layer(ol, x)
+    assert_gaps(ref, layers[0].top_k)
+    g = run_forward(m, dl, x, n_layers=1)
+    nb = x.shape[0]
+    check_routing(g["idx"][0], None, ref, ref["logits"], layers[0].top_k, what)
+    check_union(g["slot"][0], g["wmap"][0], ref, eaddr_of(dl, 0), nb, what)
+    return assert_close_rows(g["out"], ref["out"], ref["moe"], what=what)
+
+
+def test_c0_one_layer(moe):
+    layers = synth.make_config_layers("c0", seed=0)
+    x, _ = find_x(oracle.Layer(layers[0]), 1, seed=0)
+    check_layer(moe, layers, x, "c0")
+
+
+@pytest.mark.parametrize("nb", [1, 2, 3, 4])
+def test_small_ragged_shapes(moe, nb):
+    """Several blocks of 128 inputs on both projections, a 64-row output tail
+    of a 768-wide hidden state, shared expert, odd k."""
+    rng = np.random.default_rng(100 + nb)
+    layers = [synth.make_layer(rng, 768, 40, 5, 384, 4, shared=True)]
+    x, _ = find_x(oracle.Layer(layers[0]), nb, seed=7)
+    check_layer(moe, layers, x, f"ragged nb={nb}")
+
+
+@pytest.mark.parametrize("bits", [4, 3, 2])
+@pytest.mark.parametrize("flags", [0, synth.RESIDUAL | synth.PRENORM])
+def test_bits_and_flags_small(moe, bits, flags):
+    rng = np.random.default_rng(200 + bits)
+    layers = [synth.make_layer(rng, 512, 16, 3, 256, bits, shared=True, flags=flags,
+                               scale=(0.01, 0.04) if bits < 4 else (0.005, 0.02))]
+    x, _ = find_x(oracle.Layer(layers[0]), 3, seed=11)
+    check_layer(moe, layers, x, f"bits={bits} flags={flags}")
+
+
+@pytest.fixture(scope="module")
+def c2(moe):
+    layers = synth.make_config_layers("c2", seed=2)
+    return layers, moe.DeviceLayers(layers), oracle.Layer(layers[0])
+
+
+@pytest.mark.parametrize("nb,target_u", [(1, 10), (2, 20), (3, 30), (4, 20), (4, 30), (4, 40)])
+def test_c2_verify_batch(moe, c2, nb, target_u):
+    layers, dl, ol = c2
+    if nb == 1:
+        x, _ = find_x(ol, 1, seed=30)
+    else:
+        x, _, _ = find_x_union(ol, nb, seed=40 + target_u, target_u=target_u)
+    check_layer(moe, layers, x, f"c2 nb={nb} U~{target_u}", dl=dl)
+
+
+@pytest.mark.parametrize("name", ["c3b3", "c3b2"])
+@pytest.mark.parametrize("nb", [1, 4])
+def test_c3_lowbit(moe, name, nb):
+    layers = synth.make_config_layers(name, seed=3)
+    ol = oracle.Layer(layers[0])
+    x = find_x(ol, 1, seed=50)[0] if nb == 1 else find_x_union(ol, 4, seed=60, target_u=40)[0]
+    check_layer(moe, layers, x, f"{name} nb={nb}")
+
+
+def test_batch_rows_match_single_rows(moe, c2):
+    layers, dl, ol = c2
+    x, _, _ = find_x_union(ol, 4, seed=70, target_u=30)
+    g4 = run_forward(moe, dl, x, n_layers=1)
+    ref = oracle.moe_layer(ol, x)
+    for b in range(4):
+        g1 = run_forward(moe, dl, x[b:b + 1], n_layers=1)
+        assert list(g1["idx"][0][0]) == list(g4["idx"][0][b])
+        assert_close_rows(g1["out"], g4["out"][b:b + 1], ref["moe"][b:b + 1], tol=5e-4, what="batch vs single")
+
+
+def test_deterministic(moe, c2):
+    layers, dl, ol = c2
+    x, _, _ = find_x_union(ol, 4, seed=80, target_u=40)
+    a = run_forward(moe, dl, x, n_layers=1)
+    b = run_forward(moe, dl, x, n_layers=1)
+    assert np.array_equal(a["out"].view(np.uint32), b["out"].view(np.uint32))
+
+
+def test_route_only(moe, c2):
+    layers, dl, ol = c2
+    x, _, _ = find_x_union(ol, 4, seed=90, target_u=30)
+    ref = oracle.moe_layer(ol, x)
+    nb, k, E = 4, layers[0].top_k, layers[0].n_experts
+    xt = torch.from_numpy(x).cuda()
+    idx = torch.zeros((nb, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((nb, k), dtype=torch.float32, device="cuda")
+    slot = torch.zeros(64, dtype=torch.int64, device="cuda")
+    wmap = torch.zeros((4, 64), dtype=torch.float32, device="cuda")
+    logits = torch.zeros((nb, E), dtype=torch.float32, device="cuda")
+    ws = moe.alloc_workspace(moe.forward_workspace(dl.c, nb, 1))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.route(dl, xt, idx, w, slot, wmap, ws, status, logits=logits)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    lg = logits.cpu().numpy()
+    assert np.abs(lg - ref["logits"]).max() < 1e-4 * np.abs(ref["logits"]).max()
+    check_routing(idx.cpu().numpy(), w.cpu().numpy(), ref, ref["logits"], k, "route")
+    check_union(slot.cpu().numpy(), wmap.cpu().numpy(), ref, eaddr_of(dl, 0), nb, "route")
+
+
+@pytest.fixture(scope="module")
+def c1(moe):
+    """48 stacked layers (hidden 2048, 128 experts, k 8, inter 768, shared expert,
+    unit RMSNorm before each layer, residual add), nb = 1; x seeded so that
+    every layer of the oracle's trajectory keeps a top-k gap >= 1e-3."""
+    layers = synth.make_config_layers("c1", seed=1)
+    ols = [oracle.Layer(l) for l in layers]
+    for s in range(100, 140):
+        x = synth.make_x(np.random.default_rng(s), 1, 2048)
+        cur, inputs, idx, ok = x.astype(np.float64), [], [], True
+        for l in range(len(layers)):
+            r = oracle.moe_layer(ols[l], cur)
+            if topk_gap(r["logits"][0], 8) < GAP:
+                ok = False
+                break
+            inputs.append(cur)
+            idx.append(r["idx"])
+            cur = r["out"]
+        if ok:
+            f = dict(out=cur, inputs=np.stack(inputs), idx=np.stack(idx))
+            return layers, moe.DeviceLayers(layers), ols, x, f
+    pytest.fail("no seed keeps the 48-layer trajectory's top-k gaps")
+
+
+def test_c1_stacked_end_to_end(moe, c1):
+    layers, dl, ols, x, f = c1
+    g = run_forward(moe, dl, x)
+    for l in range(len(layers)):
+        assert sorted(g["idx"][l][0]) == sorted(f["idx"][l][0]), f"layer {l} ids"
+    final = f["out"]
+    assert_close_rows(g["out"], final, final, what="c1 final stream")
+
+
+@pytest.mark.parametrize("layer", [0, 1, 23, 47])
+def test_c1_teacher_forced_layer(moe, c1, layer):
+    layers, dl, ols, x, f = c1
+    xin = f["inputs"][layer].astype(np.float32)
+    ref = oracle.moe_layer(ols[layer], xin.astype(np.float64))
+    g = run_forward(moe, dl, xin, n_layers=1, offset=layer)
+    check_routing(g["idx"][0], None, ref, ref["logits"], 8, f"layer {layer}")
+    assert_close_rows(g["out"], ref["out"], ref["moe"], what=f"c1 layer {layer}")
+
+
+def test_bounded_wait_reports_timeout(moe):
+    """A wait that can never be satisfied gives up within the limit and the
+    kernel reports MOE_ETIMEOUT; the context stays usable afterwards."""
+    rng = np.random.default_rng(300)
+    layers = [synth.make_layer(rng, 256, 8, 2, 128, 4, shared=True)]
+    dl = moe.DeviceLayers(layers)
+    dl.set_flags(moe.TEST_WITHHOLD)
+    x = torch.from_numpy(synth.make_x(rng, 1, 256)).cuda()
+    out = torch.empty_like(x)
+    ws = moe.alloc_workspace(moe.forward_workspace(dl.c, 1, 1))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    old = os.environ.get("MOE_TIMEOUT_MS")
+    os.environ["MOE_TIMEOUT_MS"] = "50"
+    try:
+        moe.forward(dl, x, out, ws, status)
+        torch.cuda.synchronize()
+    finally:
+        if old is None:
+            del os.environ["MOE_TIMEOUT_MS"]
+        else:
+            os.environ["MOE_TIMEOUT_MS"] = old
+    assert status.item() == moe.ETIMEOUT
+    dl.set_flags(0)
+    moe.forward(dl, x, out, ws, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
