@@ -119,7 +119,7 @@ def run_ours(args, rank, world, device):
     name = args.workload
     cfg = synth.CONFIGS[name]
     nb = args.nb or cfg["nb"]
-    layers = synth.make_device_layers(name, seed=1 + rank, device=device)
+    layers = synth.make_device_layers(name, seed=1 + rank, device=device, n_layers=args.layers or None)
     dl = moe.DeviceLayers(layers, device=device)
     nl = dl.n
     H = cfg["hidden"]
@@ -157,10 +157,12 @@ def run_ours(args, rank, world, device):
     if dist:
         td.barrier()
     torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("timed")
     ev0.record(stream)
     for _ in range(args.steps):
         step()
     ev1.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     if dist:
         td.barrier()
@@ -234,6 +236,7 @@ def main():
     ap.add_argument("--workload", default="c1", choices=sorted(WORKLOADS))
     ap.add_argument("--nb", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--layers", type=int, default=0, help="override the stack depth (profiling a smaller case)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -242,14 +245,14 @@ def main():
     from quantized_routed_expert_fn_gb300 import synth
     cfg = synth.CONFIGS[args.workload]
     nb = args.nb or cfg["nb"]
-    config = {"workload": WORKLOADS[args.workload], "nb": nb, "layers": cfg["n_layers"],
+    config = {"workload": WORKLOADS[args.workload], "nb": nb, "layers": args.layers or cfg["n_layers"],
               "l2": "inputs larger than L2 (each step streams every layer's union records once)"}
 
     if args.impl == "reference":
         if rank != 0:
             return
         s = oracle_sample(args.workload, nb, budget_s=min(args.cpu_budget, 20.0))
-        ms = 1000.0 * nb * cfg["n_layers"] / s["value"]
+        ms = 1000.0 * nb * (args.layers or cfg["n_layers"]) / s["value"]
         line = {"metric": METRIC, "value": s["value"], "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config, "impl": "reference",

@@ -126,10 +126,6 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return fail(MOE_ECUDA, "cudaGetDevice failed");
-  int grid = 0;
-  if (moe::decode_grid(dev, H, E, (int)L0.bits, &grid) != 0)
-    return fail(MOE_ECUDA, "decode kernel cannot be resident (shared memory %d bytes)",
-                moe::decode_smem_bytes(H, E, (int)L0.bits));
 
   static_assert(sizeof(moe::FwdParams) < 32000, "kernel parameters too large");
   moe::FwdParams p;
@@ -160,10 +156,13 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
     q.flags = L.flags & (MOE_RESIDUAL | MOE_PRENORM);
     if (L.flags & MOE_TEST_WITHHOLD) p.withhold = 1;
   }
+  int grid = 0, smem = 0;
+  if (moe::decode_plan(dev, p, &grid, &smem) != 0)
+    return fail(MOE_ECUDA, "decode kernel cannot be resident on this device (hidden %d, experts %d)", H, E);
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)nl * moe::kCntPerLayer * 4, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), st);
-  if (e == cudaSuccess) e = moe::launch_decode(p, grid, st);
+  if (e == cudaSuccess) e = moe::launch_decode(p, grid, smem, st);
   if (e != cudaSuccess) return fail(MOE_ECUDA, "launch failed: %s", cudaGetErrorString(e));
   return MOE_OK;
 }

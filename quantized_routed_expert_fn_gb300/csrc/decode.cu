@@ -8,19 +8,21 @@
 //   T  every CTA waits for all router rows, then computes top-k, softmax and
 //      the union itself (identical in every CTA, so no second grid-wide
 //      handshake); CTA 0 publishes slot table, weight map and ids.
-//   G  gate_up units (internal slot, 16 gate rows + the matching 16 up rows):
-//      codes stream from HBM straight into registers, are expanded to exact
-//      bf16 integers and multiplied on the tensor cores against the staged
-//      activations; scale and bias apply per 64-code group in fp32;
-//      h = silu(gate) * up is written as bf16 hi/lo fragments for the down
-//      projection.  A per-slot counter publishes completion.
-//   D  down units (slot, 64 output rows): wait for the slot's h, multiply,
-//      fold the routing weight (or the shared gate) into the result and store
-//      a per-slot partial.  The last unit of a 64-row range (atomic ticket)
-//      sums the slots in a fixed order, adds the residual and writes the
-//      layer output.  No float atomics: results are bitwise reproducible.
-// Every wait polls a counter with a deadline (%globaltimer); on expiry the
-// kernel records MOE_ETIMEOUT and returns instead of hanging.
+//   G  gate_up units (internal slot, 16 gate rows + the matching 16 up rows)
+//   D  down units (slot, 64 output rows).
+// Weight tiles of the units reach shared memory through bulk (TMA) copies:
+// one thread keeps a ring of `stages` units in flight, so HBM streams while
+// the warps compute.  The shared expert's first gate_up units do not depend
+// on routing and are requested before the layer input is even available.
+// Codes are expanded to exact bf16 integers and multiplied on the tensor
+// cores against the staged activations; scale and bias apply per 64-code
+// group in fp32; h = silu(gate) * up is stored as bf16 hi/lo fragments for
+// the down projection; the down result is scaled by the routing weight (or
+// the shared gate) and kept per slot; the last unit of each 64-row range
+// (atomic ticket) sums the slots in a fixed order, adds the residual and
+// writes the layer output.  No float atomics: results are reproducible.
+// Every wait has a deadline (%globaltimer); on expiry the kernel records
+// MOE_ETIMEOUT and returns instead of hanging.
 //
 // Sources: `Gpu::router_b`, `Gpu::experts_b`, `encode_block`, the `slot_tab`
 // / `wmap` fields (struct Gpu page), `union_of`, `struct Q`, `MAX_NB`,
@@ -56,6 +58,9 @@ __device__ __forceinline__ uint32_t split_part(float v, int hl) {
   return hl ? f2bf(v - __uint_as_float(h << 16)) : h;
 }
 
+__device__ __forceinline__ int cdiv_mul(int c, int n, int g) { return (int)(((long long)c * n + g - 1) / g); }
+__device__ __forceinline__ int fdiv_mul(int c, int n, int g) { return (int)((long long)c * n / g); }
+
 // Thread 0: poll *p until it reaches target, the call aborts, or the deadline passes.
 __device__ bool wait_geq(const unsigned *p, unsigned target, const FwdParams &P) {
   const uint64_t t0 = globaltimer();
@@ -73,93 +78,128 @@ __device__ bool wait_geq(const unsigned *p, unsigned target, const FwdParams &P)
 }
 
 __device__ bool cta_wait(const unsigned *p, unsigned target, const FwdParams &P, volatile int *flag) {
-  if (threadIdx.x == 0) {
-    bool ok = wait_geq(p, target, P);
-    __threadfence();
-    *flag = ok;
-  }
+  if (threadIdx.x == 0) *flag = wait_geq(p, target, P);
   __syncthreads();
   const bool ok = *flag;
   __syncthreads();
   return ok;
 }
 
+// All threads: publish this CTA's writes, then add v to *p (release).
 __device__ void cta_signal(unsigned *p, unsigned v) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(p, v);
-  }
+  if (threadIdx.x == 0) red_release_add(p, v);
 }
 
-// Activation fragments of one block of 128 positions for the codec whose pair
-// table is (plo, phi): entry [blk][m][lane] holds the two bf16x2 A registers
-// of MMA step m for lane (g, t): row g = hl*4 + b, value part hl (0 hi, 1 lo)
-// of input row b, at positions 32t + pair code indices.
-__device__ void stage_frags(const float *xf, int H, int nb, const int *plo, const int *phi, uint2 *xa) {
-  const int nblk = H / 128;
-  for (int e = threadIdx.x; e < nblk * 256; e += NT) {
-    const int ln = e & 31, m = (e >> 5) & 7, blk = e >> 8;
-    const int g = ln >> 2, t = ln & 3, hl = g >> 2, b = g & 3;
-    uint32_t r0 = 0, r1 = 0;
-    if (b < nb) {
-      const float *base = xf + b * H + blk * 128 + 32 * t;
-      r0 = split_part(base[plo[2 * m]], hl) | (split_part(base[phi[2 * m]], hl) << 16);
-      r1 = split_part(base[plo[2 * m + 1]], hl) | (split_part(base[phi[2 * m + 1]], hl) << 16);
+// All threads: wait for ring stage `u` (its copies landed).  A wait that
+// passes the deadline records MOE_ETIMEOUT and keeps waiting (the copies
+// in flight target this CTA's shared memory) for up to one more deadline.
+__device__ bool stage_wait(uint64_t *bar, uint32_t parity, const FwdParams &P) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  bool late = false;
+  while (!mbar_try_wait(bar, parity)) {
+    const uint64_t dt = globaltimer() - t0;
+    if (!late && dt > P.timeout_ns) {
+      atomicCAS(P.status, 0, kStatusTimeout);
+      late = true;
     }
-    xa[e] = make_uint2(r0, r1);
+    if (dt > 2 * P.timeout_ns) return false;
+  }
+  return !late;
+}
+
+// Thread 0, on an error return: wait (bounded) for the copies still in
+// flight into this CTA's ring, units [from, to) of the call's sequence.
+__device__ void drain_ring(uint64_t *bars, unsigned from, unsigned to, int S, const FwdParams &P) {
+  if (threadIdx.x != 0) return;
+  for (unsigned u = from; u < to; u++) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&bars[u % S], (u / S) & 1u))
+      if (globaltimer() - t0 > P.timeout_ns) return;
   }
 }
 
+// ------------------------------------------------------------ activation staging
+
+// Thread (blk, b, t) turns the 32 inputs x[b][blk*128 + 32t .. +32) into the
+// bf16 hi / lo A-fragment registers of lanes (hl*4 + b, t) for the 8 MMA
+// steps of the block, in codec B's pair order; also the 64-input group sums.
 template <int B>
-struct ItemRegs {
+__device__ void stage_frags(const float *xf, int H, int nb, uint2 *xa, float *xs) {
+  const int nblk = H / 128;
+  for (int j = threadIdx.x; j < nblk * 16; j += NT) {
+    const int t = j & 3, b = (j >> 2) & 3, blk = j >> 4;
+    float v[32];
+    if (b < nb) {
+      const float4 *src = reinterpret_cast<const float4 *>(xf + b * H + blk * 128 + 32 * t);
+#pragma unroll
+      for (int i = 0; i < 8; i++) {
+        const float4 q = src[i];
+        v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; i++) v[i] = 0.f;
+    }
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+#pragma unroll
+      for (int hl = 0; hl < 2; hl++) {
+        const uint32_t r0 = split_part(v[Codec<B>::lo(2 * m)], hl) | (split_part(v[Codec<B>::hi(2 * m)], hl) << 16);
+        const uint32_t r1 =
+            split_part(v[Codec<B>::lo(2 * m + 1)], hl) | (split_part(v[Codec<B>::hi(2 * m + 1)], hl) << 16);
+        xa[(blk * 8 + m) * 32 + 4 * (hl * 4 + b) + t] = make_uint2(r0, r1);
+      }
+    }
+    if (xs) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; i++) s += v[i];
+      s += __shfl_xor_sync(FULL, s, 1);
+      if ((t & 1) == 0) xs[b * (H / 64) + 2 * blk + (t >> 1)] = s;
+    }
+  }
+}
+
+// ------------------------------------------------------------ tensor-core items
+
+// One item: 8 weight rows x one block of 128 inputs.  Codes and the scale /
+// bias pairs come from the stage in shared memory; a[] are the activation
+// fragments of the block.  Returns, in lanes 0..15 (b = lane/4), the results
+// of rows 2t and 2t+1 of the item (already summed over hi and lo parts).
+template <int B>
+__device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uint8_t *sc, const uint8_t *bi,
+                                             int sp, const uint2 (&a)[8], bool lowT, bool hl0, float xs0,
+                                             float xs1, float mul, float &o0, float &o1) {
   uint32_t w[Codec<B>::kWords];
-  uint32_t s0, s1, b0, b1;
-};
-
-// Load one item: codes of weight row (row0 + g) in block kb, and the scale /
-// bias pairs (groups 2kb, 2kb+1) of rows row0 + 2t and row0 + 2t + 1.
-template <int B>
-__device__ __forceinline__ void load_item(ItemRegs<B> &it, const uint8_t *rec, const QOff &q, int inp,
-                                          int row0, int kb, int g, int t) {
-  const size_t rowbytes = (size_t)inp * B / 8;
-  const uint8_t *cp = rec + q.w + (size_t)(row0 + g) * rowbytes + kb * (16 * B) + t * (4 * B);
   if constexpr (B == 4) {
-    uint4 v = ldg_stream4(cp);
-    it.w[0] = v.x, it.w[1] = v.y, it.w[2] = v.z, it.w[3] = v.w;
+    const uint4 v = *reinterpret_cast<const uint4 *>(codes_row);
+    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
   } else if constexpr (B == 2) {
-    uint2 v = ldg_stream2(cp);
-    it.w[0] = v.x, it.w[1] = v.y;
+    const uint2 v = *reinterpret_cast<const uint2 *>(codes_row);
+    w[0] = v.x, w[1] = v.y;
   } else {
-    it.w[0] = ldg_stream1(cp), it.w[1] = ldg_stream1(cp + 4), it.w[2] = ldg_stream1(cp + 8);
+    const uint32_t *p = reinterpret_cast<const uint32_t *>(codes_row);
+    w[0] = p[0], w[1] = p[1], w[2] = p[2];
   }
-  const size_t sp = (size_t)(inp / 64) * 2;
-  const size_t r = (size_t)(row0 + 2 * t);
-  it.s0 = ldg_stream1(rec + q.s + r * sp + kb * 4);
-  it.s1 = ldg_stream1(rec + q.s + (r + 1) * sp + kb * 4);
-  it.b0 = ldg_stream1(rec + q.b + r * sp + kb * 4);
-  it.b1 = ldg_stream1(rec + q.b + (r + 1) * sp + kb * 4);
-}
-
-// One item on the tensor cores: 8 MMA steps over a block of 128 inputs for
-// 8 weight rows, then per-group scale and bias in fp32.  Returns, in lanes
-// 0..15 (b = lane/4), the results of rows 2t and 2t+1 of the item.
-template <int B>
-__device__ __forceinline__ void item_compute(const ItemRegs<B> &it, const uint2 (&a)[8], bool lowT, bool hl0,
-                                             float xs0, float xs1, float mul, float &o0, float &o1) {
+  const uint32_t s0 = *reinterpret_cast<const uint32_t *>(sc);
+  const uint32_t s1 = *reinterpret_cast<const uint32_t *>(sc + sp);
+  const uint32_t b0 = *reinterpret_cast<const uint32_t *>(bi);
+  const uint32_t b1 = *reinterpret_cast<const uint32_t *>(bi + sp);
   uint32_t bf[16];
-  Codec<B>::unpack(it.w, bf);
+  Codec<B>::unpack(w, bf);
   float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int m = 0; m < 8; m++) {
     const uint32_t x0 = a[m].x, x1 = a[m].y;
     mma_bf16_16816(d, lowT ? x0 : 0u, lowT ? 0u : x0, lowT ? x1 : 0u, lowT ? 0u : x1, bf[2 * m], bf[2 * m + 1]);
   }
-  float r0 = bf16lo(it.s0) * d[0] + bf16hi(it.s0) * d[2];
-  float r1 = bf16lo(it.s1) * d[1] + bf16hi(it.s1) * d[3];
+  float r0 = bf16lo(s0) * d[0] + bf16hi(s0) * d[2];
+  float r1 = bf16lo(s1) * d[1] + bf16hi(s1) * d[3];
   if (hl0) {
-    r0 += bf16lo(it.b0) * xs0 + bf16hi(it.b0) * xs1;
-    r1 += bf16lo(it.b1) * xs0 + bf16hi(it.b1) * xs1;
+    r0 += bf16lo(b0) * xs0 + bf16hi(b0) * xs1;
+    r1 += bf16lo(b1) * xs0 + bf16hi(b1) * xs1;
   }
   r0 *= mul;
   r1 *= mul;
@@ -167,7 +207,7 @@ __device__ __forceinline__ void item_compute(const ItemRegs<B> &it, const uint2 
   o1 = r1 + __shfl_xor_sync(FULL, r1, 16);
 }
 
-// items per warp: the smallest divisor of ntiles that covers all items
+// items per warp: the smallest power of two covering all items, capped at ntiles
 __device__ __forceinline__ int items_per_warp(int nitems, int ntiles) {
   const int need = (nitems + NW - 1) / NW;
   int ipw = 1;
@@ -175,94 +215,70 @@ __device__ __forceinline__ int items_per_warp(int nitems, int ntiles) {
   return ipw < ntiles ? ipw : ntiles;
 }
 
-// gate_up unit: rows [c0, c0+16) of the gate and [I+c0, I+c0+16) of the up
-// projection, all H inputs.  Writes red[(kb*4 + nt)*32 + row*4 + b].
+// Stage layout of a gate_up unit: codes of 16 gate rows then 16 up rows
+// (32 rows), then their scales (32 rows), then their biases (32 rows).
+// Writes red[(kb*4 + nt)*32 + row*4 + b].
 template <int B>
-__device__ void gate_up_unit(const uint8_t *rec, const QOff &q, int H, int I, int c0, const uint2 *xa,
-                             const float *xs, int nb, float *red) {
+__device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const float *xs, int nb, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int nblk = H / 128, ntg = 4;
-  const int nitems = nblk * ntg;
-  const int ipw = items_per_warp(nitems, ntg);
+  const int g = lane >> 2, t = lane & 3, b = g & 3;
+  const int nblk = H / 128;
+  const int nitems = nblk * 4;
+  const int ipw = items_per_warp(nitems, 4);
   const int i0 = warp * ipw;
-  if (i0 < nitems) {
-    const int kb = i0 / ntg;
-    ItemRegs<B> it[MAXIT];
+  if (i0 >= nitems) return;
+  const int kb = i0 >> 2;
+  const int rb = H * B / 8, sp = H / 32;
+  uint2 a[8];
 #pragma unroll
-    for (int k = 0; k < MAXIT; k++) {
-      if (k < ipw) {
-        const int nt = i0 % ntg + k;
-        const int row0 = nt < 2 ? c0 + nt * 8 : I + c0 + (nt - 2) * 8;
-        load_item<B>(it[k], rec, q, H, row0, kb, g, t);
-      }
-    }
-    uint2 a[8];
+  for (int m = 0; m < 8; m++) a[m] = xa[(kb * 8 + m) * 32 + lane];
+  const float xs0 = xs[b * (H / 64) + 2 * kb], xs1 = xs[b * (H / 64) + 2 * kb + 1];
+  const uint8_t *sc = st + 32 * rb, *bi = sc + 32 * sp;
 #pragma unroll
-    for (int m = 0; m < 8; m++) a[m] = xa[(kb * 8 + m) * 32 + lane];
-    const int b = g & 3;
-    const float xs0 = xs[b * (H / 64) + 2 * kb], xs1 = xs[b * (H / 64) + 2 * kb + 1];
-#pragma unroll
-    for (int k = 0; k < MAXIT; k++) {
-      if (k < ipw) {
-        float o0, o1;
-        item_compute<B>(it[k], a, t < 2, g < 4, xs0, xs1, 1.f, o0, o1);
-        const int nt = i0 % ntg + k;
-        if (lane < 16 && b < nb) {
-          red[(kb * ntg + nt) * 32 + (2 * t) * 4 + b] = o0;
-          red[(kb * ntg + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
-        }
+  for (int k = 0; k < MAXIT; k++) {
+    if (k < ipw) {
+      const int nt = (i0 & 3) + k;
+      float o0, o1;
+      item_compute<B>(st + (8 * nt + g) * rb + kb * (16 * B) + t * (4 * B), sc + (8 * nt + 2 * t) * sp + kb * 4,
+                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, a, t < 2, g < 4, xs0, xs1, 1.f, o0, o1);
+      if (lane < 16 && b < nb) {
+        red[(kb * 4 + nt) * 32 + (2 * t) * 4 + b] = o0;
+        red[(kb * 4 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
       }
     }
   }
 }
 
-// down unit: output rows [r0, r0+64) of one slot; A fragments of h come from
-// the workspace.  mul[b] is the routing weight (or shared gate) of row b.
+// Stage layout of a down unit: codes of 64 output rows, their scales, their
+// biases.  a[] / hs0 / hs1: this warp's h fragments and group sums.
 template <int B>
-__device__ void down_unit(const uint8_t *rec, const QOff &q, int H, int I, int r0, const uint2 *hf,
-                          const float *mul, int nb, float *red) {
+__device__ void down_compute(const uint8_t *st, int I, const uint2 (&a)[8], float hs0, float hs1, float mb, int nb,
+                             float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  const int nblk = I / 128;
-  const int nitems = nblk * 8;
+  const int g = lane >> 2, t = lane & 3, b = g & 3;
+  const int nitems = (I / 128) * 8;
   const int ipw = items_per_warp(nitems, 8);
   const int i0 = warp * ipw;
-  if (i0 < nitems) {
-    const int kb = i0 / 8;
-    ItemRegs<B> it[MAXIT];
+  if (i0 >= nitems) return;
+  const int kb = i0 >> 3;
+  const int rb = I * B / 8, sp = I / 32;
+  const uint8_t *sc = st + 64 * rb, *bi = sc + 64 * sp;
 #pragma unroll
-    for (int k = 0; k < MAXIT; k++) {
-      if (k < ipw) load_item<B>(it[k], rec, q, I, r0 + (i0 % 8 + k) * 8, kb, g, t);
-    }
-    uint2 a[8];
-    float hs = 0.f;
-#pragma unroll
-    for (int m = 0; m < 8; m++) {
-      a[m] = __ldcg(hf + (kb * 8 + m) * 32 + lane);
-      hs += bf16lo(a[m].x) + bf16hi(a[m].x) + bf16lo(a[m].y) + bf16hi(a[m].y);
-    }
-    // group sums of h: lanes t, t^1 share a group; add the lo part (g^4)
-    hs += __shfl_xor_sync(FULL, hs, 1);
-    hs += __shfl_xor_sync(FULL, hs, 16);
-    const float other = __shfl_xor_sync(FULL, hs, 2);
-    const float xs0 = t < 2 ? hs : other, xs1 = t < 2 ? other : hs;
-    const int b = g & 3;
-    const float mb = b < nb ? mul[b] : 0.f;
-#pragma unroll
-    for (int k = 0; k < MAXIT; k++) {
-      if (k < ipw) {
-        float o0, o1;
-        item_compute<B>(it[k], a, t < 2, g < 4, xs0, xs1, mb, o0, o1);
-        const int nt = i0 % 8 + k;
-        if (lane < 16 && b < nb) {
-          red[(kb * 8 + nt) * 32 + (2 * t) * 4 + b] = o0;
-          red[(kb * 8 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
-        }
+  for (int k = 0; k < MAXIT; k++) {
+    if (k < ipw) {
+      const int nt = (i0 & 7) + k;
+      float o0, o1;
+      item_compute<B>(st + (8 * nt + g) * rb + kb * (16 * B) + t * (4 * B), sc + (8 * nt + 2 * t) * sp + kb * 4,
+                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, a, t < 2, g < 4, hs0, hs1, mb, o0, o1);
+      if (lane < 16 && b < nb) {
+        red[(kb * 8 + nt) * 32 + (2 * t) * 4 + b] = o0;
+        red[(kb * 8 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
       }
     }
   }
 }
+
+// ------------------------------------------------------------ routing
 
 // Top-k of one row of E logits (ties to the lower id), then softmax over the
 // k chosen.  Lane l holds ids [l*P, l*P+P).
@@ -299,7 +315,7 @@ __device__ void topk_warp(const float *lg, int E, int K, int *idx, float *w) {
 }
 
 // Union of the [nb][K] ids in first-seen order (warp 0).  Writes uni[],
-// wm[b][slot] and returns U in *nu.  rk is 64 ints of scratch.
+// wm[b][slot] and *nu = U.  rk is 64 ints of scratch.
 __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int *uni, float *wm, int *rk,
                            volatile int *nu) {
   const int lane = threadIdx.x & 31;
@@ -340,101 +356,188 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
   __syncwarp();
 }
 
+// ------------------------------------------------------------ unit schedule
+
+struct Sched {
+  int hsi, ups, nrt, U, nslots;
+  int early;        // shared gate_up units assigned before routing
+  int nA, sA0;      // early shared units of this CTA
+  int nB, rB0;      // gate_up units after routing (routed only if early, else shared + routed)
+  int nD, d0;       // down units
+  __device__ int n() const { return nA + nB + nD; }
+};
+
+struct UnitDesc {
+  int down, slot, row0;  // row0: gate_up chunk start (inter rows) or down output row start
+  const uint8_t *rec;
+  QOff q;
+  int bits;
+};
+
+template <int BITS>
+__device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP &L, const int *uni) {
+  UnitDesc d;
+  if (q < s.nA) {
+    d.down = 0, d.slot = 0, d.row0 = (s.sA0 + q) * 16;
+  } else if (q < s.nA + s.nB) {
+    const int r = s.rB0 + (q - s.nA);
+    d.down = 0;
+    d.slot = (s.early ? s.hsi : 0) + r / s.ups;
+    d.row0 = (r % s.ups) * 16;
+  } else {
+    const int r = s.d0 + (q - s.nA - s.nB);
+    d.down = 1, d.slot = r / s.nrt, d.row0 = (r % s.nrt) * 64;
+  }
+  const bool shared = s.hsi && d.slot == 0;
+  d.rec = shared ? L.srec : reinterpret_cast<const uint8_t *>(L.eaddr[uni[d.slot - s.hsi]]);
+  d.q = shared ? (d.down ? L.sdn : L.sgu) : (d.down ? L.dn : L.gu);
+  d.bits = shared ? 4 : BITS;
+  return d;
+}
+
+// Thread 0: request the weight tile of one unit into its ring stage.
+__device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_t *bar, int *status) {
+  if (d.rec == nullptr || ((uintptr_t)d.rec & 15u)) {
+    atomicCAS(status, 0, kStatusDevice);
+    mbar_expect_tx(bar, 0);  // completes the phase with no bytes
+    return;
+  }
+  fence_proxy_async_smem();
+  if (!d.down) {
+    const uint32_t rb = H * d.bits / 8, sp = H / 32;
+    const uint32_t bytes = 32 * rb + 64 * sp;
+    mbar_expect_tx(bar, bytes);
+    const uint8_t *c = d.rec + d.q.w, *s = d.rec + d.q.s, *b = d.rec + d.q.b;
+    bulk_g2s(st, c + (size_t)d.row0 * rb, 16 * rb, bar);
+    bulk_g2s(st + 16 * rb, c + (size_t)(I + d.row0) * rb, 16 * rb, bar);
+    bulk_g2s(st + 32 * rb, s + (size_t)d.row0 * sp, 16 * sp, bar);
+    bulk_g2s(st + 32 * rb + 16 * sp, s + (size_t)(I + d.row0) * sp, 16 * sp, bar);
+    bulk_g2s(st + 32 * rb + 32 * sp, b + (size_t)d.row0 * sp, 16 * sp, bar);
+    bulk_g2s(st + 32 * rb + 48 * sp, b + (size_t)(I + d.row0) * sp, 16 * sp, bar);
+  } else {
+    const uint32_t rb = I * d.bits / 8, sp = I / 32;
+    mbar_expect_tx(bar, 64 * rb + 128 * sp);
+    bulk_g2s(st, d.rec + d.q.w + (size_t)d.row0 * rb, 64 * rb, bar);
+    bulk_g2s(st + 64 * rb, d.rec + d.q.s + (size_t)d.row0 * sp, 64 * sp, bar);
+    bulk_g2s(st + 64 * rb + 64 * sp, d.rec + d.q.b + (size_t)d.row0 * sp, 64 * sp, bar);
+  }
+}
+
+// ------------------------------------------------------------ the kernel
+
 template <int BITS>
 __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ FwdParams P) {
-  extern __shared__ __align__(16) unsigned char sm[];
+  extern __shared__ __align__(128) unsigned char sm[];
   const int H = P.H, E = P.E, K = P.K, I = P.I, nb = P.nb;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = gridDim.x, cta = blockIdx.x;
   const int nblkH = H / 128, nblkI = I / 128;
   const int E1 = (E + 1 + 3) & ~3;
   const int ng = H / 64;
+  const int S = P.stages;
 
-  float *xf = reinterpret_cast<float *>(sm);                 // [4][H]
-  uint2 *xa = reinterpret_cast<uint2 *>(xf + 4 * H);         // [nblkH][8][32] routed codec order
-  uint2 *xa4 = BITS == 4 ? xa : xa + nblkH * 256;            // shared (4-bit) order
-  float *xs = reinterpret_cast<float *>(xa4 + nblkH * 256);  // [4][H/64]
-  float *lg = xs + 4 * ng;                                   // [4][E1]
-  float *red = lg + 4 * E1;                                  // [2048]
-  int *sidx = reinterpret_cast<int *>(red + 2048);           // [4][32]
-  float *sw = reinterpret_cast<float *>(sidx + 128);         // [4][32]
-  int *uni = reinterpret_cast<int *>(sw + 128);              // [64]
-  float *wm = reinterpret_cast<float *>(uni + 64);           // [4][64]
-  float *gam = wm + 256;                                     // [4]
-  volatile int *sflag = reinterpret_cast<volatile int *>(gam + 4);  // [16]
-  int *ptab = const_cast<int *>(reinterpret_cast<volatile int *>(sflag + 16));  // [2 codecs][lo,hi][16]
+  uint8_t *stages = sm;                                                  // [S][stage_bytes]
+  float *xf = reinterpret_cast<float *>(sm + (size_t)S * P.stage_bytes);  // [4][H]
+  uint2 *xa = reinterpret_cast<uint2 *>(xf + 4 * H);                     // [nblkH][8][32] routed codec order
+  uint2 *xa4 = BITS == 4 ? xa : xa + nblkH * 256;                        // shared (4-bit) order
+  float *xs = reinterpret_cast<float *>(xa4 + nblkH * 256);              // [4][H/64]
+  float *lg = xs + 4 * ng;                                               // [4][E1]
+  float *red = lg + 4 * E1;                                              // [2048]
+  int *sidx = reinterpret_cast<int *>(red + 2048);                       // [4][32]
+  float *sw = reinterpret_cast<float *>(sidx + 128);                     // [4][32]
+  int *uni = reinterpret_cast<int *>(sw + 128);                          // [64]
+  float *wm = reinterpret_cast<float *>(uni + 64);                       // [4][64]
+  float *gam = wm + 256;                                                 // [4]
+  volatile int *sflag = reinterpret_cast<volatile int *>(gam + 4);       // [12]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(gam + 16);               // [kMaxStages]
 
-  if (tid < 64) {
-    const int which = tid >> 5, lohi = (tid >> 4) & 1, p = tid & 15;
-    const int bits = which == 0 ? BITS : 4;
-    ptab[tid] = lohi ? pair_hi(bits, p) : pair_lo(bits, p);
+  if (tid == 0) {
+    for (int s = 0; s < S; s++) mbar_init(&bars[s], 1);
+    fence_mbar_init();
   }
   __syncthreads();
-  const int *plo_r = ptab, *phi_r = ptab + 16, *plo_4 = ptab + 32, *phi_4 = ptab + 48;
 
+  unsigned qbase = 0;  // units requested so far in this call (ring position)
   for (int l = 0; l < P.nl; l++) {
     const LayerP &L = P.L[l];
     unsigned *cnt = P.cnt + (size_t)l * kCntPerLayer;
     const bool hs = L.sgate != nullptr;
-    const int hsi = hs ? 1 : 0;
     const float *src = l == 0 ? P.x : P.xbuf + (size_t)l * 4 * H;
     float *dst = l == P.nl - 1 ? P.out : P.xbuf + (size_t)(l + 1) * 4 * H;
 
+    Sched s;
+    s.hsi = hs ? 1 : 0;
+    s.ups = I / 16;
+    s.nrt = H / 64;
+    s.early = hs && !P.route_only && (K + 1) * s.ups >= G;
+    s.sA0 = s.early ? cdiv_mul(cta, s.ups, G) : 0;
+    s.nA = s.early ? cdiv_mul(cta + 1, s.ups, G) - s.sA0 : 0;
+    s.nB = s.nD = s.rB0 = s.d0 = 0;
+    s.U = 0;
+    int issued = 0;
+    if (tid == 0) {
+      for (; issued < s.nA && issued < S; issued++) {
+        const unsigned u = qbase + issued;
+        issue_unit(get_unit<BITS>(issued, s, L, uni), H, I, stages + (size_t)(u % S) * P.stage_bytes,
+                   &bars[u % S], P.status);
+      }
+    }
+    issued = s.nA < S ? s.nA : S;
+
     // ---- R: input, norm, fragments, router rows
-    if (l > 0 && !cta_wait(P.cnt + (size_t)(l - 1) * kCntPerLayer + kCntRows, (unsigned)(H / 64), P, sflag))
+    if (l > 0 && !cta_wait(P.cnt + (size_t)(l - 1) * kCntPerLayer + kCntRows, (unsigned)(H / 64), P, sflag)) {
+      drain_ring(bars, qbase, qbase + issued, S, P);
       return;
+    }
     for (int i = tid; i < 4 * H; i += NT) xf[i] = i < nb * H ? __ldcg(src + i) : 0.f;
     __syncthreads();
     if (L.flags & kPrenorm) {
       if (warp < nb) {
         float ss = 0.f;
-        for (int j = (tid & 31); j < H; j += 32) ss += xf[warp * H + j] * xf[warp * H + j];
+        for (int j = lane; j < H; j += 32) ss += xf[warp * H + j] * xf[warp * H + j];
         ss = warp_sum(ss);
-        if ((tid & 31) == 0) red[warp] = 1.0f / sqrtf(ss / (float)H + 1e-6f);
+        if (lane == 0) red[warp] = 1.0f / sqrtf(ss / (float)H + 1e-6f);
       }
       __syncthreads();
       for (int i = tid; i < nb * H; i += NT) xf[i] *= red[i / H];
       __syncthreads();
     }
-    stage_frags(xf, H, nb, plo_r, phi_r, xa);
-    if (BITS != 4 && hs) stage_frags(xf, H, nb, plo_4, phi_4, xa4);
-    for (int i = tid; i < 4 * ng; i += NT) {
-      const float *p = xf + (i / ng) * H + (i % ng) * 64;
-      float s = 0.f;
-      for (int j = 0; j < 64; j++) s += p[j];
-      xs[i] = s;
-    }
-    const int R = E + hsi;
-    const int rr0 = (int)((long long)cta * R / G), rr1 = (int)((long long)(cta + 1) * R / G);
+    stage_frags<BITS>(xf, H, nb, xa, xs);
+    if (BITS != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr);
+    const int R = E + s.hsi;
+    const int rr0 = fdiv_mul(cta, R, G), rr1 = fdiv_mul(cta + 1, R, G);
     const int nch = H / 256;
     const int nitem = (rr1 - rr0) * nch;
     __syncthreads();
     for (int it = warp; it < nitem; it += NW) {
-      const int row = rr0 + it / nch, ch = it % nch, ln = tid & 31;
+      const int row = rr0 + it / nch, ch = it % nch;
       const uint16_t *wrow = row < E ? L.router + (size_t)row * H : L.sgate;
-      const uint4 wv = ldg_stream4(wrow + ch * 256 + ln * 8);
+      const uint4 wv = ldg_stream4(wrow + ch * 256 + lane * 8);
       const float wf[8] = {bf16lo(wv.x), bf16hi(wv.x), bf16lo(wv.y), bf16hi(wv.y),
                            bf16lo(wv.z), bf16hi(wv.z), bf16lo(wv.w), bf16hi(wv.w)};
       for (int b = 0; b < nb; b++) {
-        const float *xp = xf + b * H + ch * 256 + ln * 8;
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; j++) acc += wf[j] * xp[j];
+        const float4 *xp = reinterpret_cast<const float4 *>(xf + b * H + ch * 256 + lane * 8);
+        const float4 x0 = xp[0], x1 = xp[1];
+        float acc = wf[0] * x0.x + wf[1] * x0.y + wf[2] * x0.z + wf[3] * x0.w + wf[4] * x1.x + wf[5] * x1.y +
+                    wf[6] * x1.z + wf[7] * x1.w;
         acc = warp_sum(acc);
-        if (ln == 0) red[it * 4 + b] = acc;
+        if (lane == 0) red[it * 4 + b] = acc;
       }
     }
     __syncthreads();
     for (int j = tid; j < (rr1 - rr0) * nb; j += NT) {
       const int r = j / nb, b = j % nb;
-      float s = 0.f;
-      for (int ch = 0; ch < nch; ch++) s += red[(r * nch + ch) * 4 + b];
-      P.logits[((size_t)l * 4 + b) * (E + 1) + rr0 + r] = s;
+      float sum = 0.f;
+      for (int ch = 0; ch < nch; ch++) sum += red[(r * nch + ch) * 4 + b];
+      P.logits[((size_t)l * 4 + b) * (E + 1) + rr0 + r] = sum;
     }
     if (rr1 > rr0) cta_signal(cnt + kCntRouter, (unsigned)(rr1 - rr0));
 
     // ---- T: top-k, softmax, union
-    if (!cta_wait(cnt + kCntRouter, (unsigned)(R + (P.withhold ? 1 : 0)), P, sflag)) return;
+    if (!cta_wait(cnt + kCntRouter, (unsigned)(R + (P.withhold ? 1 : 0)), P, sflag)) {
+      drain_ring(bars, qbase, qbase + issued, S, P);
+      return;
+    }
     for (int i = tid; i < nb * (E + 1); i += NT) {
       const int b = i / (E + 1), e = i % (E + 1);
       lg[b * E1 + e] = e < R ? __ldcg(P.logits + ((size_t)l * 4 + b) * (E + 1) + e) : 0.f;
@@ -445,18 +548,19 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     __syncthreads();
     if (warp == 0) union_warp(sidx, sw, nb, K, uni, wm, reinterpret_cast<int *>(red), sflag + 1);
     __syncthreads();
-    const int U = sflag[1];
+    s.U = sflag[1];
     if (cta == 0) {
       if (P.slot_tab)
         for (int j = tid; j < kSlotStride; j += NT) {
-          uint64_t v = j < U ? L.eaddr[uni[j]] : 0ull;
-          if (j == kSlotStride - 2 || j == kSlotStride - 1) v = (uint64_t)U;
+          uint64_t v = j < s.U ? L.eaddr[uni[j]] : 0ull;
+          if (j == kSlotStride - 2 || j == kSlotStride - 1) v = (uint64_t)s.U;
           P.slot_tab[(size_t)l * kSlotStride + j] = v;
         }
       if (P.wmap)
         for (int j = tid; j < kMaxNb * kSlotStride; j += NT) P.wmap[(size_t)l * kMaxNb * kSlotStride + j] = wm[j];
       if (P.topk_idx)
-        for (int j = tid; j < nb * K; j += NT) P.topk_idx[(size_t)l * nb * K + j] = (uint32_t)sidx[(j / K) * 32 + j % K];
+        for (int j = tid; j < nb * K; j += NT)
+          P.topk_idx[(size_t)l * nb * K + j] = (uint32_t)sidx[(j / K) * 32 + j % K];
       if (P.topk_w)
         for (int j = tid; j < nb * K; j += NT) P.topk_w[(size_t)l * nb * K + j] = sw[(j / K) * 32 + j % K];
       if (P.logits_out)
@@ -464,129 +568,207 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     }
     if (P.route_only) continue;
 
-    // ---- G: gate_up units
-    const int nslots = U + hsi;
-    const int ups = I / 16;
-    const int NU = nslots * ups;
-    const int u0 = (int)((long long)cta * NU / G), u1 = (int)((long long)(cta + 1) * NU / G);
-    for (int u = u0; u < u1; u++) {
-      const int slot = u / ups, c0 = (u % ups) * 16;
-      const bool shared = hs && slot == 0;
-      const uint8_t *rec = shared ? L.srec : reinterpret_cast<const uint8_t *>(L.eaddr[uni[slot - hsi]]);
-      const bool ok = rec != nullptr && ((uintptr_t)rec & 15u) == 0;
-      if (!ok && tid == 0) atomicCAS(P.status, 0, kStatusDevice);
-      if (ok) {
-        if (shared)
-          gate_up_unit<4>(rec, L.sgu, H, I, c0, xa4, xs, nb, red);
-        else
-          gate_up_unit<BITS>(rec, L.gu, H, I, c0, xa, xs, nb, red);
-      }
-      __syncthreads();
-      // epilogue: h = silu(gate) * up for 16 rows x nb, scattered as bf16 hi/lo
-      // A fragments in the order of this slot's down codec
-      if (tid < 16 * nb) {
-        const int i = tid & 15, b = tid >> 4;
-        float gsum = 0.f, usum = 0.f;
-        for (int kb = 0; kb < nblkH; kb++) {
-          gsum += red[(kb * 4 + (i >> 3)) * 32 + (i & 7) * 4 + b];
-          usum += red[(kb * 4 + 2 + (i >> 3)) * 32 + (i & 7) * 4 + b];
-        }
-        const float h = ok ? gsum / (1.f + expf(-gsum)) * usum : 0.f;
-        const int pos = c0 + i;
-        const int blk = pos >> 7, c = pos & 127, tq = c >> 5, cc = c & 31;
-        const int *plo = shared ? plo_4 : plo_r, *phi = shared ? phi_4 : phi_r;
-        int pi = 0, el = 0;
-        for (int p = 0; p < 16; p++) {
-          if (plo[p] == cc) pi = p, el = 0;
-          if (phi[p] == cc) pi = p, el = 1;
-        }
-        const uint32_t hi = f2bf(h), lo = f2bf(h - __uint_as_float(hi << 16));
-        uint16_t *hb = P.hfrag + (size_t)slot * nblkI * 8 * 32 * 4;
-        const int m = pi >> 1, reg = pi & 1;
-#pragma unroll
-        for (int hl = 0; hl < 2; hl++) {
-          const int ln = 4 * (hl * 4 + b) + tq;
-          hb[(((blk * 8 + m) * 32 + ln) * 2 + reg) * 2 + el] = (uint16_t)(hl ? lo : hi);
-        }
-      }
-      cta_signal(cnt + kCntGu + slot, 1u);
+    // ---- schedule of this CTA's units for the layer
+    s.nslots = s.U + s.hsi;
+    if (s.early) {
+      const int T = (s.U + 1) * s.ups;  // shared + routed gate_up units
+      s.rB0 = fdiv_mul(cta, T, G) - cdiv_mul(cta, s.ups, G);
+      s.nB = fdiv_mul(cta + 1, T, G) - cdiv_mul(cta + 1, s.ups, G) - s.rB0;
+    } else {
+      const int T = s.nslots * s.ups;
+      s.rB0 = fdiv_mul(cta, T, G);
+      s.nB = fdiv_mul(cta + 1, T, G) - s.rB0;
     }
+    const int ND = s.nslots * s.nrt;
+    s.d0 = fdiv_mul(cta, ND, G);
+    s.nD = fdiv_mul(cta + 1, ND, G) - s.d0;
+    const int n = s.n();
+    if (tid == 0) {
+      for (int q = issued; q < n && q < S; q++) {
+        const unsigned u = qbase + q;
+        issue_unit(get_unit<BITS>(q, s, L, uni), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
+                   P.status);
+      }
+    }
+    issued = n < S ? n : S;
 
-    // ---- D: down units + finalisation
-    const int nrt = H / 64;
-    const int ND = nslots * nrt;
-    const int d0 = (int)((long long)cta * ND / G), d1 = (int)((long long)(cta + 1) * ND / G);
+    // ---- G + D: the unit loop
     int cur = -1;
-    for (int u = d0; u < d1; u++) {
-      const int slot = u / nrt, rt = u % nrt;
-      if (slot != cur) {
-        if (!cta_wait(cnt + kCntGu + slot, (unsigned)ups, P, sflag)) return;
-        cur = slot;
-      }
-      const bool shared = hs && slot == 0;
-      const uint8_t *rec = shared ? L.srec : reinterpret_cast<const uint8_t *>(L.eaddr[uni[slot - hsi]]);
-      const bool ok = rec != nullptr && ((uintptr_t)rec & 15u) == 0;
-      float mul[4];
-#pragma unroll
-      for (int b = 0; b < 4; b++) mul[b] = shared ? gam[b] : wm[b * 64 + slot - hsi];
-      const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag + (size_t)slot * nblkI * 8 * 32 * 4);
-      if (ok) {
-        if (shared)
-          down_unit<4>(rec, L.sdn, H, I, rt * 64, hf, mul, nb, red);
-        else
-          down_unit<BITS>(rec, L.dn, H, I, rt * 64, hf, mul, nb, red);
-      }
-      __syncthreads();
-      for (int j = tid; j < 64 * nb; j += NT) {
-        const int r = j & 63, b = j >> 6;
-        float y = 0.f;
-        if (ok)
-          for (int kb = 0; kb < nblkI; kb++) y += red[(kb * 8 + (r >> 3)) * 32 + (r & 7) * 4 + b];
-        P.ypart[((size_t)slot * 4 + b) * H + rt * 64 + r] = y;
-      }
-      __syncthreads();
-      if (tid == 0) {
-        __threadfence();
-        const unsigned old = atomicAdd(cnt + kCntDn + rt, 1u);
-        sflag[2] = old == (unsigned)(nslots - 1);
-      }
-      __syncthreads();
-      if (sflag[2]) {
-        __threadfence();
-        for (int j = tid; j < 64 * nb; j += NT) {
-          const int r = j & 63, b = j >> 6, o = rt * 64 + r;
-          float s = 0.f;
-          for (int sl = 0; sl < nslots; sl++) s += __ldcg(P.ypart + ((size_t)sl * 4 + b) * H + o);
-          if (L.flags & kResidual) s += __ldcg(src + (size_t)b * H + o);
-          dst[(size_t)b * H + o] = s;
+    uint2 da[8];
+    float hs0 = 0.f, hs1 = 0.f;
+    for (int q = 0; q < n; q++) {
+      const UnitDesc d = get_unit<BITS>(q, s, L, uni);
+      const unsigned u = qbase + q;
+      const uint8_t *st = stages + (size_t)(u % S) * P.stage_bytes;
+      const bool shared = s.hsi && d.slot == 0;
+      if (d.down && d.slot != cur) {
+        // h of this slot complete?  then load this warp's fragments of it
+        if (!cta_wait(cnt + kCntGu + d.slot, (unsigned)s.ups, P, sflag)) {
+          drain_ring(bars, u, qbase + (unsigned)(q + S < n ? q + S : n), S, P);
+          return;
         }
-        cta_signal(cnt + kCntRows, 1u);
+        cur = d.slot;
+        const int nitems = nblkI * 8;
+        const int ipw = items_per_warp(nitems, 8);
+        const int kb = (warp * ipw < nitems) ? (warp * ipw) >> 3 : 0;
+        const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag + (size_t)d.slot * nblkI * 8 * 32 * 4);
+        float hsum = 0.f;
+#pragma unroll
+        for (int m = 0; m < 8; m++) {
+          da[m] = __ldcg(hf + (kb * 8 + m) * 32 + lane);
+          hsum += bf16lo(da[m].x) + bf16hi(da[m].x) + bf16lo(da[m].y) + bf16hi(da[m].y);
+        }
+        hsum += __shfl_xor_sync(FULL, hsum, 1);
+        hsum += __shfl_xor_sync(FULL, hsum, 16);
+        const float other = __shfl_xor_sync(FULL, hsum, 2);
+        hs0 = (lane & 3) < 2 ? hsum : other;
+        hs1 = (lane & 3) < 2 ? other : hsum;
+      }
+      if (!__syncthreads_and(stage_wait(&bars[u % S], (u / S) & 1u, P))) {
+        drain_ring(bars, u + 1, qbase + (unsigned)(q + S < n ? q + S : n), S, P);
+        return;
+      }
+      const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
+      if (ok) {
+        if (!d.down) {
+          if (shared)
+            gate_up_compute<4>(st, H, xa4, xs, nb, red);
+          else
+            gate_up_compute<BITS>(st, H, xa, xs, nb, red);
+        } else {
+          const int b = (lane >> 2) & 3;
+          const float mb = b < nb ? (shared ? gam[b] : wm[b * 64 + d.slot - s.hsi]) : 0.f;
+          if (shared)
+            down_compute<4>(st, I, da, hs0, hs1, mb, nb, red);
+          else
+            down_compute<BITS>(st, I, da, hs0, hs1, mb, nb, red);
+        }
       }
       __syncthreads();
+      // the stage is free: request the unit S places ahead into it
+      if (tid == 0 && q + S < n) {
+        issue_unit(get_unit<BITS>(q + S, s, L, uni), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
+                   P.status);
+      }
+      if (!d.down) {
+        // h = silu(gate) * up for 16 rows x nb, scattered as bf16 hi/lo A
+        // fragments in the pair order of this slot's down codec
+        if (tid < 16 * nb) {
+          const int i = tid & 15, b = tid >> 4;
+          float gsum = 0.f, usum = 0.f;
+          for (int kb = 0; kb < nblkH; kb++) {
+            gsum += red[(kb * 4 + (i >> 3)) * 32 + (i & 7) * 4 + b];
+            usum += red[(kb * 4 + 2 + (i >> 3)) * 32 + (i & 7) * 4 + b];
+          }
+          const float h = ok ? gsum / (1.f + expf(-gsum)) * usum : 0.f;
+          const int pos = d.row0 + i;
+          const int blk = pos >> 7, c = pos & 127, tq = c >> 5, cc = c & 31;
+          int pi = 0, el = 0;
+#pragma unroll
+          for (int p = 0; p < 16; p++) {
+            const int lo = shared || BITS == 4 ? Codec<4>::lo(p) : Codec<BITS>::lo(p);
+            const int hi = shared || BITS == 4 ? Codec<4>::hi(p) : Codec<BITS>::hi(p);
+            if (lo == cc) pi = p, el = 0;
+            if (hi == cc) pi = p, el = 1;
+          }
+          const uint32_t hi = f2bf(h), lo = f2bf(h - __uint_as_float(hi << 16));
+          uint16_t *hb = P.hfrag + (size_t)d.slot * nblkI * 8 * 32 * 4;
+          const int m = pi >> 1, reg = pi & 1;
+          hb[(((blk * 8 + m) * 32 + 4 * b + tq) * 2 + reg) * 2 + el] = (uint16_t)hi;
+          hb[(((blk * 8 + m) * 32 + 4 * (4 + b) + tq) * 2 + reg) * 2 + el] = (uint16_t)lo;
+        }
+        cta_signal(cnt + kCntGu + d.slot, 1u);
+      } else {
+        const int rt = d.row0 / 64;
+        for (int j = tid; j < 64 * nb; j += NT) {
+          const int r = j & 63, b = j >> 6;
+          float y = 0.f;
+          if (ok)
+            for (int kb = 0; kb < nblkI; kb++) y += red[(kb * 8 + (r >> 3)) * 32 + (r & 7) * 4 + b];
+          P.ypart[((size_t)d.slot * 4 + b) * H + d.row0 + r] = y;
+        }
+        __syncthreads();
+        if (tid == 0) sflag[2] = atom_acq_rel_add(cnt + kCntDn + rt, 1u) == (unsigned)(s.nslots - 1);
+        __syncthreads();
+        if (sflag[2]) {
+          // last unit of this 64-row range: sum the slots in a fixed order
+          const int tpo = nb == 1 ? 8 : (nb == 2 ? 4 : 2);
+          for (int j = tid; j < 64 * nb * tpo; j += NT) {
+            const int o = j / tpo, part = j % tpo;
+            const int r = o & 63, b = o >> 6;
+            const float *yp = P.ypart + (size_t)b * H + d.row0 + r;
+            float acc = 0.f;
+#pragma unroll 4
+            for (int sl = part; sl < s.nslots; sl += tpo) acc += __ldcg(yp + (size_t)sl * 4 * H);
+            for (int off = tpo >> 1; off; off >>= 1) acc += __shfl_down_sync(FULL, acc, off, tpo);
+            if (part == 0) {
+              if (L.flags & kResidual) acc += __ldcg(src + (size_t)b * H + d.row0 + r);
+              dst[(size_t)b * H + d.row0 + r] = acc;
+            }
+          }
+          cta_signal(cnt + kCntRows, 1u);
+        }
+        __syncthreads();
+      }
     }
+    qbase += (unsigned)n;
   }
 }
 
 }  // namespace
 
-int decode_smem_bytes(int H, int E, int bits) {
+static int fixed_smem(int H, int E, int bits) {
   const int nblkH = H / 128;
   const int E1 = (E + 1 + 3) & ~3;
-  size_t b = 0;
-  b += (size_t)4 * H * 4;                          // xf
-  b += (size_t)nblkH * 256 * 8 * (bits == 4 ? 1 : 2);  // xa (+ xa4)
-  b += (size_t)4 * (H / 64) * 4;                   // xs
-  b += (size_t)4 * E1 * 4;                         // lg
+  int b = 0;
+  b += 4 * H * 4;                                  // xf
+  b += nblkH * 256 * 8 * (bits == 4 ? 1 : 2);      // xa (+ xa4)
+  b += 4 * (H / 64) * 4;                           // xs
+  b += 4 * E1 * 4;                                 // lg
   b += 2048 * 4;                                   // red
-  b += (128 + 128 + 64 + 256 + 4 + 16 + 64) * 4;   // sidx sw uni wm gam sflag ptab
-  return (int)b;
+  b += (128 + 128 + 64 + 256 + 16) * 4;            // sidx sw uni wm gam+flags
+  b += kMaxStages * 8;                             // barriers
+  return b;
+}
+
+static int stage_bytes(int H, int I) {
+  // the 4-bit tiles are the largest (the shared expert is always 4-bit)
+  const int gu = 32 * (H * 4 / 8) + 64 * (H / 32);
+  const int dn = 64 * (I * 4 / 8) + 128 * (I / 32);
+  const int m = gu > dn ? gu : dn;
+  return (m + 127) & ~127;
 }
 
 template <int BITS>
-static cudaError_t launch_t(const FwdParams &p, int grid, cudaStream_t st) {
-  const int smem = decode_smem_bytes(p.H, p.E, BITS);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
+static int occupancy_t(int smem) {
+  int n = 0;
+  if (cudaFuncSetAttribute(decode_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS>, NT, smem) != cudaSuccess) return 0;
+  return n;
+}
+
+int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes) {
+  int sms = 0, optin = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) return -1;
+  const int fixed = fixed_smem(p.H, p.E, p.bits);
+  const int sb = stage_bytes(p.H, p.I);
+  int S = (optin - fixed) / sb;
+  if (S > kMaxStages) S = kMaxStages;
+  if (S < 1) return -1;
+  p.stages = S;
+  p.stage_bytes = sb;
+  const int smem = fixed + S * sb;
+  const int occ = p.bits == 4 ? occupancy_t<4>(smem) : p.bits == 3 ? occupancy_t<3>(smem) : occupancy_t<2>(smem);
+  if (occ < 1) return -1;
+  *grid = sms;
+  *smem_bytes = smem;
+  return 0;
+}
+
+template <int BITS>
+static cudaError_t launch_t(const FwdParams &p, int grid, int smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(NT);
@@ -600,32 +782,13 @@ static cudaError_t launch_t(const FwdParams &p, int grid, cudaStream_t st) {
   return cudaLaunchKernelEx(&cfg, decode_kernel<BITS>, p);
 }
 
-cudaError_t launch_decode(const FwdParams &p, int grid, cudaStream_t st) {
+cudaError_t launch_decode(const FwdParams &p, int grid, int smem, cudaStream_t st) {
   switch (p.bits) {
-    case 4: return launch_t<4>(p, grid, st);
-    case 3: return launch_t<3>(p, grid, st);
-    case 2: return launch_t<2>(p, grid, st);
+    case 4: return launch_t<4>(p, grid, smem, st);
+    case 3: return launch_t<3>(p, grid, smem, st);
+    case 2: return launch_t<2>(p, grid, smem, st);
     default: return cudaErrorInvalidValue;
   }
-}
-
-template <int BITS>
-static int occupancy_t(int smem) {
-  int n = 0;
-  cudaFuncSetAttribute(decode_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS>, NT, smem) != cudaSuccess) return 0;
-  return n;
-}
-
-// Grid of the cooperative launch: one CTA per SM (all co-resident).
-int decode_grid(int device, int H, int E, int bits, int *grid) {
-  int sms = 0;
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return -1;
-  const int smem = decode_smem_bytes(H, E, bits);
-  const int occ = bits == 4 ? occupancy_t<4>(smem) : bits == 3 ? occupancy_t<3>(smem) : occupancy_t<2>(smem);
-  if (occ < 1) return -1;
-  *grid = sms;
-  return 0;
 }
 
 }  // namespace moe

@@ -45,12 +45,16 @@ struct FwdParams {
   uint16_t *hfrag;        // [64][I/128][8][32][2][2] bf16 activation fragments of h
   float *ypart;           // [64][4][H]   per-slot weighted down outputs
   unsigned long long timeout_ns;
+  int stages;            // weight-tile ring depth (bulk copies in flight)
+  int stage_bytes;       // bytes of one ring stage
   LayerP L[kMaxLayers];
 };
 
+constexpr int kMaxStages = 4;
+
 // Launch helpers (decode.cu)
-int decode_smem_bytes(int H, int E, int bits);
-cudaError_t launch_decode(const FwdParams &p, int grid, cudaStream_t st);
-int decode_grid(int device, int H, int E, int bits, int *grid);
+// Fills p.stages / p.stage_bytes and the grid for this device; returns 0 or -1.
+int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes);
+cudaError_t launch_decode(const FwdParams &p, int grid, int smem_bytes, cudaStream_t st);
 
 }  // namespace moe

@@ -53,7 +53,9 @@ def check_layer(m, layers, x, what, dl=None):
     nb = x.shape[0]
     check_routing(g["idx"][0], None, ref, ref["logits"], layers[0].top_k, what)
     check_union(g["slot"][0], g["wmap"][0], ref, eaddr_of(dl, 0), nb, what)
-    return assert_close_rows(g["out"], ref["out"], ref["moe"], what=what)
+    r = assert_close_rows(g["out"], ref["out"], ref["moe"], what=what)
+    print(f"[parity] {what}: max err = {r:.4f} of the bound (2e-3 x row RMS)")
+    return r
 
 
 def test_c0_one_layer(moe):
@@ -178,6 +180,8 @@ def test_c1_stacked_end_to_end(moe, c1):
     for l in range(len(layers)):
         assert sorted(g["idx"][l][0]) == sorted(f["idx"][l][0]), f"layer {l} ids"
     final = f["out"]
+    err = np.abs(g["out"] - final).max() / (2e-3 * np.sqrt((final ** 2).mean()))
+    print(f"[parity] c1 48-layer final stream: max err = {err:.4f} of 2e-3 x RMS")
     assert_close_rows(g["out"], final, final, what="c1 final stream")
 
 
@@ -188,7 +192,8 @@ def test_c1_teacher_forced_layer(moe, c1, layer):
     ref = oracle.moe_layer(ols[layer], xin.astype(np.float64))
     g = run_forward(moe, dl, xin, n_layers=1, offset=layer)
     check_routing(g["idx"][0], None, ref, ref["logits"], 8, f"layer {layer}")
-    assert_close_rows(g["out"], ref["out"], ref["moe"], what=f"c1 layer {layer}")
+    r = assert_close_rows(g["out"], ref["out"], ref["moe"], what=f"c1 layer {layer}")
+    print(f"[parity] c1 teacher-forced layer {layer}: max err = {r:.4f} of the bound")
 
 
 def test_bounded_wait_reports_timeout(moe):
