@@ -119,12 +119,27 @@ int moe_route(const moe_layer *L, const float *x, int nb, float *logits, uint32_
  *            bytes, 256-byte aligned; its contents need no initialisation
  *   slot_tab [n_layers][64] uint64, wmap [n_layers][4][64] float32 (see moe_route)
  *   topk_idx [n_layers][nb][top_k] uint32, or NULL
- * Supported shapes: hidden % 256 == 0 and <= 4096, inter % 128 == 0 and <= 1024,
+ * Supported shapes: hidden % 256 == 0 and <= 2048, inter % 128 == 0 and <= 1024,
  * n_experts <= 1024, top_k <= 32, top_k * nb < 64, group == 64.
  * Returns MOE_OK or a negative moe_status. */
 int moe_forward(const moe_layer *layers, int n_layers, const float *x, int nb, float *out,
                 void *work, size_t work_bytes, uint64_t *slot_tab, float *wmap,
                 uint32_t *topk_idx, int *dev_status, moe_stream_t stream);
+
+/* moe_forward plus per-phase device timestamps (the `PhaseTimer` / `GpuTiming`
+ * GPU timestamps of the struct Gpu page, here %globaltimer nanoseconds).
+ *   phase_ns  device array [n_layers][MOE_TRACE_CTAS][MOE_TRACE_PHASES] uint64;
+ *             thread 0 of CTA c stamps, for each layer: 0 layer start, 1 layer
+ *             input available, 2 input staged, 3 router rows published,
+ *             4 all router rows seen, 5 expert units start, 6 first down unit,
+ *             7 layer done.  Entries of CTAs beyond the grid, and phases a CTA
+ *             skips (6 when it has no down unit), are left untouched.
+ * Timing costs a few stores per layer; results equal moe_forward's. */
+#define MOE_TRACE_CTAS 1024
+#define MOE_TRACE_PHASES 8
+int moe_forward_traced(const moe_layer *layers, int n_layers, const float *x, int nb, float *out,
+                       void *work, size_t work_bytes, uint64_t *slot_tab, float *wmap,
+                       uint32_t *topk_idx, int *dev_status, uint64_t *phase_ns, moe_stream_t stream);
 
 /* Workspace bytes moe_forward needs for these layers and nb rows (0 if the
  * arguments are invalid). */

@@ -111,7 +111,7 @@ bool overlap(const void *a, size_t na, const void *b, size_t nb) {
 
 int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, void *work, size_t work_bytes,
         uint64_t *slot_tab, float *wmap, uint32_t *topk_idx, float *topk_w, float *logits, int *status,
-        moe_stream_t stream, int route_only) {
+        moe_stream_t stream, int route_only, uint64_t *trace = nullptr) {
   const moe_layer &L0 = layers[0];
   const int H = (int)L0.hidden, E = (int)L0.n_experts, I = (int)L0.inter;
   if (!x) return fail(MOE_EINVAL, "x is NULL");
@@ -142,6 +142,7 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   p.hfrag = (uint16_t *)(base + w.hfrag);
   p.ypart = (float *)(base + w.ypart);
   p.timeout_ns = timeout_ns();
+  p.trace = reinterpret_cast<unsigned long long *>(trace);
   for (int l = 0; l < nl; l++) {
     const moe_layer &L = layers[l];
     moe::LayerP &q = p.L[l];
@@ -197,6 +198,17 @@ int moe_forward(const moe_layer *layers, int n_layers, const float *x, int nb, f
   if (r != MOE_OK) return r;
   return run(layers, n_layers, x, nb, out, work, work_bytes, slot_tab, wmap, topk_idx, nullptr, nullptr,
              dev_status, stream, 0);
+}
+
+int moe_forward_traced(const moe_layer *layers, int n_layers, const float *x, int nb, float *out, void *work,
+                       size_t work_bytes, uint64_t *slot_tab, float *wmap, uint32_t *topk_idx, int *dev_status,
+                       uint64_t *phase_ns, moe_stream_t stream) {
+  int r = check_layers(layers, n_layers, nb);
+  if (r == MOE_OK) r = check_offsets_fit(layers, n_layers);
+  if (r != MOE_OK) return r;
+  if (!phase_ns) return fail(MOE_EINVAL, "phase_ns is NULL");
+  return run(layers, n_layers, x, nb, out, work, work_bytes, slot_tab, wmap, topk_idx, nullptr, nullptr,
+             dev_status, stream, 0, phase_ns);
 }
 
 int moe_route(const moe_layer *L, const float *x, int nb, float *logits, uint32_t *topk_idx, float *topk_w,

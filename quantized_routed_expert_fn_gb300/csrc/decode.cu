@@ -459,6 +459,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
 
   unsigned qbase = 0;  // units requested so far in this call (ring position)
   for (int l = 0; l < P.nl; l++) {
+#define MOE_STAMP(k)                                                                             \
+  if (P.trace && tid == 0 && cta < kTraceCtas)                                                   \
+    P.trace[((size_t)l * kTraceCtas + cta) * kTracePhases + (k)] = globaltimer();
+    MOE_STAMP(0)
     const LayerP &L = P.L[l];
     unsigned *cnt = P.cnt + (size_t)l * kCntPerLayer;
     const bool hs = L.sgate != nullptr;
@@ -489,6 +493,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       drain_ring(bars, qbase, qbase + issued, S, P);
       return;
     }
+    MOE_STAMP(1)
     for (int i = tid; i < 4 * H; i += NT) xf[i] = i < nb * H ? __ldcg(src + i) : 0.f;
     __syncthreads();
     if (L.flags & kPrenorm) {
@@ -509,6 +514,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     const int nch = H / 256;
     const int nitem = (rr1 - rr0) * nch;
     __syncthreads();
+    MOE_STAMP(2)
     for (int it = warp; it < nitem; it += NW) {
       const int row = rr0 + it / nch, ch = it % nch;
       const uint16_t *wrow = row < E ? L.router + (size_t)row * H : L.sgate;
@@ -532,12 +538,14 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       P.logits[((size_t)l * 4 + b) * (E + 1) + rr0 + r] = sum;
     }
     if (rr1 > rr0) cta_signal(cnt + kCntRouter, (unsigned)(rr1 - rr0));
+    MOE_STAMP(3)
 
     // ---- T: top-k, softmax, union
     if (!cta_wait(cnt + kCntRouter, (unsigned)(R + (P.withhold ? 1 : 0)), P, sflag)) {
       drain_ring(bars, qbase, qbase + issued, S, P);
       return;
     }
+    MOE_STAMP(4)
     for (int i = tid; i < nb * (E + 1); i += NT) {
       const int b = i / (E + 1), e = i % (E + 1);
       lg[b * E1 + e] = e < R ? __ldcg(P.logits + ((size_t)l * 4 + b) * (E + 1) + e) : 0.f;
@@ -593,10 +601,12 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     issued = n < S ? n : S;
 
     // ---- G + D: the unit loop
+    MOE_STAMP(5)
     int cur = -1;
     uint2 da[8];
     float hs0 = 0.f, hs1 = 0.f;
     for (int q = 0; q < n; q++) {
+      if (q == s.nA + s.nB) MOE_STAMP(6)
       const UnitDesc d = get_unit<BITS>(q, s, L, uni);
       const unsigned u = qbase + q;
       const uint8_t *st = stages + (size_t)(u % S) * P.stage_bytes;
@@ -712,6 +722,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       }
     }
     qbase += (unsigned)n;
+    MOE_STAMP(7)
+#undef MOE_STAMP
   }
 }
 

@@ -45,12 +45,15 @@ struct FwdParams {
   uint16_t *hfrag;        // [64][I/128][8][32][2][2] bf16 activation fragments of h
   float *ypart;           // [64][4][H]   per-slot weighted down outputs
   unsigned long long timeout_ns;
+  unsigned long long *trace;  // [nl][kTraceCtas][kTracePhases] %globaltimer stamps, or nullptr
   int stages;            // weight-tile ring depth (bulk copies in flight)
   int stage_bytes;       // bytes of one ring stage
   LayerP L[kMaxLayers];
 };
 
 constexpr int kMaxStages = 4;
+constexpr int kTraceCtas = 1024;
+constexpr int kTracePhases = 8;
 
 // Launch helpers (decode.cu)
 // Fills p.stages / p.stage_bytes and the grid for this device; returns 0 or -1.

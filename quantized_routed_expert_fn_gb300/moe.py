@@ -23,7 +23,8 @@ OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EDEVICE, ENOSPACE = 0, -1, -2, -3, 
 STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_EALIGN", -4: "MOE_ECUDA",
                 -5: "MOE_ETIMEOUT", -6: "MOE_EDEVICE", -7: "MOE_ENOSPACE"}
 
-EXPORTS = ["moe_route", "moe_forward", "moe_forward_workspace", "moe_last_error"]
+EXPORTS = ["moe_route", "moe_forward", "moe_forward_traced", "moe_forward_workspace", "moe_last_error"]
+TRACE_CTAS, TRACE_PHASES = 1024, 8
 
 
 class MoeQ(ctypes.Structure):
@@ -64,6 +65,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.moe_forward_workspace.argtypes = [ctypes.POINTER(MoeLayer), i32, i32]
         L.moe_forward.restype = i32
         L.moe_forward.argtypes = [ctypes.POINTER(MoeLayer), i32, vp, i32, vp, vp, sz, vp, vp, vp, vp, vp]
+        L.moe_forward_traced.restype = i32
+        L.moe_forward_traced.argtypes = [ctypes.POINTER(MoeLayer), i32, vp, i32, vp, vp, sz, vp, vp, vp, vp, vp, vp]
         L.moe_route.restype = i32
         L.moe_route.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         _lib = L
@@ -156,6 +159,15 @@ def forward(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, work: torc
     wp, wb = _aligned(work)
     _check(lib().moe_forward(arr, n, _p(x), x.shape[0], _p(out), wp, wb, _p(slot_tab), _p(wmap), _p(topk_idx),
                              _p(status), _stream(stream)))
+
+
+def forward_traced(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, work: torch.Tensor,
+                   status: torch.Tensor, trace: torch.Tensor, slot_tab=None, wmap=None, topk_idx=None,
+                   stream=None) -> None:
+    """moe_forward with per-phase timestamps into trace (int64 [n_layers][1024][8])."""
+    wp, wb = _aligned(work)
+    _check(lib().moe_forward_traced(layers.c, layers.n, _p(x), x.shape[0], _p(out), wp, wb, _p(slot_tab), _p(wmap),
+                                    _p(topk_idx), _p(status), _p(trace), _stream(stream)))
 
 
 def route(layers: DeviceLayers, x: torch.Tensor, topk_idx, topk_w, slot_row, wmap_row, work, status,
