@@ -375,7 +375,8 @@ struct UnitDesc {
 };
 
 template <int BITS>
-__device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP &L, const int *uni) {
+__device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP &L,
+                                             const uint8_t *const *rect) {
   UnitDesc d;
   if (q < s.nA) {
     d.down = 0, d.slot = 0, d.row0 = (s.sA0 + q) * 16;
@@ -389,7 +390,7 @@ __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP
     d.down = 1, d.slot = r / s.nrt, d.row0 = (r % s.nrt) * 64;
   }
   const bool shared = s.hsi && d.slot == 0;
-  d.rec = shared ? L.srec : reinterpret_cast<const uint8_t *>(L.eaddr[uni[d.slot - s.hsi]]);
+  d.rec = shared ? L.srec : rect[d.slot];
   d.q = shared ? (d.down ? L.sdn : L.sgu) : (d.down ? L.dn : L.gu);
   d.bits = shared ? 4 : BITS;
   return d;
@@ -450,6 +451,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   float *gam = wm + 256;                                                 // [4]
   volatile int *sflag = reinterpret_cast<volatile int *>(gam + 4);       // [12]
   uint64_t *bars = reinterpret_cast<uint64_t *>(gam + 16);               // [kMaxStages]
+  const uint8_t **rect = reinterpret_cast<const uint8_t **>(bars + kMaxStages);  // [64] slot -> record
+  uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(rect + 64);                  // [E] expert addresses
 
   if (tid == 0) {
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1);
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     if (tid == 0) {
       for (; issued < s.nA && issued < S; issued++) {
         const unsigned u = qbase + issued;
-        issue_unit(get_unit<BITS>(issued, s, L, uni), H, I, stages + (size_t)(u % S) * P.stage_bytes,
+        issue_unit(get_unit<BITS>(issued, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes,
                    &bars[u % S], P.status);
       }
     }
@@ -494,19 +497,55 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       return;
     }
     MOE_STAMP(1)
-    for (int i = tid; i < 4 * H; i += NT) xf[i] = i < nb * H ? __ldcg(src + i) : 0.f;
-    __syncthreads();
-    if (L.flags & kPrenorm) {
-      if (warp < nb) {
-        float ss = 0.f;
-        for (int j = lane; j < H; j += 32) ss += xf[warp * H + j] * xf[warp * H + j];
-        ss = warp_sum(ss);
-        if (lane == 0) red[warp] = 1.0f / sqrtf(ss / (float)H + 1e-6f);
+    {
+      // one round trip: each thread loads up to 4 float4 of the nb rows
+      const int n4 = nb * H / 4, h4 = H / 4;
+      const float4 *src4 = reinterpret_cast<const float4 *>(src);
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int i = tid + k * NT;
+        v[k] = i < n4 ? __ldcg(src4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      __syncthreads();
-      for (int i = tid; i < nb * H; i += NT) xf[i] *= red[i / H];
-      __syncthreads();
+      if (L.flags & kPrenorm) {
+        // per-row sums of squares: thread partials -> warp sums -> CTA sums (fixed order)
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const int i = tid + k * NT;
+          if (i < n4) {
+            const float q = v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+            ss[i / h4] += q;
+          }
+        }
+#pragma unroll
+        for (int b = 0; b < 4; b++) ss[b] = warp_sum(ss[b]);
+        if (lane == 0)
+          for (int b = 0; b < 4; b++) red[warp * 4 + b] = ss[b];
+        __syncthreads();
+        if (tid < 4) {
+          float t = 0.f;
+          for (int w = 0; w < NW; w++) t += red[w * 4 + tid];
+          red[64 + tid] = 1.0f / sqrtf(t / (float)H + 1e-6f);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const int i = tid + k * NT;
+          if (i < n4) {
+            const float r = red[64 + i / h4];
+            v[k].x *= r, v[k].y *= r, v[k].z *= r, v[k].w *= r;
+          }
+        }
+      }
+      float4 *xf4 = reinterpret_cast<float4 *>(xf);
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int i = tid + k * NT;
+        if (i < H) xf4[i] = v[k];  // rows b >= nb hold zeros
+      }
     }
+    __syncthreads();
     stage_frags<BITS>(xf, H, nb, xa, xs);
     if (BITS != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr);
     const int R = E + s.hsi;
@@ -515,19 +554,34 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     const int nitem = (rr1 - rr0) * nch;
     __syncthreads();
     MOE_STAMP(2)
-    for (int it = warp; it < nitem; it += NW) {
-      const int row = rr0 + it / nch, ch = it % nch;
-      const uint16_t *wrow = row < E ? L.router + (size_t)row * H : L.sgate;
-      const uint4 wv = ldg_stream4(wrow + ch * 256 + lane * 8);
-      const float wf[8] = {bf16lo(wv.x), bf16hi(wv.x), bf16lo(wv.y), bf16hi(wv.y),
-                           bf16lo(wv.z), bf16hi(wv.z), bf16lo(wv.w), bf16hi(wv.w)};
-      for (int b = 0; b < nb; b++) {
-        const float4 *xp = reinterpret_cast<const float4 *>(xf + b * H + ch * 256 + lane * 8);
-        const float4 x0 = xp[0], x1 = xp[1];
-        float acc = wf[0] * x0.x + wf[1] * x0.y + wf[2] * x0.z + wf[3] * x0.w + wf[4] * x1.x + wf[5] * x1.y +
-                    wf[6] * x1.z + wf[7] * x1.w;
-        acc = warp_sum(acc);
-        if (lane == 0) red[it * 4 + b] = acc;
+    {
+      // every router load of this warp in flight at once (<= 4 items per warp)
+      uint4 wv[4];
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int it = warp + k * NW;
+        if (it < nitem) {
+          const int row = rr0 + it / nch, ch = it % nch;
+          const uint16_t *wrow = row < E ? L.router + (size_t)row * H : L.sgate;
+          wv[k] = ldg_stream4(wrow + ch * 256 + lane * 8);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int it = warp + k * NW;
+        if (it < nitem) {
+          const int ch = it % nch;
+          const float wf[8] = {bf16lo(wv[k].x), bf16hi(wv[k].x), bf16lo(wv[k].y), bf16hi(wv[k].y),
+                               bf16lo(wv[k].z), bf16hi(wv[k].z), bf16lo(wv[k].w), bf16hi(wv[k].w)};
+          for (int b = 0; b < nb; b++) {
+            const float4 *xp = reinterpret_cast<const float4 *>(xf + b * H + ch * 256 + lane * 8);
+            const float4 x0 = xp[0], x1 = xp[1];
+            float acc = wf[0] * x0.x + wf[1] * x0.y + wf[2] * x0.z + wf[3] * x0.w + wf[4] * x1.x +
+                        wf[5] * x1.y + wf[6] * x1.z + wf[7] * x1.w;
+            acc = warp_sum(acc);
+            if (lane == 0) red[it * 4 + b] = acc;
+          }
+        }
       }
     }
     __syncthreads();
@@ -539,6 +593,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     }
     if (rr1 > rr0) cta_signal(cnt + kCntRouter, (unsigned)(rr1 - rr0));
     MOE_STAMP(3)
+    // expert addresses (for the slot table) while the other CTAs finish their router rows
+    for (int e = tid; e < E; e += NT) eaddr_s[e] = L.eaddr[e];
 
     // ---- T: top-k, softmax, union
     if (!cta_wait(cnt + kCntRouter, (unsigned)(R + (P.withhold ? 1 : 0)), P, sflag)) {
@@ -557,10 +613,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     if (warp == 0) union_warp(sidx, sw, nb, K, uni, wm, reinterpret_cast<int *>(red), sflag + 1);
     __syncthreads();
     s.U = sflag[1];
+    if (tid < s.U) rect[tid + s.hsi] = reinterpret_cast<const uint8_t *>(eaddr_s[uni[tid]]);
     if (cta == 0) {
       if (P.slot_tab)
         for (int j = tid; j < kSlotStride; j += NT) {
-          uint64_t v = j < s.U ? L.eaddr[uni[j]] : 0ull;
+          uint64_t v = j < s.U ? eaddr_s[uni[j]] : 0ull;
           if (j == kSlotStride - 2 || j == kSlotStride - 1) v = (uint64_t)s.U;
           P.slot_tab[(size_t)l * kSlotStride + j] = v;
         }
@@ -577,6 +634,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     if (P.route_only) continue;
 
     // ---- schedule of this CTA's units for the layer
+    __syncthreads();
     s.nslots = s.U + s.hsi;
     if (s.early) {
       const int T = (s.U + 1) * s.ups;  // shared + routed gate_up units
@@ -594,7 +652,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     if (tid == 0) {
       for (int q = issued; q < n && q < S; q++) {
         const unsigned u = qbase + q;
-        issue_unit(get_unit<BITS>(q, s, L, uni), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
+        issue_unit(get_unit<BITS>(q, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
                    P.status);
       }
     }
@@ -606,8 +664,17 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     uint2 da[8];
     float hs0 = 0.f, hs1 = 0.f;
     for (int q = 0; q < n; q++) {
-      if (q == s.nA + s.nB) MOE_STAMP(6)
-      const UnitDesc d = get_unit<BITS>(q, s, L, uni);
+      if (q == s.nA + s.nB) {
+        MOE_STAMP(6)
+        if (tid == 0 && l + 1 < P.nl) {
+          // the next layer's router rows of this CTA, toward L2 while the down units run
+          const LayerP &Ln = P.L[l + 1];
+          const int re = rr1 < E ? rr1 : E;
+          if (re > rr0) prefetch_l2(Ln.router + (size_t)rr0 * H, (uint32_t)((re - rr0) * H * 2));
+          if (rr1 > E && Ln.sgate) prefetch_l2(Ln.sgate, (uint32_t)(H * 2));
+        }
+      }
+      const UnitDesc d = get_unit<BITS>(q, s, L, rect);
       const unsigned u = qbase + q;
       const uint8_t *st = stages + (size_t)(u % S) * P.stage_bytes;
       const bool shared = s.hsi && d.slot == 0;
@@ -657,19 +724,31 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       __syncthreads();
       // the stage is free: request the unit S places ahead into it
       if (tid == 0 && q + S < n) {
-        issue_unit(get_unit<BITS>(q + S, s, L, uni), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
+        issue_unit(get_unit<BITS>(q + S, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
                    P.status);
       }
       if (!d.down) {
         // h = silu(gate) * up for 16 rows x nb, scattered as bf16 hi/lo A
         // fragments in the pair order of this slot's down codec
+        // lanes (row i of 32 = 16 gate + 16 up, b, kb-part): sums over the blocks
+        {
+          const int i = tid >> 4, kp = tid & 15;  // 512 threads = 32 rows x 16 parts
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int kb = kp; kb < nblkH; kb += 16) {
+            const float4 r4 = *reinterpret_cast<const float4 *>(&red[(kb * 4 + (i >> 3)) * 32 + (i & 7) * 4]);
+            acc[0] += r4.x, acc[1] += r4.y, acc[2] += r4.z, acc[3] += r4.w;
+          }
+#pragma unroll
+          for (int b = 0; b < 4; b++)
+#pragma unroll
+            for (int o = 8; o; o >>= 1) acc[b] += __shfl_xor_sync(FULL, acc[b], o);
+          __syncthreads();
+          if (kp == 0) *reinterpret_cast<float4 *>(&red[i * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+          __syncthreads();
+        }
         if (tid < 16 * nb) {
           const int i = tid & 15, b = tid >> 4;
-          float gsum = 0.f, usum = 0.f;
-          for (int kb = 0; kb < nblkH; kb++) {
-            gsum += red[(kb * 4 + (i >> 3)) * 32 + (i & 7) * 4 + b];
-            usum += red[(kb * 4 + 2 + (i >> 3)) * 32 + (i & 7) * 4 + b];
-          }
+          const float gsum = red[i * 4 + b], usum = red[(16 + i) * 4 + b];
           const float h = ok ? gsum / (1.f + expf(-gsum)) * usum : 0.f;
           const int pos = d.row0 + i;
           const int blk = pos >> 7, c = pos & 127, tq = c >> 5, cc = c & 31;
@@ -740,6 +819,8 @@ static int fixed_smem(int H, int E, int bits) {
   b += 2048 * 4;                                   // red
   b += (128 + 128 + 64 + 256 + 16) * 4;            // sidx sw uni wm gam+flags
   b += kMaxStages * 8;                             // barriers
+  b += 64 * 8;                                     // slot -> record table
+  b += ((E + 1) & ~1) * 8;                         // expert addresses
   return b;
 }
 
