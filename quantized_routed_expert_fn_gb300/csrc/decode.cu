@@ -38,6 +38,7 @@ namespace {
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int MAXIT = 4;
+constexpr int kProducer = 32;  // issues the bulk copies (thread 0 does the cross-CTA releases)
 constexpr unsigned FULL = 0xffffffffu;
 constexpr uint32_t kResidual = 1, kPrenorm = 2;
 
@@ -56,6 +57,13 @@ __device__ __forceinline__ uint32_t orderable(float f) {
 __device__ __forceinline__ uint32_t split_part(float v, int hl) {
   uint32_t h = f2bf(v);
   return hl ? f2bf(v - __uint_as_float(h << 16)) : h;
+}
+
+// (a, b) -> bf16x2 hi = (bf16(a), bf16(b)) and lo = bf16 of the remainders (a first, low half)
+__device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t &lo) {
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(hi) : "f"(b), "f"(a));
+  const float ra = a - __uint_as_float(hi << 16), rb = b - __uint_as_float(hi & 0xffff0000u);
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(rb), "f"(ra));
 }
 
 __device__ __forceinline__ int cdiv_mul(int c, int n, int g) { return (int)(((long long)c * n + g - 1) / g); }
@@ -112,7 +120,7 @@ __device__ bool stage_wait(uint64_t *bar, uint32_t parity, const FwdParams &P) {
 // Thread 0, on an error return: wait (bounded) for the copies still in
 // flight into this CTA's ring, units [from, to) of the call's sequence.
 __device__ void drain_ring(uint64_t *bars, unsigned from, unsigned to, int S, const FwdParams &P) {
-  if (threadIdx.x != 0) return;
+  if (threadIdx.x != 0) return;  // any one thread keeps the CTA (and its ring) alive until the copies land
   for (unsigned u = from; u < to; u++) {
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&bars[u % S], (u / S) & 1u))
@@ -144,13 +152,11 @@ __device__ void stage_frags(const float *xf, int H, int nb, uint2 *xa, float *xs
     }
 #pragma unroll
     for (int m = 0; m < 8; m++) {
-#pragma unroll
-      for (int hl = 0; hl < 2; hl++) {
-        const uint32_t r0 = split_part(v[Codec<B>::lo(2 * m)], hl) | (split_part(v[Codec<B>::hi(2 * m)], hl) << 16);
-        const uint32_t r1 =
-            split_part(v[Codec<B>::lo(2 * m + 1)], hl) | (split_part(v[Codec<B>::hi(2 * m + 1)], hl) << 16);
-        xa[(blk * 8 + m) * 32 + 4 * (hl * 4 + b) + t] = make_uint2(r0, r1);
-      }
+      uint32_t hi0, lo0, hi1, lo1;
+      split2(v[Codec<B>::lo(2 * m)], v[Codec<B>::hi(2 * m)], hi0, lo0);
+      split2(v[Codec<B>::lo(2 * m + 1)], v[Codec<B>::hi(2 * m + 1)], hi1, lo1);
+      xa[(blk * 8 + m) * 32 + 4 * b + t] = make_uint2(hi0, hi1);
+      xa[(blk * 8 + m) * 32 + 4 * (4 + b) + t] = make_uint2(lo0, lo1);
     }
     if (xs) {
       float s = 0.f;
@@ -403,7 +409,6 @@ __device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_
     mbar_expect_tx(bar, 0);  // completes the phase with no bytes
     return;
   }
-  fence_proxy_async_smem();
   if (!d.down) {
     const uint32_t rb = H * d.bits / 8, sp = H / 32;
     const uint32_t bytes = 32 * rb + 64 * sp;
@@ -482,7 +487,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.nB = s.nD = s.rB0 = s.d0 = 0;
     s.U = 0;
     int issued = 0;
-    if (tid == 0) {
+    if (tid == kProducer) {
       for (; issued < s.nA && issued < S; issued++) {
         const unsigned u = qbase + issued;
         issue_unit(get_unit<BITS>(issued, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes,
@@ -649,7 +654,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.d0 = fdiv_mul(cta, ND, G);
     s.nD = fdiv_mul(cta + 1, ND, G) - s.d0;
     const int n = s.n();
-    if (tid == 0) {
+    if (tid == kProducer) {
       for (int q = issued; q < n && q < S; q++) {
         const unsigned u = qbase + q;
         issue_unit(get_unit<BITS>(q, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
@@ -723,7 +728,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       }
       __syncthreads();
       // the stage is free: request the unit S places ahead into it
-      if (tid == 0 && q + S < n) {
+      if (tid == kProducer && q + S < n) {
         issue_unit(get_unit<BITS>(q + S, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
                    P.status);
       }
