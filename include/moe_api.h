@@ -132,11 +132,14 @@ int moe_forward(const moe_layer *layers, int n_layers, const float *x, int nb, f
  *             thread 0 of CTA c stamps, for each layer: 0 layer start, 1 layer
  *             input available, 2 input staged, 3 router rows published,
  *             4 all router rows seen, 5 expert units start, 6 first down unit,
- *             7 layer done.  Entries of CTAs beyond the grid, and phases a CTA
- *             skips (6 when it has no down unit), are left untouched.
+ *             7 layer done, 8 logits loaded, 9 top-k done, 10 union done,
+ *             11 first unit's tile landed, 12 first unit computed, 13 first
+ *             unit published, 14 last gate_up unit published, 15 first down
+ *             unit published.  Entries of CTAs beyond the grid, and phases a
+ *             CTA skips, are left untouched.
  * Timing costs a few stores per layer; results equal moe_forward's. */
 #define MOE_TRACE_CTAS 1024
-#define MOE_TRACE_PHASES 8
+#define MOE_TRACE_PHASES 16
 int moe_forward_traced(const moe_layer *layers, int n_layers, const float *x, int nb, float *out,
                        void *work, size_t work_bytes, uint64_t *slot_tab, float *wmap,
                        uint32_t *topk_idx, int *dev_status, uint64_t *phase_ns, moe_stream_t stream);

@@ -612,11 +612,14 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       lg[b * E1 + e] = e < R ? __ldcg(P.logits + ((size_t)l * 4 + b) * (E + 1) + e) : 0.f;
     }
     __syncthreads();
+    MOE_STAMP(8)
     if (warp < nb) topk_warp(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
     if (tid < 4) gam[tid] = (hs && tid < nb) ? 1.f / (1.f + expf(-lg[tid * E1 + E])) : 0.f;
     __syncthreads();
+    MOE_STAMP(9)
     if (warp == 0) union_warp(sidx, sw, nb, K, uni, wm, reinterpret_cast<int *>(red), sflag + 1);
     __syncthreads();
+    MOE_STAMP(10)
     s.U = sflag[1];
     if (tid < s.U) rect[tid + s.hsi] = reinterpret_cast<const uint8_t *>(eaddr_s[uni[tid]]);
     if (cta == 0) {
@@ -710,6 +713,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         drain_ring(bars, u + 1, qbase + (unsigned)(q + S < n ? q + S : n), S, P);
         return;
       }
+      if (q == 0) MOE_STAMP(11)
       const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
       if (ok) {
         if (!d.down) {
@@ -727,6 +731,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         }
       }
       __syncthreads();
+      if (q == 0) MOE_STAMP(12)
       // the stage is free: request the unit S places ahead into it
       if (tid == kProducer && q + S < n) {
         issue_unit(get_unit<BITS>(q + S, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
@@ -772,6 +777,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           hb[(((blk * 8 + m) * 32 + 4 * (4 + b) + tq) * 2 + reg) * 2 + el] = (uint16_t)lo;
         }
         cta_signal(cnt + kCntGu + d.slot, 1u);
+        if (q == 0) MOE_STAMP(13)
+        if (q == s.nA + s.nB - 1) MOE_STAMP(14)
       } else {
         const int rt = d.row0 / 64;
         for (int j = tid; j < 64 * nb; j += NT) {
@@ -803,6 +810,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           cta_signal(cnt + kCntRows, 1u);
         }
         __syncthreads();
+        if (q == s.nA + s.nB) MOE_STAMP(15)
       }
     }
     qbase += (unsigned)n;

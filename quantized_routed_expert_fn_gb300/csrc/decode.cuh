@@ -53,7 +53,7 @@ struct FwdParams {
 
 constexpr int kMaxStages = 4;
 constexpr int kTraceCtas = 1024;
-constexpr int kTracePhases = 8;
+constexpr int kTracePhases = 16;
 
 // Launch helpers (decode.cu)
 // Fills p.stages / p.stage_bytes and the grid for this device; returns 0 or -1.

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_EALIGN
                 -5: "MOE_ETIMEOUT", -6: "MOE_EDEVICE", -7: "MOE_ENOSPACE"}
 
 EXPORTS = ["moe_route", "moe_forward", "moe_forward_traced", "moe_forward_workspace", "moe_last_error"]
-TRACE_CTAS, TRACE_PHASES = 1024, 8
+TRACE_CTAS, TRACE_PHASES = 1024, 16
 
 
 class MoeQ(ctypes.Structure):
@@ -164,7 +164,7 @@ def forward(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, work: torc
 def forward_traced(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, work: torch.Tensor,
                    status: torch.Tensor, trace: torch.Tensor, slot_tab=None, wmap=None, topk_idx=None,
                    stream=None) -> None:
-    """moe_forward with per-phase timestamps into trace (int64 [n_layers][1024][8])."""
+    """moe_forward with per-phase timestamps into trace (int64 [n_layers][1024][16])."""
     wp, wb = _aligned(work)
     _check(lib().moe_forward_traced(layers.c, layers.n, _p(x), x.shape[0], _p(out), wp, wb, _p(slot_tab), _p(wmap),
                                     _p(topk_idx), _p(status), _p(trace), _stream(stream)))
