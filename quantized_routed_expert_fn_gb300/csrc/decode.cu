@@ -66,8 +66,9 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t 
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(rb), "f"(ra));
 }
 
-__device__ __forceinline__ int cdiv_mul(int c, int n, int g) { return (int)(((long long)c * n + g - 1) / g); }
-__device__ __forceinline__ int fdiv_mul(int c, int n, int g) { return (int)((long long)c * n / g); }
+// ceil(c*n/g), floor(c*n/g); c*n stays far below 2^31 for every shape accepted
+__device__ __forceinline__ int cdiv_mul(int c, int n, int g) { return (c * n + g - 1) / g; }
+__device__ __forceinline__ int fdiv_mul(int c, int n, int g) { return c * n / g; }
 
 // Thread 0: poll *p until it reaches target, the call aborts, or the deadline passes.
 __device__ bool wait_geq(const unsigned *p, unsigned target, const FwdParams &P) {
@@ -170,13 +171,29 @@ __device__ void stage_frags(const float *xf, int H, int nb, uint2 *xa, float *xs
 
 // ------------------------------------------------------------ tensor-core items
 
+// The four A registers of each MMA step: lanes with t < 2 carry codes of the
+// block's first group (A rows 0..7), lanes with t >= 2 of its second group
+// (rows 8..15); the other half of each lane's A fragment is zero.
+struct AFrag {
+  uint32_t r[8][4];
+};
+__device__ __forceinline__ void make_afrag(const uint2 (&x)[8], bool lowT, AFrag &A) {
+#pragma unroll
+  for (int m = 0; m < 8; m++) {
+    A.r[m][0] = lowT ? x[m].x : 0u;
+    A.r[m][1] = lowT ? 0u : x[m].x;
+    A.r[m][2] = lowT ? x[m].y : 0u;
+    A.r[m][3] = lowT ? 0u : x[m].y;
+  }
+}
+
 // One item: 8 weight rows x one block of 128 inputs.  Codes and the scale /
-// bias pairs come from the stage in shared memory; a[] are the activation
+// bias pairs come from the stage in shared memory; A holds the activation
 // fragments of the block.  Returns, in lanes 0..15 (b = lane/4), the results
 // of rows 2t and 2t+1 of the item (already summed over hi and lo parts).
 template <int B>
 __device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uint8_t *sc, const uint8_t *bi,
-                                             int sp, const uint2 (&a)[8], bool lowT, bool hl0, float xs0,
+                                             int sp, const AFrag &A, bool hl0, float xs0,
                                              float xs1, float mul, float &o0, float &o1) {
   uint32_t w[Codec<B>::kWords];
   if constexpr (B == 4) {
@@ -195,12 +212,14 @@ __device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uin
   const uint32_t b1 = *reinterpret_cast<const uint32_t *>(bi + sp);
   uint32_t bf[16];
   Codec<B>::unpack(w, bf);
-  float d[4] = {0.f, 0.f, 0.f, 0.f};
+  float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int m = 0; m < 8; m++) {
-    const uint32_t x0 = a[m].x, x1 = a[m].y;
-    mma_bf16_16816(d, lowT ? x0 : 0u, lowT ? 0u : x0, lowT ? x1 : 0u, lowT ? 0u : x1, bf[2 * m], bf[2 * m + 1]);
+  for (int m = 0; m < 8; m += 2) {
+    mma_bf16_16816(d, A.r[m][0], A.r[m][1], A.r[m][2], A.r[m][3], bf[2 * m], bf[2 * m + 1]);
+    mma_bf16_16816(e, A.r[m + 1][0], A.r[m + 1][1], A.r[m + 1][2], A.r[m + 1][3], bf[2 * m + 2], bf[2 * m + 3]);
   }
+#pragma unroll
+  for (int i = 0; i < 4; i++) d[i] += e[i];
   float r0 = bf16lo(s0) * d[0] + bf16hi(s0) * d[2];
   float r1 = bf16lo(s1) * d[1] + bf16hi(s1) * d[3];
   if (hl0) {
@@ -238,15 +257,17 @@ __device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const
   uint2 a[8];
 #pragma unroll
   for (int m = 0; m < 8; m++) a[m] = xa[(kb * 8 + m) * 32 + lane];
+  AFrag A;
+  make_afrag(a, t < 2, A);
   const float xs0 = xs[b * (H / 64) + 2 * kb], xs1 = xs[b * (H / 64) + 2 * kb + 1];
   const uint8_t *sc = st + 32 * rb, *bi = sc + 32 * sp;
-#pragma unroll
-  for (int k = 0; k < MAXIT; k++) {
-    if (k < ipw) {
+#pragma unroll 1
+  for (int k = 0; k < ipw; k++) {
+    {
       const int nt = (i0 & 3) + k;
       float o0, o1;
       item_compute<B>(st + (8 * nt + g) * rb + kb * (16 * B) + t * (4 * B), sc + (8 * nt + 2 * t) * sp + kb * 4,
-                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, a, t < 2, g < 4, xs0, xs1, 1.f, o0, o1);
+                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, A, g < 4, xs0, xs1, 1.f, o0, o1);
       if (lane < 16 && b < nb) {
         red[(kb * 4 + nt) * 32 + (2 * t) * 4 + b] = o0;
         red[(kb * 4 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
@@ -258,7 +279,7 @@ __device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const
 // Stage layout of a down unit: codes of 64 output rows, their scales, their
 // biases.  a[] / hs0 / hs1: this warp's h fragments and group sums.
 template <int B>
-__device__ void down_compute(const uint8_t *st, int I, const uint2 (&a)[8], float hs0, float hs1, float mb, int nb,
+__device__ void down_compute(const uint8_t *st, int I, const AFrag &A, float hs0, float hs1, float mb, int nb,
                              float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3, b = g & 3;
@@ -269,13 +290,13 @@ __device__ void down_compute(const uint8_t *st, int I, const uint2 (&a)[8], floa
   const int kb = i0 >> 3;
   const int rb = I * B / 8, sp = I / 32;
   const uint8_t *sc = st + 64 * rb, *bi = sc + 64 * sp;
-#pragma unroll
-  for (int k = 0; k < MAXIT; k++) {
-    if (k < ipw) {
+#pragma unroll 1
+  for (int k = 0; k < ipw; k++) {
+    {
       const int nt = (i0 & 7) + k;
       float o0, o1;
       item_compute<B>(st + (8 * nt + g) * rb + kb * (16 * B) + t * (4 * B), sc + (8 * nt + 2 * t) * sp + kb * 4,
-                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, a, t < 2, g < 4, hs0, hs1, mb, o0, o1);
+                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, A, g < 4, hs0, hs1, mb, o0, o1);
       if (lane < 16 && b < nb) {
         red[(kb * 8 + nt) * 32 + (2 * t) * 4 + b] = o0;
         red[(kb * 8 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
@@ -286,32 +307,42 @@ __device__ void down_compute(const uint8_t *st, int I, const uint2 (&a)[8], floa
 
 // ------------------------------------------------------------ routing
 
-// Top-k of one row of E logits (ties to the lower id), then softmax over the
-// k chosen.  Lane l holds ids [l*P, l*P+P).
+// Top-k of one row of E <= 1024 logits (ties to the lower id), then softmax
+// over the k chosen.  Lane l holds ids [l*P, l*P+P) as order-preserving keys
+// in registers; each round one warp max picks the winner, whose lane alone
+// rescans its keys.
 __device__ void topk_warp(const float *lg, int E, int K, int *idx, float *w) {
   const int lane = threadIdx.x & 31;
   const int P = (E + 31) / 32;
-  uint32_t taken = 0;
+  uint32_t key[32];
+#pragma unroll
+  for (int i = 0; i < 32; i++) {
+    const int e = lane * P + i;
+    key[i] = (i < P && e < E) ? orderable(lg[e]) : 0u;
+  }
+  uint32_t bk = 0;
+  int bi = 0;
+#pragma unroll
+  for (int i = 0; i < 32; i++)
+    if (key[i] > bk) bk = key[i], bi = i;
+#pragma unroll 1
   for (int r = 0; r < K; r++) {
-    uint32_t bk = 0;
-    int bi = 0;
-    for (int i = 0; i < P; i++) {
-      const int e = lane * P + i;
-      if (e < E && !((taken >> i) & 1u)) {
-        const uint32_t key = orderable(lg[e]);
-        if (key > bk) bk = key, bi = i;
-      }
-    }
     const uint32_t m = __reduce_max_sync(FULL, bk);
-    const uint32_t bal = __ballot_sync(FULL, bk == m);
-    const int wl = __ffs(bal) - 1;
+    const int wl = __ffs(__ballot_sync(FULL, bk == m)) - 1;
     if (lane == wl) {
-      taken |= 1u << bi;
       idx[r] = lane * P + bi;
       w[r] = lg[lane * P + bi];
+      uint32_t nbk = 0;
+      int nbi = 0;
+#pragma unroll
+      for (int i = 0; i < 32; i++) {
+        if (i == bi) key[i] = 0u;
+        if (key[i] > nbk) nbk = key[i], nbi = i;
+      }
+      bk = nbk, bi = nbi;
     }
-    __syncwarp();
   }
+  __syncwarp();
   const float mx = w[0];
   const float ev = lane < K ? expf(w[lane] - mx) : 0.f;
   const float z = warp_sum(ev);
@@ -321,25 +352,31 @@ __device__ void topk_warp(const float *lg, int E, int K, int *idx, float *w) {
 }
 
 // Union of the [nb][K] ids in first-seen order (warp 0).  Writes uni[],
-// wm[b][slot] and *nu = U.  rk is 64 ints of scratch.
+// wm[b][slot] and *nu = U.  rk is 64 ints of scratch.  Position p = b*K + r.
 __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int *uni, float *wm, int *rk,
                            volatile int *nu) {
   const int lane = threadIdx.x & 31;
-  const int n = nb * K;
   for (int j = lane; j < 256; j += 32) wm[j] = 0.f;
-  int id[2], first[2], fpos[2];
+  int id[2], first[2], fpos[2], pb[2], pr[2];
 #pragma unroll
   for (int h = 0; h < 2; h++) {
     const int pos = lane + 32 * h;
+    int b = 0, r = pos;
+    while (b < nb && r >= K) r -= K, b++;
+    pb[h] = b, pr[h] = r;
     id[h] = -1, first[h] = 0, fpos[h] = pos;
-    if (pos < n) {
-      id[h] = sidx[(pos / K) * 32 + pos % K];
+    if (b < nb) {
+      id[h] = sidx[b * 32 + r];
       first[h] = 1;
-      for (int j = 0; j < pos; j++) {
-        if (sidx[(j / K) * 32 + j % K] == id[h]) {
-          first[h] = 0;
-          fpos[h] = j;
-          break;
+      int q = 0;
+      for (int b2 = 0; b2 <= b && first[h]; b2++) {
+        const int rend = b2 < b ? K : r;
+        for (int r2 = 0; r2 < rend; r2++, q++) {
+          if (sidx[b2 * 32 + r2] == id[h]) {
+            first[h] = 0;
+            fpos[h] = q;
+            break;
+          }
         }
       }
     }
@@ -351,11 +388,10 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
   __syncwarp();
 #pragma unroll
   for (int h = 0; h < 2; h++) {
-    const int pos = lane + 32 * h;
-    if (pos < n) {
+    if (pb[h] < nb) {
       const int slot = rk[fpos[h]];
       if (first[h]) uni[slot] = id[h];
-      wm[(pos / K) * 64 + slot] = sw[(pos / K) * 32 + pos % K];
+      wm[pb[h] * 64 + slot] = sw[pb[h] * 32 + pr[h]];
     }
   }
   if (lane == 0) *nu = __popc(b0) + __popc(b1);
@@ -669,7 +705,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     // ---- G + D: the unit loop
     MOE_STAMP(5)
     int cur = -1;
-    uint2 da[8];
+    AFrag DA;
     float hs0 = 0.f, hs1 = 0.f;
     for (int q = 0; q < n; q++) {
       if (q == s.nA + s.nB) {
@@ -698,11 +734,13 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         const int kb = (warp * ipw < nitems) ? (warp * ipw) >> 3 : 0;
         const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag + (size_t)d.slot * nblkI * 8 * 32 * 4);
         float hsum = 0.f;
+        uint2 da[8];
 #pragma unroll
-        for (int m = 0; m < 8; m++) {
-          da[m] = __ldcg(hf + (kb * 8 + m) * 32 + lane);
+        for (int m = 0; m < 8; m++) da[m] = __ldcg(hf + (kb * 8 + m) * 32 + lane);
+#pragma unroll
+        for (int m = 0; m < 8; m++)
           hsum += bf16lo(da[m].x) + bf16hi(da[m].x) + bf16lo(da[m].y) + bf16hi(da[m].y);
-        }
+        make_afrag(da, (lane & 3) < 2, DA);
         hsum += __shfl_xor_sync(FULL, hsum, 1);
         hsum += __shfl_xor_sync(FULL, hsum, 16);
         const float other = __shfl_xor_sync(FULL, hsum, 2);
@@ -725,9 +763,9 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           const int b = (lane >> 2) & 3;
           const float mb = b < nb ? (shared ? gam[b] : wm[b * 64 + d.slot - s.hsi]) : 0.f;
           if (shared)
-            down_compute<4>(st, I, da, hs0, hs1, mb, nb, red);
+            down_compute<4>(st, I, DA, hs0, hs1, mb, nb, red);
           else
-            down_compute<BITS>(st, I, da, hs0, hs1, mb, nb, red);
+            down_compute<BITS>(st, I, DA, hs0, hs1, mb, nb, red);
         }
       }
       __syncthreads();
