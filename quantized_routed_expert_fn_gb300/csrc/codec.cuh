@@ -17,8 +17,12 @@
 // k-slots (2t, 2t+1) and (2t+8, 2t+9).  Which code goes to which pair is a
 // free permutation (the dot product does not care) chosen so that one mask
 // places both codes of a pair in the mantissas of 128.0 (bf16 0x4300):
-// 128 + q*2^s is exact for q*2^s < 128; one bf16 FMA by 2^-s then removes
-// the offset exactly.  The activation fragments use the same permutation.
+// the B value is 128 + q*2^s, exact for q*2^s < 128.  Neither the 2^s nor
+// the 128 is removed here: the activation at that k-slot is pre-scaled by
+// 2^-s (exact), so the product is q*x + 128*2^-s*x, and the MMA accumulator
+// starts at -128 * sum(2^-s * x) over the group, which cancels the offset.
+// Unpacking is therefore only shifts and one mask-or per pair.  The
+// activation fragments use the same permutation and exponents.
 #pragma once
 
 #include <cstdint>
@@ -29,10 +33,8 @@ namespace moe {
 
 constexpr uint32_t kMagic = 0x43004300u;  // bf16x2 (128, 128)
 
-// bf16 of 2^-s, and of -128 * 2^-s
-__host__ __device__ constexpr uint32_t bf_pow2neg(int s) { return 0x3f80u - 0x80u * (uint32_t)s; }
-__host__ __device__ constexpr uint32_t bf_off(int s) { return 0xc300u - 0x80u * (uint32_t)s; }
-__host__ __device__ constexpr uint32_t pk(uint32_t lo, uint32_t hi) { return lo | (hi << 16); }
+// 2^-s as a float (s = 0..7)
+__host__ __device__ constexpr float pow2neg(int s) { return 1.0f / (float)(1 << s); }
 
 template <int BITS>
 struct Codec;
@@ -43,14 +45,13 @@ struct Codec<4> {
   static constexpr int kWords = 4;
   __host__ __device__ static constexpr int lo(int p) { return 8 * (p / 4) + p % 4; }
   __host__ __device__ static constexpr int hi(int p) { return lo(p) + 4; }
+  __host__ __device__ static constexpr int slo(int) { return 0; }
+  __host__ __device__ static constexpr int shi(int) { return 0; }
   __device__ static __forceinline__ void unpack(const uint32_t (&w)[kWords], uint32_t (&bf)[16]) {
 #pragma unroll
     for (int p = 0; p < 4; p++) {
 #pragma unroll
-      for (int j = 0; j < 4; j++) {
-        uint32_t v = ((w[p] >> (4 * j)) & 0x000f000fu) | kMagic;
-        bf[4 * p + j] = bfma2(v, 0x3f803f80u, 0xc300c300u);
-      }
+      for (int j = 0; j < 4; j++) bf[4 * p + j] = ((w[p] >> (4 * j)) & 0x000f000fu) | kMagic;
     }
   }
 };
@@ -62,17 +63,18 @@ struct Codec<2> {
   static constexpr int kWords = 2;
   __host__ __device__ static constexpr int lo(int p) { return 16 * (p / 8) + p % 8; }
   __host__ __device__ static constexpr int hi(int p) { return lo(p) + 8; }
+  // pair j of a word is read from w >> 6k, k = j / 3, at shift s = 2 (j - 3k)
+  __host__ __device__ static constexpr int slo(int p) { return 2 * (p % 8 - 3 * ((p % 8) / 3)); }
+  __host__ __device__ static constexpr int shi(int p) { return slo(p); }
   __device__ static __forceinline__ void unpack(const uint32_t (&w)[kWords], uint32_t (&bf)[16]) {
 #pragma unroll
     for (int p = 0; p < 2; p++) {
       const uint32_t src[3] = {w[p], w[p] >> 6, w[p] >> 12};
 #pragma unroll
       for (int j = 0; j < 8; j++) {
-        const int k = j < 3 ? 0 : (j < 6 ? 1 : 2);
-        const int s = 2 * (j - 3 * k);
+        const int s = slo(j);
         const uint32_t mask = (3u << s) | (3u << (16 + s));
-        uint32_t v = (src[k] & mask) | kMagic;
-        bf[8 * p + j] = bfma2(v, pk(bf_pow2neg(s), bf_pow2neg(s)), pk(bf_off(s), bf_off(s)));
+        bf[8 * p + j] = (src[j / 3] & mask) | kMagic;
       }
     }
   }
@@ -101,6 +103,8 @@ struct Codec<3> {
   static constexpr int kWords = 3;
   __host__ __device__ static constexpr int lo(int p) { return pair3(p).lo; }
   __host__ __device__ static constexpr int hi(int p) { return pair3(p).hi; }
+  __host__ __device__ static constexpr int slo(int p) { return pair3(p).slo; }
+  __host__ __device__ static constexpr int shi(int p) { return pair3(p).shi; }
   __device__ static __forceinline__ uint32_t window(const uint32_t (&w)[kWords], int o) {
     if (o < 0) return w[0] << (-o);
     if (o == 0) return w[0];
@@ -116,18 +120,10 @@ struct Codec<3> {
       const Pair3 q = pair3(p);
       const uint32_t win = window(w, q.o);
       const uint32_t mask = (7u << q.slo) | (7u << (16 + q.shi));
-      uint32_t v = (win & mask) | kMagic;
-      bf[p] = bfma2(v, pk(bf_pow2neg(q.slo), bf_pow2neg(q.shi)), pk(bf_off(q.slo), bf_off(q.shi)));
+      bf[p] = (win & mask) | kMagic;
     }
   }
 };
 
-// Runtime lookup of the pair tables (activation staging and h scatter).
-__host__ __device__ inline int pair_lo(int bits, int p) {
-  return bits == 4 ? Codec<4>::lo(p) : (bits == 2 ? Codec<2>::lo(p) : Codec<3>::lo(p));
-}
-__host__ __device__ inline int pair_hi(int bits, int p) {
-  return bits == 4 ? Codec<4>::hi(p) : (bits == 2 ? Codec<2>::hi(p) : Codec<3>::hi(p));
-}
 
 }  // namespace moe

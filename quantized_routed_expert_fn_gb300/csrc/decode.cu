@@ -133,9 +133,11 @@ __device__ void drain_ring(uint64_t *bars, unsigned from, unsigned to, int S, co
 
 // Thread (blk, b, t) turns the 32 inputs x[b][blk*128 + 32t .. +32) into the
 // bf16 hi / lo A-fragment registers of lanes (hl*4 + b, t) for the 8 MMA
-// steps of the block, in codec B's pair order; also the 64-input group sums.
+// steps of the block, in codec B's pair order, each input pre-scaled by the
+// 2^-s of its pair half (exact).  Also per 64-input group: xs = sum of x
+// (bias term) and cs = 128 * sum of 2^-s x (the offset the codes carry).
 template <int B>
-__device__ void stage_frags(const float *xf, int H, int nb, uint2 *xa, float *xs) {
+__device__ void stage_frags(const float *xf, int H, int nb, uint2 *xa, float *xs, float *cs) {
   const int nblk = H / 128;
   for (int j = threadIdx.x; j < nblk * 16; j += NT) {
     const int t = j & 3, b = (j >> 2) & 3, blk = j >> 4;
@@ -151,20 +153,28 @@ __device__ void stage_frags(const float *xf, int H, int nb, uint2 *xa, float *xs
 #pragma unroll
       for (int i = 0; i < 32; i++) v[i] = 0.f;
     }
+    float sx = 0.f, sc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; i++) sx += v[i];
 #pragma unroll
     for (int m = 0; m < 8; m++) {
+      const int p0 = 2 * m, p1 = 2 * m + 1;
+      const float a0 = v[Codec<B>::lo(p0)] * pow2neg(Codec<B>::slo(p0));
+      const float a1 = v[Codec<B>::hi(p0)] * pow2neg(Codec<B>::shi(p0));
+      const float a2 = v[Codec<B>::lo(p1)] * pow2neg(Codec<B>::slo(p1));
+      const float a3 = v[Codec<B>::hi(p1)] * pow2neg(Codec<B>::shi(p1));
+      sc += (a0 + a1) + (a2 + a3);
       uint32_t hi0, lo0, hi1, lo1;
-      split2(v[Codec<B>::lo(2 * m)], v[Codec<B>::hi(2 * m)], hi0, lo0);
-      split2(v[Codec<B>::lo(2 * m + 1)], v[Codec<B>::hi(2 * m + 1)], hi1, lo1);
+      split2(a0, a1, hi0, lo0);
+      split2(a2, a3, hi1, lo1);
       xa[(blk * 8 + m) * 32 + 4 * b + t] = make_uint2(hi0, hi1);
       xa[(blk * 8 + m) * 32 + 4 * (4 + b) + t] = make_uint2(lo0, lo1);
     }
-    if (xs) {
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < 32; i++) s += v[i];
-      s += __shfl_xor_sync(FULL, s, 1);
-      if ((t & 1) == 0) xs[b * (H / 64) + 2 * blk + (t >> 1)] = s;
+    sx += __shfl_xor_sync(FULL, sx, 1);
+    sc += __shfl_xor_sync(FULL, sc, 1);
+    if ((t & 1) == 0) {
+      if (xs) xs[b * (H / 64) + 2 * blk + (t >> 1)] = sx;
+      cs[b * (H / 64) + 2 * blk + (t >> 1)] = 128.f * sc;
     }
   }
 }
@@ -191,10 +201,13 @@ __device__ __forceinline__ void make_afrag(const uint2 (&x)[8], bool lowT, AFrag
 // bias pairs come from the stage in shared memory; A holds the activation
 // fragments of the block.  Returns, in lanes 0..15 (b = lane/4), the results
 // of rows 2t and 2t+1 of the item (already summed over hi and lo parts).
+// ci0 / ci1: accumulator start of the lane's rows for the block's two groups
+// (minus the offset sum on hi lanes, 0 on lo lanes); xs0 / xs1: the groups'
+// input sums on hi lanes, 0 on lo lanes (so the bias enters once).
 template <int B>
 __device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uint8_t *sc, const uint8_t *bi,
-                                             int sp, const AFrag &A, bool hl0, float xs0,
-                                             float xs1, float mul, float &o0, float &o1) {
+                                             int sp, const AFrag &A, float ci0, float ci1, float xs0,
+                                             float xs1, float &o0, float &o1) {
   uint32_t w[Codec<B>::kWords];
   if constexpr (B == 4) {
     const uint4 v = *reinterpret_cast<const uint4 *>(codes_row);
@@ -212,7 +225,7 @@ __device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uin
   const uint32_t b1 = *reinterpret_cast<const uint32_t *>(bi + sp);
   uint32_t bf[16];
   Codec<B>::unpack(w, bf);
-  float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+  float d[4] = {ci0, ci0, ci1, ci1}, e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int m = 0; m < 8; m += 2) {
     mma_bf16_16816(d, A.r[m][0], A.r[m][1], A.r[m][2], A.r[m][3], bf[2 * m], bf[2 * m + 1]);
@@ -222,12 +235,8 @@ __device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uin
   for (int i = 0; i < 4; i++) d[i] += e[i];
   float r0 = bf16lo(s0) * d[0] + bf16hi(s0) * d[2];
   float r1 = bf16lo(s1) * d[1] + bf16hi(s1) * d[3];
-  if (hl0) {
-    r0 += bf16lo(b0) * xs0 + bf16hi(b0) * xs1;
-    r1 += bf16lo(b1) * xs0 + bf16hi(b1) * xs1;
-  }
-  r0 *= mul;
-  r1 *= mul;
+  r0 += bf16lo(b0) * xs0 + bf16hi(b0) * xs1;
+  r1 += bf16lo(b1) * xs0 + bf16hi(b1) * xs1;
   o0 = r0 + __shfl_xor_sync(FULL, r0, 16);
   o1 = r1 + __shfl_xor_sync(FULL, r1, 16);
 }
@@ -243,8 +252,16 @@ __device__ __forceinline__ int items_per_warp(int nitems, int ntiles) {
 // Stage layout of a gate_up unit: codes of 16 gate rows then 16 up rows
 // (32 rows), then their scales (32 rows), then their biases (32 rows).
 // Writes red[(kb*4 + nt)*32 + row*4 + b].
+#ifdef MOE_DEBUG_CYCLES
+__device__ long long g_dbg_cycles[64];
+#define MOE_DBG(k) if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < 4) g_dbg_cycles[(threadIdx.x >> 5) * 16 + (k)] = clock64();
+#else
+#define MOE_DBG(k)
+#endif
+
 template <int B>
-__device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const float *xs, int nb, float *red) {
+__device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const float *xs, const float *cs, int nb,
+                                float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3, b = g & 3;
   const int nblk = H / 128;
@@ -254,12 +271,16 @@ __device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const
   if (i0 >= nitems) return;
   const int kb = i0 >> 2;
   const int rb = H * B / 8, sp = H / 32;
+  MOE_DBG(0)
   uint2 a[8];
 #pragma unroll
   for (int m = 0; m < 8; m++) a[m] = xa[(kb * 8 + m) * 32 + lane];
   AFrag A;
   make_afrag(a, t < 2, A);
-  const float xs0 = xs[b * (H / 64) + 2 * kb], xs1 = xs[b * (H / 64) + 2 * kb + 1];
+  MOE_DBG(1)
+  const bool hl0 = g < 4;
+  const float xs0 = hl0 ? xs[b * (H / 64) + 2 * kb] : 0.f, xs1 = hl0 ? xs[b * (H / 64) + 2 * kb + 1] : 0.f;
+  const float ci0 = hl0 ? -cs[b * (H / 64) + 2 * kb] : 0.f, ci1 = hl0 ? -cs[b * (H / 64) + 2 * kb + 1] : 0.f;
   const uint8_t *sc = st + 32 * rb, *bi = sc + 32 * sp;
 #pragma unroll 1
   for (int k = 0; k < ipw; k++) {
@@ -267,11 +288,12 @@ __device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const
       const int nt = (i0 & 3) + k;
       float o0, o1;
       item_compute<B>(st + (8 * nt + g) * rb + kb * (16 * B) + t * (4 * B), sc + (8 * nt + 2 * t) * sp + kb * 4,
-                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, A, g < 4, xs0, xs1, 1.f, o0, o1);
+                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, A, ci0, ci1, xs0, xs1, o0, o1);
       if (lane < 16 && b < nb) {
         red[(kb * 4 + nt) * 32 + (2 * t) * 4 + b] = o0;
         red[(kb * 4 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
       }
+      MOE_DBG(2 + k)
     }
   }
 }
@@ -279,8 +301,8 @@ __device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const
 // Stage layout of a down unit: codes of 64 output rows, their scales, their
 // biases.  a[] / hs0 / hs1: this warp's h fragments and group sums.
 template <int B>
-__device__ void down_compute(const uint8_t *st, int I, const AFrag &A, float hs0, float hs1, float mb, int nb,
-                             float *red) {
+__device__ void down_compute(const uint8_t *st, int I, const uint2 (&x)[8], float ci0, float ci1, float hs0,
+                             float hs1, int nb, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3, b = g & 3;
   const int nitems = (I / 128) * 8;
@@ -289,6 +311,8 @@ __device__ void down_compute(const uint8_t *st, int I, const AFrag &A, float hs0
   if (i0 >= nitems) return;
   const int kb = i0 >> 3;
   const int rb = I * B / 8, sp = I / 32;
+  AFrag A;
+  make_afrag(x, t < 2, A);
   const uint8_t *sc = st + 64 * rb, *bi = sc + 64 * sp;
 #pragma unroll 1
   for (int k = 0; k < ipw; k++) {
@@ -296,7 +320,7 @@ __device__ void down_compute(const uint8_t *st, int I, const AFrag &A, float hs0
       const int nt = (i0 & 7) + k;
       float o0, o1;
       item_compute<B>(st + (8 * nt + g) * rb + kb * (16 * B) + t * (4 * B), sc + (8 * nt + 2 * t) * sp + kb * 4,
-                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, A, g < 4, hs0, hs1, mb, o0, o1);
+                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, A, ci0, ci1, hs0, hs1, o0, o1);
       if (lane < 16 && b < nb) {
         red[(kb * 8 + nt) * 32 + (2 * t) * 4 + b] = o0;
         red[(kb * 8 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
@@ -311,19 +335,20 @@ __device__ void down_compute(const uint8_t *st, int I, const AFrag &A, float hs0
 // over the k chosen.  Lane l holds ids [l*P, l*P+P) as order-preserving keys
 // in registers; each round one warp max picks the winner, whose lane alone
 // rescans its keys.
+template <int PM>
 __device__ void topk_warp(const float *lg, int E, int K, int *idx, float *w) {
   const int lane = threadIdx.x & 31;
   const int P = (E + 31) / 32;
-  uint32_t key[32];
+  uint32_t key[PM];
 #pragma unroll
-  for (int i = 0; i < 32; i++) {
+  for (int i = 0; i < PM; i++) {
     const int e = lane * P + i;
     key[i] = (i < P && e < E) ? orderable(lg[e]) : 0u;
   }
   uint32_t bk = 0;
   int bi = 0;
 #pragma unroll
-  for (int i = 0; i < 32; i++)
+  for (int i = 0; i < PM; i++)
     if (key[i] > bk) bk = key[i], bi = i;
 #pragma unroll 1
   for (int r = 0; r < K; r++) {
@@ -335,7 +360,7 @@ __device__ void topk_warp(const float *lg, int E, int K, int *idx, float *w) {
       uint32_t nbk = 0;
       int nbi = 0;
 #pragma unroll
-      for (int i = 0; i < 32; i++) {
+      for (int i = 0; i < PM; i++) {
         if (i == bi) key[i] = 0u;
         if (key[i] > nbk) nbk = key[i], nbi = i;
       }
@@ -482,8 +507,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   float *xf = reinterpret_cast<float *>(sm + (size_t)S * P.stage_bytes);  // [4][H]
   uint2 *xa = reinterpret_cast<uint2 *>(xf + 4 * H);                     // [nblkH][8][32] routed codec order
   uint2 *xa4 = BITS == 4 ? xa : xa + nblkH * 256;                        // shared (4-bit) order
-  float *xs = reinterpret_cast<float *>(xa4 + nblkH * 256);              // [4][H/64]
-  float *lg = xs + 4 * ng;                                               // [4][E1]
+  float *xs = reinterpret_cast<float *>(xa4 + nblkH * 256);              // [4][H/64] group sums of x
+  float *cs = xs + 4 * ng;                                               // [4][H/64] offset sums, routed order
+  float *cs4 = cs + 4 * ng;                                              // [4][H/64] offset sums, 4-bit order
+  float *lg = cs4 + 4 * ng;                                              // [4][E1]
   float *red = lg + 4 * E1;                                              // [2048]
   int *sidx = reinterpret_cast<int *>(red + 2048);                       // [4][32]
   float *sw = reinterpret_cast<float *>(sidx + 128);                     // [4][32]
@@ -587,8 +614,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       }
     }
     __syncthreads();
-    stage_frags<BITS>(xf, H, nb, xa, xs);
-    if (BITS != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr);
+    stage_frags<BITS>(xf, H, nb, xa, xs, cs);
+    if (BITS != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr, cs4);
     const int R = E + s.hsi;
     const int rr0 = fdiv_mul(cta, R, G), rr1 = fdiv_mul(cta + 1, R, G);
     const int nch = H / 256;
@@ -649,7 +676,16 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     }
     __syncthreads();
     MOE_STAMP(8)
-    if (warp < nb) topk_warp(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+    if (warp < nb) {
+      if (E <= 128)
+        topk_warp<4>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+      else if (E <= 256)
+        topk_warp<8>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+      else if (E <= 512)
+        topk_warp<16>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+      else
+        topk_warp<32>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+    }
     if (tid < 4) gam[tid] = (hs && tid < nb) ? 1.f / (1.f + expf(-lg[tid * E1 + E])) : 0.f;
     __syncthreads();
     MOE_STAMP(9)
@@ -705,8 +741,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     // ---- G + D: the unit loop
     MOE_STAMP(5)
     int cur = -1;
-    AFrag DA;
-    float hs0 = 0.f, hs1 = 0.f;
+    uint2 da[8];
+    float hs0 = 0.f, hs1 = 0.f, dc0 = 0.f, dc1 = 0.f;
     for (int q = 0; q < n; q++) {
       if (q == s.nA + s.nB) {
         MOE_STAMP(6)
@@ -733,19 +769,36 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         const int ipw = items_per_warp(nitems, 8);
         const int kb = (warp * ipw < nitems) ? (warp * ipw) >> 3 : 0;
         const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag + (size_t)d.slot * nblkI * 8 * 32 * 4);
-        float hsum = 0.f;
-        uint2 da[8];
 #pragma unroll
         for (int m = 0; m < 8; m++) da[m] = __ldcg(hf + (kb * 8 + m) * 32 + lane);
+        // sums of the lane's 32 fragment values: as the MMA sees them (scaled
+        // by 2^-s: the offset) and unscaled (h itself: the bias term)
+        float ssc = 0.f, sun = 0.f;
+        if (shared || BITS == 4) {
 #pragma unroll
-        for (int m = 0; m < 8; m++)
-          hsum += bf16lo(da[m].x) + bf16hi(da[m].x) + bf16lo(da[m].y) + bf16hi(da[m].y);
-        make_afrag(da, (lane & 3) < 2, DA);
-        hsum += __shfl_xor_sync(FULL, hsum, 1);
-        hsum += __shfl_xor_sync(FULL, hsum, 16);
-        const float other = __shfl_xor_sync(FULL, hsum, 2);
-        hs0 = (lane & 3) < 2 ? hsum : other;
-        hs1 = (lane & 3) < 2 ? other : hsum;
+          for (int m = 0; m < 8; m++)
+            ssc += bf16lo(da[m].x) + bf16hi(da[m].x) + bf16lo(da[m].y) + bf16hi(da[m].y);
+          sun = ssc;
+        } else {
+#pragma unroll
+          for (int m = 0; m < 8; m++) {
+            const float v0 = bf16lo(da[m].x), v1 = bf16hi(da[m].x), v2 = bf16lo(da[m].y), v3 = bf16hi(da[m].y);
+            ssc += v0 + v1 + v2 + v3;
+            sun += v0 * (float)(1 << Codec<BITS>::slo(2 * m)) + v1 * (float)(1 << Codec<BITS>::shi(2 * m)) +
+                   v2 * (float)(1 << Codec<BITS>::slo(2 * m + 1)) + v3 * (float)(1 << Codec<BITS>::shi(2 * m + 1));
+          }
+        }
+        // lanes t, t^1 share a group; add the lo part (lane ^ 16)
+        ssc += __shfl_xor_sync(FULL, ssc, 1);
+        ssc += __shfl_xor_sync(FULL, ssc, 16);
+        sun += __shfl_xor_sync(FULL, sun, 1);
+        sun += __shfl_xor_sync(FULL, sun, 16);
+        const float osc = __shfl_xor_sync(FULL, ssc, 2), oun = __shfl_xor_sync(FULL, sun, 2);
+        const bool hl0 = (lane >> 2) < 4, first = (lane & 3) < 2;
+        hs0 = hl0 ? (first ? sun : oun) : 0.f;
+        hs1 = hl0 ? (first ? oun : sun) : 0.f;
+        dc0 = hl0 ? -128.f * (first ? ssc : osc) : 0.f;
+        dc1 = hl0 ? -128.f * (first ? osc : ssc) : 0.f;
       }
       if (!__syncthreads_and(stage_wait(&bars[u % S], (u / S) & 1u, P))) {
         drain_ring(bars, u + 1, qbase + (unsigned)(q + S < n ? q + S : n), S, P);
@@ -756,16 +809,14 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       if (ok) {
         if (!d.down) {
           if (shared)
-            gate_up_compute<4>(st, H, xa4, xs, nb, red);
+            gate_up_compute<4>(st, H, xa4, xs, BITS == 4 ? cs : cs4, nb, red);
           else
-            gate_up_compute<BITS>(st, H, xa, xs, nb, red);
+            gate_up_compute<BITS>(st, H, xa, xs, cs, nb, red);
         } else {
-          const int b = (lane >> 2) & 3;
-          const float mb = b < nb ? (shared ? gam[b] : wm[b * 64 + d.slot - s.hsi]) : 0.f;
           if (shared)
-            down_compute<4>(st, I, DA, hs0, hs1, mb, nb, red);
+            down_compute<4>(st, I, da, dc0, dc1, hs0, hs1, nb, red);
           else
-            down_compute<BITS>(st, I, DA, hs0, hs1, mb, nb, red);
+            down_compute<BITS>(st, I, da, dc0, dc1, hs0, hs1, nb, red);
         }
       }
       __syncthreads();
@@ -800,15 +851,17 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           const float h = ok ? gsum / (1.f + expf(-gsum)) * usum : 0.f;
           const int pos = d.row0 + i;
           const int blk = pos >> 7, c = pos & 127, tq = c >> 5, cc = c & 31;
-          int pi = 0, el = 0;
+          int pi = 0, el = 0, sh = 0;
 #pragma unroll
           for (int p = 0; p < 16; p++) {
-            const int lo = shared || BITS == 4 ? Codec<4>::lo(p) : Codec<BITS>::lo(p);
-            const int hi = shared || BITS == 4 ? Codec<4>::hi(p) : Codec<BITS>::hi(p);
-            if (lo == cc) pi = p, el = 0;
-            if (hi == cc) pi = p, el = 1;
+            const bool c4 = shared || BITS == 4;
+            const int lo = c4 ? Codec<4>::lo(p) : Codec<BITS>::lo(p);
+            const int hi = c4 ? Codec<4>::hi(p) : Codec<BITS>::hi(p);
+            if (lo == cc) pi = p, el = 0, sh = c4 ? Codec<4>::slo(p) : Codec<BITS>::slo(p);
+            if (hi == cc) pi = p, el = 1, sh = c4 ? Codec<4>::shi(p) : Codec<BITS>::shi(p);
           }
-          const uint32_t hi = f2bf(h), lo = f2bf(h - __uint_as_float(hi << 16));
+          const float hv = h * __uint_as_float((uint32_t)(127 - sh) << 23);  // h * 2^-sh, exact
+          const uint32_t hi = f2bf(hv), lo = f2bf(hv - __uint_as_float(hi << 16));
           uint16_t *hb = P.hfrag + (size_t)d.slot * nblkI * 8 * 32 * 4;
           const int m = pi >> 1, reg = pi & 1;
           hb[(((blk * 8 + m) * 32 + 4 * b + tq) * 2 + reg) * 2 + el] = (uint16_t)hi;
@@ -824,7 +877,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           float y = 0.f;
           if (ok)
             for (int kb = 0; kb < nblkI; kb++) y += red[(kb * 8 + (r >> 3)) * 32 + (r & 7) * 4 + b];
-          P.ypart[((size_t)d.slot * 4 + b) * H + d.row0 + r] = y;
+          const float mb = shared ? gam[b] : wm[b * 64 + d.slot - s.hsi];
+          P.ypart[((size_t)d.slot * 4 + b) * H + d.row0 + r] = mb * y;
         }
         __syncthreads();
         if (tid == 0) sflag[2] = atom_acq_rel_add(cnt + kCntDn + rt, 1u) == (unsigned)(s.nslots - 1);
@@ -865,7 +919,7 @@ static int fixed_smem(int H, int E, int bits) {
   int b = 0;
   b += 4 * H * 4;                                  // xf
   b += nblkH * 256 * 8 * (bits == 4 ? 1 : 2);      // xa (+ xa4)
-  b += 4 * (H / 64) * 4;                           // xs
+  b += 3 * 4 * (H / 64) * 4;                       // xs, cs, cs4
   b += 4 * E1 * 4;                                 // lg
   b += 2048 * 4;                                   // red
   b += (128 + 128 + 64 + 256 + 16) * 4;            // sidx sw uni wm gam+flags
@@ -925,6 +979,12 @@ static cudaError_t launch_t(const FwdParams &p, int grid, int smem, cudaStream_t
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_kernel<BITS>, p);
 }
+
+#ifdef MOE_DEBUG_CYCLES
+extern "C" int moe_debug_cycles(long long *host64) {
+  return (int)cudaMemcpyFromSymbol(host64, g_dbg_cycles, sizeof(long long) * 64);
+}
+#endif
 
 cudaError_t launch_decode(const FwdParams &p, int grid, int smem, cudaStream_t st) {
   switch (p.bits) {
