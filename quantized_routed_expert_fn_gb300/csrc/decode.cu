@@ -38,7 +38,17 @@ namespace {
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int MAXIT = 4;
-constexpr int kProducer = 32;  // issues the bulk copies (thread 0 does the cross-CTA releases)
+constexpr int kTscWords = 2 * 16 * 33 > 2 * 8 * 65 ? 2 * 16 * 33 : 2 * 8 * 65;  // transposed scales of a unit
+constexpr int kProducerWarp = 1;  // issues the bulk copies (thread 0 does the cross-CTA releases)
+
+// Shared-memory row pitch of a staged code row of rb bytes: padded so that
+// the lanes of one load phase (two rows x 64 B at 4 bits, four rows x 32 B
+// at 2 bits, eight rows x 4 x 4 B at 12-byte stride at 3 bits) hit distinct
+// banks: pitch = 64, 32, 16 (mod 128) for 4, 2, 3 bits.
+__host__ __device__ constexpr int code_pitch(int rb, int bits) {
+  const int target = bits == 4 ? 64 : (bits == 2 ? 32 : 16);
+  return rb + ((target - rb % 128) + 128) % 128;
+}
 constexpr unsigned FULL = 0xffffffffu;
 constexpr uint32_t kResidual = 1, kPrenorm = 2;
 
@@ -205,8 +215,8 @@ __device__ __forceinline__ void make_afrag(const uint2 (&x)[8], bool lowT, AFrag
 // (minus the offset sum on hi lanes, 0 on lo lanes); xs0 / xs1: the groups'
 // input sums on hi lanes, 0 on lo lanes (so the bias enters once).
 template <int B>
-__device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uint8_t *sc, const uint8_t *bi,
-                                             int sp, const AFrag &A, float ci0, float ci1, float xs0,
+__device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uint32_t *sc, const uint32_t *bi,
+                                             const AFrag &A, float ci0, float ci1, float xs0,
                                              float xs1, float &o0, float &o1) {
   uint32_t w[Codec<B>::kWords];
   if constexpr (B == 4) {
@@ -219,10 +229,7 @@ __device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uin
     const uint32_t *p = reinterpret_cast<const uint32_t *>(codes_row);
     w[0] = p[0], w[1] = p[1], w[2] = p[2];
   }
-  const uint32_t s0 = *reinterpret_cast<const uint32_t *>(sc);
-  const uint32_t s1 = *reinterpret_cast<const uint32_t *>(sc + sp);
-  const uint32_t b0 = *reinterpret_cast<const uint32_t *>(bi);
-  const uint32_t b1 = *reinterpret_cast<const uint32_t *>(bi + sp);
+  const uint32_t s0 = sc[0], s1 = sc[1], b0 = bi[0], b1 = bi[1];
   uint32_t bf[16];
   Codec<B>::unpack(w, bf);
   float d[4] = {ci0, ci0, ci1, ci1}, e[4] = {0.f, 0.f, 0.f, 0.f};
@@ -260,8 +267,8 @@ __device__ long long g_dbg_cycles[64];
 #endif
 
 template <int B>
-__device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const float *xs, const float *cs, int nb,
-                                float *red) {
+__device__ void gate_up_compute(const uint8_t *st, const uint32_t *T, int H, const uint2 *xa, const float *xs,
+                                const float *cs, int nb, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3, b = g & 3;
   const int nblk = H / 128;
@@ -270,7 +277,7 @@ __device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const
   const int i0 = warp * ipw;
   if (i0 >= nitems) return;
   const int kb = i0 >> 2;
-  const int rb = H * B / 8, sp = H / 32;
+  const int pitch = code_pitch(H * B / 8, B), np = H / 128;
   MOE_DBG(0)
   uint2 a[8];
 #pragma unroll
@@ -281,14 +288,14 @@ __device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const
   const bool hl0 = g < 4;
   const float xs0 = hl0 ? xs[b * (H / 64) + 2 * kb] : 0.f, xs1 = hl0 ? xs[b * (H / 64) + 2 * kb + 1] : 0.f;
   const float ci0 = hl0 ? -cs[b * (H / 64) + 2 * kb] : 0.f, ci1 = hl0 ? -cs[b * (H / 64) + 2 * kb + 1] : 0.f;
-  const uint8_t *sc = st + 32 * rb, *bi = sc + 32 * sp;
+  const uint32_t *sc = T + kb * 33, *bi = T + (np + kb) * 33;
 #pragma unroll 1
   for (int k = 0; k < ipw; k++) {
     {
       const int nt = (i0 & 3) + k;
       float o0, o1;
-      item_compute<B>(st + (8 * nt + g) * rb + kb * (16 * B) + t * (4 * B), sc + (8 * nt + 2 * t) * sp + kb * 4,
-                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, A, ci0, ci1, xs0, xs1, o0, o1);
+      item_compute<B>(st + (8 * nt + g) * pitch + kb * (16 * B) + t * (4 * B), sc + 8 * nt + 2 * t,
+                      bi + 8 * nt + 2 * t, A, ci0, ci1, xs0, xs1, o0, o1);
       if (lane < 16 && b < nb) {
         red[(kb * 4 + nt) * 32 + (2 * t) * 4 + b] = o0;
         red[(kb * 4 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
@@ -301,8 +308,8 @@ __device__ void gate_up_compute(const uint8_t *st, int H, const uint2 *xa, const
 // Stage layout of a down unit: codes of 64 output rows, their scales, their
 // biases.  a[] / hs0 / hs1: this warp's h fragments and group sums.
 template <int B>
-__device__ void down_compute(const uint8_t *st, int I, const uint2 (&x)[8], float ci0, float ci1, float hs0,
-                             float hs1, int nb, float *red) {
+__device__ void down_compute(const uint8_t *st, const uint32_t *T, int I, const uint2 (&x)[8], float ci0, float ci1,
+                             float hs0, float hs1, int nb, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3, b = g & 3;
   const int nitems = (I / 128) * 8;
@@ -310,17 +317,17 @@ __device__ void down_compute(const uint8_t *st, int I, const uint2 (&x)[8], floa
   const int i0 = warp * ipw;
   if (i0 >= nitems) return;
   const int kb = i0 >> 3;
-  const int rb = I * B / 8, sp = I / 32;
+  const int pitch = code_pitch(I * B / 8, B), np = I / 128;
   AFrag A;
   make_afrag(x, t < 2, A);
-  const uint8_t *sc = st + 64 * rb, *bi = sc + 64 * sp;
+  const uint32_t *sc = T + kb * 65, *bi = T + (np + kb) * 65;
 #pragma unroll 1
   for (int k = 0; k < ipw; k++) {
     {
       const int nt = (i0 & 7) + k;
       float o0, o1;
-      item_compute<B>(st + (8 * nt + g) * rb + kb * (16 * B) + t * (4 * B), sc + (8 * nt + 2 * t) * sp + kb * 4,
-                      bi + (8 * nt + 2 * t) * sp + kb * 4, sp, A, ci0, ci1, hs0, hs1, o0, o1);
+      item_compute<B>(st + (8 * nt + g) * pitch + kb * (16 * B) + t * (4 * B), sc + 8 * nt + 2 * t,
+                      bi + 8 * nt + 2 * t, A, ci0, ci1, hs0, hs1, o0, o1);
       if (lane < 16 && b < nb) {
         red[(kb * 8 + nt) * 32 + (2 * t) * 4 + b] = o0;
         red[(kb * 8 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
@@ -463,30 +470,53 @@ __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP
   return d;
 }
 
-// Thread 0: request the weight tile of one unit into its ring stage.
+// Producer warp: request the weight tile of one unit into its ring stage.
+// Code rows land at the padded pitch (one bulk copy per row, the warp's
+// lanes issuing in parallel); scales and biases land row-major.
 __device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_t *bar, int *status) {
+  const int lane = threadIdx.x & 31;
   if (d.rec == nullptr || ((uintptr_t)d.rec & 15u)) {
-    atomicCAS(status, 0, kStatusDevice);
-    mbar_expect_tx(bar, 0);  // completes the phase with no bytes
+    if (lane == 0) {
+      atomicCAS(status, 0, kStatusDevice);
+      mbar_expect_tx(bar, 0);  // completes the phase with no bytes
+    }
     return;
   }
-  if (!d.down) {
-    const uint32_t rb = H * d.bits / 8, sp = H / 32;
-    const uint32_t bytes = 32 * rb + 64 * sp;
-    mbar_expect_tx(bar, bytes);
-    const uint8_t *c = d.rec + d.q.w, *s = d.rec + d.q.s, *b = d.rec + d.q.b;
-    bulk_g2s(st, c + (size_t)d.row0 * rb, 16 * rb, bar);
-    bulk_g2s(st + 16 * rb, c + (size_t)(I + d.row0) * rb, 16 * rb, bar);
-    bulk_g2s(st + 32 * rb, s + (size_t)d.row0 * sp, 16 * sp, bar);
-    bulk_g2s(st + 32 * rb + 16 * sp, s + (size_t)(I + d.row0) * sp, 16 * sp, bar);
-    bulk_g2s(st + 32 * rb + 32 * sp, b + (size_t)d.row0 * sp, 16 * sp, bar);
-    bulk_g2s(st + 32 * rb + 48 * sp, b + (size_t)(I + d.row0) * sp, 16 * sp, bar);
-  } else {
-    const uint32_t rb = I * d.bits / 8, sp = I / 32;
-    mbar_expect_tx(bar, 64 * rb + 128 * sp);
-    bulk_g2s(st, d.rec + d.q.w + (size_t)d.row0 * rb, 64 * rb, bar);
-    bulk_g2s(st + 64 * rb, d.rec + d.q.s + (size_t)d.row0 * sp, 64 * sp, bar);
-    bulk_g2s(st + 64 * rb + 64 * sp, d.rec + d.q.b + (size_t)d.row0 * sp, 64 * sp, bar);
+  const int inp = d.down ? I : H;
+  const uint32_t rb = inp * d.bits / 8, sp = inp / 32, pitch = code_pitch(rb, d.bits);
+  const int rows = d.down ? 64 : 32;
+  if (lane == 0) mbar_expect_tx(bar, rows * (rb + 2 * sp));
+  __syncwarp();
+  const uint8_t *c = d.rec + d.q.w;
+  for (int r = lane; r < rows; r += 32) {
+    // gate_up: rows 0..15 the gate rows row0.., 16..31 the up rows I+row0..
+    const int src = d.down ? d.row0 + r : (r < 16 ? d.row0 + r : I + d.row0 + r - 16);
+    bulk_g2s(st + r * pitch, c + (size_t)src * rb, rb, bar);
+  }
+  if (lane == 0) {
+    uint8_t *sdst = st + rows * pitch;
+    if (d.down) {
+      bulk_g2s(sdst, d.rec + d.q.s + (size_t)d.row0 * sp, 64 * sp, bar);
+      bulk_g2s(sdst + 64 * sp, d.rec + d.q.b + (size_t)d.row0 * sp, 64 * sp, bar);
+    } else {
+      bulk_g2s(sdst, d.rec + d.q.s + (size_t)d.row0 * sp, 16 * sp, bar);
+      bulk_g2s(sdst + 16 * sp, d.rec + d.q.s + (size_t)(I + d.row0) * sp, 16 * sp, bar);
+      bulk_g2s(sdst + 32 * sp, d.rec + d.q.b + (size_t)d.row0 * sp, 16 * sp, bar);
+      bulk_g2s(sdst + 48 * sp, d.rec + d.q.b + (size_t)(I + d.row0) * sp, 16 * sp, bar);
+    }
+  }
+}
+
+// All threads: transpose the unit's scales and biases, [row][pair] u32
+// (two groups of a block per u32) -> T[which][pair][row] with row stride
+// rows + 1, so that an item's lanes read their rows without conflicts.
+__device__ void transpose_scales(const uint8_t *sd, int rows, int npair, uint32_t *T) {
+  const uint32_t *src = reinterpret_cast<const uint32_t *>(sd);
+  const int per = rows * npair;
+  for (int e = threadIdx.x; e < 2 * per; e += NT) {
+    const int which = e / per, rem = e - which * per;
+    const int r = rem / npair, kb = rem - r * npair;
+    T[(which * npair + kb) * (rows + 1) + r] = src[e];
   }
 }
 
@@ -520,7 +550,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   volatile int *sflag = reinterpret_cast<volatile int *>(gam + 4);       // [12]
   uint64_t *bars = reinterpret_cast<uint64_t *>(gam + 16);               // [kMaxStages]
   const uint8_t **rect = reinterpret_cast<const uint8_t **>(bars + kMaxStages);  // [64] slot -> record
-  uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(rect + 64);                  // [E] expert addresses
+  uint32_t *tsc = reinterpret_cast<uint32_t *>(rect + 64);                      // [1056] transposed scales
+  uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(tsc + kTscWords);           // [E] expert addresses
 
   if (tid == 0) {
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1);
@@ -550,7 +581,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.nB = s.nD = s.rB0 = s.d0 = 0;
     s.U = 0;
     int issued = 0;
-    if (tid == kProducer) {
+    if (warp == kProducerWarp) {
       for (; issued < s.nA && issued < S; issued++) {
         const unsigned u = qbase + issued;
         issue_unit(get_unit<BITS>(issued, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes,
@@ -729,7 +760,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.d0 = fdiv_mul(cta, ND, G);
     s.nD = fdiv_mul(cta + 1, ND, G) - s.d0;
     const int n = s.n();
-    if (tid == kProducer) {
+    if (warp == kProducerWarp) {
       for (int q = issued; q < n && q < S; q++) {
         const unsigned u = qbase + q;
         issue_unit(get_unit<BITS>(q, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
@@ -807,22 +838,27 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       if (q == 0) MOE_STAMP(11)
       const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
       if (ok) {
+        const int rows = d.down ? 64 : 32, inp = d.down ? I : H;
+        transpose_scales(st + rows * code_pitch(inp * d.bits / 8, d.bits), rows, inp / 128, tsc);
+      }
+      __syncthreads();
+      if (ok) {
         if (!d.down) {
           if (shared)
-            gate_up_compute<4>(st, H, xa4, xs, BITS == 4 ? cs : cs4, nb, red);
+            gate_up_compute<4>(st, tsc, H, xa4, xs, BITS == 4 ? cs : cs4, nb, red);
           else
-            gate_up_compute<BITS>(st, H, xa, xs, cs, nb, red);
+            gate_up_compute<BITS>(st, tsc, H, xa, xs, cs, nb, red);
         } else {
           if (shared)
-            down_compute<4>(st, I, da, dc0, dc1, hs0, hs1, nb, red);
+            down_compute<4>(st, tsc, I, da, dc0, dc1, hs0, hs1, nb, red);
           else
-            down_compute<BITS>(st, I, da, dc0, dc1, hs0, hs1, nb, red);
+            down_compute<BITS>(st, tsc, I, da, dc0, dc1, hs0, hs1, nb, red);
         }
       }
       __syncthreads();
       if (q == 0) MOE_STAMP(12)
       // the stage is free: request the unit S places ahead into it
-      if (tid == kProducer && q + S < n) {
+      if (warp == kProducerWarp && q + S < n) {
         issue_unit(get_unit<BITS>(q + S, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
                    P.status);
       }
@@ -925,14 +961,15 @@ static int fixed_smem(int H, int E, int bits) {
   b += (128 + 128 + 64 + 256 + 16) * 4;            // sidx sw uni wm gam+flags
   b += kMaxStages * 8;                             // barriers
   b += 64 * 8;                                     // slot -> record table
+  b += kTscWords * 4;                              // transposed scales
   b += ((E + 1) & ~1) * 8;                         // expert addresses
   return b;
 }
 
 static int stage_bytes(int H, int I) {
   // the 4-bit tiles are the largest (the shared expert is always 4-bit)
-  const int gu = 32 * (H * 4 / 8) + 64 * (H / 32);
-  const int dn = 64 * (I * 4 / 8) + 128 * (I / 32);
+  const int gu = 32 * code_pitch(H * 4 / 8, 4) + 64 * (H / 32);
+  const int dn = 64 * code_pitch(I * 4 / 8, 4) + 128 * (I / 32);
   const int m = gu > dn ? gu : dn;
   return (m + 127) & ~127;
 }
