@@ -41,14 +41,9 @@ constexpr int MAXIT = 4;
 constexpr int kTscWords = 2 * 16 * 33 > 2 * 8 * 65 ? 2 * 16 * 33 : 2 * 8 * 65;  // transposed scales of a unit
 constexpr int kProducerWarp = 1;  // issues the bulk copies (thread 0 does the cross-CTA releases)
 
-// Shared-memory row pitch of a staged code row of rb bytes: padded so that
-// the lanes of one load phase (two rows x 64 B at 4 bits, four rows x 32 B
-// at 2 bits, eight rows x 4 x 4 B at 12-byte stride at 3 bits) hit distinct
-// banks: pitch = 64, 32, 16 (mod 128) for 4, 2, 3 bits.
-__host__ __device__ constexpr int code_pitch(int rb, int bits) {
-  const int target = bits == 4 ? 64 : (bits == 2 ? 32 : 16);
-  return rb + ((target - rb % 128) + 128) % 128;
-}
+// Shared-memory row pitch of a staged code row of rb bytes (rows land
+// contiguously: one bulk copy per block of rows).
+__host__ __device__ constexpr int code_pitch(int rb, int) { return rb; }
 constexpr unsigned FULL = 0xffffffffu;
 constexpr uint32_t kResidual = 1, kPrenorm = 2;
 
@@ -140,17 +135,32 @@ __device__ void drain_ring(uint64_t *bars, unsigned from, unsigned to, int S, co
 }
 
 // ------------------------------------------------------------ activation staging
+//
+// MMA layout (m16n8k16, bf16 in, fp32 accumulate): A = 16 weight rows x 16
+// k-slots of codes, B = 16 k-slots x 8 activation columns.  A block of 128
+// inputs takes 8 MMA steps; lane (g, t) holds, for weight rows g and g+8, the
+// 32 codes of quad position t (group t/2 of the block).  Column n of B is
+// (group y = n/4, part hl = (n/2)&1 (bf16 hi or lo of the input), row bb = n&1)
+// of activation rows b = 2*half + bb; B is zero where the k-slot belongs to
+// the other group, so each column sums exactly one 64-code group.
 
-// Thread (blk, b, t) turns the 32 inputs x[b][blk*128 + 32t .. +32) into the
-// bf16 hi / lo A-fragment registers of lanes (hl*4 + b, t) for the 8 MMA
-// steps of the block, in codec B's pair order, each input pre-scaled by the
-// 2^-s of its pair half (exact).  Also per 64-input group: xs = sum of x
-// (bias term) and cs = 128 * sum of 2^-s x (the offset the codes carry).
+// Thread (blk, t, b) turns the 32 inputs x[b][blk*128 + 32t .. +32) into the
+// nonzero B registers of the lanes (col, t) with col in group t/2, for the 8
+// MMA steps, in codec B's pair order, each input pre-scaled by the 2^-s of
+// its pair half (exact).  Per 64-input group: xs = sum of x (bias term),
+// cs = 128 * sum of 2^-s x (the offset the codes carry).
+// Compact layout (the other group's zero columns are not stored):
+// xb[blk][half][m][t][hl][bb], uint2 = k-slots (2t,2t+1), (2t+8,2t+9).
+__device__ __forceinline__ int frag_index(int blk, int half, int m, int t, int hl, int bb) {
+  return (((blk * 2 + half) * 8 + m) * 4 + t) * 4 + hl * 2 + bb;
+}
 template <int B>
-__device__ void stage_frags(const float *xf, int H, int nb, uint2 *xa, float *xs, float *cs) {
+__device__ void stage_frags(const float *xf, int H, int nb, uint2 *xb, float *xs, float *cs) {
   const int nblk = H / 128;
   for (int j = threadIdx.x; j < nblk * 16; j += NT) {
     const int t = j & 3, b = (j >> 2) & 3, blk = j >> 4;
+    const int y = t >> 1, half = b >> 1, bb = b & 1;
+    (void)y;
     float v[32];
     if (b < nb) {
       const float4 *src = reinterpret_cast<const float4 *>(xf + b * H + blk * 128 + 32 * t);
@@ -177,75 +187,77 @@ __device__ void stage_frags(const float *xf, int H, int nb, uint2 *xa, float *xs
       uint32_t hi0, lo0, hi1, lo1;
       split2(a0, a1, hi0, lo0);
       split2(a2, a3, hi1, lo1);
-      xa[(blk * 8 + m) * 32 + 4 * b + t] = make_uint2(hi0, hi1);
-      xa[(blk * 8 + m) * 32 + 4 * (4 + b) + t] = make_uint2(lo0, lo1);
+      xb[frag_index(blk, half, m, t, 0, bb)] = make_uint2(hi0, hi1);
+      xb[frag_index(blk, half, m, t, 1, bb)] = make_uint2(lo0, lo1);
     }
     sx += __shfl_xor_sync(FULL, sx, 1);
     sc += __shfl_xor_sync(FULL, sc, 1);
     if ((t & 1) == 0) {
-      if (xs) xs[b * (H / 64) + 2 * blk + (t >> 1)] = sx;
-      cs[b * (H / 64) + 2 * blk + (t >> 1)] = 128.f * sc;
+      if (xs) xs[b * (H / 64) + 2 * blk + y] = sx;
+      cs[b * (H / 64) + 2 * blk + y] = 128.f * sc;
     }
   }
 }
 
 // ------------------------------------------------------------ tensor-core items
 
-// The four A registers of each MMA step: lanes with t < 2 carry codes of the
-// block's first group (A rows 0..7), lanes with t >= 2 of its second group
-// (rows 8..15); the other half of each lane's A fragment is zero.
-struct AFrag {
-  uint32_t r[8][4];
+// Column-pair constants of one lane for one half of the activation rows:
+// accumulator start (minus the offset sum of the lane's group on hi-part
+// columns, 0 on lo-part ones) and the group's input sums (hi-part columns
+// only, so the bias enters once).
+struct ColC {
+  float c0, c1, x0, x1;
 };
-__device__ __forceinline__ void make_afrag(const uint2 (&x)[8], bool lowT, AFrag &A) {
-#pragma unroll
-  for (int m = 0; m < 8; m++) {
-    A.r[m][0] = lowT ? x[m].x : 0u;
-    A.r[m][1] = lowT ? 0u : x[m].x;
-    A.r[m][2] = lowT ? x[m].y : 0u;
-    A.r[m][3] = lowT ? 0u : x[m].y;
-  }
-}
 
-// One item: 8 weight rows x one block of 128 inputs.  Codes and the scale /
-// bias pairs come from the stage in shared memory; A holds the activation
-// fragments of the block.  Returns, in lanes 0..15 (b = lane/4), the results
-// of rows 2t and 2t+1 of the item (already summed over hi and lo parts).
-// ci0 / ci1: accumulator start of the lane's rows for the block's two groups
-// (minus the offset sum on hi lanes, 0 on lo lanes); xs0 / xs1: the groups'
-// input sums on hi lanes, 0 on lo lanes (so the bias enters once).
-template <int B>
-__device__ __forceinline__ void item_compute(const uint8_t *codes_row, const uint32_t *sc, const uint32_t *bi,
-                                             const AFrag &A, float ci0, float ci1, float xs0,
-                                             float xs1, float &o0, float &o1) {
-  uint32_t w[Codec<B>::kWords];
+// One item: 16 weight rows (stage rows r0 .. r0+15) x one block of 128
+// inputs, for nh halves of the activation rows.  Codes come from the stage;
+// sc / bi point at the transposed scale / bias pairs of rows r0.. for this
+// block.  Returns per lane (t == 0 lanes after the sums) the outputs of rows
+// g and g+8 for activation rows b = 2*half + {0,1}.
+template <int B, int NH>
+__device__ __forceinline__ void item_compute(const uint8_t *row_g, const uint8_t *row_g8, const uint32_t *sc,
+                                             const uint32_t *bi, int g, int y, const uint2 (&xb)[NH][8],
+                                             const ColC (&cc)[NH], float (&o)[NH][4]) {
+  uint32_t wa[Codec<B>::kWords], wb[Codec<B>::kWords];
   if constexpr (B == 4) {
-    const uint4 v = *reinterpret_cast<const uint4 *>(codes_row);
-    w[0] = v.x, w[1] = v.y, w[2] = v.z, w[3] = v.w;
+    const uint4 va = *reinterpret_cast<const uint4 *>(row_g), vb = *reinterpret_cast<const uint4 *>(row_g8);
+    wa[0] = va.x, wa[1] = va.y, wa[2] = va.z, wa[3] = va.w;
+    wb[0] = vb.x, wb[1] = vb.y, wb[2] = vb.z, wb[3] = vb.w;
   } else if constexpr (B == 2) {
-    const uint2 v = *reinterpret_cast<const uint2 *>(codes_row);
-    w[0] = v.x, w[1] = v.y;
+    const uint2 va = *reinterpret_cast<const uint2 *>(row_g), vb = *reinterpret_cast<const uint2 *>(row_g8);
+    wa[0] = va.x, wa[1] = va.y, wb[0] = vb.x, wb[1] = vb.y;
   } else {
-    const uint32_t *p = reinterpret_cast<const uint32_t *>(codes_row);
-    w[0] = p[0], w[1] = p[1], w[2] = p[2];
+    const uint32_t *pa = reinterpret_cast<const uint32_t *>(row_g), *pb = reinterpret_cast<const uint32_t *>(row_g8);
+    wa[0] = pa[0], wa[1] = pa[1], wa[2] = pa[2], wb[0] = pb[0], wb[1] = pb[1], wb[2] = pb[2];
   }
-  const uint32_t s0 = sc[0], s1 = sc[1], b0 = bi[0], b1 = bi[1];
-  uint32_t bf[16];
-  Codec<B>::unpack(w, bf);
-  float d[4] = {ci0, ci0, ci1, ci1}, e[4] = {0.f, 0.f, 0.f, 0.f};
+  const uint32_t sg = sc[g], sg8 = sc[g + 8], bg = bi[g], bg8 = bi[g + 8];
+  uint32_t fa[16], fb[16];
+  Codec<B>::unpack(wa, fa);
+  Codec<B>::unpack(wb, fb);
+  const float s0 = y ? bf16hi(sg) : bf16lo(sg), s8 = y ? bf16hi(sg8) : bf16lo(sg8);
+  const float b0 = y ? bf16hi(bg) : bf16lo(bg), b8 = y ? bf16hi(bg8) : bf16lo(bg8);
 #pragma unroll
-  for (int m = 0; m < 8; m += 2) {
-    mma_bf16_16816(d, A.r[m][0], A.r[m][1], A.r[m][2], A.r[m][3], bf[2 * m], bf[2 * m + 1]);
-    mma_bf16_16816(e, A.r[m + 1][0], A.r[m + 1][1], A.r[m + 1][2], A.r[m + 1][3], bf[2 * m + 2], bf[2 * m + 3]);
+  for (int h = 0; h < NH; h++) {
+    float d[4] = {cc[h].c0, cc[h].c1, cc[h].c0, cc[h].c1}, e[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int m = 0; m < 8; m += 2) {
+      mma_bf16_16816(d, fa[2 * m], fb[2 * m], fa[2 * m + 1], fb[2 * m + 1], xb[h][m].x, xb[h][m].y);
+      mma_bf16_16816(e, fa[2 * m + 2], fb[2 * m + 2], fa[2 * m + 3], fb[2 * m + 3], xb[h][m + 1].x, xb[h][m + 1].y);
+    }
+    float r0 = s0 * (d[0] + e[0]) + b0 * cc[h].x0;
+    float r1 = s0 * (d[1] + e[1]) + b0 * cc[h].x1;
+    float r2 = s8 * (d[2] + e[2]) + b8 * cc[h].x0;
+    float r3 = s8 * (d[3] + e[3]) + b8 * cc[h].x1;
+    // sum over the quad: parts hi / lo (t, t^1) and the two groups (t, t^2)
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      r0 += __shfl_xor_sync(FULL, r0, off);
+      r1 += __shfl_xor_sync(FULL, r1, off);
+      r2 += __shfl_xor_sync(FULL, r2, off);
+      r3 += __shfl_xor_sync(FULL, r3, off);
+    }
+    o[h][0] = r0, o[h][1] = r1, o[h][2] = r2, o[h][3] = r3;
   }
-#pragma unroll
-  for (int i = 0; i < 4; i++) d[i] += e[i];
-  float r0 = bf16lo(s0) * d[0] + bf16hi(s0) * d[2];
-  float r1 = bf16lo(s1) * d[1] + bf16hi(s1) * d[3];
-  r0 += bf16lo(b0) * xs0 + bf16hi(b0) * xs1;
-  r1 += bf16lo(b1) * xs0 + bf16hi(b1) * xs1;
-  o0 = r0 + __shfl_xor_sync(FULL, r0, 16);
-  o1 = r1 + __shfl_xor_sync(FULL, r1, 16);
 }
 
 // items per warp: the smallest power of two covering all items, capped at ntiles
@@ -256,82 +268,154 @@ __device__ __forceinline__ int items_per_warp(int nitems, int ntiles) {
   return ipw < ntiles ? ipw : ntiles;
 }
 
-// Stage layout of a gate_up unit: codes of 16 gate rows then 16 up rows
-// (32 rows), then their scales (32 rows), then their biases (32 rows).
-// Writes red[(kb*4 + nt)*32 + row*4 + b].
-#ifdef MOE_DEBUG_CYCLES
-__device__ long long g_dbg_cycles[64];
-#define MOE_DBG(k) if (blockIdx.x == 0 && (threadIdx.x & 31) == 0 && (threadIdx.x >> 5) < 4) g_dbg_cycles[(threadIdx.x >> 5) * 16 + (k)] = clock64();
-#else
-#define MOE_DBG(k)
-#endif
+// B registers of lane (g, t) for one block and half: its column's entry if
+// the column belongs to the lane's group, else zero.
+template <int NH>
+__device__ __forceinline__ void load_bfrag(const uint2 *xb, int blk, int lane, uint2 (&x)[NH][8]) {
+  const int g = lane >> 2, t = lane & 3;
+  const bool mine = (g >> 2) == (t >> 1);
+#pragma unroll
+  for (int h = 0; h < NH; h++)
+#pragma unroll
+    for (int m = 0; m < 8; m++) {
+      const uint2 v = xb[frag_index(blk, h, m, t, (g >> 1) & 1, g & 1)];
+      x[h][m] = mine ? v : make_uint2(0u, 0u);
+    }
+}
 
-template <int B>
-__device__ void gate_up_compute(const uint8_t *st, const uint32_t *T, int H, const uint2 *xa, const float *xs,
+// Column constants of lane (g, t) for one half from the group sums of
+// activation rows b = 2*half, 2*half+1 (xs: input sums, cs: offset sums).
+__device__ __forceinline__ ColC col_consts(float cs0, float cs1, float xs0, float xs1, bool hipart) {
+  ColC c;
+  c.c0 = hipart ? -cs0 : 0.f, c.c1 = hipart ? -cs1 : 0.f;
+  c.x0 = hipart ? xs0 : 0.f, c.x1 = hipart ? xs1 : 0.f;
+  return c;
+}
+
+// Items of a gate_up unit: (block kb, row tile 0 = the 16 gate rows, 1 = the
+// 16 up rows).  Writes red[(kb*2 + tile)*64 + row*4 + b].
+template <int B, int NH>
+__device__ void gate_up_compute(const uint8_t *st, const uint32_t *T, int H, const uint2 *xb, const float *xs,
                                 const float *cs, int nb, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3, b = g & 3;
+  const int g = lane >> 2, t = lane & 3, y = t >> 1;
   const int nblk = H / 128;
-  const int nitems = nblk * 4;
-  const int ipw = items_per_warp(nitems, 4);
+  const int nitems = nblk * 2;
+  const int ipw = items_per_warp(nitems, 2);
   const int i0 = warp * ipw;
   if (i0 >= nitems) return;
-  const int kb = i0 >> 2;
-  const int pitch = code_pitch(H * B / 8, B), np = H / 128;
-  MOE_DBG(0)
-  uint2 a[8];
+  const int kb = i0 >> 1;
+  const int rb = H * B / 8, np = H / 128, ng = H / 64;
+  uint2 x[NH][8];
+  ColC cc[NH];
+  load_bfrag<NH>(xb, kb, lane, x);
 #pragma unroll
-  for (int m = 0; m < 8; m++) a[m] = xa[(kb * 8 + m) * 32 + lane];
-  AFrag A;
-  make_afrag(a, t < 2, A);
-  MOE_DBG(1)
-  const bool hl0 = g < 4;
-  const float xs0 = hl0 ? xs[b * (H / 64) + 2 * kb] : 0.f, xs1 = hl0 ? xs[b * (H / 64) + 2 * kb + 1] : 0.f;
-  const float ci0 = hl0 ? -cs[b * (H / 64) + 2 * kb] : 0.f, ci1 = hl0 ? -cs[b * (H / 64) + 2 * kb + 1] : 0.f;
+  for (int h = 0; h < NH; h++) {
+    const int b0 = 2 * h, b1 = 2 * h + 1, grp = 2 * kb + y;
+    cc[h] = col_consts(cs[b0 * ng + grp], cs[b1 * ng + grp], xs[b0 * ng + grp], xs[b1 * ng + grp], (t & 1) == 0);
+  }
   const uint32_t *sc = T + kb * 33, *bi = T + (np + kb) * 33;
 #pragma unroll 1
   for (int k = 0; k < ipw; k++) {
-    {
-      const int nt = (i0 & 3) + k;
-      float o0, o1;
-      item_compute<B>(st + (8 * nt + g) * pitch + kb * (16 * B) + t * (4 * B), sc + 8 * nt + 2 * t,
-                      bi + 8 * nt + 2 * t, A, ci0, ci1, xs0, xs1, o0, o1);
-      if (lane < 16 && b < nb) {
-        red[(kb * 4 + nt) * 32 + (2 * t) * 4 + b] = o0;
-        red[(kb * 4 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
+    const int tile = (i0 & 1) + k;
+    const int r0 = 16 * tile;
+    float o[NH][4];
+    item_compute<B, NH>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
+                        st + (r0 + g + 8) * rb + kb * (16 * B) + t * (4 * B), sc + r0, bi + r0, g, y, x, cc, o);
+    if (t == 0) {
+      float *rp = red + (kb * 2 + tile) * 64;
+#pragma unroll
+      for (int h = 0; h < NH; h++) {
+        *reinterpret_cast<float2 *>(rp + g * 4 + 2 * h) = make_float2(o[h][0], o[h][1]);
+        *reinterpret_cast<float2 *>(rp + (g + 8) * 4 + 2 * h) = make_float2(o[h][2], o[h][3]);
       }
-      MOE_DBG(2 + k)
     }
   }
 }
 
-// Stage layout of a down unit: codes of 64 output rows, their scales, their
-// biases.  a[] / hs0 / hs1: this warp's h fragments and group sums.
-template <int B>
-__device__ void down_compute(const uint8_t *st, const uint32_t *T, int I, const uint2 (&x)[8], float ci0, float ci1,
-                             float hs0, float hs1, int nb, float *red) {
+// Items of a down unit: (block kb, row tile of 16 of the unit's 64 output
+// rows).  xb / xs / cs: the slot's h fragments and group sums, staged in
+// shared memory.  Writes red[(kb*4 + tile)*64 + row*4 + b].
+template <int B, int NH>
+__device__ void down_compute(const uint8_t *st, const uint32_t *T, int I, const uint2 *xb, const float *xs,
+                             const float *cs, int nb, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g = lane >> 2, t = lane & 3, b = g & 3;
-  const int nitems = (I / 128) * 8;
-  const int ipw = items_per_warp(nitems, 8);
+  const int g = lane >> 2, t = lane & 3, y = t >> 1;
+  const int nitems = (I / 128) * 4;
+  const int ipw = items_per_warp(nitems, 4);
   const int i0 = warp * ipw;
   if (i0 >= nitems) return;
-  const int kb = i0 >> 3;
-  const int pitch = code_pitch(I * B / 8, B), np = I / 128;
-  AFrag A;
-  make_afrag(x, t < 2, A);
+  const int kb = i0 >> 2;
+  const int rb = I * B / 8, np = I / 128, ng = I / 64;
+  uint2 x[NH][8];
+  ColC cc[NH];
+  load_bfrag<NH>(xb, kb, lane, x);
+#pragma unroll
+  for (int h = 0; h < NH; h++) {
+    const int b0 = 2 * h, b1 = 2 * h + 1, grp = 2 * kb + y;
+    cc[h] = col_consts(cs[b0 * ng + grp], cs[b1 * ng + grp], xs[b0 * ng + grp], xs[b1 * ng + grp], (t & 1) == 0);
+  }
   const uint32_t *sc = T + kb * 65, *bi = T + (np + kb) * 65;
 #pragma unroll 1
   for (int k = 0; k < ipw; k++) {
-    {
-      const int nt = (i0 & 7) + k;
-      float o0, o1;
-      item_compute<B>(st + (8 * nt + g) * pitch + kb * (16 * B) + t * (4 * B), sc + 8 * nt + 2 * t,
-                      bi + 8 * nt + 2 * t, A, ci0, ci1, hs0, hs1, o0, o1);
-      if (lane < 16 && b < nb) {
-        red[(kb * 8 + nt) * 32 + (2 * t) * 4 + b] = o0;
-        red[(kb * 8 + nt) * 32 + (2 * t + 1) * 4 + b] = o1;
+    const int tile = (i0 & 3) + k;
+    const int r0 = 16 * tile;
+    float o[NH][4];
+    item_compute<B, NH>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
+                        st + (r0 + g + 8) * rb + kb * (16 * B) + t * (4 * B), sc + r0, bi + r0, g, y, x, cc, o);
+    if (t == 0) {
+      float *rp = red + (kb * 4 + tile) * 64;
+#pragma unroll
+      for (int h = 0; h < NH; h++) {
+        *reinterpret_cast<float2 *>(rp + g * 4 + 2 * h) = make_float2(o[h][0], o[h][1]);
+        *reinterpret_cast<float2 *>(rp + (g + 8) * 4 + 2 * h) = make_float2(o[h][2], o[h][3]);
       }
+    }
+  }
+}
+
+// All threads: bring one slot's h fragments into shared memory and form its
+// per-group sums: hxs = sum of h (bias term), hcs = 128 * sum of 2^-s h as the
+// MMA sees it (offset), [b][I/64].  Codec C is the slot's down codec.
+template <int C>
+__device__ void stage_h(const uint2 *hf, int I, int nb, uint2 *hsm, float *hxs, float *hcs) {
+  const int nblk = I / 128;
+  const int n = nblk * 256;
+  for (int i = threadIdx.x; i < n; i += NT) hsm[i] = __ldcg(hf + i);
+  __syncthreads();
+  // thread (kb, y, b, part): 4 of the 32 entries (t in {2y, 2y+1}, m, hl) of a group
+  const int ng = I / 64;
+  for (int j = threadIdx.x; j < nblk * 64; j += NT) {
+    const int part = j & 7, b = (j >> 3) & 3, y = (j >> 5) & 1, kb = j >> 6;
+    float ssc = 0.f, sun = 0.f;
+    if (b < nb) {
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int e = part * 4 + k;  // e = (t - 2y) * 16 + m * 2 + hl
+        const int tt = 2 * y + (e >> 4), m = (e >> 1) & 7, hl = e & 1;
+        const uint2 v = hsm[frag_index(kb, b >> 1, m, tt, hl, b & 1)];
+        const float v0 = bf16lo(v.x), v1 = bf16hi(v.x), v2 = bf16lo(v.y), v3 = bf16hi(v.y);
+        ssc += v0 + v1 + v2 + v3;
+        float w0 = 1.f, w1 = 1.f, w2 = 1.f, w3 = 1.f;
+        if (C != 4) {
+#pragma unroll
+          for (int mm = 0; mm < 8; mm++)
+            if (mm == m) {
+              w0 = (float)(1 << Codec<C>::slo(2 * mm)), w1 = (float)(1 << Codec<C>::shi(2 * mm));
+              w2 = (float)(1 << Codec<C>::slo(2 * mm + 1)), w3 = (float)(1 << Codec<C>::shi(2 * mm + 1));
+            }
+        }
+        sun += v0 * w0 + v1 * w1 + v2 * w2 + v3 * w3;
+      }
+    }
+#pragma unroll
+    for (int o = 4; o; o >>= 1) {
+      ssc += __shfl_xor_sync(FULL, ssc, o);
+      sun += __shfl_xor_sync(FULL, sun, o);
+    }
+    if (part == 0) {
+      hcs[b * ng + 2 * kb + y] = 128.f * ssc;
+      hxs[b * ng + 2 * kb + y] = sun;
     }
   }
 }
@@ -470,40 +554,33 @@ __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP
   return d;
 }
 
-// Producer warp: request the weight tile of one unit into its ring stage.
-// Code rows land at the padded pitch (one bulk copy per row, the warp's
-// lanes issuing in parallel); scales and biases land row-major.
+// Producer warp: request the weight tile of one unit into its ring stage:
+// the code rows (gate_up: 16 gate rows then the matching 16 up rows; down:
+// 64 output rows), then their scales, then their biases, row-major.
 __device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_t *bar, int *status) {
-  const int lane = threadIdx.x & 31;
+  if ((threadIdx.x & 31) != 0) return;
   if (d.rec == nullptr || ((uintptr_t)d.rec & 15u)) {
-    if (lane == 0) {
-      atomicCAS(status, 0, kStatusDevice);
-      mbar_expect_tx(bar, 0);  // completes the phase with no bytes
-    }
+    atomicCAS(status, 0, kStatusDevice);
+    mbar_expect_tx(bar, 0);  // completes the phase with no bytes
     return;
   }
   const int inp = d.down ? I : H;
-  const uint32_t rb = inp * d.bits / 8, sp = inp / 32, pitch = code_pitch(rb, d.bits);
+  const uint32_t rb = inp * d.bits / 8, sp = inp / 32;
   const int rows = d.down ? 64 : 32;
-  if (lane == 0) mbar_expect_tx(bar, rows * (rb + 2 * sp));
-  __syncwarp();
-  const uint8_t *c = d.rec + d.q.w;
-  for (int r = lane; r < rows; r += 32) {
-    // gate_up: rows 0..15 the gate rows row0.., 16..31 the up rows I+row0..
-    const int src = d.down ? d.row0 + r : (r < 16 ? d.row0 + r : I + d.row0 + r - 16);
-    bulk_g2s(st + r * pitch, c + (size_t)src * rb, rb, bar);
-  }
-  if (lane == 0) {
-    uint8_t *sdst = st + rows * pitch;
-    if (d.down) {
-      bulk_g2s(sdst, d.rec + d.q.s + (size_t)d.row0 * sp, 64 * sp, bar);
-      bulk_g2s(sdst + 64 * sp, d.rec + d.q.b + (size_t)d.row0 * sp, 64 * sp, bar);
-    } else {
-      bulk_g2s(sdst, d.rec + d.q.s + (size_t)d.row0 * sp, 16 * sp, bar);
-      bulk_g2s(sdst + 16 * sp, d.rec + d.q.s + (size_t)(I + d.row0) * sp, 16 * sp, bar);
-      bulk_g2s(sdst + 32 * sp, d.rec + d.q.b + (size_t)d.row0 * sp, 16 * sp, bar);
-      bulk_g2s(sdst + 48 * sp, d.rec + d.q.b + (size_t)(I + d.row0) * sp, 16 * sp, bar);
-    }
+  mbar_expect_tx(bar, rows * (rb + 2 * sp));
+  const uint8_t *c = d.rec + d.q.w, *sc = d.rec + d.q.s, *bi = d.rec + d.q.b;
+  uint8_t *sdst = st + rows * rb;
+  if (d.down) {
+    bulk_g2s(st, c + (size_t)d.row0 * rb, 64 * rb, bar);
+    bulk_g2s(sdst, sc + (size_t)d.row0 * sp, 64 * sp, bar);
+    bulk_g2s(sdst + 64 * sp, bi + (size_t)d.row0 * sp, 64 * sp, bar);
+  } else {
+    bulk_g2s(st, c + (size_t)d.row0 * rb, 16 * rb, bar);
+    bulk_g2s(st + 16 * rb, c + (size_t)(I + d.row0) * rb, 16 * rb, bar);
+    bulk_g2s(sdst, sc + (size_t)d.row0 * sp, 16 * sp, bar);
+    bulk_g2s(sdst + 16 * sp, sc + (size_t)(I + d.row0) * sp, 16 * sp, bar);
+    bulk_g2s(sdst + 32 * sp, bi + (size_t)d.row0 * sp, 16 * sp, bar);
+    bulk_g2s(sdst + 48 * sp, bi + (size_t)(I + d.row0) * sp, 16 * sp, bar);
   }
 }
 
@@ -551,7 +628,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   uint64_t *bars = reinterpret_cast<uint64_t *>(gam + 16);               // [kMaxStages]
   const uint8_t **rect = reinterpret_cast<const uint8_t **>(bars + kMaxStages);  // [64] slot -> record
   uint32_t *tsc = reinterpret_cast<uint32_t *>(rect + 64);                      // [1056] transposed scales
-  uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(tsc + kTscWords);           // [E] expert addresses
+  uint2 *hsm = reinterpret_cast<uint2 *>(tsc + kTscWords);                      // [I/128 * 256] h fragments
+  float *hxs = reinterpret_cast<float *>(hsm + 8 * 256);                        // [4][I/64] sums of h
+  float *hcs = hxs + 64;                                                        // [4][I/64] offset sums
+  uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(hcs + 64);                   // [E] expert addresses
 
   if (tid == 0) {
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1);
@@ -772,8 +852,6 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     // ---- G + D: the unit loop
     MOE_STAMP(5)
     int cur = -1;
-    uint2 da[8];
-    float hs0 = 0.f, hs1 = 0.f, dc0 = 0.f, dc1 = 0.f;
     for (int q = 0; q < n; q++) {
       if (q == s.nA + s.nB) {
         MOE_STAMP(6)
@@ -790,46 +868,17 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       const uint8_t *st = stages + (size_t)(u % S) * P.stage_bytes;
       const bool shared = s.hsi && d.slot == 0;
       if (d.down && d.slot != cur) {
-        // h of this slot complete?  then load this warp's fragments of it
+        // h of this slot complete?  then stage its fragments and group sums
         if (!cta_wait(cnt + kCntGu + d.slot, (unsigned)s.ups, P, sflag)) {
           drain_ring(bars, u, qbase + (unsigned)(q + S < n ? q + S : n), S, P);
           return;
         }
         cur = d.slot;
-        const int nitems = nblkI * 8;
-        const int ipw = items_per_warp(nitems, 8);
-        const int kb = (warp * ipw < nitems) ? (warp * ipw) >> 3 : 0;
-        const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag + (size_t)d.slot * nblkI * 8 * 32 * 4);
-#pragma unroll
-        for (int m = 0; m < 8; m++) da[m] = __ldcg(hf + (kb * 8 + m) * 32 + lane);
-        // sums of the lane's 32 fragment values: as the MMA sees them (scaled
-        // by 2^-s: the offset) and unscaled (h itself: the bias term)
-        float ssc = 0.f, sun = 0.f;
-        if (shared || BITS == 4) {
-#pragma unroll
-          for (int m = 0; m < 8; m++)
-            ssc += bf16lo(da[m].x) + bf16hi(da[m].x) + bf16lo(da[m].y) + bf16hi(da[m].y);
-          sun = ssc;
-        } else {
-#pragma unroll
-          for (int m = 0; m < 8; m++) {
-            const float v0 = bf16lo(da[m].x), v1 = bf16hi(da[m].x), v2 = bf16lo(da[m].y), v3 = bf16hi(da[m].y);
-            ssc += v0 + v1 + v2 + v3;
-            sun += v0 * (float)(1 << Codec<BITS>::slo(2 * m)) + v1 * (float)(1 << Codec<BITS>::shi(2 * m)) +
-                   v2 * (float)(1 << Codec<BITS>::slo(2 * m + 1)) + v3 * (float)(1 << Codec<BITS>::shi(2 * m + 1));
-          }
-        }
-        // lanes t, t^1 share a group; add the lo part (lane ^ 16)
-        ssc += __shfl_xor_sync(FULL, ssc, 1);
-        ssc += __shfl_xor_sync(FULL, ssc, 16);
-        sun += __shfl_xor_sync(FULL, sun, 1);
-        sun += __shfl_xor_sync(FULL, sun, 16);
-        const float osc = __shfl_xor_sync(FULL, ssc, 2), oun = __shfl_xor_sync(FULL, sun, 2);
-        const bool hl0 = (lane >> 2) < 4, first = (lane & 3) < 2;
-        hs0 = hl0 ? (first ? sun : oun) : 0.f;
-        hs1 = hl0 ? (first ? oun : sun) : 0.f;
-        dc0 = hl0 ? -128.f * (first ? ssc : osc) : 0.f;
-        dc1 = hl0 ? -128.f * (first ? osc : ssc) : 0.f;
+        const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag) + (size_t)d.slot * nblkI * 256;
+        if (shared || BITS == 4)
+          stage_h<4>(hf, I, nb, hsm, hxs, hcs);
+        else
+          stage_h<BITS>(hf, I, nb, hsm, hxs, hcs);
       }
       if (!__syncthreads_and(stage_wait(&bars[u % S], (u / S) & 1u, P))) {
         drain_ring(bars, u + 1, qbase + (unsigned)(q + S < n ? q + S : n), S, P);
@@ -843,16 +892,24 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       }
       __syncthreads();
       if (ok) {
+        const float *csx = shared && BITS != 4 ? cs4 : cs;
+        const uint2 *xbx = shared ? xa4 : xa;
         if (!d.down) {
-          if (shared)
-            gate_up_compute<4>(st, tsc, H, xa4, xs, BITS == 4 ? cs : cs4, nb, red);
-          else
-            gate_up_compute<BITS>(st, tsc, H, xa, xs, cs, nb, red);
+          if (nb <= 2) {
+            if (shared) gate_up_compute<4, 1>(st, tsc, H, xbx, xs, csx, nb, red);
+            else gate_up_compute<BITS, 1>(st, tsc, H, xbx, xs, csx, nb, red);
+          } else {
+            if (shared) gate_up_compute<4, 2>(st, tsc, H, xbx, xs, csx, nb, red);
+            else gate_up_compute<BITS, 2>(st, tsc, H, xbx, xs, csx, nb, red);
+          }
         } else {
-          if (shared)
-            down_compute<4>(st, tsc, I, da, dc0, dc1, hs0, hs1, nb, red);
-          else
-            down_compute<BITS>(st, tsc, I, da, dc0, dc1, hs0, hs1, nb, red);
+          if (nb <= 2) {
+            if (shared) down_compute<4, 1>(st, tsc, I, hsm, hxs, hcs, nb, red);
+            else down_compute<BITS, 1>(st, tsc, I, hsm, hxs, hcs, nb, red);
+          } else {
+            if (shared) down_compute<4, 2>(st, tsc, I, hsm, hxs, hcs, nb, red);
+            else down_compute<BITS, 2>(st, tsc, I, hsm, hxs, hcs, nb, red);
+          }
         }
       }
       __syncthreads();
@@ -870,7 +927,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           const int i = tid >> 4, kp = tid & 15;  // 512 threads = 32 rows x 16 parts
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
           for (int kb = kp; kb < nblkH; kb += 16) {
-            const float4 r4 = *reinterpret_cast<const float4 *>(&red[(kb * 4 + (i >> 3)) * 32 + (i & 7) * 4]);
+            const float4 r4 = *reinterpret_cast<const float4 *>(&red[(kb * 2 + (i >> 4)) * 64 + (i & 15) * 4]);
             acc[0] += r4.x, acc[1] += r4.y, acc[2] += r4.z, acc[3] += r4.w;
           }
 #pragma unroll
@@ -898,10 +955,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           }
           const float hv = h * __uint_as_float((uint32_t)(127 - sh) << 23);  // h * 2^-sh, exact
           const uint32_t hi = f2bf(hv), lo = f2bf(hv - __uint_as_float(hi << 16));
-          uint16_t *hb = P.hfrag + (size_t)d.slot * nblkI * 8 * 32 * 4;
+          uint16_t *hb = P.hfrag + (size_t)d.slot * nblkI * 256 * 4;
           const int m = pi >> 1, reg = pi & 1;
-          hb[(((blk * 8 + m) * 32 + 4 * b + tq) * 2 + reg) * 2 + el] = (uint16_t)hi;
-          hb[(((blk * 8 + m) * 32 + 4 * (4 + b) + tq) * 2 + reg) * 2 + el] = (uint16_t)lo;
+          hb[frag_index(blk, b >> 1, m, tq, 0, b & 1) * 4 + reg * 2 + el] = (uint16_t)hi;
+          hb[frag_index(blk, b >> 1, m, tq, 1, b & 1) * 4 + reg * 2 + el] = (uint16_t)lo;
         }
         cta_signal(cnt + kCntGu + d.slot, 1u);
         if (q == 0) MOE_STAMP(13)
@@ -912,7 +969,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           const int r = j & 63, b = j >> 6;
           float y = 0.f;
           if (ok)
-            for (int kb = 0; kb < nblkI; kb++) y += red[(kb * 8 + (r >> 3)) * 32 + (r & 7) * 4 + b];
+            for (int kb = 0; kb < nblkI; kb++) y += red[(kb * 4 + (r >> 4)) * 64 + (r & 15) * 4 + b];
           const float mb = shared ? gam[b] : wm[b * 64 + d.slot - s.hsi];
           P.ypart[((size_t)d.slot * 4 + b) * H + d.row0 + r] = mb * y;
         }
@@ -962,6 +1019,7 @@ static int fixed_smem(int H, int E, int bits) {
   b += kMaxStages * 8;                             // barriers
   b += 64 * 8;                                     // slot -> record table
   b += kTscWords * 4;                              // transposed scales
+  b += 8 * 256 * 8 + 2 * 64 * 4;                   // staged h fragments and sums
   b += ((E + 1) & ~1) * 8;                         // expert addresses
   return b;
 }
