@@ -1075,12 +1075,6 @@ static cudaError_t launch_t(const FwdParams &p, int grid, int smem, cudaStream_t
   return cudaLaunchKernelEx(&cfg, decode_kernel<BITS>, p);
 }
 
-#ifdef MOE_DEBUG_CYCLES
-extern "C" int moe_debug_cycles(long long *host64) {
-  return (int)cudaMemcpyFromSymbol(host64, g_dbg_cycles, sizeof(long long) * 64);
-}
-#endif
-
 cudaError_t launch_decode(const FwdParams &p, int grid, int smem, cudaStream_t st) {
   switch (p.bits) {
     case 4: return launch_t<4>(p, grid, smem, st);
