@@ -34,7 +34,7 @@ struct WsLayout {
   size_t cnt, logits, xbuf, hfrag, ypart, total;
 };
 
-WsLayout ws_layout(int H, int E, int I, int nl) {
+WsLayout ws_layout(int H, int E, int I, int nl, int nb) {
   WsLayout w{};
   size_t off = 0;
   w.cnt = off;
@@ -42,11 +42,11 @@ WsLayout ws_layout(int H, int E, int I, int nl) {
   w.logits = off;
   off += align256((size_t)nl * 4 * (E + 1) * 4);
   w.xbuf = off;
-  off += align256((size_t)nl * 4 * H * 4);
+  off += align256((size_t)nl * nb * H * 4);
   w.hfrag = off;
   off += align256((size_t)64 * I * 16);
   w.ypart = off;
-  off += align256((size_t)64 * 4 * H * 4);
+  off += align256((size_t)64 * nb * H * 4);
   w.total = off;
   return w;
 }
@@ -121,7 +121,7 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   if ((uintptr_t)work & 255u) return fail(MOE_EALIGN, "work must be 256-byte aligned");
   if (!route_only && overlap(x, (size_t)nb * H * 4, out, (size_t)nb * H * 4))
     return fail(MOE_EINVAL, "out overlaps x");
-  const WsLayout w = ws_layout(H, E, I, nl);
+  const WsLayout w = ws_layout(H, E, I, nl, nb);
   if (work_bytes < w.total) return fail(MOE_ENOSPACE, "work holds %zu bytes, %zu needed", work_bytes, w.total);
 
   int dev = 0;
@@ -187,7 +187,7 @@ const char *moe_last_error(void) { return g_err.c_str(); }
 size_t moe_forward_workspace(const moe_layer *layers, int n_layers, int nb) {
   if (check_layers(layers, n_layers, nb) != MOE_OK) return 0;
   const moe_layer &L0 = layers[0];
-  return ws_layout((int)L0.hidden, (int)L0.n_experts, (int)L0.inter, n_layers).total;
+  return ws_layout((int)L0.hidden, (int)L0.n_experts, (int)L0.inter, n_layers, nb).total;
 }
 
 int moe_forward(const moe_layer *layers, int n_layers, const float *x, int nb, float *out, void *work,

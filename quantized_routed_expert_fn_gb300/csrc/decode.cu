@@ -648,8 +648,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     const LayerP &L = P.L[l];
     unsigned *cnt = P.cnt + (size_t)l * kCntPerLayer;
     const bool hs = L.sgate != nullptr;
-    const float *src = l == 0 ? P.x : P.xbuf + (size_t)l * 4 * H;
-    float *dst = l == P.nl - 1 ? P.out : P.xbuf + (size_t)(l + 1) * 4 * H;
+    const float *src = l == 0 ? P.x : P.xbuf + (size_t)l * nb * H;
+    float *dst = l == P.nl - 1 ? P.out : P.xbuf + (size_t)(l + 1) * nb * H;
 
     Sched s;
     s.hsi = hs ? 1 : 0;
@@ -971,7 +971,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           if (ok)
             for (int kb = 0; kb < nblkI; kb++) y += red[(kb * 4 + (r >> 4)) * 64 + (r & 15) * 4 + b];
           const float mb = shared ? gam[b] : wm[b * 64 + d.slot - s.hsi];
-          P.ypart[((size_t)d.slot * 4 + b) * H + d.row0 + r] = mb * y;
+          P.ypart[((size_t)d.slot * nb + b) * H + d.row0 + r] = mb * y;
         }
         __syncthreads();
         if (tid == 0) sflag[2] = atom_acq_rel_add(cnt + kCntDn + rt, 1u) == (unsigned)(s.nslots - 1);
@@ -985,7 +985,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
             const float *yp = P.ypart + (size_t)b * H + d.row0 + r;
             float acc = 0.f;
 #pragma unroll 4
-            for (int sl = part; sl < s.nslots; sl += tpo) acc += __ldcg(yp + (size_t)sl * 4 * H);
+            for (int sl = part; sl < s.nslots; sl += tpo) acc += __ldcg(yp + (size_t)sl * nb * H);
             for (int off = tpo >> 1; off; off >>= 1) acc += __shfl_down_sync(FULL, acc, off, tpo);
             if (part == 0) {
               if (L.flags & kResidual) acc += __ldcg(src + (size_t)b * H + d.row0 + r);

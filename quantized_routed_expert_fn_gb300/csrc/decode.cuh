@@ -41,9 +41,9 @@ struct FwdParams {
   int *status;
   unsigned *cnt;          // [nl][kCntPerLayer]
   float *logits;          // [nl][4][E+1]
-  float *xbuf;            // [nl][4][H]   input of layer l (l >= 1)
+  float *xbuf;            // [nl][nb][H]  input of layer l (l >= 1)
   uint16_t *hfrag;        // [64][I/128][8][32][2][2] bf16 activation fragments of h
-  float *ypart;           // [64][4][H]   per-slot weighted down outputs
+  float *ypart;           // [64][nb][H]  per-slot weighted down outputs
   unsigned long long timeout_ns;
   unsigned long long *trace;  // [nl][kTraceCtas][kTracePhases] %globaltimer stamps, or nullptr
   int stages;            // weight-tile ring depth (bulk copies in flight)
