@@ -183,10 +183,13 @@ __device__ void stage_frags(const float *xf, int H, int nb, uint2 *xb, float *xs
       const float a1 = v[Codec<B>::hi(p0)] * pow2neg(Codec<B>::shi(p0));
       const float a2 = v[Codec<B>::lo(p1)] * pow2neg(Codec<B>::slo(p1));
       const float a3 = v[Codec<B>::hi(p1)] * pow2neg(Codec<B>::shi(p1));
-      sc += (a0 + a1) + (a2 + a3);
       uint32_t hi0, lo0, hi1, lo1;
       split2(a0, a1, hi0, lo0);
       split2(a2, a3, hi1, lo1);
+      // the offset sum from exactly the values the MMA sees (hi + lo), so the
+      // 128 offset cancels without amplifying the split's residual
+      sc += (bf16lo(hi0) + bf16lo(lo0)) + (bf16hi(hi0) + bf16hi(lo0)) + (bf16lo(hi1) + bf16lo(lo1)) +
+            (bf16hi(hi1) + bf16hi(lo1));
       xb[frag_index(blk, half, m, t, 0, bb)] = make_uint2(hi0, hi1);
       xb[frag_index(blk, half, m, t, 1, bb)] = make_uint2(lo0, lo1);
     }
