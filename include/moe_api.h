@@ -144,6 +144,30 @@ int moe_forward_traced(const moe_layer *layers, int n_layers, const float *x, in
                        void *work, size_t work_bytes, uint64_t *slot_tab, float *wmap,
                        uint32_t *topk_idx, int *dev_status, uint64_t *phase_ns, moe_stream_t stream);
 
+/* moe_forward for callers that cannot allocate device memory when they run
+ * the step -- e.g. code being captured into a CUDA graph, engines that own
+ * all device memory through their own pool, or loops that must not risk the
+ * device-wide synchronisation an allocation can cause.  (The pages have no
+ * counterpart: their engine sizes all scratch once at load.)
+ * Same arguments and results as moe_forward, minus the workspace: the
+ * library uses one fixed, process-lifetime device array of
+ * MOE_NOALLOC_MAX_WORKSPACE bytes on each GPU that loads it.
+ *   - Layers whose moe_forward_workspace exceeds that size are rejected with
+ *     MOE_ENOSPACE before anything runs (48 layers of hidden 2048, 128 experts,
+ *     inter 768 need about 1.8 MiB at nb 1; the same stack at nb 4 needs 4.4
+ *     MiB and is rejected).
+ *   - The first call on a device looks the array's address up once
+ *     (cudaGetSymbolAddress with that device current); make that first call
+ *     before capturing a stream into a graph.
+ *   - Every call on a device shares the array, so calls whose executions
+ *     overlap on the GPU (different streams, or graph branches) race; order
+ *     them on one stream.  Each call clears the parts that must start at zero.
+ *   - No allocation or free is made, by the library or any routine it calls. */
+#define MOE_NOALLOC_MAX_WORKSPACE (4u << 20)
+int moe_forward_noalloc(const moe_layer *layers, int n_layers, const float *x, int nb, float *out,
+                        uint64_t *slot_tab, float *wmap, uint32_t *topk_idx, int *dev_status,
+                        moe_stream_t stream);
+
 /* Workspace bytes moe_forward needs for these layers and nb rows (0 if the
  * arguments are invalid). */
 size_t moe_forward_workspace(const moe_layer *layers, int n_layers, int nb);

@@ -9,6 +9,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <string>
 
 #include "decode.cuh"
@@ -178,6 +179,40 @@ int check_offsets_fit(const moe_layer *layers, int nl) {
   return MOE_OK;
 }
 
+// ---- fixed scratch for callers that cannot allocate device memory
+//
+// Some callers cannot make device allocations at the point where they run
+// the MoE step: code being recorded into a CUDA graph (an allocation there
+// is either forbidden or turns into a graph node the caller did not plan),
+// engines that hand every byte of device memory to their own pool and allow
+// no outside allocations, and latency-critical loops that must not risk the
+// implicit device synchronisation a cudaMalloc / cudaFree may cause.  For
+// them moe_forward_noalloc runs the same kernel on this fixed array instead
+// of a caller-provided workspace.  The array lives for the life of the
+// process on every GPU that loads this library.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_MAX_WORKSPACE];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[128];  // per device: the array's device address
+
+// Device address of the scratch array on the current device, looked up once
+// per device (cudaGetSymbolAddress with that device current).
+int noalloc_scratch(void **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MOE_ECUDA, "cudaGetDevice failed");
+  if (dev < 0 || dev >= 128) return fail(MOE_ECUDA, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(MOE_ECUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -209,6 +244,23 @@ int moe_forward_traced(const moe_layer *layers, int n_layers, const float *x, in
   if (!phase_ns) return fail(MOE_EINVAL, "phase_ns is NULL");
   return run(layers, n_layers, x, nb, out, work, work_bytes, slot_tab, wmap, topk_idx, nullptr, nullptr,
              dev_status, stream, 0, phase_ns);
+}
+
+int moe_forward_noalloc(const moe_layer *layers, int n_layers, const float *x, int nb, float *out,
+                        uint64_t *slot_tab, float *wmap, uint32_t *topk_idx, int *dev_status,
+                        moe_stream_t stream) {
+  int r = check_layers(layers, n_layers, nb);
+  if (r == MOE_OK) r = check_offsets_fit(layers, n_layers);
+  if (r != MOE_OK) return r;
+  const moe_layer &L0 = layers[0];
+  const size_t need = ws_layout((int)L0.hidden, (int)L0.n_experts, (int)L0.inter, n_layers, nb).total;
+  if (need > MOE_NOALLOC_MAX_WORKSPACE)
+    return fail(MOE_ENOSPACE, "these layers need %zu bytes of scratch; the fixed scratch holds %u", need,
+                (unsigned)MOE_NOALLOC_MAX_WORKSPACE);
+  void *work = nullptr;
+  if ((r = noalloc_scratch(&work)) != MOE_OK) return r;
+  return run(layers, n_layers, x, nb, out, work, MOE_NOALLOC_MAX_WORKSPACE, slot_tab, wmap, topk_idx, nullptr,
+             nullptr, dev_status, stream, 0);
 }
 
 int moe_route(const moe_layer *L, const float *x, int nb, float *logits, uint32_t *topk_idx, float *topk_w,

@@ -23,7 +23,9 @@ OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EDEVICE, ENOSPACE = 0, -1, -2, -3, 
 STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_EALIGN", -4: "MOE_ECUDA",
                 -5: "MOE_ETIMEOUT", -6: "MOE_EDEVICE", -7: "MOE_ENOSPACE"}
 
-EXPORTS = ["moe_route", "moe_forward", "moe_forward_traced", "moe_forward_workspace", "moe_last_error"]
+EXPORTS = ["moe_route", "moe_forward", "moe_forward_traced", "moe_forward_noalloc", "moe_forward_workspace",
+           "moe_last_error"]
+NOALLOC_MAX_WORKSPACE = 4 << 20
 TRACE_CTAS, TRACE_PHASES = 1024, 16
 
 
@@ -67,6 +69,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.moe_forward.argtypes = [ctypes.POINTER(MoeLayer), i32, vp, i32, vp, vp, sz, vp, vp, vp, vp, vp]
         L.moe_forward_traced.restype = i32
         L.moe_forward_traced.argtypes = [ctypes.POINTER(MoeLayer), i32, vp, i32, vp, vp, sz, vp, vp, vp, vp, vp, vp]
+        L.moe_forward_noalloc.restype = i32
+        L.moe_forward_noalloc.argtypes = [ctypes.POINTER(MoeLayer), i32, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_route.restype = i32
         L.moe_route.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         _lib = L
@@ -168,6 +172,13 @@ def forward_traced(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, wor
     wp, wb = _aligned(work)
     _check(lib().moe_forward_traced(layers.c, layers.n, _p(x), x.shape[0], _p(out), wp, wb, _p(slot_tab), _p(wmap),
                                     _p(topk_idx), _p(status), _p(trace), _stream(stream)))
+
+
+def forward_noalloc(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, status: torch.Tensor,
+                    slot_tab=None, wmap=None, topk_idx=None, stream=None) -> None:
+    """moe_forward on the library's fixed scratch (no workspace, no allocation)."""
+    _check(lib().moe_forward_noalloc(layers.c, layers.n, _p(x), x.shape[0], _p(out), _p(slot_tab), _p(wmap),
+                                     _p(topk_idx), _p(status), _stream(stream)))
 
 
 def route(layers: DeviceLayers, x: torch.Tensor, topk_idx, topk_w, slot_row, wmap_row, work, status,
