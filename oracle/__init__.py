@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_route.argtypes = [ctypes.POINTER(OLayer), i32, p, p, p, p, p]
         _lib.oracle_moe_forward.argtypes = [ctypes.POINTER(OLayer), i32, i32, p, p, p, p]
         _lib.oracle_prefill_rows.argtypes = [ctypes.POINTER(OLayer), p, p, i32, i32, p, p, p]
+        _lib.oracle_route_rows.argtypes = [ctypes.POINTER(OLayer), p, i32, p, p, p, p]
+        _lib.oracle_group.restype = i32
+        _lib.oracle_group.argtypes = [i32, i32, i32, p, p, p, p, p, p]
         _lib.oracle_threads.restype = i32
     return _lib
 
@@ -194,6 +197,33 @@ def prefill_rows(layer: Layer, x: np.ndarray, rows, mirror: bool) -> dict:
     lib().oracle_prefill_rows(ctypes.byref(layer.c), _ptr(x), _ptr(rows), n, int(mirror),
                               _ptr(out), _ptr(idx), _ptr(w))
     return dict(out=out, idx=idx, w=w)
+
+
+def route_rows(layer: Layer, x: np.ndarray) -> dict:
+    """Routing of every row of a prefill chunk: logits, idx, w, gamma (None without a shared expert)."""
+    src = layer.src
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    n = x.shape[0]
+    r = dict(logits=np.empty((n, src.n_experts)), idx=np.empty((n, src.top_k), dtype=np.int32),
+             w=np.empty((n, src.top_k)), gamma=np.empty(n) if src.shared_gate is not None else None)
+    lib().oracle_route_rows(ctypes.byref(layer.c), _ptr(x), n, _ptr(r["logits"]), _ptr(r["idx"]), _ptr(r["w"]),
+                            _ptr(r["gamma"]))
+    return r
+
+
+def group(n_experts: int, idx: np.ndarray, w: np.ndarray, gamma: np.ndarray | None) -> dict:
+    """Rows grouped by expert (then the shared group): offs [G+1], rows, wts."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    n, k = idx.shape
+    G = n_experts + (1 if gamma is not None else 0)
+    ent = n * k + (n if gamma is not None else 0)
+    offs = np.empty(G + 1, dtype=np.int32)
+    rows = np.empty(ent, dtype=np.int32)
+    wts = np.empty(ent)
+    g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float64)
+    lib().oracle_group(n_experts, k, n, _ptr(idx), _ptr(w), _ptr(g), _ptr(offs), _ptr(rows), _ptr(wts))
+    return dict(offs=offs, rows=rows, wts=wts)
 
 
 def threads() -> int:

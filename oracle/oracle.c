@@ -396,6 +396,62 @@ void oracle_prefill_rows(const oracle_layer_t *L, const float *x, const int64_t 
   }
 }
 
+/* ------------------------------------------------------------ prefill grouping */
+
+/* Routing of n independent rows of a prefill chunk: per row, as in
+ * oracle_route, the logits, the top-k ids and weights; gamma[r] =
+ * sigmoid(shared_gate . x^_r) when the layer has a shared expert. */
+void oracle_route_rows(const oracle_layer_t *L, const float *x, int n, double *logits, int32_t *idx,
+                       double *w, double *gamma) {
+  const int H = L->hidden, E = L->n_experts, k = L->top_k;
+#pragma omp parallel for schedule(dynamic, 16)
+  for (int r = 0; r < n; r++) {
+    double *xb = (double *)malloc(sizeof(double) * H);
+    for (int i = 0; i < H; i++) xb[i] = x[(int64_t)r * H + i];
+    if (L->flags & ORACLE_PRENORM) rmsnorm(xb, H, xb);
+    router_row(L, xb, logits + (int64_t)r * E);
+    oracle_topk_softmax(logits + (int64_t)r * E, E, k, idx + (int64_t)r * k, w + (int64_t)r * k);
+    if (L->shared_gate && gamma) {
+      double acc = 0.0;
+      for (int i = 0; i < H; i++) acc += oracle_bf16(L->shared_gate[i]) * xb[i];
+      gamma[r] = sigmoid(acc);
+    }
+    free(xb);
+  }
+}
+
+/* Rows grouped by expert (`ExpertJob` / `prepare_expert_jobs`, struct Gpu
+ * page): group e lists, in ascending row order, the rows whose top-k holds e,
+ * with the row's weight for e; with a shared expert, group E lists every row
+ * with weight gamma[r].  Group g's entries are [offs[g], offs[g+1]).  Returns
+ * the number of groups. */
+int oracle_group(int E, int k, int n, const int32_t *idx, const double *w, const double *gamma,
+                 int32_t *offs, int32_t *rows, double *wts) {
+  int pos = 0;
+  for (int e = 0; e < E; e++) {
+    offs[e] = pos;
+    for (int r = 0; r < n; r++)
+      for (int j = 0; j < k; j++)
+        if (idx[(int64_t)r * k + j] == e) {
+          rows[pos] = r;
+          wts[pos] = w[(int64_t)r * k + j];
+          pos++;
+        }
+  }
+  int G = E;
+  if (gamma) {
+    offs[E] = pos;
+    for (int r = 0; r < n; r++) {
+      rows[pos] = r;
+      wts[pos] = gamma[r];
+      pos++;
+    }
+    G = E + 1;
+  }
+  offs[G] = pos;
+  return G;
+}
+
 /* Threads an OpenMP region here would use (1 without OpenMP). */
 int oracle_threads(void) {
 #ifdef _OPENMP

@@ -311,3 +311,104 @@ def test_prefill_rows_match_layer_and_mirror_is_bf16():
     assert np.all(np.abs(mir["out"] - exact["out"]) < 3e-2 * rms)
     m32 = mir["out"].astype(np.float32)
     assert np.array_equal(m32.view(np.uint32) & 0xFFFF, np.zeros_like(m32, dtype=np.uint32))
+
+
+# ------------------------------------------------------------------ prefill routing and grouping
+
+def _np_rmsnorm(x):
+    return x / np.sqrt((x * x).mean(axis=1, keepdims=True) + 1e-6)
+
+
+@pytest.mark.parametrize("flags", [0, synth.PRENORM])
+def test_route_rows_match_numpy_bruteforce(flags):
+    rng = np.random.default_rng(31)
+    layer = synth.make_layer(rng, 256, 24, 5, 64, 4, flags=flags)
+    ol = oracle.Layer(layer)
+    x = rng.normal(size=(40, 256)).astype(np.float32)
+    r = oracle.route_rows(ol, x)
+    xh = x.astype(np.float64)
+    if flags & synth.PRENORM:
+        xh = _np_rmsnorm(xh)
+    R = synth.bf16_bits_to_f32(layer.router).astype(np.float64)
+    logits = xh @ R.T
+    assert np.allclose(r["logits"], logits, rtol=1e-12, atol=1e-12)
+    for b in range(x.shape[0]):
+        order = np.lexsort((np.arange(24), -logits[b].astype(np.float32)))[:5]
+        assert r["idx"][b].tolist() == order.tolist()
+        assert np.allclose(r["w"][b], scipy.special.softmax(logits[b][order]), rtol=1e-12, atol=0)
+    sg = synth.bf16_bits_to_f32(layer.shared_gate).astype(np.float64)
+    assert np.allclose(r["gamma"], scipy.special.expit(xh @ sg), rtol=1e-12, atol=0)
+
+
+def test_group_hand_example():
+    # 4 rows, 3 experts, k = 2; worked by hand:
+    #   row 0 -> {2, 0}, row 1 -> {0, 1}, row 2 -> {2, 1}, row 3 -> {1, 0}
+    #   expert 0: rows 0, 1, 3; expert 1: rows 1, 2, 3; expert 2: rows 0, 2;
+    #   shared group: rows 0..3
+    idx = np.array([[2, 0], [0, 1], [2, 1], [1, 0]])
+    w = np.array([[0.6, 0.4], [0.7, 0.3], [0.55, 0.45], [0.9, 0.1]])
+    gamma = np.array([0.1, 0.2, 0.3, 0.4])
+    g = oracle.group(3, idx, w, gamma)
+    assert g["offs"].tolist() == [0, 3, 6, 8, 12]
+    assert g["rows"].tolist() == [0, 1, 3, 1, 2, 3, 0, 2, 0, 1, 2, 3]
+    assert g["wts"].tolist() == [0.4, 0.7, 0.1, 0.3, 0.45, 0.9, 0.6, 0.55, 0.1, 0.2, 0.3, 0.4]
+    g2 = oracle.group(3, idx, w, None)
+    assert g2["offs"].tolist() == [0, 3, 6, 8]
+    assert g2["rows"].tolist() == [0, 1, 3, 1, 2, 3, 0, 2]
+
+
+def test_group_invariants_random():
+    rng = np.random.default_rng(32)
+    n, E, k = 300, 37, 6
+    idx = np.stack([rng.choice(E, size=k, replace=False) for _ in range(n)]).astype(np.int32)
+    w = rng.random((n, k))
+    g = oracle.group(E, idx, w, None)
+    offs, rows, wts = g["offs"], g["rows"], g["wts"]
+    assert np.array_equal(np.diff(offs), np.bincount(idx.ravel(), minlength=E))
+    seen = set()
+    for e in range(E):
+        rs = rows[offs[e]:offs[e + 1]]
+        assert np.all(np.diff(rs) > 0), "rows ascend inside a group"
+        for p, r in zip(range(offs[e], offs[e + 1]), rs):
+            j = int(np.nonzero(idx[r] == e)[0][0])
+            assert wts[p] == w[r, j]
+            seen.add((int(r), e))
+    assert len(seen) == n * k
+
+
+def test_prefill_mirror_matches_dense_bf16_bruteforce():
+    """The bf16 mirror equals a dense numpy evaluation with x^, W, h and the
+    output rounded to bf16 (round to nearest even, via float32, exact here)."""
+    rng = np.random.default_rng(33)
+    H, E, k, I = 128, 6, 2, 64
+    layer = synth.make_layer(rng, H, E, k, I, 4, flags=synth.RESIDUAL | synth.PRENORM)
+    ol = oracle.Layer(layer)
+    x = rng.normal(size=(5, H)).astype(np.float32)
+    got = oracle.prefill_rows(ol, x, np.arange(5), mirror=True)
+
+    def bf(a):
+        return synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(np.asarray(a, dtype=np.float32))).astype(np.float64)
+
+    def dense(rec, lay, bits):
+        return bf(oracle.dequant(rec, lay.gate_up, bits)), bf(oracle.dequant(rec, lay.down, bits))
+
+    xh = _np_rmsnorm(x.astype(np.float64))
+    xe = bf(xh)
+    R = synth.bf16_bits_to_f32(layer.router).astype(np.float64)
+    sg = synth.bf16_bits_to_f32(layer.shared_gate).astype(np.float64)
+    for b in range(5):
+        lg = R @ xh[b]
+        ids = np.lexsort((np.arange(E), -lg.astype(np.float32)))[:k]
+        wt = scipy.special.softmax(lg[ids])
+        acc = np.zeros(H)
+        experts = [(layer.records[e], layer.layout, layer.bits, wt[j]) for j, e in enumerate(ids)]
+        experts.append((layer.shared_record, layer.shared_layout, 4, scipy.special.expit(sg @ xh[b])))
+        for rec, lay, bits, wgt in experts:
+            Wgu, Wd = dense(rec, lay, bits)
+            gu = Wgu @ xe[b]
+            h = bf(gu[:I] / (1.0 + np.exp(-gu[:I])) * gu[I:])
+            acc += wgt * (Wd @ h)
+        want = bf(acc + x[b])
+        ulp = np.abs(want) * 2.0 ** -7
+        assert np.all(np.abs(got["out"][b] - want) <= ulp), f"row {b}"
+        assert np.mean(got["out"][b] == want) > 0.99
