@@ -69,7 +69,7 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_route.restype = i32
         _lib.oracle_route.argtypes = [ctypes.POINTER(OLayer), i32, p, p, p, p, p]
         _lib.oracle_moe_forward.argtypes = [ctypes.POINTER(OLayer), i32, i32, p, p, p, p]
-        _lib.oracle_prefill_rows.argtypes = [ctypes.POINTER(OLayer), p, p, i32, i32, p, p, p]
+        _lib.oracle_prefill_rows.argtypes = [ctypes.POINTER(OLayer), p, p, i32, i32, p, p, p, p]
         _lib.oracle_route_rows.argtypes = [ctypes.POINTER(OLayer), p, i32, p, p, p, p]
         _lib.oracle_group.restype = i32
         _lib.oracle_group.argtypes = [i32, i32, i32, p, p, p, p, p, p]
@@ -187,6 +187,8 @@ def moe_forward(layers: list[Layer], x: np.ndarray) -> dict:
 
 
 def prefill_rows(layer: Layer, x: np.ndarray, rows, mirror: bool) -> dict:
+    """Listed rows of a prefill chunk: out, idx, w; in mirror mode also
+    `allow`, the one-flip allowance of the h rounding (a test tolerance term)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     n = rows.shape[0]
@@ -194,9 +196,10 @@ def prefill_rows(layer: Layer, x: np.ndarray, rows, mirror: bool) -> dict:
     out = np.empty((n, H))
     idx = np.empty((n, k), dtype=np.int32)
     w = np.empty((n, k))
+    allow = np.zeros((n, H)) if mirror else None
     lib().oracle_prefill_rows(ctypes.byref(layer.c), _ptr(x), _ptr(rows), n, int(mirror),
-                              _ptr(out), _ptr(idx), _ptr(w))
-    return dict(out=out, idx=idx, w=w)
+                              _ptr(out), _ptr(idx), _ptr(w), _ptr(allow))
+    return dict(out=out, idx=idx, w=w, allow=allow)
 
 
 def route_rows(layer: Layer, x: np.ndarray) -> dict:

@@ -123,9 +123,10 @@ void oracle_dequant(const uint8_t *rec, const oq_t *q, int bits, double *W) {
 }
 
 /* y[out] = W x for one projection (dequantized row by row), optionally
- * rounding each weight to bf16 first (mirror mode). */
+ * rounding each weight to bf16 first (mirror mode); yabs[out] (may be NULL)
+ * receives sum_i |W[o][i] x[i]|. */
 static void qmatvec(const uint8_t *rec, const oq_t *q, int bits, const double *x, double *y,
-                    int mirror) {
+                    int mirror, double *yabs) {
   const int64_t words_per_row = (int64_t)q->inp * bits / 32;
   const int64_t groups = q->inp / 64;
   const uint32_t *codes = (const uint32_t *)(rec + q->w);
@@ -133,43 +134,99 @@ static void qmatvec(const uint8_t *rec, const oq_t *q, int bits, const double *x
   const uint16_t *bi = (const uint16_t *)(rec + q->b);
   for (int64_t o = 0; o < q->out; o++) {
     const uint32_t *row = codes + o * words_per_row;
-    double acc = 0.0;
+    double acc = 0.0, aabs = 0.0;
     for (int64_t i = 0; i < q->inp; i++) {
       int64_t g = i / 64;
       double w = oracle_bf16(sc[o * groups + g]) * (double)oracle_code_at(row, i, bits) +
                  oracle_bf16(bi[o * groups + g]);
       if (mirror) w = round_bf16(w);
       acc += w * x[i];
+      aabs += fabs(w * x[i]);
     }
     y[o] = acc;
+    if (yabs) yabs[o] = aabs;
   }
 }
 
+/* One dequantized weight W[o][i] of a projection (bf16-rounded when mirror). */
+static double qweight(const uint8_t *rec, const oq_t *q, int bits, int64_t o, int64_t i, int mirror) {
+  const int64_t words_per_row = (int64_t)q->inp * bits / 32;
+  const int64_t groups = q->inp / 64;
+  const uint32_t *row = (const uint32_t *)(rec + q->w) + o * words_per_row;
+  const uint16_t *sc = (const uint16_t *)(rec + q->s);
+  const uint16_t *bi = (const uint16_t *)(rec + q->b);
+  double w = oracle_bf16(sc[o * groups + i / 64]) * (double)oracle_code_at(row, i, bits) +
+             oracle_bf16(bi[o * groups + i / 64]);
+  return mirror ? round_bf16(w) : w;
+}
+
+/* bf16 neighbours of a bf16 value r (r != 0): the next value away from zero
+ * and the next toward zero. */
+static void bf16_neighbours(double r, double *away, double *toward) {
+  float f = (float)r;
+  uint32_t u, a, t;
+  memcpy(&u, &f, 4);
+  a = u + 0x10000u;
+  t = u - 0x10000u;
+  float fa, ft;
+  memcpy(&fa, &a, 4);
+  memcpy(&ft, &t, 4);
+  *away = fa;
+  *toward = ft;
+}
+
 /* One expert on one row: gu = W_gu x (2*inter outputs: gate then up),
- * h = silu(gate) * up, y = W_d h.  `y` has `hidden` entries. */
+ * h = silu(gate) * up, y = W_d h.  `y` has `hidden` entries.
+ *
+ * Tolerance helper of the bf16 mirror (test infrastructure, not a value of
+ * the method): when `allow` is given, each h whose exact value lies within
+ * the fp32 accuracy band of a bf16 rounding boundary may round to either
+ * side in a kernel that accumulates in fp32; the largest output change one
+ * such flip can cause, |weight * W_d[o][i] * (other side - rounded h)|, is
+ * max-accumulated into allow[o].  The band is 2^-20 times the sums of
+ * absolute products feeding gate and up (|silu'| <= 1.1), plus 2^-22 |h|
+ * for the rounding of silu and the product. */
 static void expert_row(const uint8_t *rec, const oq_t *gu, const oq_t *dn, int bits, int inter,
-                       const double *x, double *y, int mirror) {
+                       const double *x, double *y, int mirror, double weight, double *allow) {
   double *g = (double *)malloc(sizeof(double) * 2 * (size_t)inter);
+  double *gabs = (double *)malloc(sizeof(double) * 2 * (size_t)inter);
   double *h = (double *)malloc(sizeof(double) * (size_t)inter);
-  qmatvec(rec, gu, bits, x, g, mirror);
+  qmatvec(rec, gu, bits, x, g, mirror, gabs);
   for (int i = 0; i < inter; i++) {
-    h[i] = silu(g[i]) * g[inter + i];
-    if (mirror) h[i] = round_bf16(h[i]);
+    const double hs = silu(g[i]) * g[inter + i];
+    h[i] = mirror ? round_bf16(hs) : hs;
+    if (mirror && allow && h[i] != 0.0) {
+      double away, toward;
+      bf16_neighbours(h[i], &away, &toward);
+      /* the boundary on hs's side of the rounded value, and the value across it */
+      const int out_side = fabs(hs) > fabs(h[i]);
+      const double other = out_side ? away : toward;
+      const double boundary = 0.5 * (h[i] + other);
+      const double band = ldexp(fabs(silu(g[i])) * gabs[inter + i] + 1.1 * fabs(g[inter + i]) * gabs[i], -20) +
+                          ldexp(fabs(hs), -22);
+      if (fabs(hs - boundary) <= band) {
+        for (uint32_t o = 0; o < dn->out; o++) {
+          const double d = fabs(weight * qweight(rec, dn, bits, o, i, 1) * (other - h[i]));
+          if (d > allow[o]) allow[o] = d;
+        }
+      }
+    }
   }
-  qmatvec(rec, dn, bits, h, y, mirror);
+  qmatvec(rec, dn, bits, h, y, mirror, NULL);
   free(g);
+  free(gabs);
   free(h);
 }
 
 /* Exported for the brute-force pin: expert `e` of a layer on one row. */
 void oracle_expert(const oracle_layer_t *L, int e, const double *x, double *y) {
   expert_row(L->experts + (uint64_t)e * L->stride, &L->gate_up, &L->down, L->bits, L->inter, x, y,
-             0);
+             0, 1.0, NULL);
 }
 
 /* Exported for the brute-force pin: the shared expert on one row (4-bit). */
 void oracle_shared_expert(const oracle_layer_t *L, const double *x, double *y) {
-  expert_row(L->shared_record, &L->sh_gate_up, &L->sh_down, 4, L->inter, x, y, 0);
+  expert_row(L->shared_record, &L->sh_gate_up, &L->sh_down, 4, L->inter, x, y, 0, 1.0, NULL);
 }
 
 /* ------------------------------------------------------------ routing */
@@ -353,9 +410,11 @@ void oracle_moe_forward(const oracle_layer_t *layers, int n_layers, int nb, cons
  * route in double, then evaluate the experts either exactly (mirror = 0) or
  * with bf16 rounding of x^, W, h and the output (mirror = 1).  Rows are
  * independent, so they are spread over host threads.
- *   x [t][H] float32; rows [n]; out [n][H]; idx [n][k]; w [n][k]. */
+ *   x [t][H] float32; rows [n]; out [n][H]; idx [n][k]; w [n][k];
+ *   allow [n][H] or NULL: in mirror mode, the one-flip allowance of
+ *   expert_row over the row's experts (max), a test tolerance term. */
 void oracle_prefill_rows(const oracle_layer_t *L, const float *x, const int64_t *rows, int n,
-                         int mirror, double *out, int32_t *idx, double *w) {
+                         int mirror, double *out, int32_t *idx, double *w, double *allow) {
   const int H = L->hidden, E = L->n_experts, k = L->top_k;
 #pragma omp parallel for schedule(dynamic, 1)
   for (int n_i = 0; n_i < n; n_i++) {
@@ -366,6 +425,9 @@ void oracle_prefill_rows(const oracle_layer_t *L, const float *x, const int64_t 
     int32_t *id = idx + (int64_t)n_i * k;
     double *wt = w + (int64_t)n_i * k;
     double *ob = out + (int64_t)n_i * H;
+    double *al = allow ? allow + (int64_t)n_i * H : NULL;
+    if (al)
+      for (int i = 0; i < H; i++) al[i] = 0.0;
     const float *xr = x + rows[n_i] * H;
     for (int i = 0; i < H; i++) xb[i] = xr[i];
     if (L->flags & ORACLE_PRENORM) rmsnorm(xb, H, xb);
@@ -375,14 +437,14 @@ void oracle_prefill_rows(const oracle_layer_t *L, const float *x, const int64_t 
     for (int i = 0; i < H; i++) ob[i] = 0.0;
     for (int r = 0; r < k; r++) {
       expert_row(L->experts + (uint64_t)id[r] * L->stride, &L->gate_up, &L->down, L->bits,
-                 L->inter, xe, y, mirror);
+                 L->inter, xe, y, mirror, wt[r], al);
       for (int i = 0; i < H; i++) ob[i] += wt[r] * y[i];
     }
     if (L->shared_gate) {
       double acc = 0.0;
       for (int i = 0; i < H; i++) acc += oracle_bf16(L->shared_gate[i]) * xb[i];
       double gm = sigmoid(acc);
-      expert_row(L->shared_record, &L->sh_gate_up, &L->sh_down, 4, L->inter, xe, y, mirror);
+      expert_row(L->shared_record, &L->sh_gate_up, &L->sh_down, 4, L->inter, xe, y, mirror, gm, al);
       for (int i = 0; i < H; i++) ob[i] += gm * y[i];
     }
     if (L->flags & ORACLE_RESIDUAL)
