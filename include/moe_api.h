@@ -168,6 +168,48 @@ int moe_forward_noalloc(const moe_layer *layers, int n_layers, const float *x, i
                         uint64_t *slot_tab, float *wmap, uint32_t *topk_idx, int *dev_status,
                         moe_stream_t stream);
 
+/* Prefill chunk: t rows through ONE layer on the tensor cores (the prefill
+ * MoE of the struct Gpu page, `pf_experts`: the shared expert over every row,
+ * then the routed experts one at a time -- gather the expert's rows, compute,
+ * scatter-add -- with the rows grouped by expert as `ExpertJob` /
+ * `prepare_expert_jobs` do).  Per row the routing equals moe_route's (steps
+ * 1-2 above); the experts then run as grouped GEMMs with bf16 operands:
+ *   x^ is rounded to bf16, every dequantized weight is rounded to bf16
+ *   (bf16(scale * code + bias)), h = silu(gate) * up is rounded to bf16, the
+ *   products accumulate in fp32, and
+ *   out[r] = bf16( sum_j w_j * y_j[r] + sigmoid(shared_gate . x^[r]) *
+ *                  y_shared[r]  (+ x[r] when MOE_RESIDUAL) ).
+ * The router itself reads x^ at fp32 accuracy (x^ split into two bf16 terms).
+ *   L        host pointer to one layer; routed records must be 4-bit
+ *   x        [t][hidden] float32, 16-byte aligned; t in 1..1048576
+ *   out      [t][hidden] bf16 (uint16 bit patterns); must not overlap x
+ *   work     device workspace of at least moe_prefill_workspace(L, t) bytes,
+ *            256-byte aligned; its contents need no initialisation
+ *   topk_idx [t][top_k] uint32 (descending logit), or NULL
+ * Supported shapes: hidden % 256 == 0 (<= 16384), inter % 64 == 0 (<= 16384),
+ * n_experts <= 1024, top_k <= 32, group == 64.
+ * Returns MOE_OK or a negative moe_status; device-side failures (a null or
+ * misaligned record address, a bounded wait that gave up) land in *dev_status. */
+int moe_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *work, size_t work_bytes,
+                uint32_t *topk_idx, int *dev_status, moe_stream_t stream);
+
+/* Workspace bytes moe_prefill and moe_prefill_group need for t rows (0 if the
+ * arguments are invalid). */
+size_t moe_prefill_workspace(const moe_layer *L, int t);
+
+/* The routing and grouping stage of moe_prefill alone (same arguments):
+ *   topk_idx   [t][top_k] uint32, topk_w [t][top_k] float32 (as moe_route)
+ *   group_offs [G + 1] int32: G = n_experts (+1 when the layer has a shared
+ *              expert, which is group n_experts and holds every row);
+ *              group g's entries are [group_offs[g], group_offs[g+1])
+ *   group_rows [t*top_k (+t)] int32: the row of each entry; inside a group
+ *              rows ascend (a stable grouping)
+ *   group_w    [t*top_k (+t)] float32: the entry's routing weight (shared
+ *              group: the row's sigmoid gate) */
+int moe_prefill_group(const moe_layer *L, const float *x, int t, uint32_t *topk_idx, float *topk_w,
+                      int32_t *group_offs, int32_t *group_rows, float *group_w, void *work,
+                      size_t work_bytes, int *dev_status, moe_stream_t stream);
+
 /* Workspace bytes moe_forward needs for these layers and nb rows (0 if the
  * arguments are invalid). */
 size_t moe_forward_workspace(const moe_layer *layers, int n_layers, int nb);

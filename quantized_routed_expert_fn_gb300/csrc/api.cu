@@ -14,6 +14,7 @@
 
 #include "decode.cuh"
 #include "moe_api.h"
+#include "prefill.cuh"
 
 namespace {
 
@@ -213,6 +214,77 @@ int noalloc_scratch(void **out) {
   return MOE_OK;
 }
 
+// ---- prefill chunk
+
+constexpr int kMaxPrefillRows = 1 << 20;
+
+int check_prefill(const moe_layer *L, int t) {
+  if (!L) return fail(MOE_EINVAL, "layer is NULL");
+  if (t < 1 || t > kMaxPrefillRows) return fail(MOE_EINVAL, "t %d outside 1..%d", t, kMaxPrefillRows);
+  const uint32_t H = L->hidden, E = L->n_experts, K = L->top_k, I = L->inter;
+  if (H == 0 || H % 256) return fail(MOE_ESHAPE, "hidden %u must be a positive multiple of 256", H);
+  if (H > 16384) return fail(MOE_ESHAPE, "hidden %u above 16384", H);
+  if (I == 0 || I % 64 || I > 16384) return fail(MOE_ESHAPE, "inter %u must be a multiple of 64 in 64..16384", I);
+  if (E < 1 || E > 1024) return fail(MOE_ESHAPE, "n_experts %u outside 1..1024", E);
+  if (K < 1 || K > E || K > 32) return fail(MOE_ESHAPE, "top_k %u outside 1..min(n_experts, 32)", K);
+  if (L->bits != 4) return fail(MOE_ESHAPE, "prefill takes 4-bit routed records; bits %u", L->bits);
+  if (L->group != 64) return fail(MOE_ESHAPE, "group %u, only 64 is supported", L->group);
+  if (L->flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM)) return fail(MOE_EINVAL, "unknown flags 0x%x", L->flags);
+  if (!L->router || !L->expert_addr) return fail(MOE_EINVAL, "router / expert_addr NULL");
+  if ((uintptr_t)L->router & 15u) return fail(MOE_EALIGN, "router not 16-byte aligned");
+  if (!L->shared_gate != !L->shared_record)
+    return fail(MOE_EINVAL, "shared_gate and shared_record must both be set or both NULL");
+  int r;
+  if (L->shared_gate) {
+    if (((uintptr_t)L->shared_gate | (uintptr_t)L->shared_record) & 15u)
+      return fail(MOE_EALIGN, "shared gate / record not 16-byte aligned");
+    if ((r = check_q(L->sh_gate_up, 2 * I, H, "sh_gate_up", 0))) return r;
+    if ((r = check_q(L->sh_down, H, I, "sh_down", 0))) return r;
+  }
+  if ((r = check_q(L->gate_up, 2 * I, H, "gate_up", 0))) return r;
+  if ((r = check_q(L->down, H, I, "down", 0))) return r;
+  return check_offsets_fit(L, 1);
+}
+
+size_t prefill_bytes(const moe_layer *L, int t) {
+  return moe::pf_workspace_bytes((int)L->hidden, (int)L->n_experts, (int)L->top_k, (int)L->inter, t);
+}
+
+int run_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *work, size_t work_bytes,
+                uint32_t *topk_idx, float *topk_w, int *status, moe_stream_t stream, int route_only) {
+  const int H = (int)L->hidden;
+  if (!x) return fail(MOE_EINVAL, "x is NULL");
+  if (!route_only && !out) return fail(MOE_EINVAL, "out is NULL");
+  if (!status) return fail(MOE_EINVAL, "dev_status is NULL");
+  if (!work) return fail(MOE_EINVAL, "work is NULL");
+  if ((uintptr_t)work & 255u) return fail(MOE_EALIGN, "work must be 256-byte aligned");
+  if ((uintptr_t)x & 15u) return fail(MOE_EALIGN, "x must be 16-byte aligned");
+  if (!route_only && overlap(x, (size_t)t * H * 4, out, (size_t)t * H * 2))
+    return fail(MOE_EINVAL, "out overlaps x");
+  const size_t need = prefill_bytes(L, t);
+  if (work_bytes < need) return fail(MOE_ENOSPACE, "work holds %zu bytes, %zu needed", work_bytes, need);
+  moe::PfParams p;
+  memset(&p, 0, sizeof p);
+  p.H = H, p.E = (int)L->n_experts, p.K = (int)L->top_k, p.I = (int)L->inter, p.t = t;
+  p.flags = L->flags & (MOE_RESIDUAL | MOE_PRENORM);
+  p.route_only = route_only;
+  p.x = x, p.out = out;
+  p.router = L->router, p.sgate = L->shared_gate;
+  p.srec = (const uint8_t *)L->shared_record;
+  p.eaddr = L->expert_addr;
+  p.gu = {(uint32_t)L->gate_up.w, (uint32_t)L->gate_up.s, (uint32_t)L->gate_up.b};
+  p.dn = {(uint32_t)L->down.w, (uint32_t)L->down.s, (uint32_t)L->down.b};
+  p.sgu = {(uint32_t)L->sh_gate_up.w, (uint32_t)L->sh_gate_up.s, (uint32_t)L->sh_gate_up.b};
+  p.sdn = {(uint32_t)L->sh_down.w, (uint32_t)L->sh_down.s, (uint32_t)L->sh_down.b};
+  p.topk_out = topk_idx, p.topkw_out = topk_w;
+  p.status = status;
+  p.timeout_ns = timeout_ns();
+  moe::pf_carve(p, work);
+  const cudaError_t e = moe::pf_launch(p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(MOE_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
+  return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -273,6 +345,40 @@ int moe_route(const moe_layer *L, const float *x, int nb, float *logits, uint32_
     return fail(MOE_EINVAL, "topk_idx, topk_w, slot_row and wmap_row are required");
   return run(L, 1, x, nb, nullptr, work, work_bytes, slot_row, wmap_row, topk_idx, topk_w, logits, dev_status,
              stream, 1);
+}
+
+size_t moe_prefill_workspace(const moe_layer *L, int t) {
+  if (check_prefill(L, t) != MOE_OK) return 0;
+  return prefill_bytes(L, t);
+}
+
+int moe_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *work, size_t work_bytes,
+                uint32_t *topk_idx, int *dev_status, moe_stream_t stream) {
+  const int r = check_prefill(L, t);
+  if (r != MOE_OK) return r;
+  return run_prefill(L, x, t, out, work, work_bytes, topk_idx, nullptr, dev_status, stream, 0);
+}
+
+int moe_prefill_group(const moe_layer *L, const float *x, int t, uint32_t *topk_idx, float *topk_w,
+                      int32_t *group_offs, int32_t *group_rows, float *group_w, void *work, size_t work_bytes,
+                      int *dev_status, moe_stream_t stream) {
+  int r = check_prefill(L, t);
+  if (r != MOE_OK) return r;
+  if (!topk_idx || !topk_w || !group_offs || !group_rows || !group_w)
+    return fail(MOE_EINVAL, "topk_idx, topk_w, group_offs, group_rows and group_w are required");
+  if ((r = run_prefill(L, x, t, nullptr, work, work_bytes, topk_idx, topk_w, dev_status, stream, 1))) return r;
+  moe::PfParams p;
+  memset(&p, 0, sizeof p);
+  p.H = (int)L->hidden, p.E = (int)L->n_experts, p.K = (int)L->top_k, p.I = (int)L->inter, p.t = t;
+  moe::pf_carve(p, work);
+  const int G = p.E + (L->shared_gate ? 1 : 0);
+  const size_t ent = (size_t)t * p.K + (L->shared_gate ? (size_t)t : 0);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(group_offs, p.offs, (size_t)(G + 1) * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(group_rows, p.rows, ent * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(group_w, p.wts, ent * 4, cudaMemcpyDeviceToDevice, st);
+  if (e != cudaSuccess) return fail(MOE_ECUDA, "copy of the grouping failed: %s", cudaGetErrorString(e));
+  return MOE_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,52 @@
+// prefill.cuh -- parameters of the prefill-chunk path (t rows through one layer).
+#pragma once
+
+#include <cstdint>
+
+#include "decode.cuh"
+
+namespace moe {
+
+struct PfItem {
+  int g, mt, n0, nlen;  // group (expert, or E = shared), row tile, first grouped entry, entries
+};
+
+constexpr int kPfTileN = 256;  // token columns per tensor-core tile
+constexpr int kPfChunk = 64;   // tokens per chunk of the stable grouping
+
+struct PfParams {
+  int H, E, K, I, t;
+  uint32_t flags;
+  int route_only;          // stop after the grouping
+  const float *x;          // [t][H]
+  uint16_t *out;           // bf16 [t][H]
+  const uint16_t *router, *sgate;
+  const uint8_t *srec;
+  const uint64_t *eaddr;
+  QOff gu, dn, sgu, sdn;
+  uint32_t *topk_out;      // [t][K] or nullptr
+  float *topkw_out;        // [t][K] or nullptr
+  int *status;
+  unsigned long long timeout_ns;
+  // workspace
+  uint16_t *xr_hi, *xr_lo;  // bf16 [t][H], natural order: router operand (hi + lo split of x^)
+  uint16_t *xg;             // bf16 [t][H], x^ rounded, k permuted within 8-blocks: expert operand
+  float *gam;               // [t] shared-expert gate
+  float *logits;            // [t][E]
+  int *tk_idx;              // [t][K]
+  float *tk_w;              // [t][K]
+  int *chist;               // [nch][E] per-chunk expert counts, then per-chunk list bases
+  int *offs;                // [E+2] first grouped entry of each group; offs[G] = total
+  int *rows;                // [t*(K+1)] token of each grouped entry
+  float *wts;               // [t*(K+1)] its weight
+  PfItem *items1, *items2;  // gate_up / down work lists
+  int *nitems;              // [2]
+  uint16_t *hbuf;           // bf16 [t*(K+1)][I], k permuted within 8-blocks
+  float *Y;                 // [t][H] fp32 accumulator
+};
+
+size_t pf_workspace_bytes(int H, int E, int K, int I, int t);
+void pf_carve(PfParams &p, void *work);
+cudaError_t pf_launch(PfParams &p, cudaStream_t st);
+
+}  // namespace moe

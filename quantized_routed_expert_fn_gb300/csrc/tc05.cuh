@@ -1,0 +1,103 @@
+// tc05.cuh -- 5th-generation tensor core (tcgen05) primitives for sm_100-family
+// GPUs, written as inline PTX: TMEM allocation, shared-memory matrix and
+// instruction descriptors, MMA issue / commit, TMEM loads.
+//
+// Operands used here: A (M = 128 rows) and B (N rows) both K-major bf16 in
+// shared memory with the 128-byte swizzle: a row holds 64 consecutive k
+// (128 B); 8 rows form a 1024-byte atom in which 16-byte chunk c of row r
+// sits at chunk position c ^ r.  One MMA covers k = 16 (32 bytes of a row);
+// the next k-step starts 32 bytes further (the hardware applies the swizzle
+// to the address bits, so advancing the start address inside an atom is
+// exact).  Accumulators are fp32 in TMEM: lane = row of A, column = row of B.
+#pragma once
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+namespace tc05 {
+
+// byte offset of (row, 16-byte chunk) inside a K-major 128B-swizzled tile
+__host__ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk) {
+  return (uint32_t)((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Shared-memory matrix descriptor: start address, leading byte offset (unused
+// for swizzled K-major, set to 16 B), stride byte offset 1024 B (8-row atoms),
+// descriptor version 1, base offset 0 (tiles 1024-byte aligned), 128B swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr >> 4) & 0x3fffu);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
+// M = 128, N = n (multiple of 16, 16..256).
+__host__ __device__ __forceinline__ uint32_t idesc_bf16(int n) {
+  return (1u << 4)                 // D format fp32
+         | (1u << 7)               // A format bf16
+         | (1u << 10)              // B format bf16
+         | ((uint32_t)(n >> 3) << 17)
+         | ((uint32_t)(128 >> 4) << 24);
+}
+
+// One warp: allocate ncols TMEM columns (power of two >= 32); the address is
+// written to *dst (shared memory).
+__device__ __forceinline__ void alloc(uint32_t *dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// One thread: D[tmem] (+)= A * B over k = 16.
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                    uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// One thread: arrive on the mbarrier once all MMAs issued so far complete.
+__device__ __forceinline__ void commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Warp: 32 consecutive fp32 columns of the warp's 32 TMEM lanes.
+__device__ __forceinline__ void ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+// cp.async of 16 bytes global -> shared (L2 only), and its group wait
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+}  // namespace tc05
+}  // namespace moe

@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_EALIGN
                 -5: "MOE_ETIMEOUT", -6: "MOE_EDEVICE", -7: "MOE_ENOSPACE"}
 
 EXPORTS = ["moe_route", "moe_forward", "moe_forward_traced", "moe_forward_noalloc", "moe_forward_workspace",
-           "moe_last_error"]
+           "moe_prefill", "moe_prefill_workspace", "moe_prefill_group", "moe_last_error"]
 NOALLOC_MAX_WORKSPACE = 4 << 20
 TRACE_CTAS, TRACE_PHASES = 1024, 16
 
@@ -73,6 +73,12 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.moe_forward_noalloc.argtypes = [ctypes.POINTER(MoeLayer), i32, vp, i32, vp, vp, vp, vp, vp, vp]
         L.moe_route.restype = i32
         L.moe_route.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+        L.moe_prefill_workspace.restype = sz
+        L.moe_prefill_workspace.argtypes = [ctypes.POINTER(MoeLayer), i32]
+        L.moe_prefill.restype = i32
+        L.moe_prefill.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, sz, vp, vp, vp]
+        L.moe_prefill_group.restype = i32
+        L.moe_prefill_group.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         _lib = L
     return _lib
 
@@ -187,3 +193,28 @@ def route(layers: DeviceLayers, x: torch.Tensor, topk_idx, topk_w, slot_row, wma
     wp, wb = _aligned(work)
     _check(lib().moe_route(arr, _p(x), x.shape[0], _p(logits), _p(topk_idx), _p(topk_w), _p(slot_row),
                            _p(wmap_row), wp, wb, _p(status), _stream(stream)))
+
+
+def _layer_ptr(layers: DeviceLayers, layer: int):
+    return ctypes.cast(ctypes.byref(layers.c, layer * ctypes.sizeof(MoeLayer)), ctypes.POINTER(MoeLayer))
+
+
+def prefill_workspace(layers: DeviceLayers, t: int, layer: int = 0) -> int:
+    return int(lib().moe_prefill_workspace(_layer_ptr(layers, layer), t))
+
+
+def prefill(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, work: torch.Tensor, status: torch.Tensor,
+            topk_idx=None, layer: int = 0, stream=None) -> None:
+    """moe_prefill: x float32 [t][H] -> out bf16 bits (int16 tensor) [t][H]."""
+    wp, wb = _aligned(work)
+    _check(lib().moe_prefill(_layer_ptr(layers, layer), _p(x), x.shape[0], _p(out), wp, wb, _p(topk_idx),
+                             _p(status), _stream(stream)))
+
+
+def prefill_group(layers: DeviceLayers, x: torch.Tensor, topk_idx, topk_w, group_offs, group_rows, group_w,
+                  work, status, layer: int = 0, stream=None) -> None:
+    """moe_prefill_group: routing and the stable expert grouping of a prefill chunk."""
+    wp, wb = _aligned(work)
+    _check(lib().moe_prefill_group(_layer_ptr(layers, layer), _p(x), x.shape[0], _p(topk_idx), _p(topk_w),
+                                   _p(group_offs), _p(group_rows), _p(group_w), wp, wb, _p(status),
+                                   _stream(stream)))

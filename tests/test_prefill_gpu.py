@@ -1,0 +1,217 @@
+"""GPU parity of the prefill chunk path (moe_prefill, moe_prefill_group) against the oracle.
+
+Outputs are bf16, so they are graded against the oracle's bf16 mirror (x^, the
+dequantized weights, h and the output rounded to bf16 where the tensor-core
+path stores bf16): |gpu - oracle| <= 2e-3 * RMS(MoE row) + 1 bf16 ulp of the
+oracle element + the oracle's one-flip allowance.  The allowance covers an h
+whose exact value sits within fp32 accumulation accuracy of a bf16 rounding
+boundary, so that a kernel summing in fp32 may round it to the other side;
+one such flip moves the output by |w * W_d[o][i] * (bf16 step of h_i)|, and
+the allowance is the largest such move among the row's ambiguous h.
+Routing ids are exact where the k-th and (k+1)-th logits differ by at least
+1e-3; the grouping is exact (it is a function of the ids).
+"""
+import numpy as np
+import pytest
+
+import oracle
+from helpers import GAP, TOL, topk_gap
+from quantized_routed_expert_fn_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from quantized_routed_expert_fn_gb300 import build, moe as m
+    build.build()
+    m.lib()
+    return m
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    _, e = np.frexp(np.abs(v))  # |v| = f * 2^e, f in [0.5, 1)
+    return np.ldexp(1.0, e - 8)
+
+
+def gaps_of(logits, k):
+    return np.array([topk_gap(logits[b], k) for b in range(logits.shape[0])])
+
+
+def rows_with_gap(ol, rng, t, H, zipf=False):
+    """t rows (seeded) whose top-k gap is >= GAP; rows are independent, so
+    rows without the gap are dropped and replaced."""
+    k = ol.src.top_k
+    keep = []
+    while sum(len(a) for a in keep) < t:
+        x = synth.make_prefill_x(rng, t, H) if zipf else rng.normal(size=(t, H)).astype(np.float32)
+        g = gaps_of(oracle.route_rows(ol, x)["logits"], k)
+        keep.append(x[g >= GAP])
+    return np.ascontiguousarray(np.concatenate(keep)[:t])
+
+
+def run_prefill(m, dl, x):
+    t, H = x.shape
+    k = dl.src[0].top_k
+    xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+    out = torch.empty((t, H), dtype=torch.int16, device="cuda")
+    idx = torch.zeros((t, k), dtype=torch.int32, device="cuda")
+    ws = m.alloc_workspace(m.prefill_workspace(dl, t))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.prefill(dl, xt, out, ws, status, idx)
+    torch.cuda.synchronize()
+    assert status.item() == 0, m.STATUS_NAMES.get(status.item())
+    o = synth.bf16_bits_to_f32(out.cpu().numpy().view(np.uint16)).astype(np.float64)
+    return o, idx.cpu().numpy()
+
+
+def run_group(m, dl, x):
+    t, H = x.shape
+    L = dl.src[0]
+    k, E = L.top_k, L.n_experts
+    shared = L.shared_gate is not None
+    G = E + (1 if shared else 0)
+    ent = t * k + (t if shared else 0)
+    xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+    idx = torch.zeros((t, k), dtype=torch.int32, device="cuda")
+    w = torch.zeros((t, k), dtype=torch.float32, device="cuda")
+    offs = torch.full((G + 1,), -1, dtype=torch.int32, device="cuda")
+    rows = torch.full((ent,), -1, dtype=torch.int32, device="cuda")
+    wts = torch.zeros((ent,), dtype=torch.float32, device="cuda")
+    ws = m.alloc_workspace(m.prefill_workspace(dl, t))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    m.prefill_group(dl, xt, idx, w, offs, rows, wts, ws, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0, m.STATUS_NAMES.get(status.item())
+    return {k_: v.cpu().numpy() for k_, v in dict(idx=idx, w=w, offs=offs, rows=rows, wts=wts).items()}
+
+
+def moe_rms(ref_out, x, flags):
+    moe_part = ref_out - (x.astype(np.float64) if flags & synth.RESIDUAL else 0.0)
+    return np.sqrt((moe_part ** 2).mean(axis=1))
+
+
+def assert_prefill_close(got, ref, x, flags, rows, what):
+    out, allow = ref["out"], ref["allow"]
+    rms = moe_rms(out, x[rows], flags)
+    base = TOL * rms[:, None] + bf16_ulp(out)
+    bound = base + allow
+    err = np.abs(got - out)
+    bad = err > bound
+    assert not bad.any(), f"{what}: {bad.sum()} elements over the bound, worst row {np.argmax(bad.any(axis=1))}"
+    r = float((err / bound).max())
+    n_base = int((err > base).sum())
+    print(f"[parity] {what}: max err = {r:.4f} of the bound (2e-3 x row RMS + 1 bf16 ulp + flip allowance); "
+          f"{n_base} of {err.size} elements need the allowance; mean allowance {float((allow / rms[:, None]).mean()):.2e} x RMS")
+    return r
+
+
+SMALL = [
+    # H, E, k, I, t, shared, flags
+    (256, 8, 2, 128, 1, False, 0),
+    (256, 8, 2, 128, 37, True, 0),
+    (768, 40, 5, 384, 300, True, synth.RESIDUAL | synth.PRENORM),
+    (512, 130, 4, 192, 129, True, synth.PRENORM),
+    (256, 4, 4, 64, 600, False, synth.RESIDUAL),
+]
+
+
+@pytest.mark.parametrize("H,E,k,I,t,shared,flags", SMALL)
+def test_prefill_small(moe, H, E, k, I, t, shared, flags):
+    """Several token tiles with a ragged tail, expert groups above the 256-token
+    tile, a router tile with padded experts, k == E, t == 1."""
+    rng = np.random.default_rng(1000 + H + E + t)
+    layer = synth.make_layer(rng, H, E, k, I, 4, shared=shared, flags=flags)
+    ol = oracle.Layer(layer)
+    x = rows_with_gap(ol, rng, t, H)
+    dl = moe.DeviceLayers([layer])
+    got, idx = run_prefill(moe, dl, x)
+    ref = oracle.prefill_rows(ol, x, np.arange(t), mirror=True)
+    assert np.array_equal(idx, ref["idx"]), "top-k ids"
+    assert_prefill_close(got, ref, x, flags, np.arange(t), f"prefill H{H} E{E} k{k} I{I} t{t}")
+
+
+@pytest.mark.parametrize("H,E,k,I,t,shared,flags", SMALL)
+def test_prefill_group_small(moe, H, E, k, I, t, shared, flags):
+    rng = np.random.default_rng(2000 + H + E + t)
+    layer = synth.make_layer(rng, H, E, k, I, 4, shared=shared, flags=flags)
+    ol = oracle.Layer(layer)
+    x = rows_with_gap(ol, rng, t, H)
+    g = run_group(moe, moe.DeviceLayers([layer]), x)
+    r = oracle.route_rows(ol, x)
+    assert np.array_equal(g["idx"], r["idx"])
+    # the router reads x^ as two bf16 terms (relative error <= 2^-16), so
+    # weights agree to about 1e-6; 1e-5 as in the decode routing tests
+    assert np.allclose(g["w"], r["w"], rtol=0, atol=1e-5)
+    ref = oracle.group(E, r["idx"], r["w"], r["gamma"])
+    assert np.array_equal(g["offs"], ref["offs"]), "group offsets"
+    assert np.array_equal(g["rows"], ref["rows"]), "grouped rows (stable order)"
+    assert np.allclose(g["wts"], ref["wts"], rtol=0, atol=1e-5), "grouped weights"
+
+
+def test_prefill_rejects_lowbit_records(moe):
+    rng = np.random.default_rng(5)
+    layer = synth.make_layer(rng, 256, 8, 2, 128, 3, shared=False)
+    dl = moe.DeviceLayers([layer])
+    assert moe.prefill_workspace(dl, 16) == 0
+    x = torch.zeros((16, 256), dtype=torch.float32, device="cuda")
+    out = torch.empty((16, 256), dtype=torch.int16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = moe.alloc_workspace(1 << 20)
+    with pytest.raises(moe.MoeError) as e:
+        moe.prefill(dl, x, out, ws, status)
+    assert e.value.code == moe.ESHAPE
+
+
+@pytest.fixture(scope="module")
+def c4():
+    """The 4096-token prefill chunk: hidden 2048, 512 experts, top-10, inter 512,
+    shared expert, Zipf(1.1) expert popularity through the router's bias channel."""
+    rng = np.random.default_rng(4)
+    layer = synth.make_config_layers("c4", seed=4)[0]
+    synth.zipf_router(rng, layer)
+    x = synth.make_prefill_x(rng, 4096, layer.hidden)
+    return layer, oracle.Layer(layer), x
+
+
+def test_prefill_c4_full_size(moe, c4):
+    layer, ol, x = c4
+    t, k, E = x.shape[0], layer.top_k, layer.n_experts
+    dl = moe.DeviceLayers([layer])
+    got, idx = run_prefill(moe, dl, x)
+    r = oracle.route_rows(ol, x)
+    gaps = gaps_of(r["logits"], k)
+    clear = gaps >= GAP
+    # rows with a clear top-k: exact ids; near ties: the first k-1 ids agree and
+    # the k-th is an expert whose logit is within GAP of the oracle's k-th
+    assert np.array_equal(idx[clear], r["idx"][clear])
+    for b in np.nonzero(~clear)[0]:
+        assert sorted(idx[b][:k - 1]) == sorted(r["idx"][b][:k - 1])
+        kth = np.sort(r["logits"][b].astype(np.float32))[::-1][k - 1]
+        assert abs(float(r["logits"][b][idx[b][k - 1]]) - float(kth)) < GAP
+    same = np.array([sorted(idx[b]) == sorted(r["idx"][b]) for b in range(t)])
+    counts = np.bincount(r["idx"].ravel(), minlength=E)
+    print(f"[c4] rows with a top-k gap < {GAP}: {int((~clear).sum())}; id sets differing: {int((~same).sum())}; "
+          f"expert rows max {counts.max()} min {counts.min()} empty {(counts == 0).sum()}")
+    # outputs on sampled rows (first, last, rows routed to the rarest used experts, random)
+    srng = np.random.default_rng(44)
+    rare = [int(np.nonzero((r["idx"] == e).any(axis=1))[0][0]) for e in np.argsort(counts) if counts[e] > 0][:8]
+    sample = sorted(set([0, t - 1] + rare + srng.choice(t, 38, replace=False).tolist()))
+    sample = [b for b in sample if same[b]]
+    ref = oracle.prefill_rows(ol, x, np.array(sample), mirror=True)
+    assert_prefill_close(got[sample], ref, x, layer.flags, np.array(sample), f"c4 t=4096 ({len(sample)} rows)")
+
+
+def test_prefill_c4_group(moe, c4):
+    """Full-size grouping: exactly the oracle's grouping of the GPU's own ids."""
+    layer, ol, x = c4
+    g = run_group(moe, moe.DeviceLayers([layer]), x)
+    r = oracle.route_rows(ol, x)
+    ref = oracle.group(layer.n_experts, g["idx"], g["w"].astype(np.float64), r["gamma"])
+    assert np.array_equal(g["offs"], ref["offs"])
+    assert np.array_equal(g["rows"], ref["rows"])
+    assert np.allclose(g["wts"][:-x.shape[0]], ref["wts"][:-x.shape[0]], rtol=0, atol=0), "routed weights placed"
+    assert np.allclose(g["wts"][-x.shape[0]:], r["gamma"], rtol=0, atol=1e-6), "shared gate"
