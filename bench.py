@@ -8,7 +8,10 @@ Metric: MoE-layer rows per second = nb * layers / step time; the HBM roofline
 fraction of the kernel is reported beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c1|c2|c3b3|c3b2] [--nb NB]
+                  [--workload c1|c2|c3b3|c3b2|c4] [--nb NB]
+
+--workload c4 times the prefill chunk instead (moe_prefill, 9 kernels per
+step; the roofline is the tensor-pipe one of its largest GEMM).
 
 Under torchrun each rank runs an independent replica on its own GPU (the path
 has no exchange step); value = rows of all ranks / max time over ranks.
@@ -34,16 +37,18 @@ WORKLOADS = {
     "c2": "one MoE layer, verify batch nb=4: hidden 2048, 512 experts, top-10, inter 512, shared expert, 4-bit g64",
     "c3b3": "one MoE layer, nb=4: hidden 2048, 512 experts, top-10, inter 512, 3-bit routed records",
     "c3b2": "one MoE layer, nb=4: hidden 2048, 512 experts, top-10, inter 512, 2-bit routed records",
+    "c4": "prefill chunk of 4096 rows through one MoE layer: hidden 2048, 512 experts, top-10, inter 512, "
+          "shared expert, 4-bit g64 records, Zipf(1.1) expert popularity; bf16 tensor-core GEMMs, bf16 out",
 }
 METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 1 GB300"
 
 
-def load_peaks():
+def load_peaks(kind="hbm"):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return float(d["hbm_gbs" if kind == "hbm" else "bf16_tflops"]), "measured"
+    return (6800.0 if kind == "hbm" else 1900.0), "fallback"
 
 
 class ClockSampler:
@@ -204,6 +209,127 @@ def run_ours(args, rank, world, device):
                 peak=peak, peak_kind=peak_kind, clocks=clocks, unions=unions)
 
 
+def run_prefill(args, rank, world, device):
+    """One step = one moe_prefill call over the 4096-row chunk (9 kernels)."""
+    import torch
+    from quantized_routed_expert_fn_gb300 import build, moe, synth
+
+    build.build()
+    moe.lib()
+    torch.cuda.set_device(device)
+    cfg = synth.CONFIGS["c4"]
+    t = args.nb or cfg["nb"]
+    H, E, k, I = cfg["hidden"], cfg["n_experts"], cfg["top_k"], cfg["inter"]
+    layers = synth.make_device_layers("c4", seed=1 + rank, device=device)
+    rng = np.random.default_rng(40 + rank)
+    layers[0].router = torch.from_numpy(synth.zipf_router_bits(rng, E, H).view(np.int16)).to(device)
+    dl = moe.DeviceLayers(layers, device=device)
+    x_host = torch.from_numpy(synth.make_prefill_x(rng, t, H))
+    x = x_host.to(device)
+    out = torch.empty((t, H), dtype=torch.int16, device=device)
+    idx = torch.zeros((t, k), dtype=torch.int32, device=device)
+    ws = moe.alloc_workspace(moe.prefill_workspace(dl, t), device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    nk = moe.PREFILL_KERNELS
+
+    def new_events():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+        for e in evs:
+            e.record(stream)  # creates the event
+        return evs
+
+    for _ in range(max(args.warmup, 3)):
+        moe.prefill(dl, x, out, ws, status, idx, stream=stream)
+    torch.cuda.synchronize()
+    if status.item() != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
+    ids = idx.cpu().numpy()
+    counts = np.bincount(ids.ravel(), minlength=E)
+    used = int((counts > 0).sum())
+    ent = t * k + t  # routed entries + the shared expert over every row
+    flops = {"router_gemm": 2.0 * E * t * 2 * H, "gate_up_gemm": 2.0 * ent * 2 * I * H,
+             "down_gemm": 2.0 * ent * H * I}
+    from quantized_routed_expert_fn_gb300.synth import record_layout
+    rec = record_bytes(record_layout(H, I, 4))
+    bytes_per_step = (used + 1) * rec + E * H * 2 + H * 2 + t * H * 4 + t * H * 2
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as td
+    sets = [new_events() for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        td.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for i in range(args.steps):
+        moe.prefill_timed(dl, x, out, ws, status, sets[i], idx, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        td.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    clocks = sampler.stop() if sampler else None
+    if status.item() != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
+    kernel_ms = {name: sum(s[j].elapsed_time(s[j + 1]) for s in sets) / args.steps
+                 for j, name in enumerate(moe.PREFILL_KERNEL_NAMES)}
+
+    x_pin = x_host.pin_memory()
+    o_pin = torch.empty((t, H), dtype=torch.int16).pin_memory()
+
+    def e2e_step():
+        x.copy_(x_pin, non_blocking=True)
+        moe.prefill(dl, x, out, ws, status, idx, stream=stream)
+        o_pin.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        td.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if dist:
+        tt = torch.tensor([ms, e2e_ms], device=device)
+        td.all_reduce(tt, op=td.ReduceOp.MAX)
+        ms, e2e_ms = float(tt[0]), float(tt[1])
+    top = max(flops, key=lambda n: kernel_ms[n])
+    peak, peak_kind = load_peaks("tensor")
+    achieved = flops[top] / (kernel_ms[top] * 1e-3) / 1e12
+    return dict(ms=ms, e2e_ms=e2e_ms, rows=t * world, t=t, kernel_ms=kernel_ms, top=top, flops=flops,
+                achieved=achieved, peak=peak, peak_kind=peak_kind, clocks=clocks, bytes=bytes_per_step,
+                used_experts=used, max_rows=int(counts.max()))
+
+
+def oracle_prefill_sample(t, budget_s):
+    """Time the oracle's prefill rows (bf16 mirror, as the parity tests use it)
+    on host cores over the first rows of the same chunk, drawn on the host."""
+    import oracle
+    from quantized_routed_expert_fn_gb300 import synth
+    rng = np.random.default_rng(40)
+    layer = synth.make_config_layers("c4", seed=1000, n_layers=1)[0]
+    synth.zipf_router(rng, layer)
+    x = synth.make_prefill_x(rng, t, layer.hidden)
+    ol = oracle.Layer(layer)
+    cores = oracle.threads()
+    done, secs, chunk = 0, 0.0, max(cores, 1)
+    while secs < budget_s and done < t:
+        rows = np.arange(done, min(t, done + chunk))
+        t0 = time.perf_counter()
+        oracle.prefill_rows(ol, x, rows, mirror=True)
+        secs += time.perf_counter() - t0
+        done += len(rows)
+    return dict(value=done / secs, rows=done, seconds=secs, cores=cores)
+
+
 def oracle_sample(name, nb, budget_s):
     """Time the oracle (as it stands) on host cores on the first layers of the
     same workload, drawn on the host with the same distributions."""
@@ -248,6 +374,22 @@ def main():
     config = {"workload": WORKLOADS[args.workload], "nb": nb, "layers": args.layers or cfg["n_layers"],
               "l2": "inputs larger than L2 (each step streams every layer's union records once)"}
 
+    if args.workload == "c4":
+        config = {"workload": WORKLOADS["c4"], "t": nb, "layers": 1,
+                  "l2": "inputs larger than L2 (about 0.9 GB of expert records per step)"}
+    if args.impl == "reference" and args.workload == "c4":
+        if rank != 0:
+            return
+        s = oracle_prefill_sample(nb, budget_s=min(args.cpu_budget, 20.0))
+        line = {"metric": METRIC, "value": s["value"], "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": 1000.0 * nb / s["value"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+                "impl": "reference",
+                "cpu_baseline": {"value": s["value"], "unit": "rows/s", "cores": s["cores"], "kind": "oracle",
+                                 "sample": f"first {s['rows']} rows of the chunk, {s['seconds']:.1f} s"},
+                "e2e": {"value": s["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
     if args.impl == "reference":
         if rank != 0:
             return
@@ -267,6 +409,35 @@ def main():
         import torch.distributed as td
         td.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
     device = torch.device(f"cuda:{local}")
+    if args.workload == "c4":
+        r = run_prefill(args, rank, world, device)
+        if rank == 0:
+            cpu = oracle_prefill_sample(nb, budget_s=args.cpu_budget)
+            H = synth.CONFIGS["c4"]["hidden"]
+            line = {
+                "metric": METRIC, "value": r["rows"] / (r["ms"] * 1e-3), "unit": "rows/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
+                "e2e": {"value": r["rows"] / (r["e2e_ms"] * 1e-3), "unit": "rows/s",
+                        "h2d_bytes_per_step": nb * H * 4, "d2h_bytes_per_step": nb * H * 2},
+                "gpu_launches": args.steps * 9,
+                "roofline": {"bound": "tensor", "achieved": r["achieved"], "peak": r["peak"], "unit": "TFLOP/s",
+                             "frac": r["achieved"] / r["peak"], "traffic": None, "kernel": r["top"],
+                             "peak_source": r["peak_kind"] + " bf16 burst",
+                             "algorithmic_flops_per_launch": r["flops"][r["top"]]},
+                "kernel_ms": r["kernel_ms"],
+                "gemm_tflops": {n: r["flops"][n] / (r["kernel_ms"][n] * 1e-3) / 1e12 for n in r["flops"]},
+                "step_hbm_gbs": r["bytes"] / (r["ms"] * 1e-3) / 1e9,
+                "used_experts": r["used_experts"], "max_expert_rows": r["max_rows"],
+                "cpu_baseline": {"value": cpu["value"], "unit": "rows/s", "cores": cpu["cores"], "kind": "oracle",
+                                 "sample": f"first {cpu['rows']} rows of the chunk (bf16 mirror), "
+                                           f"{cpu['seconds']:.1f} s"},
+                "clocks": r["clocks"],
+            }
+            print(json.dumps(line))
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
     r = run_ours(args, rank, world, device)
     if rank != 0:
         if world > 1:

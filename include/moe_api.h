@@ -193,6 +193,19 @@ int moe_forward_noalloc(const moe_layer *layers, int n_layers, const float *x, i
 int moe_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *work, size_t work_bytes,
                 uint32_t *topk_idx, int *dev_status, moe_stream_t stream);
 
+/* moe_prefill plus device timing of its kernels (the `PhaseTimer` /
+ * `GpuTiming` GPU timestamps of the struct Gpu page, here CUDA events):
+ *   events  host array of MOE_PREFILL_KERNELS + 1 caller-created cudaEvent_t
+ *           (as void *); events[i] is recorded on the stream before kernel i
+ *           and events[MOE_PREFILL_KERNELS] after the last.  Kernels, in
+ *           order: 0 prep (x^, bf16 operands, shared gate), 1 router GEMM,
+ *           2 top-k, 3 grouping scan, 4 grouping fill, 5 expert operand
+ *           rows in group order, 6 gate_up GEMM, 7 down GEMM, 8 bf16 output.
+ * Results equal moe_prefill's. */
+#define MOE_PREFILL_KERNELS 9
+int moe_prefill_timed(const moe_layer *L, const float *x, int t, uint16_t *out, void *work, size_t work_bytes,
+                      uint32_t *topk_idx, int *dev_status, void *const *events, moe_stream_t stream);
+
 /* Workspace bytes moe_prefill and moe_prefill_group need for t rows (0 if the
  * arguments are invalid). */
 size_t moe_prefill_workspace(const moe_layer *L, int t);

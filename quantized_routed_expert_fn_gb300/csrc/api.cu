@@ -16,6 +16,8 @@
 #include "moe_api.h"
 #include "prefill.cuh"
 
+static_assert(MOE_PREFILL_KERNELS == moe::kPfStages, "prefill kernel count");
+
 namespace {
 
 thread_local std::string g_err;
@@ -251,7 +253,8 @@ size_t prefill_bytes(const moe_layer *L, int t) {
 }
 
 int run_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *work, size_t work_bytes,
-                uint32_t *topk_idx, float *topk_w, int *status, moe_stream_t stream, int route_only) {
+                uint32_t *topk_idx, float *topk_w, int *status, moe_stream_t stream, int route_only,
+                void *const *events = nullptr) {
   const int H = (int)L->hidden;
   if (!x) return fail(MOE_EINVAL, "x is NULL");
   if (!route_only && !out) return fail(MOE_EINVAL, "out is NULL");
@@ -280,7 +283,13 @@ int run_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *
   p.status = status;
   p.timeout_ns = timeout_ns();
   moe::pf_carve(p, work);
-  const cudaError_t e = moe::pf_launch(p, (cudaStream_t)stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&p.n_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return fail(MOE_ECUDA, "device query failed");
+  const char *why = "";
+  if (moe::pf_tensor_maps(p, &why) != 0) return fail(MOE_ECUDA, "%s", why);
+  const cudaError_t e = moe::pf_launch(p, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t const *>(events));
   if (e != cudaSuccess) return fail(MOE_ECUDA, "prefill launch failed: %s", cudaGetErrorString(e));
   return MOE_OK;
 }
@@ -357,6 +366,16 @@ int moe_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *
   const int r = check_prefill(L, t);
   if (r != MOE_OK) return r;
   return run_prefill(L, x, t, out, work, work_bytes, topk_idx, nullptr, dev_status, stream, 0);
+}
+
+int moe_prefill_timed(const moe_layer *L, const float *x, int t, uint16_t *out, void *work, size_t work_bytes,
+                      uint32_t *topk_idx, int *dev_status, void *const *events, moe_stream_t stream) {
+  const int r = check_prefill(L, t);
+  if (r != MOE_OK) return r;
+  if (!events) return fail(MOE_EINVAL, "events is NULL");
+  for (int i = 0; i <= MOE_PREFILL_KERNELS; i++)
+    if (!events[i]) return fail(MOE_EINVAL, "events[%d] is NULL", i);
+  return run_prefill(L, x, t, out, work, work_bytes, topk_idx, nullptr, dev_status, stream, 0, events);
 }
 
 int moe_prefill_group(const moe_layer *L, const float *x, int t, uint32_t *topk_idx, float *topk_w,

@@ -24,7 +24,10 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_EALIGN
                 -5: "MOE_ETIMEOUT", -6: "MOE_EDEVICE", -7: "MOE_ENOSPACE"}
 
 EXPORTS = ["moe_route", "moe_forward", "moe_forward_traced", "moe_forward_noalloc", "moe_forward_workspace",
-           "moe_prefill", "moe_prefill_workspace", "moe_prefill_group", "moe_last_error"]
+           "moe_prefill", "moe_prefill_timed", "moe_prefill_workspace", "moe_prefill_group", "moe_last_error"]
+PREFILL_KERNELS = 9
+PREFILL_KERNEL_NAMES = ["prep", "router_gemm", "topk", "group_scan", "group_fill", "gather", "gate_up_gemm",
+                        "down_gemm", "output"]
 NOALLOC_MAX_WORKSPACE = 4 << 20
 TRACE_CTAS, TRACE_PHASES = 1024, 16
 
@@ -77,6 +80,8 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.moe_prefill_workspace.argtypes = [ctypes.POINTER(MoeLayer), i32]
         L.moe_prefill.restype = i32
         L.moe_prefill.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, sz, vp, vp, vp]
+        L.moe_prefill_timed.restype = i32
+        L.moe_prefill_timed.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, sz, vp, vp, vp, vp]
         L.moe_prefill_group.restype = i32
         L.moe_prefill_group.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
         _lib = L
@@ -218,3 +223,14 @@ def prefill_group(layers: DeviceLayers, x: torch.Tensor, topk_idx, topk_w, group
     _check(lib().moe_prefill_group(_layer_ptr(layers, layer), _p(x), x.shape[0], _p(topk_idx), _p(topk_w),
                                    _p(group_offs), _p(group_rows), _p(group_w), wp, wb, _p(status),
                                    _stream(stream)))
+
+
+def prefill_timed(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, work: torch.Tensor,
+                  status: torch.Tensor, events, topk_idx=None, layer: int = 0, stream=None) -> None:
+    """moe_prefill recording events[i] (torch.cuda.Event, already recorded once so
+    that it exists) before kernel i and events[PREFILL_KERNELS] after the last."""
+    assert len(events) == PREFILL_KERNELS + 1
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    wp, wb = _aligned(work)
+    _check(lib().moe_prefill_timed(_layer_ptr(layers, layer), _p(x), x.shape[0], _p(out), wp, wb, _p(topk_idx),
+                                   _p(status), arr, _stream(stream)))

@@ -228,15 +228,18 @@ def make_config_layers(name: str, seed: int = 0, n_layers: int | None = None, **
     return layers
 
 
-def zipf_router(rng, layer: Layer, s: float = 1.1, noise_std: float = 0.028) -> None:
+def zipf_router_bits(rng, n_experts: int, hidden: int, s: float = 1.1, noise_std: float = 0.028) -> np.ndarray:
     """Prefill popularity: channel 0 of x is held at 1 and router column 0 carries
     `-s*ln(rank)` for a seeded permutation of expert ranks, the rest N(0, noise_std);
-    top-k then draws experts roughly as Zipf(s) without replacement."""
-    E, H = layer.n_experts, layer.hidden
-    rank = rng.permutation(E) + 1
-    r = rng.normal(0.0, noise_std, size=(E, H)).astype(np.float32)
+    top-k then draws experts roughly as Zipf(s) without replacement.  bf16 bits [E][H]."""
+    rank = rng.permutation(n_experts) + 1
+    r = rng.normal(0.0, noise_std, size=(n_experts, hidden)).astype(np.float32)
     r[:, 0] = (-s * np.log(rank)).astype(np.float32)
-    layer.router = f32_to_bf16_bits(r)
+    return f32_to_bf16_bits(r)
+
+
+def zipf_router(rng, layer: Layer, s: float = 1.1, noise_std: float = 0.028) -> None:
+    layer.router = zipf_router_bits(rng, layer.n_experts, layer.hidden, s, noise_std)
 
 
 def make_prefill_x(rng, t: int, hidden: int) -> np.ndarray:
