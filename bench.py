@@ -10,7 +10,7 @@ fraction of the kernel is reported beside it.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload c1|c2|c3b3|c3b2|c4] [--nb NB]
 
---workload c4 times the prefill chunk instead (moe_prefill, 9 kernels per
+--workload c4 times the prefill chunk instead (moe_prefill, 10 kernels per
 step; the roofline is the tensor-pipe one of its largest GEMM).
 
 Under torchrun each rank runs an independent replica on its own GPU (the path
@@ -210,7 +210,7 @@ def run_ours(args, rank, world, device):
 
 
 def run_prefill(args, rank, world, device):
-    """One step = one moe_prefill call over the 4096-row chunk (9 kernels)."""
+    """One step = one moe_prefill call over the 4096-row chunk (10 kernels)."""
     import torch
     from quantized_routed_expert_fn_gb300 import build, moe, synth
 
@@ -420,7 +420,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
                 "e2e": {"value": r["rows"] / (r["e2e_ms"] * 1e-3), "unit": "rows/s",
                         "h2d_bytes_per_step": nb * H * 4, "d2h_bytes_per_step": nb * H * 2},
-                "gpu_launches": args.steps * 9,
+                "gpu_launches": args.steps * 10,
                 "roofline": {"bound": "tensor", "achieved": r["achieved"], "peak": r["peak"], "unit": "TFLOP/s",
                              "frac": r["achieved"] / r["peak"], "traffic": None, "kernel": r["top"],
                              "peak_source": r["peak_kind"] + " bf16 burst",

@@ -199,10 +199,11 @@ int moe_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *
  *           (as void *); events[i] is recorded on the stream before kernel i
  *           and events[MOE_PREFILL_KERNELS] after the last.  Kernels, in
  *           order: 0 prep (x^, bf16 operands, shared gate), 1 router GEMM,
- *           2 top-k, 3 grouping scan, 4 grouping fill, 5 expert operand
- *           rows in group order, 6 gate_up GEMM, 7 down GEMM, 8 bf16 output.
+ *           2 top-k, 3 per-expert counts, 4 group offsets and work lists,
+ *           5 grouped row lists, 6 expert operand rows in group order,
+ *           7 gate_up GEMM, 8 down GEMM, 9 bf16 output.
  * Results equal moe_prefill's. */
-#define MOE_PREFILL_KERNELS 9
+#define MOE_PREFILL_KERNELS 10
 int moe_prefill_timed(const moe_layer *L, const float *x, int t, uint16_t *out, void *work, size_t work_bytes,
                       uint32_t *topk_idx, int *dev_status, void *const *events, moe_stream_t stream);
 

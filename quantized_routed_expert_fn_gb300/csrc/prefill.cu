@@ -65,16 +65,20 @@ __device__ bool pf_wait(uint64_t *bar, uint32_t par, const PfParams &P) {
 }
 
 // ------------------------------------------------------------ prep
-// Block per token: x^, router operands (hi/lo, natural order), expert operand
-// (bf16 of x^, permuted), shared gate sigmoid(sg . x^).
+// Block per token, thread per 8-element block: x^, the router operands
+// (hi/lo, natural order), the expert operand (bf16 of x^, k permuted within
+// the block), the shared gate sigmoid(sg . x^).  16-byte loads and stores.
 __global__ void pf_prep(const __grid_constant__ PfParams P) {
   __shared__ float red[32];
-  const int tok = blockIdx.x, H = P.H, nw = blockDim.x >> 5;
-  const float *xr = P.x + (size_t)tok * H;
+  const int tok = blockIdx.x, H = P.H, nw = blockDim.x >> 5, nb8 = H / 8;
+  const float4 *xr = reinterpret_cast<const float4 *>(P.x + (size_t)tok * H);
   float scale = 1.f;
   if (P.flags & kPrenormF) {
     float ss = 0.f;
-    for (int i = threadIdx.x; i < H; i += blockDim.x) ss += xr[i] * xr[i];
+    for (int b = threadIdx.x; b < nb8; b += blockDim.x) {
+      const float4 a = xr[2 * b], c = xr[2 * b + 1];
+      ss += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + c.x * c.x + c.y * c.y + c.z * c.z + c.w * c.w;
+    }
     ss = warp_sum_f(ss);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
     __syncthreads();
@@ -84,14 +88,31 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
     __syncthreads();
   }
   float gdot = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    const float v = xr[i] * scale;
-    const uint32_t hi = f2bf_rn(v);
-    const uint32_t lo = f2bf_rn(v - __uint_as_float(hi << 16));
-    P.xr_hi[(size_t)tok * H + i] = (uint16_t)hi;
-    P.xr_lo[(size_t)tok * H + i] = (uint16_t)lo;
-    P.xg[(size_t)tok * H + (i & ~7) + perm8(i & 7)] = (uint16_t)hi;
-    if (P.sgate) gdot += __uint_as_float((uint32_t)P.sgate[i] << 16) * v;
+  const size_t rb = (size_t)tok * H;
+  for (int b = threadIdx.x; b < nb8; b += blockDim.x) {
+    const float4 a = xr[2 * b], c = xr[2 * b + 1];
+    const float v[8] = {a.x * scale, a.y * scale, a.z * scale, a.w * scale,
+                        c.x * scale, c.y * scale, c.z * scale, c.w * scale};
+    uint32_t hi[8], lo[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      hi[j] = f2bf_rn(v[j]);
+      lo[j] = f2bf_rn(v[j] - __uint_as_float(hi[j] << 16));
+    }
+    *reinterpret_cast<uint4 *>(P.xr_hi + rb + 8 * b) =
+        make_uint4(hi[0] | hi[1] << 16, hi[2] | hi[3] << 16, hi[4] | hi[5] << 16, hi[6] | hi[7] << 16);
+    *reinterpret_cast<uint4 *>(P.xr_lo + rb + 8 * b) =
+        make_uint4(lo[0] | lo[1] << 16, lo[2] | lo[3] << 16, lo[4] | lo[5] << 16, lo[6] | lo[7] << 16);
+    // positions 0..7 of the permuted block hold natural indices 0,4,1,5,2,6,3,7
+    *reinterpret_cast<uint4 *>(P.xg + rb + 8 * b) =
+        make_uint4(hi[0] | hi[4] << 16, hi[1] | hi[5] << 16, hi[2] | hi[6] << 16, hi[3] | hi[7] << 16);
+    if (P.sgate) {
+      const uint4 g = *reinterpret_cast<const uint4 *>(P.sgate + 8 * b);
+      const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int j = 0; j < 4; j++)
+        gdot += __uint_as_float(gw[j] << 16) * v[2 * j] + __uint_as_float(gw[j] & 0xffff0000u) * v[2 * j + 1];
+    }
   }
   if (P.sgate) {
     gdot = warp_sum_f(gdot);
@@ -124,7 +145,7 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 // Every mbarrier wait is bounded; a wait that gives up records
 // MOE_ETIMEOUT in *status and its role stops, so the CTA ends.
 
-constexpr int kWsThreads = 320;
+constexpr int kWsThreads = 448;
 constexpr int kS = 3;                      // A / B pipeline stages
 constexpr int kChunk = 4;                  // k-stages per staged chunk of codes
 constexpr int kStgCodes = 128 * 128;       // 128 rows x 128 bytes of codes (4 stages)
@@ -188,38 +209,44 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t par, const PfP
   return __shfl_sync(FULLM, ok ? 1 : 0, 0) != 0;
 }
 
-// Weight row `r` of a tile: gate_up tiles hold 64 gate rows then the 64
-// matching up rows; down tiles 128 output rows.
+// Weight row of tile row r.  A gate_up tile covers 64 intermediate indices
+// mt*64 .. mt*64+63: each 32-row quadrant q holds the gate rows of indices
+// 16q .. 16q+15 followed by their up rows, so that the epilogue finds gate i
+// and up i in lanes l and l + 16 of one warp.  A down tile: 128 output rows.
+// (Row parity = parity of r in both layouts.)
 template <int MODE>
 __device__ __forceinline__ int ws_weight_row(const PfParams &P, int mt, int r) {
   if constexpr (MODE == MODE_GATE_UP)
-    return r < 64 ? mt * 64 + r : P.I + mt * 64 + (r - 64);
+    return ((r & 16) ? P.I : 0) + mt * 64 + 16 * (r >> 5) + (r & 15);
   else
     return mt * 128 + r;
 }
 
 // Stage one chunk of codes (k-stages 4kc .. 4kc+3 of a tile) into shared
-// memory: 128 rows x 128 bytes, copied by 8 threads per row segment so that
-// each warp instruction reads four whole 128-byte lines (16-byte pieces
-// placed at piece ^ (row & 7) against bank conflicts); plus, per row and
-// stage, the 4-byte words holding its scale and bias.  A segment may run
-// past the end of a row, into bytes of the same record (codes are followed
-// by the scale and bias tables); those bytes are never used.
+// memory, by the 256 producer threads (t): 128 rows x 128 bytes, copied by 8
+// threads per row segment so that each warp instruction reads four whole
+// 128-byte lines (16-byte pieces placed at piece ^ (row & 7) against bank
+// conflicts); plus, per row and stage, the 4-byte words holding its scale
+// and bias.  A segment may run past the end of a row, into bytes of the same
+// record (codes are followed by the scale and bias tables); those bytes are
+// never used.
 template <int MODE>
-__device__ __forceinline__ void stage_chunk(const PfParams &P, const PfItem &it, int kc, int nk, int r, uint8_t *buf) {
+__device__ __forceinline__ void stage_chunk(const PfParams &P, const PfItem &it, int kc, int nk, int t, uint8_t *buf) {
   if (item_ok<MODE>(it)) {
     const uint8_t *rec = reinterpret_cast<const uint8_t *>(it.rec);
     const QOff q = it.g == P.E ? (MODE == MODE_GATE_UP ? P.sgu : P.sdn) : (MODE == MODE_GATE_UP ? P.gu : P.dn);
     const int inp = MODE == MODE_GATE_UP ? P.H : P.I;
 #pragma unroll
-    for (int i = 0; i < 8; i++) {
-      const int idx = i * 128 + r, row = idx >> 3, part = idx & 7;
+    for (int i = 0; i < 4; i++) {
+      const int idx = i * 256 + t, row = idx >> 3, part = idx & 7;
       const size_t src = q.w + (size_t)ws_weight_row<MODE>(P, it.mt, row) * (inp / 2) + kc * 128 + part * 16;
       tc05::cp16(buf + row * 128 + ((part ^ (row & 7)) << 4), rec + src);
     }
+    const int r = t & 127;
     const size_t gbase = (size_t)ws_weight_row<MODE>(P, it.mt, r) * (inp / 64);
 #pragma unroll
-    for (int u = 0; u < kChunk; u++) {
+    for (int v = 0; v < 2; v++) {
+      const int u = 2 * (t >> 7) + v;
       const int kk = min(kc * kChunk + u, nk - 1);
       const size_t gi = (gbase + kk) * 2;
       tc05::cp4(buf + kStgCodes + (r * kChunk + u) * 8, rec + ((q.s + gi) & ~(size_t)3));
@@ -229,18 +256,18 @@ __device__ __forceinline__ void stage_chunk(const PfParams &P, const PfItem &it,
   tc05::cp_commit();
 }
 
-// 64 codes of row r, stage u of a staged chunk -> bf16(scale * code + bias),
-// k permuted within 8-blocks, into row r of a swizzled A stage
-__device__ __forceinline__ void ws_dequant_row(const uint8_t *buf, int r, int u, uint32_t half, uint8_t *sA) {
-  const uint8_t *row = buf + r * 128;
-  const uint4 c0 = *reinterpret_cast<const uint4 *>(row + (((2 * u) ^ (r & 7)) << 4));
-  const uint4 c1 = *reinterpret_cast<const uint4 *>(row + (((2 * u + 1) ^ (r & 7)) << 4));
+// Half hf (codes 32hf .. 32hf+31) of row r's 64 codes of stage u of a
+// staged chunk -> bf16(scale * code + bias), k permuted within 8-blocks,
+// into chunks 4hf .. 4hf+3 of row r of a swizzled A stage
+__device__ __forceinline__ void ws_dequant_half(const uint8_t *buf, int r, int hf, int u, uint32_t half,
+                                                uint8_t *sA) {
+  const uint4 c = *reinterpret_cast<const uint4 *>(buf + r * 128 + (((2 * u + hf) ^ (r & 7)) << 4));
   const uint2 sbw = *reinterpret_cast<const uint2 *>(buf + kStgCodes + (r * kChunk + u) * 8);
   const uint32_t s = (sbw.x >> (16 * half)) & 0xffffu, b = (sbw.y >> (16 * half)) & 0xffffu;
   const uint32_t s2 = s * 0x10001u, b2 = b * 0x10001u;
-  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-  for (int ch = 0; ch < 8; ch++) {
+  for (int ch = 0; ch < 4; ch++) {
     uint32_t pr[4];
 #pragma unroll
     for (int j = 0; j < 4; j++) {
@@ -248,7 +275,7 @@ __device__ __forceinline__ void ws_dequant_row(const uint8_t *buf, int r, int u,
       const uint32_t qv = bfma2(v, 0x3f803f80u, 0xc300c300u);              // the codes, exact
       pr[j] = bfma2(qv, s2, b2);                                            // bf16(s*q + b)
     }
-    *reinterpret_cast<uint4 *>(sA + tc05::sw128_offset(r, ch)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+    *reinterpret_cast<uint4 *>(sA + tc05::sw128_offset(r, 4 * hf + ch)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
   }
 }
 
@@ -266,7 +293,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
   if (tid == 0) {
     for (int s = 0; s < kS; s++) {
       mbar_init(&B.full_b[s], 1);
-      mbar_init(&B.full_a[s], 4);
+      mbar_init(&B.full_a[s], 8);
       mbar_init(&B.empty[s], 1);
     }
     for (int b = 0; b < 2; b++) {
@@ -365,10 +392,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
     // copies still in flight land before the CTA ends
     if (lane == 0 && f > 0) pf_wait(&B.full_b[(f - 1) % kS], (uint32_t)(((f - 1) / kS) & 1), P);
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ---------------------------------------------------------------- A producers
     if constexpr (MODE != MODE_ROUTER) {
-      const int r = tid - 64;
+      const int t = tid - 64, r = t & 127, hf = t >> 7;  // row; half of its 64 codes
       const int nct = (nk + kChunk - 1) / kChunk;  // chunks per tile
       const int total = my_tiles * nct;
       const int inp = MODE == MODE_GATE_UP ? P.H : P.I;
@@ -389,7 +416,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
           slt = lt;
           if (lt + 1 < my_tiles) snext = ws_item<MODE>(P, tile_of(lt + 1));
         }
-        stage_chunk<MODE>(P, scur, c - lt * nct, nk, r, stg + (c % kNStg) * kStgBuf);
+        stage_chunk<MODE>(P, scur, c - lt * nct, nk, t, stg + (c % kNStg) * kStgBuf);
       };
       issue(0);
       issue(1);
@@ -398,7 +425,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       bool ok = true;
       for (int c = 0; c < total && ok; c++) {
         tc05::cp_wait_group<1>();  // this thread's copies of chunk c are done
-        tc05::named_sync(3, 128);  // everyone's are; everyone is done reading chunk c - 1
+        tc05::named_sync(3, 256);  // everyone's are; everyone is done reading chunk c - 1
         issue(c + 2);
         const int lt = c / nct, kc = c - lt * nct;
         const uint8_t *buf = stg + (c % kNStg) * kStgBuf;
@@ -411,23 +438,24 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
           }
           // scale / bias: the half of the staged 4-byte word holding entry row * G + kk
           const uint32_t half = (rodd + (uint32_t)kk) & 1u;
-          ws_dequant_row(buf, r, u, half, sm + s * kStageA);
+          ws_dequant_half(buf, r, hf, u, half, sm + s * kStageA);
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) tc05::mbar_arrive(&B.full_a[s]);
         }
-        // the four producer warps stop together (they share a named barrier)
-        ok = tc05::named_and(4, 128, ok);
+        // the eight producer warps stop together (they share a named barrier)
+        ok = tc05::named_and(4, 256, ok);
       }
       tc05::cp_wait_group<0>();  // nothing in flight into shared memory at the end
     }
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;    // TMEM lane quadrant this warp may read
-    const int et = tid - 192;  // 0..127 over the epilogue warps
+    const int et = tid - 320;  // 0..127 over the epilogue warps
     int *trow = reinterpret_cast<int *>(sm + kOffTile);
     float *twt = reinterpret_cast<float *>(sm + kOffTile) + kPfTileN;
     PfItem nx{};
+    unsigned hcnt = 0;  // gate_up: h chunks written so far (their buffers alternate)
     int pr[2] = {0, 0};
     float pw[2] = {0.f, 0.f};
     auto fetch_entries = [&](const PfItem &it) {  // down: this thread's two entries of a tile
@@ -470,7 +498,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
           } else if constexpr (MODE == MODE_DOWN) {
             // transpose the warp's 32 rows x 32 tokens through shared memory,
             // then one 16-byte reduction per (token, 4 rows)
-            float *tb = reinterpret_cast<float *>(sm + kOffEpi) + (warp - 6) * 1024;
+            float *tb = reinterpret_cast<float *>(sm + kOffEpi) + (warp - 10) * 1024;
 #pragma unroll
             for (int j = 0; j < 32; j++) tb[j * 32 + lane] = v[j];
             __syncwarp();
@@ -487,26 +515,22 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
             }
             __syncwarp();
           } else {
-            // up rows (quadrants 2, 3) -> shared; h = silu(gate) * up on quadrants 0, 1
-            float *xch = reinterpret_cast<float *>(sm + kOffEpi);
-            uint16_t *hs = reinterpret_cast<uint16_t *>(xch + 64 * 33);  // [32 tokens][64] bf16, permuted k
-            tc05::named_sync(1, 128);
-            if (q >= 2)
+            // lanes l < 16 hold gate, lanes l + 16 up, of index i = 16q + (l & 15):
+            // the gate lane takes columns 0..15, the up lane 16..31, each
+            // fetching the partner's value with one exchange per column
+            const int up = lane >> 4, i = 16 * q + (lane & 15);
+            uint16_t *hs = reinterpret_cast<uint16_t *>(sm + kOffEpi) + (hcnt++ & 1) * (32 * 64);
 #pragma unroll
-              for (int j = 0; j < 32; j++) xch[(32 * (q - 2) + lane) * 33 + j] = v[j];
-            tc05::named_sync(1, 128);
-            if (q < 2) {
-              const int i = 32 * q + lane;
-#pragma unroll
-              for (int j = 0; j < 32; j++) {
-                const float g = v[j], u = xch[i * 33 + j];
-                const float h = g / (1.f + expf(-g)) * u;
-                hs[j * 64 + (i & ~7) + perm8(i & 7)] = (uint16_t)f2bf_rn(h);
-              }
+            for (int j = 0; j < 16; j++) {
+              const float mine = up ? v[16 + j] : v[j];
+              const float other = __shfl_xor_sync(FULLM, up ? v[j] : v[16 + j], 16);
+              const float g = up ? other : mine, u = up ? mine : other;
+              const float h = __fdividef(g, 1.f + __expf(-g)) * u;
+              hs[(16 * up + j) * 64 + (i & ~7) + perm8(i & 7)] = (uint16_t)f2bf_rn(h);
             }
-            tc05::named_sync(1, 128);
-            for (int i = et; i < 32 * 8; i += 128) {
-              const int j = i >> 3, c = i & 7;
+            tc05::named_sync(1, 128);  // h of 32 tokens x 64 indices complete (buffers alternate)
+            for (int k = et; k < 32 * 8; k += 128) {
+              const int j = k >> 3, c = k & 7;
               if (c0 + j < T.nlen)
                 *reinterpret_cast<uint4 *>(P.hbuf + (size_t)(T.n0 + c0 + j) * P.I + T.mt * 64 + c * 8) =
                     *reinterpret_cast<const uint4 *>(hs + j * 64 + c * 8);
@@ -548,18 +572,20 @@ __device__ __forceinline__ uint32_t orderable_f(float f) {
 }
 
 // Warp per token: top-k (ties to the lower id) of E <= 1024 logits, softmax
-// over the k chosen, per-(chunk, expert) counts.
+// over the k chosen, per-(chunk, expert) counts.  Lane l holds experts
+// l, l + 32, ... (coalesced loads); each round takes the largest key, and
+// among equal keys the lowest expert id.
 __global__ void pf_topk(const __grid_constant__ PfParams P) {
   const int lane = threadIdx.x & 31;
   const int tok = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (tok >= P.t) return;
-  const int E = P.E, K = P.K, PP = (E + 31) / 32;
+  const int E = P.E, K = P.K;
   const float *lg = P.logits + (size_t)tok * E;
   uint32_t key[32];
 #pragma unroll
   for (int i = 0; i < 32; i++) {
-    const int e = lane * PP + i;
-    key[i] = (i < PP && e < E) ? orderable_f(lg[e]) : 0u;
+    const int e = i * 32 + lane;
+    key[i] = e < E ? orderable_f(lg[e]) : 0u;
   }
   uint32_t bk = 0;
   int bi = 0;
@@ -570,10 +596,9 @@ __global__ void pf_topk(const __grid_constant__ PfParams P) {
   int myid = 0;
   for (int r = 0; r < K; r++) {
     const uint32_t m = __reduce_max_sync(FULLM, bk);
-    const int wl = __ffs(__ballot_sync(FULLM, bk == m)) - 1;
-    const int id = __shfl_sync(FULLM, lane * PP + bi, wl);
-    if (lane == r) myid = id, myl = lg[id];
-    if (lane == wl) {
+    const uint32_t id = __reduce_min_sync(FULLM, bk == m ? (uint32_t)(bi * 32 + lane) : 0xffffffffu);
+    if (lane == r) myid = (int)id, myl = lg[id];
+    if (lane == (int)(id & 31)) {
       uint32_t nbk = 0;
       int nbi = 0;
 #pragma unroll
@@ -593,7 +618,7 @@ __global__ void pf_topk(const __grid_constant__ PfParams P) {
     P.tk_w[(size_t)tok * K + lane] = w;
     if (P.topk_out) P.topk_out[(size_t)tok * K + lane] = (uint32_t)myid;
     if (P.topkw_out) P.topkw_out[(size_t)tok * K + lane] = w;
-    atomicAdd(&P.chist[(tok / kPfChunk) * E + myid], 1);
+    atomicAdd(&P.chist[(size_t)myid * ((P.t + kPfChunk - 1) / kPfChunk) + tok / kPfChunk], 1);
   }
 }
 
@@ -624,55 +649,76 @@ __device__ int block_exscan(int v, int *sh, int *total) {
   return r;
 }
 
-// One block of 1024 threads: groups g = 2i, 2i+1 per thread (experts, then
-// the shared expert with all tokens): offsets, per-chunk list bases, tile
-// work lists.
+// Warp per expert e: its count (sum over token chunks) into counts[e], and
+// in place the exclusive prefix of its chunk counts -- the place, within
+// the expert's list, of each chunk's first entry.
+__global__ void pf_group_count(const __grid_constant__ PfParams P) {
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (e >= P.E) return;
+  const int nch = (P.t + kPfChunk - 1) / kPfChunk;
+  int *h = P.chist + (size_t)e * nch;
+  int base = 0;
+  for (int k0 = 0; k0 < nch; k0 += 32) {
+    const int k = k0 + lane;
+    const int c = k < nch ? h[k] : 0;
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULLM, x, o);
+      if (lane >= o) x += y;
+    }
+    if (k < nch) h[k] = base + x - c;
+    base += __shfl_sync(FULLM, x, 31);
+  }
+  if (lane == 0) P.counts[e] = base;
+}
+
+// One block of 1024 threads.  Groups: the experts, then the shared expert
+// with every token.  Exclusive scans of the group sizes and of their
+// 256-token chunk counts give the group offsets and the tile work lists
+// (one item per thread).
 __global__ void __launch_bounds__(1024) pf_group(const __grid_constant__ PfParams P) {
-  __shared__ int sh[32];
-  const int E = P.E, G = E + (P.sgate ? 1 : 0), nch = (P.t + kPfChunk - 1) / kPfChunk;
+  __shared__ int s_off[1027], s_ch[1027], sh[32];
+  __shared__ uint64_t s_rec[1025];
+  const int E = P.E, G = E + (P.sgate ? 1 : 0);
   const int nmt1 = P.I / 64, nmt2 = P.H / 128;
-  int m[2], ch[2];
+  for (int g = threadIdx.x; g < G; g += blockDim.x)
+    s_rec[g] = g < E ? P.eaddr[g] : reinterpret_cast<uint64_t>(P.srec);
+  int m2[2], c2[2];
 #pragma unroll
   for (int u = 0; u < 2; u++) {
     const int g = 2 * threadIdx.x + u;
-    int c = 0;
-    if (g < E)
-      for (int k = 0; k < nch; k++) c += P.chist[k * E + g];
-    else if (g < G)
-      c = P.t;
-    m[u] = c;
-    ch[u] = (c + kPfTileN - 1) / kPfTileN;
+    m2[u] = g < E ? P.counts[g] : (g < G ? P.t : 0);
+    c2[u] = (m2[u] + kPfTileN - 1) / kPfTileN;
   }
   int tot_m, tot_ch;
-  const int om = block_exscan(m[0] + m[1], sh, &tot_m);
-  const int oc = block_exscan(ch[0] + ch[1], sh, &tot_ch);
-  const int offs[2] = {om, om + m[0]}, ocs[2] = {oc, oc + ch[0]};
+  const int om = block_exscan(m2[0] + m2[1], sh, &tot_m);
+  const int oc = block_exscan(c2[0] + c2[1], sh, &tot_ch);  // ends with a block barrier
 #pragma unroll
   for (int u = 0; u < 2; u++) {
     const int g = 2 * threadIdx.x + u;
     if (g < G) {
-      P.offs[g] = offs[u];
-      if (g < E) {  // chunk bases: ascending chunks keep ascending tokens
-        int b = offs[u];
-        for (int k = 0; k < nch; k++) {
-          const int c = P.chist[k * E + g];
-          P.chist[k * E + g] = b;
-          b += c;
-        }
-      }
-      const uint64_t rec = g < E ? P.eaddr[g] : reinterpret_cast<uint64_t>(P.srec);
-      int a = ocs[u] * nmt1, bb = ocs[u] * nmt2;
-      for (int c = 0; c < ch[u]; c++) {
-        const int n0 = offs[u] + c * kPfTileN, nl = min(kPfTileN, m[u] - c * kPfTileN);
-        for (int mt = 0; mt < nmt1; mt++) P.items1[a++] = PfItem{g, mt, n0, nl, rec};
-        for (int mt = 0; mt < nmt2; mt++) P.items2[bb++] = PfItem{g, mt, n0, nl, rec};
-      }
+      s_off[g] = u ? om + m2[0] : om;
+      s_ch[g] = u ? oc + c2[0] : oc;
     }
   }
   if (threadIdx.x == 0) {
-    P.offs[G] = tot_m;
+    s_off[G] = tot_m, s_ch[G] = tot_ch;
     P.nitems[0] = tot_ch * nmt1, P.nitems[1] = tot_ch * nmt2;
   }
+  __syncthreads();
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) P.offs[g] = s_off[g];
+  auto item = [&](int cc, int mt) {  // cc: global chunk index
+    int lo = 0, hi = G;              // the last group g with s_ch[g] <= cc (it holds chunk cc)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_ch[mid] <= cc) lo = mid; else hi = mid;
+    }
+    const int g = lo, c = cc - s_ch[g], m = s_off[g + 1] - s_off[g];
+    return PfItem{g, mt, s_off[g] + c * kPfTileN, min(kPfTileN, m - c * kPfTileN), s_rec[g]};
+  };
+  for (int i = threadIdx.x; i < tot_ch * nmt1; i += blockDim.x) P.items1[i] = item(i / nmt1, i % nmt1);
+  for (int i = threadIdx.x; i < tot_ch * nmt2; i += blockDim.x) P.items2[i] = item(i / nmt2, i % nmt2);
 }
 
 // One warp per chunk of kPfChunk tokens: the chunk's (token, expert) pairs in
@@ -681,7 +727,8 @@ __global__ void __launch_bounds__(1024) pf_group(const __grid_constant__ PfParam
 __global__ void pf_fill(const __grid_constant__ PfParams P) {
   extern __shared__ int cnt[];  // [E] next place of each expert for this chunk
   const int E = P.E, K = P.K, c = blockIdx.x, lane = threadIdx.x;
-  for (int e = lane; e < E; e += 32) cnt[e] = P.chist[c * E + e];
+  const int nch = (P.t + kPfChunk - 1) / kPfChunk;
+  for (int e = lane; e < E; e += 32) cnt[e] = P.offs[e] + P.chist[(size_t)e * nch + c];
   __syncwarp();
   const int t0 = c * kPfChunk, t1 = min(P.t, t0 + kPfChunk);
   for (int i0 = t0 * K; i0 < t1 * K; i0 += 32) {
@@ -739,6 +786,7 @@ void carve(int H, int E, int K, int I, int t, F &&take) {
   take(6, (size_t)t * K * 4);    // tk_w
   take(7, nch * E * 4);          // chist
   take(8, (size_t)(E + 2) * 4);  // offs
+  take(17, (size_t)(E + 2) * 4); // counts
   take(9, ent * 4);              // rows
   take(10, ent * 4);             // wts
   take(11, items * (I / 64) * sizeof(PfItem));
@@ -760,7 +808,7 @@ size_t pf_workspace_bytes(int H, int E, int K, int I, int t) {
 void pf_carve(PfParams &p, void *work) {
   char *base = reinterpret_cast<char *>(work);
   size_t o = 0;
-  void *ptr[17];
+  void *ptr[18];
   carve(p.H, p.E, p.K, p.I, p.t, [&](int k, size_t n) {
     ptr[k] = base + o;
     o += al(n);
@@ -782,6 +830,7 @@ void pf_carve(PfParams &p, void *work) {
   p.hbuf = (uint16_t *)ptr[14];
   p.Y = (float *)ptr[15];
   p.xc = (uint16_t *)ptr[16];
+  p.counts = (int *)ptr[17];
 }
 
 namespace {
@@ -856,19 +905,21 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if ((e = mark(2))) return e;
   pf_topk<<<(t + 7) / 8, 256, 0, st>>>(p);
   if ((e = mark(3))) return e;
-  pf_group<<<1, 1024, 0, st>>>(p);
+  pf_group_count<<<(p.E + 7) / 8, 256, 0, st>>>(p);
   if ((e = mark(4))) return e;
-  pf_fill<<<nch, 32, (size_t)p.E * 4, st>>>(p);
+  pf_group<<<1, 1024, 0, st>>>(p);
   if ((e = mark(5))) return e;
+  pf_fill<<<nch, 32, (size_t)p.E * 4, st>>>(p);
+  if ((e = mark(6))) return e;
   if (!p.route_only) {
     pf_gather<<<(int)((ent_cap + 7) / 8), 256, 0, st>>>(p);
-    if ((e = mark(6))) return e;
-    pf_gemm<MODE_GATE_UP><<<p.n_sms, kWsThreads, kWsSmem, st>>>(p);
     if ((e = mark(7))) return e;
-    pf_gemm<MODE_DOWN><<<p.n_sms, kWsThreads, kWsSmem, st>>>(p);
+    pf_gemm<MODE_GATE_UP><<<p.n_sms, kWsThreads, kWsSmem, st>>>(p);
     if ((e = mark(8))) return e;
-    pf_final<<<1024, 256, 0, st>>>(p);
+    pf_gemm<MODE_DOWN><<<p.n_sms, kWsThreads, kWsSmem, st>>>(p);
     if ((e = mark(9))) return e;
+    pf_final<<<1024, 256, 0, st>>>(p);
+    if ((e = mark(10))) return e;
   }
   return cudaGetLastError();
 }

@@ -15,7 +15,7 @@ struct PfItem {
 };
 
 constexpr int kPfTileN = 256;  // token columns per tensor-core tile
-constexpr int kPfChunk = 64;   // tokens per chunk of the stable grouping
+constexpr int kPfChunk = 32;   // tokens per chunk of the stable grouping
 
 struct PfParams {
   // TMA descriptors (bf16, 128B swizzle): router rows [E][H] (box 64 x 128),
@@ -49,7 +49,8 @@ struct PfParams {
   float *logits;            // [t][E]
   int *tk_idx;              // [t][K]
   float *tk_w;              // [t][K]
-  int *chist;               // [nch][E] per-chunk expert counts, then per-chunk list bases
+  int *chist;               // [E][nch] per-(expert, token chunk) counts, then their places in the list
+  int *counts;              // [E] entries per expert
   int *offs;                // [E+2] first grouped entry of each group; offs[G] = total
   int *rows;                // [t*(K+1)] token of each grouped entry
   float *wts;               // [t*(K+1)] its weight
@@ -60,7 +61,7 @@ struct PfParams {
   uint16_t *xc;             // bf16 [t*(K+1)][H]: xg rows in group order
 };
 
-constexpr int kPfStages = 9;  // kernels of one prefill call, in launch order
+constexpr int kPfStages = 10;  // kernels of one prefill call, in launch order
 
 size_t pf_workspace_bytes(int H, int E, int K, int I, int t);
 void pf_carve(PfParams &p, void *work);

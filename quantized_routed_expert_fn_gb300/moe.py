@@ -25,9 +25,9 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_EALIGN
 
 EXPORTS = ["moe_route", "moe_forward", "moe_forward_traced", "moe_forward_noalloc", "moe_forward_workspace",
            "moe_prefill", "moe_prefill_timed", "moe_prefill_workspace", "moe_prefill_group", "moe_last_error"]
-PREFILL_KERNELS = 9
-PREFILL_KERNEL_NAMES = ["prep", "router_gemm", "topk", "group_scan", "group_fill", "gather", "gate_up_gemm",
-                        "down_gemm", "output"]
+PREFILL_KERNELS = 10
+PREFILL_KERNEL_NAMES = ["prep", "router_gemm", "topk", "group_count", "group_scan", "group_fill", "gather",
+                        "gate_up_gemm", "down_gemm", "output"]
 NOALLOC_MAX_WORKSPACE = 4 << 20
 TRACE_CTAS, TRACE_PHASES = 1024, 16
 
