@@ -43,6 +43,29 @@ WORKLOADS = {
 METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 1 GB300"
 
 
+# DRAM traffic per launch of the dominant kernel, from one ncu capture each
+# (profiles/decode_c1.md, profiles/prefill_c4.md).  Reported only while the
+# kernel's sources hash to the value they had when the counters were taken.
+NCU_TRAFFIC = {
+    "c1": dict(bytes=1205.5e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],
+               sha="12bc742223679df9"),
+    "c4": dict(bytes=640.8e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
+               sha="5970757fc5113eaf"),
+}
+
+
+def ncu_traffic(workload):
+    import hashlib
+    t = NCU_TRAFFIC.get(workload)
+    if t is None:
+        return None
+    m = hashlib.sha256()
+    for f in t["sources"]:
+        with open(os.path.join(ROOT, "quantized_routed_expert_fn_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    return t["bytes"] if m.hexdigest()[:16] == t["sha"] else None
+
+
 def load_peaks(kind="hbm"):
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -93,6 +116,22 @@ class ClockSampler:
         os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def reduce_over_ranks(values, world: int, device="cpu"):
+    """Max of each timing over the ranks: the slowest replica sets the job time."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as td
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    td.all_reduce(t, op=td.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_rows_per_s(rows_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank's rows over the (max) step time."""
+    return rows_per_rank * world / (ms * 1e-3)
 
 
 def layer_bytes(L, union_size: int, nb: int) -> int:
@@ -198,10 +237,7 @@ def run_ours(args, rank, world, device):
     if dist:
         td.barrier()
 
-    if dist:
-        t = torch.tensor([ms, e2e_ms], device=device)
-        td.all_reduce(t, op=td.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = reduce_over_ranks([ms, e2e_ms], world, device)
     rows = nb * nl * world
     peak, peak_kind = load_peaks()
     achieved = bytes_per_step / (ms * 1e-3) / 1e9
@@ -297,10 +333,7 @@ def run_prefill(args, rank, world, device):
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if dist:
-        tt = torch.tensor([ms, e2e_ms], device=device)
-        td.all_reduce(tt, op=td.ReduceOp.MAX)
-        ms, e2e_ms = float(tt[0]), float(tt[1])
+    ms, e2e_ms = reduce_over_ranks([ms, e2e_ms], world, device)
     top = max(flops, key=lambda n: kernel_ms[n])
     peak, peak_kind = load_peaks("tensor")
     achieved = flops[top] / (kernel_ms[top] * 1e-3) / 1e12
@@ -415,14 +448,16 @@ def main():
             cpu = oracle_prefill_sample(nb, budget_s=args.cpu_budget)
             H = synth.CONFIGS["c4"]["hidden"]
             line = {
-                "metric": METRIC, "value": r["rows"] / (r["ms"] * 1e-3), "unit": "rows/s", "n_gpus": world,
+                "metric": METRIC, "value": job_rows_per_s(r["t"], world, r["ms"]), "unit": "rows/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config,
-                "e2e": {"value": r["rows"] / (r["e2e_ms"] * 1e-3), "unit": "rows/s",
+                "e2e": {"value": job_rows_per_s(r["t"], world, r["e2e_ms"]), "unit": "rows/s",
                         "h2d_bytes_per_step": nb * H * 4, "d2h_bytes_per_step": nb * H * 2},
                 "gpu_launches": args.steps * 10,
                 "roofline": {"bound": "tensor", "achieved": r["achieved"], "peak": r["peak"], "unit": "TFLOP/s",
-                             "frac": r["achieved"] / r["peak"], "traffic": None, "kernel": r["top"],
+                             "frac": r["achieved"] / r["peak"],
+                             "traffic": ncu_traffic("c4") if r["top"] == "gate_up_gemm" else None,
+                             "kernel": r["top"],
                              "peak_source": r["peak_kind"] + " bf16 burst",
                              "algorithmic_flops_per_launch": r["flops"][r["top"]]},
                 "kernel_ms": r["kernel_ms"],
@@ -444,8 +479,8 @@ def main():
             torch.distributed.destroy_process_group()
         return
     cpu = oracle_sample(args.workload, nb, budget_s=args.cpu_budget) if world == 1 or rank == 0 else None
-    value = r["rows"] / (r["ms"] * 1e-3)
-    e2e_value = r["rows"] / (r["e2e_ms"] * 1e-3)
+    value = job_rows_per_s(r["nb"] * r["nl"], world, r["ms"])
+    e2e_value = job_rows_per_s(r["nb"] * r["nl"], world, r["e2e_ms"])
     line = {
         "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True, "scaling": "weak",
@@ -454,7 +489,8 @@ def main():
                 "d2h_bytes_per_step": nb * cfg["hidden"] * 4},
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
-                     "frac": r["achieved"] / r["peak"], "traffic": None,
+                     "frac": r["achieved"] / r["peak"],
+                     "traffic": ncu_traffic(args.workload) if args.workload == "c1" and not args.layers else None,
                      "peak_source": r["peak_kind"], "algorithmic_bytes_per_launch": r["bytes"]},
         "cpu_baseline": {"value": cpu["value"], "unit": "rows/s", "cores": cpu["cores"], "kind": "oracle",
                          "sample": f"first {cpu['layers']} layers of the workload, {cpu['seconds']:.1f} s"},
