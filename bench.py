@@ -49,8 +49,8 @@ METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 
 NCU_TRAFFIC = {
     "c1": dict(bytes=1205.5e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],
                sha="12bc742223679df9"),
-    "c4": dict(bytes=640.8e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
-               sha="5970757fc5113eaf"),
+    "c4": dict(bytes=640.7e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
+               sha="bb6773a973c065ce"),
 }
 
 

@@ -10,11 +10,11 @@
 //   group   scan -> offsets of the groups (experts, then the shared expert
 //           with all t tokens); per-chunk bases; tile work lists
 //   fill    token lists in ascending token order (stable), routing weights
-//   gate_up per (group, 64 gate + 64 up rows, <= 256 tokens): weights
-//           dequantized to bf16 into 128B-swizzled shared memory (A), token
-//           rows gathered (B), tcgen05 MMA into TMEM; epilogue
+//   gate_up per (group, 64 gate + 64 up rows, <= kPfTileN tokens): weights
+//           dequantized to bf16 into tensor memory (A), token rows in group
+//           order through TMA (B), tcgen05 MMA into TMEM; epilogue
 //           h = silu(gate) * up -> bf16
-//   down    per (group, 128 output rows, <= 256 tokens): A = dequantized
+//   down    per (group, 128 output rows, <= kPfTileN tokens): A = dequantized
 //           down rows, B = h; epilogue Y[token] += weight * y (fp32)
 //   final   out = bf16(Y) (+ x for a residual layer)
 // The k order inside every 8-element block is permuted the same way on both
@@ -32,8 +32,6 @@ constexpr unsigned FULLM = 0xffffffffu;
 constexpr uint32_t kResidualF = 1, kPrenormF = 2;
 enum { MODE_ROUTER = 0, MODE_GATE_UP = 1, MODE_DOWN = 2 };
 
-constexpr int kStageA = 128 * 128;       // 128 rows x 64 k bf16
-constexpr int kStageB = kPfTileN * 128;  // 256 rows x 64 k bf16
 
 __device__ __forceinline__ uint32_t f2bf_rn(float f) {
   uint32_t u = __float_as_uint(f);
@@ -129,40 +127,60 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 // ------------------------------------------------------------ tensor-core GEMM
 //
 // Persistent, warp-specialised: one CTA per SM walks tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... of a 128 x N (N <= 256) output tile list; K
-// goes in stages of 64 through a ring of kS shared-memory stages.
+// blockIdx.x + gridDim.x, ... of a 128 x N output tile list (N <= 256 for
+// the router, <= kPfTileN for the expert GEMMs); K goes in stages of 64.
+// B (token rows) passes through a ring of kSB 128B-swizzled shared-memory
+// stages.  The expert GEMMs' A (dequantized weight rows) passes through a
+// ring of kSA stages in tensor memory, 32 columns each (row r in TMEM lane
+// r, bf16 pairs along k), and feeds tcgen05.mma from there; the router's A
+// (bf16 rows of R) comes by TMA into shared memory beside its B.
 //   warp 0      lane 0 issues the tcgen05 MMAs of a stage once its operands
 //               have landed and commits them (stage free / accumulator full)
 //   warp 1      TMA: B rows (and the router's A rows) of each stage
-//   warps 2-9   A producers, two groups of four warps taking alternate
-//               stages: thread r of a group dequantizes weight row r of the
-//               tile (64 codes = one group per stage) to bf16 in the
-//               swizzled layout; each group's loads run four of its stages
-//               (eight stages in all) ahead, enough bytes in flight to
-//               stream the codes at HBM rate
+//   warps 2-9   A producers: all 256 threads stage the codes of four
+//               k-stages (128 rows x 128 bytes, plus scale / bias words)
+//               into shared memory with coalesced cp.async, three chunks in
+//               the air; then warp w dequantizes half hf = (w - 2) / 4 of the
+//               64 codes of rows 32 (w % 4) .. +31 -- the TMEM lanes warp w
+//               may write -- and stores the 16 bf16 pairs with tcgen05.st
 //   warps 10-13 epilogue: TMEM -> registers -> global, from one of two
 //               accumulators while the MMAs fill the other
 // Every mbarrier wait is bounded; a wait that gives up records
 // MOE_ETIMEOUT in *status and its role stops, so the CTA ends.
 
 constexpr int kWsThreads = 448;
-constexpr int kS = 3;                      // A / B pipeline stages
+constexpr int kSB = 6;                     // B stages (shared memory)
+constexpr int kSA = 4;                     // A stages (tensor memory; expert GEMMs)
+constexpr int kAccCols = 192;              // TMEM columns of one accumulator (expert GEMMs; N <= 192)
+constexpr int kTmemA = 2 * kAccCols;       // first TMEM column of the A ring: kSA x 32 columns
+static_assert(kTmemA + 32 * kSA <= 512, "tensor memory");
 constexpr int kChunk = 4;                  // k-stages per staged chunk of codes
 constexpr int kStgCodes = 128 * 128;       // 128 rows x 128 bytes of codes (4 stages)
 constexpr int kStgSB = 128 * kChunk * 8;   // per row and stage: scale word, bias word
 constexpr int kStgBuf = kStgCodes + kStgSB;
 constexpr int kNStg = 3;                   // staged chunks: one being read, two in flight
-constexpr int kOffB = kS * kStageA;        // B stages follow the A stages
-constexpr int kOffStg = kOffB + kS * kStageB;
-constexpr int kOffEpi = kOffStg + kNStg * kStgBuf;
-constexpr int kEpiBytes = 16384;           // down: 4 warps x 32 x 32 fp32; gate_up: exchange + h rows
-constexpr int kOffTile = kOffEpi + kEpiBytes;
-constexpr int kOffBars = kOffTile + 2 * kPfTileN * 4;
-constexpr int kWsSmem = kOffBars + 256 + 1024;  // + alignment slack
-static_assert(kWsSmem <= 227 * 1024, "shared memory");
+constexpr int kEpiBytes = 16384;           // down: 4 warps x 32 x 32 fp32; gate_up: h rows
+
+// Shared-memory layout of one pf_gemm instantiation (offsets 1024-aligned
+// where the 128B swizzle needs it).  Router: kSB stages of A (128 router
+// rows) and B (128 token rows).  Expert GEMMs: kSB stages of B (up to
+// kPfTileN token rows) and the staged code chunks; A lives in TMEM.
+template <int MODE>
+struct Lay {
+  static constexpr int stageB = MODE == MODE_ROUTER ? 128 * 128 : kPfTileN * 128;
+  static constexpr int offA = kSB * stageB;
+  static constexpr int offStg = offA + (MODE == MODE_ROUTER ? kSB * 128 * 128 : 0);
+  static constexpr int offEpi = offStg + (MODE == MODE_ROUTER ? 0 : kNStg * kStgBuf);
+  static constexpr int offTile = offEpi + kEpiBytes;
+  static constexpr int offBars = offTile + 2 * kPfTileN * 4;
+  static constexpr int smem = offBars + 512 + 1024;  // + alignment slack
+  static constexpr int accCols = MODE == MODE_ROUTER ? 256 : kAccCols;
+  static_assert(smem <= 227 * 1024, "shared memory");
+  static_assert(stageB % 1024 == 0 && offA % 1024 == 0, "swizzled stages");
+};
 
 struct WsBars {
-  uint64_t full_b[kS], full_a[kS], empty[kS], acc_full[2], acc_empty[2], drain;
+  uint64_t full_b[kSB], empty_b[kSB], full_a[kSA], empty_a[kSA], acc_full[2], acc_empty[2], drain;
   uint32_t tmem;
 };
 
@@ -196,6 +214,20 @@ __device__ __forceinline__ PfItem ws_item(const PfParams &P, int ti) {
 }
 
 __device__ __forceinline__ int tile_n(const PfItem &it) { return (it.nlen + 15) & ~15; }
+
+// Token rows a B stage loads per k-panel for N columns: 128-row boxes, then
+// 32-row boxes for the rest.
+__device__ __forceinline__ int panel_rows(int N) { return (N & ~127) + (((N & 127) + 31) & ~31); }
+
+// k-panels per B stage (expert GEMMs): a narrow tile carries several panels
+// in one stage buffer, so that each TMA round trip (a latency of thousands
+// of cycles) feeds more MMAs.  A divisor of nk.
+__device__ __forceinline__ int panels_per_stage(int N, int nk) {
+  const int r = panel_rows(N);
+  for (int p = 4; p > 1; p >>= 1)
+    if (p * r <= kPfTileN && nk % p == 0) return p;
+  return 1;
+}
 
 template <int MODE>
 __device__ __forceinline__ bool item_ok(const PfItem &it) {
@@ -257,33 +289,31 @@ __device__ __forceinline__ void stage_chunk(const PfParams &P, const PfItem &it,
 }
 
 // Half hf (codes 32hf .. 32hf+31) of row r's 64 codes of stage u of a
-// staged chunk -> bf16(scale * code + bias), k permuted within 8-blocks,
-// into chunks 4hf .. 4hf+3 of row r of a swizzled A stage
+// staged chunk -> bf16(scale * code + bias), k permuted within 8-blocks, as
+// 16 words of two bf16 each (the row's A columns 16hf .. 16hf+15)
 __device__ __forceinline__ void ws_dequant_half(const uint8_t *buf, int r, int hf, int u, uint32_t half,
-                                                uint8_t *sA) {
+                                                uint32_t (&a)[16]) {
   const uint4 c = *reinterpret_cast<const uint4 *>(buf + r * 128 + (((2 * u + hf) ^ (r & 7)) << 4));
   const uint2 sbw = *reinterpret_cast<const uint2 *>(buf + kStgCodes + (r * kChunk + u) * 8);
   const uint32_t s = (sbw.x >> (16 * half)) & 0xffffu, b = (sbw.y >> (16 * half)) & 0xffffu;
   const uint32_t s2 = s * 0x10001u, b2 = b * 0x10001u;
   const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-  for (int ch = 0; ch < 4; ch++) {
-    uint32_t pr[4];
+  for (int ch = 0; ch < 4; ch++)
 #pragma unroll
     for (int j = 0; j < 4; j++) {
       const uint32_t v = ((w[ch] >> (4 * j)) & 0x000f000fu) | 0x43004300u;  // (128 + n_j, 128 + n_{j+4})
       const uint32_t qv = bfma2(v, 0x3f803f80u, 0xc300c300u);              // the codes, exact
-      pr[j] = bfma2(qv, s2, b2);                                            // bf16(s*q + b)
+      a[4 * ch + j] = bfma2(qv, s2, b2);                                    // bf16(s*q + b)
     }
-    *reinterpret_cast<uint4 *>(sA + tc05::sw128_offset(r, 4 * hf + ch)) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-  }
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__ PfParams P) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
-  WsBars &B = *reinterpret_cast<WsBars *>(sm + kOffBars);
+  using LY = Lay<MODE>;
+  WsBars &B = *reinterpret_cast<WsBars *>(sm + LY::offBars);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ntiles = ws_num_tiles<MODE>(P);
   const int nk = ws_nk<MODE>(P);
@@ -291,10 +321,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
   auto tile_of = [&](int lt) { return (int)blockIdx.x + lt * (int)gridDim.x; };
 
   if (tid == 0) {
-    for (int s = 0; s < kS; s++) {
+    for (int s = 0; s < kSB; s++) {
       mbar_init(&B.full_b[s], 1);
+      mbar_init(&B.empty_b[s], 1);
+    }
+    for (int s = 0; s < kSA; s++) {
       mbar_init(&B.full_a[s], 8);
-      mbar_init(&B.empty[s], 1);
+      mbar_init(&B.empty_a[s], 1);
     }
     for (int b = 0; b < 2; b++) {
       mbar_init(&B.acc_full[b], 1);
@@ -311,95 +344,141 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
 
   if (warp == 0) {
     // ---------------------------------------------------------------- MMA issue
-    if (lane == 0) {
-      int f = 0;
+    // The whole warp walks the loop (warp-uniform state, waits by lane 0 with
+    // the outcome broadcast); one elected lane issues each MMA group and
+    // commit.  Ring positions and phases are kept incrementally: this loop is
+    // on the critical path.
+    {
+      int sa = 0, sb = 0;
+      uint32_t pa = 0, pb = 0;
       bool ok = true;
       PfItem nx{};
+      const uint64_t desc0 = tc05::sdesc(smem_u32(sm));  // + (byte offset >> 4) within shared memory
       if (my_tiles > 0) nx = ws_item<MODE>(P, tile_of(0));
       for (int lt = 0; lt < my_tiles && ok; lt++) {
         const PfItem cur = nx;
         if (lt + 1 < my_tiles) nx = ws_item<MODE>(P, tile_of(lt + 1));
         const int b = lt & 1;
-        if (!pf_wait(&B.acc_empty[b], (uint32_t)(((lt >> 1) & 1) ^ 1), P)) {
+        if (!warp_wait(&B.acc_empty[b], (uint32_t)(((lt >> 1) & 1) ^ 1), P)) {
           ok = false;
           break;
         }
         tc05::fence_after();
-        const uint32_t d = tmem + (uint32_t)(b * 256);
-        const uint32_t idesc = tc05::idesc_bf16(tile_n(cur));
-        for (int kk = 0; kk < nk; kk++, f++) {
-          const int s = f % kS;
-          const uint32_t par = (uint32_t)((f / kS) & 1);
-          if (!pf_wait(&B.full_b[s], par, P) || (MODE != MODE_ROUTER && !pf_wait(&B.full_a[s], par, P))) {
-            ok = false;
-            break;
+        const uint32_t d = tmem + (uint32_t)(b * LY::accCols);
+        const int N = tile_n(cur);
+        const uint32_t idesc = tc05::idesc_bf16(N);
+        const int ppb = MODE == MODE_ROUTER ? 1 : panels_per_stage(N, nk);
+        const uint32_t pstep = (uint32_t)(panel_rows(N) * 128) >> 4;  // descriptor step per panel
+        int pp = 0;
+        uint64_t bdesc = desc0;
+        for (int kk = 0; kk < nk; kk++) {
+          if (pp == 0) {
+            if (!warp_wait(&B.full_b[sb], pb, P)) {
+              ok = false;
+              break;
+            }
+            bdesc = desc0 + (uint32_t)(sb * LY::stageB >> 4);
           }
-          tc05::fence_after();
-          const uint32_t a0 = smem_u32(sm + s * kStageA), b0 = smem_u32(sm + kOffB + s * kStageB);
+          if constexpr (MODE == MODE_ROUTER) {
+            tc05::fence_after();
+            const uint64_t adesc = desc0 + (uint32_t)((LY::offA + sb * 128 * 128) >> 4);
+            if (tc05::elect_one()) {
 #pragma unroll
-          for (int j = 0; j < 4; j++)
-            tc05::mma(d, tc05::sdesc(a0 + 32 * j), tc05::sdesc(b0 + 32 * j), idesc, (kk | j) != 0);
-          tc05::commit(&B.empty[s]);
+              for (int j = 0; j < 4; j++) tc05::mma(d, adesc + 2 * j, bdesc + 2 * j, idesc, (kk | j) != 0);
+            }
+            __syncwarp();
+          } else {
+            if (!warp_wait(&B.full_a[sa], pa, P)) {
+              ok = false;
+              break;
+            }
+            tc05::fence_after();
+            if (tc05::elect_one()) {
+              tc05::mma_ts_k64(d, tmem + (uint32_t)(kTmemA + 32 * sa), bdesc, idesc, kk != 0);
+              tc05::commit(&B.empty_a[sa]);
+            }
+            __syncwarp();
+            if (++sa == kSA) sa = 0, pa ^= 1;
+          }
+          bdesc += pstep;
+          if (++pp == ppb) {
+            if (tc05::elect_one()) tc05::commit(&B.empty_b[sb]);
+            __syncwarp();
+            pp = 0;
+            if (++sb == kSB) sb = 0, pb ^= 1;
+          }
         }
-        if (ok) tc05::commit(&B.acc_full[b]);
+        if (ok) {
+          if (tc05::elect_one()) tc05::commit(&B.acc_full[b]);
+          __syncwarp();
+        }
       }
       // every MMA issued here has completed before TMEM is released
-      tc05::commit(&B.drain);
-      pf_wait(&B.drain, 0, P);
+      if (tc05::elect_one()) tc05::commit(&B.drain);
+      __syncwarp();
+      warp_wait(&B.drain, 0, P);
     }
-    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- B producer (TMA)
     // router: 128 token rows of x^ hi / lo and the 128 router rows; gate_up
     // and down: the tile's rows of the grouped operand (x^ rows gathered in
     // group order, or h), boxes of 128 rows then 32-row boxes for the tail
-    int f = 0;
+    int f = 0;  // B stages
     PfItem ia{}, ib{};
     if (my_tiles > 0) ia = ws_item<MODE>(P, tile_of(0));
     bool ok = true;
     for (int lt = 0; lt < my_tiles && ok; lt++) {
       if (lt + 1 < my_tiles) ib = ws_item<MODE>(P, tile_of(lt + 1));
       const int N = tile_n(ia);
-      const int n128 = N >> 7, n32 = ((N & 127) + 31) >> 5;
-      const uint32_t bytes = MODE == MODE_ROUTER ? (uint32_t)(kStageA + 128 * 128)
-                                                 : (uint32_t)(n128 * 128 + n32 * 32) * 128u;
+      const int n128 = N >> 7, n32 = ((N & 127) + 31) >> 5, nops = n128 + n32;
+      const int ppb = MODE == MODE_ROUTER ? 1 : panels_per_stage(N, nk), prow = panel_rows(N);
+      const uint32_t bytes = MODE == MODE_ROUTER ? (uint32_t)(2 * 128 * 128) : (uint32_t)(ppb * prow * 128);
       const CUtensorMap *m128 = MODE == MODE_GATE_UP ? &P.tm_xc : &P.tm_h;
       const CUtensorMap *m32 = MODE == MODE_GATE_UP ? &P.tm_xc32 : &P.tm_h32;
-      for (int kk = 0; kk < nk; kk++, f++) {
-        const int s = f % kS;
-        if (!warp_wait(&B.empty[s], (uint32_t)(((f / kS) & 1) ^ 1), P)) {
+      const int ent = P.t * (P.K + 1);  // rows of one k-panel of xc / h
+      for (int kk = 0; kk < nk; kk += ppb, f++) {
+        const int s = f % kSB;
+        if (!warp_wait(&B.empty_b[s], (uint32_t)(((f / kSB) & 1) ^ 1), P)) {
           ok = false;
           break;
         }
-        uint8_t *sb = sm + kOffB + s * kStageB;
+        uint8_t *sb = sm + s * LY::stageB;
         if (lane == 0) mbar_expect_tx(&B.full_b[s], bytes);
         __syncwarp();
         if constexpr (MODE == MODE_ROUTER) {
           const int nq = P.H / 64, kq = kk % nq, yb = (kk < nq ? 0 : P.t) + ia.n0;
           if (lane == 0) {
-            tc05::tma_load_2d(sm + s * kStageA, &P.tm_router, kq * 64, ia.mt * 128, &B.full_b[s]);
+            tc05::tma_load_2d(sm + LY::offA + s * 128 * 128, &P.tm_router, kq * 64, ia.mt * 128, &B.full_b[s]);
             tc05::tma_load_2d(sb, &P.tm_xr, kq * 64, yb, &B.full_b[s]);
           }
         } else {
-          if (lane < n128) tc05::tma_load_2d(sb + lane * 128 * 128, m128, kk * 64, ia.n0 + lane * 128, &B.full_b[s]);
-          if (lane < n32)
-            tc05::tma_load_2d(sb + (n128 * 128 + lane * 32) * 128, m32, kk * 64, ia.n0 + n128 * 128 + lane * 32,
+          // k-panels kk .. kk+ppb-1, one after another; in each the tile's
+          // rows are contiguous (rows past the tile feed only accumulator
+          // columns that are never stored).  Lane l: box l % nops of panel
+          // l / nops.
+          if (lane < ppb * nops) {
+            const int pp = lane / nops, o = lane - pp * nops;
+            const int r0 = o < n128 ? 128 * o : 128 * n128 + 32 * (o - n128);
+            tc05::tma_load_2d(sb + (pp * prow + r0) * 128, o < n128 ? m128 : m32, 0, (kk + pp) * ent + ia.n0 + r0,
                               &B.full_b[s]);
+          }
         }
       }
       ia = ib;
     }
     // copies still in flight land before the CTA ends
-    if (lane == 0 && f > 0) pf_wait(&B.full_b[(f - 1) % kS], (uint32_t)(((f - 1) / kS) & 1), P);
+    if (lane == 0 && f > 0) pf_wait(&B.full_b[(f - 1) % kSB], (uint32_t)(((f - 1) / kSB) & 1), P);
     __syncwarp();
   } else if (warp < 10) {
     // ---------------------------------------------------------------- A producers
     if constexpr (MODE != MODE_ROUTER) {
-      const int t = tid - 64, r = t & 127, hf = t >> 7;  // row; half of its 64 codes
+      // thread t stages codes; thread (warp, lane) dequantizes tile row
+      // r = 32 * (warp % 4) + lane (the TMEM lanes its warp may write), half hf
+      const int t = tid - 64, r = 32 * (warp & 3) + lane, hf = (warp - 2) >> 2;
       const int nct = (nk + kChunk - 1) / kChunk;  // chunks per tile
       const int total = my_tiles * nct;
       const int inp = MODE == MODE_GATE_UP ? P.H : P.I;
-      uint8_t *stg = sm + kOffStg;
+      uint8_t *stg = sm + LY::offStg;
       // items of the staging position's tile and of the tile after it
       PfItem scur{}, snext{};
       int slt = 0;
@@ -431,17 +510,20 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         const uint8_t *buf = stg + (c % kNStg) * kStgBuf;
         const int ns = min(kChunk, nk - kc * kChunk);
         for (int u = 0; u < ns; u++) {
-          const int kk = kc * kChunk + u, f = lt * nk + kk, s = f % kS;
-          if (!warp_wait(&B.empty[s], (uint32_t)(((f / kS) & 1) ^ 1), P)) {
+          const int kk = kc * kChunk + u, f = lt * nk + kk, sa = f % kSA;
+          if (!warp_wait(&B.empty_a[sa], (uint32_t)(((f / kSA) & 1) ^ 1), P)) {
             ok = false;
             break;
           }
+          tc05::fence_after();  // after the MMAs that read this A stage
           // scale / bias: the half of the staged 4-byte word holding entry row * G + kk
           const uint32_t half = (rodd + (uint32_t)kk) & 1u;
-          ws_dequant_half(buf, r, hf, u, half, sm + s * kStageA);
-          fence_proxy_async_smem();
+          uint32_t av[16];
+          ws_dequant_half(buf, r, hf, u, half, av);
+          tc05::st16_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemA + 32 * sa + 16 * hf), av);
+          tc05::fence_before();
           __syncwarp();
-          if (lane == 0) tc05::mbar_arrive(&B.full_a[s]);
+          if (lane == 0) tc05::mbar_arrive(&B.full_a[sa]);
         }
         // the eight producer warps stop together (they share a named barrier)
         ok = tc05::named_and(4, 256, ok);
@@ -452,8 +534,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;    // TMEM lane quadrant this warp may read
     const int et = tid - 320;  // 0..127 over the epilogue warps
-    int *trow = reinterpret_cast<int *>(sm + kOffTile);
-    float *twt = reinterpret_cast<float *>(sm + kOffTile) + kPfTileN;
+    int *trow = reinterpret_cast<int *>(sm + LY::offTile);
+    float *twt = reinterpret_cast<float *>(sm + LY::offTile) + kPfTileN;
     PfItem nx{};
     unsigned hcnt = 0;  // gate_up: h chunks written so far (their buffers alternate)
     int pr[2] = {0, 0};
@@ -461,7 +543,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
     auto fetch_entries = [&](const PfItem &it) {  // down: this thread's two entries of a tile
 #pragma unroll
       for (int h = 0; h < 2; h++) {
-        const int j = et + 128 * h;
+        const int j = et + 128 * h;  // entries past kPfTileN do not exist
         pr[h] = j < it.nlen ? P.rows[it.n0 + j] : 0;
         pw[h] = j < it.nlen ? P.wts[it.n0 + j] : 0.f;
       }
@@ -478,13 +560,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       if (MODE == MODE_DOWN) {
         tc05::named_sync(1, 128);  // the previous tile's readers are done
 #pragma unroll
-        for (int h = 0; h < 2; h++) trow[et + 128 * h] = pr[h], twt[et + 128 * h] = pw[h];
+        for (int h = 0; h < 2; h++)
+          if (et + 128 * h < kPfTileN) trow[et + 128 * h] = pr[h], twt[et + 128 * h] = pw[h];
         tc05::named_sync(1, 128);
       }
       // the four epilogue warps stop together (they share named barriers)
       if (!tc05::named_and(2, 128, warp_wait(&B.acc_full[b], (uint32_t)((lt >> 1) & 1), P))) break;
       tc05::fence_after();
-      const uint32_t tl = tmem + (uint32_t)(b * 256) + ((uint32_t)(32 * q) << 16);
+      const uint32_t tl = tmem + (uint32_t)(b * LY::accCols) + ((uint32_t)(32 * q) << 16);
       if (item_ok<MODE>(T)) {
         for (int c0 = 0; c0 < N; c0 += 32) {
           float v[32];
@@ -498,7 +581,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
           } else if constexpr (MODE == MODE_DOWN) {
             // transpose the warp's 32 rows x 32 tokens through shared memory,
             // then one 16-byte reduction per (token, 4 rows)
-            float *tb = reinterpret_cast<float *>(sm + kOffEpi) + (warp - 10) * 1024;
+            float *tb = reinterpret_cast<float *>(sm + LY::offEpi) + (warp - 10) * 1024;
 #pragma unroll
             for (int j = 0; j < 32; j++) tb[j * 32 + lane] = v[j];
             __syncwarp();
@@ -519,7 +602,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
             // the gate lane takes columns 0..15, the up lane 16..31, each
             // fetching the partner's value with one exchange per column
             const int up = lane >> 4, i = 16 * q + (lane & 15);
-            uint16_t *hs = reinterpret_cast<uint16_t *>(sm + kOffEpi) + (hcnt++ & 1) * (32 * 64);
+            uint16_t *hs = reinterpret_cast<uint16_t *>(sm + LY::offEpi) + (hcnt++ & 1) * (32 * 64);
 #pragma unroll
             for (int j = 0; j < 16; j++) {
               const float mine = up ? v[16 + j] : v[j];
@@ -532,7 +615,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
             for (int k = et; k < 32 * 8; k += 128) {
               const int j = k >> 3, c = k & 7;
               if (c0 + j < T.nlen)
-                *reinterpret_cast<uint4 *>(P.hbuf + (size_t)(T.n0 + c0 + j) * P.I + T.mt * 64 + c * 8) =
+                *reinterpret_cast<uint4 *>(P.hbuf + ((size_t)T.mt * P.t * (P.K + 1) + T.n0 + c0 + j) * 64 + c * 8) =
                     *reinterpret_cast<const uint4 *>(hs + j * 64 + c * 8);
             }
           }
@@ -552,16 +635,19 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
   if (warp == 0) tc05::dealloc(tmem, 512);
 }
 
-// Expert operand rows in group order: xc[e] = x^ row of grouped entry e
-// (warp per entry, 16-byte copies), so that the gate_up GEMM reads its
-// token rows as plain TMA boxes.
+// Expert operand rows in group order, in k-panels: panel p holds elements
+// 64p .. 64p+63 of the x^ row of every grouped entry e (warp per entry,
+// 16-byte copies).  One k-stage of a gate_up tile's B is then one contiguous
+// block of its rows x 128 bytes.  (h uses the same layout for the down GEMM.)
 __global__ void pf_gather(const __grid_constant__ PfParams P) {
   const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int G = P.E + (P.sgate ? 1 : 0);
   if (e >= P.offs[G]) return;
   const uint4 *src = reinterpret_cast<const uint4 *>(P.xg + (size_t)P.rows[e] * P.H);
-  uint4 *dst = reinterpret_cast<uint4 *>(P.xc + (size_t)e * P.H);
-  for (int i = lane; i < P.H / 8; i += 32) dst[i] = src[i];
+  const size_t ent = (size_t)P.t * (P.K + 1);
+  // piece i (8 elements) of the row goes to k-panel i / 8
+  for (int i = lane; i < P.H / 8; i += 32)
+    reinterpret_cast<uint4 *>(P.xc + ((size_t)(i >> 3) * ent + e) * 64)[i & 7] = src[i];
 }
 
 // ------------------------------------------------------------ routing
@@ -675,7 +761,7 @@ __global__ void pf_group_count(const __grid_constant__ PfParams P) {
 
 // One block of 1024 threads.  Groups: the experts, then the shared expert
 // with every token.  Exclusive scans of the group sizes and of their
-// 256-token chunk counts give the group offsets and the tile work lists
+// kPfTileN-token chunk counts give the group offsets and the tile work lists
 // (one item per thread).
 __global__ void __launch_bounds__(1024) pf_group(const __grid_constant__ PfParams P) {
   __shared__ int s_off[1027], s_ch[1027], sh[32];
@@ -767,7 +853,7 @@ __global__ void pf_final(const __grid_constant__ PfParams P) {
 size_t al(size_t n) { return (n + 1023) & ~(size_t)1023; }
 
 // upper bound of the work items of one GEMM: sum over groups of
-// ceil(m_g / 256) <= entries / 256 + groups
+// ceil(m_g / kPfTileN) <= entries / kPfTileN + groups
 size_t max_items(int E, int K, int t) {
   const size_t ent = (size_t)t * (K + 1);
   return ent / kPfTileN + (size_t)E + 2;
@@ -853,6 +939,7 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 [rows][cols] row-major, box (64 columns = 128 bytes) x box_rows, 128B swizzle
+// (a k-panel buffer is [cols / 64 * entries][64])
 bool make_map(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -875,8 +962,9 @@ int pf_tensor_maps(PfParams &p, const char **why) {
   }
   const uint64_t ent = t * (uint64_t)(p.K + 1);
   if (!make_map(&p.tm_router, p.router, H, (uint64_t)p.E, 128) || !make_map(&p.tm_xr, p.xr_hi, H, 2 * t, 128) ||
-      !make_map(&p.tm_h, p.hbuf, (uint64_t)p.I, ent, 128) || !make_map(&p.tm_h32, p.hbuf, (uint64_t)p.I, ent, 32) ||
-      !make_map(&p.tm_xc, p.xc, H, ent, 128) || !make_map(&p.tm_xc32, p.xc, H, ent, 32)) {
+      !make_map(&p.tm_h, p.hbuf, 64, (uint64_t)p.I / 64 * ent, 128) ||
+      !make_map(&p.tm_h32, p.hbuf, 64, (uint64_t)p.I / 64 * ent, 32) ||
+      !make_map(&p.tm_xc, p.xc, 64, H / 64 * ent, 128) || !make_map(&p.tm_xc32, p.xc, 64, H / 64 * ent, 32)) {
     *why = "cuTensorMapEncodeTiled rejected a tensor map";
     return -1;
   }
@@ -891,17 +979,20 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if ((e = cudaMemsetAsync(p.chist, 0, (size_t)nch * p.E * 4, st))) return e;
   if ((e = cudaMemsetAsync(p.status, 0, 4, st))) return e;
   if (!p.route_only && (e = cudaMemsetAsync(p.Y, 0, (size_t)t * p.H * 4, st))) return e;
-  if ((e = cudaFuncSetAttribute(pf_gemm<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWsSmem)))
+  if ((e = cudaFuncSetAttribute(pf_gemm<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Lay<MODE_ROUTER>::smem)))
     return e;
-  if ((e = cudaFuncSetAttribute(pf_gemm<MODE_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWsSmem)))
+  if ((e = cudaFuncSetAttribute(pf_gemm<MODE_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Lay<MODE_GATE_UP>::smem)))
     return e;
-  if ((e = cudaFuncSetAttribute(pf_gemm<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kWsSmem))) return e;
+  if ((e = cudaFuncSetAttribute(pf_gemm<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay<MODE_DOWN>::smem)))
+    return e;
   const int ntr = ((p.E + 127) / 128) * ((t + 127) / 128);
   const int g_router = ntr < p.n_sms ? ntr : p.n_sms;
   if ((e = mark(0))) return e;
   pf_prep<<<t, 256, 0, st>>>(p);
   if ((e = mark(1))) return e;
-  pf_gemm<MODE_ROUTER><<<g_router, kWsThreads, kWsSmem, st>>>(p);
+  pf_gemm<MODE_ROUTER><<<g_router, kWsThreads, Lay<MODE_ROUTER>::smem, st>>>(p);
   if ((e = mark(2))) return e;
   pf_topk<<<(t + 7) / 8, 256, 0, st>>>(p);
   if ((e = mark(3))) return e;
@@ -914,9 +1005,9 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if (!p.route_only) {
     pf_gather<<<(int)((ent_cap + 7) / 8), 256, 0, st>>>(p);
     if ((e = mark(7))) return e;
-    pf_gemm<MODE_GATE_UP><<<p.n_sms, kWsThreads, kWsSmem, st>>>(p);
+    pf_gemm<MODE_GATE_UP><<<p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st>>>(p);
     if ((e = mark(8))) return e;
-    pf_gemm<MODE_DOWN><<<p.n_sms, kWsThreads, kWsSmem, st>>>(p);
+    pf_gemm<MODE_DOWN><<<p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st>>>(p);
     if ((e = mark(9))) return e;
     pf_final<<<1024, 256, 0, st>>>(p);
     if ((e = mark(10))) return e;

@@ -14,7 +14,7 @@ struct PfItem {
   uint64_t rec;         // the group's record address
 };
 
-constexpr int kPfTileN = 256;  // token columns per tensor-core tile
+constexpr int kPfTileN = 192;  // token columns per tensor-core tile
 constexpr int kPfChunk = 32;   // tokens per chunk of the stable grouping
 
 struct PfParams {
@@ -56,9 +56,9 @@ struct PfParams {
   float *wts;               // [t*(K+1)] its weight
   PfItem *items1, *items2;  // gate_up / down work lists
   int *nitems;              // [2]
-  uint16_t *hbuf;           // bf16 [t*(K+1)][I], k permuted within 8-blocks
+  uint16_t *hbuf;           // bf16 [I/64][t*(K+1)][64] (k-panels), k permuted within 8-blocks
   float *Y;                 // [t][H] fp32 accumulator
-  uint16_t *xc;             // bf16 [t*(K+1)][H]: xg rows in group order
+  uint16_t *xc;             // bf16 [H/64][t*(K+1)][64] (k-panels): xg rows in group order
 };
 
 constexpr int kPfStages = 10;  // kernels of one prefill call, in launch order

@@ -68,6 +68,53 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
       : "memory");
 }
 
+// One thread: D[tmem] (+)= A * B over k = 16 with A read from tensor memory
+// (128 lanes = rows; 8 consecutive 32-bit columns, two bf16 each, in k order).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Warp (converged): true in exactly one lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(r));
+  return r != 0;
+}
+
+// One thread: the four K=16 MMAs of a 64-wide k-stage, A in TMEM (columns
+// a, a+8, a+16, a+24), B from the 128B-swizzled K-major stage whose
+// descriptor is b_desc (each step moves 32 bytes along k: +2 in the
+// descriptor's address field).  accumulate: whether the first MMA adds to D.
+__device__ __forceinline__ void mma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.eq.b32 q, %4, %4;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, q;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, q;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(a_tmem + 8), "l"(b_desc + 2), "r"(a_tmem + 16),
+      "l"(b_desc + 4), "r"(a_tmem + 24), "l"(b_desc + 6)
+      : "memory");
+}
+
+// Warp: 16 consecutive 32-bit columns of the warp's 32 TMEM lanes from
+// registers, then wait until the stores have completed.
+__device__ __forceinline__ void st16_wait(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // One thread: arrive on the mbarrier once all MMAs issued so far complete.
 __device__ __forceinline__ void commit(uint64_t *bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
