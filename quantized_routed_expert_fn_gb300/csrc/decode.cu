@@ -38,7 +38,6 @@ namespace {
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int MAXIT = 4;
-constexpr int kTscWords = 2 * 16 * 33 > 2 * 8 * 65 ? 2 * 16 * 33 : 2 * 8 * 65;  // transposed scales of a unit
 constexpr int kProducerWarp = 1;  // issues the bulk copies (thread 0 does the cross-CTA releases)
 
 // Shared-memory row pitch of a staged code row of rb bytes (rows land
@@ -214,12 +213,12 @@ struct ColC {
 
 // One item: 16 weight rows (stage rows r0 .. r0+15) x one block of 128
 // inputs, for nh halves of the activation rows.  Codes come from the stage;
-// sc / bi point at the transposed scale / bias pairs of rows r0.. for this
-// block.  Returns per lane (t == 0 lanes after the sums) the outputs of rows
+// sc / bi point at the scale / bias pair word of row r0 for this block, the
+// words of the next rows `ss` words apart (the stage's [row][pair] tables).  Returns per lane (t == 0 lanes after the sums) the outputs of rows
 // g and g+8 for activation rows b = 2*half + {0,1}.
 template <int B, int NH>
 __device__ __forceinline__ void item_compute(const uint8_t *row_g, const uint8_t *row_g8, const uint32_t *sc,
-                                             const uint32_t *bi, int g, int y, const uint2 (&xb)[NH][8],
+                                             const uint32_t *bi, int ss, int g, int y, const uint2 (&xb)[NH][8],
                                              const ColC (&cc)[NH], float (&o)[NH][4]) {
   uint32_t wa[Codec<B>::kWords], wb[Codec<B>::kWords];
   if constexpr (B == 4) {
@@ -233,7 +232,7 @@ __device__ __forceinline__ void item_compute(const uint8_t *row_g, const uint8_t
     const uint32_t *pa = reinterpret_cast<const uint32_t *>(row_g), *pb = reinterpret_cast<const uint32_t *>(row_g8);
     wa[0] = pa[0], wa[1] = pa[1], wa[2] = pa[2], wb[0] = pb[0], wb[1] = pb[1], wb[2] = pb[2];
   }
-  const uint32_t sg = sc[g], sg8 = sc[g + 8], bg = bi[g], bg8 = bi[g + 8];
+  const uint32_t sg = sc[g * ss], sg8 = sc[(g + 8) * ss], bg = bi[g * ss], bg8 = bi[(g + 8) * ss];
   uint32_t fa[16], fb[16];
   Codec<B>::unpack(wa, fa);
   Codec<B>::unpack(wb, fb);
@@ -296,9 +295,10 @@ __device__ __forceinline__ ColC col_consts(float cs0, float cs1, float xs0, floa
 }
 
 // Items of a gate_up unit: (block kb, row tile 0 = the 16 gate rows, 1 = the
-// 16 up rows).  Writes red[(kb*2 + tile)*64 + row*4 + b].
+// 16 up rows).  sw: the unit's scale words [32][H/128], then its bias words.
+// Writes red[(kb*2 + tile)*64 + row*4 + b].
 template <int B, int NH>
-__device__ void gate_up_compute(const uint8_t *st, const uint32_t *T, int H, const uint2 *xb, const float *xs,
+__device__ void gate_up_compute(const uint8_t *st, const uint32_t *sw, int H, const uint2 *xb, const float *xs,
                                 const float *cs, int nb, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3, y = t >> 1;
@@ -317,14 +317,15 @@ __device__ void gate_up_compute(const uint8_t *st, const uint32_t *T, int H, con
     const int b0 = 2 * h, b1 = 2 * h + 1, grp = 2 * kb + y;
     cc[h] = col_consts(cs[b0 * ng + grp], cs[b1 * ng + grp], xs[b0 * ng + grp], xs[b1 * ng + grp], (t & 1) == 0);
   }
-  const uint32_t *sc = T + kb * 33, *bi = T + (np + kb) * 33;
+  const uint32_t *sc = sw + kb, *bi = sw + 32 * np + kb;
 #pragma unroll 1
   for (int k = 0; k < ipw; k++) {
     const int tile = (i0 & 1) + k;
     const int r0 = 16 * tile;
     float o[NH][4];
     item_compute<B, NH>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
-                        st + (r0 + g + 8) * rb + kb * (16 * B) + t * (4 * B), sc + r0, bi + r0, g, y, x, cc, o);
+                        st + (r0 + g + 8) * rb + kb * (16 * B) + t * (4 * B), sc + r0 * np, bi + r0 * np, np, g, y,
+                        x, cc, o);
     if (t == 0) {
       float *rp = red + (kb * 2 + tile) * 64;
 #pragma unroll
@@ -338,9 +339,10 @@ __device__ void gate_up_compute(const uint8_t *st, const uint32_t *T, int H, con
 
 // Items of a down unit: (block kb, row tile of 16 of the unit's 64 output
 // rows).  xb / xs / cs: the slot's h fragments and group sums, staged in
-// shared memory.  Writes red[(kb*4 + tile)*64 + row*4 + b].
+// shared memory.  sw: the unit's scale words [64][I/128], then its bias
+// words.  Writes red[(kb*4 + tile)*64 + row*4 + b].
 template <int B, int NH>
-__device__ void down_compute(const uint8_t *st, const uint32_t *T, int I, const uint2 *xb, const float *xs,
+__device__ void down_compute(const uint8_t *st, const uint32_t *sw, int I, const uint2 *xb, const float *xs,
                              const float *cs, int nb, float *red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3, y = t >> 1;
@@ -358,14 +360,15 @@ __device__ void down_compute(const uint8_t *st, const uint32_t *T, int I, const 
     const int b0 = 2 * h, b1 = 2 * h + 1, grp = 2 * kb + y;
     cc[h] = col_consts(cs[b0 * ng + grp], cs[b1 * ng + grp], xs[b0 * ng + grp], xs[b1 * ng + grp], (t & 1) == 0);
   }
-  const uint32_t *sc = T + kb * 65, *bi = T + (np + kb) * 65;
+  const uint32_t *sc = sw + kb, *bi = sw + 64 * np + kb;
 #pragma unroll 1
   for (int k = 0; k < ipw; k++) {
     const int tile = (i0 & 3) + k;
     const int r0 = 16 * tile;
     float o[NH][4];
     item_compute<B, NH>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
-                        st + (r0 + g + 8) * rb + kb * (16 * B) + t * (4 * B), sc + r0, bi + r0, g, y, x, cc, o);
+                        st + (r0 + g + 8) * rb + kb * (16 * B) + t * (4 * B), sc + r0 * np, bi + r0 * np, np, g, y,
+                        x, cc, o);
     if (t == 0) {
       float *rp = red + (kb * 4 + tile) * 64;
 #pragma unroll
@@ -587,19 +590,6 @@ __device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_
   }
 }
 
-// All threads: transpose the unit's scales and biases, [row][pair] u32
-// (two groups of a block per u32) -> T[which][pair][row] with row stride
-// rows + 1, so that an item's lanes read their rows without conflicts.
-__device__ void transpose_scales(const uint8_t *sd, int rows, int npair, uint32_t *T) {
-  const uint32_t *src = reinterpret_cast<const uint32_t *>(sd);
-  const int per = rows * npair;
-  for (int e = threadIdx.x; e < 2 * per; e += NT) {
-    const int which = e / per, rem = e - which * per;
-    const int r = rem / npair, kb = rem - r * npair;
-    T[(which * npair + kb) * (rows + 1) + r] = src[e];
-  }
-}
-
 // ------------------------------------------------------------ the kernel
 
 template <int BITS>
@@ -630,8 +620,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   volatile int *sflag = reinterpret_cast<volatile int *>(gam + 4);       // [12]
   uint64_t *bars = reinterpret_cast<uint64_t *>(gam + 16);               // [kMaxStages]
   const uint8_t **rect = reinterpret_cast<const uint8_t **>(bars + kMaxStages);  // [64] slot -> record
-  uint32_t *tsc = reinterpret_cast<uint32_t *>(rect + 64);                      // [1056] transposed scales
-  uint2 *hsm = reinterpret_cast<uint2 *>(tsc + kTscWords);                      // [I/128 * 256] h fragments
+  uint2 *hsm = reinterpret_cast<uint2 *>(rect + 64);                            // [I/128 * 256] h fragments
   float *hxs = reinterpret_cast<float *>(hsm + 8 * 256);                        // [4][I/64] sums of h
   float *hcs = hxs + 64;                                                        // [4][I/64] offset sums
   uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(hcs + 64);                   // [E] expert addresses
@@ -891,10 +880,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
       if (ok) {
         const int rows = d.down ? 64 : 32, inp = d.down ? I : H;
-        transpose_scales(st + rows * code_pitch(inp * d.bits / 8, d.bits), rows, inp / 128, tsc);
-      }
-      __syncthreads();
-      if (ok) {
+        const uint32_t *tsc = reinterpret_cast<const uint32_t *>(st + rows * code_pitch(inp * d.bits / 8, d.bits));
         const float *csx = shared && BITS != 4 ? cs4 : cs;
         const uint2 *xbx = shared ? xa4 : xa;
         if (!d.down) {
@@ -924,26 +910,15 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       }
       if (!d.down) {
         // h = silu(gate) * up for 16 rows x nb, scattered as bf16 hi/lo A
-        // fragments in the pair order of this slot's down codec
-        // lanes (row i of 32 = 16 gate + 16 up, b, kb-part): sums over the blocks
-        {
-          const int i = tid >> 4, kp = tid & 15;  // 512 threads = 32 rows x 16 parts
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int kb = kp; kb < nblkH; kb += 16) {
-            const float4 r4 = *reinterpret_cast<const float4 *>(&red[(kb * 2 + (i >> 4)) * 64 + (i & 15) * 4]);
-            acc[0] += r4.x, acc[1] += r4.y, acc[2] += r4.z, acc[3] += r4.w;
-          }
-#pragma unroll
-          for (int b = 0; b < 4; b++)
-#pragma unroll
-            for (int o = 8; o; o >>= 1) acc[b] += __shfl_xor_sync(FULL, acc[b], o);
-          __syncthreads();
-          if (kp == 0) *reinterpret_cast<float4 *>(&red[i * 4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-          __syncthreads();
-        }
+        // fragments in the pair order of this slot's down codec; thread
+        // (i, b) sums its gate and up rows over the blocks in block order
         if (tid < 16 * nb) {
           const int i = tid & 15, b = tid >> 4;
-          const float gsum = red[i * 4 + b], usum = red[(16 + i) * 4 + b];
+          float gsum = 0.f, usum = 0.f;
+          for (int kb = 0; kb < nblkH; kb++) {
+            gsum += red[(kb * 2) * 64 + i * 4 + b];
+            usum += red[(kb * 2 + 1) * 64 + i * 4 + b];
+          }
           const float h = ok ? gsum / (1.f + expf(-gsum)) * usum : 0.f;
           const int pos = d.row0 + i;
           const int blk = pos >> 7, c = pos & 127, tq = c >> 5, cc = c & 31;
@@ -1021,7 +996,6 @@ static int fixed_smem(int H, int E, int bits) {
   b += (128 + 128 + 64 + 256 + 16) * 4;            // sidx sw uni wm gam+flags
   b += kMaxStages * 8;                             // barriers
   b += 64 * 8;                                     // slot -> record table
-  b += kTscWords * 4;                              // transposed scales
   b += 8 * 256 * 8 + 2 * 64 * 4;                   // staged h fragments and sums
   b += ((E + 1) & ~1) * 8;                         // expert addresses
   return b;
