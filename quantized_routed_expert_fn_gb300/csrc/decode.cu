@@ -39,6 +39,12 @@ constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int MAXIT = 4;
 constexpr int kProducerWarp = 1;  // issues the bulk copies (thread 0 does the cross-CTA releases)
+// The weight units of a layer go to two groups of eight warps in turn (unit q
+// to group q % 2), so that one group's reductions, global writes and
+// releases overlap the other group's tensor-core work.
+constexpr int kGroups = 2;
+constexpr int GT = NT / kGroups;  // threads of a group
+constexpr int GW = GT / 32;       // warps of a group
 
 // Shared-memory row pitch of a staged code row of rb bytes (rows land
 // contiguously: one bulk copy per block of rows).
@@ -104,6 +110,32 @@ __device__ void cta_signal(unsigned *p, unsigned v) {
   if (threadIdx.x == 0) red_release_add(p, v);
 }
 
+// Unit group g (threads GT*g .. GT*g+GT-1): barrier 1 + g, and the same with
+// an AND over a predicate.
+__device__ __forceinline__ void grp_sync(int g) { asm volatile("bar.sync %0, %1;" ::"r"(1 + g), "r"(GT) : "memory"); }
+__device__ __forceinline__ bool grp_and(int g, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(1 + g), "r"(GT)
+      : "memory");
+  return r != 0;
+}
+
+// Group g: cta_wait / cta_signal for one unit group (gt: thread index in it).
+__device__ bool grp_wait(const unsigned *p, unsigned target, const FwdParams &P, volatile int *flag, int g, int gt) {
+  if (gt == 0) *flag = wait_geq(p, target, P);
+  grp_sync(g);
+  const bool ok = *flag;
+  grp_sync(g);
+  return ok;
+}
+__device__ void grp_signal(unsigned *p, unsigned v, int g, int gt) {
+  grp_sync(g);
+  if (gt == 0) red_release_add(p, v);
+}
+
 // All threads: wait for ring stage `u` (its copies landed).  A wait that
 // passes the deadline records MOE_ETIMEOUT and keeps waiting (the copies
 // in flight target this CTA's shared memory) for up to one more deadline.
@@ -124,11 +156,22 @@ __device__ bool stage_wait(uint64_t *bar, uint32_t parity, const FwdParams &P) {
 
 // Thread 0, on an error return: wait (bounded) for the copies still in
 // flight into this CTA's ring, units [from, to) of the call's sequence.
+// (drain_stages: the same for the last unit issued into each stage.)
 __device__ void drain_ring(uint64_t *bars, unsigned from, unsigned to, int S, const FwdParams &P) {
   if (threadIdx.x != 0) return;  // any one thread keeps the CTA (and its ring) alive until the copies land
   for (unsigned u = from; u < to; u++) {
     const uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&bars[u % S], (u / S) & 1u))
+      if (globaltimer() - t0 > P.timeout_ns) return;
+  }
+}
+
+__device__ void drain_stages(uint64_t *bars, const unsigned *last, int S, const FwdParams &P) {
+  if (threadIdx.x != 0) return;
+  for (int s = 0; s < S; s++) {
+    if (last[s] == 0xffffffffu) continue;
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(&bars[s], (last[s] / S) & 1u))
       if (globaltimer() - t0 > P.timeout_ns) return;
   }
 }
@@ -262,14 +305,6 @@ __device__ __forceinline__ void item_compute(const uint8_t *row_g, const uint8_t
   }
 }
 
-// items per warp: the smallest power of two covering all items, capped at ntiles
-__device__ __forceinline__ int items_per_warp(int nitems, int ntiles) {
-  const int need = (nitems + NW - 1) / NW;
-  int ipw = 1;
-  while (ipw < need) ipw *= 2;
-  return ipw < ntiles ? ipw : ntiles;
-}
-
 // B registers of lane (g, t) for one block and half: its column's entry if
 // the column belongs to the lane's group, else zero.
 template <int NH>
@@ -297,18 +332,17 @@ __device__ __forceinline__ ColC col_consts(float cs0, float cs1, float xs0, floa
 // Items of a gate_up unit: (block kb, row tile 0 = the 16 gate rows, 1 = the
 // 16 up rows).  sw: the unit's scale words [32][H/128], then its bias words.
 // Writes red[(kb*2 + tile)*64 + row*4 + b].
+// Warp wi of nw takes blocks wi, wi + nw, ... (both tiles of a block share
+// its activation registers).
 template <int B, int NH>
 __device__ void gate_up_compute(const uint8_t *st, const uint32_t *sw, int H, const uint2 *xb, const float *xs,
-                                const float *cs, int nb, float *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+                                const float *cs, int nb, float *red, int wi, int nw) {
+  const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3, y = t >> 1;
   const int nblk = H / 128;
-  const int nitems = nblk * 2;
-  const int ipw = items_per_warp(nitems, 2);
-  const int i0 = warp * ipw;
-  if (i0 >= nitems) return;
-  const int kb = i0 >> 1;
   const int rb = H * B / 8, np = H / 128, ng = H / 64;
+#pragma unroll 1
+  for (int kb = wi; kb < nblk; kb += nw) {
   uint2 x[NH][8];
   ColC cc[NH];
   load_bfrag<NH>(xb, kb, lane, x);
@@ -319,8 +353,7 @@ __device__ void gate_up_compute(const uint8_t *st, const uint32_t *sw, int H, co
   }
   const uint32_t *sc = sw + kb, *bi = sw + 32 * np + kb;
 #pragma unroll 1
-  for (int k = 0; k < ipw; k++) {
-    const int tile = (i0 & 1) + k;
+  for (int tile = 0; tile < 2; tile++) {
     const int r0 = 16 * tile;
     float o[NH][4];
     item_compute<B, NH>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
@@ -335,23 +368,25 @@ __device__ void gate_up_compute(const uint8_t *st, const uint32_t *sw, int H, co
       }
     }
   }
+  }
 }
 
 // Items of a down unit: (block kb, row tile of 16 of the unit's 64 output
 // rows).  xb / xs / cs: the slot's h fragments and group sums, staged in
 // shared memory.  sw: the unit's scale words [64][I/128], then its bias
 // words.  Writes red[(kb*4 + tile)*64 + row*4 + b].
+// Warp wi of nw takes passes wi, wi + nw, ... of two row tiles of one
+// block (pass p: block p / 2, tiles 2 (p % 2) and 2 (p % 2) + 1).
 template <int B, int NH>
 __device__ void down_compute(const uint8_t *st, const uint32_t *sw, int I, const uint2 *xb, const float *xs,
-                             const float *cs, int nb, float *red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+                             const float *cs, int nb, float *red, int wi, int nw) {
+  const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3, y = t >> 1;
-  const int nitems = (I / 128) * 4;
-  const int ipw = items_per_warp(nitems, 4);
-  const int i0 = warp * ipw;
-  if (i0 >= nitems) return;
-  const int kb = i0 >> 2;
+  const int npass = (I / 128) * 2;
   const int rb = I * B / 8, np = I / 128, ng = I / 64;
+#pragma unroll 1
+  for (int pass = wi; pass < npass; pass += nw) {
+  const int kb = pass >> 1;
   uint2 x[NH][8];
   ColC cc[NH];
   load_bfrag<NH>(xb, kb, lane, x);
@@ -362,8 +397,8 @@ __device__ void down_compute(const uint8_t *st, const uint32_t *sw, int I, const
   }
   const uint32_t *sc = sw + kb, *bi = sw + 64 * np + kb;
 #pragma unroll 1
-  for (int k = 0; k < ipw; k++) {
-    const int tile = (i0 & 3) + k;
+  for (int k = 0; k < 2; k++) {
+    const int tile = 2 * (pass & 1) + k;
     const int r0 = 16 * tile;
     float o[NH][4];
     item_compute<B, NH>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
@@ -378,20 +413,21 @@ __device__ void down_compute(const uint8_t *st, const uint32_t *sw, int I, const
       }
     }
   }
+  }
 }
 
-// All threads: bring one slot's h fragments into shared memory and form its
-// per-group sums: hxs = sum of h (bias term), hcs = 128 * sum of 2^-s h as the
+// One unit group (g; gt: thread index in it): bring one slot's h fragments
+// into shared memory and form its per-group sums: hxs = sum of h (bias term), hcs = 128 * sum of 2^-s h as the
 // MMA sees it (offset), [b][I/64].  Codec C is the slot's down codec.
 template <int C>
-__device__ void stage_h(const uint2 *hf, int I, int nb, uint2 *hsm, float *hxs, float *hcs) {
+__device__ void stage_h(const uint2 *hf, int I, int nb, uint2 *hsm, float *hxs, float *hcs, int g, int gt) {
   const int nblk = I / 128;
   const int n = nblk * 256;
-  for (int i = threadIdx.x; i < n; i += NT) hsm[i] = __ldcg(hf + i);
-  __syncthreads();
+  for (int i = gt; i < n; i += GT) hsm[i] = __ldcg(hf + i);
+  grp_sync(g);
   // thread (kb, y, b, part): 4 of the 32 entries (t in {2y, 2y+1}, m, hl) of a group
   const int ng = I / 64;
-  for (int j = threadIdx.x; j < nblk * 64; j += NT) {
+  for (int j = gt; j < nblk * 64; j += GT) {
     const int part = j & 7, b = (j >> 3) & 3, y = (j >> 5) & 1, kb = j >> 6;
     float ssc = 0.f, sun = 0.f;
     if (b < nb) {
@@ -604,15 +640,15 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   const int S = P.stages;
 
   uint8_t *stages = sm;                                                  // [S][stage_bytes]
-  float *xf = reinterpret_cast<float *>(sm + (size_t)S * P.stage_bytes);  // [4][H]
-  uint2 *xa = reinterpret_cast<uint2 *>(xf + 4 * H);                     // [nblkH][8][32] routed codec order
+  float *xf = reinterpret_cast<float *>(sm + (size_t)S * P.stage_bytes);  // [nb][H]
+  uint2 *xa = reinterpret_cast<uint2 *>(xf + nb * H);                    // [nblkH][8][32] routed codec order
   uint2 *xa4 = BITS == 4 ? xa : xa + nblkH * 256;                        // shared (4-bit) order
   float *xs = reinterpret_cast<float *>(xa4 + nblkH * 256);              // [4][H/64] group sums of x
   float *cs = xs + 4 * ng;                                               // [4][H/64] offset sums, routed order
   float *cs4 = cs + 4 * ng;                                              // [4][H/64] offset sums, 4-bit order
   float *lg = cs4 + 4 * ng;                                              // [4][E1]
-  float *red = lg + 4 * E1;                                              // [2048]
-  int *sidx = reinterpret_cast<int *>(red + 2048);                       // [4][32]
+  float *red = lg + 4 * E1;                                              // [2][2048]: one per unit group
+  int *sidx = reinterpret_cast<int *>(red + 2 * 2048);                   // [4][32]
   float *sw = reinterpret_cast<float *>(sidx + 128);                     // [4][32]
   int *uni = reinterpret_cast<int *>(sw + 128);                          // [64]
   float *wm = reinterpret_cast<float *>(uni + 64);                       // [4][64]
@@ -620,16 +656,22 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   volatile int *sflag = reinterpret_cast<volatile int *>(gam + 4);       // [12]
   uint64_t *bars = reinterpret_cast<uint64_t *>(gam + 16);               // [kMaxStages]
   const uint8_t **rect = reinterpret_cast<const uint8_t **>(bars + kMaxStages);  // [64] slot -> record
-  uint2 *hsm = reinterpret_cast<uint2 *>(rect + 64);                            // [I/128 * 256] h fragments
-  float *hxs = reinterpret_cast<float *>(hsm + 8 * 256);                        // [4][I/64] sums of h
-  float *hcs = hxs + 64;                                                        // [4][I/64] offset sums
-  uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(hcs + 64);                   // [E] expert addresses
+  // per unit group: staged h fragments [I/128 * 256], their sums [4][I/64], offset sums [4][I/64]
+  uint2 *hsm = reinterpret_cast<uint2 *>(rect + 64);
+  const int hsz = nblkI * 256 * 2 + 2 * 64;  // 32-bit words per group
+  uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(reinterpret_cast<uint32_t *>(hsm) + 2 * hsz);  // [E]
+  unsigned *stg_unit = reinterpret_cast<unsigned *>(eaddr_s + ((E + 1) & ~1));  // [S] last unit issued per stage
 
   if (tid == 0) {
-    for (int s = 0; s < S; s++) mbar_init(&bars[s], 1);
+    for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu;
     fence_mbar_init();
   }
   __syncthreads();
+  // warp lane 0 of an issuing warp: unit q of the layer into its ring stage
+  auto issue_at = [&](const UnitDesc &d, unsigned u) {
+    issue_unit(d, H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S], P.status);
+    if (lane == 0) stg_unit[u % S] = u;
+  };
 
   unsigned qbase = 0;  // units requested so far in this call (ring position)
   for (int l = 0; l < P.nl; l++) {
@@ -637,6 +679,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   if (P.trace && tid == 0 && cta < kTraceCtas)                                                   \
     P.trace[((size_t)l * kTraceCtas + cta) * kTracePhases + (k)] = globaltimer();
     MOE_STAMP(0)
+    if (l == 0 && tid == 0) sflag[8] = 0;
     const LayerP &L = P.L[l];
     unsigned *cnt = P.cnt + (size_t)l * kCntPerLayer;
     const bool hs = L.sgate != nullptr;
@@ -654,11 +697,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.U = 0;
     int issued = 0;
     if (warp == kProducerWarp) {
-      for (; issued < s.nA && issued < S; issued++) {
-        const unsigned u = qbase + issued;
-        issue_unit(get_unit<BITS>(issued, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes,
-                   &bars[u % S], P.status);
-      }
+      for (; issued < s.nA && issued < S; issued++) issue_at(get_unit<BITS>(issued, s, L, rect), qbase + issued);
     }
     issued = s.nA < S ? s.nA : S;
 
@@ -713,7 +752,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
 #pragma unroll
       for (int k = 0; k < 4; k++) {
         const int i = tid + k * NT;
-        if (i < H) xf4[i] = v[k];  // rows b >= nb hold zeros
+        if (i < n4) xf4[i] = v[k];
       }
     }
     __syncthreads();
@@ -833,148 +872,160 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.nD = fdiv_mul(cta + 1, ND, G) - s.d0;
     const int n = s.n();
     if (warp == kProducerWarp) {
-      for (int q = issued; q < n && q < S; q++) {
-        const unsigned u = qbase + q;
-        issue_unit(get_unit<BITS>(q, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
-                   P.status);
-      }
+      for (int q = issued; q < n && q < S; q++) issue_at(get_unit<BITS>(q, s, L, rect), qbase + q);
     }
     issued = n < S ? n : S;
 
-    // ---- G + D: the unit loop
+    // ---- G + D: the unit loop, unit q to group q % 2
     MOE_STAMP(5)
-    int cur = -1;
-    for (int q = 0; q < n; q++) {
-      if (q == s.nA + s.nB) {
-        MOE_STAMP(6)
-        if (tid == 0 && l + 1 < P.nl) {
-          // the next layer's router rows of this CTA, toward L2 while the down units run
-          const LayerP &Ln = P.L[l + 1];
-          const int re = rr1 < E ? rr1 : E;
-          if (re > rr0) prefetch_l2(Ln.router + (size_t)rr0 * H, (uint32_t)((re - rr0) * H * 2));
-          if (rr1 > E && Ln.sgate) prefetch_l2(Ln.sgate, (uint32_t)(H * 2));
+    {
+      const int grp = warp / GW, gw = warp % GW, gt = tid % GT;
+      float *gred = red + grp * 2048;
+      uint2 *ghsm = reinterpret_cast<uint2 *>(reinterpret_cast<uint32_t *>(hsm) + grp * hsz);
+      float *ghxs = reinterpret_cast<float *>(ghsm + nblkI * 256), *ghcs = ghxs + 64;
+      volatile int *gflag = sflag + 4 + 2 * grp;  // [0]: wait outcome, [1]: last-unit ticket
+      int cur = -1;
+      bool alive = true;
+      // stamp k from whichever group runs the unit
+#define MOE_GSTAMP(k)                                                                            \
+  if (P.trace && gt == 0 && cta < kTraceCtas)                                                    \
+    P.trace[((size_t)l * kTraceCtas + cta) * kTracePhases + (k)] = globaltimer();
+      for (int q = grp; q < n && alive; q += kGroups) {
+        if (q == s.nA + s.nB) {
+          MOE_GSTAMP(6)
+          if (gt == 0 && l + 1 < P.nl) {
+            // the next layer's router rows of this CTA, toward L2 while the down units run
+            const LayerP &Ln = P.L[l + 1];
+            const int re = rr1 < E ? rr1 : E;
+            if (re > rr0) prefetch_l2(Ln.router + (size_t)rr0 * H, (uint32_t)((re - rr0) * H * 2));
+            if (rr1 > E && Ln.sgate) prefetch_l2(Ln.sgate, (uint32_t)(H * 2));
+          }
         }
-      }
-      const UnitDesc d = get_unit<BITS>(q, s, L, rect);
-      const unsigned u = qbase + q;
-      const uint8_t *st = stages + (size_t)(u % S) * P.stage_bytes;
-      const bool shared = s.hsi && d.slot == 0;
-      if (d.down && d.slot != cur) {
-        // h of this slot complete?  then stage its fragments and group sums
-        if (!cta_wait(cnt + kCntGu + d.slot, (unsigned)s.ups, P, sflag)) {
-          drain_ring(bars, u, qbase + (unsigned)(q + S < n ? q + S : n), S, P);
-          return;
+        const UnitDesc d = get_unit<BITS>(q, s, L, rect);
+        const unsigned u = qbase + q;
+        const uint8_t *st = stages + (size_t)(u % S) * P.stage_bytes;
+        const bool shared = s.hsi && d.slot == 0;
+        if (d.down && d.slot != cur) {
+          // h of this slot complete?  then stage its fragments and group sums
+          if (!grp_wait(cnt + kCntGu + d.slot, (unsigned)s.ups, P, gflag, grp, gt)) {
+            alive = false;
+            break;
+          }
+          cur = d.slot;
+          const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag) + (size_t)d.slot * nblkI * 256;
+          if (shared || BITS == 4)
+            stage_h<4>(hf, I, nb, ghsm, ghxs, ghcs, grp, gt);
+          else
+            stage_h<BITS>(hf, I, nb, ghsm, ghxs, ghcs, grp, gt);
         }
-        cur = d.slot;
-        const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag) + (size_t)d.slot * nblkI * 256;
-        if (shared || BITS == 4)
-          stage_h<4>(hf, I, nb, hsm, hxs, hcs);
-        else
-          stage_h<BITS>(hf, I, nb, hsm, hxs, hcs);
-      }
-      if (!__syncthreads_and(stage_wait(&bars[u % S], (u / S) & 1u, P))) {
-        drain_ring(bars, u + 1, qbase + (unsigned)(q + S < n ? q + S : n), S, P);
-        return;
-      }
-      if (q == 0) MOE_STAMP(11)
-      const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
-      if (ok) {
-        const int rows = d.down ? 64 : 32, inp = d.down ? I : H;
-        const uint32_t *tsc = reinterpret_cast<const uint32_t *>(st + rows * code_pitch(inp * d.bits / 8, d.bits));
-        const float *csx = shared && BITS != 4 ? cs4 : cs;
-        const uint2 *xbx = shared ? xa4 : xa;
-        if (!d.down) {
-          if (nb <= 2) {
-            if (shared) gate_up_compute<4, 1>(st, tsc, H, xbx, xs, csx, nb, red);
-            else gate_up_compute<BITS, 1>(st, tsc, H, xbx, xs, csx, nb, red);
+        if (!grp_and(grp, stage_wait(&bars[u % S], (u / S) & 1u, P))) {
+          alive = false;
+          break;
+        }
+        if (q == 0) MOE_STAMP(11)
+        const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
+        if (ok) {
+          const int rows = d.down ? 64 : 32, inp = d.down ? I : H;
+          const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + rows * code_pitch(inp * d.bits / 8, d.bits));
+          const float *csx = shared && BITS != 4 ? cs4 : cs;
+          const uint2 *xbx = shared ? xa4 : xa;
+          if (!d.down) {
+            if (nb <= 2) {
+              if (shared) gate_up_compute<4, 1>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              else gate_up_compute<BITS, 1>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+            } else {
+              if (shared) gate_up_compute<4, 2>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              else gate_up_compute<BITS, 2>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+            }
           } else {
-            if (shared) gate_up_compute<4, 2>(st, tsc, H, xbx, xs, csx, nb, red);
-            else gate_up_compute<BITS, 2>(st, tsc, H, xbx, xs, csx, nb, red);
-          }
-        } else {
-          if (nb <= 2) {
-            if (shared) down_compute<4, 1>(st, tsc, I, hsm, hxs, hcs, nb, red);
-            else down_compute<BITS, 1>(st, tsc, I, hsm, hxs, hcs, nb, red);
-          } else {
-            if (shared) down_compute<4, 2>(st, tsc, I, hsm, hxs, hcs, nb, red);
-            else down_compute<BITS, 2>(st, tsc, I, hsm, hxs, hcs, nb, red);
-          }
-        }
-      }
-      __syncthreads();
-      if (q == 0) MOE_STAMP(12)
-      // the stage is free: request the unit S places ahead into it
-      if (warp == kProducerWarp && q + S < n) {
-        issue_unit(get_unit<BITS>(q + S, s, L, rect), H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S],
-                   P.status);
-      }
-      if (!d.down) {
-        // h = silu(gate) * up for 16 rows x nb, scattered as bf16 hi/lo A
-        // fragments in the pair order of this slot's down codec; thread
-        // (i, b) sums its gate and up rows over the blocks in block order
-        if (tid < 16 * nb) {
-          const int i = tid & 15, b = tid >> 4;
-          float gsum = 0.f, usum = 0.f;
-          for (int kb = 0; kb < nblkH; kb++) {
-            gsum += red[(kb * 2) * 64 + i * 4 + b];
-            usum += red[(kb * 2 + 1) * 64 + i * 4 + b];
-          }
-          const float h = ok ? gsum / (1.f + expf(-gsum)) * usum : 0.f;
-          const int pos = d.row0 + i;
-          const int blk = pos >> 7, c = pos & 127, tq = c >> 5, cc = c & 31;
-          int pi = 0, el = 0, sh = 0;
-#pragma unroll
-          for (int p = 0; p < 16; p++) {
-            const bool c4 = shared || BITS == 4;
-            const int lo = c4 ? Codec<4>::lo(p) : Codec<BITS>::lo(p);
-            const int hi = c4 ? Codec<4>::hi(p) : Codec<BITS>::hi(p);
-            if (lo == cc) pi = p, el = 0, sh = c4 ? Codec<4>::slo(p) : Codec<BITS>::slo(p);
-            if (hi == cc) pi = p, el = 1, sh = c4 ? Codec<4>::shi(p) : Codec<BITS>::shi(p);
-          }
-          const float hv = h * __uint_as_float((uint32_t)(127 - sh) << 23);  // h * 2^-sh, exact
-          const uint32_t hi = f2bf(hv), lo = f2bf(hv - __uint_as_float(hi << 16));
-          uint16_t *hb = P.hfrag + (size_t)d.slot * nblkI * 256 * 4;
-          const int m = pi >> 1, reg = pi & 1;
-          hb[frag_index(blk, b >> 1, m, tq, 0, b & 1) * 4 + reg * 2 + el] = (uint16_t)hi;
-          hb[frag_index(blk, b >> 1, m, tq, 1, b & 1) * 4 + reg * 2 + el] = (uint16_t)lo;
-        }
-        cta_signal(cnt + kCntGu + d.slot, 1u);
-        if (q == 0) MOE_STAMP(13)
-        if (q == s.nA + s.nB - 1) MOE_STAMP(14)
-      } else {
-        const int rt = d.row0 / 64;
-        for (int j = tid; j < 64 * nb; j += NT) {
-          const int r = j & 63, b = j >> 6;
-          float y = 0.f;
-          if (ok)
-            for (int kb = 0; kb < nblkI; kb++) y += red[(kb * 4 + (r >> 4)) * 64 + (r & 15) * 4 + b];
-          const float mb = shared ? gam[b] : wm[b * 64 + d.slot - s.hsi];
-          P.ypart[((size_t)d.slot * nb + b) * H + d.row0 + r] = mb * y;
-        }
-        __syncthreads();
-        if (tid == 0) sflag[2] = atom_acq_rel_add(cnt + kCntDn + rt, 1u) == (unsigned)(s.nslots - 1);
-        __syncthreads();
-        if (sflag[2]) {
-          // last unit of this 64-row range: sum the slots in a fixed order
-          const int tpo = nb == 1 ? 8 : (nb == 2 ? 4 : 2);
-          for (int j = tid; j < 64 * nb * tpo; j += NT) {
-            const int o = j / tpo, part = j % tpo;
-            const int r = o & 63, b = o >> 6;
-            const float *yp = P.ypart + (size_t)b * H + d.row0 + r;
-            float acc = 0.f;
-#pragma unroll 4
-            for (int sl = part; sl < s.nslots; sl += tpo) acc += __ldcg(yp + (size_t)sl * nb * H);
-            for (int off = tpo >> 1; off; off >>= 1) acc += __shfl_down_sync(FULL, acc, off, tpo);
-            if (part == 0) {
-              if (L.flags & kResidual) acc += __ldcg(src + (size_t)b * H + d.row0 + r);
-              dst[(size_t)b * H + d.row0 + r] = acc;
+            if (nb <= 2) {
+              if (shared) down_compute<4, 1>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              else down_compute<BITS, 1>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+            } else {
+              if (shared) down_compute<4, 2>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              else down_compute<BITS, 2>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
             }
           }
-          cta_signal(cnt + kCntRows, 1u);
         }
-        __syncthreads();
-        if (q == s.nA + s.nB) MOE_STAMP(15)
+        grp_sync(grp);
+        if (q == 0) MOE_STAMP(12)
+        // the stage is free: request the unit S places ahead into it
+        if (gw == kProducerWarp && q + S < n) issue_at(get_unit<BITS>(q + S, s, L, rect), u + S);
+        if (!d.down) {
+          // h = silu(gate) * up for 16 rows x nb, scattered as bf16 hi/lo A
+          // fragments in the pair order of this slot's down codec; thread
+          // (i, b) sums its gate and up rows over the blocks in block order
+          if (gt < 16 * nb) {
+            const int i = gt & 15, b = gt >> 4;
+            float gsum = 0.f, usum = 0.f;
+            for (int kb = 0; kb < nblkH; kb++) {
+              gsum += gred[(kb * 2) * 64 + i * 4 + b];
+              usum += gred[(kb * 2 + 1) * 64 + i * 4 + b];
+            }
+            const float h = ok ? gsum / (1.f + expf(-gsum)) * usum : 0.f;
+            const int pos = d.row0 + i;
+            const int blk = pos >> 7, c = pos & 127, tq = c >> 5, cc = c & 31;
+            int pi = 0, el = 0, sh = 0;
+#pragma unroll
+            for (int p = 0; p < 16; p++) {
+              const bool c4 = shared || BITS == 4;
+              const int lo = c4 ? Codec<4>::lo(p) : Codec<BITS>::lo(p);
+              const int hi = c4 ? Codec<4>::hi(p) : Codec<BITS>::hi(p);
+              if (lo == cc) pi = p, el = 0, sh = c4 ? Codec<4>::slo(p) : Codec<BITS>::slo(p);
+              if (hi == cc) pi = p, el = 1, sh = c4 ? Codec<4>::shi(p) : Codec<BITS>::shi(p);
+            }
+            const float hv = h * __uint_as_float((uint32_t)(127 - sh) << 23);  // h * 2^-sh, exact
+            const uint32_t hi = f2bf(hv), lo = f2bf(hv - __uint_as_float(hi << 16));
+            uint16_t *hb = P.hfrag + (size_t)d.slot * nblkI * 256 * 4;
+            const int m = pi >> 1, reg = pi & 1;
+            hb[frag_index(blk, b >> 1, m, tq, 0, b & 1) * 4 + reg * 2 + el] = (uint16_t)hi;
+            hb[frag_index(blk, b >> 1, m, tq, 1, b & 1) * 4 + reg * 2 + el] = (uint16_t)lo;
+          }
+          grp_signal(cnt + kCntGu + d.slot, 1u, grp, gt);
+          if (q == 0) MOE_STAMP(13)
+          if (q == s.nA + s.nB - 1) MOE_GSTAMP(14)
+        } else {
+          const int rt = d.row0 / 64;
+          for (int j = gt; j < 64 * nb; j += GT) {
+            const int r = j & 63, b = j >> 6;
+            float y = 0.f;
+            if (ok)
+              for (int kb = 0; kb < nblkI; kb++) y += gred[(kb * 4 + (r >> 4)) * 64 + (r & 15) * 4 + b];
+            const float mb = shared ? gam[b] : wm[b * 64 + d.slot - s.hsi];
+            P.ypart[((size_t)d.slot * nb + b) * H + d.row0 + r] = mb * y;
+          }
+          grp_sync(grp);
+          if (gt == 0) gflag[1] = atom_acq_rel_add(cnt + kCntDn + rt, 1u) == (unsigned)(s.nslots - 1);
+          grp_sync(grp);
+          if (gflag[1]) {
+            // last unit of this 64-row range: sum the slots in a fixed order
+            const int tpo = nb == 1 ? 8 : (nb == 2 ? 4 : 2);
+            for (int j = gt; j < 64 * nb * tpo; j += GT) {
+              const int o = j / tpo, part = j % tpo;
+              const int r = o & 63, b = o >> 6;
+              const float *yp = P.ypart + (size_t)b * H + d.row0 + r;
+              float acc = 0.f;
+#pragma unroll 4
+              for (int sl = part; sl < s.nslots; sl += tpo) acc += __ldcg(yp + (size_t)sl * nb * H);
+              for (int off = tpo >> 1; off; off >>= 1) acc += __shfl_down_sync(FULL, acc, off, tpo);
+              if (part == 0) {
+                if (L.flags & kResidual) acc += __ldcg(src + (size_t)b * H + d.row0 + r);
+                dst[(size_t)b * H + d.row0 + r] = acc;
+              }
+            }
+            grp_signal(cnt + kCntRows, 1u, grp, gt);
+          }
+          grp_sync(grp);
+          if (q == s.nA + s.nB) MOE_GSTAMP(15)
+        }
       }
+      if (!alive) sflag[8] = 1;
+#undef MOE_GSTAMP
+    }
+    __syncthreads();  // both groups are done with the layer's units
+    if (sflag[8]) {
+      drain_stages(bars, stg_unit, S, P);
+      return;
     }
     qbase += (unsigned)n;
     MOE_STAMP(7)
@@ -984,20 +1035,21 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
 
 }  // namespace
 
-static int fixed_smem(int H, int E, int bits) {
+static int fixed_smem(int H, int E, int I, int nb, int bits) {
   const int nblkH = H / 128;
   const int E1 = (E + 1 + 3) & ~3;
   int b = 0;
-  b += 4 * H * 4;                                  // xf
+  b += nb * H * 4;                                 // xf
   b += nblkH * 256 * 8 * (bits == 4 ? 1 : 2);      // xa (+ xa4)
   b += 3 * 4 * (H / 64) * 4;                       // xs, cs, cs4
   b += 4 * E1 * 4;                                 // lg
-  b += 2048 * 4;                                   // red
+  b += 2 * 2048 * 4;                               // red, one per unit group
   b += (128 + 128 + 64 + 256 + 16) * 4;            // sidx sw uni wm gam+flags
   b += kMaxStages * 8;                             // barriers
   b += 64 * 8;                                     // slot -> record table
-  b += 8 * 256 * 8 + 2 * 64 * 4;                   // staged h fragments and sums
+  b += 2 * ((I / 128) * 256 * 8 + 2 * 64 * 4);     // staged h fragments and sums, one per unit group
   b += ((E + 1) & ~1) * 8;                         // expert addresses
+  b += kMaxStages * 4;                             // last unit issued per stage
   return b;
 }
 
@@ -1022,7 +1074,7 @@ int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes) {
   int sms = 0, optin = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return -1;
   if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) return -1;
-  const int fixed = fixed_smem(p.H, p.E, p.bits);
+  const int fixed = fixed_smem(p.H, p.E, p.I, p.nb, p.bits);
   const int sb = stage_bytes(p.H, p.I);
   int S = (optin - fixed) / sb;
   if (S > kMaxStages) S = kMaxStages;
