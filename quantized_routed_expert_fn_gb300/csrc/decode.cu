@@ -186,11 +186,13 @@ __device__ void drain_stages(uint64_t *bars, const unsigned *last, int S, const 
 // of activation rows b = 2*half + bb; B is zero where the k-slot belongs to
 // the other group, so each column sums exactly one 64-code group.
 
-// Thread (blk, t, b) turns the 32 inputs x[b][blk*128 + 32t .. +32) into the
-// nonzero B registers of the lanes (col, t) with col in group t/2, for the 8
-// MMA steps, in codec B's pair order, each input pre-scaled by the 2^-s of
-// its pair half (exact).  Per 64-input group: xs = sum of x (bias term),
-// cs = 128 * sum of 2^-s x (the offset the codes carry).
+// Thread pair (blk, t, b) turns the 32 inputs x[b][blk*128 + 32t .. +32) into
+// the nonzero B registers of the lanes (col, t) with col in group t/2, for
+// the 8 MMA steps (thread hh of the pair: steps 4hh .. 4hh+3), in codec B's
+// pair order, each input pre-scaled by the 2^-s of its pair half (exact).
+// Per 64-input group: xs = sum of x (bias term), cs = 128 * sum of 2^-s x
+// (the offset the codes carry).  Rows b >= nb are never written here: their
+// registers and sums stay at the zeros set when the kernel starts.
 // Compact layout (the other group's zero columns are not stored):
 // xb[blk][half][m][t][hl][bb], uint2 = k-slots (2t,2t+1), (2t+8,2t+9).
 __device__ __forceinline__ int frag_index(int blk, int half, int m, int t, int hl, int bb) {
@@ -198,46 +200,60 @@ __device__ __forceinline__ int frag_index(int blk, int half, int m, int t, int h
 }
 template <int B>
 __device__ void stage_frags(const float *xf, int H, int nb, uint2 *xb, float *xs, float *cs) {
-  const int nblk = H / 128;
-  for (int j = threadIdx.x; j < nblk * 16; j += NT) {
-    const int t = j & 3, b = (j >> 2) & 3, blk = j >> 4;
-    const int y = t >> 1, half = b >> 1, bb = b & 1;
-    (void)y;
+  const int nblk = H / 128, per = nblk * 8, total = per * nb;
+  const int lane = threadIdx.x & 31;
+  // j = ((b * nblk + blk) * 4 + t) * 2 + hh; whole warps run each pass (shuffles)
+  for (int j0 = (threadIdx.x & ~31); j0 < total; j0 += NT) {
+    const int j = j0 + lane;
+    const bool valid = j < total;
+    int b = 0, jj = valid ? j : 0;
+    while (jj >= per) jj -= per, b++;
+    const int hh = jj & 1, t = (jj >> 1) & 3, blk = jj >> 3;
+    const int half = b >> 1, bb = b & 1;
     float v[32];
-    if (b < nb) {
-      const float4 *src = reinterpret_cast<const float4 *>(xf + b * H + blk * 128 + 32 * t);
+    const float4 *src = reinterpret_cast<const float4 *>(xf + b * H + blk * 128 + 32 * t);
 #pragma unroll
-      for (int i = 0; i < 8; i++) {
-        const float4 q = src[i];
-        v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; i++) v[i] = 0.f;
+    for (int i = 0; i < 8; i++) {
+      const float4 q = valid ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[4 * i] = q.x, v[4 * i + 1] = q.y, v[4 * i + 2] = q.z, v[4 * i + 3] = q.w;
     }
     float sx = 0.f, sc = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; i++) sx += v[i];
+    for (int i = 0; i < 16; i++) sx += hh ? v[16 + i] : v[i];
 #pragma unroll
-    for (int m = 0; m < 8; m++) {
-      const int p0 = 2 * m, p1 = 2 * m + 1;
-      const float a0 = v[Codec<B>::lo(p0)] * pow2neg(Codec<B>::slo(p0));
-      const float a1 = v[Codec<B>::hi(p0)] * pow2neg(Codec<B>::shi(p0));
-      const float a2 = v[Codec<B>::lo(p1)] * pow2neg(Codec<B>::slo(p1));
-      const float a3 = v[Codec<B>::hi(p1)] * pow2neg(Codec<B>::shi(p1));
+    for (int mq = 0; mq < 4; mq++) {
+      const int m = 4 * hh + mq;
+      float a[4];
+#pragma unroll
+      for (int hm = 0; hm < 2; hm++) {  // this thread's half selects the pairs at compile time per branch
+#pragma unroll
+        for (int k = 0; k < 2; k++) {
+          const int p = 2 * (4 * hm + mq) + k;
+          if (hm == hh) {
+            a[2 * k] = v[Codec<B>::lo(p)] * pow2neg(Codec<B>::slo(p));
+            a[2 * k + 1] = v[Codec<B>::hi(p)] * pow2neg(Codec<B>::shi(p));
+          }
+        }
+      }
       uint32_t hi0, lo0, hi1, lo1;
-      split2(a0, a1, hi0, lo0);
-      split2(a2, a3, hi1, lo1);
+      split2(a[0], a[1], hi0, lo0);
+      split2(a[2], a[3], hi1, lo1);
       // the offset sum from exactly the values the MMA sees (hi + lo), so the
       // 128 offset cancels without amplifying the split's residual
       sc += (bf16lo(hi0) + bf16lo(lo0)) + (bf16hi(hi0) + bf16hi(lo0)) + (bf16lo(hi1) + bf16lo(lo1)) +
             (bf16hi(hi1) + bf16hi(lo1));
-      xb[frag_index(blk, half, m, t, 0, bb)] = make_uint2(hi0, hi1);
-      xb[frag_index(blk, half, m, t, 1, bb)] = make_uint2(lo0, lo1);
+      if (valid) {
+        xb[frag_index(blk, half, m, t, 0, bb)] = make_uint2(hi0, hi1);
+        xb[frag_index(blk, half, m, t, 1, bb)] = make_uint2(lo0, lo1);
+      }
     }
+    // the pair (hh), then the two quad positions of the group (t, t ^ 1)
     sx += __shfl_xor_sync(FULL, sx, 1);
     sc += __shfl_xor_sync(FULL, sc, 1);
-    if ((t & 1) == 0) {
+    sx += __shfl_xor_sync(FULL, sx, 2);
+    sc += __shfl_xor_sync(FULL, sc, 2);
+    if (valid && hh == 0 && (t & 1) == 0) {
+      const int y = t >> 1;
       if (xs) xs[b * (H / 64) + 2 * blk + y] = sx;
       cs[b * (H / 64) + 2 * blk + y] = 128.f * sc;
     }
@@ -465,31 +481,31 @@ __device__ void stage_h(const uint2 *hf, int I, int nb, uint2 *hsm, float *hxs, 
 // ------------------------------------------------------------ routing
 
 // Top-k of one row of E <= 1024 logits (ties to the lower id), then softmax
-// over the k chosen.  Lane l holds ids [l*P, l*P+P) as order-preserving keys
-// in registers; each round one warp max picks the winner, whose lane alone
-// rescans its keys.
+// over the k chosen.  Lane l holds ids l, l + 32, ... as order-preserving
+// keys in registers; each round one warp max finds the largest key and one
+// warp min the lowest id holding it; the winner's lane rescans its keys, and
+// lane r keeps the r-th winner, so nothing is written until the end.
 template <int PM>
 __device__ void topk_warp(const float *lg, int E, int K, int *idx, float *w) {
   const int lane = threadIdx.x & 31;
-  const int P = (E + 31) / 32;
   uint32_t key[PM];
 #pragma unroll
   for (int i = 0; i < PM; i++) {
-    const int e = lane * P + i;
-    key[i] = (i < P && e < E) ? orderable(lg[e]) : 0u;
+    const int e = i * 32 + lane;
+    key[i] = e < E ? orderable(lg[e]) : 0u;
   }
   uint32_t bk = 0;
   int bi = 0;
 #pragma unroll
   for (int i = 0; i < PM; i++)
     if (key[i] > bk) bk = key[i], bi = i;
+  int myid = 0;
 #pragma unroll 1
   for (int r = 0; r < K; r++) {
     const uint32_t m = __reduce_max_sync(FULL, bk);
-    const int wl = __ffs(__ballot_sync(FULL, bk == m)) - 1;
-    if (lane == wl) {
-      idx[r] = lane * P + bi;
-      w[r] = lg[lane * P + bi];
+    const uint32_t id = __reduce_min_sync(FULL, bk == m ? (uint32_t)(bi * 32 + lane) : 0xffffffffu);
+    if (lane == r) myid = (int)id;
+    if (lane == (int)(id & 31)) {
       uint32_t nbk = 0;
       int nbi = 0;
 #pragma unroll
@@ -500,12 +516,11 @@ __device__ void topk_warp(const float *lg, int E, int K, int *idx, float *w) {
       bk = nbk, bi = nbi;
     }
   }
-  __syncwarp();
-  const float mx = w[0];
-  const float ev = lane < K ? expf(w[lane] - mx) : 0.f;
+  const float myl = lane < K ? lg[myid] : 0.f;
+  const float mx = __shfl_sync(FULL, myl, 0);
+  const float ev = lane < K ? expf(myl - mx) : 0.f;
   const float z = warp_sum(ev);
-  __syncwarp();
-  if (lane < K) w[lane] = ev / z;
+  if (lane < K) idx[lane] = myid, w[lane] = ev / z;
   __syncwarp();
 }
 
@@ -515,6 +530,13 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
                            volatile int *nu) {
   const int lane = threadIdx.x & 31;
   for (int j = lane; j < 256; j += 32) wm[j] = 0.f;
+  if (nb == 1) {  // one row: its k ids are distinct, in rank order
+    __syncwarp();
+    if (lane < K) uni[lane] = sidx[lane], wm[lane] = sw[lane];
+    if (lane == 0) *nu = K;
+    __syncwarp();
+    return;
+  }
   int id[2], first[2], fpos[2], pb[2], pr[2];
 #pragma unroll
   for (int h = 0; h < 2; h++) {
@@ -666,6 +688,9 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu;
     fence_mbar_init();
   }
+  // activation registers and sums: rows b >= nb stay zero for the whole call
+  for (uint32_t *z = reinterpret_cast<uint32_t *>(xa) + tid; z < reinterpret_cast<uint32_t *>(cs4 + 4 * ng); z += NT)
+    *z = 0u;
   __syncthreads();
   // warp lane 0 of an issuing warp: unit q of the layer into its ring stage
   auto issue_at = [&](const UnitDesc &d, unsigned u) {
