@@ -44,7 +44,7 @@ WsLayout ws_layout(int H, int E, int I, int nl, int nb) {
   w.cnt = off;
   off += align256((size_t)nl * moe::kCntPerLayer * 4);
   w.logits = off;
-  off += align256((size_t)nl * 4 * (E + 1) * 4);
+  off += align256((size_t)nl * 4 * (E + 1) * 8);
   w.xbuf = off;
   off += align256((size_t)nl * nb * H * 4);
   w.hfrag = off;
@@ -141,7 +141,7 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   p.status = status;
   char *base = (char *)work;
   p.cnt = (unsigned *)(base + w.cnt);
-  p.logits = (float *)(base + w.logits);
+  p.logits = (unsigned long long *)(base + w.logits);
   p.xbuf = (float *)(base + w.xbuf);
   p.hfrag = (uint16_t *)(base + w.hfrag);
   p.ypart = (float *)(base + w.ypart);
@@ -165,7 +165,8 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   if (moe::decode_plan(dev, p, &grid, &smem) != 0)
     return fail(MOE_ECUDA, "decode kernel cannot be resident on this device (hidden %d, experts %d)", H, E);
   cudaStream_t st = (cudaStream_t)stream;
-  cudaError_t e = cudaMemsetAsync(p.cnt, 0, (size_t)nl * moe::kCntPerLayer * 4, st);
+  // counters and the logit exchange words start at zero every call (they are adjacent)
+  cudaError_t e = cudaMemsetAsync(p.cnt, 0, w.xbuf - w.cnt, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), st);
   if (e == cudaSuccess) e = moe::launch_decode(p, grid, smem, st);
   if (e != cudaSuccess) return fail(MOE_ECUDA, "launch failed: %s", cudaGetErrorString(e));

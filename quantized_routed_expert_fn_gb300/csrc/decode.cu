@@ -824,24 +824,52 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       const int r = j / nb, b = j % nb;
       float sum = 0.f;
       for (int ch = 0; ch < nch; ch++) sum += red[(r * nch + ch) * 4 + b];
-      P.logits[((size_t)l * 4 + b) * (E + 1) + rr0 + r] = sum;
+      // value and ready flag in one 64-bit store: no release fence
+      if (!(P.withhold && rr0 + r == 0))
+        st_relaxed_u64(P.logits + ((size_t)l * 4 + b) * (E + 1) + rr0 + r,
+                       (1ull << 32) | __float_as_uint(sum));
     }
-    if (rr1 > rr0) cta_signal(cnt + kCntRouter, (unsigned)(rr1 - rr0));
     MOE_STAMP(3)
     // expert addresses (for the slot table) while the other CTAs finish their router rows
     for (int e = tid; e < E; e += NT) eaddr_s[e] = L.eaddr[e];
 
     // ---- T: top-k, softmax, union
-    if (!cta_wait(cnt + kCntRouter, (unsigned)(R + (P.withhold ? 1 : 0)), P, sflag)) {
-      drain_ring(bars, qbase, qbase + issued, S, P);
-      return;
+    // every logit of the layer, each polled until its writer's flag shows
+    {
+      bool ok = true;
+      for (int i = tid; i < nb * (E + 1); i += NT) {
+        const int b = i / (E + 1), e = i % (E + 1);
+        float v = 0.f;
+        if (e < R) {
+          const unsigned long long *p = P.logits + ((size_t)l * 4 + b) * (E + 1) + e;
+          unsigned long long u = ld_relaxed_u64(p);
+          if ((u >> 32) == 0) {
+            const uint64_t t0 = globaltimer();
+            unsigned spins = 0;
+            while (((u = ld_relaxed_u64(p)) >> 32) == 0) {
+              if ((++spins & 31u) == 0) {
+                if (ld_volatile_int(P.status) != 0) {
+                  ok = false;
+                  break;
+                }
+                if (globaltimer() - t0 > P.timeout_ns) {
+                  atomicCAS(P.status, 0, kStatusTimeout);
+                  ok = false;
+                  break;
+                }
+              }
+            }
+          }
+          v = __uint_as_float((uint32_t)u);
+        }
+        lg[b * E1 + e] = v;
+      }
+      if (!__syncthreads_and(ok)) {
+        drain_ring(bars, qbase, qbase + issued, S, P);
+        return;
+      }
     }
     MOE_STAMP(4)
-    for (int i = tid; i < nb * (E + 1); i += NT) {
-      const int b = i / (E + 1), e = i % (E + 1);
-      lg[b * E1 + e] = e < R ? __ldcg(P.logits + ((size_t)l * 4 + b) * (E + 1) + e) : 0.f;
-    }
-    __syncthreads();
     MOE_STAMP(8)
     if (warp < nb) {
       if (E <= 128)

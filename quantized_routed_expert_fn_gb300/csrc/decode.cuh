@@ -21,7 +21,7 @@ struct LayerP {
 };
 
 // per-layer counters in the workspace (uint32 each)
-constexpr int kCntRouter = 0;  // router rows finished
+constexpr int kCntRouter = 0;  // reserved (router logits carry their own ready flags)
 constexpr int kCntRows = 1;    // 64-row output ranges finalised
 constexpr int kCntGu = 8;      // [64] gate_up units finished per internal slot
 constexpr int kCntDn = 72;     // [H/64] down units finished per output range
@@ -40,7 +40,7 @@ struct FwdParams {
   float *logits_out;      // [nb][E] (route only) or nullptr
   int *status;
   unsigned *cnt;          // [nl][kCntPerLayer]
-  float *logits;          // [nl][4][E+1]
+  unsigned long long *logits;  // [nl][4][E+1] {fp32 bits, 1 once written}; zeroed per call
   float *xbuf;            // [nl][nb][H]  input of layer l (l >= 1)
   uint16_t *hfrag;        // [64][I/128][8][32][2][2] bf16 activation fragments of h
   float *ypart;           // [64][nb][H]  per-slot weighted down outputs
