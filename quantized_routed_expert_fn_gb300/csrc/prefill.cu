@@ -131,7 +131,7 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 // the router, <= kPfTileN for the expert GEMMs); K goes in stages of 64.
 // B (token rows) passes through a ring of kSB 128B-swizzled shared-memory
 // stages.  The expert GEMMs' A (dequantized weight rows) passes through a
-// ring of kSA stages in tensor memory, 32 columns each (row r in TMEM lane
+// ring of kSA stages in tensor memory, kPA k-panels of 32 columns each (row r in TMEM lane
 // r, bf16 pairs along k), and feeds tcgen05.mma from there; the router's A
 // (bf16 rows of R) comes by TMA into shared memory beside its B.
 //   warp 0      lane 0 issues the tcgen05 MMAs of a stage once its operands
@@ -150,10 +150,11 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 
 constexpr int kWsThreads = 448;
 constexpr int kSB = 6;                     // B stages (shared memory)
-constexpr int kSA = 4;                     // A stages (tensor memory; expert GEMMs)
+constexpr int kSA = 2;                     // A stages (tensor memory; expert GEMMs)
+constexpr int kPA = 2;                     // k-panels per A stage (one handshake per two panels)
 constexpr int kAccCols = 192;              // TMEM columns of one accumulator (expert GEMMs; N <= 192)
-constexpr int kTmemA = 2 * kAccCols;       // first TMEM column of the A ring: kSA x 32 columns
-static_assert(kTmemA + 32 * kSA <= 512, "tensor memory");
+constexpr int kTmemA = 2 * kAccCols;       // first TMEM column of the A ring: kSA x kPA x 32 columns
+static_assert(kTmemA + 32 * kPA * kSA <= 512, "tensor memory");
 constexpr int kChunk = 4;                  // k-stages per staged chunk of codes
 constexpr int kStgCodes = 128 * 128;       // 128 rows x 128 bytes of codes (4 stages)
 constexpr int kStgSB = 128 * kChunk * 8;   // per row and stage: scale word, bias word
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         const uint32_t idesc = tc05::idesc_bf16(N);
         const int ppb = MODE == MODE_ROUTER ? 1 : panels_per_stage(N, nk);
         const uint32_t pstep = (uint32_t)(panel_rows(N) * 128) >> 4;  // descriptor step per panel
-        int pp = 0;
+        int pp = 0, ap = 0;  // panel within the B stage, within the A stage
         uint64_t bdesc = desc0;
         for (int kk = 0; kk < nk; kk++) {
           if (pp == 0) {
@@ -388,17 +389,23 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
             }
             __syncwarp();
           } else {
-            if (!warp_wait(&B.full_a[sa], pa, P)) {
+            if (ap == 0 && !warp_wait(&B.full_a[sa], pa, P)) {
               ok = false;
               break;
             }
             tc05::fence_after();
+            const bool last = ap == kPA - 1 || kk == nk - 1;  // the A stage's last panel
             if (tc05::elect_one()) {
-              tc05::mma_ts_k64(d, tmem + (uint32_t)(kTmemA + 32 * sa), bdesc, idesc, kk != 0);
-              tc05::commit(&B.empty_a[sa]);
+              tc05::mma_ts_k64(d, tmem + (uint32_t)(kTmemA + 32 * (kPA * sa + ap)), bdesc, idesc, kk != 0);
+              if (last) tc05::commit(&B.empty_a[sa]);
             }
             __syncwarp();
-            if (++sa == kSA) sa = 0, pa ^= 1;
+            if (last) {
+              ap = 0;
+              if (++sa == kSA) sa = 0, pa ^= 1;
+            } else {
+              ap++;
+            }
           }
           bdesc += pstep;
           if (++pp == ppb) {
@@ -510,20 +517,27 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         const uint8_t *buf = stg + (c % kNStg) * kStgBuf;
         const int ns = min(kChunk, nk - kc * kChunk);
         for (int u = 0; u < ns; u++) {
-          const int kk = kc * kChunk + u, f = lt * nk + kk, sa = f % kSA;
-          if (!warp_wait(&B.empty_a[sa], (uint32_t)(((f / kSA) & 1) ^ 1), P)) {
-            ok = false;
-            break;
+          // A stage ga of this CTA's sequence: (nk + kPA - 1) / kPA stages a tile
+          const int kk = kc * kChunk + u, ap = kk % kPA;
+          const int ga = lt * ((nk + kPA - 1) / kPA) + kk / kPA, sa = ga % kSA;
+          if (ap == 0) {
+            if (!warp_wait(&B.empty_a[sa], (uint32_t)(((ga / kSA) & 1) ^ 1), P)) {
+              ok = false;
+              break;
+            }
+            tc05::fence_after();  // after the MMAs that read this A stage
           }
-          tc05::fence_after();  // after the MMAs that read this A stage
           // scale / bias: the half of the staged 4-byte word holding entry row * G + kk
           const uint32_t half = (rodd + (uint32_t)kk) & 1u;
           uint32_t av[16];
           ws_dequant_half(buf, r, hf, u, half, av);
-          tc05::st16_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemA + 32 * sa + 16 * hf), av);
-          tc05::fence_before();
-          __syncwarp();
-          if (lane == 0) tc05::mbar_arrive(&B.full_a[sa]);
+          tc05::st16_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemA + 32 * (kPA * sa + ap) + 16 * hf),
+                          av);
+          if (ap == kPA - 1 || kk == nk - 1) {
+            tc05::fence_before();
+            __syncwarp();
+            if (lane == 0) tc05::mbar_arrive(&B.full_a[sa]);
+          }
         }
         // the eight producer warps stop together (they share a named barrier)
         ok = tc05::named_and(4, 256, ok);
