@@ -138,11 +138,12 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 //               have landed and commits them (stage free / accumulator full)
 //   warp 1      TMA: B rows (and the router's A rows) of each stage
 //   warps 2-9   A producers: all 256 threads stage the codes of four
-//               k-stages (128 rows x 128 bytes, plus scale / bias words)
+//               k-panels (128 rows x 128 bytes, plus scale / bias words)
 //               into shared memory with coalesced cp.async, three chunks in
-//               the air; then warp w dequantizes half hf = (w - 2) / 4 of the
-//               64 codes of rows 32 (w % 4) .. +31 -- the TMEM lanes warp w
-//               may write -- and stores the 16 bf16 pairs with tcgen05.st
+//               the air; an A stage holds kPA = 2 panels, and warp w fills
+//               panel (w - 2) / 4 of it: rows 32 (w % 4) .. +31 -- the TMEM
+//               lanes warp w may write -- 64 codes each, stored as 32 bf16
+//               pairs with tcgen05.st
 //   warps 10-13 epilogue: TMEM -> registers -> global, from one of two
 //               accumulators while the MMAs fill the other
 // Every mbarrier wait is bounded; a wait that gives up records
@@ -289,24 +290,26 @@ __device__ __forceinline__ void stage_chunk(const PfParams &P, const PfItem &it,
   tc05::cp_commit();
 }
 
-// Half hf (codes 32hf .. 32hf+31) of row r's 64 codes of stage u of a
-// staged chunk -> bf16(scale * code + bias), k permuted within 8-blocks, as
-// 16 words of two bf16 each (the row's A columns 16hf .. 16hf+15)
-__device__ __forceinline__ void ws_dequant_half(const uint8_t *buf, int r, int hf, int u, uint32_t half,
-                                                uint32_t (&a)[16]) {
-  const uint4 c = *reinterpret_cast<const uint4 *>(buf + r * 128 + (((2 * u + hf) ^ (r & 7)) << 4));
+// Row r's 64 codes of k-panel u of a staged chunk -> bf16(scale * code +
+// bias), k permuted within 8-blocks, as 32 words of two bf16 each (the row's
+// 32 A columns of the panel)
+__device__ __forceinline__ void ws_dequant_row(const uint8_t *buf, int r, int u, uint32_t half, uint32_t (&a)[32]) {
   const uint2 sbw = *reinterpret_cast<const uint2 *>(buf + kStgCodes + (r * kChunk + u) * 8);
   const uint32_t s = (sbw.x >> (16 * half)) & 0xffffu, b = (sbw.y >> (16 * half)) & 0xffffu;
   const uint32_t s2 = s * 0x10001u, b2 = b * 0x10001u;
-  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-  for (int ch = 0; ch < 4; ch++)
+  for (int hf = 0; hf < 2; hf++) {
+    const uint4 c = *reinterpret_cast<const uint4 *>(buf + r * 128 + (((2 * u + hf) ^ (r & 7)) << 4));
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const uint32_t v = ((w[ch] >> (4 * j)) & 0x000f000fu) | 0x43004300u;  // (128 + n_j, 128 + n_{j+4})
-      const uint32_t qv = bfma2(v, 0x3f803f80u, 0xc300c300u);              // the codes, exact
-      a[4 * ch + j] = bfma2(qv, s2, b2);                                    // bf16(s*q + b)
-    }
+    for (int ch = 0; ch < 4; ch++)
+#pragma unroll
+      for (int j = 0; j < 4; j++) {
+        const uint32_t v = ((w[ch] >> (4 * j)) & 0x000f000fu) | 0x43004300u;  // (128 + n_j, 128 + n_{j+4})
+        const uint32_t qv = bfma2(v, 0x3f803f80u, 0xc300c300u);              // the codes, exact
+        a[16 * hf + 4 * ch + j] = bfma2(qv, s2, b2);                         // bf16(s*q + b)
+      }
+  }
 }
 
 template <int MODE>
@@ -516,28 +519,27 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         const int lt = c / nct, kc = c - lt * nct;
         const uint8_t *buf = stg + (c % kNStg) * kStgBuf;
         const int ns = min(kChunk, nk - kc * kChunk);
-        for (int u = 0; u < ns; u++) {
-          // A stage ga of this CTA's sequence: (nk + kPA - 1) / kPA stages a tile
-          const int kk = kc * kChunk + u, ap = kk % kPA;
-          const int ga = lt * ((nk + kPA - 1) / kPA) + kk / kPA, sa = ga % kSA;
-          if (ap == 0) {
-            if (!warp_wait(&B.empty_a[sa], (uint32_t)(((ga / kSA) & 1) ^ 1), P)) {
-              ok = false;
-              break;
-            }
-            tc05::fence_after();  // after the MMAs that read this A stage
+        for (int u0 = 0; u0 < ns; u0 += kPA) {
+          // A stage ga of this CTA's sequence ((nk + kPA - 1) / kPA stages a
+          // tile): warp group hf fills its panel u0 + hf, if the stage has it
+          const int ga = lt * ((nk + kPA - 1) / kPA) + (kc * kChunk + u0) / kPA, sa = ga % kSA;
+          if (!warp_wait(&B.empty_a[sa], (uint32_t)(((ga / kSA) & 1) ^ 1), P)) {
+            ok = false;
+            break;
           }
-          // scale / bias: the half of the staged 4-byte word holding entry row * G + kk
-          const uint32_t half = (rodd + (uint32_t)kk) & 1u;
-          uint32_t av[16];
-          ws_dequant_half(buf, r, hf, u, half, av);
-          tc05::st16_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemA + 32 * (kPA * sa + ap) + 16 * hf),
-                          av);
-          if (ap == kPA - 1 || kk == nk - 1) {
-            tc05::fence_before();
-            __syncwarp();
-            if (lane == 0) tc05::mbar_arrive(&B.full_a[sa]);
+          tc05::fence_after();  // after the MMAs that read this A stage
+          const int u = u0 + hf;
+          if (u < ns) {
+            const int kk = kc * kChunk + u;
+            // scale / bias: the half of the staged 4-byte word holding entry row * G + kk
+            const uint32_t half = (rodd + (uint32_t)kk) & 1u;
+            uint32_t av[32];
+            ws_dequant_row(buf, r, u, half, av);
+            tc05::st32_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemA + 32 * (kPA * sa + hf)), av);
           }
+          tc05::fence_before();
+          __syncwarp();
+          if (lane == 0) tc05::mbar_arrive(&B.full_a[sa]);
         }
         // the eight producer warps stop together (they share a named barrier)
         ok = tc05::named_and(4, 256, ok);
