@@ -140,10 +140,11 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 //   warps 2-9   A producers: all 256 threads stage the codes of four
 //               k-panels (128 rows x 128 bytes, plus scale / bias words)
 //               into shared memory with coalesced cp.async, three chunks in
-//               the air; an A stage holds kPA = 2 panels, and warp w fills
-//               panel (w - 2) / 4 of it: rows 32 (w % 4) .. +31 -- the TMEM
-//               lanes warp w may write -- 64 codes each, stored as 32 bf16
-//               pairs with tcgen05.st
+//               the air; an A stage holds kPA = 2 panels, and a chunk's two
+//               A stages go to the two groups of four warps (w - 2) / 4:
+//               warp w fills rows 32 (w % 4) .. +31 -- the TMEM lanes it may
+//               write -- 64 codes a panel, stored as 32 bf16 pairs per panel
+//               with tcgen05.st
 //   warps 10-13 epilogue: TMEM -> registers -> global, from one of two
 //               accumulators while the MMAs fill the other
 // Every mbarrier wait is bounded; a wait that gives up records
@@ -256,35 +257,59 @@ __device__ __forceinline__ int ws_weight_row(const PfParams &P, int mt, int r) {
     return mt * 128 + r;
 }
 
-// Stage one chunk of codes (k-stages 4kc .. 4kc+3 of a tile) into shared
-// memory, by the 256 producer threads (t): 128 rows x 128 bytes, copied by 8
-// threads per row segment so that each warp instruction reads four whole
-// 128-byte lines (16-byte pieces placed at piece ^ (row & 7) against bank
-// conflicts); plus, per row and stage, the 4-byte words holding its scale
-// and bias.  A segment may run past the end of a row, into bytes of the same
-// record (codes are followed by the scale and bias tables); those bytes are
-// never used.
+// Global sources of one staging thread t for a tile, formed once per tile:
+// its four 16-byte code segments (row (i * 256 + t) / 8, piece t % 8, at
+// k-panel 0) and the scale / bias words of row t % 128.
+struct StgRows {
+  const uint8_t *c[4];
+  const uint8_t *s, *b;
+  bool ok;
+};
+
 template <int MODE>
-__device__ __forceinline__ void stage_chunk(const PfParams &P, const PfItem &it, int kc, int nk, int t, uint8_t *buf) {
-  if (item_ok<MODE>(it)) {
+__device__ __forceinline__ StgRows stage_rows(const PfParams &P, const PfItem &it, int t) {
+  StgRows sr{};
+  sr.ok = item_ok<MODE>(it);
+  if (sr.ok) {
     const uint8_t *rec = reinterpret_cast<const uint8_t *>(it.rec);
     const QOff q = it.g == P.E ? (MODE == MODE_GATE_UP ? P.sgu : P.sdn) : (MODE == MODE_GATE_UP ? P.gu : P.dn);
     const int inp = MODE == MODE_GATE_UP ? P.H : P.I;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
       const int idx = i * 256 + t, row = idx >> 3, part = idx & 7;
-      const size_t src = q.w + (size_t)ws_weight_row<MODE>(P, it.mt, row) * (inp / 2) + kc * 128 + part * 16;
-      tc05::cp16(buf + row * 128 + ((part ^ (row & 7)) << 4), rec + src);
+      sr.c[i] = rec + q.w + (size_t)ws_weight_row<MODE>(P, it.mt, row) * (inp / 2) + part * 16;
+    }
+    const size_t g2 = (size_t)ws_weight_row<MODE>(P, it.mt, t & 127) * (inp / 64) * 2;
+    sr.s = rec + q.s + g2;
+    sr.b = rec + q.b + g2;
+  }
+  return sr;
+}
+
+// Stage one chunk of codes (k-panels 4kc .. 4kc+3 of a tile) into shared
+// memory, by the 256 producer threads (t): 128 rows x 128 bytes, copied by 8
+// threads per row segment so that each warp instruction reads four whole
+// 128-byte lines (16-byte pieces placed at piece ^ (row & 7) against bank
+// conflicts); plus, per row and panel, the 4-byte words holding its scale
+// and bias.  A segment may run past the end of a row, into bytes of the same
+// record (codes are followed by the scale and bias tables); those bytes are
+// never used.
+__device__ __forceinline__ void stage_chunk(const StgRows &sr, int kc, int nk, int t, uint8_t *buf) {
+  if (sr.ok) {
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+      const int idx = i * 256 + t, row = idx >> 3, part = idx & 7;
+      tc05::cp16(buf + row * 128 + ((part ^ (row & 7)) << 4), sr.c[i] + kc * 128);
     }
     const int r = t & 127;
-    const size_t gbase = (size_t)ws_weight_row<MODE>(P, it.mt, r) * (inp / 64);
 #pragma unroll
     for (int v = 0; v < 2; v++) {
       const int u = 2 * (t >> 7) + v;
       const int kk = min(kc * kChunk + u, nk - 1);
-      const size_t gi = (gbase + kk) * 2;
-      tc05::cp4(buf + kStgCodes + (r * kChunk + u) * 8, rec + ((q.s + gi) & ~(size_t)3));
-      tc05::cp4(buf + kStgCodes + (r * kChunk + u) * 8 + 4, rec + ((q.b + gi) & ~(size_t)3));
+      tc05::cp4(buf + kStgCodes + (r * kChunk + u) * 8,
+                reinterpret_cast<const uint8_t *>((uintptr_t)(sr.s + kk * 2) & ~(uintptr_t)3));
+      tc05::cp4(buf + kStgCodes + (r * kChunk + u) * 8 + 4,
+                reinterpret_cast<const uint8_t *>((uintptr_t)(sr.b + kk * 2) & ~(uintptr_t)3));
     }
   }
   tc05::cp_commit();
@@ -330,7 +355,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       mbar_init(&B.empty_b[s], 1);
     }
     for (int s = 0; s < kSA; s++) {
-      mbar_init(&B.full_a[s], 8);
+      mbar_init(&B.full_a[s], 4);  // the four warps of one dequant group
       mbar_init(&B.empty_a[s], 1);
     }
     for (int b = 0; b < 2; b++) {
@@ -483,16 +508,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
     // ---------------------------------------------------------------- A producers
     if constexpr (MODE != MODE_ROUTER) {
       // thread t stages codes; thread (warp, lane) dequantizes tile row
-      // r = 32 * (warp % 4) + lane (the TMEM lanes its warp may write), half hf
+      // r = 32 * (warp % 4) + lane (the TMEM lanes its warp may write); warp
+      // group hf fills the chunk's A stage hf (k-panels 2hf, 2hf + 1)
       const int t = tid - 64, r = 32 * (warp & 3) + lane, hf = (warp - 2) >> 2;
       const int nct = (nk + kChunk - 1) / kChunk;  // chunks per tile
       const int total = my_tiles * nct;
       const int inp = MODE == MODE_GATE_UP ? P.H : P.I;
       uint8_t *stg = sm + LY::offStg;
       // items of the staging position's tile and of the tile after it
-      PfItem scur{}, snext{};
+      PfItem snext{};
+      StgRows srow{};
       int slt = 0;
-      if (my_tiles > 0) scur = ws_item<MODE>(P, tile_of(0));
+      if (my_tiles > 0) srow = stage_rows<MODE>(P, ws_item<MODE>(P, tile_of(0)), t);
       if (my_tiles > 1) snext = ws_item<MODE>(P, tile_of(1));
       auto issue = [&](int c) {
         if (c >= total) {
@@ -501,11 +528,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         }
         const int lt = c / nct;
         if (lt != slt) {
-          scur = lt == slt + 1 ? snext : ws_item<MODE>(P, tile_of(lt));
+          srow = stage_rows<MODE>(P, lt == slt + 1 ? snext : ws_item<MODE>(P, tile_of(lt)), t);
           slt = lt;
           if (lt + 1 < my_tiles) snext = ws_item<MODE>(P, tile_of(lt + 1));
         }
-        stage_chunk<MODE>(P, scur, c - lt * nct, nk, t, stg + (c % kNStg) * kStgBuf);
+        stage_chunk(srow, c - lt * nct, nk, t, stg + (c % kNStg) * kStgBuf);
       };
       issue(0);
       issue(1);
@@ -519,27 +546,29 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         const int lt = c / nct, kc = c - lt * nct;
         const uint8_t *buf = stg + (c % kNStg) * kStgBuf;
         const int ns = min(kChunk, nk - kc * kChunk);
-        for (int u0 = 0; u0 < ns; u0 += kPA) {
-          // A stage ga of this CTA's sequence ((nk + kPA - 1) / kPA stages a
-          // tile): warp group hf fills its panel u0 + hf, if the stage has it
+        const int u0 = kPA * hf;  // this group's A stage of the chunk, if the chunk has it
+        if (u0 < ns) {
+          // A stage ga of this CTA's sequence ((nk + kPA - 1) / kPA stages a tile)
           const int ga = lt * ((nk + kPA - 1) / kPA) + (kc * kChunk + u0) / kPA, sa = ga % kSA;
-          if (!warp_wait(&B.empty_a[sa], (uint32_t)(((ga / kSA) & 1) ^ 1), P)) {
-            ok = false;
-            break;
-          }
-          tc05::fence_after();  // after the MMAs that read this A stage
-          const int u = u0 + hf;
-          if (u < ns) {
-            const int kk = kc * kChunk + u;
+          if (warp_wait(&B.empty_a[sa], (uint32_t)(((ga / kSA) & 1) ^ 1), P)) {
+            tc05::fence_after();  // after the MMAs that read this A stage
+            const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemA + 32 * kPA * sa);
             // scale / bias: the half of the staged 4-byte word holding entry row * G + kk
-            const uint32_t half = (rodd + (uint32_t)kk) & 1u;
-            uint32_t av[32];
-            ws_dequant_row(buf, r, u, half, av);
-            tc05::st32_wait(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemA + 32 * (kPA * sa + hf)), av);
+            const int kk0 = kc * kChunk + u0;
+            uint32_t av0[32], av1[32];
+            ws_dequant_row(buf, r, u0, (rodd + (uint32_t)kk0) & 1u, av0);
+            tc05::st32(ta, av0);
+            if (u0 + 1 < ns) {
+              ws_dequant_row(buf, r, u0 + 1, (rodd + (uint32_t)kk0 + 1u) & 1u, av1);
+              tc05::st32(ta + 32, av1);
+            }
+            tc05::wait_st();
+            tc05::fence_before();
+            __syncwarp();
+            if (lane == 0) tc05::mbar_arrive(&B.full_a[sa]);
+          } else {
+            ok = false;
           }
-          tc05::fence_before();
-          __syncwarp();
-          if (lane == 0) tc05::mbar_arrive(&B.full_a[sa]);
         }
         // the eight producer warps stop together (they share a named barrier)
         ok = tc05::named_and(4, 256, ok);
