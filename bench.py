@@ -49,8 +49,8 @@ METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 
 NCU_TRAFFIC = {
     "c1": dict(bytes=1206.6e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],
                sha="77dd22dd36d405ab"),
-    "c4": dict(bytes=640.7e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
-               sha="bb6773a973c065ce"),
+    "c4": dict(bytes=640.6e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
+               sha="00e9adc179317485"),
 }
 
 
