@@ -180,7 +180,9 @@ int moe_forward_noalloc(const moe_layer *layers, int n_layers, const float *x, i
  *   out[r] = bf16( sum_j w_j * y_j[r] + sigmoid(shared_gate . x^[r]) *
  *                  y_shared[r]  (+ x[r] when MOE_RESIDUAL) ).
  * The router itself reads x^ at fp32 accuracy (x^ split into two bf16 terms).
- *   L        host pointer to one layer; routed records must be 4-bit
+ *   L        host pointer to one layer; routed records 4-, 3- or 2-bit (the
+ *            shared record is 4-bit); 3-bit records need inter % 128 == 0 so
+ *            that their code rows are whole 16-byte pieces
  *   x        [t][hidden] float32, 16-byte aligned; t in 1..1048576
  *   out      [t][hidden] bf16 (uint16 bit patterns); must not overlap x
  *   work     device workspace of at least moe_prefill_workspace(L, t) bytes,

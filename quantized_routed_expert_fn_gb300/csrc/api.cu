@@ -230,7 +230,11 @@ int check_prefill(const moe_layer *L, int t) {
   if (I == 0 || I % 64 || I > 16384) return fail(MOE_ESHAPE, "inter %u must be a multiple of 64 in 64..16384", I);
   if (E < 1 || E > 1024) return fail(MOE_ESHAPE, "n_experts %u outside 1..1024", E);
   if (K < 1 || K > E || K > 32) return fail(MOE_ESHAPE, "top_k %u outside 1..min(n_experts, 32)", K);
-  if (L->bits != 4) return fail(MOE_ESHAPE, "prefill takes 4-bit routed records; bits %u", L->bits);
+  if (L->bits != 2 && L->bits != 3 && L->bits != 4) return fail(MOE_ESHAPE, "bits %u not in {2,3,4}", L->bits);
+  // the GEMMs stage code rows with 16-byte copies: a 3-bit row (3 * in / 8
+  // bytes) is 16-byte aligned when in is a multiple of 128
+  if (L->bits == 3 && I % 128)
+    return fail(MOE_ESHAPE, "3-bit prefill needs inter %% 128 == 0 (16-byte code rows); inter %u", I);
   if (L->group != 64) return fail(MOE_ESHAPE, "group %u, only 64 is supported", L->group);
   if (L->flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM)) return fail(MOE_EINVAL, "unknown flags 0x%x", L->flags);
   if (!L->router || !L->expert_addr) return fail(MOE_EINVAL, "router / expert_addr NULL");
@@ -270,6 +274,7 @@ int run_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *
   moe::PfParams p;
   memset(&p, 0, sizeof p);
   p.H = H, p.E = (int)L->n_experts, p.K = (int)L->top_k, p.I = (int)L->inter, p.t = t;
+  p.bits = (int)L->bits;
   p.flags = L->flags & (MOE_RESIDUAL | MOE_PRENORM);
   p.route_only = route_only;
   p.x = x, p.out = out;

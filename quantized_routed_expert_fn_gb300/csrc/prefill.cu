@@ -259,14 +259,23 @@ __device__ __forceinline__ int ws_weight_row(const PfParams &P, int mt, int r) {
 
 // Global sources of one staging thread t for a tile, formed once per tile:
 // its four 16-byte code segments (row (i * 256 + t) / 8, piece t % 8, at
-// k-panel 0) and the scale / bias words of row t % 128.
+// k-panel 0; a chunk's row segment is 32 * bits bytes, so pieces past
+// 2 * bits are not copied) and the scale / bias words of row t % 128.
 struct StgRows {
   const uint8_t *c[4];
   const uint8_t *s, *b;
+  int seg;  // bytes of a row per chunk of four k-panels
   bool ok;
 };
 
-template <int MODE>
+// code width of a tile's record: the shared expert's is 4-bit; LB: the
+// routed records may be narrower (else every record is 4-bit)
+template <bool LB>
+__device__ __forceinline__ int item_bits(const PfParams &P, const PfItem &it) {
+  return LB && it.g != P.E ? P.bits : 4;
+}
+
+template <int MODE, bool LB>
 __device__ __forceinline__ StgRows stage_rows(const PfParams &P, const PfItem &it, int t) {
   StgRows sr{};
   sr.ok = item_ok<MODE>(it);
@@ -274,10 +283,14 @@ __device__ __forceinline__ StgRows stage_rows(const PfParams &P, const PfItem &i
     const uint8_t *rec = reinterpret_cast<const uint8_t *>(it.rec);
     const QOff q = it.g == P.E ? (MODE == MODE_GATE_UP ? P.sgu : P.sdn) : (MODE == MODE_GATE_UP ? P.gu : P.dn);
     const int inp = MODE == MODE_GATE_UP ? P.H : P.I;
+    const int bits = item_bits<LB>(P, it);
+    sr.seg = 32 * bits;
 #pragma unroll
     for (int i = 0; i < 4; i++) {
       const int idx = i * 256 + t, row = idx >> 3, part = idx & 7;
-      sr.c[i] = rec + q.w + (size_t)ws_weight_row<MODE>(P, it.mt, row) * (inp / 2) + part * 16;
+      sr.c[i] = part < 2 * bits
+                    ? rec + q.w + (size_t)ws_weight_row<MODE>(P, it.mt, row) * (inp / 8 * bits) + part * 16
+                    : nullptr;
     }
     const size_t g2 = (size_t)ws_weight_row<MODE>(P, it.mt, t & 127) * (inp / 64) * 2;
     sr.s = rec + q.s + g2;
@@ -299,7 +312,7 @@ __device__ __forceinline__ void stage_chunk(const StgRows &sr, int kc, int nk, i
 #pragma unroll
     for (int i = 0; i < 4; i++) {
       const int idx = i * 256 + t, row = idx >> 3, part = idx & 7;
-      tc05::cp16(buf + row * 128 + ((part ^ (row & 7)) << 4), sr.c[i] + kc * 128);
+      if (sr.c[i]) tc05::cp16(buf + row * 128 + ((part ^ (row & 7)) << 4), sr.c[i] + kc * sr.seg);
     }
     const int r = t & 127;
 #pragma unroll
@@ -317,7 +330,8 @@ __device__ __forceinline__ void stage_chunk(const StgRows &sr, int kc, int nk, i
 
 // Row r's 64 codes of k-panel u of a staged chunk -> bf16(scale * code +
 // bias), k permuted within 8-blocks, as 32 words of two bf16 each (the row's
-// 32 A columns of the panel)
+// 32 A columns of the panel).  4-bit records; ws_dequant_row_lb below takes
+// 2- and 3-bit ones into the same layout.
 __device__ __forceinline__ void ws_dequant_row(const uint8_t *buf, int r, int u, uint32_t half, uint32_t (&a)[32]) {
   const uint2 sbw = *reinterpret_cast<const uint2 *>(buf + kStgCodes + (r * kChunk + u) * 8);
   const uint32_t s = (sbw.x >> (16 * half)) & 0xffffu, b = (sbw.y >> (16 * half)) & 0xffffu;
@@ -337,7 +351,51 @@ __device__ __forceinline__ void ws_dequant_row(const uint8_t *buf, int r, int u,
   }
 }
 
-template <int MODE>
+// Code i (0..63) of a panel's little-endian bitstream w of B-bit codes.
+template <int B>
+__device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[2 * B], int i) {
+  const int bit = B * i, wi = bit >> 5, off = bit & 31;
+  uint32_t v = w[wi] >> off;
+  if (off + B > 32) v |= w[wi + 1] << (32 - off);
+  return v & ((1u << B) - 1u);
+}
+
+// ws_dequant_row for B = 2 or 3: the panel's 8B code bytes sit at byte 8Bu of
+// the row's staged segment (8-byte loads never straddle a 16-byte piece);
+// word 4ch + j of the output pairs codes 8ch + j and 8ch + j + 4, as for 4 bits.
+template <int B>
+__device__ __forceinline__ void ws_dequant_row_lb(const uint8_t *buf, int r, int u, uint32_t half, uint32_t (&a)[32]) {
+  const uint2 sbw = *reinterpret_cast<const uint2 *>(buf + kStgCodes + (r * kChunk + u) * 8);
+  const uint32_t s = (sbw.x >> (16 * half)) & 0xffffu, b = (sbw.y >> (16 * half)) & 0xffffu;
+  const uint32_t s2 = s * 0x10001u, b2 = b * 0x10001u;
+  uint32_t w[2 * B];
+#pragma unroll
+  for (int k = 0; k < B; k++) {
+    const int byte = 8 * B * u + 8 * k;
+    const uint2 q = *reinterpret_cast<const uint2 *>(buf + r * 128 + (((byte >> 4) ^ (r & 7)) << 4) + (byte & 15));
+    w[2 * k] = q.x, w[2 * k + 1] = q.y;
+  }
+#pragma unroll
+  for (int ch = 0; ch < 8; ch++)
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      const uint32_t v = code_at<B>(w, 8 * ch + j) | (code_at<B>(w, 8 * ch + j + 4) << 16) | 0x43004300u;
+      const uint32_t qv = bfma2(v, 0x3f803f80u, 0xc300c300u);  // the codes, exact
+      a[4 * ch + j] = bfma2(qv, s2, b2);                      // bf16(s*q + b)
+    }
+}
+
+__device__ __forceinline__ void dequant_row_bits(int bits, const uint8_t *buf, int r, int u, uint32_t half,
+                                                 uint32_t (&a)[32]) {
+  if (bits == 4)
+    ws_dequant_row(buf, r, u, half, a);
+  else if (bits == 3)
+    ws_dequant_row_lb<3>(buf, r, u, half, a);
+  else
+    ws_dequant_row_lb<2>(buf, r, u, half, a);
+}
+
+template <int MODE, bool LB = false>
 __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__ PfParams P) {
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
@@ -519,7 +577,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       PfItem snext{};
       StgRows srow{};
       int slt = 0;
-      if (my_tiles > 0) srow = stage_rows<MODE>(P, ws_item<MODE>(P, tile_of(0)), t);
+      if (my_tiles > 0) srow = stage_rows<MODE, LB>(P, ws_item<MODE>(P, tile_of(0)), t);
       if (my_tiles > 1) snext = ws_item<MODE>(P, tile_of(1));
       auto issue = [&](int c) {
         if (c >= total) {
@@ -528,7 +586,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         }
         const int lt = c / nct;
         if (lt != slt) {
-          srow = stage_rows<MODE>(P, lt == slt + 1 ? snext : ws_item<MODE>(P, tile_of(lt)), t);
+          srow = stage_rows<MODE, LB>(P, lt == slt + 1 ? snext : ws_item<MODE>(P, tile_of(lt)), t);
           slt = lt;
           if (lt + 1 < my_tiles) snext = ws_item<MODE>(P, tile_of(lt + 1));
         }
@@ -538,6 +596,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       issue(1);
       // parity of the weight row = parity of r (tile row bases are even)
       const uint32_t rodd = (uint32_t)(r & (inp / 64) & 1);
+      int qlt = -1, qbits = 4;  // the tile being dequantized and its code width
       bool ok = true;
       for (int c = 0; c < total && ok; c++) {
         tc05::cp_wait_group<1>();  // this thread's copies of chunk c are done
@@ -546,6 +605,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         const int lt = c / nct, kc = c - lt * nct;
         const uint8_t *buf = stg + (c % kNStg) * kStgBuf;
         const int ns = min(kChunk, nk - kc * kChunk);
+        if (LB && lt != qlt) qbits = item_bits<LB>(P, ws_item<MODE>(P, tile_of(lt))), qlt = lt;
         const int u0 = kPA * hf;  // this group's A stage of the chunk, if the chunk has it
         if (u0 < ns) {
           // A stage ga of this CTA's sequence ((nk + kPA - 1) / kPA stages a tile)
@@ -556,10 +616,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
             // scale / bias: the half of the staged 4-byte word holding entry row * G + kk
             const int kk0 = kc * kChunk + u0;
             uint32_t av0[32], av1[32];
-            ws_dequant_row(buf, r, u0, (rodd + (uint32_t)kk0) & 1u, av0);
+            if (LB) dequant_row_bits(qbits, buf, r, u0, (rodd + (uint32_t)kk0) & 1u, av0);
+            else ws_dequant_row(buf, r, u0, (rodd + (uint32_t)kk0) & 1u, av0);
             tc05::st32(ta, av0);
             if (u0 + 1 < ns) {
-              ws_dequant_row(buf, r, u0 + 1, (rodd + (uint32_t)kk0 + 1u) & 1u, av1);
+              if (LB) dequant_row_bits(qbits, buf, r, u0 + 1, (rodd + (uint32_t)kk0 + 1u) & 1u, av1);
+              else ws_dequant_row(buf, r, u0 + 1, (rodd + (uint32_t)kk0 + 1u) & 1u, av1);
               tc05::st32(ta + 32, av1);
             }
             tc05::wait_st();
@@ -1027,6 +1089,12 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if ((e = cudaFuncSetAttribute(pf_gemm<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Lay<MODE_ROUTER>::smem)))
     return e;
+  if ((e = cudaFuncSetAttribute(pf_gemm<MODE_GATE_UP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Lay<MODE_GATE_UP>::smem)))
+    return e;
+  if ((e = cudaFuncSetAttribute(pf_gemm<MODE_DOWN, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                Lay<MODE_DOWN>::smem)))
+    return e;
   if ((e = cudaFuncSetAttribute(pf_gemm<MODE_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 Lay<MODE_GATE_UP>::smem)))
     return e;
@@ -1050,9 +1118,15 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if (!p.route_only) {
     pf_gather<<<(int)((ent_cap + 7) / 8), 256, 0, st>>>(p);
     if ((e = mark(7))) return e;
-    pf_gemm<MODE_GATE_UP><<<p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st>>>(p);
+    if (p.bits == 4)
+      pf_gemm<MODE_GATE_UP><<<p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st>>>(p);
+    else
+      pf_gemm<MODE_GATE_UP, true><<<p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st>>>(p);
     if ((e = mark(8))) return e;
-    pf_gemm<MODE_DOWN><<<p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st>>>(p);
+    if (p.bits == 4)
+      pf_gemm<MODE_DOWN><<<p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st>>>(p);
+    else
+      pf_gemm<MODE_DOWN, true><<<p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st>>>(p);
     if ((e = mark(9))) return e;
     pf_final<<<1024, 256, 0, st>>>(p);
     if ((e = mark(10))) return e;

@@ -29,6 +29,7 @@ struct PfParams {
   CUtensorMap tm_h;
   CUtensorMap tm_h32;
   int H, E, K, I, t;
+  int bits;                // routed records' code width (2, 3 or 4); the shared record is 4-bit
   int n_sms;
   uint32_t flags;
   int route_only;          // stop after the grouping

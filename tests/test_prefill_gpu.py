@@ -152,9 +152,34 @@ def test_prefill_group_small(moe, H, E, k, I, t, shared, flags):
     assert np.allclose(g["wts"], ref["wts"], rtol=0, atol=1e-5), "grouped weights"
 
 
-def test_prefill_rejects_lowbit_records(moe):
+LOWBIT = [
+    # H, E, k, I, t, shared, flags, bits
+    (768, 40, 5, 384, 300, True, synth.RESIDUAL | synth.PRENORM, 3),
+    (512, 130, 4, 256, 129, True, synth.PRENORM, 3),
+    (768, 40, 5, 384, 300, True, synth.RESIDUAL | synth.PRENORM, 2),
+    (256, 8, 2, 192, 37, False, 0, 2),
+]
+
+
+@pytest.mark.parametrize("H,E,k,I,t,shared,flags,bits", LOWBIT)
+def test_prefill_lowbit(moe, H, E, k, I, t, shared, flags, bits):
+    """2- and 3-bit routed records (the shared expert stays 4-bit): codes that
+    straddle 32-bit words, rows of 16 or 24 bytes a k-panel."""
+    rng = np.random.default_rng(3000 + H + E + t + bits)
+    layer = synth.make_layer(rng, H, E, k, I, bits, shared=shared, flags=flags, scale=(0.01, 0.04), bias_noise=0.0)
+    ol = oracle.Layer(layer)
+    x = rows_with_gap(ol, rng, t, H)
+    dl = moe.DeviceLayers([layer])
+    got, idx = run_prefill(moe, dl, x)
+    ref = oracle.prefill_rows(ol, x, np.arange(t), mirror=True)
+    assert np.array_equal(idx, ref["idx"]), "top-k ids"
+    assert_prefill_close(got, ref, x, flags, np.arange(t), f"prefill {bits}-bit H{H} E{E} k{k} I{I} t{t}")
+
+
+def test_prefill_rejects_unaligned_3bit_rows(moe):
+    # 3-bit rows of inter 192 codes are 72 bytes: not a multiple of 16
     rng = np.random.default_rng(5)
-    layer = synth.make_layer(rng, 256, 8, 2, 128, 3, shared=False)
+    layer = synth.make_layer(rng, 256, 8, 2, 192, 3, shared=False)
     dl = moe.DeviceLayers([layer])
     assert moe.prefill_workspace(dl, 16) == 0
     x = torch.zeros((16, 256), dtype=torch.float32, device="cuda")
