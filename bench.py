@@ -8,7 +8,7 @@ Metric: MoE-layer rows per second = nb * layers / step time; the HBM roofline
 fraction of the kernel is reported beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload c1|c2|c3b3|c3b2|c4] [--nb NB]
+                  [--workload c1|c2|c3b3|c3b2|c4|c4b3] [--nb NB]
 
 --workload c4 times the prefill chunk instead (moe_prefill, 10 kernels per
 step; the roofline is the tensor-pipe one of its largest GEMM).
@@ -39,6 +39,9 @@ WORKLOADS = {
     "c3b2": "one MoE layer, nb=4: hidden 2048, 512 experts, top-10, inter 512, 2-bit routed records",
     "c4": "prefill chunk of 4096 rows through one MoE layer: hidden 2048, 512 experts, top-10, inter 512, "
           "shared expert, 4-bit g64 records, Zipf(1.1) expert popularity; bf16 tensor-core GEMMs, bf16 out",
+    "c4b3": "prefill chunk of 4096 rows through one MoE layer: hidden 2048, 512 experts, top-10, inter 512, "
+            "shared expert (4-bit), 3-bit g64 routed records, Zipf(1.1) expert popularity; bf16 tensor-core "
+            "GEMMs, bf16 out",
 }
 METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 1 GB300"
 
@@ -47,10 +50,10 @@ METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 
 # (profiles/decode_c1.md, profiles/prefill_c4.md).  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
 NCU_TRAFFIC = {
-    "c1": dict(bytes=1206.6e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],
-               sha="77dd22dd36d405ab"),
-    "c4": dict(bytes=640.6e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
-               sha="00e9adc179317485"),
+    "c1": dict(bytes=1207.1e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],
+               sha="ccd00c4b5cd811dc"),
+    "c4": dict(bytes=641.1e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
+               sha="f2a1fa0502aa2f91"),
 }
 
 
@@ -253,10 +256,10 @@ def run_prefill(args, rank, world, device):
     build.build()
     moe.lib()
     torch.cuda.set_device(device)
-    cfg = synth.CONFIGS["c4"]
+    cfg = synth.CONFIGS[args.workload]
     t = args.nb or cfg["nb"]
     H, E, k, I = cfg["hidden"], cfg["n_experts"], cfg["top_k"], cfg["inter"]
-    layers = synth.make_device_layers("c4", seed=1 + rank, device=device)
+    layers = synth.make_device_layers(args.workload, seed=1 + rank, device=device)
     rng = np.random.default_rng(40 + rank)
     layers[0].router = torch.from_numpy(synth.zipf_router_bits(rng, E, H).view(np.int16)).to(device)
     dl = moe.DeviceLayers(layers, device=device)
@@ -287,8 +290,8 @@ def run_prefill(args, rank, world, device):
     flops = {"router_gemm": 2.0 * E * t * 2 * H, "gate_up_gemm": 2.0 * ent * 2 * I * H,
              "down_gemm": 2.0 * ent * H * I}
     from quantized_routed_expert_fn_gb300.synth import record_layout
-    rec = record_bytes(record_layout(H, I, 4))
-    bytes_per_step = (used + 1) * rec + E * H * 2 + H * 2 + t * H * 4 + t * H * 2
+    rec, srec = record_bytes(record_layout(H, I, cfg["bits"])), record_bytes(record_layout(H, I, 4))
+    bytes_per_step = used * rec + srec + E * H * 2 + H * 2 + t * H * 4 + t * H * 2
 
     dist = world > 1
     if dist:
@@ -342,13 +345,13 @@ def run_prefill(args, rank, world, device):
                 used_experts=used, max_rows=int(counts.max()))
 
 
-def oracle_prefill_sample(t, budget_s):
+def oracle_prefill_sample(t, budget_s, workload="c4"):
     """Time the oracle's prefill rows (bf16 mirror, as the parity tests use it)
     on host cores over the first rows of the same chunk, drawn on the host."""
     import oracle
     from quantized_routed_expert_fn_gb300 import synth
     rng = np.random.default_rng(40)
-    layer = synth.make_config_layers("c4", seed=1000, n_layers=1)[0]
+    layer = synth.make_config_layers(workload, seed=1000, n_layers=1)[0]
     synth.zipf_router(rng, layer)
     x = synth.make_prefill_x(rng, t, layer.hidden)
     ol = oracle.Layer(layer)
@@ -407,13 +410,14 @@ def main():
     config = {"workload": WORKLOADS[args.workload], "nb": nb, "layers": args.layers or cfg["n_layers"],
               "l2": "inputs larger than L2 (each step streams every layer's union records once)"}
 
-    if args.workload == "c4":
-        config = {"workload": WORKLOADS["c4"], "t": nb, "layers": 1,
+    prefill = args.workload in ("c4", "c4b3")
+    if prefill:
+        config = {"workload": WORKLOADS[args.workload], "t": nb, "layers": 1,
                   "l2": "inputs larger than L2 (about 0.9 GB of expert records per step)"}
-    if args.impl == "reference" and args.workload == "c4":
+    if args.impl == "reference" and prefill:
         if rank != 0:
             return
-        s = oracle_prefill_sample(nb, budget_s=min(args.cpu_budget, 20.0))
+        s = oracle_prefill_sample(nb, budget_s=min(args.cpu_budget, 20.0), workload=args.workload)
         line = {"metric": METRIC, "value": s["value"], "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": 1000.0 * nb / s["value"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
@@ -442,11 +446,11 @@ def main():
         import torch.distributed as td
         td.init_process_group("nccl", device_id=torch.device(f"cuda:{local}"))
     device = torch.device(f"cuda:{local}")
-    if args.workload == "c4":
+    if prefill:
         r = run_prefill(args, rank, world, device)
         if rank == 0:
-            cpu = oracle_prefill_sample(nb, budget_s=args.cpu_budget)
-            H = synth.CONFIGS["c4"]["hidden"]
+            cpu = oracle_prefill_sample(nb, budget_s=args.cpu_budget, workload=args.workload)
+            H = synth.CONFIGS[args.workload]["hidden"]
             line = {
                 "metric": METRIC, "value": job_rows_per_s(r["t"], world, r["ms"]), "unit": "rows/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms"], "higher_is_better": True,
@@ -456,7 +460,7 @@ def main():
                 "gpu_launches": args.steps * 10,
                 "roofline": {"bound": "tensor", "achieved": r["achieved"], "peak": r["peak"], "unit": "TFLOP/s",
                              "frac": r["achieved"] / r["peak"],
-                             "traffic": ncu_traffic("c4") if r["top"] == "gate_up_gemm" else None,
+                             "traffic": ncu_traffic(args.workload) if r["top"] == "gate_up_gemm" else None,
                              "kernel": r["top"],
                              "peak_source": r["peak_kind"] + " bf16 burst",
                              "algorithmic_flops_per_launch": r["flops"][r["top"]]},

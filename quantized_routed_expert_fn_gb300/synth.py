@@ -211,6 +211,9 @@ CONFIGS = {
                  scale=(0.01, 0.04), bias_noise=0.0),
     # prefill chunk of 4096 tokens
     "c4": dict(hidden=2048, n_experts=512, top_k=10, inter=512, bits=4, shared=True, n_layers=1, nb=4096),
+    # the same chunk over 3-bit routed records
+    "c4b3": dict(hidden=2048, n_experts=512, top_k=10, inter=512, bits=3, shared=True, n_layers=1, nb=4096,
+                 scale=(0.01, 0.04), bias_noise=0.0),
 }
 
 
