@@ -37,7 +37,6 @@ namespace {
 
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
-constexpr int MAXIT = 4;
 constexpr int kProducerWarp = 1;  // issues the bulk copies (thread 0 does the cross-CTA releases)
 // The weight units of a layer go to two groups of eight warps in turn (unit q
 // to group q % 2), so that one group's reductions, global writes and
@@ -61,12 +60,6 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ uint32_t orderable(float f) {
   uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// bf16 hi / lo split of an fp32 value: v ~= hi + lo to 16 significant bits.
-__device__ __forceinline__ uint32_t split_part(float v, int hl) {
-  uint32_t h = f2bf(v);
-  return hl ? f2bf(v - __uint_as_float(h << 16)) : h;
 }
 
 // (a, b) -> bf16x2 hi = (bf16(a), bf16(b)) and lo = bf16 of the remainders (a first, low half)
@@ -102,12 +95,6 @@ __device__ bool cta_wait(const unsigned *p, unsigned target, const FwdParams &P,
   const bool ok = *flag;
   __syncthreads();
   return ok;
-}
-
-// All threads: publish this CTA's writes, then add v to *p (release).
-__device__ void cta_signal(unsigned *p, unsigned v) {
-  __syncthreads();
-  if (threadIdx.x == 0) red_release_add(p, v);
 }
 
 // Unit group g (threads GT*g .. GT*g+GT-1): barrier 1 + g, and the same with

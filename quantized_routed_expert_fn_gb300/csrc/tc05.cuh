@@ -68,17 +68,6 @@ __device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b
       : "memory");
 }
 
-// One thread: D[tmem] (+)= A * B over k = 16 with A read from tensor memory
-// (128 lanes = rows; 8 consecutive 32-bit columns, two bf16 each, in k order).
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // Warp (converged): true in exactly one lane.
 __device__ __forceinline__ bool elect_one() {
   uint32_t r;
@@ -86,8 +75,9 @@ __device__ __forceinline__ bool elect_one() {
   return r != 0;
 }
 
-// One thread: the four K=16 MMAs of a 64-wide k-stage, A in TMEM (columns
-// a, a+8, a+16, a+24), B from the 128B-swizzled K-major stage whose
+// One thread: the four K=16 MMAs of a 64-wide k-stage, A in TMEM (128 lanes
+// = rows; columns a, a+8, a+16, a+24, each 8 columns of two bf16 in k
+// order), B from the 128B-swizzled K-major stage whose
 // descriptor is b_desc (each step moves 32 bytes along k: +2 in the
 // descriptor's address field).  accumulate: whether the first MMA adds to D.
 __device__ __forceinline__ void mma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
@@ -103,18 +93,6 @@ __device__ __forceinline__ void mma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
-// Warp: 16 consecutive 32-bit columns of the warp's 32 TMEM lanes from
-// registers, then wait until the stores have completed.
-__device__ __forceinline__ void st16_wait(uint32_t taddr, const uint32_t (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // Warp: 32 consecutive 32-bit columns from registers; the registers must
 // stay untouched until wait_st().
 __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&v)[32]) {
@@ -128,19 +106,6 @@ __device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&v)[32]) {
       : "memory");
 }
 __device__ __forceinline__ void wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// The same for 32 columns, waiting for the stores.
-__device__ __forceinline__ void st32_wait(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 
 // One thread: arrive on the mbarrier once all MMAs issued so far complete.
 __device__ __forceinline__ void commit(uint64_t *bar) {
