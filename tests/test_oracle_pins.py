@@ -376,12 +376,14 @@ def test_group_invariants_random():
     assert len(seen) == n * k
 
 
-def test_prefill_mirror_matches_dense_bf16_bruteforce():
+@pytest.mark.parametrize("bits", [4, 3, 2])
+def test_prefill_mirror_matches_dense_bf16_bruteforce(bits):
     """The bf16 mirror equals a dense numpy evaluation with x^, W, h and the
-    output rounded to bf16 (round to nearest even, via float32, exact here)."""
-    rng = np.random.default_rng(33)
+    output rounded to bf16 (round to nearest even, via float32, exact here);
+    routed records of every width, the shared record 4-bit."""
+    rng = np.random.default_rng(33 + bits)
     H, E, k, I = 128, 6, 2, 64
-    layer = synth.make_layer(rng, H, E, k, I, 4, flags=synth.RESIDUAL | synth.PRENORM)
+    layer = synth.make_layer(rng, H, E, k, I, bits, flags=synth.RESIDUAL | synth.PRENORM)
     ol = oracle.Layer(layer)
     x = rng.normal(size=(5, H)).astype(np.float32)
     got = oracle.prefill_rows(ol, x, np.arange(5), mirror=True)
