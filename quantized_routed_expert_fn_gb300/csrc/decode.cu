@@ -4,16 +4,19 @@
 //   R  each CTA loads the layer input (applying the unit RMSNorm when asked),
 //      stages it as bf16 hi/lo tensor-core fragments, and computes its share of
 //      the router rows (bf16 router x fp32 input on CUDA cores) plus the
-//      shared-gate dot; a release counter publishes the logits.
-//   T  every CTA waits for all router rows, then computes top-k, softmax and
-//      the union itself (identical in every CTA, so no second grid-wide
+//      shared-gate dot, each logit published as one 64-bit word that carries
+//      its own ready flag.
+//   T  every CTA polls all logits, then computes top-k, softmax and the
+//      union itself (identical in every CTA, so no second grid-wide
 //      handshake); CTA 0 publishes slot table, weight map and ids.
 //   G  gate_up units (internal slot, 16 gate rows + the matching 16 up rows)
 //   D  down units (slot, 64 output rows).
-// Weight tiles of the units reach shared memory through bulk (TMA) copies:
-// one thread keeps a ring of `stages` units in flight, so HBM streams while
-// the warps compute.  The shared expert's first gate_up units do not depend
-// on routing and are requested before the layer input is even available.
+// Weight tiles of the units reach shared memory through bulk (TMA) copies
+// into a ring of `stages` units, so HBM streams while the warps compute; the
+// units go to two groups of eight warps in turn (named barriers per group),
+// and the group that frees a stage requests the unit `stages` places ahead.
+// The shared expert's first gate_up units do not depend on routing and are
+// requested before the layer input is even available.
 // Codes are expanded to exact bf16 integers and multiplied on the tensor
 // cores against the staged activations; scale and bias apply per 64-code
 // group in fp32; h = silu(gate) * up is stored as bf16 hi/lo fragments for
@@ -37,7 +40,7 @@ namespace {
 
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
-constexpr int kProducerWarp = 1;  // issues the bulk copies (thread 0 does the cross-CTA releases)
+constexpr int kProducerWarp = 1;  // warp (of the CTA, then of each unit group) that issues the bulk copies
 // The weight units of a layer go to two groups of eight warps in turn (unit q
 // to group q % 2), so that one group's reductions, global writes and
 // releases overlap the other group's tensor-core work.
