@@ -72,8 +72,7 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t &hi, uint32_t 
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(lo) : "f"(rb), "f"(ra));
 }
 
-// ceil(c*n/g), floor(c*n/g); c*n stays far below 2^31 for every shape accepted
-__device__ __forceinline__ int cdiv_mul(int c, int n, int g) { return (c * n + g - 1) / g; }
+// floor(c*n/g); c*n stays far below 2^31 for every shape accepted
 __device__ __forceinline__ int fdiv_mul(int c, int n, int g) { return c * n / g; }
 
 // Thread 0: poll *p until it reaches target, the call aborts, or the deadline passes.
@@ -570,14 +569,22 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
 
 // ------------------------------------------------------------ unit schedule
 
+// The layer's gate_up units form one list, slot by slot (the shared expert's
+// first), and so do its down units; CTA c takes list entries c, c + G,
+// c + 2G, ... of each (G = grid size).  A slot's units then sit in the same
+// position of consecutive CTAs, so slots complete in waves and the first
+// down units find their h ready early.  The shared expert's gate_up units are
+// known before routing (nA of this CTA's first units).
 struct Sched {
   int hsi, ups, nrt, U, nslots;
-  int early;        // shared gate_up units assigned before routing
-  int nA, sA0;      // early shared units of this CTA
-  int nB, rB0;      // gate_up units after routing (routed only if early, else shared + routed)
-  int nD, d0;       // down units
-  __device__ int n() const { return nA + nB + nD; }
+  int nA;    // this CTA's shared gate_up units (requested before routing)
+  int nGU;   // this CTA's gate_up units (shared + routed)
+  int nD;    // this CTA's down units
+  __device__ int n() const { return nGU + nD; }
 };
+
+// entries c, c + G, ... of a list of T
+__device__ __forceinline__ int rr_count(int c, int T, int G) { return T > c ? (T - c + G - 1) / G : 0; }
 
 struct UnitDesc {
   int down, slot, row0;  // row0: gate_up chunk start (inter rows) or down output row start
@@ -590,16 +597,13 @@ template <int BITS>
 __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP &L,
                                              const uint8_t *const *rect) {
   UnitDesc d;
-  if (q < s.nA) {
-    d.down = 0, d.slot = 0, d.row0 = (s.sA0 + q) * 16;
-  } else if (q < s.nA + s.nB) {
-    const int r = s.rB0 + (q - s.nA);
-    d.down = 0;
-    d.slot = (s.early ? s.hsi : 0) + r / s.ups;
-    d.row0 = (r % s.ups) * 16;
+  const int c = blockIdx.x, G = gridDim.x;
+  if (q < s.nGU) {
+    const int u = c + q * G;  // entry of the gate_up list
+    d.down = 0, d.slot = u / s.ups, d.row0 = (u % s.ups) * 16;
   } else {
-    const int r = s.d0 + (q - s.nA - s.nB);
-    d.down = 1, d.slot = r / s.nrt, d.row0 = (r % s.nrt) * 64;
+    const int v = c + (q - s.nGU) * G;  // entry of the down list
+    d.down = 1, d.slot = v / s.nrt, d.row0 = (v % s.nrt) * 64;
   }
   const bool shared = s.hsi && d.slot == 0;
   d.rec = shared ? L.srec : rect[d.slot];
@@ -705,10 +709,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.hsi = hs ? 1 : 0;
     s.ups = I / 16;
     s.nrt = H / 64;
-    s.early = hs && !P.route_only && (K + 1) * s.ups >= G;
-    s.sA0 = s.early ? cdiv_mul(cta, s.ups, G) : 0;
-    s.nA = s.early ? cdiv_mul(cta + 1, s.ups, G) - s.sA0 : 0;
-    s.nB = s.nD = s.rB0 = s.d0 = 0;
+    s.nA = hs && !P.route_only ? rr_count(cta, s.ups, G) : 0;
+    s.nGU = s.nA, s.nD = 0;  // until routing is known
     s.U = 0;
     int issued = 0;
     if (warp == kProducerWarp) {
@@ -901,18 +903,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     // ---- schedule of this CTA's units for the layer
     __syncthreads();
     s.nslots = s.U + s.hsi;
-    if (s.early) {
-      const int T = (s.U + 1) * s.ups;  // shared + routed gate_up units
-      s.rB0 = fdiv_mul(cta, T, G) - cdiv_mul(cta, s.ups, G);
-      s.nB = fdiv_mul(cta + 1, T, G) - cdiv_mul(cta + 1, s.ups, G) - s.rB0;
-    } else {
-      const int T = s.nslots * s.ups;
-      s.rB0 = fdiv_mul(cta, T, G);
-      s.nB = fdiv_mul(cta + 1, T, G) - s.rB0;
-    }
-    const int ND = s.nslots * s.nrt;
-    s.d0 = fdiv_mul(cta, ND, G);
-    s.nD = fdiv_mul(cta + 1, ND, G) - s.d0;
+    s.nGU = rr_count(cta, s.nslots * s.ups, G);
+    s.nD = rr_count(cta, s.nslots * s.nrt, G);
     const int n = s.n();
     if (warp == kProducerWarp) {
       for (int q = issued; q < n && q < S; q++) issue_at(get_unit<BITS>(q, s, L, rect), qbase + q);
@@ -934,7 +926,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   if (P.trace && gt == 0 && cta < kTraceCtas)                                                    \
     P.trace[((size_t)l * kTraceCtas + cta) * kTracePhases + (k)] = globaltimer();
       for (int q = grp; q < n && alive; q += kGroups) {
-        if (q == s.nA + s.nB) {
+        if (q == s.nGU) {
           MOE_GSTAMP(6)
           if (gt == 0 && l + 1 < P.nl) {
             // the next layer's router rows of this CTA, toward L2 while the down units run
@@ -1026,7 +1018,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           }
           grp_signal(cnt + kCntGu + d.slot, 1u, grp, gt);
           if (q == 0) MOE_STAMP(13)
-          if (q == s.nA + s.nB - 1) MOE_GSTAMP(14)
+          if (q == s.nGU - 1) MOE_GSTAMP(14)
         } else {
           const int rt = d.row0 / 64;
           for (int j = gt; j < 64 * nb; j += GT) {
@@ -1059,7 +1051,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
             grp_signal(cnt + kCntRows, 1u, grp, gt);
           }
           grp_sync(grp);
-          if (q == s.nA + s.nB) MOE_GSTAMP(15)
+          if (q == s.nGU) MOE_GSTAMP(15)
         }
       }
       if (!alive) sflag[8] = 1;
