@@ -106,3 +106,27 @@ def test_route_requires_outputs(m):
     arr = _struct(m, L)
     r = m.lib().moe_route(arr, 0x1000, 1, None, None, 0x2000, 0x3000, 0x4000, 0x100000, 1 << 30, 0x5000, None)
     assert r == -1
+
+
+@pytest.mark.parametrize("bits,inter,ok", [(4, 256, True), (3, 256, True), (2, 256, True), (2, 192, True),
+                                           (3, 192, False), (5, 256, False)])
+def test_prefill_workspace_by_width(m, bits, inter, ok):
+    """moe_prefill_workspace sizes 4/3/2-bit layers alike and returns 0 for
+    layers prefill rejects: a width outside {2, 3, 4}, or 3-bit rows that are
+    not whole 16-byte pieces (inter % 128 != 0)."""
+    L = _layer(I=inter, bits=bits if bits != 5 else 4)
+    arr = _struct(m, L, bits=bits)
+    n = m.lib().moe_prefill_workspace(arr, 4096)
+    assert (n > 0) == ok, m.last_error()
+    if ok:
+        ref = m.lib().moe_prefill_workspace(_struct(m, _layer(I=inter)), 4096)
+        assert n == ref  # the workspace does not depend on the record width
+
+
+def test_prefill_rejects_bad_calls(m):
+    L = _layer()
+    arr = _struct(m, L)
+    lib = m.lib()
+    assert lib.moe_prefill_workspace(arr, 0) == 0
+    assert lib.moe_prefill_workspace(arr, (1 << 20) + 1) == 0
+    assert lib.moe_prefill_workspace(_struct(m, L, top_k=33), 16) == 0
