@@ -681,6 +681,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   if (tid == 0) {
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu;
     fence_mbar_init();
+    sflag[9] = 0;
   }
   // activation registers and sums: rows b >= nb stay zero for the whole call
   for (uint32_t *z = reinterpret_cast<uint32_t *>(xa) + tid; z < reinterpret_cast<uint32_t *>(cs4 + 4 * ng); z += NT)
@@ -925,7 +926,14 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
 #define MOE_GSTAMP(k)                                                                            \
   if (P.trace && gt == 0 && cta < kTraceCtas)                                                    \
     P.trace[((size_t)l * kTraceCtas + cta) * kTracePhases + (k)] = globaltimer();
-      for (int q = grp; q < n && alive; q += kGroups) {
+      // the groups take the layer's units in order, each the next free one
+      // (sflag[9]: next unit; sflag[10 + g]: group g's pick), so neither
+      // group idles while the other still has several units
+      for (;;) {
+        if (gt == 0) sflag[10 + grp] = atomicAdd(const_cast<int *>(sflag + 9), 1);
+        grp_sync(grp);
+        const int q = sflag[10 + grp];
+        if (q >= n || !alive) break;
         if (q == s.nGU) {
           MOE_GSTAMP(6)
           if (gt == 0 && l + 1 < P.nl) {
@@ -1062,6 +1070,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       drain_stages(bars, stg_unit, S, P);
       return;
     }
+    if (tid == 0) sflag[9] = 0;  // the next layer's unit counter (read after several barriers)
     qbase += (unsigned)n;
     MOE_STAMP(7)
 #undef MOE_STAMP
