@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_group.restype = i32
         _lib.oracle_group.argtypes = [i32, i32, i32, p, p, p, p, p, p]
         _lib.oracle_threads.restype = i32
+        _lib.oracle_round_bf16.restype = d
+        _lib.oracle_round_bf16.argtypes = [d]
+        _lib.oracle_expert_mirror.argtypes = [p, ctypes.POINTER(OQ), ctypes.POINTER(OQ), i32, i32, p, d, p, p]
     return _lib
 
 
@@ -227,6 +230,23 @@ def group(n_experts: int, idx: np.ndarray, w: np.ndarray, gamma: np.ndarray | No
     g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float64)
     lib().oracle_group(n_experts, k, n, _ptr(idx), _ptr(w), _ptr(g), _ptr(offs), _ptr(rows), _ptr(wts))
     return dict(offs=offs, rows=rows, wts=wts)
+
+
+def round_bf16(v: float) -> float:
+    """The oracle's bf16 rounding (nearest, ties to even) of one value."""
+    return float(lib().oracle_round_bf16(float(v)))
+
+
+def expert_mirror(record: np.ndarray, layout, x: np.ndarray, weight: float) -> dict:
+    """One expert record on one row in bf16-mirror mode: y and the one-flip
+    allowance of the h rounding (a test tolerance term)."""
+    record = np.ascontiguousarray(record, dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    y = np.empty(layout.hidden)
+    allow = np.zeros(layout.hidden)
+    lib().oracle_expert_mirror(_ptr(record), ctypes.byref(_oq(layout.gate_up)), ctypes.byref(_oq(layout.down)),
+                               layout.bits, layout.inter, _ptr(x), float(weight), _ptr(y), _ptr(allow))
+    return dict(y=y, allow=allow)
 
 
 def threads() -> int:

@@ -218,6 +218,17 @@ static void expert_row(const uint8_t *rec, const oq_t *gu, const oq_t *dn, int b
   free(h);
 }
 
+/* Exported for the rounding pin: round_bf16 on one value. */
+double oracle_round_bf16(double v) { return round_bf16(v); }
+
+/* Exported for the allowance pin: one expert on one row in mirror mode, with
+ * the one-flip allowance of its h rounding max-accumulated into allow[hidden]
+ * (which the caller zeroes). */
+void oracle_expert_mirror(const uint8_t *rec, const oq_t *gu, const oq_t *dn, int bits, int inter,
+                          const double *x, double weight, double *y, double *allow) {
+  expert_row(rec, gu, dn, bits, inter, x, y, 1, weight, allow);
+}
+
 /* Exported for the brute-force pin: expert `e` of a layer on one row. */
 void oracle_expert(const oracle_layer_t *L, int e, const double *x, double *y) {
   expert_row(L->experts + (uint64_t)e * L->stride, &L->gate_up, &L->down, L->bits, L->inter, x, y,

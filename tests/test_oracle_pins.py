@@ -414,3 +414,82 @@ def test_prefill_mirror_matches_dense_bf16_bruteforce(bits):
         ulp = np.abs(want) * 2.0 ** -7
         assert np.all(np.abs(got["out"][b] - want) <= ulp), f"row {b}"
         assert np.mean(got["out"][b] == want) > 0.99
+
+
+# ------------------------------------------------------------------ bf16 mirror helpers
+
+def test_round_bf16_fixtures():
+    """The mirror's bf16 rounding against hand-written round-to-nearest-even
+    cases: exact ties both ways, values just off a tie, negatives, a carry
+    into the exponent."""
+    n = 0
+    for line in _golden_lines("bf16_round.txt"):
+        v, b = line.split()
+        got = oracle.round_bf16(float(v))
+        want = oracle.bf16(int(b, 16))
+        assert got == want, f"{v}: {got!r} != {want!r} (bits {b})"
+        n += 1
+    assert n >= 12
+
+
+def _allowance_record(q63: int):
+    """A hand-built 4-bit expert, hidden 64, inter 64 (one 64-code group per row):
+      gate row 0: scale 0.5, codes (2, 1 x 62, 0)       -> g0 = 32 on the x below
+      up row 0:   scale 2^-14, codes 15 x 34, 1, 0 ..., q63 at position 63
+                                                      -> u0 = 2^-14 (511 + q63 2^-11)
+      every other up row: scale 0 -> u = 0, h = 0 (never near a boundary)
+      down: fixed bf16 weights, W_d[o][0] = (o + 1) / 64 (scale 1/64, code o % 15 + 1)
+    with x = (1 x 63, 2^-11).  Then h0 = silu(32) u0 = 511/512 + q63 2^-20 (up to
+    a relative 1.3e-14): just above the bf16 midpoint 0.998046875 between
+    0.99609375 and 1.0, so h0 rounds to 1.0 and the value across the boundary
+    is 0.99609375 (one step of 2^-8 below)."""
+    lay = synth.record_layout(64, 64, 4)
+    rec = np.zeros(lay.stride, dtype=np.uint8)
+    gu, dn = lay.gate_up, lay.down
+    codes = np.zeros((128, 64), dtype=np.uint32)
+    codes[0, 0], codes[0, 1:63] = 2, 1
+    codes[64, :34], codes[64, 34], codes[64, 63] = 15, 1, q63
+    rec[gu.w:gu.w + 128 * 32] = synth.pack_codes(codes, 4).reshape(-1).view(np.uint8)
+    s = np.zeros(128, dtype=np.uint16)
+    s[0], s[64] = 0x3F00, 0x3880  # 0.5, 2^-14
+    rec[gu.s:gu.s + 256] = s.view(np.uint8)
+    dcodes = np.zeros((64, 64), dtype=np.uint32)
+    dcodes[:, 0] = np.arange(64) % 15 + 1
+    dcodes[:, 1:] = 3
+    rec[dn.w:dn.w + 64 * 32] = synth.pack_codes(dcodes, 4).reshape(-1).view(np.uint8)
+    rec[dn.s:dn.s + 128] = np.full(64, 0x3C80, dtype=np.uint16).view(np.uint8)  # 1/64
+    x = np.ones(64)
+    x[63] = 2.0 ** -11
+    return rec, lay, x, (dcodes[:, 0] / 64.0)
+
+
+def test_flip_allowance_hand_case():
+    """The allowance that widens the prefill bound, pinned by hand.  The band
+    of h0 is 2^-20 (|silu(g)| sum|up terms| + 1.1 |u| sum|gate terms|) +
+    2^-22 |h| ~= 2^-20 (0.998 + 1.098) + 2.4e-7 ~= 2.24e-6.
+      q63 = 2: h0 sits 2 x 2^-20 = 1.9e-6 above the midpoint -> inside the band:
+               allow[o] = |w W_d[o][0] (0.99609375 - 1.0)| = |w W_d[o][0]| 2^-8 exactly;
+      q63 = 3: 3 x 2^-20 = 2.9e-6 above it -> outside: allow = 0.
+    A band exponent one off either way (-19 or -21), a truncating bf16 round,
+    or the neighbour taken on the wrong side each breaks one of the two."""
+    w = 0.75
+    rec, lay, x, wd0 = _allowance_record(2)
+    assert oracle.round_bf16(0.998046875 + 2 * 2.0 ** -20) == 1.0
+    r = oracle.expert_mirror(rec, lay, x, w)
+    np.testing.assert_array_equal(r["allow"], np.abs(w * wd0) * 2.0 ** -8)
+    rec, lay, x, _ = _allowance_record(3)
+    r = oracle.expert_mirror(rec, lay, x, w)
+    assert np.all(r["allow"] == 0.0)
+
+
+def test_flip_allowance_zero_far_from_boundaries():
+    """h exactly on a bf16 value far from any midpoint (h0 = 1.0 - 1.3e-14 with
+    up codes summing to 512) carries no allowance."""
+    rec, lay, x, _ = _allowance_record(0)
+    codes = np.zeros((128, 64), dtype=np.uint32)
+    codes[0, 0], codes[0, 1:63] = 2, 1
+    codes[64, :34], codes[64, 34], codes[64, 35] = 15, 1, 1  # sum 512 -> h0 = silu(32)/32 ~ 1.0
+    gu = lay.gate_up
+    rec[gu.w:gu.w + 128 * 32] = synth.pack_codes(codes, 4).reshape(-1).view(np.uint8)
+    r = oracle.expert_mirror(rec, lay, x, 1.0)
+    assert np.all(r["allow"] == 0.0)
