@@ -154,11 +154,13 @@ int moe_forward_traced(const moe_layer *layers, int n_layers, const float *x, in
  * MOE_NOALLOC_MAX_WORKSPACE bytes on each GPU that loads it.
  *   - Layers whose moe_forward_workspace exceeds that size are rejected with
  *     MOE_ENOSPACE before anything runs (48 layers of hidden 2048, 128 experts,
- *     inter 768 need about 1.8 MiB at nb 1; the same stack at nb 4 needs 4.4
+ *     inter 768 need about 2.3 MiB at nb 1; the same stack at nb 4 needs 4.9
  *     MiB and is rejected).
- *   - The first call on a device looks the array's address up once
- *     (cudaGetSymbolAddress with that device current); make that first call
- *     before capturing a stream into a graph.
+ *   - The first call in each CUDA context looks the array's address up once
+ *     (cudaGetSymbolAddress with that context current) and keeps it for that
+ *     context; make that first call before capturing a stream into a graph.
+ *     A cudaDeviceReset ends the context and the array's contents with it:
+ *     the next call, in the new context, looks the address up again.
  *   - Every call on a device shares the array, so calls whose executions
  *     overlap on the GPU (different streams, or graph branches) race; order
  *     them on one stream.  Each call clears the parts that must start at zero.

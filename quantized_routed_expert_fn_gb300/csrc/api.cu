@@ -5,6 +5,8 @@
 // top_k * rows < SLOT_STRIDE; shared expert width == expert width; Q4 code
 // offsets 16-byte aligned, kept here as 256-byte alignment of every tensor)
 // plus the limits of these kernels.
+#include <cuda.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
@@ -35,16 +37,16 @@ int fail(int code, const char *fmt, ...) {
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t cnt, logits, xbuf, hfrag, ypart, total;
+  size_t cnt, lgw, xbuf, hfrag, ypart, total;
 };
 
-WsLayout ws_layout(int H, int E, int I, int nl, int nb) {
+WsLayout ws_layout(int H, int I, int nl, int nb) {
   WsLayout w{};
   size_t off = 0;
   w.cnt = off;
   off += align256((size_t)nl * moe::kCntPerLayer * 4);
-  w.logits = off;
-  off += align256((size_t)nl * 4 * (E + 1) * 8);
+  w.lgw = off;
+  off += align256((size_t)2 * moe::kMaxGrid * moe::kLogitWords * 8);
   w.xbuf = off;
   off += align256((size_t)nl * nb * H * 4);
   w.hfrag = off;
@@ -125,7 +127,7 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   if ((uintptr_t)work & 255u) return fail(MOE_EALIGN, "work must be 256-byte aligned");
   if (!route_only && overlap(x, (size_t)nb * H * 4, out, (size_t)nb * H * 4))
     return fail(MOE_EINVAL, "out overlaps x");
-  const WsLayout w = ws_layout(H, E, I, nl, nb);
+  const WsLayout w = ws_layout(H, I, nl, nb);
   if (work_bytes < w.total) return fail(MOE_ENOSPACE, "work holds %zu bytes, %zu needed", work_bytes, w.total);
 
   int dev = 0;
@@ -141,7 +143,7 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   p.status = status;
   char *base = (char *)work;
   p.cnt = (unsigned *)(base + w.cnt);
-  p.logits = (unsigned long long *)(base + w.logits);
+  p.lgw = (unsigned long long *)(base + w.lgw);
   p.xbuf = (float *)(base + w.xbuf);
   p.hfrag = (uint16_t *)(base + w.hfrag);
   p.ypart = (float *)(base + w.ypart);
@@ -197,23 +199,70 @@ int check_offsets_fit(const moe_layer *layers, int nl) {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[MOE_NOALLOC_MAX_WORKSPACE];
 
 std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[128];  // per device: the array's device address
 
-// Device address of the scratch array on the current device, looked up once
-// per device (cudaGetSymbolAddress with that device current).
-int noalloc_scratch(void **out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return fail(MOE_ECUDA, "cudaGetDevice failed");
-  if (dev < 0 || dev >= 128) return fail(MOE_ECUDA, "device ordinal %d out of range", dev);
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void *p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || !p)
-      return fail(MOE_ECUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
-    g_noalloc_ptr[dev] = p;
+// The array's device address depends on the CUDA context that loaded this
+// library's module, not only on the device number: after cudaDeviceReset, or
+// with another context current on the same device, an address looked up
+// earlier is no longer valid.  So the cache is keyed by the driver's context
+// id (unique for the life of the process; a context made after a reset gets
+// a new id).  The two driver calls are reached through the runtime's entry
+// point table, so the library needs no link against libcuda.
+struct NoallocEntry {
+  unsigned long long ctx_id;
+  void *ptr;
+};
+constexpr int kNoallocCache = 64;
+NoallocEntry g_noalloc_cache[kNoallocCache];
+int g_noalloc_used = 0;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// Id of the context current on this thread (0 if none is current yet).
+int current_ctx_id(unsigned long long *id) {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  if (!get_cur || !get_id) {
+    cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = q1;
+    void *f1 = nullptr, *f2 = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1) != cudaSuccess ||
+        cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+        q1 != cudaDriverEntryPointSuccess || q2 != cudaDriverEntryPointSuccess || !f1 || !f2)
+      return fail(MOE_ECUDA, "driver entry points cuCtxGetCurrent / cuCtxGetId are unavailable");
+    get_cur = reinterpret_cast<CtxGetCurrentFn>(f1);
+    get_id = reinterpret_cast<CtxGetIdFn>(f2);
   }
-  *out = g_noalloc_ptr[dev];
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS) return fail(MOE_ECUDA, "cuCtxGetCurrent failed");
+  *id = 0;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return fail(MOE_ECUDA, "cuCtxGetId failed");
+  return MOE_OK;
+}
+
+// Device address of the scratch array in the current context: looked up once
+// per context with cudaGetSymbolAddress (which also makes the runtime's
+// context current if none was), then served from the cache.
+int noalloc_scratch(void **out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  unsigned long long id = 0;
+  int r = current_ctx_id(&id);
+  if (r != MOE_OK) return r;
+  for (int i = 0; id != 0 && i < g_noalloc_used; i++)
+    if (g_noalloc_cache[i].ctx_id == id) {
+      *out = g_noalloc_cache[i].ptr;
+      return MOE_OK;
+    }
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || !p)
+    return fail(MOE_ECUDA, "cudaGetSymbolAddress of the fixed scratch failed: %s", cudaGetErrorString(e));
+  if (id == 0 && (r = current_ctx_id(&id)) != MOE_OK) return r;
+  if (id != 0) {
+    // a full table recycles its oldest entry (contexts of long-gone resets)
+    const int slot = g_noalloc_used < kNoallocCache ? g_noalloc_used++ : (int)(id % kNoallocCache);
+    g_noalloc_cache[slot] = {id, p};
+  }
+  *out = p;
   return MOE_OK;
 }
 
@@ -309,7 +358,7 @@ const char *moe_last_error(void) { return g_err.c_str(); }
 size_t moe_forward_workspace(const moe_layer *layers, int n_layers, int nb) {
   if (check_layers(layers, n_layers, nb) != MOE_OK) return 0;
   const moe_layer &L0 = layers[0];
-  return ws_layout((int)L0.hidden, (int)L0.n_experts, (int)L0.inter, n_layers, nb).total;
+  return ws_layout((int)L0.hidden, (int)L0.inter, n_layers, nb).total;
 }
 
 int moe_forward(const moe_layer *layers, int n_layers, const float *x, int nb, float *out, void *work,
@@ -340,7 +389,7 @@ int moe_forward_noalloc(const moe_layer *layers, int n_layers, const float *x, i
   if (r == MOE_OK) r = check_offsets_fit(layers, n_layers);
   if (r != MOE_OK) return r;
   const moe_layer &L0 = layers[0];
-  const size_t need = ws_layout((int)L0.hidden, (int)L0.n_experts, (int)L0.inter, n_layers, nb).total;
+  const size_t need = ws_layout((int)L0.hidden, (int)L0.inter, n_layers, nb).total;
   if (need > MOE_NOALLOC_MAX_WORKSPACE)
     return fail(MOE_ENOSPACE, "these layers need %zu bytes of scratch; the fixed scratch holds %u", need,
                 (unsigned)MOE_NOALLOC_MAX_WORKSPACE);

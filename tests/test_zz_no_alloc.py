@@ -55,13 +55,21 @@ def test_noalloc_matches_workspace_call_twice(moe):
 
 def test_noalloc_rejects_layers_beyond_its_scratch(moe):
     # 64 layers of hidden 2048 / 512 experts need more than the fixed scratch
-    L = synth.make_layer(np.random.default_rng(0), 2048, 512, 10, 512, 4, shared=True)
-    dl = moe.DeviceLayers([L] * 64)
-    need = moe.forward_workspace(dl, 4)
+    # at nb 4.  One small layer (inter 128) is uploaded once and its ABI struct
+    # repeated 64 times: the size check runs on the host before anything reads
+    # the weights.
+    L = synth.make_layer(np.random.default_rng(0), 2048, 512, 10, 128, 4, shared=True)
+    one = moe.DeviceLayers([L])
+
+    class Stack:
+        c = (moe.MoeLayer * 64)(*([one.c[0]] * 64))
+        n = 64
+
+    need = moe.forward_workspace(Stack.c, 4)
     assert need > moe.NOALLOC_MAX_WORKSPACE
     x = torch.zeros((4, 2048), device="cuda")
     out = torch.empty_like(x)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     with pytest.raises(moe.MoeError) as e:
-        moe.forward_noalloc(dl, x, out, status)
+        moe.forward_noalloc(Stack, x, out, status)
     assert e.value.code == moe.ENOSPACE
