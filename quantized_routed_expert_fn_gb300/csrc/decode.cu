@@ -514,8 +514,11 @@ __device__ void topk_warp(const float *lg, int E, int K, int *idx, float *w) {
 }
 
 // Union of the [nb][K] ids in first-seen order (warp 0).  Writes uni[],
-// wm[b][slot] and *nu = U.  rk is 64 ints of scratch.  Position p = b*K + r.
-__device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int *uni, float *wm, int *rk,
+// wm[b][slot] and *nu = U.  posof[E] holds INT_MAX on entry and on exit; rk
+// is 64 ints of scratch.  Position p = b*K + r: each position records itself
+// in posof[id] by an atomic min, so the first occurrence of every id is the
+// position that survives; firsts are ranked by a ballot.
+__device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int *uni, float *wm, int *posof, int *rk,
                            volatile int *nu) {
   const int lane = threadIdx.x & 31;
   for (int j = lane; j < 256; j += 32) wm[j] = 0.f;
@@ -526,30 +529,19 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
     __syncwarp();
     return;
   }
-  int id[2], first[2], fpos[2], pb[2], pr[2];
+  const int n = nb * K;
+  int id[2], pb[2], pr[2];
 #pragma unroll
   for (int h = 0; h < 2; h++) {
-    const int pos = lane + 32 * h;
-    int b = 0, r = pos;
-    while (b < nb && r >= K) r -= K, b++;
-    pb[h] = b, pr[h] = r;
-    id[h] = -1, first[h] = 0, fpos[h] = pos;
-    if (b < nb) {
-      id[h] = sidx[b * 32 + r];
-      first[h] = 1;
-      int q = 0;
-      for (int b2 = 0; b2 <= b && first[h]; b2++) {
-        const int rend = b2 < b ? K : r;
-        for (int r2 = 0; r2 < rend; r2++, q++) {
-          if (sidx[b2 * 32 + r2] == id[h]) {
-            first[h] = 0;
-            fpos[h] = q;
-            break;
-          }
-        }
-      }
-    }
+    const int p = lane + 32 * h;
+    pb[h] = p / K, pr[h] = p - (p / K) * K;
+    id[h] = p < n ? sidx[pb[h] * 32 + pr[h]] : -1;
+    if (p < n) atomicMin(&posof[id[h]], p);
   }
+  __syncwarp();
+  bool first[2];
+#pragma unroll
+  for (int h = 0; h < 2; h++) first[h] = lane + 32 * h < n && posof[id[h]] == lane + 32 * h;
   const uint32_t b0 = __ballot_sync(FULL, first[0]), b1 = __ballot_sync(FULL, first[1]);
   const uint32_t lt = (1u << lane) - 1u;
   if (first[0]) rk[lane] = __popc(b0 & lt);
@@ -557,14 +549,76 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
   __syncwarp();
 #pragma unroll
   for (int h = 0; h < 2; h++) {
-    if (pb[h] < nb) {
-      const int slot = rk[fpos[h]];
+    if (lane + 32 * h < n) {
+      const int slot = rk[posof[id[h]]];
       if (first[h]) uni[slot] = id[h];
       wm[pb[h] * 64 + slot] = sw[pb[h] * 32 + pr[h]];
     }
   }
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; h++)
+    if (lane + 32 * h < n) posof[id[h]] = 0x7fffffff;
   if (lane == 0) *nu = __popc(b0) + __popc(b1);
   __syncwarp();
+}
+
+// Every CTA's logits of layer l into lg[b][e].  Word (c, j) of writer CTA c
+// holds logit row rr0(c) + j / nb of activation row j % nb, tagged with
+// l + 1, in the half of the buffer for l's parity.  The half cannot be
+// rewritten under a reader: layer l + 2's rows are written only after layer
+// l + 1 has finished, which needs every CTA's layer l + 1 router rows, which
+// each CTA writes after it has read layer l's logits.  A tag other than
+// l + 1 is waited out (and a wait that runs out reports a timeout).
+// Batches of four words: every load of a batch first, then the tags.  (Out
+// of line: its temporaries stay out of the unit loop's registers.)
+__device__ __noinline__ bool read_logits(const FwdParams &P, int l, int Rl, int E1, float *lg) {
+  const unsigned tag = (unsigned)l + 1u;
+  const unsigned long long *buf = P.lgw + (size_t)(l & 1) * kMaxGrid * kLogitWords;
+  const int tid = threadIdx.x, G = gridDim.x, nb = P.nb;
+  bool ok = true;
+  const int per = ((Rl + G - 1) / G) * nb, total = G * per;
+  for (int t0 = tid; t0 < total; t0 += 4 * NT) {
+    unsigned long long w[4];
+    int word[4], dst[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const int t = t0 + k * NT;
+      word[k] = -1;
+      if (t < total) {
+        const int c = t / per, j = t - c * per;
+        const int c0 = fdiv_mul(c, Rl, G), c1 = fdiv_mul(c + 1, Rl, G);
+        if (j < (c1 - c0) * nb) {
+          word[k] = c * kLogitWords + j;
+          dst[k] = (j % nb) * E1 + c0 + j / nb;
+          w[k] = ld_relaxed_u64(buf + word[k]);
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      if (word[k] < 0 || !ok) continue;
+      if ((unsigned)(w[k] >> 32) != tag) {
+        const uint64_t t0w = globaltimer();
+        unsigned spins = 0;
+        while ((unsigned)((w[k] = ld_relaxed_u64(buf + word[k])) >> 32) != tag) {
+          if ((++spins & 15u) == 0) {
+            if (ld_volatile_int(P.status) != 0) {
+              ok = false;
+              break;
+            }
+            if (globaltimer() - t0w > P.timeout_ns) {
+              atomicCAS(P.status, 0, kStatusTimeout);
+              ok = false;
+              break;
+            }
+          }
+        }
+      }
+      lg[dst[k]] = __uint_as_float((uint32_t)w[k]);
+    }
+  }
+  return ok;
 }
 
 // ------------------------------------------------------------ unit schedule
@@ -677,6 +731,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   const int hsz = nblkI * 256 * 2 + 2 * 64;  // 32-bit words per group
   uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(reinterpret_cast<uint32_t *>(hsm) + 2 * hsz);  // [E]
   unsigned *stg_unit = reinterpret_cast<unsigned *>(eaddr_s + ((E + 1) & ~1));  // [S] last unit issued per stage
+  int *posof = reinterpret_cast<int *>(stg_unit + kMaxStages);                   // [E] union scratch, INT_MAX between uses
 
   if (tid == 0) {
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu;
@@ -686,6 +741,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   // activation registers and sums: rows b >= nb stay zero for the whole call
   for (uint32_t *z = reinterpret_cast<uint32_t *>(xa) + tid; z < reinterpret_cast<uint32_t *>(cs4 + 4 * ng); z += NT)
     *z = 0u;
+  for (int e = tid; e < E; e += NT) posof[e] = 0x7fffffff;
   __syncthreads();
   // warp lane 0 of an issuing warp: unit q of the layer into its ring stage
   auto issue_at = [&](const UnitDesc &d, unsigned u) {
@@ -720,6 +776,24 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     issued = s.nA < S ? s.nA : S;
 
     // ---- R: input, norm, fragments, router rows
+    // Loads that need no input go first, so they overlap the wait for the
+    // previous layer: this CTA's router rows (every load of a warp in
+    // flight at once, <= 4 items per warp) and the expert addresses.
+    const int R = E + s.hsi;
+    const int rr0 = fdiv_mul(cta, R, G), rr1 = fdiv_mul(cta + 1, R, G);
+    const int nch = H / 256;
+    const int nitem = (rr1 - rr0) * nch;
+    uint4 wv[4];
+#pragma unroll
+    for (int k = 0; k < 4; k++) {
+      const int it = warp + k * NW;
+      if (it < nitem) {
+        const int row = rr0 + it / nch, ch = it % nch;
+        const uint16_t *wrow = row < E ? L.router + (size_t)row * H : L.sgate;
+        wv[k] = ldg_stream4(wrow + ch * 256 + lane * 8);
+      }
+    }
+    for (int e = tid; e < E; e += NT) eaddr_s[e] = L.eaddr[e];
     if (l > 0 && !cta_wait(P.cnt + (size_t)(l - 1) * kCntPerLayer + kCntRows, (unsigned)(H / 64), P, sflag)) {
       drain_ring(bars, qbase, qbase + issued, S, P);
       return;
@@ -776,24 +850,9 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     __syncthreads();
     stage_frags<BITS>(xf, H, nb, xa, xs, cs);
     if (BITS != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr, cs4);
-    const int R = E + s.hsi;
-    const int rr0 = fdiv_mul(cta, R, G), rr1 = fdiv_mul(cta + 1, R, G);
-    const int nch = H / 256;
-    const int nitem = (rr1 - rr0) * nch;
     __syncthreads();
     MOE_STAMP(2)
     {
-      // every router load of this warp in flight at once (<= 4 items per warp)
-      uint4 wv[4];
-#pragma unroll
-      for (int k = 0; k < 4; k++) {
-        const int it = warp + k * NW;
-        if (it < nitem) {
-          const int row = rr0 + it / nch, ch = it % nch;
-          const uint16_t *wrow = row < E ? L.router + (size_t)row * H : L.sgate;
-          wv[k] = ldg_stream4(wrow + ch * 256 + lane * 8);
-        }
-      }
 #pragma unroll
       for (int k = 0; k < 4; k++) {
         const int it = warp + k * NW;
@@ -817,50 +876,18 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       const int r = j / nb, b = j % nb;
       float sum = 0.f;
       for (int ch = 0; ch < nch; ch++) sum += red[(r * nch + ch) * 4 + b];
-      // value and ready flag in one 64-bit store: no release fence
+      // value and layer tag in one 64-bit store: no release fence
       if (!(P.withhold && rr0 + r == 0))
-        st_relaxed_u64(P.logits + ((size_t)l * 4 + b) * (E + 1) + rr0 + r,
-                       (1ull << 32) | __float_as_uint(sum));
+        st_relaxed_u64(P.lgw + ((size_t)(l & 1) * kMaxGrid + cta) * kLogitWords + j,
+                       ((unsigned long long)(l + 1) << 32) | __float_as_uint(sum));
     }
     MOE_STAMP(3)
-    // expert addresses (for the slot table) while the other CTAs finish their router rows
-    for (int e = tid; e < E; e += NT) eaddr_s[e] = L.eaddr[e];
 
     // ---- T: top-k, softmax, union
-    // every logit of the layer, each polled until its writer's flag shows
-    {
-      bool ok = true;
-      for (int i = tid; i < nb * (E + 1); i += NT) {
-        const int b = i / (E + 1), e = i % (E + 1);
-        float v = 0.f;
-        if (e < R) {
-          const unsigned long long *p = P.logits + ((size_t)l * 4 + b) * (E + 1) + e;
-          unsigned long long u = ld_relaxed_u64(p);
-          if ((u >> 32) == 0) {
-            const uint64_t t0 = globaltimer();
-            unsigned spins = 0;
-            while (((u = ld_relaxed_u64(p)) >> 32) == 0) {
-              if ((++spins & 31u) == 0) {
-                if (ld_volatile_int(P.status) != 0) {
-                  ok = false;
-                  break;
-                }
-                if (globaltimer() - t0 > P.timeout_ns) {
-                  atomicCAS(P.status, 0, kStatusTimeout);
-                  ok = false;
-                  break;
-                }
-              }
-            }
-          }
-          v = __uint_as_float((uint32_t)u);
-        }
-        lg[b * E1 + e] = v;
-      }
-      if (!__syncthreads_and(ok)) {
-        drain_ring(bars, qbase, qbase + issued, S, P);
-        return;
-      }
+    // every logit of the layer, each polled until its writer's tag shows
+    if (!__syncthreads_and(read_logits(P, l, R, E1, lg))) {
+      drain_ring(bars, qbase, qbase + issued, S, P);
+      return;
     }
     MOE_STAMP(4)
     MOE_STAMP(8)
@@ -877,7 +904,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     if (tid < 4) gam[tid] = (hs && tid < nb) ? 1.f / (1.f + expf(-lg[tid * E1 + E])) : 0.f;
     __syncthreads();
     MOE_STAMP(9)
-    if (warp == 0) union_warp(sidx, sw, nb, K, uni, wm, reinterpret_cast<int *>(red), sflag + 1);
+    if (warp == 0) union_warp(sidx, sw, nb, K, uni, wm, posof, reinterpret_cast<int *>(red), sflag + 1);
     __syncthreads();
     MOE_STAMP(10)
     s.U = sflag[1];
@@ -899,7 +926,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       if (P.logits_out)
         for (int j = tid; j < nb * E; j += NT) P.logits_out[j] = lg[(j / E) * E1 + j % E];
     }
-    if (P.route_only) continue;
+    if (P.route_only) {
+      __syncthreads();  // eaddr_s is rewritten at the top of the next layer
+      continue;
+    }
 
     // ---- schedule of this CTA's units for the layer
     __syncthreads();
@@ -950,7 +980,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         const bool shared = s.hsi && d.slot == 0;
         if (d.down && d.slot != cur) {
           // h of this slot complete?  then stage its fragments and group sums
-          if (!grp_wait(cnt + kCntGu + d.slot, (unsigned)s.ups, P, gflag, grp, gt)) {
+          if (!grp_wait(cnt + kCntGu + d.slot * kCntPad, (unsigned)s.ups, P, gflag, grp, gt)) {
             alive = false;
             break;
           }
@@ -1024,7 +1054,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
             hb[frag_index(blk, b >> 1, m, tq, 0, b & 1) * 4 + reg * 2 + el] = (uint16_t)hi;
             hb[frag_index(blk, b >> 1, m, tq, 1, b & 1) * 4 + reg * 2 + el] = (uint16_t)lo;
           }
-          grp_signal(cnt + kCntGu + d.slot, 1u, grp, gt);
+          grp_signal(cnt + kCntGu + d.slot * kCntPad, 1u, grp, gt);
           if (q == 0) MOE_STAMP(13)
           if (q == s.nGU - 1) MOE_GSTAMP(14)
         } else {
@@ -1038,7 +1068,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
             P.ypart[((size_t)d.slot * nb + b) * H + d.row0 + r] = mb * y;
           }
           grp_sync(grp);
-          if (gt == 0) gflag[1] = atom_acq_rel_add(cnt + kCntDn + rt, 1u) == (unsigned)(s.nslots - 1);
+          if (gt == 0) gflag[1] = atom_acq_rel_add(cnt + kCntDn + rt * kCntPad, 1u) == (unsigned)(s.nslots - 1);
           grp_sync(grp);
           if (gflag[1]) {
             // last unit of this 64-row range: sum the slots in a fixed order
@@ -1094,6 +1124,7 @@ static int fixed_smem(int H, int E, int I, int nb, int bits) {
   b += 2 * ((I / 128) * 256 * 8 + 2 * 64 * 4);     // staged h fragments and sums, one per unit group
   b += ((E + 1) & ~1) * 8;                         // expert addresses
   b += kMaxStages * 4;                             // last unit issued per stage
+  b += E * 4;                                      // union scratch
   return b;
 }
 
@@ -1128,7 +1159,10 @@ int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes) {
   const int smem = fixed + S * sb;
   const int occ = p.bits == 4 ? occupancy_t<4>(smem) : p.bits == 3 ? occupancy_t<3>(smem) : occupancy_t<2>(smem);
   if (occ < 1) return -1;
-  *grid = sms;
+  const int G = sms < kMaxGrid ? sms : kMaxGrid;
+  // every CTA's router rows x activation rows fit its logit words
+  if ((p.E + 1 + G - 1) / G * p.nb > kLogitWords) return -1;
+  *grid = G;
   *smem_bytes = smem;
   return 0;
 }

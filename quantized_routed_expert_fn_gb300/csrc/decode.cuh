@@ -20,12 +20,16 @@ struct LayerP {
   uint32_t flags;
 };
 
-// per-layer counters in the workspace (uint32 each)
-constexpr int kCntRouter = 0;  // reserved (router logits carry their own ready flags)
-constexpr int kCntRows = 1;    // 64-row output ranges finalised
-constexpr int kCntGu = 8;      // [64] gate_up units finished per internal slot
-constexpr int kCntDn = 72;     // [H/64] down units finished per output range
-constexpr int kCntPerLayer = 256;
+// Per-layer counters in the workspace (uint32 each), every counter on a
+// 128-byte line of its own: a line that many SMs poll while others update
+// it makes the updates microseconds late.
+constexpr int kCntPad = 32;                              // words per counter line
+constexpr int kCntRows = 0;                              // 64-row output ranges finalised
+constexpr int kCntGu = kCntPad;                          // [64] gate_up units finished per internal slot
+constexpr int kCntDn = kCntGu + 64 * kCntPad;            // [H/64 <= 32] down units finished per output range
+constexpr int kCntPerLayer = kCntDn + 32 * kCntPad;
+constexpr int kMaxGrid = 160;    // CTAs of the decode kernel at most (one per SM)
+constexpr int kLogitWords = 32;  // flagged logit words per CTA (two 128-byte lines of one writer)
 
 struct FwdParams {
   int H, E, K, I, nb, nl, bits;
@@ -40,7 +44,8 @@ struct FwdParams {
   float *logits_out;      // [nb][E] (route only) or nullptr
   int *status;
   unsigned *cnt;          // [nl][kCntPerLayer]
-  unsigned long long *logits;  // [nl][4][E+1] {fp32 bits, 1 once written}; zeroed per call
+  unsigned long long *lgw;  // [kMaxGrid][kLogitWords] router logits {fp32 bits, layer + 1}, CTA c's
+                            // rows x nb; zeroed per call, reused by every layer
   float *xbuf;            // [nl][nb][H]  input of layer l (l >= 1)
   uint16_t *hfrag;        // [64][I/128][8][32][2][2] bf16 activation fragments of h
   float *ypart;           // [64][nb][H]  per-slot weighted down outputs
@@ -57,6 +62,7 @@ constexpr int kTracePhases = 16;
 
 // Launch helpers (decode.cu)
 // Fills p.stages / p.stage_bytes and the grid for this device; returns 0 or -1.
+// The grid is one CTA per SM, at most kMaxGrid.
 int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes);
 cudaError_t launch_decode(const FwdParams &p, int grid, int smem_bytes, cudaStream_t st);
 
