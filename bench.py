@@ -47,7 +47,7 @@ METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 
 
 
 # DRAM traffic per launch of the dominant kernel, from one ncu capture each
-# (profiles/decode_c1.md, profiles/prefill_c4.md).  Reported only while the
+# (the decode and prefill capture summaries under profiles/).  Reported only while the
 # kernel's sources hash to the value they had when the counters were taken.
 NCU_TRAFFIC = {
     "c1": dict(bytes=1211.6e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],

@@ -5,16 +5,17 @@
 //      stages it as bf16 hi/lo tensor-core fragments, and computes its share of
 //      the router rows (bf16 router x fp32 input on CUDA cores) plus the
 //      shared-gate dot, each logit published as one 64-bit word that carries
-//      its own ready flag.
-//   T  every CTA polls all logits, then computes top-k, softmax and the
+//      its layer as a tag (a CTA's words sit together, one writer per line).
+//   T  every CTA reads all logits in batches, then computes top-k, softmax and the
 //      union itself (identical in every CTA, so no second grid-wide
 //      handshake); CTA 0 publishes slot table, weight map and ids.
 //   G  gate_up units (internal slot, 16 gate rows + the matching 16 up rows)
 //   D  down units (slot, 64 output rows).
 // Weight tiles of the units reach shared memory through bulk (TMA) copies
-// into a ring of `stages` units, so HBM streams while the warps compute; the
-// units go to two groups of eight warps in turn (named barriers per group),
-// and the group that frees a stage requests the unit `stages` places ahead.
+// into a ring of `stages` units, so HBM streams while the warps compute; two
+// groups of eight warps (named barriers per group) each take the next unit
+// not yet taken, and the group that frees a stage requests the unit `stages`
+// places ahead.
 // The shared expert's first gate_up units do not depend on routing and are
 // requested before the layer input is even available.
 // Codes are expanded to exact bf16 integers and multiplied on the tensor
@@ -41,9 +42,10 @@ namespace {
 constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int kProducerWarp = 1;  // warp (of the CTA, then of each unit group) that issues the bulk copies
-// The weight units of a layer go to two groups of eight warps in turn (unit q
-// to group q % 2), so that one group's reductions, global writes and
-// releases overlap the other group's tensor-core work.
+// The weight units of a layer go to two groups of eight warps, each taking
+// the next unit not yet taken (a shared-memory counter), so that one group's
+// reductions, global writes and releases overlap the other group's
+// tensor-core work and neither idles while units remain.
 constexpr int kGroups = 2;
 constexpr int GT = NT / kGroups;  // threads of a group
 constexpr int GW = GT / 32;       // warps of a group
@@ -942,7 +944,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     }
     issued = n < S ? n : S;
 
-    // ---- G + D: the unit loop, unit q to group q % 2
+    // ---- G + D: the unit loop, each group taking the next free unit
     MOE_STAMP(5)
     {
       const int grp = warp / GW, gw = warp % GW, gt = tid % GT;
