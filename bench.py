@@ -156,6 +156,179 @@ def record_bytes(lay) -> int:
     return tot
 
 
+def l2_bytes(device) -> int:
+    import torch
+    return int(torch.cuda.get_device_properties(device).L2_cache_size)
+
+
+def decode_inputs(base, nb: int, n_views: int, seed: int) -> list:
+    """n_views inputs [nb][H] whose top-k sets are pairwise disjoint over the
+    views and the rows: row b of view i is the normalised sum of the router
+    rows of k experts drawn without replacement (plus noise), so those k
+    experts lead its logits by a wide margin.  Returns float32 arrays."""
+    import torch
+    R = base.router.view(torch.bfloat16).float().cpu().numpy().astype(np.float64)
+    E, H = R.shape
+    k = base.top_k
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(E)
+    xs = []
+    for i in range(n_views):
+        S = perm[(i * nb * k) % E:][: nb * k]
+        if len(S) < nb * k:  # wrap around the permutation
+            S = np.concatenate([S, perm[: nb * k - len(S)]])
+        x = R[S.reshape(nb, k)].sum(axis=1) + rng.normal(0.0, 0.05, (nb, H))
+        x /= np.sqrt((x * x).mean(axis=1, keepdims=True))
+        xs.append(x.astype(np.float32))
+    return xs
+
+
+def decode_setup(name, nb, device, seed, n_layers=None):
+    """Device layers and inputs of a decode workload.
+
+    The 48-layer stack reads every layer's union once per step (about 1.2 GB,
+    several times L2).  A one-layer workload would re-read the same records
+    every step, so it rotates views: each view has its own router,
+    shared-gate and shared-record copies over a common routed-record pool (a
+    second pool once one cannot hold enough disjoint unions), and its own
+    input whose union is disjoint from every other view's.  The number of
+    views is the smallest that makes one cycle touch at least 4x the L2 size
+    queried at run time, so no record, router or shared record is read again
+    before at least that many other bytes."""
+    import dataclasses
+    import torch
+    from quantized_routed_expert_fn_gb300 import moe, synth
+    cfg = synth.CONFIGS[name]
+    layers = synth.make_device_layers(name, seed=seed, device=device, n_layers=n_layers or None)
+    if len(layers) > 1:
+        gen = torch.Generator(device="cpu").manual_seed(100 + seed)
+        x = torch.randn((nb, cfg["hidden"]), generator=gen, dtype=torch.float32)
+        if nb > 1:  # correlated rows
+            c = torch.randn((1, cfg["hidden"]), generator=gen)
+            x = (0.55 ** 0.5) * c + (0.45 ** 0.5) * x
+        return dict(views=[moe.DeviceLayers(layers, device=device)], xs=[x], layers=layers,
+                    rotation=None)
+    base = layers[0]
+    L2 = l2_bytes(device)
+    U = nb * base.top_k
+    per_view = layer_bytes(base, U, nb)
+    n_views = max(2, -(-4 * L2 // per_view))
+    per_pool = base.n_experts // U
+    pools = [base]
+    while len(pools) * per_pool < n_views:
+        pools.append(synth.make_device_layers(name, seed=seed + 1000 * len(pools), device=device, n_layers=1)[0])
+    views, xs = [], []
+    for i in range(n_views):
+        pool = pools[i // per_pool]
+        v = dataclasses.replace(
+            pool, router=pool.router.clone(),
+            shared_gate=None if pool.shared_gate is None else pool.shared_gate.clone(),
+            shared_record=None if pool.shared_record is None else pool.shared_record.clone())
+        views.append(v)
+    for pi, pool in enumerate(pools):
+        n_here = min(per_pool, n_views - pi * per_pool)
+        xs += [torch.from_numpy(x) for x in decode_inputs(pool, nb, n_here, seed=11 + seed + pi)]
+    return dict(views=[moe.DeviceLayers([v], device=device) for v in views], xs=xs, layers=views,
+                rotation=dict(views=n_views, pools=len(pools), l2_bytes=L2))
+
+
+def time_decode(setup, nb, steps, warmup, rank, world, device, e2e=True):
+    """Device-timed and end-to-end moe_forward over the setup's views in turn."""
+    import torch
+    from quantized_routed_expert_fn_gb300 import moe
+    views, xs_host = setup["views"], setup["xs"]
+    nv, nl = len(views), views[0].n
+    H = xs_host[0].shape[1]
+    xs = [x.to(device) for x in xs_host]
+    out = torch.empty((nb, H), dtype=torch.float32, device=device)
+    ws = moe.alloc_workspace(moe.forward_workspace(views[0], nb), device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    slot = torch.zeros((nl, 64), dtype=torch.int64, device=device)
+    wmap = torch.zeros((nl, 4, 64), dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    # every view once: its union sizes and record addresses
+    unions, addrs = [], []
+    for i in range(nv):
+        moe.forward(views[i], xs[i], out, ws, status, slot, wmap, stream=stream)
+        torch.cuda.synchronize()
+        if status.item() != 0:
+            raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
+        st = slot.cpu()
+        u = [int(v) for v in st[:, 63].tolist()]
+        unions.append(u)
+        addrs.append(set(int(a) for l in range(nl) for a in st[l, : u[l]].tolist()))
+    for s in range(max(warmup, 3)):
+        moe.forward(views[s % nv], xs[s % nv], out, ws, status, slot, wmap, stream=stream)
+    torch.cuda.synchronize()
+    bytes_per_view = [sum(layer_bytes(L, u, nb) for L, u in zip(views[i].src, unions[i])) for i in range(nv)]
+    bytes_per_step = sum(bytes_per_view[s % nv] for s in range(steps)) / steps
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as td
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist:
+        td.barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for s in range(steps):
+        moe.forward(views[s % nv], xs[s % nv], out, ws, status, slot, wmap, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        td.barrier()
+    ms = ev0.elapsed_time(ev1) / steps
+    clocks = sampler.stop() if sampler else None
+    if status.item() != 0:
+        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
+
+    e2e_ms = None
+    if e2e:
+        # end to end through the same call with host buffers: H2D of x, D2H of out
+        x_pin = [x.pin_memory() for x in xs_host]
+        o_pin = torch.empty((nb, H), dtype=torch.float32).pin_memory()
+        xd = torch.empty((nb, H), dtype=torch.float32, device=device)
+
+        def e2e_step(s):
+            xd.copy_(x_pin[s % nv], non_blocking=True)
+            moe.forward(views[s % nv], xd, out, ws, status, slot, wmap, stream=stream)
+            o_pin.copy_(out, non_blocking=True)
+
+        for s in range(3):
+            e2e_step(s)
+        torch.cuda.synchronize()
+        if dist:
+            td.barrier()
+        t0 = time.perf_counter()
+        for s in range(steps):
+            e2e_step(s)
+        torch.cuda.synchronize()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / steps
+        if dist:
+            td.barrier()
+        ms, e2e_ms = reduce_over_ranks([ms, e2e_ms], world, device)
+    peak, peak_kind = load_peaks()
+    achieved = bytes_per_step / (ms * 1e-3) / 1e9
+    rot = setup["rotation"]
+    if rot is None:
+        L2 = l2_bytes(device)
+        l2 = (f"inputs larger than L2: each step reads every layer's union once, {bytes_per_step / 1e6:.0f} MB "
+              f"= {bytes_per_step / L2:.1f}x the {L2 / 1e6:.0f} MB L2 (queried at run time)")
+    else:
+        distinct = len(set().union(*addrs)) == sum(len(a) for a in addrs)
+        cycle = sum(bytes_per_view)
+        l2 = (f"{nv} rotated views (own router, shared gate and shared record copies over "
+              f"{rot['pools']} routed-record pool(s)), inputs built for "
+              f"{'pairwise-disjoint' if distinct else 'overlapping'} unions: one cycle reads "
+              f"{cycle / 1e6:.0f} MB = {cycle / rot['l2_bytes']:.1f}x the {rot['l2_bytes'] / 1e6:.0f} MB L2 "
+              f"(queried at run time) before any byte is read again")
+    return dict(ms=ms, e2e_ms=e2e_ms, nb=nb, nl=nl, bytes=bytes_per_step, achieved=achieved, peak=peak,
+                peak_kind=peak_kind, clocks=clocks, unions=sorted(set(u for uu in unions for u in uu)), l2=l2)
+
+
 def run_ours(args, rank, world, device):
     import torch
     from quantized_routed_expert_fn_gb300 import build, moe, synth
@@ -163,89 +336,42 @@ def run_ours(args, rank, world, device):
     build.build()
     moe.lib()
     torch.cuda.set_device(device)
-    name = args.workload
-    cfg = synth.CONFIGS[name]
+    cfg = synth.CONFIGS[args.workload]
     nb = args.nb or cfg["nb"]
-    layers = synth.make_device_layers(name, seed=1 + rank, device=device, n_layers=args.layers or None)
-    dl = moe.DeviceLayers(layers, device=device)
-    nl = dl.n
-    H = cfg["hidden"]
-    gen = torch.Generator(device="cpu").manual_seed(100 + rank)
-    x_host = torch.randn((nb, H), generator=gen, dtype=torch.float32)
-    if nb > 1:  # correlated rows: union of about 30 of 40 possible experts
-        c = torch.randn((1, H), generator=gen)
-        x_host = (0.55 ** 0.5) * c + (0.45 ** 0.5) * x_host
-    x = x_host.to(device)
-    out = torch.empty_like(x)
-    ws = moe.alloc_workspace(moe.forward_workspace(dl, nb), device=device)
-    status = torch.zeros(1, dtype=torch.int32, device=device)
-    slot = torch.zeros((nl, 64), dtype=torch.int64, device=device)
-    wmap = torch.zeros((nl, 4, 64), dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
+    setup = decode_setup(args.workload, nb, device, seed=1 + rank, n_layers=args.layers or None)
+    return time_decode(setup, nb, args.steps, args.warmup, rank, world, device)
 
-    def step():
-        moe.forward(dl, x, out, ws, status, slot, wmap, stream=stream)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
-    if status.item() != 0:
-        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
-    unions = [int(v) for v in slot[:, 63].cpu().tolist()]
-    bytes_per_step = sum(layer_bytes(L, u, nb) for L, u in zip(layers, unions))
-
-    dist = world > 1
-    if dist:
-        import torch.distributed as td
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    time.sleep(0.3)
-    # device-timed region: inputs resident in HBM
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if dist:
-        td.barrier()
-    torch.cuda.synchronize()
-    torch.cuda.nvtx.range_push("timed")
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.nvtx.range_pop()
-    torch.cuda.synchronize()
-    if dist:
-        td.barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    clocks = sampler.stop() if sampler else None
-    if status.item() != 0:
-        raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
-
-    # end to end through the same call with host buffers: H2D of x, D2H of out
-    x_pin = x_host.pin_memory()
-    o_pin = torch.empty((nb, H), dtype=torch.float32).pin_memory()
-
-    def e2e_step():
-        x.copy_(x_pin, non_blocking=True)
-        moe.forward(dl, x, out, ws, status, slot, wmap, stream=stream)
-        o_pin.copy_(out, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    if dist:
-        td.barrier()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
-    if dist:
-        td.barrier()
-
-    ms, e2e_ms = reduce_over_ranks([ms, e2e_ms], world, device)
-    rows = nb * nl * world
-    peak, peak_kind = load_peaks()
-    achieved = bytes_per_step / (ms * 1e-3) / 1e9
-    return dict(ms=ms, e2e_ms=e2e_ms, rows=rows, nb=nb, nl=nl, bytes=bytes_per_step, achieved=achieved,
-                peak=peak, peak_kind=peak_kind, clocks=clocks, unions=unions)
+def extras(args, device):
+    """The other decode and prefill workloads of the metric, timed on this GPU
+    after the headline: verify batches, low-bit records, the prefill chunk."""
+    import argparse as _ap
+    import torch
+    res = {}
+    for name, nb in (("c2", 4), ("c2", 1), ("c3b3", 4), ("c3b3", 1), ("c3b2", 4), ("c3b2", 1)):
+        setup = decode_setup(name, nb, device, seed=1)
+        r = time_decode(setup, nb, args.steps, args.warmup, 0, 1, device, e2e=False)
+        res[f"{name}_nb{nb}"] = {
+            "workload": WORKLOADS[name].replace("nb=4", f"nb={nb}"), "ms_per_step": r["ms"],
+            "rows_per_s": nb / (r["ms"] * 1e-3), "union_sizes": r["unions"],
+            "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
+                         "frac": r["achieved"] / r["peak"], "peak_source": r["peak_kind"],
+                         "algorithmic_bytes_per_launch": r["bytes"]},
+            "l2": r["l2"], "clocks": r["clocks"]}
+        del setup
+        torch.cuda.empty_cache()
+    a = _ap.Namespace(**vars(args))
+    a.workload, a.nb = "c4", 0
+    r = run_prefill(a, 0, 1, device)
+    gu = r["flops"]["gate_up_gemm"] / (r["kernel_ms"]["gate_up_gemm"] * 1e-3) / 1e12
+    dn = r["flops"]["down_gemm"] / (r["kernel_ms"]["down_gemm"] * 1e-3) / 1e12
+    res["c4"] = {"workload": WORKLOADS["c4"], "ms_per_step": r["ms"], "rows_per_s": r["t"] / (r["ms"] * 1e-3),
+                 "roofline": {"bound": "tensor", "kernel": "gate_up_gemm", "achieved": gu, "peak": r["peak"],
+                              "unit": "TFLOP/s", "frac": gu / r["peak"], "peak_source": r["peak_kind"] + " bf16 burst",
+                              "algorithmic_flops_per_launch": r["flops"]["gate_up_gemm"]},
+                 "down_gemm": {"achieved": dn, "frac": dn / r["peak"]},
+                 "kernel_ms": r["kernel_ms"], "clocks": r["clocks"]}
+    return res
 
 
 def run_prefill(args, rank, world, device):
@@ -366,27 +492,80 @@ def oracle_prefill_sample(t, budget_s, workload="c4"):
     return dict(value=done / secs, rows=done, seconds=secs, cores=cores)
 
 
-def oracle_sample(name, nb, budget_s):
-    """Time the oracle (as it stands) on host cores on the first layers of the
-    same workload, drawn on the host with the same distributions."""
+def oracle_sample(name, nb, budget_s, parallel=False, n_src=2):
+    """Time the oracle (as it stands) on host cores over the first layers of
+    the same workload, drawn on the host with the same distributions; layers
+    cycle over n_src generated ones (the time of a layer does not depend on
+    its values).  parallel: the matvecs' output rows over every host thread."""
     import oracle
     from quantized_routed_expert_fn_gb300 import synth
     cfg = synth.CONFIGS[name]
     rng = np.random.default_rng(5)
     x = synth.make_x(rng, nb, cfg["hidden"])
+    src = [oracle.Layer(L) for L in synth.make_config_layers(name, seed=1000, n_layers=min(n_src, cfg["n_layers"]))]
+    oracle.set_parallel_rows(parallel)
     layers_done, t_total = 0, 0.0
-    layer_iter = 0
-    while t_total < budget_s and layer_iter < cfg["n_layers"]:
-        L = synth.make_config_layers(name, seed=1000 + layer_iter, n_layers=1)[0]
-        ol = oracle.Layer(L)
-        t0 = time.perf_counter()
-        r = oracle.moe_layer(ol, x)
-        t_total += time.perf_counter() - t0
-        x = r["out"]
-        layers_done += 1
-        layer_iter += 1
-    # the oracle's layer path is serial C: one host core
-    return dict(value=nb * layers_done / t_total, layers=layers_done, seconds=t_total, cores=1)
+    try:
+        while t_total < budget_s and layers_done < cfg["n_layers"]:
+            t0 = time.perf_counter()
+            r = oracle.moe_layer(src[layers_done % len(src)], x)
+            t_total += time.perf_counter() - t0
+            x = r["out"]
+            layers_done += 1
+    finally:
+        oracle.set_parallel_rows(False)
+    return dict(value=nb * layers_done / t_total, layers=layers_done, seconds=t_total,
+                cores=oracle.threads() if parallel else 1)
+
+
+def reference_arm(args, config, prefill):
+    """The reference arm: the oracle, as it stands, on all host cores.  Each of
+    the W + K steps is a bounded sample of the workload -- one layer of nb rows
+    (decode) or a fixed block of the chunk's rows (prefill) -- and the line
+    reports exactly the K steps it timed."""
+    import oracle
+    from quantized_routed_expert_fn_gb300 import synth
+    cfg = synth.CONFIGS[args.workload]
+    nb = args.nb or cfg["nb"]
+    cores = oracle.threads()
+    config = dict(config, l2="not applicable: the oracle runs on the host")
+    if prefill:
+        rng = np.random.default_rng(40)
+        layer = synth.make_config_layers(args.workload, seed=1000, n_layers=1)[0]
+        synth.zipf_router(rng, layer)
+        x = synth.make_prefill_x(rng, nb, layer.hidden)
+        ol = oracle.Layer(layer)
+        per = max(cores, 8)
+        rows_of = lambda s: np.arange(s * per, s * per + per) % nb
+
+        def step(s):
+            oracle.prefill_rows(ol, x, rows_of(s), mirror=True)
+        rows_per_step, what = per, f"{per} rows of the chunk (bf16 mirror)"
+    else:
+        src = [oracle.Layer(L) for L in synth.make_config_layers(args.workload, seed=1000,
+                                                                 n_layers=min(2, cfg["n_layers"]))]
+        state = {"x": synth.make_x(np.random.default_rng(5), nb, cfg["hidden"])}
+        oracle.set_parallel_rows(True)
+
+        def step(s):
+            state["x"] = oracle.moe_layer(src[s % len(src)], state["x"])["out"]
+        rows_per_step, what = nb, f"one layer of {nb} row(s), output rows over the host threads"
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(args.warmup + s)
+    secs = time.perf_counter() - t0
+    oracle.set_parallel_rows(False)
+    value = rows_per_step * args.steps / secs
+    line = {"metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
+            "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                             "sample": f"each step {what}; {args.steps} steps in {secs:.1f} s"},
+            "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
 
 
 def main():
@@ -397,8 +576,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c1", choices=sorted(WORKLOADS))
     ap.add_argument("--nb", type=int, default=0)
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--layers", type=int, default=0, help="override the stack depth (profiling a smaller case)")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="c1 only: skip the other workloads' figures")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -414,31 +595,9 @@ def main():
     if prefill:
         config = {"workload": WORKLOADS[args.workload], "t": nb, "layers": 1,
                   "l2": "inputs larger than L2 (about 0.9 GB of expert records per step)"}
-    if args.impl == "reference" and prefill:
-        if rank != 0:
-            return
-        s = oracle_prefill_sample(nb, budget_s=min(args.cpu_budget, 20.0), workload=args.workload)
-        line = {"metric": METRIC, "value": s["value"], "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": 1000.0 * nb / s["value"], "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config,
-                "impl": "reference",
-                "cpu_baseline": {"value": s["value"], "unit": "rows/s", "cores": s["cores"], "kind": "oracle",
-                                 "sample": f"first {s['rows']} rows of the chunk, {s['seconds']:.1f} s"},
-                "e2e": {"value": s["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
-        return
     if args.impl == "reference":
-        if rank != 0:
-            return
-        s = oracle_sample(args.workload, nb, budget_s=min(args.cpu_budget, 20.0))
-        ms = 1000.0 * nb * (args.layers or cfg["n_layers"]) / s["value"]
-        line = {"metric": METRIC, "value": s["value"], "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config, "impl": "reference",
-                "cpu_baseline": {"value": s["value"], "unit": "rows/s", "cores": s["cores"], "kind": "oracle",
-                                 "sample": f"first {s['layers']} layers of the workload, {s['seconds']:.1f} s"},
-                "e2e": {"value": s["value"], "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-        print(json.dumps(line))
+        if rank == 0:
+            reference_arm(args, config, prefill)
         return
 
     import torch
@@ -482,7 +641,9 @@ def main():
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    cpu = oracle_sample(args.workload, nb, budget_s=args.cpu_budget) if world == 1 or rank == 0 else None
+    config["l2"] = r["l2"]
+    cpu1 = oracle_sample(args.workload, nb, budget_s=args.cpu_budget, parallel=False)
+    cpun = oracle_sample(args.workload, nb, budget_s=args.cpu_budget, parallel=True)
     value = job_rows_per_s(r["nb"] * r["nl"], world, r["ms"])
     e2e_value = job_rows_per_s(r["nb"] * r["nl"], world, r["e2e_ms"])
     line = {
@@ -496,11 +657,16 @@ def main():
                      "frac": r["achieved"] / r["peak"],
                      "traffic": ncu_traffic(args.workload) if args.workload == "c1" and not args.layers else None,
                      "peak_source": r["peak_kind"], "algorithmic_bytes_per_launch": r["bytes"]},
-        "cpu_baseline": {"value": cpu["value"], "unit": "rows/s", "cores": cpu["cores"], "kind": "oracle",
-                         "sample": f"first {cpu['layers']} layers of the workload, {cpu['seconds']:.1f} s"},
+        "cpu_baseline": {"value": cpun["value"], "unit": "rows/s", "cores": cpun["cores"], "kind": "oracle",
+                         "sample": f"first {cpun['layers']} layers of the workload, {cpun['seconds']:.1f} s, "
+                                   f"output rows over {cpun['cores']} host threads"},
+        "cpu_baseline_1core": {"value": cpu1["value"], "unit": "rows/s", "cores": 1, "kind": "oracle",
+                               "sample": f"first {cpu1['layers']} layers of the workload, {cpu1['seconds']:.1f} s"},
         "clocks": r["clocks"],
-        "union_sizes": sorted(set(r["unions"])),
+        "union_sizes": r["unions"],
     }
+    if args.extras and world == 1 and args.workload == "c1" and not args.layers:
+        line["extras"] = extras(args, device)
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -74,6 +74,7 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_group.restype = i32
         _lib.oracle_group.argtypes = [i32, i32, i32, p, p, p, p, p, p]
         _lib.oracle_threads.restype = i32
+        _lib.oracle_set_parallel_rows.argtypes = [i32]
         _lib.oracle_round_bf16.restype = d
         _lib.oracle_round_bf16.argtypes = [d]
         _lib.oracle_expert_mirror.argtypes = [p, ctypes.POINTER(OQ), ctypes.POINTER(OQ), i32, i32, p, d, p, p]
@@ -251,3 +252,9 @@ def expert_mirror(record: np.ndarray, layout, x: np.ndarray, weight: float) -> d
 
 def threads() -> int:
     return int(lib().oracle_threads())
+
+
+def set_parallel_rows(on: bool) -> None:
+    """Spread the decode matvecs' output rows over host threads (timing only;
+    every output is computed the same way either way)."""
+    lib().oracle_set_parallel_rows(1 if on else 0)

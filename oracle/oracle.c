@@ -65,6 +65,20 @@ typedef struct {
 
 enum { ORACLE_RESIDUAL = 1, ORACLE_PRENORM = 2 };
 
+/* Threads over output rows in the decode matvecs (router rows, projection
+ * rows).  Off by default; each output is still computed by one thread in the
+ * same order, so results do not depend on it.  Only used to time the oracle
+ * on all host cores. */
+static int g_par_rows = 0;
+void oracle_set_parallel_rows(int on) { g_par_rows = on; }
+static int par_rows(void) {
+#ifdef _OPENMP
+  return g_par_rows && !omp_in_parallel();
+#else
+  return 0;
+#endif
+}
+
 /* ------------------------------------------------------------ scalars */
 
 /* The value a bf16 bit pattern denotes (exact in double). */
@@ -132,6 +146,7 @@ static void qmatvec(const uint8_t *rec, const oq_t *q, int bits, const double *x
   const uint32_t *codes = (const uint32_t *)(rec + q->w);
   const uint16_t *sc = (const uint16_t *)(rec + q->s);
   const uint16_t *bi = (const uint16_t *)(rec + q->b);
+#pragma omp parallel for schedule(static) if (par_rows())
   for (int64_t o = 0; o < q->out; o++) {
     const uint32_t *row = codes + o * words_per_row;
     double acc = 0.0, aabs = 0.0;
@@ -252,6 +267,7 @@ static void rmsnorm(const double *x, int H, double *xn) {
 
 /* Router logits of one row: L[e] = sum_i R[e][i] x[i]. */
 static void router_row(const oracle_layer_t *L, const double *x, double *logit) {
+#pragma omp parallel for schedule(static) if (par_rows())
   for (int e = 0; e < L->n_experts; e++) {
     double acc = 0.0;
     const uint16_t *r = L->router + (int64_t)e * L->hidden;
