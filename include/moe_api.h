@@ -76,8 +76,9 @@ typedef struct {
 enum {
   MOE_RESIDUAL = 1, /* out = x + MoE(x^) */
   MOE_PRENORM = 2,  /* x^ = x / sqrt(mean(x^2) + 1e-6) feeds router, gate and experts */
-  MOE_TEST_WITHHOLD = 0x100 /* failure-detection test only: the router's completion is
-                               never released, so the kernel's bounded wait must give up
+  MOE_TEST_WITHHOLD = 0x100 /* failure-detection test only: decode never releases the
+                               router's completion, prefill never completes one pipeline
+                               stage of its gate_up GEMM; the bounded waits must give up
                                and report MOE_ETIMEOUT */
 };
 

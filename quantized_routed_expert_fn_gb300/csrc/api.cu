@@ -285,7 +285,8 @@ int check_prefill(const moe_layer *L, int t) {
   if (L->bits == 3 && I % 128)
     return fail(MOE_ESHAPE, "3-bit prefill needs inter %% 128 == 0 (16-byte code rows); inter %u", I);
   if (L->group != 64) return fail(MOE_ESHAPE, "group %u, only 64 is supported", L->group);
-  if (L->flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM)) return fail(MOE_EINVAL, "unknown flags 0x%x", L->flags);
+  if (L->flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM | MOE_TEST_WITHHOLD))
+    return fail(MOE_EINVAL, "unknown flags 0x%x", L->flags);
   if (!L->router || !L->expert_addr) return fail(MOE_EINVAL, "router / expert_addr NULL");
   if ((uintptr_t)L->router & 15u) return fail(MOE_EALIGN, "router not 16-byte aligned");
   if (!L->shared_gate != !L->shared_record)
@@ -325,6 +326,7 @@ int run_prefill(const moe_layer *L, const float *x, int t, uint16_t *out, void *
   p.H = H, p.E = (int)L->n_experts, p.K = (int)L->top_k, p.I = (int)L->inter, p.t = t;
   p.bits = (int)L->bits;
   p.flags = L->flags & (MOE_RESIDUAL | MOE_PRENORM);
+  p.withhold = (L->flags & MOE_TEST_WITHHOLD) != 0;
   p.route_only = route_only;
   p.x = x, p.out = out;
   p.router = L->router, p.sgate = L->shared_gate;

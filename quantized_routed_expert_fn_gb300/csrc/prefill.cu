@@ -559,8 +559,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       }
       ia = ib;
     }
-    // copies still in flight land before the CTA ends
-    if (lane == 0 && f > 0) pf_wait(&B.full_b[(f - 1) % kSB], (uint32_t)(((f - 1) / kSB) & 1), P);
+    // copies still in flight land before the CTA ends: the last issue of
+    // every stage (after a timeout the consumer may have stopped early, so
+    // the earlier stages' copies need not have been waited for)
+    if (lane == 0)
+      for (int g = f > kSB ? f - kSB : 0; g < f; g++) pf_wait(&B.full_b[g % kSB], (uint32_t)((g / kSB) & 1), P);
     __syncwarp();
   } else if (warp < 10) {
     // ---------------------------------------------------------------- A producers
@@ -627,7 +630,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
             tc05::wait_st();
             tc05::fence_before();
             __syncwarp();
-            if (lane == 0) tc05::mbar_arrive(&B.full_a[sa]);
+            // (failure-detection test: one warp of CTA 0 withholds its
+            // arrive on the first A stage of the gate_up GEMM, so that the
+            // MMA warp's bounded wait runs out and every wait after it too)
+            const bool withheld = MODE == MODE_GATE_UP && P.withhold && blockIdx.x == 0 && c == 0 && warp == 2;
+            if (lane == 0 && !withheld) tc05::mbar_arrive(&B.full_a[sa]);
           } else {
             ok = false;
           }

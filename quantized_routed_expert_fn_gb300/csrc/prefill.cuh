@@ -33,6 +33,7 @@ struct PfParams {
   int n_sms;
   uint32_t flags;
   int route_only;          // stop after the grouping
+  int withhold;            // failure-detection test: CTA 0 of the gate_up GEMM never completes its first A stage
   const float *x;          // [t][H]
   uint16_t *out;           // bf16 [t][H]
   const uint16_t *router, *sgate;

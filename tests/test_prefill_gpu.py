@@ -191,19 +191,53 @@ def test_prefill_rejects_unaligned_3bit_rows(moe):
     assert e.value.code == moe.ESHAPE
 
 
-@pytest.fixture(scope="module")
-def c4():
+def full_size_chunk(workload):
     """The 4096-token prefill chunk: hidden 2048, 512 experts, top-10, inter 512,
     shared expert, Zipf(1.1) expert popularity through the router's bias channel."""
     rng = np.random.default_rng(4)
-    layer = synth.make_config_layers("c4", seed=4)[0]
+    layer = synth.make_config_layers(workload, seed=4)[0]
     synth.zipf_router(rng, layer)
     x = synth.make_prefill_x(rng, 4096, layer.hidden)
     return layer, oracle.Layer(layer), x
 
 
-def test_prefill_c4_full_size(moe, c4):
-    layer, ol, x = c4
+@pytest.fixture(scope="module")
+def c4():
+    return full_size_chunk("c4")
+
+
+@pytest.fixture(scope="module")
+def c4b3():
+    return full_size_chunk("c4b3")
+
+
+TILE_N = 192  # token columns of one tensor-core tile of the grouped GEMMs
+
+
+def sampled_rows(ids, same, n_min=512, seed=44):
+    """Rows to grade at full size: the first and last rows; one row in every
+    token tile of the largest expert group (its rows in group order are the
+    routed rows in token order); a row routed to each of the 64 rarest used
+    experts; random rows up to n_min.  Only rows whose GPU id set equals the
+    oracle's are kept (their outputs are comparable)."""
+    t = ids.shape[0]
+    counts = np.bincount(ids.ravel())
+    members = np.nonzero((ids == int(np.argmax(counts))).any(axis=1))[0]
+    tiles = members[::TILE_N].tolist() + [int(members[-1])]
+    used = [int(e) for e in np.argsort(counts, kind="stable") if counts[e] > 0][:64]
+    rare = [int(np.nonzero((ids == e).any(axis=1))[0][0]) for e in used]
+    pick = set([0, t - 1] + tiles + rare)
+    srng = np.random.default_rng(seed)
+    for b in srng.permutation(t):
+        if len([r for r in pick if same[r]]) >= n_min:
+            break
+        pick.add(int(b))
+    rows = np.array(sorted(r for r in pick if same[r]))
+    return rows, dict(tiles=len(tiles), rare=len(rare), largest=int(counts.max()))
+
+
+def check_full_size(moe, chunk, what):
+    layer, ol, x = chunk
     t, k, E = x.shape[0], layer.top_k, layer.n_experts
     dl = moe.DeviceLayers([layer])
     got, idx = run_prefill(moe, dl, x)
@@ -219,15 +253,63 @@ def test_prefill_c4_full_size(moe, c4):
         assert abs(float(r["logits"][b][idx[b][k - 1]]) - float(kth)) < GAP
     same = np.array([sorted(idx[b]) == sorted(r["idx"][b]) for b in range(t)])
     counts = np.bincount(r["idx"].ravel(), minlength=E)
-    print(f"[c4] rows with a top-k gap < {GAP}: {int((~clear).sum())}; id sets differing: {int((~same).sum())}; "
+    print(f"[{what}] rows with a top-k gap < {GAP}: {int((~clear).sum())}; id sets differing: {int((~same).sum())}; "
           f"expert rows max {counts.max()} min {counts.min()} empty {(counts == 0).sum()}")
-    # outputs on sampled rows (first, last, rows routed to the rarest used experts, random)
-    srng = np.random.default_rng(44)
-    rare = [int(np.nonzero((r["idx"] == e).any(axis=1))[0][0]) for e in np.argsort(counts) if counts[e] > 0][:8]
-    sample = sorted(set([0, t - 1] + rare + srng.choice(t, 38, replace=False).tolist()))
-    sample = [b for b in sample if same[b]]
-    ref = oracle.prefill_rows(ol, x, np.array(sample), mirror=True)
-    assert_prefill_close(got[sample], ref, x, layer.flags, np.array(sample), f"c4 t=4096 ({len(sample)} rows)")
+    rows, info = sampled_rows(r["idx"], same)
+    assert len(rows) >= 512
+    ref = oracle.prefill_rows(ol, x, rows, mirror=True)
+    assert_prefill_close(got[rows], ref, x, layer.flags, rows,
+                         f"{what} t=4096 ({len(rows)} rows: {info['tiles']} tiles of the largest group of "
+                         f"{info['largest']}, {info['rare']} rarest experts)")
+    # reported, not graded: the distance from the exact (unrounded) oracle
+    exact = oracle.prefill_rows(ol, x, rows, mirror=False)
+    rms = moe_rms(exact["out"], x[rows], layer.flags)
+    rel = np.abs(got[rows] - exact["out"]) / rms[:, None]
+    print(f"[{what}] against the exact oracle (no bf16 rounding): max |err| = {rel.max():.3e} x row RMS, "
+          f"mean {rel.mean():.3e} x row RMS")
+
+
+def test_prefill_c4_full_size(moe, c4):
+    check_full_size(moe, c4, "c4")
+
+
+def test_prefill_c4b3_full_size(moe, c4b3):
+    """The same chunk over 3-bit routed records (the shared expert stays 4-bit)."""
+    check_full_size(moe, c4b3, "c4b3")
+
+
+def test_prefill_bounded_wait_reports_timeout(moe):
+    """A pipeline stage of the gate_up GEMM that never completes: every wait
+    behind it gives up within the limit, the call reports MOE_ETIMEOUT, and
+    the next call on the same context is correct."""
+    import os
+    rng = np.random.default_rng(301)
+    H, E, k, I, t = 256, 8, 2, 128, 64
+    layer = synth.make_layer(rng, H, E, k, I, 4, shared=True)
+    ol = oracle.Layer(layer)
+    x = rows_with_gap(ol, rng, t, H)
+    dl = moe.DeviceLayers([layer])
+    dl.set_flags(moe.TEST_WITHHOLD)
+    xt = torch.from_numpy(x).cuda()
+    out = torch.empty((t, H), dtype=torch.int16, device="cuda")
+    ws = moe.alloc_workspace(moe.prefill_workspace(dl, t))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    old = os.environ.get("MOE_TIMEOUT_MS")
+    os.environ["MOE_TIMEOUT_MS"] = "50"
+    try:
+        moe.prefill(dl, xt, out, ws, status)
+        torch.cuda.synchronize()
+    finally:
+        if old is None:
+            del os.environ["MOE_TIMEOUT_MS"]
+        else:
+            os.environ["MOE_TIMEOUT_MS"] = old
+    assert status.item() == moe.ETIMEOUT, moe.STATUS_NAMES.get(status.item())
+    dl.set_flags(0)
+    got, idx = run_prefill(moe, dl, x)
+    ref = oracle.prefill_rows(ol, x, np.arange(t), mirror=True)
+    assert np.array_equal(idx, ref["idx"])
+    assert_prefill_close(got, ref, x, 0, np.arange(t), "prefill after a timed-out call")
 
 
 def test_prefill_c4_group(moe, c4):
