@@ -69,7 +69,11 @@ typedef struct {
   const uint16_t *shared_gate; /* bf16 [hidden]; NULL = no shared expert */
   const void *shared_record;   /* 4-bit record of the shared expert (NULL iff shared_gate is) */
   moe_q sh_gate_up, sh_down;   /* relative to shared_record */
-  const uint64_t *expert_addr; /* device array [n_experts] of record base addresses */
+  const uint64_t *expert_addr; /* device array [n_experts] of record base addresses; 0 = the
+                                  record is not resident on this GPU (an expert-parallel
+                                  shard): the expert is routed as usual but contributes
+                                  nothing here (decode; prefill reports MOE_EDEVICE
+                                  when a row routes to such an expert) */
   moe_q gate_up, down;         /* relative to each routed record */
 } moe_layer;
 
@@ -102,9 +106,10 @@ enum moe_status {
  *   logits   [nb][n_experts] float32, or NULL
  *   topk_idx [nb][top_k] uint32 (descending logit)
  *   topk_w   [nb][top_k] float32 (sum to 1 per row)
- *   slot_row [64] uint64: record addresses of the union in first-seen order,
- *            [62] = [63] = union size (every record is resident)
- *   wmap_row [4][64] float32: row b's weight for union slot j, else 0
+ *   slot_row [64] uint64: record addresses of the union's resident experts
+ *            (expert_addr != 0) in first-seen order; [62] = their count,
+ *            [63] = the union size (equal when every record is resident)
+ *   wmap_row [4][64] float32: row b's weight for slot j of slot_row, else 0
  *   work     device workspace of at least moe_forward_workspace(L, 1, nb) bytes
  * Returns MOE_OK or a negative moe_status. */
 int moe_route(const moe_layer *L, const float *x, int nb, float *logits, uint32_t *topk_idx,

@@ -565,6 +565,43 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
   __syncwarp();
 }
 
+// The union's slots whose record is resident on this GPU (address != 0; an
+// expert-parallel shard holds only its own experts' records), kept in union
+// order (warp 0).  wm columns move with their slots; *nres = their count.
+__device__ void resident_compact(int *uni, float *wm, const uint64_t *eaddr_s, int U, volatile int *nres) {
+  const int lane = threadIdx.x & 31;
+  int id[2];
+  bool res[2];
+  float w[2][4];
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    const int j = lane + 32 * h;
+    id[h] = j < U ? uni[j] : 0;
+    res[h] = j < U && eaddr_s[id[h]] != 0ull;
+#pragma unroll
+    for (int b = 0; b < 4; b++) w[h][b] = wm[b * 64 + j];
+  }
+  const uint32_t b0 = __ballot_sync(FULL, res[0]), b1 = __ballot_sync(FULL, res[1]);
+  const uint32_t lt = (1u << lane) - 1u;
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; h++)
+#pragma unroll
+    for (int b = 0; b < 4; b++) wm[b * 64 + lane + 32 * h] = 0.f;
+  __syncwarp();
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    if (res[h]) {
+      const int pos = h == 0 ? __popc(b0 & lt) : __popc(b0) + __popc(b1 & lt);
+      uni[pos] = id[h];
+#pragma unroll
+      for (int b = 0; b < 4; b++) wm[b * 64 + pos] = w[h][b];
+    }
+  }
+  if (lane == 0) *nres = __popc(b0) + __popc(b1);
+  __syncwarp();
+}
+
 // Every CTA's logits of layer l into lg[b][e].  Word (c, j) of writer CTA c
 // holds logit row rr0(c) + j / nb of activation row j % nb, tagged with
 // l + 1, in the half of the buffer for l's parity.  The half cannot be
@@ -906,16 +943,21 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     if (tid < 4) gam[tid] = (hs && tid < nb) ? 1.f / (1.f + expf(-lg[tid * E1 + E])) : 0.f;
     __syncthreads();
     MOE_STAMP(9)
-    if (warp == 0) union_warp(sidx, sw, nb, K, uni, wm, posof, reinterpret_cast<int *>(red), sflag + 1);
+    if (warp == 0) {
+      union_warp(sidx, sw, nb, K, uni, wm, posof, reinterpret_cast<int *>(red), sflag + 1);
+      resident_compact(uni, wm, eaddr_s, sflag[1], sflag + 2);
+    }
     __syncthreads();
     MOE_STAMP(10)
-    s.U = sflag[1];
+    const int Uall = sflag[1];
+    s.U = sflag[2];  // the resident slots: the ones this GPU computes
     if (tid < s.U) rect[tid + s.hsi] = reinterpret_cast<const uint8_t *>(eaddr_s[uni[tid]]);
     if (cta == 0) {
       if (P.slot_tab)
         for (int j = tid; j < kSlotStride; j += NT) {
           uint64_t v = j < s.U ? eaddr_s[uni[j]] : 0ull;
-          if (j == kSlotStride - 2 || j == kSlotStride - 1) v = (uint64_t)s.U;
+          if (j == kSlotStride - 2) v = (uint64_t)s.U;
+          if (j == kSlotStride - 1) v = (uint64_t)Uall;
           P.slot_tab[(size_t)l * kSlotStride + j] = v;
         }
       if (P.wmap)
@@ -943,6 +985,20 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       for (int q = issued; q < n && q < S; q++) issue_at(get_unit<BITS>(q, s, L, rect), qbase + q);
     }
     issued = n < S ? n : S;
+    if (s.nslots == 0) {
+      // nothing of this layer is resident here (an expert-parallel shard
+      // whose experts no row chose, without the shared expert): the output
+      // is the residual, or zero; CTA c writes 64-row ranges c, c + G, ...
+      for (int rt = cta; rt < ng; rt += G) {
+        for (int j = tid; j < 64 * nb; j += NT) {
+          const int r = j & 63, b = j >> 6;
+          const size_t o = (size_t)b * H + rt * 64 + r;
+          dst[o] = (L.flags & kResidual) ? __ldcg(src + o) : 0.f;
+        }
+        __syncthreads();
+        if (tid == 0) red_release_add(cnt + kCntRows, 1u);
+      }
+    }
 
     // ---- G + D: the unit loop, each group taking the next free unit
     MOE_STAMP(5)
