@@ -30,7 +30,8 @@ class OLayer(ctypes.Structure):
                 ("router", ctypes.c_void_p), ("shared_gate", ctypes.c_void_p),
                 ("shared_record", ctypes.c_void_p), ("sh_gate_up", OQ), ("sh_down", OQ),
                 ("experts", ctypes.c_void_p), ("stride", ctypes.c_uint64),
-                ("gate_up", OQ), ("down", OQ)]
+                ("gate_up", OQ), ("down", OQ),
+                ("expert_bits", ctypes.c_void_p), ("gate_up_w", OQ * 3), ("down_w", OQ * 3)]
 
 
 def build(force: bool = False) -> str:
@@ -101,6 +102,14 @@ class Layer:
                         _oq(sl.gate_up) if sl else OQ(), _oq(sl.down) if sl else OQ(),
                         _ptr(layer.records), layer.layout.stride,
                         _oq(layer.layout.gate_up), _oq(layer.layout.down))
+        if getattr(layer, "expert_bits", None) is not None:
+            # mixed widths: each routed record at its own width, the
+            # projections' offsets per width (index 4 - width)
+            self._keep.append(layer.expert_bits)
+            self.c.expert_bits = _ptr(layer.expert_bits)
+            for i, b in enumerate((4, 3, 2)):
+                self.c.gate_up_w[i] = _oq(layer.layouts[b].gate_up)
+                self.c.down_w[i] = _oq(layer.layouts[b].down)
 
 
 def code_at(words: np.ndarray, i: int, bits: int) -> int:

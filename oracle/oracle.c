@@ -29,6 +29,9 @@
  *    name the gate but not its activation; sigmoid is the reading taken.
  *  - `expert_qmm_from` (struct Gpu page): low-bit (3/2-bit) records only for
  *    routed experts; "dense projections stay Q4", so the shared expert is 4-bit.
+ *  - `encode_block` (struct Gpu page): fetched records carry the miss
+ *    precision while resident ones keep theirs, so one union may mix 4-, 3-
+ *    and 2-bit records; each routed expert is evaluated at its own width.
  *  - `encode_block` (struct Gpu page): the block output feeds the next block
  *    through a fused norm; stacked layers here use x_{l+1} = x_l + MoE(x^_l)
  *    with x^ the unit-weight RMSNorm (eps 1e-6) when the layer's flags ask.
@@ -61,6 +64,11 @@ typedef struct {
   const uint8_t *experts;        /* E records, `stride` bytes apart */
   uint64_t stride;
   oq_t gate_up, down;
+  /* Mixed widths (NULL = every routed record has `bits`): the code width of
+   * each routed record, and the projections' offsets inside a record of
+   * width 4, 3 and 2 (index 4 - width). */
+  const uint8_t *expert_bits;
+  oq_t gate_up_w[3], down_w[3];
 } oracle_layer_t;
 
 enum { ORACLE_RESIDUAL = 1, ORACLE_PRENORM = 2 };
@@ -244,10 +252,28 @@ void oracle_expert_mirror(const uint8_t *rec, const oq_t *gu, const oq_t *dn, in
   expert_row(rec, gu, dn, bits, inter, x, y, 1, weight, allow);
 }
 
+/* Record, projections and width of routed expert e. */
+static void routed_record(const oracle_layer_t *L, int e, const uint8_t **rec, const oq_t **gu, const oq_t **dn,
+                          int *bits) {
+  *rec = L->experts + (uint64_t)e * L->stride;
+  if (L->expert_bits) {
+    *bits = L->expert_bits[e];
+    *gu = &L->gate_up_w[4 - *bits];
+    *dn = &L->down_w[4 - *bits];
+  } else {
+    *bits = L->bits;
+    *gu = &L->gate_up;
+    *dn = &L->down;
+  }
+}
+
 /* Exported for the brute-force pin: expert `e` of a layer on one row. */
 void oracle_expert(const oracle_layer_t *L, int e, const double *x, double *y) {
-  expert_row(L->experts + (uint64_t)e * L->stride, &L->gate_up, &L->down, L->bits, L->inter, x, y,
-             0, 1.0, NULL);
+  const uint8_t *rec;
+  const oq_t *gu, *dn;
+  int bits;
+  routed_record(L, e, &rec, &gu, &dn, &bits);
+  expert_row(rec, gu, dn, bits, L->inter, x, y, 0, 1.0, NULL);
 }
 
 /* Exported for the brute-force pin: the shared expert on one row (4-bit). */
@@ -463,8 +489,11 @@ void oracle_prefill_rows(const oracle_layer_t *L, const float *x, const int64_t 
     for (int i = 0; i < H; i++) xe[i] = mirror ? round_bf16(xb[i]) : xb[i];
     for (int i = 0; i < H; i++) ob[i] = 0.0;
     for (int r = 0; r < k; r++) {
-      expert_row(L->experts + (uint64_t)id[r] * L->stride, &L->gate_up, &L->down, L->bits,
-                 L->inter, xe, y, mirror, wt[r], al);
+      const uint8_t *rec;
+      const oq_t *gu, *dn;
+      int bits;
+      routed_record(L, id[r], &rec, &gu, &dn, &bits);
+      expert_row(rec, gu, dn, bits, L->inter, xe, y, mirror, wt[r], al);
       for (int i = 0; i < H; i++) ob[i] += wt[r] * y[i];
     }
     if (L->shared_gate) {

@@ -161,6 +161,11 @@ class Layer:
     shared_layout: RecordLayout | None
     records: np.ndarray           # uint8 [E][stride]
     layout: RecordLayout
+    # mixed widths: the code width of each routed record (uint8 [E]) and the
+    # record layout of each width; records stay `layout.stride` (the 4-bit
+    # stride) apart, a narrower record using the front of its slot
+    expert_bits: np.ndarray | None = None
+    layouts: dict | None = None
 
 
 # per-layer flags (same values as the C ABI)
@@ -181,6 +186,32 @@ def make_layer(rng, hidden: int, n_experts: int, top_k: int, inter: int, bits: i
         sg = f32_to_bf16_bits(rng.normal(0.0, gate_std, size=hidden).astype(np.float32))
         srec = make_records(rng, 1, slay, shared_scale[0], shared_scale[1], shared_bias_noise)[0]
     return Layer(hidden, n_experts, top_k, inter, bits, flags, router, sg, srec, slay, records, lay)
+
+
+LOWBIT_SCALE, LOWBIT_BIAS_NOISE = (0.01, 0.04), 0.0
+
+
+def make_mixed_layer(rng, hidden: int, n_experts: int, top_k: int, inter: int, expert_bits,
+                     shared: bool = True, flags: int = 0) -> Layer:
+    """A layer whose routed records have per-expert widths (4, 3 or 2 bits):
+    4-bit records drawn as in make_layer, 3- and 2-bit ones with the low-bit
+    scales (and no bias noise) of the low-bit workloads."""
+    expert_bits = np.ascontiguousarray(expert_bits, dtype=np.uint8)
+    assert expert_bits.shape == (n_experts,) and set(expert_bits.tolist()) <= {2, 3, 4}
+    layouts = {b: record_layout(hidden, inter, b) for b in (4, 3, 2)}
+    base = make_layer(rng, hidden, n_experts, top_k, inter, 4, shared=shared, flags=flags)
+    recs = np.zeros_like(base.records)
+    for e in range(n_experts):
+        b = int(expert_bits[e])
+        lay = layouts[b]
+        if b == 4:
+            recs[e] = base.records[e]
+        else:
+            recs[e, :lay.stride] = make_records(rng, 1, lay, LOWBIT_SCALE[0], LOWBIT_SCALE[1], LOWBIT_BIAS_NOISE)[0]
+    base.records = recs
+    base.expert_bits = expert_bits
+    base.layouts = layouts
+    return base
 
 
 def make_x(rng, nb: int, hidden: int, rho: float = 0.0) -> np.ndarray:

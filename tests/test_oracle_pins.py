@@ -235,6 +235,58 @@ def test_dense_bruteforce_all_experts_masked(bits, shared, flags):
         assert np.allclose(r["out"][b], dense, rtol=1e-9, atol=1e-12)
 
 
+@pytest.mark.parametrize("flags", [0, synth.RESIDUAL | synth.PRENORM])
+def test_mixed_width_dense_bruteforce(flags):
+    """A union mixing 4-, 3- and 2-bit records: every expert evaluated densely
+    at its own width by the independent numpy decoding, weighted by the
+    masked, renormalised softmax; must equal the oracle's routed evaluation
+    (which picks each record's width and offsets from the per-expert array)."""
+    H, E, k, I, nb = 128, 12, 4, 64, 4
+    rng = np.random.default_rng(31)
+    eb = np.array([4, 3, 2] * 4, dtype=np.uint8)
+    rng.shuffle(eb)
+    layer = synth.make_mixed_layer(rng, H, E, k, I, eb, shared=True, flags=flags)
+    x = rng.normal(size=(nb, H))
+    r = oracle.moe_layer(oracle.Layer(layer), x)
+    assert set(eb[r["union"]].tolist()) == {2, 3, 4}, "the union should hold every width"
+    R = synth.bf16_bits_to_f32(layer.router).astype(np.float64)
+    for b in range(nb):
+        xb = x[b]
+        if flags & synth.PRENORM:
+            xb = xb / np.sqrt(np.mean(xb * xb) + 1e-6)
+        logits = R @ xb
+        p = scipy.special.softmax(logits)
+        top = np.argsort(-logits, kind="stable")[:k]
+        mask = np.zeros(E)
+        mask[top] = 1
+        wts = p * mask / (p * mask).sum()
+        dense = sum(wts[e] * _np_expert(layer.records[e], layer.layouts[int(eb[e])], int(eb[e]), xb)
+                    for e in range(E))
+        sg = synth.bf16_bits_to_f32(layer.shared_gate).astype(np.float64)
+        dense = dense + scipy.special.expit(sg @ xb) * _np_expert(layer.shared_record, layer.shared_layout, 4, xb)
+        if flags & synth.RESIDUAL:
+            dense = dense + x[b]
+        assert sorted(r["idx"][b]) == sorted(top)
+        assert np.allclose(r["out"][b], dense, rtol=1e-9, atol=1e-12)
+
+
+def test_mixed_width_reads_each_record_at_its_own_width():
+    """Reading a narrower record with the 4-bit layout gives a different
+    expert: the per-expert widths are not a no-op."""
+    H, E, k, I = 128, 6, 2, 64
+    rng = np.random.default_rng(32)
+    eb = np.array([4, 3, 2, 4, 3, 2], dtype=np.uint8)
+    layer = synth.make_mixed_layer(rng, H, E, k, I, eb, shared=False)
+    ol = oracle.Layer(layer)
+    x = rng.normal(size=H)
+    for e in range(E):
+        b = int(eb[e])
+        y = oracle.expert(ol, e, x)
+        assert np.allclose(y, _np_expert(layer.records[e], layer.layouts[b], b, x), rtol=1e-9, atol=1e-12)
+        if b != 4:
+            assert not np.allclose(y, _np_expert(layer.records[e], layer.layouts[4], 4, x), rtol=1e-3)
+
+
 def test_batch_rows_are_independent():
     rng = np.random.default_rng(20)
     layer = oracle.Layer(synth.make_layer(rng, 128, 8, 2, 64, 4))
