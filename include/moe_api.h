@@ -75,6 +75,13 @@ typedef struct {
                                   nothing here (decode; prefill reports MOE_EDEVICE
                                   when a row routes to such an expert) */
   moe_q gate_up, down;         /* relative to each routed record */
+  /* Mixed widths (decode only): a union may hold records of different code
+   * widths, each keeping its own (the `encode_block` passage of the struct
+   * Gpu page: fetched records carry the miss precision, resident ones keep
+   * theirs).  NULL: every routed record has `bits` and the offsets above. */
+  const uint8_t *expert_bits;   /* device array [n_experts]: 4, 3 or 2 per routed record, or NULL */
+  moe_q gate_up_w[3], down_w[3]; /* with expert_bits: the offsets inside a record of width 4, 3
+                                    and 2 (index 4 - width); `bits`, gate_up and down unused */
 } moe_layer;
 
 enum {

@@ -70,6 +70,7 @@ int check_layers(const moe_layer *layers, int nl, int nb) {
   if (nb < 1 || nb > MOE_MAX_NB) return fail(MOE_EINVAL, "nb %d outside 1..%d", nb, MOE_MAX_NB);
   const moe_layer &L0 = layers[0];
   const uint32_t H = L0.hidden, E = L0.n_experts, K = L0.top_k, I = L0.inter, bits = L0.bits;
+  const bool mixed = L0.expert_bits != nullptr;
   if (H == 0 || H % 256) return fail(MOE_ESHAPE, "hidden %u must be a positive multiple of 256", H);
   if (H > 2048) return fail(MOE_ESHAPE, "hidden %u above the decode kernel's limit 2048", H);
   if (I == 0 || I % 128) return fail(MOE_ESHAPE, "inter %u must be a positive multiple of 128", I);
@@ -77,11 +78,14 @@ int check_layers(const moe_layer *layers, int nl, int nb) {
   if (E < 1 || E > 1024) return fail(MOE_ESHAPE, "n_experts %u outside 1..1024", E);
   if (K < 1 || K > E || K > 32) return fail(MOE_ESHAPE, "top_k %u outside 1..min(n_experts, 32)", K);
   if (K * (uint32_t)nb >= MOE_SLOT_STRIDE) return fail(MOE_ESHAPE, "top_k * nb = %u must be < 64", K * nb);
-  if (bits != 2 && bits != 3 && bits != 4) return fail(MOE_ESHAPE, "bits %u not in {2,3,4}", bits);
+  if (!mixed && bits != 2 && bits != 3 && bits != 4) return fail(MOE_ESHAPE, "bits %u not in {2,3,4}", bits);
   for (int l = 0; l < nl; l++) {
     const moe_layer &L = layers[l];
-    if (L.hidden != H || L.n_experts != E || L.top_k != K || L.inter != I || L.bits != bits)
-      return fail(MOE_ESHAPE, "layer %d: dimensions or bits differ from layer 0", l);
+    if (L.hidden != H || L.n_experts != E || L.top_k != K || L.inter != I)
+      return fail(MOE_ESHAPE, "layer %d: dimensions differ from layer 0", l);
+    if ((L.expert_bits != nullptr) != mixed)
+      return fail(MOE_EINVAL, "layer %d: expert_bits must be set on every layer or on none", l);
+    if (!mixed && L.bits != bits) return fail(MOE_ESHAPE, "layer %d: bits differ from layer 0", l);
     if (L.group != 64) return fail(MOE_ESHAPE, "layer %d: group %u, only 64 is supported", l, L.group);
     if (L.flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM | MOE_TEST_WITHHOLD))
       return fail(MOE_EINVAL, "layer %d: unknown flags 0x%x", l, L.flags);
@@ -97,8 +101,15 @@ int check_layers(const moe_layer *layers, int nl, int nb) {
       if ((r = check_q(L.sh_down, H, I, "sh_down", l))) return r;
     }
     int r;
-    if ((r = check_q(L.gate_up, 2 * I, H, "gate_up", l))) return r;
-    if ((r = check_q(L.down, H, I, "down", l))) return r;
+    if (mixed) {
+      for (int i = 0; i < 3; i++) {
+        if ((r = check_q(L.gate_up_w[i], 2 * I, H, "gate_up_w", l))) return r;
+        if ((r = check_q(L.down_w[i], H, I, "down_w", l))) return r;
+      }
+    } else {
+      if ((r = check_q(L.gate_up, 2 * I, H, "gate_up", l))) return r;
+      if ((r = check_q(L.down, H, I, "down", l))) return r;
+    }
   }
   return MOE_OK;
 }
@@ -136,7 +147,8 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   static_assert(sizeof(moe::FwdParams) < 32000, "kernel parameters too large");
   moe::FwdParams p;
   memset(&p, 0, sizeof p);
-  p.H = H, p.E = E, p.K = (int)L0.top_k, p.I = I, p.nb = nb, p.nl = nl, p.bits = (int)L0.bits;
+  p.H = H, p.E = E, p.K = (int)L0.top_k, p.I = I, p.nb = nb, p.nl = nl;
+  p.bits = L0.expert_bits ? 0 : (int)L0.bits;  // 0: the mixed-width kernel instance
   p.route_only = route_only;
   p.x = x, p.out = out;
   p.slot_tab = slot_tab, p.wmap = wmap, p.topk_idx = topk_idx, p.topk_w = topk_w, p.logits_out = logits;
@@ -162,6 +174,12 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
     q.sdn = {(uint32_t)L.sh_down.w, (uint32_t)L.sh_down.s, (uint32_t)L.sh_down.b};
     q.flags = L.flags & (MOE_RESIDUAL | MOE_PRENORM);
     if (L.flags & MOE_TEST_WITHHOLD) p.withhold = 1;
+    q.ebits = L.expert_bits;
+    if (L.expert_bits)
+      for (int i = 0; i < 3; i++) {
+        q.guw[i] = {(uint32_t)L.gate_up_w[i].w, (uint32_t)L.gate_up_w[i].s, (uint32_t)L.gate_up_w[i].b};
+        q.dnw[i] = {(uint32_t)L.down_w[i].w, (uint32_t)L.down_w[i].s, (uint32_t)L.down_w[i].b};
+      }
   }
   int grid = 0, smem = 0;
   if (moe::decode_plan(dev, p, &grid, &smem) != 0)
@@ -178,7 +196,8 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
 int check_offsets_fit(const moe_layer *layers, int nl) {
   for (int l = 0; l < nl; l++) {
     const moe_layer &L = layers[l];
-    const moe_q *qs[4] = {&L.gate_up, &L.down, &L.sh_gate_up, &L.sh_down};
+    const moe_q *qs[10] = {&L.gate_up,      &L.down,         &L.sh_gate_up,   &L.sh_down,      &L.gate_up_w[0],
+                           &L.gate_up_w[1], &L.gate_up_w[2], &L.down_w[0],    &L.down_w[1],    &L.down_w[2]};
     for (const moe_q *q : qs)
       if ((q->w | q->s | q->b) >> 32) return fail(MOE_ESHAPE, "layer %d: record offsets must be < 4 GiB", l);
   }
@@ -279,6 +298,7 @@ int check_prefill(const moe_layer *L, int t) {
   if (I == 0 || I % 64 || I > 16384) return fail(MOE_ESHAPE, "inter %u must be a multiple of 64 in 64..16384", I);
   if (E < 1 || E > 1024) return fail(MOE_ESHAPE, "n_experts %u outside 1..1024", E);
   if (K < 1 || K > E || K > 32) return fail(MOE_ESHAPE, "top_k %u outside 1..min(n_experts, 32)", K);
+  if (L->expert_bits) return fail(MOE_EINVAL, "mixed record widths (expert_bits) are supported by decode only");
   if (L->bits != 2 && L->bits != 3 && L->bits != 4) return fail(MOE_ESHAPE, "bits %u not in {2,3,4}", L->bits);
   // the GEMMs stage code rows with 16-byte copies: a 3-bit row (3 * in / 8
   // bytes) is 16-byte aligned when in is a multiple of 128

@@ -125,5 +125,50 @@ struct Codec<3> {
   }
 };
 
+// The same codes in the pair order of the 4-bit codec (lo, hi and shifts of
+// Codec<4>), so that records of every width can share one set of
+// activation fragments: the codec a union mixing widths uses.  Pair p holds
+// codes 8(p/4) + p%4 and 8(p/4) + p%4 + 4 of the lane's 32, both at shift 0.
+template <int BITS>
+struct CodecO4;
+
+template <>
+struct CodecO4<4> : Codec<4> {};
+
+// 2-bit: the codes 8h..8h+7 of word w are bytes 2h (codes 8h..8h+3) and
+// 2h+1 (8h+4..8h+7); a byte permute puts them at bits 0 and 16, so pair j of
+// the group is one shift and one mask-or away.
+template <>
+struct CodecO4<2> {
+  static constexpr int kWords = 2;
+  __device__ static __forceinline__ void unpack(const uint32_t (&w)[kWords], uint32_t (&bf)[16]) {
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+      const int h = g & 1;
+      // result bytes: w.byte(2h), 0, w.byte(2h+1), 0 (selector 4 = the zero operand's byte 0)
+      const uint32_t v = __byte_perm(w[g >> 1], 0u, (2 * h) | (4 << 4) | ((2 * h + 1) << 8) | (4 << 12));
+#pragma unroll
+      for (int j = 0; j < 4; j++) bf[4 * g + j] = ((v >> (2 * j)) & 0x00030003u) | kMagic;
+    }
+  }
+};
+
+// 3-bit: the codes 8g..8g+7 are the 24 bits of the 96-bit stream from bit
+// 24g; codes 4..7 of that window move up by 4 bits (to bit 16 + 3j) with
+// one shift and one bit select, then pair j is one shift and one mask-or.
+template <>
+struct CodecO4<3> {
+  static constexpr int kWords = 3;
+  __device__ static __forceinline__ void unpack(const uint32_t (&w)[kWords], uint32_t (&bf)[16]) {
+    const uint32_t win[4] = {w[0], __funnelshift_r(w[0], w[1], 24), __funnelshift_r(w[1], w[2], 16), w[2] >> 8};
+#pragma unroll
+    for (int g = 0; g < 4; g++) {
+      const uint32_t v = win[g];
+      const uint32_t u = (v & 0x0000ffffu) | ((v << 4) & 0xffff0000u);
+#pragma unroll
+      for (int j = 0; j < 4; j++) bf[4 * g + j] = ((u >> (3 * j)) & 0x00070007u) | kMagic;
+    }
+  }
+};
 
 }  // namespace moe

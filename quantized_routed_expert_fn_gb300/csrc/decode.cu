@@ -33,6 +33,8 @@
 // `SLOT_STRIDE` (gpu.rs source page).
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "codec.cuh"
 #include "decode.cuh"
 
@@ -266,11 +268,13 @@ struct ColC {
 // sc / bi point at the scale / bias pair word of row r0 for this block, the
 // words of the next rows `ss` words apart (the stage's [row][pair] tables).  Returns per lane (t == 0 lanes after the sums) the outputs of rows
 // g and g+8 for activation rows b = 2*half + {0,1}.
-template <int B, int NH>
+template <int B, int NH, bool O4 = false>
 __device__ __forceinline__ void item_compute(const uint8_t *row_g, const uint8_t *row_g8, const uint32_t *sc,
                                              const uint32_t *bi, int ss, int g, int y, const uint2 (&xb)[NH][8],
                                              const ColC (&cc)[NH], float (&o)[NH][4]) {
-  uint32_t wa[Codec<B>::kWords], wb[Codec<B>::kWords];
+  // O4: the 4-bit pair order for every width (a union mixing widths)
+  using C = typename std::conditional<O4, CodecO4<B>, Codec<B>>::type;
+  uint32_t wa[C::kWords], wb[C::kWords];
   if constexpr (B == 4) {
     const uint4 va = *reinterpret_cast<const uint4 *>(row_g), vb = *reinterpret_cast<const uint4 *>(row_g8);
     wa[0] = va.x, wa[1] = va.y, wa[2] = va.z, wa[3] = va.w;
@@ -284,8 +288,8 @@ __device__ __forceinline__ void item_compute(const uint8_t *row_g, const uint8_t
   }
   const uint32_t sg = sc[g * ss], sg8 = sc[(g + 8) * ss], bg = bi[g * ss], bg8 = bi[(g + 8) * ss];
   uint32_t fa[16], fb[16];
-  Codec<B>::unpack(wa, fa);
-  Codec<B>::unpack(wb, fb);
+  C::unpack(wa, fa);
+  C::unpack(wb, fb);
   const float s0 = y ? bf16hi(sg) : bf16lo(sg), s8 = y ? bf16hi(sg8) : bf16lo(sg8);
   const float b0 = y ? bf16hi(bg) : bf16lo(bg), b8 = y ? bf16hi(bg8) : bf16lo(bg8);
 #pragma unroll
@@ -341,7 +345,7 @@ __device__ __forceinline__ ColC col_consts(float cs0, float cs1, float xs0, floa
 // Writes red[(kb*2 + tile)*64 + row*4 + b].
 // Warp wi of nw takes blocks wi, wi + nw, ... (both tiles of a block share
 // its activation registers).
-template <int B, int NH>
+template <int B, int NH, bool O4 = false>
 __device__ void gate_up_compute(const uint8_t *st, const uint32_t *sw, int H, const uint2 *xb, const float *xs,
                                 const float *cs, int nb, float *red, int wi, int nw) {
   const int lane = threadIdx.x & 31;
@@ -363,7 +367,7 @@ __device__ void gate_up_compute(const uint8_t *st, const uint32_t *sw, int H, co
   for (int tile = 0; tile < 2; tile++) {
     const int r0 = 16 * tile;
     float o[NH][4];
-    item_compute<B, NH>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
+    item_compute<B, NH, O4>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
                         st + (r0 + g + 8) * rb + kb * (16 * B) + t * (4 * B), sc + r0 * np, bi + r0 * np, np, g, y,
                         x, cc, o);
     if (t == 0) {
@@ -384,7 +388,7 @@ __device__ void gate_up_compute(const uint8_t *st, const uint32_t *sw, int H, co
 // words.  Writes red[(kb*4 + tile)*64 + row*4 + b].
 // Warp wi of nw takes passes wi, wi + nw, ... of two row tiles of one
 // block (pass p: block p / 2, tiles 2 (p % 2) and 2 (p % 2) + 1).
-template <int B, int NH>
+template <int B, int NH, bool O4 = false>
 __device__ void down_compute(const uint8_t *st, const uint32_t *sw, int I, const uint2 *xb, const float *xs,
                              const float *cs, int nb, float *red, int wi, int nw) {
   const int lane = threadIdx.x & 31;
@@ -408,7 +412,7 @@ __device__ void down_compute(const uint8_t *st, const uint32_t *sw, int I, const
     const int tile = 2 * (pass & 1) + k;
     const int r0 = 16 * tile;
     float o[NH][4];
-    item_compute<B, NH>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
+    item_compute<B, NH, O4>(st + (r0 + g) * rb + kb * (16 * B) + t * (4 * B),
                         st + (r0 + g + 8) * rb + kb * (16 * B) + t * (4 * B), sc + r0 * np, bi + r0 * np, np, g, y,
                         x, cc, o);
     if (t == 0) {
@@ -686,9 +690,10 @@ struct UnitDesc {
   int bits;
 };
 
+// BITS = 0: a union mixing widths; slot j's width is sbits[j].
 template <int BITS>
 __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP &L,
-                                             const uint8_t *const *rect) {
+                                             const uint8_t *const *rect, const int *sbits) {
   UnitDesc d;
   const int c = blockIdx.x, G = gridDim.x;
   if (q < s.nGU) {
@@ -700,8 +705,13 @@ __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP
   }
   const bool shared = s.hsi && d.slot == 0;
   d.rec = shared ? L.srec : rect[d.slot];
-  d.q = shared ? (d.down ? L.sdn : L.sgu) : (d.down ? L.dn : L.gu);
-  d.bits = shared ? 4 : BITS;
+  if (BITS == 0 && !shared) {
+    d.bits = sbits[d.slot];
+    d.q = d.down ? L.dnw[4 - d.bits] : L.guw[4 - d.bits];
+  } else {
+    d.q = shared ? (d.down ? L.sdn : L.sgu) : (d.down ? L.dn : L.gu);
+    d.bits = shared ? 4 : BITS;
+  }
   return d;
 }
 
@@ -747,11 +757,14 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   const int E1 = (E + 1 + 3) & ~3;
   const int ng = H / 64;
   const int S = P.stages;
+  // codec order of the routed activation fragments: BITS's own, or the
+  // 4-bit order that every width can read when the union mixes widths
+  constexpr int AB = BITS == 0 ? 4 : BITS;
 
   uint8_t *stages = sm;                                                  // [S][stage_bytes]
   float *xf = reinterpret_cast<float *>(sm + (size_t)S * P.stage_bytes);  // [nb][H]
   uint2 *xa = reinterpret_cast<uint2 *>(xf + nb * H);                    // [nblkH][8][32] routed codec order
-  uint2 *xa4 = BITS == 4 ? xa : xa + nblkH * 256;                        // shared (4-bit) order
+  uint2 *xa4 = AB == 4 ? xa : xa + nblkH * 256;                          // shared (4-bit) order
   float *xs = reinterpret_cast<float *>(xa4 + nblkH * 256);              // [4][H/64] group sums of x
   float *cs = xs + 4 * ng;                                               // [4][H/64] offset sums, routed order
   float *cs4 = cs + 4 * ng;                                              // [4][H/64] offset sums, 4-bit order
@@ -771,6 +784,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(reinterpret_cast<uint32_t *>(hsm) + 2 * hsz);  // [E]
   unsigned *stg_unit = reinterpret_cast<unsigned *>(eaddr_s + ((E + 1) & ~1));  // [S] last unit issued per stage
   int *posof = reinterpret_cast<int *>(stg_unit + kMaxStages);                   // [E] union scratch, INT_MAX between uses
+  int *sbits = posof + E;                                                        // [64] slot -> code width (mixed)
+  uint8_t *eb_s = reinterpret_cast<uint8_t *>(sbits + 64);                       // [E] expert -> code width (mixed)
 
   if (tid == 0) {
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu;
@@ -810,7 +825,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.U = 0;
     int issued = 0;
     if (warp == kProducerWarp) {
-      for (; issued < s.nA && issued < S; issued++) issue_at(get_unit<BITS>(issued, s, L, rect), qbase + issued);
+      for (; issued < s.nA && issued < S; issued++)
+        issue_at(get_unit<BITS>(issued, s, L, rect, sbits), qbase + issued);
     }
     issued = s.nA < S ? s.nA : S;
 
@@ -833,6 +849,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       }
     }
     for (int e = tid; e < E; e += NT) eaddr_s[e] = L.eaddr[e];
+    if (BITS == 0)
+      for (int e = tid; e < E; e += NT) eb_s[e] = L.ebits[e];
     if (l > 0 && !cta_wait(P.cnt + (size_t)(l - 1) * kCntPerLayer + kCntRows, (unsigned)(H / 64), P, sflag)) {
       drain_ring(bars, qbase, qbase + issued, S, P);
       return;
@@ -887,8 +905,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       }
     }
     __syncthreads();
-    stage_frags<BITS>(xf, H, nb, xa, xs, cs);
-    if (BITS != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr, cs4);
+    stage_frags<AB>(xf, H, nb, xa, xs, cs);
+    if (AB != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr, cs4);
     __syncthreads();
     MOE_STAMP(2)
     {
@@ -951,7 +969,16 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     MOE_STAMP(10)
     const int Uall = sflag[1];
     s.U = sflag[2];  // the resident slots: the ones this GPU computes
-    if (tid < s.U) rect[tid + s.hsi] = reinterpret_cast<const uint8_t *>(eaddr_s[uni[tid]]);
+    if (tid < s.U) {
+      rect[tid + s.hsi] = reinterpret_cast<const uint8_t *>(eaddr_s[uni[tid]]);
+      if (BITS == 0) {
+        const int b = eb_s[uni[tid]];
+        // a width outside {2, 3, 4} is reported; its units then read the
+        // fewest bytes (2-bit), which stay inside a record of any width
+        if (b < 2 || b > 4) atomicCAS(P.status, 0, kStatusDevice);
+        sbits[tid + s.hsi] = b >= 2 && b <= 4 ? b : 2;
+      }
+    }
     if (cta == 0) {
       if (P.slot_tab)
         for (int j = tid; j < kSlotStride; j += NT) {
@@ -982,7 +1009,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.nD = rr_count(cta, s.nslots * s.nrt, G);
     const int n = s.n();
     if (warp == kProducerWarp) {
-      for (int q = issued; q < n && q < S; q++) issue_at(get_unit<BITS>(q, s, L, rect), qbase + q);
+      for (int q = issued; q < n && q < S; q++) issue_at(get_unit<BITS>(q, s, L, rect, sbits), qbase + q);
     }
     issued = n < S ? n : S;
     if (s.nslots == 0) {
@@ -1032,7 +1059,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
             if (rr1 > E && Ln.sgate) prefetch_l2(Ln.sgate, (uint32_t)(H * 2));
           }
         }
-        const UnitDesc d = get_unit<BITS>(q, s, L, rect);
+        const UnitDesc d = get_unit<BITS>(q, s, L, rect, sbits);
         const unsigned u = qbase + q;
         const uint8_t *st = stages + (size_t)(u % S) * P.stage_bytes;
         const bool shared = s.hsi && d.slot == 0;
@@ -1044,10 +1071,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           }
           cur = d.slot;
           const uint2 *hf = reinterpret_cast<const uint2 *>(P.hfrag) + (size_t)d.slot * nblkI * 256;
-          if (shared || BITS == 4)
+          if (shared || AB == 4)
             stage_h<4>(hf, I, nb, ghsm, ghxs, ghcs, grp, gt);
           else
-            stage_h<BITS>(hf, I, nb, ghsm, ghxs, ghcs, grp, gt);
+            stage_h<AB>(hf, I, nb, ghsm, ghxs, ghcs, grp, gt);
         }
         if (!grp_and(grp, stage_wait(&bars[u % S], (u / S) & 1u, P))) {
           alive = false;
@@ -1058,30 +1085,41 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         if (ok) {
           const int rows = d.down ? 64 : 32, inp = d.down ? I : H;
           const uint32_t *sw = reinterpret_cast<const uint32_t *>(st + rows * code_pitch(inp * d.bits / 8, d.bits));
-          const float *csx = shared && BITS != 4 ? cs4 : cs;
+          const float *csx = shared && AB != 4 ? cs4 : cs;
           const uint2 *xbx = shared ? xa4 : xa;
+          // the unit's codec: 4-bit for the shared expert, BITS's own, or
+          // (mixed widths) the slot's width read in the 4-bit pair order
+          const int cb = shared ? 4 : (BITS == 0 ? d.bits : BITS);
           if (!d.down) {
             if (nb <= 2) {
-              if (shared) gate_up_compute<4, 1>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
-              else gate_up_compute<BITS, 1>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              if (cb == 4) gate_up_compute<4, 1>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              else if (BITS == 0 && cb == 3) gate_up_compute<3, 1, true>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              else if (BITS == 0) gate_up_compute<2, 1, true>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              else gate_up_compute<AB, 1>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
             } else {
-              if (shared) gate_up_compute<4, 2>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
-              else gate_up_compute<BITS, 2>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              if (cb == 4) gate_up_compute<4, 2>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              else if (BITS == 0 && cb == 3) gate_up_compute<3, 2, true>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              else if (BITS == 0) gate_up_compute<2, 2, true>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
+              else gate_up_compute<AB, 2>(st, sw, H, xbx, xs, csx, nb, gred, gw, GW);
             }
           } else {
             if (nb <= 2) {
-              if (shared) down_compute<4, 1>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
-              else down_compute<BITS, 1>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              if (cb == 4) down_compute<4, 1>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              else if (BITS == 0 && cb == 3) down_compute<3, 1, true>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              else if (BITS == 0) down_compute<2, 1, true>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              else down_compute<AB, 1>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
             } else {
-              if (shared) down_compute<4, 2>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
-              else down_compute<BITS, 2>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              if (cb == 4) down_compute<4, 2>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              else if (BITS == 0 && cb == 3) down_compute<3, 2, true>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              else if (BITS == 0) down_compute<2, 2, true>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
+              else down_compute<AB, 2>(st, sw, I, ghsm, ghxs, ghcs, nb, gred, gw, GW);
             }
           }
         }
         grp_sync(grp);
         if (q == 0) MOE_STAMP(12)
         // the stage is free: request the unit S places ahead into it
-        if (gw == kProducerWarp && q + S < n) issue_at(get_unit<BITS>(q + S, s, L, rect), u + S);
+        if (gw == kProducerWarp && q + S < n) issue_at(get_unit<BITS>(q + S, s, L, rect, sbits), u + S);
         if (!d.down) {
           // h = silu(gate) * up for 16 rows x nb, scattered as bf16 hi/lo A
           // fragments in the pair order of this slot's down codec; thread
@@ -1099,11 +1137,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
             int pi = 0, el = 0, sh = 0;
 #pragma unroll
             for (int p = 0; p < 16; p++) {
-              const bool c4 = shared || BITS == 4;
-              const int lo = c4 ? Codec<4>::lo(p) : Codec<BITS>::lo(p);
-              const int hi = c4 ? Codec<4>::hi(p) : Codec<BITS>::hi(p);
-              if (lo == cc) pi = p, el = 0, sh = c4 ? Codec<4>::slo(p) : Codec<BITS>::slo(p);
-              if (hi == cc) pi = p, el = 1, sh = c4 ? Codec<4>::shi(p) : Codec<BITS>::shi(p);
+              const bool c4 = shared || AB == 4;
+              const int lo = c4 ? Codec<4>::lo(p) : Codec<AB>::lo(p);
+              const int hi = c4 ? Codec<4>::hi(p) : Codec<AB>::hi(p);
+              if (lo == cc) pi = p, el = 0, sh = c4 ? Codec<4>::slo(p) : Codec<AB>::slo(p);
+              if (hi == cc) pi = p, el = 1, sh = c4 ? Codec<4>::shi(p) : Codec<AB>::shi(p);
             }
             const float hv = h * __uint_as_float((uint32_t)(127 - sh) << 23);  // h * 2^-sh, exact
             const uint32_t hi = f2bf(hv), lo = f2bf(hv - __uint_as_float(hi << 16));
@@ -1172,7 +1210,7 @@ static int fixed_smem(int H, int E, int I, int nb, int bits) {
   const int E1 = (E + 1 + 3) & ~3;
   int b = 0;
   b += nb * H * 4;                                 // xf
-  b += nblkH * 256 * 8 * (bits == 4 ? 1 : 2);      // xa (+ xa4)
+  b += nblkH * 256 * 8 * (bits == 4 || bits == 0 ? 1 : 2);  // xa (+ xa4; one 4-bit order when widths mix)
   b += 3 * 4 * (H / 64) * 4;                       // xs, cs, cs4
   b += 4 * E1 * 4;                                 // lg
   b += 2 * 2048 * 4;                               // red, one per unit group
@@ -1183,6 +1221,7 @@ static int fixed_smem(int H, int E, int I, int nb, int bits) {
   b += ((E + 1) & ~1) * 8;                         // expert addresses
   b += kMaxStages * 4;                             // last unit issued per stage
   b += E * 4;                                      // union scratch
+  b += 64 * 4 + ((E + 15) & ~15);                  // slot widths, expert widths (mixed)
   return b;
 }
 
@@ -1215,7 +1254,10 @@ int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes) {
   p.stages = S;
   p.stage_bytes = sb;
   const int smem = fixed + S * sb;
-  const int occ = p.bits == 4 ? occupancy_t<4>(smem) : p.bits == 3 ? occupancy_t<3>(smem) : occupancy_t<2>(smem);
+  const int occ = p.bits == 4   ? occupancy_t<4>(smem)
+                  : p.bits == 3 ? occupancy_t<3>(smem)
+                  : p.bits == 2 ? occupancy_t<2>(smem)
+                                : occupancy_t<0>(smem);
   if (occ < 1) return -1;
   const int G = sms < kMaxGrid ? sms : kMaxGrid;
   // every CTA's router rows x activation rows fit its logit words
@@ -1245,6 +1287,7 @@ cudaError_t launch_decode(const FwdParams &p, int grid, int smem, cudaStream_t s
     case 4: return launch_t<4>(p, grid, smem, st);
     case 3: return launch_t<3>(p, grid, smem, st);
     case 2: return launch_t<2>(p, grid, smem, st);
+    case 0: return launch_t<0>(p, grid, smem, st);
     default: return cudaErrorInvalidValue;
   }
 }

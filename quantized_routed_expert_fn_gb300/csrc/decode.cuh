@@ -18,6 +18,8 @@ struct LayerP {
   const uint64_t *eaddr;   // [E] record base addresses
   QOff gu, dn, sgu, sdn;
   uint32_t flags;
+  const uint8_t *ebits;    // [E] code width of each routed record (kernel instance 0, mixed widths)
+  QOff guw[3], dnw[3];     // mixed widths: offsets in a record of width 4, 3, 2 (index 4 - width)
 };
 
 // Per-layer counters in the workspace (uint32 each), every counter on a
@@ -32,7 +34,7 @@ constexpr int kMaxGrid = 160;    // CTAs of the decode kernel at most (one per S
 constexpr int kLogitWords = 32;  // flagged logit words per CTA (two 128-byte lines of one writer)
 
 struct FwdParams {
-  int H, E, K, I, nb, nl, bits;
+  int H, E, K, I, nb, nl, bits;  // bits: routed width, or 0 when each record carries its own
   int route_only;
   int withhold;  // failure-detection test: never release the router count
   const float *x;

@@ -44,7 +44,8 @@ class MoeLayer(ctypes.Structure):
                 ("router", ctypes.c_void_p), ("shared_gate", ctypes.c_void_p), ("shared_record", ctypes.c_void_p),
                 ("sh_gate_up", MoeQ), ("sh_down", MoeQ),
                 ("expert_addr", ctypes.c_void_p),
-                ("gate_up", MoeQ), ("down", MoeQ)]
+                ("gate_up", MoeQ), ("down", MoeQ),
+                ("expert_bits", ctypes.c_void_p), ("gate_up_w", MoeQ * 3), ("down_w", MoeQ * 3)]
 
 
 class MoeError(RuntimeError):
@@ -114,7 +115,8 @@ class DeviceLayers:
     """Device copies of synth.Layer weights plus the ABI structs that point at them."""
 
     def __init__(self, layers, device="cuda"):
-        self.tensors = []
+        self.tensors = []  # per layer: router, records, expert addresses, shared gate, shared record
+        self.keep = []
         arr = (MoeLayer * len(layers))()
         for i, L in enumerate(layers):
             if isinstance(L, synth.DeviceLayer):
@@ -140,6 +142,15 @@ class DeviceLayers:
                 c.sh_gate_up, c.sh_down = _q(L.shared_layout.gate_up), _q(L.shared_layout.down)
             c.expert_addr = eaddr.data_ptr()
             c.gate_up, c.down = _q(L.layout.gate_up), _q(L.layout.down)
+            if getattr(L, "expert_bits", None) is not None:
+                # mixed widths: a width per routed record, offsets per width
+                eb = L.expert_bits
+                eb = eb if isinstance(eb, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(eb))
+                eb = eb.to(device=recs.device, dtype=torch.uint8)
+                self.keep.append(eb)
+                c.expert_bits = eb.data_ptr()
+                for j, b in enumerate((4, 3, 2)):
+                    c.gate_up_w[j], c.down_w[j] = _q(L.layouts[b].gate_up), _q(L.layouts[b].down)
         self.c = arr
         self.n = len(layers)
         self.src = layers

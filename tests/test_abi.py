@@ -130,3 +130,43 @@ def test_prefill_rejects_bad_calls(m):
     assert lib.moe_prefill_workspace(arr, 0) == 0
     assert lib.moe_prefill_workspace(arr, (1 << 20) + 1) == 0
     assert lib.moe_prefill_workspace(_struct(m, L, top_k=33), 16) == 0
+
+
+def _mixed_struct(m, L, n_layers=1):
+    arr = (m.MoeLayer * n_layers)()
+    for i in range(n_layers):
+        arr[i] = _struct(m, L)[0]
+        c = arr[i]
+        c.expert_bits = 0x50000
+        for j, b in enumerate((4, 3, 2)):
+            lay = synth.record_layout(L.hidden, L.inter, b)
+            c.gate_up_w[j], c.down_w[j] = m._q(lay.gate_up), m._q(lay.down)
+    return arr
+
+
+def _forward(m, arr, n=1):
+    return m.lib().moe_forward(arr, n, 0x1000, 1, 0x200000, 0x100000, 1 << 30, None, None, None, 0x3000, None)
+
+
+def test_mixed_width_layers_host_checks(m):
+    """Per-record widths: the per-width offsets are checked like the uniform
+    ones, every layer of a call must say the same, and prefill rejects them."""
+    L = _layer()
+    assert m.lib().moe_forward_workspace(_mixed_struct(m, L), 1, 4) > 0
+    arr = _mixed_struct(m, L)
+    q = arr[0].down_w[2]
+    arr[0].down_w[2] = m.MoeQ(q.w + 16, q.s, q.b, q.out, q.inp)
+    assert _forward(m, arr) == -3, m.last_error()
+    arr = _mixed_struct(m, L)
+    q = arr[0].gate_up_w[1]
+    arr[0].gate_up_w[1] = m.MoeQ(q.w, q.s, q.b, q.out, q.inp + 64)
+    assert _forward(m, arr) == -2, m.last_error()
+    arr = _mixed_struct(m, L, n_layers=2)
+    arr[1].expert_bits = None
+    assert _forward(m, arr, 2) == -1, m.last_error()
+    # the uniform offsets are not consulted when widths are per record
+    arr = _mixed_struct(m, L)
+    arr[0].bits = 7
+    arr[0].gate_up = m.MoeQ(1, 1, 1, 1, 1)
+    assert m.lib().moe_forward_workspace(arr, 1, 1) > 0, m.last_error()
+    assert m.lib().moe_prefill_workspace(_mixed_struct(m, L), 16) == 0

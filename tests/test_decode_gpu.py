@@ -239,3 +239,89 @@ def test_bounded_wait_reports_timeout(moe):
     moe.forward(dl, x, out, ws, status)
     torch.cuda.synchronize()
     assert status.item() == 0
+
+
+# ---------------------------------------------------------------- mixed widths
+
+def mixed_widths(E, seed):
+    """4-, 3- and 2-bit records in equal shares, in a seeded order."""
+    eb = np.array([4, 3, 2] * (E // 3 + 1), dtype=np.uint8)[:E]
+    np.random.default_rng(seed).shuffle(eb)
+    return eb
+
+
+def x_with_all_widths(ol, eb, nb, seed):
+    """Seeded x with the top-k gap whose union holds every width (or, for one
+    row, as many as its k experts allow)."""
+    best = None
+    for s in range(seed, seed + 4000, 100):
+        x, _ = find_x(ol, nb, s)
+        u = oracle.route(ol, x)["union"]
+        w = set(eb[u].tolist())
+        if w == {2, 3, 4}:
+            return x, w
+        if best is None or len(w) > len(best[1]):
+            best = (x, w)
+    return best
+
+
+@pytest.mark.parametrize("nb,H,E,k,I,flags", [
+    (1, 512, 24, 6, 256, 0),
+    (4, 1024, 48, 6, 384, synth.RESIDUAL | synth.PRENORM),
+    (3, 2048, 64, 8, 512, synth.RESIDUAL | synth.PRENORM),
+    (2, 256, 12, 4, 128, synth.PRENORM),
+])
+def test_mixed_width_union(moe, nb, H, E, k, I, flags):
+    """One union holding 4-, 3- and 2-bit records, each read at its own width
+    (per-expert widths): ids, union and weights exact, outputs within
+    2e-3 x row RMS of the oracle."""
+    rng = np.random.default_rng(700 + nb + H)
+    eb = mixed_widths(E, 701 + nb)
+    layer = synth.make_mixed_layer(rng, H, E, k, I, eb, shared=True, flags=flags)
+    ol = oracle.Layer(layer)
+    x, widths = x_with_all_widths(ol, eb, nb, 800 + nb)
+    assert widths == {2, 3, 4}
+    check_layer(moe, [layer], x, f"mixed widths nb={nb} H{H} E{E} k{k} I{I}")
+
+
+def test_mixed_width_c2_verify_batch(moe):
+    """The verify batch's shape (hidden 2048, 512 experts, top-10, inter 512,
+    shared expert), nb = 4, with a third of the records at each width."""
+    rng = np.random.default_rng(710)
+    eb = mixed_widths(512, 711)
+    layer = synth.make_mixed_layer(rng, 2048, 512, 10, 512, eb, shared=True)
+    ol = oracle.Layer(layer)
+    x, widths = x_with_all_widths(ol, eb, 4, 900)
+    assert widths == {2, 3, 4}
+    check_layer(moe, [layer], x, "mixed widths c2 nb=4")
+
+
+def test_mixed_width_stack(moe):
+    """Four stacked mixed-width layers: every layer along the GPU's own
+    trajectory within 2e-3 x RMS of the oracle on the same input, and the
+    stacked call equal to chained one-layer calls bit for bit."""
+    rng = np.random.default_rng(720)
+    layers = [synth.make_mixed_layer(rng, 1024, 32, 4, 256, mixed_widths(32, 721 + l), shared=True,
+                                     flags=synth.RESIDUAL | synth.PRENORM) for l in range(4)]
+    ols = [oracle.Layer(L) for L in layers]
+    dl = moe.DeviceLayers(layers)
+    for s in range(300, 340):
+        x = synth.make_x(np.random.default_rng(s), 2, 1024)
+        cur, ok = x.astype(np.float64), True
+        for ol in ols:
+            r = oracle.moe_layer(ol, cur)
+            ok &= all(topk_gap(r["logits"][b], 4) >= GAP for b in range(2))
+            cur = r["out"]
+        if ok:
+            break
+    assert ok
+    g = run_forward(moe, dl, x)
+    cur = x.astype(np.float32)
+    worst = 0.0
+    for l in range(4):
+        ref = oracle.moe_layer(ols[l], cur.astype(np.float64))
+        step = run_forward(moe, dl, cur, n_layers=1, offset=l)
+        worst = max(worst, assert_close_rows(step["out"], ref["out"], ref["moe"], what=f"mixed stack layer {l}"))
+        cur = step["out"]
+    assert np.array_equal(g["out"].view(np.uint32), cur.view(np.uint32)), "stacked call != chained calls"
+    print(f"[parity] mixed-width stack of 4 layers: max err = {worst:.4f} of the bound")
