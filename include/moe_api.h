@@ -82,6 +82,14 @@ typedef struct {
   const uint8_t *expert_bits;   /* device array [n_experts]: 4, 3 or 2 per routed record, or NULL */
   moe_q gate_up_w[3], down_w[3]; /* with expert_bits: the offsets inside a record of width 4, 3
                                     and 2 (index 4 - width); `bits`, gate_up and down unused */
+  /* Two-tier records (decode only; the `res` pool and the deadline policy of
+   * the struct Gpu page): a routed record lives in device memory or in
+   * pinned host memory that the GPU reads directly (its expert_addr is the
+   * device pointer of that host memory).  The union is computed device
+   * records first, then host ones; slot_tab[62] counts the device ones. */
+  const uint8_t *expert_tier; /* device array [n_experts]: 0 device memory, 1 host memory; NULL: all device */
+  float cut_weak;             /* host-memory experts whose routing weight is below this in every row of
+                                 the call are cut (contribute nothing); 0 = no cut */
 } moe_layer;
 
 enum {
@@ -247,6 +255,52 @@ size_t moe_forward_workspace(const moe_layer *layers, int n_layers, int nb);
 
 /* Thread-local description of the last failing host-side check or CUDA call. */
 const char *moe_last_error(void);
+
+/* ---- two-tier expert store (the `res` LRU pool and the miss counters of
+ * the struct Gpu page; the module doc of the gpu.rs source page: a fixed
+ * pool of slots, LRU managed, filled by reads of missing records).
+ *
+ * Every routed record of a layer stack lives in pinned host memory, which
+ * the GPU reads directly over NVLink-C2C; the most recently used ones are
+ * also cached in n_slots device-memory slots.  The store owns two device
+ * tables the layers point at: expert_addr[l] (each layer's
+ * moe_layer.expert_addr) and expert_tier[l] (its expert_tier).  After a
+ * step, moe_tier_update takes the step's slot tables (copied back to the
+ * host): the experts listed become most recently used, and the ones read
+ * from host memory are copied into device slots, evicting the least
+ * recently used records that step did not use.  Copies and table updates
+ * run on `stream`; run the next step on the same stream.
+ *
+ * Ownership: host_records, slots and the two tables belong to the caller
+ * and must outlive the store; host_records is registered for device access
+ * here when it is not already pinned (and unregistered by destroy).
+ * expert_addr == NULL makes a policy-only store: no device memory, no CUDA
+ * call (the slots then have stand-in addresses after the host records). */
+typedef struct moe_tier moe_tier;
+typedef struct {
+  int resident;               /* records in device slots */
+  int last_host_reads;        /* records the last step read from host memory */
+  int last_promoted;          /* of them, copied into device slots by the last update */
+  long long promotions, evictions;
+} moe_tier_stats;
+
+/*   host_records host [n_layers][n_experts][stride] bytes (record of layer l, expert e)
+ *   slots        device [n_slots][stride] bytes
+ *   expert_addr  device [n_layers][n_experts] uint64; expert_tier device [n_layers][n_experts] uint8
+ *   stride       a multiple of 256 bytes; every record starts with its 256-byte aligned layout
+ * Starts with every record in host memory and the slots empty. */
+int moe_tier_create(int n_layers, int n_experts, size_t stride, void *host_records, void *slots, int n_slots,
+                    uint64_t *expert_addr, uint8_t *expert_tier, moe_stream_t stream, moe_tier **out);
+/* slot_tab: host copy of the step's [n_layers][64] slot tables.  Returns the
+ * number of records promoted (>= 0) or a negative moe_status. */
+int moe_tier_update(moe_tier *t, const uint64_t *slot_tab, int n_layers, moe_stream_t stream);
+/* Device slot holding (layer, expert), -1 when in host memory only, -2 for bad arguments. */
+int moe_tier_slot(const moe_tier *t, int layer, int expert);
+int moe_tier_get_stats(const moe_tier *t, moe_tier_stats *stats);
+/* Host copy of the address table, [n_layers][n_experts] (as last uploaded). */
+const uint64_t *moe_tier_addresses(const moe_tier *t);
+void moe_tier_destroy(moe_tier *t);
+const char *moe_tier_last_error(void);
 
 #ifdef __cplusplus
 }

@@ -31,7 +31,8 @@ class OLayer(ctypes.Structure):
                 ("shared_record", ctypes.c_void_p), ("sh_gate_up", OQ), ("sh_down", OQ),
                 ("experts", ctypes.c_void_p), ("stride", ctypes.c_uint64),
                 ("gate_up", OQ), ("down", OQ),
-                ("expert_bits", ctypes.c_void_p), ("gate_up_w", OQ * 3), ("down_w", OQ * 3)]
+                ("expert_bits", ctypes.c_void_p), ("gate_up_w", OQ * 3), ("down_w", OQ * 3),
+                ("expert_tier", ctypes.c_void_p), ("cut_w", ctypes.c_double)]
 
 
 def build(force: bool = False) -> str:
@@ -76,6 +77,8 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_group.argtypes = [i32, i32, i32, p, p, p, p, p, p]
         _lib.oracle_threads.restype = i32
         _lib.oracle_set_parallel_rows.argtypes = [i32]
+        _lib.oracle_cut.restype = i32
+        _lib.oracle_cut.argtypes = [ctypes.POINTER(OLayer), i32, p, p, p]
         _lib.oracle_round_bf16.restype = d
         _lib.oracle_round_bf16.argtypes = [d]
         _lib.oracle_expert_mirror.argtypes = [p, ctypes.POINTER(OQ), ctypes.POINTER(OQ), i32, i32, p, d, p, p]
@@ -102,6 +105,11 @@ class Layer:
                         _oq(sl.gate_up) if sl else OQ(), _oq(sl.down) if sl else OQ(),
                         _ptr(layer.records), layer.layout.stride,
                         _oq(layer.layout.gate_up), _oq(layer.layout.down))
+        if getattr(layer, "expert_tier", None) is not None:
+            # two tiers: host-memory experts below cut_w in every row are cut
+            self._keep.append(layer.expert_tier)
+            self.c.expert_tier = _ptr(layer.expert_tier)
+            self.c.cut_w = float(getattr(layer, "cut_w", 0.0))
         if getattr(layer, "expert_bits", None) is not None:
             # mixed widths: each routed record at its own width, the
             # projections' offsets per width (index 4 - width)
@@ -171,6 +179,16 @@ def moe_layer(layer: Layer, x: np.ndarray) -> dict:
                                _ptr(r["union"]), _ptr(r["wmap"]))
     r["union"] = r["union"][:U].copy()
     return r
+
+
+def cut(layer: Layer, idx: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """The deadline cut of one call's routing: bool [E], True for each
+    host-memory expert below the layer's cut_w in every row."""
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    out = np.zeros(layer.src.n_experts, dtype=np.uint8)
+    lib().oracle_cut(ctypes.byref(layer.c), idx.shape[0], _ptr(idx), _ptr(w), _ptr(out))
+    return out.astype(bool)
 
 
 def route(layer: Layer, x: np.ndarray) -> dict:

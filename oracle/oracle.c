@@ -32,6 +32,11 @@
  *  - `encode_block` (struct Gpu page): fetched records carry the miss
  *    precision while resident ones keep theirs, so one union may mix 4-, 3-
  *    and 2-bit records; each routed expert is evaluated at its own width.
+ *  - `cut_w` field (struct Gpu page), the deadline policy: a missing expert
+ *    (here: one whose record is in host memory) whose weight is below w in
+ *    every row is cut from the late part instead of waited for.  Read here
+ *    as always cut (the deterministic worst case of the deadline), with the
+ *    weights of the experts kept unchanged.
  *  - `encode_block` (struct Gpu page): the block output feeds the next block
  *    through a fused norm; stacked layers here use x_{l+1} = x_l + MoE(x^_l)
  *    with x^ the unit-weight RMSNorm (eps 1e-6) when the layer's flags ask.
@@ -69,6 +74,12 @@ typedef struct {
    * width 4, 3 and 2 (index 4 - width). */
   const uint8_t *expert_bits;
   oq_t gate_up_w[3], down_w[3];
+  /* Two tiers (NULL = every record in device memory): 1 marks a record held
+   * in host memory; with cut_w > 0 such an expert whose weight is below
+   * cut_w in every row of the call is cut (contributes nothing; the other
+   * weights are left as they are). */
+  const uint8_t *expert_tier;
+  double cut_w;
 } oracle_layer_t;
 
 enum { ORACLE_RESIDUAL = 1, ORACLE_PRENORM = 2 };
@@ -366,6 +377,25 @@ int oracle_route(const oracle_layer_t *L, int nb, const double *x, double *logit
 
 /* ------------------------------------------------------------ one layer */
 
+/* The deadline cut of one call: cut[e] = 1 for each routed expert whose
+ * record is in host memory and whose weight is below cut_w in every one of
+ * the nb rows (0 in a row that did not route to it).  cut [E], zeroed by the
+ * caller.  Returns the number cut. */
+int oracle_cut(const oracle_layer_t *L, int nb, const int32_t *idx, const double *w, uint8_t *cut) {
+  const int k = L->top_k;
+  int n = 0;
+  if (!L->expert_tier || !(L->cut_w > 0.0)) return 0;
+  for (int i = 0; i < nb * k; i++) {
+    const int e = idx[i];
+    if (!L->expert_tier[e] || cut[e]) continue;
+    double wmax = 0.0;
+    for (int j = 0; j < nb * k; j++)
+      if (idx[j] == e && w[j] > wmax) wmax = w[j];
+    if (wmax < L->cut_w) cut[e] = 1, n++;
+  }
+  return n;
+}
+
 /* One MoE layer over nb rows.
  *   x      [nb][H]   layer input
  *   out    [nb][H]   layer output (MoE, plus x when the layer is RESIDUAL)
@@ -393,12 +423,15 @@ int oracle_moe_layer(const oracle_layer_t *L, int nb, const double *x, double *o
     oracle_topk_softmax(lg + (int64_t)b * E, E, k, id + b * k, wt + b * k);
   }
   int U = oracle_union(id, nb * k, un);
+  uint8_t *cut = (uint8_t *)calloc((size_t)E, 1);
+  oracle_cut(L, nb, id, wt, cut);
 
   for (int b = 0; b < nb; b++) {
     const double *xb = xn + (int64_t)b * H;
     double *ob = out + (int64_t)b * H;
     for (int i = 0; i < H; i++) ob[i] = 0.0;
     for (int r = 0; r < k; r++) {
+      if (cut[id[b * k + r]]) continue;
       oracle_expert(L, id[b * k + r], xb, y);
       for (int i = 0; i < H; i++) ob[i] += wt[b * k + r] * y[i];
     }
@@ -432,6 +465,7 @@ int oracle_moe_layer(const oracle_layer_t *L, int nb, const double *x, double *o
   free(id);
   free(wt);
   free(y);
+  free(cut);
   return U;
 }
 

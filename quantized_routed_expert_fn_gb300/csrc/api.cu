@@ -86,6 +86,8 @@ int check_layers(const moe_layer *layers, int nl, int nb) {
     if ((L.expert_bits != nullptr) != mixed)
       return fail(MOE_EINVAL, "layer %d: expert_bits must be set on every layer or on none", l);
     if (!mixed && L.bits != bits) return fail(MOE_ESHAPE, "layer %d: bits differ from layer 0", l);
+    if (!(L.cut_weak >= 0.f && L.cut_weak <= 1.f))
+      return fail(MOE_EINVAL, "layer %d: cut_weak %g outside [0, 1]", l, (double)L.cut_weak);
     if (L.group != 64) return fail(MOE_ESHAPE, "layer %d: group %u, only 64 is supported", l, L.group);
     if (L.flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM | MOE_TEST_WITHHOLD))
       return fail(MOE_EINVAL, "layer %d: unknown flags 0x%x", l, L.flags);
@@ -175,6 +177,8 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
     q.flags = L.flags & (MOE_RESIDUAL | MOE_PRENORM);
     if (L.flags & MOE_TEST_WITHHOLD) p.withhold = 1;
     q.ebits = L.expert_bits;
+    q.etier = L.expert_tier;
+    q.cut_w = L.cut_weak;
     if (L.expert_bits)
       for (int i = 0; i < 3; i++) {
         q.guw[i] = {(uint32_t)L.gate_up_w[i].w, (uint32_t)L.gate_up_w[i].s, (uint32_t)L.gate_up_w[i].b};
@@ -299,6 +303,8 @@ int check_prefill(const moe_layer *L, int t) {
   if (E < 1 || E > 1024) return fail(MOE_ESHAPE, "n_experts %u outside 1..1024", E);
   if (K < 1 || K > E || K > 32) return fail(MOE_ESHAPE, "top_k %u outside 1..min(n_experts, 32)", K);
   if (L->expert_bits) return fail(MOE_EINVAL, "mixed record widths (expert_bits) are supported by decode only");
+  if (L->expert_tier || L->cut_weak != 0.f)
+    return fail(MOE_EINVAL, "host-memory records (expert_tier, cut_weak) are supported by decode only");
   if (L->bits != 2 && L->bits != 3 && L->bits != 4) return fail(MOE_ESHAPE, "bits %u not in {2,3,4}", L->bits);
   // the GEMMs stage code rows with 16-byte copies: a 3-bit row (3 * in / 8
   // bytes) is 16-byte aligned when in is a multiple of 128

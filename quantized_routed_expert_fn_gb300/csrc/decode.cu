@@ -569,24 +569,36 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
   __syncwarp();
 }
 
-// The union's slots whose record is resident on this GPU (address != 0; an
-// expert-parallel shard holds only its own experts' records), kept in union
-// order (warp 0).  wm columns move with their slots; *nres = their count.
-__device__ void resident_compact(int *uni, float *wm, const uint64_t *eaddr_s, int U, volatile int *nres) {
+// The union's slots this GPU computes, in union order within each tier:
+// records in device memory first, then records in host memory.  An expert
+// whose record is not on this GPU at all (address 0: an expert-parallel
+// shard holds only its own experts) is left out, and so is a host-memory
+// one whose weight is below cut_w in every row (the deadline cut of weak
+// experts).  wm columns move with their slots; tier_out[j] = 1 for a kept
+// host-memory slot j.  nkeep[0] = slots kept, nkeep[1] = of them in device
+// memory.  (warp 0; et_s may be null: every record in device memory)
+__device__ void place_union(int *uni, float *wm, const uint64_t *eaddr_s, const uint8_t *et_s, float cut_w, int U,
+                            int *tier_out, volatile int *nkeep) {
   const int lane = threadIdx.x & 31;
   int id[2];
-  bool res[2];
+  bool dev[2], hst[2];
   float w[2][4];
 #pragma unroll
   for (int h = 0; h < 2; h++) {
     const int j = lane + 32 * h;
     id[h] = j < U ? uni[j] : 0;
-    res[h] = j < U && eaddr_s[id[h]] != 0ull;
+    float wmax = 0.f;
 #pragma unroll
-    for (int b = 0; b < 4; b++) w[h][b] = wm[b * 64 + j];
+    for (int b = 0; b < 4; b++) w[h][b] = wm[b * 64 + j], wmax = fmaxf(wmax, w[h][b]);
+    const bool here = j < U && eaddr_s[id[h]] != 0ull;
+    const bool host = et_s != nullptr && et_s[id[h]] != 0;
+    dev[h] = here && !host;
+    hst[h] = here && host && !(wmax < cut_w);
   }
-  const uint32_t b0 = __ballot_sync(FULL, res[0]), b1 = __ballot_sync(FULL, res[1]);
+  const uint32_t bd0 = __ballot_sync(FULL, dev[0]), bd1 = __ballot_sync(FULL, dev[1]);
+  const uint32_t bh0 = __ballot_sync(FULL, hst[0]), bh1 = __ballot_sync(FULL, hst[1]);
   const uint32_t lt = (1u << lane) - 1u;
+  const int nd = __popc(bd0) + __popc(bd1);
   __syncwarp();
 #pragma unroll
   for (int h = 0; h < 2; h++)
@@ -595,14 +607,16 @@ __device__ void resident_compact(int *uni, float *wm, const uint64_t *eaddr_s, i
   __syncwarp();
 #pragma unroll
   for (int h = 0; h < 2; h++) {
-    if (res[h]) {
-      const int pos = h == 0 ? __popc(b0 & lt) : __popc(b0) + __popc(b1 & lt);
+    if (dev[h] || hst[h]) {
+      const int pos = dev[h] ? (h == 0 ? __popc(bd0 & lt) : __popc(bd0) + __popc(bd1 & lt))
+                             : nd + (h == 0 ? __popc(bh0 & lt) : __popc(bh0) + __popc(bh1 & lt));
       uni[pos] = id[h];
+      tier_out[pos] = hst[h] ? 1 : 0;
 #pragma unroll
       for (int b = 0; b < 4; b++) wm[b * 64 + pos] = w[h][b];
     }
   }
-  if (lane == 0) *nres = __popc(b0) + __popc(b1);
+  if (lane == 0) nkeep[0] = nd + __popc(bh0) + __popc(bh1), nkeep[1] = nd;
   __syncwarp();
 }
 
@@ -688,12 +702,14 @@ struct UnitDesc {
   const uint8_t *rec;
   QOff q;
   int bits;
+  int host;  // the record is in host memory: its tile is read by the computing group, not bulk-copied
 };
 
-// BITS = 0: a union mixing widths; slot j's width is sbits[j].
+// BITS = 0: a union mixing widths; slot j's width is sbits[j].  stier[j]:
+// slot j's record is in host memory.
 template <int BITS>
 __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP &L,
-                                             const uint8_t *const *rect, const int *sbits) {
+                                             const uint8_t *const *rect, const int *sbits, const int *stier) {
   UnitDesc d;
   const int c = blockIdx.x, G = gridDim.x;
   if (q < s.nGU) {
@@ -705,6 +721,7 @@ __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP
   }
   const bool shared = s.hsi && d.slot == 0;
   d.rec = shared ? L.srec : rect[d.slot];
+  d.host = shared ? 0 : stier[d.slot];
   if (BITS == 0 && !shared) {
     d.bits = sbits[d.slot];
     d.q = d.down ? L.dnw[4 - d.bits] : L.guw[4 - d.bits];
@@ -725,6 +742,10 @@ __device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_
     mbar_expect_tx(bar, 0);  // completes the phase with no bytes
     return;
   }
+  if (d.host) {
+    mbar_expect_tx(bar, 0);  // the computing group reads this tile itself (fill_unit_plain)
+    return;
+  }
   const int inp = d.down ? I : H;
   const uint32_t rb = inp * d.bits / 8, sp = inp / 32;
   const int rows = d.down ? 64 : 32;
@@ -742,6 +763,44 @@ __device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_
     bulk_g2s(sdst + 16 * sp, sc + (size_t)(I + d.row0) * sp, 16 * sp, bar);
     bulk_g2s(sdst + 32 * sp, bi + (size_t)d.row0 * sp, 16 * sp, bar);
     bulk_g2s(sdst + 48 * sp, bi + (size_t)(I + d.row0) * sp, 16 * sp, bar);
+  }
+}
+
+// Unit group (thread gt of GT): the tile of a unit whose record is in host
+// memory, read with 16-byte loads over the C2C link into its stage, in the
+// layout issue_unit's bulk copies give.  (Every segment is a whole number
+// of 16-byte pieces: rows of inp * bits / 8 bytes, inp a multiple of 128;
+// scale and bias rows of inp / 32 bytes, in blocks of 16 or 64 rows.)
+__device__ void fill_unit_plain(const UnitDesc &d, int H, int I, uint8_t *st, int gt) {
+  const int inp = d.down ? I : H;
+  const uint32_t rb = inp * d.bits / 8, sp = inp / 32;
+  const int rows = d.down ? 64 : 32;
+  const uint8_t *c = d.rec + d.q.w, *sc = d.rec + d.q.s, *bi = d.rec + d.q.b;
+  uint8_t *sdst = st + rows * rb;
+  const uint8_t *src[6];
+  uint8_t *dst[6];
+  uint32_t len[6];
+  int ns;
+  if (d.down) {
+    src[0] = c + (size_t)d.row0 * rb, dst[0] = st, len[0] = 64 * rb;
+    src[1] = sc + (size_t)d.row0 * sp, dst[1] = sdst, len[1] = 64 * sp;
+    src[2] = bi + (size_t)d.row0 * sp, dst[2] = sdst + 64 * sp, len[2] = 64 * sp;
+    ns = 3;
+  } else {
+    src[0] = c + (size_t)d.row0 * rb, dst[0] = st, len[0] = 16 * rb;
+    src[1] = c + (size_t)(I + d.row0) * rb, dst[1] = st + 16 * rb, len[1] = 16 * rb;
+    src[2] = sc + (size_t)d.row0 * sp, dst[2] = sdst, len[2] = 16 * sp;
+    src[3] = sc + (size_t)(I + d.row0) * sp, dst[3] = sdst + 16 * sp, len[3] = 16 * sp;
+    src[4] = bi + (size_t)d.row0 * sp, dst[4] = sdst + 32 * sp, len[4] = 16 * sp;
+    src[5] = bi + (size_t)(I + d.row0) * sp, dst[5] = sdst + 48 * sp, len[5] = 16 * sp;
+    ns = 6;
+  }
+  for (int k = 0; k < ns; k++) {
+    const uint4 *s4 = reinterpret_cast<const uint4 *>(src[k]);
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst[k]);
+    const int n = (int)(len[k] >> 4);
+#pragma unroll 4
+    for (int i = gt; i < n; i += GT) d4[i] = __ldcg(s4 + i);
   }
 }
 
@@ -785,7 +844,9 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   unsigned *stg_unit = reinterpret_cast<unsigned *>(eaddr_s + ((E + 1) & ~1));  // [S] last unit issued per stage
   int *posof = reinterpret_cast<int *>(stg_unit + kMaxStages);                   // [E] union scratch, INT_MAX between uses
   int *sbits = posof + E;                                                        // [64] slot -> code width (mixed)
-  uint8_t *eb_s = reinterpret_cast<uint8_t *>(sbits + 64);                       // [E] expert -> code width (mixed)
+  int *stier = sbits + 64;                                                       // [64] slot -> record in host memory
+  uint8_t *eb_s = reinterpret_cast<uint8_t *>(stier + 64);                       // [E] expert -> code width (mixed)
+  uint8_t *et_s = eb_s + ((E + 15) & ~15);                                       // [E] expert -> record in host memory
 
   if (tid == 0) {
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu;
@@ -826,7 +887,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     int issued = 0;
     if (warp == kProducerWarp) {
       for (; issued < s.nA && issued < S; issued++)
-        issue_at(get_unit<BITS>(issued, s, L, rect, sbits), qbase + issued);
+        issue_at(get_unit<BITS>(issued, s, L, rect, sbits, stier), qbase + issued);
     }
     issued = s.nA < S ? s.nA : S;
 
@@ -851,6 +912,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     for (int e = tid; e < E; e += NT) eaddr_s[e] = L.eaddr[e];
     if (BITS == 0)
       for (int e = tid; e < E; e += NT) eb_s[e] = L.ebits[e];
+    if (L.etier)
+      for (int e = tid; e < E; e += NT) et_s[e] = L.etier[e];
     if (l > 0 && !cta_wait(P.cnt + (size_t)(l - 1) * kCntPerLayer + kCntRows, (unsigned)(H / 64), P, sflag)) {
       drain_ring(bars, qbase, qbase + issued, S, P);
       return;
@@ -963,12 +1026,14 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     MOE_STAMP(9)
     if (warp == 0) {
       union_warp(sidx, sw, nb, K, uni, wm, posof, reinterpret_cast<int *>(red), sflag + 1);
-      resident_compact(uni, wm, eaddr_s, sflag[1], sflag + 2);
+      place_union(uni, wm, eaddr_s, L.etier ? et_s : nullptr, L.cut_w, sflag[1], stier + s.hsi, sflag + 2);
+      if (lane == 0 && s.hsi) stier[0] = 0;  // the shared expert's record is in device memory
     }
     __syncthreads();
     MOE_STAMP(10)
     const int Uall = sflag[1];
-    s.U = sflag[2];  // the resident slots: the ones this GPU computes
+    s.U = sflag[2];  // the slots this GPU computes
+    const int Udev = sflag[3];
     if (tid < s.U) {
       rect[tid + s.hsi] = reinterpret_cast<const uint8_t *>(eaddr_s[uni[tid]]);
       if (BITS == 0) {
@@ -983,7 +1048,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       if (P.slot_tab)
         for (int j = tid; j < kSlotStride; j += NT) {
           uint64_t v = j < s.U ? eaddr_s[uni[j]] : 0ull;
-          if (j == kSlotStride - 2) v = (uint64_t)s.U;
+          if (j == kSlotStride - 2) v = (uint64_t)Udev;
           if (j == kSlotStride - 1) v = (uint64_t)Uall;
           P.slot_tab[(size_t)l * kSlotStride + j] = v;
         }
@@ -1009,7 +1074,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     s.nD = rr_count(cta, s.nslots * s.nrt, G);
     const int n = s.n();
     if (warp == kProducerWarp) {
-      for (int q = issued; q < n && q < S; q++) issue_at(get_unit<BITS>(q, s, L, rect, sbits), qbase + q);
+      for (int q = issued; q < n && q < S; q++) issue_at(get_unit<BITS>(q, s, L, rect, sbits, stier), qbase + q);
     }
     issued = n < S ? n : S;
     if (s.nslots == 0) {
@@ -1059,7 +1124,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
             if (rr1 > E && Ln.sgate) prefetch_l2(Ln.sgate, (uint32_t)(H * 2));
           }
         }
-        const UnitDesc d = get_unit<BITS>(q, s, L, rect, sbits);
+        const UnitDesc d = get_unit<BITS>(q, s, L, rect, sbits, stier);
         const unsigned u = qbase + q;
         const uint8_t *st = stages + (size_t)(u % S) * P.stage_bytes;
         const bool shared = s.hsi && d.slot == 0;
@@ -1079,6 +1144,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         if (!grp_and(grp, stage_wait(&bars[u % S], (u / S) & 1u, P))) {
           alive = false;
           break;
+        }
+        if (d.host && d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0) {
+          fill_unit_plain(d, H, I, stages + (size_t)(u % S) * P.stage_bytes, gt);
+          grp_sync(grp);
         }
         if (q == 0) MOE_STAMP(11)
         const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
@@ -1119,7 +1188,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         grp_sync(grp);
         if (q == 0) MOE_STAMP(12)
         // the stage is free: request the unit S places ahead into it
-        if (gw == kProducerWarp && q + S < n) issue_at(get_unit<BITS>(q + S, s, L, rect, sbits), u + S);
+        if (gw == kProducerWarp && q + S < n) issue_at(get_unit<BITS>(q + S, s, L, rect, sbits, stier), u + S);
         if (!d.down) {
           // h = silu(gate) * up for 16 rows x nb, scattered as bf16 hi/lo A
           // fragments in the pair order of this slot's down codec; thread
@@ -1221,7 +1290,7 @@ static int fixed_smem(int H, int E, int I, int nb, int bits) {
   b += ((E + 1) & ~1) * 8;                         // expert addresses
   b += kMaxStages * 4;                             // last unit issued per stage
   b += E * 4;                                      // union scratch
-  b += 64 * 4 + ((E + 15) & ~15);                  // slot widths, expert widths (mixed)
+  b += 2 * 64 * 4 + 2 * ((E + 15) & ~15);          // slot widths and tiers, expert widths and tiers
   return b;
 }
 

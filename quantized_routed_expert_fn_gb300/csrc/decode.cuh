@@ -20,6 +20,8 @@ struct LayerP {
   uint32_t flags;
   const uint8_t *ebits;    // [E] code width of each routed record (kernel instance 0, mixed widths)
   QOff guw[3], dnw[3];     // mixed widths: offsets in a record of width 4, 3, 2 (index 4 - width)
+  const uint8_t *etier;    // [E] 0: record in device memory, 1: in host memory; nullptr: all in device memory
+  float cut_w;             // host-tier experts below this weight in every row are cut (0: none)
 };
 
 // Per-layer counters in the workspace (uint32 each), every counter on a

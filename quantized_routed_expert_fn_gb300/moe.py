@@ -24,7 +24,9 @@ STATUS_NAMES = {0: "MOE_OK", -1: "MOE_EINVAL", -2: "MOE_ESHAPE", -3: "MOE_EALIGN
                 -5: "MOE_ETIMEOUT", -6: "MOE_EDEVICE", -7: "MOE_ENOSPACE"}
 
 EXPORTS = ["moe_route", "moe_forward", "moe_forward_traced", "moe_forward_noalloc", "moe_forward_workspace",
-           "moe_prefill", "moe_prefill_timed", "moe_prefill_workspace", "moe_prefill_group", "moe_last_error"]
+           "moe_prefill", "moe_prefill_timed", "moe_prefill_workspace", "moe_prefill_group", "moe_last_error",
+           "moe_tier_create", "moe_tier_update", "moe_tier_slot", "moe_tier_get_stats", "moe_tier_addresses",
+           "moe_tier_destroy", "moe_tier_last_error"]
 PREFILL_KERNELS = 10
 PREFILL_KERNEL_NAMES = ["prep", "router_gemm", "topk", "group_count", "group_scan", "group_fill", "gather",
                         "gate_up_gemm", "down_gemm", "output"]
@@ -45,7 +47,13 @@ class MoeLayer(ctypes.Structure):
                 ("sh_gate_up", MoeQ), ("sh_down", MoeQ),
                 ("expert_addr", ctypes.c_void_p),
                 ("gate_up", MoeQ), ("down", MoeQ),
-                ("expert_bits", ctypes.c_void_p), ("gate_up_w", MoeQ * 3), ("down_w", MoeQ * 3)]
+                ("expert_bits", ctypes.c_void_p), ("gate_up_w", MoeQ * 3), ("down_w", MoeQ * 3),
+                ("expert_tier", ctypes.c_void_p), ("cut_weak", ctypes.c_float)]
+
+
+class TierStats(ctypes.Structure):
+    _fields_ = [("resident", ctypes.c_int), ("last_host_reads", ctypes.c_int), ("last_promoted", ctypes.c_int),
+                ("promotions", ctypes.c_longlong), ("evictions", ctypes.c_longlong)]
 
 
 class MoeError(RuntimeError):
@@ -85,6 +93,19 @@ def lib(path: str | None = None) -> ctypes.CDLL:
         L.moe_prefill_timed.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, sz, vp, vp, vp, vp]
         L.moe_prefill_group.restype = i32
         L.moe_prefill_group.argtypes = [ctypes.POINTER(MoeLayer), vp, i32, vp, vp, vp, vp, vp, vp, sz, vp, vp]
+        L.moe_tier_create.restype = i32
+        L.moe_tier_create.argtypes = [i32, i32, sz, vp, vp, i32, vp, vp, vp, ctypes.POINTER(vp)]
+        L.moe_tier_update.restype = i32
+        L.moe_tier_update.argtypes = [vp, vp, i32, vp]
+        L.moe_tier_slot.restype = i32
+        L.moe_tier_slot.argtypes = [vp, i32, i32]
+        L.moe_tier_get_stats.restype = i32
+        L.moe_tier_get_stats.argtypes = [vp, ctypes.POINTER(TierStats)]
+        L.moe_tier_addresses.restype = ctypes.POINTER(ctypes.c_uint64)
+        L.moe_tier_addresses.argtypes = [vp]
+        L.moe_tier_destroy.restype = None
+        L.moe_tier_destroy.argtypes = [vp]
+        L.moe_tier_last_error.restype = ctypes.c_char_p
         _lib = L
     return _lib
 
@@ -154,6 +175,16 @@ class DeviceLayers:
         self.c = arr
         self.n = len(layers)
         self.src = layers
+
+    def set_tier(self, layer: int, expert_addr: torch.Tensor, expert_tier: torch.Tensor | None,
+                 cut_weak: float = 0.0) -> None:
+        """Point layer `layer` at other record addresses (device or host
+        memory) with their tiers (uint8 [E], 1 = host memory), and set its cut."""
+        self.keep += [expert_addr, expert_tier]
+        c = self.c[layer]
+        c.expert_addr = expert_addr.data_ptr()
+        c.expert_tier = None if expert_tier is None else expert_tier.data_ptr()
+        c.cut_weak = cut_weak
 
     def set_flags(self, flags: int) -> None:
         for i in range(self.n):
@@ -245,3 +276,57 @@ def prefill_timed(layers: DeviceLayers, x: torch.Tensor, out: torch.Tensor, work
     wp, wb = _aligned(work)
     _check(lib().moe_prefill_timed(_layer_ptr(layers, layer), _p(x), x.shape[0], _p(out), wp, wb, _p(topk_idx),
                                    _p(status), arr, _stream(stream)))
+
+
+class Tier:
+    """The two-tier expert store (moe_tier_*): records in pinned host memory,
+    the most recently used ones cached in device slots.
+
+    host_records: address (int) or pinned uint8 tensor [n_layers][n_experts][stride];
+    slots: device uint8 tensor [n_slots][stride] or None; expert_addr /
+    expert_tier: device int64 / uint8 tensors [n_layers][n_experts], or None
+    for a policy-only store (no CUDA call)."""
+
+    def __init__(self, n_layers, n_experts, stride, host_records, n_slots, slots=None, expert_addr=None,
+                 expert_tier=None, stream=None):
+        self.n_layers, self.n_experts, self.stride = n_layers, n_experts, stride
+        self._keep = [host_records, slots, expert_addr, expert_tier]
+        h = host_records if isinstance(host_records, int) else host_records.data_ptr()
+        self.dry = expert_addr is None
+        t = ctypes.c_void_p()
+        code = lib().moe_tier_create(n_layers, n_experts, stride, h, _p(slots), n_slots, _p(expert_addr),
+                                     _p(expert_tier), None if self.dry else _stream(stream), ctypes.byref(t))
+        if code != OK:
+            raise MoeError(code, lib().moe_tier_last_error().decode())
+        self.t = t
+
+    def update(self, slot_tab, stream=None) -> int:
+        """slot_tab: host uint64 array [n_layers][64] of the step just run."""
+        st = np.ascontiguousarray(slot_tab, dtype=np.uint64)
+        r = lib().moe_tier_update(self.t, st.ctypes.data, st.shape[0], None if self.dry else _stream(stream))
+        if r < 0:
+            raise MoeError(r, lib().moe_tier_last_error().decode())
+        return r
+
+    def slot(self, layer: int, expert: int) -> int:
+        return int(lib().moe_tier_slot(self.t, layer, expert))
+
+    def stats(self) -> dict:
+        s = TierStats()
+        _check(lib().moe_tier_get_stats(self.t, ctypes.byref(s)))
+        return {f: getattr(s, f) for f, _ in TierStats._fields_}
+
+    def addresses(self) -> np.ndarray:
+        p = lib().moe_tier_addresses(self.t)
+        return np.ctypeslib.as_array(p, shape=(self.n_layers, self.n_experts)).copy()
+
+    def close(self) -> None:
+        if self.t:
+            lib().moe_tier_destroy(self.t)
+            self.t = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -69,7 +69,7 @@ def test_workspace_size(m):
 @pytest.mark.parametrize("over,code", [
     (dict(hidden=300), -2), (dict(inter=200), -2), (dict(group=32), -2), (dict(bits=5), -2),
     (dict(top_k=0), -2), (dict(flags=0x80), -1), (dict(router=0), -1), (dict(router=0x10008), -3),
-    (dict(shared_gate=0), -1),
+    (dict(shared_gate=0), -1), (dict(cut_weak=1.5), -1), (dict(cut_weak=-0.1), -1),
 ])
 def test_forward_rejects_bad_layers(m, over, code):
     L = _layer()
@@ -170,3 +170,11 @@ def test_mixed_width_layers_host_checks(m):
     arr[0].gate_up = m.MoeQ(1, 1, 1, 1, 1)
     assert m.lib().moe_forward_workspace(arr, 1, 1) > 0, m.last_error()
     assert m.lib().moe_prefill_workspace(_mixed_struct(m, L), 16) == 0
+
+
+def test_prefill_rejects_host_memory_records(m):
+    """Tiers and the cut are decode features: prefill refuses a layer that uses them."""
+    L = _layer()
+    assert m.lib().moe_prefill_workspace(_struct(m, L, expert_tier=0x60000), 16) == 0
+    assert m.lib().moe_prefill_workspace(_struct(m, L, cut_weak=0.1), 16) == 0
+    assert m.lib().moe_prefill_workspace(_struct(m, L), 16) > 0

@@ -287,6 +287,87 @@ def test_mixed_width_reads_each_record_at_its_own_width():
             assert not np.allclose(y, _np_expert(layer.records[e], layer.layouts[4], 4, x), rtol=1e-3)
 
 
+# ------------------------------------------------------------------ tiers and the deadline cut
+
+def _tiered(layer, tier, cut_w):
+    import copy
+    L = copy.copy(layer)
+    L.expert_tier = np.ascontiguousarray(tier, dtype=np.uint8)
+    L.cut_w = cut_w
+    return L
+
+
+def test_cut_rule_hand_example():
+    """Two rows, top-2 of 6 experts.  Expert 3 (host memory) has weights 0.3
+    and 0.05: kept, being above w = 0.2 in one row.  Expert 4 (host) has
+    0.1 and 0.15: cut.  Expert 1 (device memory) has 0.05: never cut."""
+    rng = np.random.default_rng(40)
+    layer = synth.make_layer(rng, 128, 6, 2, 64, 4, shared=False)
+    tier = np.array([0, 0, 1, 1, 1, 0], dtype=np.uint8)
+    ol = oracle.Layer(_tiered(layer, tier, 0.2))
+    idx = np.array([[3, 4], [1, 4]], dtype=np.int32)
+    w = np.array([[0.3, 0.1], [0.05, 0.15]])
+    assert oracle.cut(ol, idx, w).tolist() == [False, False, False, False, True, False]
+    idx = np.array([[3, 1], [4, 1]], dtype=np.int32)
+    w = np.array([[0.05, 0.95], [0.05, 0.95]])
+    assert oracle.cut(ol, idx, w).tolist() == [False, False, False, True, True, False]
+    assert not oracle.cut(oracle.Layer(_tiered(layer, tier, 0.0)), idx, w).any()
+
+
+def test_cut_zero_threshold_changes_nothing():
+    rng = np.random.default_rng(41)
+    layer = synth.make_layer(rng, 128, 16, 4, 64, 4, shared=True, flags=synth.RESIDUAL | synth.PRENORM)
+    x = rng.normal(size=(4, 128))
+    base = oracle.moe_layer(oracle.Layer(layer), x)
+    tiered = oracle.moe_layer(oracle.Layer(_tiered(layer, np.arange(16) % 2, 0.0)), x)
+    assert np.array_equal(base["out"], tiered["out"])
+
+
+def test_cut_of_every_host_expert_equals_zeroed_records():
+    """With w above every possible weight, every host-memory expert is cut:
+    the same as those experts' records being all zero (weight 0 everywhere,
+    output 0), the routing unchanged."""
+    rng = np.random.default_rng(42)
+    layer = synth.make_layer(rng, 128, 16, 4, 64, 4, shared=True, flags=synth.PRENORM)
+    tier = (np.arange(16) % 3 == 0).astype(np.uint8)
+    x = rng.normal(size=(3, 128))
+    cut = oracle.moe_layer(oracle.Layer(_tiered(layer, tier, 1.0)), x)
+    import copy
+    z = copy.copy(layer)
+    z.records = layer.records.copy()
+    z.records[tier == 1] = 0
+    ref = oracle.moe_layer(oracle.Layer(z), x)
+    assert np.array_equal(cut["idx"], ref["idx"])
+    assert np.allclose(cut["out"], ref["out"], rtol=0, atol=1e-13)
+
+
+def test_cut_dense_bruteforce():
+    """Threshold in the middle of the routed weights: every expert densely,
+    each host-memory expert dropped when its max weight over the rows is
+    below w, others weighted as usual."""
+    H, E, k, I, nb = 128, 16, 4, 64, 4
+    rng = np.random.default_rng(43)
+    layer = synth.make_layer(rng, H, E, k, I, 4, shared=True)
+    tier = (rng.random(E) < 0.5).astype(np.uint8)
+    x = rng.normal(size=(nb, H))
+    R = synth.bf16_bits_to_f32(layer.router).astype(np.float64)
+    W = np.zeros((nb, E))
+    for b in range(nb):
+        logits = R @ x[b]
+        top = np.argsort(-logits, kind="stable")[:k]
+        p = scipy.special.softmax(logits[top])
+        W[b, top] = p
+    w_cut = float(np.median(W[W > 0]))
+    r = oracle.moe_layer(oracle.Layer(_tiered(layer, tier, w_cut)), x)
+    dropped = (tier == 1) & (W.max(axis=0) > 0) & (W.max(axis=0) < w_cut)
+    assert dropped.any() and ((tier == 1) & (W.max(axis=0) >= w_cut)).any()
+    sg = synth.bf16_bits_to_f32(layer.shared_gate).astype(np.float64)
+    for b in range(nb):
+        dense = sum(W[b, e] * _np_expert(layer.records[e], layer.layout, 4, x[b]) for e in range(E) if not dropped[e])
+        dense = dense + scipy.special.expit(sg @ x[b]) * _np_expert(layer.shared_record, layer.shared_layout, 4, x[b])
+        assert np.allclose(r["out"][b], dense, rtol=1e-9, atol=1e-12)
+
+
 def test_batch_rows_are_independent():
     rng = np.random.default_rng(20)
     layer = oracle.Layer(synth.make_layer(rng, 128, 8, 2, 64, 4))
