@@ -90,11 +90,19 @@ typedef struct {
   const uint8_t *expert_tier; /* device array [n_experts]: 0 device memory, 1 host memory; NULL: all device */
   float cut_weak;             /* host-memory experts whose routing weight is below this in every row of
                                  the call are cut (contribute nothing); 0 = no cut */
+  uint32_t *lookahead_idx;    /* device [nb][top_k] or NULL: with MOE_LOOKAHEAD, this layer's experts as
+                                 predicted during the previous layer (the lookahead_hit source);
+                                 0xffffffff where no prediction was made (first layer of a call) */
 } moe_layer;
 
 enum {
   MOE_RESIDUAL = 1, /* out = x + MoE(x^) */
   MOE_PRENORM = 2,  /* x^ = x / sqrt(mean(x^2) + 1e-6) feeds router, gate and experts */
+  MOE_LOOKAHEAD = 4, /* decode: while the previous layer of the same call runs, predict this
+                        layer's experts from this layer's router applied to the previous
+                        layer's input, and prefetch their device-memory records into L2
+                        (`lookahead_layer`, struct Gpu page: a one-layer lookahead router);
+                        a hint only, results do not change */
   MOE_TEST_WITHHOLD = 0x100 /* failure-detection test only: decode never releases the
                                router's completion, prefill never completes one pipeline
                                stage of its gate_up GEMM; the bounded waits must give up
@@ -175,7 +183,7 @@ int moe_forward_traced(const moe_layer *layers, int n_layers, const float *x, in
  * MOE_NOALLOC_MAX_WORKSPACE bytes on each GPU that loads it.
  *   - Layers whose moe_forward_workspace exceeds that size are rejected with
  *     MOE_ENOSPACE before anything runs (48 layers of hidden 2048, 128 experts,
- *     inter 768 need about 2.3 MiB at nb 1; the same stack at nb 4 needs 4.9
+ *     inter 768 need about 2.4 MiB at nb 1; the same stack at nb 4 needs 5.0
  *     MiB and is rejected).
  *   - The first call in each CUDA context looks the array's address up once
  *     (cudaGetSymbolAddress with that context current) and keeps it for that

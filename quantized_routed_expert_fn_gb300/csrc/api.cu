@@ -37,7 +37,7 @@ int fail(int code, const char *fmt, ...) {
 size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 struct WsLayout {
-  size_t cnt, lgw, xbuf, hfrag, ypart, total;
+  size_t cnt, lgw, lgp, xbuf, hfrag, ypart, total;
 };
 
 WsLayout ws_layout(int H, int I, int nl, int nb) {
@@ -47,6 +47,8 @@ WsLayout ws_layout(int H, int I, int nl, int nb) {
   off += align256((size_t)nl * moe::kCntPerLayer * 4);
   w.lgw = off;
   off += align256((size_t)2 * moe::kMaxGrid * moe::kLogitWords * 8);
+  w.lgp = off;
+  off += align256((size_t)2 * moe::kMaxGrid * moe::kLogitWords * 8);
   w.xbuf = off;
   off += align256((size_t)nl * nb * H * 4);
   w.hfrag = off;
@@ -55,6 +57,20 @@ WsLayout ws_layout(int H, int I, int nl, int nb) {
   off += align256((size_t)64 * nb * H * 4);
   w.total = off;
   return w;
+}
+
+// Bytes from a record's base to the end of its last tensor (codes, scales
+// and biases of gate_up and down at width `bits`).
+uint32_t record_span(const moe_q &gu, const moe_q &dn, int I, int H, int bits) {
+  const uint64_t gc = (uint64_t)2 * I * H * bits / 8, gs = (uint64_t)2 * I * (H / 64) * 2;
+  const uint64_t dc = (uint64_t)H * I * bits / 8, ds = (uint64_t)H * (I / 64) * 2;
+  uint64_t e = gu.w + gc;
+  e = e > gu.s + gs ? e : gu.s + gs;
+  e = e > gu.b + gs ? e : gu.b + gs;
+  e = e > dn.w + dc ? e : dn.w + dc;
+  e = e > dn.s + ds ? e : dn.s + ds;
+  e = e > dn.b + ds ? e : dn.b + ds;
+  return (uint32_t)((e + 15) & ~(uint64_t)15);
 }
 
 int check_q(const moe_q &q, uint32_t out, uint32_t inp, const char *what, int l) {
@@ -89,7 +105,7 @@ int check_layers(const moe_layer *layers, int nl, int nb) {
     if (!(L.cut_weak >= 0.f && L.cut_weak <= 1.f))
       return fail(MOE_EINVAL, "layer %d: cut_weak %g outside [0, 1]", l, (double)L.cut_weak);
     if (L.group != 64) return fail(MOE_ESHAPE, "layer %d: group %u, only 64 is supported", l, L.group);
-    if (L.flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM | MOE_TEST_WITHHOLD))
+    if (L.flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM | MOE_LOOKAHEAD | MOE_TEST_WITHHOLD))
       return fail(MOE_EINVAL, "layer %d: unknown flags 0x%x", l, L.flags);
     if (!L.router || !L.expert_addr) return fail(MOE_EINVAL, "layer %d: router / expert_addr NULL", l);
     if ((uintptr_t)L.router & 15u) return fail(MOE_EALIGN, "layer %d: router not 16-byte aligned", l);
@@ -158,6 +174,7 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   char *base = (char *)work;
   p.cnt = (unsigned *)(base + w.cnt);
   p.lgw = (unsigned long long *)(base + w.lgw);
+  p.lgp = (unsigned long long *)(base + w.lgp);
   p.xbuf = (float *)(base + w.xbuf);
   p.hfrag = (uint16_t *)(base + w.hfrag);
   p.ypart = (float *)(base + w.ypart);
@@ -174,11 +191,15 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
     q.dn = {(uint32_t)L.down.w, (uint32_t)L.down.s, (uint32_t)L.down.b};
     q.sgu = {(uint32_t)L.sh_gate_up.w, (uint32_t)L.sh_gate_up.s, (uint32_t)L.sh_gate_up.b};
     q.sdn = {(uint32_t)L.sh_down.w, (uint32_t)L.sh_down.s, (uint32_t)L.sh_down.b};
-    q.flags = L.flags & (MOE_RESIDUAL | MOE_PRENORM);
+    q.flags = L.flags & (MOE_RESIDUAL | MOE_PRENORM | MOE_LOOKAHEAD);
     if (L.flags & MOE_TEST_WITHHOLD) p.withhold = 1;
+    if ((L.flags & MOE_LOOKAHEAD) && l > 0) p.lookahead = 1;
     q.ebits = L.expert_bits;
     q.etier = L.expert_tier;
     q.cut_w = L.cut_weak;
+    q.la_idx = L.lookahead_idx;
+    q.span = record_span(L.gate_up, L.down, I, H, L.bits);
+    for (int i = 0; i < 3; i++) q.span_w[i] = record_span(L.gate_up_w[i], L.down_w[i], I, H, 4 - i);
     if (L.expert_bits)
       for (int i = 0; i < 3; i++) {
         q.guw[i] = {(uint32_t)L.gate_up_w[i].w, (uint32_t)L.gate_up_w[i].s, (uint32_t)L.gate_up_w[i].b};
@@ -311,7 +332,7 @@ int check_prefill(const moe_layer *L, int t) {
   if (L->bits == 3 && I % 128)
     return fail(MOE_ESHAPE, "3-bit prefill needs inter %% 128 == 0 (16-byte code rows); inter %u", I);
   if (L->group != 64) return fail(MOE_ESHAPE, "group %u, only 64 is supported", L->group);
-  if (L->flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM | MOE_TEST_WITHHOLD))
+  if (L->flags & ~(uint32_t)(MOE_RESIDUAL | MOE_PRENORM | MOE_LOOKAHEAD | MOE_TEST_WITHHOLD))
     return fail(MOE_EINVAL, "unknown flags 0x%x", L->flags);
   if (!L->router || !L->expert_addr) return fail(MOE_EINVAL, "router / expert_addr NULL");
   if ((uintptr_t)L->router & 15u) return fail(MOE_EALIGN, "router not 16-byte aligned");

@@ -56,7 +56,7 @@ constexpr int GW = GT / 32;       // warps of a group
 // contiguously: one bulk copy per block of rows).
 __host__ __device__ constexpr int code_pitch(int rb, int) { return rb; }
 constexpr unsigned FULL = 0xffffffffu;
-constexpr uint32_t kResidual = 1, kPrenorm = 2;
+constexpr uint32_t kResidual = 1, kPrenorm = 2, kLookahead = 4;
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -577,7 +577,7 @@ __device__ void union_warp(const int *sidx, const float *sw, int nb, int K, int 
 // experts).  wm columns move with their slots; tier_out[j] = 1 for a kept
 // host-memory slot j.  nkeep[0] = slots kept, nkeep[1] = of them in device
 // memory.  (warp 0; et_s may be null: every record in device memory)
-__device__ void place_union(int *uni, float *wm, const uint64_t *eaddr_s, const uint8_t *et_s, float cut_w, int U,
+__device__ __forceinline__ void place_union(int *uni, float *wm, const uint64_t *eaddr_s, const uint8_t *et_s, float cut_w, int U,
                             int *tier_out, volatile int *nkeep) {
   const int lane = threadIdx.x & 31;
   int id[2];
@@ -620,18 +620,16 @@ __device__ void place_union(int *uni, float *wm, const uint64_t *eaddr_s, const 
   __syncwarp();
 }
 
-// Every CTA's logits of layer l into lg[b][e].  Word (c, j) of writer CTA c
-// holds logit row rr0(c) + j / nb of activation row j % nb, tagged with
-// l + 1, in the half of the buffer for l's parity.  The half cannot be
-// rewritten under a reader: layer l + 2's rows are written only after layer
-// l + 1 has finished, which needs every CTA's layer l + 1 router rows, which
-// each CTA writes after it has read layer l's logits.  A tag other than
-// l + 1 is waited out (and a wait that runs out reports a timeout).
-// Batches of four words: every load of a batch first, then the tags.  (Out
-// of line: its temporaries stay out of the unit loop's registers.)
-__device__ __noinline__ bool read_logits(const FwdParams &P, int l, int Rl, int E1, float *lg) {
-  const unsigned tag = (unsigned)l + 1u;
-  const unsigned long long *buf = P.lgw + (size_t)(l & 1) * kMaxGrid * kLogitWords;
+// Every CTA's published logits into lg[b][e]: word (c, j) of writer CTA c
+// in buf holds logit row rr0(c) + j / nb (rows split over the CTAs as
+// fdiv_mul(c, Rl, G)) of activation row j % nb, tagged `tag`.  A word with
+// another tag is waited out; a wait that runs out reports a timeout, or with
+// `hint` (the lookahead prediction) only makes the call return false after
+// kHintWaitNs.  Batches of four words: every load of a batch first, then the
+// tags.  (Out of line: its temporaries stay out of the unit loop's registers.)
+constexpr uint64_t kHintWaitNs = 20000;
+__device__ __noinline__ bool read_tagged(const FwdParams &P, const unsigned long long *buf, unsigned tag, int Rl,
+                                         int E1, float *lg, bool hint) {
   const int tid = threadIdx.x, G = gridDim.x, nb = P.nb;
   bool ok = true;
   const int per = ((Rl + G - 1) / G) * nb, total = G * per;
@@ -664,8 +662,8 @@ __device__ __noinline__ bool read_logits(const FwdParams &P, int l, int Rl, int 
               ok = false;
               break;
             }
-            if (globaltimer() - t0w > P.timeout_ns) {
-              atomicCAS(P.status, 0, kStatusTimeout);
+            if (globaltimer() - t0w > (hint ? kHintWaitNs : P.timeout_ns)) {
+              if (!hint) atomicCAS(P.status, 0, kStatusTimeout);
               ok = false;
               break;
             }
@@ -676,6 +674,17 @@ __device__ __noinline__ bool read_logits(const FwdParams &P, int l, int Rl, int 
     }
   }
   return ok;
+}
+
+
+// Layer l's logits: tag l + 1, in the half of the buffer for l's parity.
+// The half cannot be rewritten under a reader: layer l + 2's rows are
+// written only after layer l + 1 has finished, which needs every CTA's layer
+// l + 1 router rows, which each CTA writes after it has read layer l's.
+// (The lookahead's logits for layer l + 1, tag l + 2, use a buffer of their
+// own on the same parity rule.)
+__device__ __noinline__ bool read_logits(const FwdParams &P, int l, int Rl, int E1, float *lg) {
+  return read_tagged(P, P.lgw + (size_t)(l & 1) * kMaxGrid * kLogitWords, (unsigned)l + 1u, Rl, E1, lg, false);
 }
 
 // ------------------------------------------------------------ unit schedule
@@ -766,47 +775,148 @@ __device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_
   }
 }
 
-// Unit group (thread gt of GT): the tile of a unit whose record is in host
-// memory, read with 16-byte loads over the C2C link into its stage, in the
-// layout issue_unit's bulk copies give.  (Every segment is a whole number
-// of 16-byte pieces: rows of inp * bits / 8 bytes, inp a multiple of 128;
-// scale and bias rows of inp / 32 bytes, in blocks of 16 or 64 rows.)
-__device__ void fill_unit_plain(const UnitDesc &d, int H, int I, uint8_t *st, int gt) {
-  const int inp = d.down ? I : H;
-  const uint32_t rb = inp * d.bits / 8, sp = inp / 32;
-  const int rows = d.down ? 64 : 32;
-  const uint8_t *c = d.rec + d.q.w, *sc = d.rec + d.q.s, *bi = d.rec + d.q.b;
-  uint8_t *sdst = st + rows * rb;
-  const uint8_t *src[6];
-  uint8_t *dst[6];
-  uint32_t len[6];
-  int ns;
-  if (d.down) {
-    src[0] = c + (size_t)d.row0 * rb, dst[0] = st, len[0] = 64 * rb;
-    src[1] = sc + (size_t)d.row0 * sp, dst[1] = sdst, len[1] = 64 * sp;
-    src[2] = bi + (size_t)d.row0 * sp, dst[2] = sdst + 64 * sp, len[2] = 64 * sp;
-    ns = 3;
-  } else {
-    src[0] = c + (size_t)d.row0 * rb, dst[0] = st, len[0] = 16 * rb;
-    src[1] = c + (size_t)(I + d.row0) * rb, dst[1] = st + 16 * rb, len[1] = 16 * rb;
-    src[2] = sc + (size_t)d.row0 * sp, dst[2] = sdst, len[2] = 16 * sp;
-    src[3] = sc + (size_t)(I + d.row0) * sp, dst[3] = sdst + 16 * sp, len[3] = 16 * sp;
-    src[4] = bi + (size_t)d.row0 * sp, dst[4] = sdst + 32 * sp, len[4] = 16 * sp;
-    src[5] = bi + (size_t)(I + d.row0) * sp, dst[5] = sdst + 48 * sp, len[5] = 16 * sp;
-    ns = 6;
+// Top-k and softmax of row b by warp b (b < nb), from lg[b][E1 stride].
+__device__ __forceinline__ void topk_rows(const float *lg, int E1, int E, int K, int nb, int *sidx, float *sw) {
+  const int warp = threadIdx.x >> 5;
+  if (warp >= nb) return;
+  if (E <= 128)
+    topk_warp<4>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+  else if (E <= 256)
+    topk_warp<8>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+  else if (E <= 512)
+    topk_warp<16>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+  else
+    topk_warp<32>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
+}
+
+// Lookahead, step 1 (every thread of the CTA): this CTA's rows of layer
+// l + 1's router on layer l's staged input xf, published to the lookahead
+// buffer with tag l + 2.  red: scratch of at least 256 floats.
+__device__ __noinline__ void lookahead_rows(const FwdParams &P, int l, const float *xf, float *red) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, cta = blockIdx.x, H = P.H, E = P.E, nb = P.nb, nch = H / 256;
+  const LayerP &Ln = P.L[l + 1];
+  const int q0 = fdiv_mul(cta, E, G), q1 = fdiv_mul(cta + 1, E, G);
+  const int nq = (q1 - q0) * nch;
+  __syncthreads();  // red is free again (the caller's sums are published)
+  uint4 pv[4];
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    const int it = warp + k * NW;
+    if (it < nq) pv[k] = ldg_stream4(Ln.router + (size_t)(q0 + it / nch) * H + (it % nch) * 256 + lane * 8);
   }
-  for (int k = 0; k < ns; k++) {
-    const uint4 *s4 = reinterpret_cast<const uint4 *>(src[k]);
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst[k]);
-    const int n = (int)(len[k] >> 4);
-#pragma unroll 4
-    for (int i = gt; i < n; i += GT) d4[i] = __ldcg(s4 + i);
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    const int it = warp + k * NW;
+    if (it < nq) {
+      const int ch = it % nch;
+      const float wf[8] = {bf16lo(pv[k].x), bf16hi(pv[k].x), bf16lo(pv[k].y), bf16hi(pv[k].y),
+                           bf16lo(pv[k].z), bf16hi(pv[k].z), bf16lo(pv[k].w), bf16hi(pv[k].w)};
+      for (int b = 0; b < nb; b++) {
+        const float4 *xp = reinterpret_cast<const float4 *>(xf + b * H + ch * 256 + lane * 8);
+        const float4 x0 = xp[0], x1 = xp[1];
+        float acc = wf[0] * x0.x + wf[1] * x0.y + wf[2] * x0.z + wf[3] * x0.w + wf[4] * x1.x + wf[5] * x1.y +
+                    wf[6] * x1.z + wf[7] * x1.w;
+        acc = warp_sum(acc);
+        if (lane == 0) red[it * 4 + b] = acc;
+      }
+    }
   }
+  __syncthreads();
+  for (int j = tid; j < (q1 - q0) * nb; j += NT) {
+    const int r = j / nb, b = j % nb;
+    float sum = 0.f;
+    for (int ch = 0; ch < nch; ch++) sum += red[(r * nch + ch) * 4 + b];
+    st_relaxed_u64(P.lgp + ((size_t)((l + 1) & 1) * kMaxGrid + cta) * kLogitWords + j,
+                   ((unsigned long long)(l + 2) << 32) | __float_as_uint(sum));
+  }
+}
+
+// Lookahead, step 2 (warp 0): the predicted experts' records (device memory
+// on this GPU only) laid end to end; this CTA prefetches its 1/G share of
+// those bytes into L2.  Lane j takes predicted experts j and j + 32.
+__device__ __noinline__ void lookahead_prefetch(const LayerP &Ln, const int *puni, int Up) {
+  const int lane = threadIdx.x & 31, G = gridDim.x, cta = blockIdx.x;
+  uint64_t spn[2] = {0, 0};
+  const uint8_t *base[2] = {nullptr, nullptr};
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    const int j = lane + 32 * h;
+    if (j < Up) {
+      const int e = puni[j];
+      const uint64_t a = Ln.eaddr[e];
+      const int t = Ln.etier ? Ln.etier[e] : 0;
+      const int b = Ln.ebits ? Ln.ebits[e] : 4;
+      if (a != 0 && t == 0 && b >= 2 && b <= 4) {
+        spn[h] = Ln.ebits ? Ln.span_w[4 - b] : Ln.span;
+        base[h] = reinterpret_cast<const uint8_t *>(a);
+      }
+    }
+  }
+  uint64_t inc[2] = {spn[0], spn[1]};
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+#pragma unroll
+    for (int h = 0; h < 2; h++) {
+      const uint64_t v = __shfl_up_sync(FULL, inc[h], o);
+      if (lane >= o) inc[h] += v;
+    }
+  }
+  const uint64_t tot0 = __shfl_sync(FULL, inc[0], 31), tot = tot0 + __shfl_sync(FULL, inc[1], 31);
+  const uint64_t lo = (tot * (uint64_t)cta / G) & ~255ull;
+  const uint64_t hi = cta + 1 == G ? tot : (tot * (uint64_t)(cta + 1) / G) & ~255ull;
+#pragma unroll
+  for (int h = 0; h < 2; h++) {
+    const uint64_t st = (h == 0 ? 0 : tot0) + inc[h] - spn[h];
+    const uint64_t a = st > lo ? st : lo, z = st + spn[h] < hi ? st + spn[h] : hi;
+    for (uint64_t o = a; o < z; o += 65536) {
+      const uint64_t n = z - o < 65536 ? z - o : 65536;
+      prefetch_l2(base[h] + (o - st), (uint32_t)n);
+    }
+  }
+}
+
+// Lookahead, step 2 (every thread of the CTA, once its units are done):
+// the predicted logits into lg, top-k per row, their union, the predicted
+// ids to the next layer's lookahead output (CTA 0), and this CTA's share of
+// the prefetch.  red (free again by now) holds the union and its scratch.
+__device__ __noinline__ void lookahead_step(const FwdParams &P, int l, float *lg, int E1, int *sidx, float *sw,
+                                            int *posof, float *red) {
+  const int tid = threadIdx.x, warp = tid >> 5, nb = P.nb, K = P.K, E = P.E;
+  const LayerP &Ln = P.L[l + 1];
+  int *puni = reinterpret_cast<int *>(red + 1024);
+  volatile int *pnu = puni + 64;
+  float *pwm = red + 2048;
+  const bool got = __syncthreads_and(
+      read_tagged(P, P.lgp + (size_t)((l + 1) & 1) * kMaxGrid * kLogitWords, (unsigned)l + 2u, E, E1, lg, true));
+  if (got) {
+    topk_rows(lg, E1, E, K, nb, sidx, sw);
+    __syncthreads();
+    if (warp == 0) union_warp(sidx, sw, nb, K, puni, pwm, posof, reinterpret_cast<int *>(red), pnu);
+    __syncthreads();
+    if (blockIdx.x == 0 && Ln.la_idx)
+      for (int j = tid; j < nb * K; j += NT) Ln.la_idx[j] = (uint32_t)sidx[(j / K) * 32 + j % K];
+    if (warp == 0) lookahead_prefetch(Ln, puni, *pnu);
+  } else if (blockIdx.x == 0 && Ln.la_idx) {
+    for (int j = tid; j < nb * K; j += NT) Ln.la_idx[j] = 0xffffffffu;
+  }
+  __syncthreads();  // lg, sidx, sw, red are the next layer's again
+}
+
+// Whether layer l predicts layer l + 1 (its flag; a call that computes
+// experts; at most four router items per warp and one CTA's words in a row
+// of the lookahead buffer).
+__device__ __forceinline__ bool lookahead_on(const FwdParams &P, int l, int G) {
+  const int rows = (P.E + G - 1) / G;
+  return l + 1 < P.nl && (P.L[l + 1].flags & kLookahead) && !P.route_only && rows * (P.H / 256) <= 4 * NW &&
+         rows * P.nb <= kLogitWords;
 }
 
 // ------------------------------------------------------------ the kernel
 
-template <int BITS>
+// LA: some layer of the call has the lookahead flag (the instance without
+// it carries none of the lookahead's code).
+template <int BITS, bool LA>
 __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ FwdParams P) {
   extern __shared__ __align__(128) unsigned char sm[];
   const int H = P.H, E = P.E, K = P.K, I = P.I, nb = P.nb;
@@ -872,6 +982,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     MOE_STAMP(0)
     if (l == 0 && tid == 0) sflag[8] = 0;
     const LayerP &L = P.L[l];
+    if (LA && l == 0 && cta == 0 && L.la_idx && (L.flags & kLookahead))  // no layer predicts the first one
+      for (int j = tid; j < nb * K; j += NT) L.la_idx[j] = 0xffffffffu;
     unsigned *cnt = P.cnt + (size_t)l * kCntPerLayer;
     const bool hs = L.sgate != nullptr;
     const float *src = l == 0 ? P.x : P.xbuf + (size_t)l * nb * H;
@@ -1002,6 +1114,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
                        ((unsigned long long)(l + 1) << 32) | __float_as_uint(sum));
     }
     MOE_STAMP(3)
+    // ---- lookahead: this CTA's rows of the next layer's router on this
+    // layer's input, published for the prediction of the next layer's
+    // experts (rows split over the CTAs as the exact ones are; one pass of
+    // at most four items per warp, so long rows or few CTAs go without)
+    if (LA && lookahead_on(P, l, G)) lookahead_rows(P, l, xf, red);
 
     // ---- T: top-k, softmax, union
     // every logit of the layer, each polled until its writer's tag shows
@@ -1011,16 +1128,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     }
     MOE_STAMP(4)
     MOE_STAMP(8)
-    if (warp < nb) {
-      if (E <= 128)
-        topk_warp<4>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
-      else if (E <= 256)
-        topk_warp<8>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
-      else if (E <= 512)
-        topk_warp<16>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
-      else
-        topk_warp<32>(lg + warp * E1, E, K, sidx + warp * 32, sw + warp * 32);
-    }
+    topk_rows(lg, E1, E, K, nb, sidx, sw);
     if (tid < 4) gam[tid] = (hs && tid < nb) ? 1.f / (1.f + expf(-lg[tid * E1 + E])) : 0.f;
     __syncthreads();
     MOE_STAMP(9)
@@ -1146,7 +1254,25 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           break;
         }
         if (d.host && d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0) {
-          fill_unit_plain(d, H, I, stages + (size_t)(u % S) * P.stage_bytes, gt);
+          // a record in host memory: the group reads the tile itself over
+          // the C2C link, every 16-byte copy in flight at once, into the
+          // layout issue_unit's bulk copies give (segments: code rows, then
+          // scale rows, then bias rows; gate_up: the gate then the up half
+          // of each; every segment a whole number of 16-byte pieces)
+          uint8_t *stg = stages + (size_t)(u % S) * P.stage_bytes;
+          const int inp = d.down ? I : H, nrow = d.down ? 64 : 16, rows = d.down ? 64 : 32;
+          const uint32_t rb = inp * d.bits / 8, sp = inp / 32;
+          for (int k = 0; k < (d.down ? 3 : 6); k++) {
+            const int kind = d.down ? k : k >> 1, half = d.down ? 0 : k & 1;
+            const uint32_t rowb = kind == 0 ? rb : sp;
+            const uint8_t *src =
+                d.rec + (kind == 0 ? d.q.w : kind == 1 ? d.q.s : d.q.b) + (size_t)(d.row0 + half * I) * rowb;
+            uint8_t *dst = kind == 0 ? stg + half * nrow * rb : stg + rows * rb + (kind - 1) * rows * sp + half * nrow * sp;
+            const int n = (int)((nrow * rowb) >> 4);
+            for (int i = gt; i < n; i += GT) cp_async16(dst + 16 * i, src + 16 * i);
+          }
+          cp_async_wait_all();
+          fence_proxy_async_smem();  // before a later bulk copy refills the stage
           grp_sync(grp);
         }
         if (q == 0) MOE_STAMP(11)
@@ -1265,6 +1391,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       drain_stages(bars, stg_unit, S, P);
       return;
     }
+    // ---- lookahead: predict the next layer's experts and prefetch this
+    // CTA's share of their records into L2, now that this CTA's units are
+    // done: the prefetches overlap the wait for the next layer's input and
+    // its routing
+    if (LA && lookahead_on(P, l, G)) lookahead_step(P, l, lg, E1, sidx, sw, posof, red);
     if (tid == 0) sflag[9] = 0;  // the next layer's unit counter (read after several barriers)
     qbase += (unsigned)n;
     MOE_STAMP(7)
@@ -1302,13 +1433,21 @@ static int stage_bytes(int H, int I) {
   return (m + 127) & ~127;
 }
 
-template <int BITS>
+template <int BITS, bool LA>
 static int occupancy_t(int smem) {
   int n = 0;
-  if (cudaFuncSetAttribute(decode_kernel<BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+  if (cudaFuncSetAttribute(decode_kernel<BITS, LA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS>, NT, smem) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<BITS, LA>, NT, smem) != cudaSuccess) return 0;
   return n;
+}
+
+template <bool LA>
+static int occupancy_b(int bits, int smem) {
+  return bits == 4   ? occupancy_t<4, LA>(smem)
+         : bits == 3 ? occupancy_t<3, LA>(smem)
+         : bits == 2 ? occupancy_t<2, LA>(smem)
+                     : occupancy_t<0, LA>(smem);
 }
 
 int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes) {
@@ -1323,10 +1462,7 @@ int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes) {
   p.stages = S;
   p.stage_bytes = sb;
   const int smem = fixed + S * sb;
-  const int occ = p.bits == 4   ? occupancy_t<4>(smem)
-                  : p.bits == 3 ? occupancy_t<3>(smem)
-                  : p.bits == 2 ? occupancy_t<2>(smem)
-                                : occupancy_t<0>(smem);
+  const int occ = p.lookahead ? occupancy_b<true>(p.bits, smem) : occupancy_b<false>(p.bits, smem);
   if (occ < 1) return -1;
   const int G = sms < kMaxGrid ? sms : kMaxGrid;
   // every CTA's router rows x activation rows fit its logit words
@@ -1336,7 +1472,7 @@ int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes) {
   return 0;
 }
 
-template <int BITS>
+template <int BITS, bool LA>
 static cudaError_t launch_t(const FwdParams &p, int grid, int smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1348,17 +1484,22 @@ static cudaError_t launch_t(const FwdParams &p, int grid, int smem, cudaStream_t
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<BITS>, p);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<BITS, LA>, p);
+}
+
+template <bool LA>
+static cudaError_t launch_b(const FwdParams &p, int grid, int smem, cudaStream_t st) {
+  switch (p.bits) {
+    case 4: return launch_t<4, LA>(p, grid, smem, st);
+    case 3: return launch_t<3, LA>(p, grid, smem, st);
+    case 2: return launch_t<2, LA>(p, grid, smem, st);
+    case 0: return launch_t<0, LA>(p, grid, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_decode(const FwdParams &p, int grid, int smem, cudaStream_t st) {
-  switch (p.bits) {
-    case 4: return launch_t<4>(p, grid, smem, st);
-    case 3: return launch_t<3>(p, grid, smem, st);
-    case 2: return launch_t<2>(p, grid, smem, st);
-    case 0: return launch_t<0>(p, grid, smem, st);
-    default: return cudaErrorInvalidValue;
-  }
+  return p.lookahead ? launch_b<true>(p, grid, smem, st) : launch_b<false>(p, grid, smem, st);
 }
 
 }  // namespace moe

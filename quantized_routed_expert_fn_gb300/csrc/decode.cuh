@@ -22,6 +22,8 @@ struct LayerP {
   QOff guw[3], dnw[3];     // mixed widths: offsets in a record of width 4, 3, 2 (index 4 - width)
   const uint8_t *etier;    // [E] 0: record in device memory, 1: in host memory; nullptr: all in device memory
   float cut_w;             // host-tier experts below this weight in every row are cut (0: none)
+  uint32_t span, span_w[3];  // bytes from a record's base to the end of its last tensor (uniform; per width)
+  uint32_t *la_idx;        // [nb][K] this layer's experts as predicted one layer early, or nullptr
 };
 
 // Per-layer counters in the workspace (uint32 each), every counter on a
@@ -39,6 +41,7 @@ struct FwdParams {
   int H, E, K, I, nb, nl, bits;  // bits: routed width, or 0 when each record carries its own
   int route_only;
   int withhold;  // failure-detection test: never release the router count
+  int lookahead;  // some layer has the lookahead flag (selects the kernel instance that carries it)
   const float *x;
   float *out;
   uint64_t *slot_tab;     // [nl][64] or nullptr
@@ -48,6 +51,7 @@ struct FwdParams {
   float *logits_out;      // [nb][E] (route only) or nullptr
   int *status;
   unsigned *cnt;          // [nl][kCntPerLayer]
+  unsigned long long *lgp;  // [2][kMaxGrid][kLogitWords] lookahead logits {fp32 bits, layer + 1 predicted}
   unsigned long long *lgw;  // [kMaxGrid][kLogitWords] router logits {fp32 bits, layer + 1}, CTA c's
                             // rows x nb; zeroed per call, reused by every layer
   float *xbuf;            // [nl][nb][H]  input of layer l (l >= 1)

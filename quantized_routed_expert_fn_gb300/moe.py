@@ -17,6 +17,7 @@ from . import synth
 
 RESIDUAL = 1
 PRENORM = 2
+LOOKAHEAD = 4
 TEST_WITHHOLD = 0x100
 
 OK, EINVAL, ESHAPE, EALIGN, ECUDA, ETIMEOUT, EDEVICE, ENOSPACE = 0, -1, -2, -3, -4, -5, -6, -7
@@ -48,7 +49,8 @@ class MoeLayer(ctypes.Structure):
                 ("expert_addr", ctypes.c_void_p),
                 ("gate_up", MoeQ), ("down", MoeQ),
                 ("expert_bits", ctypes.c_void_p), ("gate_up_w", MoeQ * 3), ("down_w", MoeQ * 3),
-                ("expert_tier", ctypes.c_void_p), ("cut_weak", ctypes.c_float)]
+                ("expert_tier", ctypes.c_void_p), ("cut_weak", ctypes.c_float),
+                ("lookahead_idx", ctypes.c_void_p)]
 
 
 class TierStats(ctypes.Structure):

@@ -325,3 +325,48 @@ def test_mixed_width_stack(moe):
         cur = step["out"]
     assert np.array_equal(g["out"].view(np.uint32), cur.view(np.uint32)), "stacked call != chained calls"
     print(f"[parity] mixed-width stack of 4 layers: max err = {worst:.4f} of the bound")
+
+
+# ---------------------------------------------------------------- lookahead
+
+def test_lookahead_predicts_and_changes_nothing(moe):
+    """With MOE_LOOKAHEAD on every layer, each layer's experts are predicted
+    during the previous layer from its router on the previous layer's
+    input, and the predicted records prefetched into L2.  The predicted ids
+    equal the oracle's routing of that input by that router (as sets per
+    row, where the top-k gap holds), the first layer reports no prediction,
+    and the outputs are bitwise those of the call without the lookahead."""
+    rng = np.random.default_rng(730)
+    nl, H, E, k, I, nb = 5, 1024, 64, 6, 256, 2
+    layers = [synth.make_layer(rng, H, E, k, I, 4, shared=True, flags=synth.RESIDUAL | synth.PRENORM)
+              for _ in range(nl)]
+    ols = [oracle.Layer(L) for L in layers]
+    x = synth.make_x(np.random.default_rng(731), nb, H)
+    dl = moe.DeviceLayers(layers)
+    base = run_forward(moe, dl, x)
+    la = torch.zeros((nl, nb, k), dtype=torch.int32, device="cuda")
+    dl.set_flags(synth.RESIDUAL | synth.PRENORM | moe.LOOKAHEAD)
+    for l in range(nl):
+        dl.c[l].lookahead_idx = la[l].data_ptr()
+    g = run_forward(moe, dl, x)
+    assert np.array_equal(g["out"].view(np.uint32), base["out"].view(np.uint32)), "lookahead changed the result"
+    pred = la.cpu().numpy().view(np.uint32)
+    assert (pred[0] == 0xffffffff).all()
+    # the GPU's own trajectory: layer l's input, routed by layer l + 1's router
+    cur = x.astype(np.float32)
+    inputs = []
+    for l in range(nl):
+        inputs.append(cur)
+        cur = run_forward(moe, dl, cur, n_layers=1, offset=l)["out"]
+    hits, total, checked = 0, 0, 0
+    for l in range(1, nl):
+        r = oracle.route(ols[l], inputs[l - 1].astype(np.float64))
+        exact = g["idx"][l]
+        for b in range(nb):
+            if topk_gap(r["logits"][b], k) >= GAP:
+                assert sorted(pred[l][b].tolist()) == sorted(r["idx"][b].tolist()), f"layer {l} row {b}"
+                checked += 1
+            hits += len(set(pred[l][b].tolist()) & set(exact[b].tolist()))
+            total += k
+    assert checked >= nb * (nl - 1) // 2
+    print(f"[lookahead] predictions checked {checked}; hit rate {hits / total:.2f} of the exact experts")
