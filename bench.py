@@ -137,11 +137,15 @@ def job_rows_per_s(rows_per_rank: int, world: int, ms: float) -> float:
     return rows_per_rank * world / (ms * 1e-3)
 
 
-def layer_bytes(L, union_size: int, nb: int) -> int:
+def layer_bytes(L, union_size: int, nb: int, widths=None) -> int:
     """Algorithmic bytes of one layer: router + shared gate + union records +
-    shared record + layer input and output."""
+    shared record + layer input and output.  widths: the code width of each
+    record read (mixed-width layers), else union_size records of L's width."""
     b = L.n_experts * L.hidden * 2
-    b += union_size * record_bytes(L.layout)
+    if widths is None:
+        b += union_size * record_bytes(L.layout)
+    else:
+        b += sum(record_bytes(L.layouts[int(w)]) for w in widths)
     if L.shared_layout is not None:
         b += L.hidden * 2 + record_bytes(L.shared_layout)
     b += 2 * nb * L.hidden * 4
@@ -183,7 +187,23 @@ def decode_inputs(base, nb: int, n_views: int, seed: int) -> list:
     return xs
 
 
-def decode_setup(name, nb, device, seed, n_layers=None):
+def view_bytes(dl, slots, nb) -> int:
+    """Algorithmic bytes of one call over the layers of dl, from its slot
+    tables: the records it listed (cut and absent ones are not read), at
+    their widths."""
+    tot = 0
+    for l, L in enumerate(dl.src):
+        row = [int(a) for a in slots[l][:62]]
+        listed = row.index(0) if 0 in row else 62
+        widths = None
+        if getattr(L, "expert_bits", None) is not None:
+            base, stride = L.records.data_ptr(), L.layout.stride
+            widths = [L.expert_bits[(a - base) // stride] for a in row[:listed]]
+        tot += layer_bytes(L, listed, nb, widths)
+    return tot
+
+
+def decode_setup(name, nb, device, seed, n_layers=None, mixed=False):
     """Device layers and inputs of a decode workload.
 
     The 48-layer stack reads every layer's union once per step (about 1.2 GB,
@@ -199,7 +219,17 @@ def decode_setup(name, nb, device, seed, n_layers=None):
     import torch
     from quantized_routed_expert_fn_gb300 import moe, synth
     cfg = synth.CONFIGS[name]
-    layers = synth.make_device_layers(name, seed=seed, device=device, n_layers=n_layers or None)
+    E = cfg["n_experts"]
+
+    def mixed_widths(s):
+        eb = np.array([4, 3, 2] * (E // 3 + 1), dtype=np.uint8)[:E]
+        np.random.default_rng(s).shuffle(eb)
+        return eb
+
+    if mixed:
+        layers = [synth.make_device_mixed_layer(name, mixed_widths(seed), seed=seed, device=device)]
+    else:
+        layers = synth.make_device_layers(name, seed=seed, device=device, n_layers=n_layers or None)
     if len(layers) > 1:
         gen = torch.Generator(device="cpu").manual_seed(100 + seed)
         x = torch.randn((nb, cfg["hidden"]), generator=gen, dtype=torch.float32)
@@ -216,7 +246,9 @@ def decode_setup(name, nb, device, seed, n_layers=None):
     per_pool = base.n_experts // U
     pools = [base]
     while len(pools) * per_pool < n_views:
-        pools.append(synth.make_device_layers(name, seed=seed + 1000 * len(pools), device=device, n_layers=1)[0])
+        s2 = seed + 1000 * len(pools)
+        pools.append(synth.make_device_mixed_layer(name, mixed_widths(s2), seed=s2, device=device) if mixed
+                     else synth.make_device_layers(name, seed=s2, device=device, n_layers=1)[0])
     views, xs = [], []
     for i in range(n_views):
         pool = pools[i // per_pool]
@@ -228,7 +260,7 @@ def decode_setup(name, nb, device, seed, n_layers=None):
     for pi, pool in enumerate(pools):
         n_here = min(per_pool, n_views - pi * per_pool)
         xs += [torch.from_numpy(x) for x in decode_inputs(pool, nb, n_here, seed=11 + seed + pi)]
-    return dict(views=[moe.DeviceLayers([v], device=device) for v in views], xs=xs, layers=views,
+    return dict(views=[moe.DeviceLayers([v], device=device) for v in views], xs=xs, layers=views, pools=pools,
                 rotation=dict(views=n_views, pools=len(pools), l2_bytes=L2))
 
 
@@ -247,21 +279,24 @@ def time_decode(setup, nb, steps, warmup, rank, world, device, e2e=True):
     wmap = torch.zeros((nl, 4, 64), dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
-    # every view once: its union sizes and record addresses
-    unions, addrs = [], []
+    # every view once: its union sizes, record addresses and bytes read
+    unions, addrs, bytes_per_view, kept = [], [], [], []
     for i in range(nv):
         moe.forward(views[i], xs[i], out, ws, status, slot, wmap, stream=stream)
         torch.cuda.synchronize()
         if status.item() != 0:
             raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")
-        st = slot.cpu()
+        st = slot.cpu().numpy().astype(np.int64)
         u = [int(v) for v in st[:, 63].tolist()]
         unions.append(u)
-        addrs.append(set(int(a) for l in range(nl) for a in st[l, : u[l]].tolist()))
+        rows = [[int(a) for a in st[l, :62]] for l in range(nl)]
+        listed = [r.index(0) if 0 in r else 62 for r in rows]
+        kept.append(sum(listed))
+        addrs.append(set(a for l in range(nl) for a in rows[l][: listed[l]]))
+        bytes_per_view.append(view_bytes(views[i], st, nb))
     for s in range(max(warmup, 3)):
         moe.forward(views[s % nv], xs[s % nv], out, ws, status, slot, wmap, stream=stream)
     torch.cuda.synchronize()
-    bytes_per_view = [sum(layer_bytes(L, u, nb) for L, u in zip(views[i].src, unions[i])) for i in range(nv)]
     bytes_per_step = sum(bytes_per_view[s % nv] for s in range(steps)) / steps
 
     dist = world > 1
@@ -326,7 +361,9 @@ def time_decode(setup, nb, steps, warmup, rank, world, device, e2e=True):
               f"{cycle / 1e6:.0f} MB = {cycle / rot['l2_bytes']:.1f}x the {rot['l2_bytes'] / 1e6:.0f} MB L2 "
               f"(queried at run time) before any byte is read again")
     return dict(ms=ms, e2e_ms=e2e_ms, nb=nb, nl=nl, bytes=bytes_per_step, achieved=achieved, peak=peak,
-                peak_kind=peak_kind, clocks=clocks, unions=sorted(set(u for uu in unions for u in uu)), l2=l2)
+                peak_kind=peak_kind, clocks=clocks, unions=sorted(set(u for uu in unions for u in uu)), l2=l2,
+                kept_per_step=sum(kept[s % nv] for s in range(steps)) / steps,
+                union_per_step=sum(sum(unions[s % nv]) for s in range(steps)) / steps)
 
 
 def run_ours(args, rank, world, device):
@@ -342,24 +379,102 @@ def run_ours(args, rank, world, device):
     return time_decode(setup, nb, args.steps, args.warmup, rank, world, device)
 
 
+def c2c_copy_gbs(device, nbytes=1 << 30, reps=5) -> float:
+    """Host -> device copy bandwidth from pinned memory (best of reps): the
+    denominator of the host-memory reads' link fraction."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    best = 0.0
+    for _ in range(reps + 1):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        d.copy_(h, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    del h, d
+    return best
+
+
+def decode_line(name, nb, r, extra=None):
+    line = {"workload": WORKLOADS[name].replace("nb=4", f"nb={nb}"), "ms_per_step": r["ms"],
+            "rows_per_s": nb * r["nl"] / (r["ms"] * 1e-3), "union_sizes": r["unions"],
+            "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
+                         "frac": r["achieved"] / r["peak"], "peak_source": r["peak_kind"],
+                         "algorithmic_bytes_per_launch": r["bytes"]},
+            "l2": r["l2"], "clocks": r["clocks"]}
+    line.update(extra or {})
+    return line
+
+
+def host_tier_extra(device, nb, cut_weak, c2c):
+    """The verify batch with every routed record in pinned host memory (a
+    two-tier store with no device slots): the kernel reads the union over
+    NVLink-C2C.  With cut_weak, host experts below it in every row are cut."""
+    import torch
+    from quantized_routed_expert_fn_gb300 import moe
+    setup = decode_setup("c2", nb, device, seed=1)
+    pool = setup["pools"][0]
+    E, stride = pool.n_experts, pool.layout.stride
+    host = torch.empty((1, E, stride), dtype=torch.uint8).pin_memory()
+    host[0].copy_(pool.records)
+    addr = torch.zeros((1, E), dtype=torch.int64, device=device)
+    tier = torch.zeros((1, E), dtype=torch.uint8, device=device)
+    store = moe.Tier(1, E, stride, host, 0, None, addr, tier)
+    for v in setup["views"]:
+        v.set_tier(0, addr[0], tier[0], cut_weak)
+    torch.cuda.synchronize()
+    r = time_decode(setup, nb, 200, 5, 0, 1, device, e2e=False)
+    rec = record_bytes(pool.layout)
+    host_bytes = r["kept_per_step"] * rec
+    link = host_bytes / (r["ms"] * 1e-3) / 1e9
+    extra = {"host_memory": {"records_read_from_host_per_step": r["kept_per_step"],
+                             "union_per_step": r["union_per_step"],
+                             "host_bytes_per_step": host_bytes, "achieved_link_gbs": link,
+                             "link_copy_gbs": c2c, "link_frac": link / c2c,
+                             "link_peak_source": "pinned host-to-device copy measured in this run"}}
+    if cut_weak:
+        extra["cut_weak"] = cut_weak
+    store.close()
+    return r, extra
+
+
 def extras(args, device):
     """The other decode and prefill workloads of the metric, timed on this GPU
-    after the headline: verify batches, low-bit records, the prefill chunk."""
+    after the headline: verify batches, low-bit records, mixed widths,
+    records in host memory (with and without the cut), the lookahead, the
+    prefill chunk."""
     import argparse as _ap
     import torch
     res = {}
     for name, nb in (("c2", 4), ("c2", 1), ("c3b3", 4), ("c3b3", 1), ("c3b2", 4), ("c3b2", 1)):
         setup = decode_setup(name, nb, device, seed=1)
         r = time_decode(setup, nb, args.steps, args.warmup, 0, 1, device, e2e=False)
-        res[f"{name}_nb{nb}"] = {
-            "workload": WORKLOADS[name].replace("nb=4", f"nb={nb}"), "ms_per_step": r["ms"],
-            "rows_per_s": nb / (r["ms"] * 1e-3), "union_sizes": r["unions"],
-            "roofline": {"bound": "hbm", "achieved": r["achieved"], "peak": r["peak"], "unit": "GB/s",
-                         "frac": r["achieved"] / r["peak"], "peak_source": r["peak_kind"],
-                         "algorithmic_bytes_per_launch": r["bytes"]},
-            "l2": r["l2"], "clocks": r["clocks"]}
+        res[f"{name}_nb{nb}"] = decode_line(name, nb, r)
         del setup
         torch.cuda.empty_cache()
+    # a union mixing 4-, 3- and 2-bit records (a third of the experts each)
+    setup = decode_setup("c2", 4, device, seed=1, mixed=True)
+    r = time_decode(setup, 4, args.steps, args.warmup, 0, 1, device, e2e=False)
+    res["c2mix_nb4"] = decode_line("c2", 4, r, {"record_widths": "4/3/2-bit, a third of the experts each"})
+    del setup
+    torch.cuda.empty_cache()
+    # every routed record in host memory, read over the C2C link
+    c2c = c2c_copy_gbs(device)
+    for key, cut in (("c2host_nb4", 0.0), ("c2hostcut_nb4", 0.08)):
+        r, extra = host_tier_extra(device, 4, cut, c2c)
+        res[key] = decode_line("c2", 4, r, extra)
+        torch.cuda.empty_cache()
+    # the 48-layer stack with the one-layer lookahead on every layer
+    setup = decode_setup("c1", 1, device, seed=1)
+    dl = setup["views"][0]
+    dl.set_flags(dl.src[0].flags | 4)
+    r = time_decode(setup, 1, args.steps, args.warmup, 0, 1, device, e2e=False)
+    res["c1_lookahead"] = decode_line("c1", 1, r, {"lookahead": "every layer predicts the next and prefetches "
+                                                                "its device-memory records into L2"})
+    del setup, dl
+    torch.cuda.empty_cache()
     a = _ap.Namespace(**vars(args))
     a.workload, a.nb = "c4", 0
     r = run_prefill(a, 0, 1, device)

@@ -744,16 +744,43 @@ __device__ __forceinline__ UnitDesc get_unit(int q, const Sched &s, const LayerP
 // Producer warp: request the weight tile of one unit into its ring stage:
 // the code rows (gate_up: 16 gate rows then the matching 16 up rows; down:
 // 64 output rows), then their scales, then their biases, row-major.
-__device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_t *bar, int *status) {
-  if ((threadIdx.x & 31) != 0) return;
-  if (d.rec == nullptr || ((uintptr_t)d.rec & 15u)) {
+// host_fill: this stage's word, 1 while its last fill was by cp.async.
+__device__ void issue_unit(const UnitDesc &d, int H, int I, uint8_t *st, uint64_t *bar, int *status,
+                           unsigned *host_fill) {
+  const int lane = threadIdx.x & 31;
+  const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
+  if (ok && d.host) {
+    // a record in host memory: the warp's lanes read the tile over the C2C
+    // link with 16-byte cp.async copies (the ordinary load path), in the
+    // layout the bulk copies below give (code rows, then scale rows, then
+    // bias rows; gate_up: the gate then the up half of each; every segment
+    // a whole number of 16-byte pieces), each lane's copies registered on
+    // the stage barrier; lane 0 then makes the phase's one arrival
+    const int inp = d.down ? I : H, nrow = d.down ? 64 : 16, rows = d.down ? 64 : 32;
+    const uint32_t rb = inp * d.bits / 8, sp = inp / 32;
+    for (int k = 0; k < (d.down ? 3 : 6); k++) {
+      const int kind = d.down ? k : k >> 1, half = d.down ? 0 : k & 1;
+      const uint32_t rowb = kind == 0 ? rb : sp;
+      const uint8_t *src =
+          d.rec + (kind == 0 ? d.q.w : kind == 1 ? d.q.s : d.q.b) + (size_t)(d.row0 + half * I) * rowb;
+      uint8_t *dst = kind == 0 ? st + half * nrow * rb : st + rows * rb + (kind - 1) * rows * sp + half * nrow * sp;
+      const int n = (int)((nrow * rowb) >> 4);
+      for (int i = lane; i < n; i += 32) cp_async16(dst + 16 * i, src + 16 * i);
+    }
+    cp_async_mbar_arrive(bar);
+    __syncwarp();
+    if (lane == 0) *host_fill = 1u, mbar_arrive(bar);
+    return;
+  }
+  if (lane != 0) return;
+  if (!ok) {
     atomicCAS(status, 0, kStatusDevice);
     mbar_expect_tx(bar, 0);  // completes the phase with no bytes
     return;
   }
-  if (d.host) {
-    mbar_expect_tx(bar, 0);  // the computing group reads this tile itself (fill_unit_plain)
-    return;
+  if (*host_fill) {  // last written by cp.async: order that before the bulk copies' writes
+    fence_proxy_async_smem();
+    *host_fill = 0u;
   }
   const int inp = d.down ? I : H;
   const uint32_t rb = inp * d.bits / 8, sp = inp / 32;
@@ -952,14 +979,15 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   const int hsz = nblkI * 256 * 2 + 2 * 64;  // 32-bit words per group
   uint64_t *eaddr_s = reinterpret_cast<uint64_t *>(reinterpret_cast<uint32_t *>(hsm) + 2 * hsz);  // [E]
   unsigned *stg_unit = reinterpret_cast<unsigned *>(eaddr_s + ((E + 1) & ~1));  // [S] last unit issued per stage
-  int *posof = reinterpret_cast<int *>(stg_unit + kMaxStages);                   // [E] union scratch, INT_MAX between uses
+  unsigned *stg_host = stg_unit + kMaxStages;                                    // [S] stage last filled by cp.async
+  int *posof = reinterpret_cast<int *>(stg_host + kMaxStages);                   // [E] union scratch, INT_MAX between uses
   int *sbits = posof + E;                                                        // [64] slot -> code width (mixed)
   int *stier = sbits + 64;                                                       // [64] slot -> record in host memory
   uint8_t *eb_s = reinterpret_cast<uint8_t *>(stier + 64);                       // [E] expert -> code width (mixed)
   uint8_t *et_s = eb_s + ((E + 15) & ~15);                                       // [E] expert -> record in host memory
 
   if (tid == 0) {
-    for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu;
+    for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu, stg_host[s] = 0u;
     fence_mbar_init();
     sflag[9] = 0;
   }
@@ -970,7 +998,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   __syncthreads();
   // warp lane 0 of an issuing warp: unit q of the layer into its ring stage
   auto issue_at = [&](const UnitDesc &d, unsigned u) {
-    issue_unit(d, H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S], P.status);
+    issue_unit(d, H, I, stages + (size_t)(u % S) * P.stage_bytes, &bars[u % S], P.status, &stg_host[u % S]);
     if (lane == 0) stg_unit[u % S] = u;
   };
 
@@ -1253,28 +1281,6 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
           alive = false;
           break;
         }
-        if (d.host && d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0) {
-          // a record in host memory: the group reads the tile itself over
-          // the C2C link, every 16-byte copy in flight at once, into the
-          // layout issue_unit's bulk copies give (segments: code rows, then
-          // scale rows, then bias rows; gate_up: the gate then the up half
-          // of each; every segment a whole number of 16-byte pieces)
-          uint8_t *stg = stages + (size_t)(u % S) * P.stage_bytes;
-          const int inp = d.down ? I : H, nrow = d.down ? 64 : 16, rows = d.down ? 64 : 32;
-          const uint32_t rb = inp * d.bits / 8, sp = inp / 32;
-          for (int k = 0; k < (d.down ? 3 : 6); k++) {
-            const int kind = d.down ? k : k >> 1, half = d.down ? 0 : k & 1;
-            const uint32_t rowb = kind == 0 ? rb : sp;
-            const uint8_t *src =
-                d.rec + (kind == 0 ? d.q.w : kind == 1 ? d.q.s : d.q.b) + (size_t)(d.row0 + half * I) * rowb;
-            uint8_t *dst = kind == 0 ? stg + half * nrow * rb : stg + rows * rb + (kind - 1) * rows * sp + half * nrow * sp;
-            const int n = (int)((nrow * rowb) >> 4);
-            for (int i = gt; i < n; i += GT) cp_async16(dst + 16 * i, src + 16 * i);
-          }
-          cp_async_wait_all();
-          fence_proxy_async_smem();  // before a later bulk copy refills the stage
-          grp_sync(grp);
-        }
         if (q == 0) MOE_STAMP(11)
         const bool ok = d.rec != nullptr && ((uintptr_t)d.rec & 15u) == 0;
         if (ok) {
@@ -1419,7 +1425,7 @@ static int fixed_smem(int H, int E, int I, int nb, int bits) {
   b += 64 * 8;                                     // slot -> record table
   b += 2 * ((I / 128) * 256 * 8 + 2 * 64 * 4);     // staged h fragments and sums, one per unit group
   b += ((E + 1) & ~1) * 8;                         // expert addresses
-  b += kMaxStages * 4;                             // last unit issued per stage
+  b += 2 * kMaxStages * 4;                         // last unit issued per stage, stage last filled by cp.async
   b += E * 4;                                      // union scratch
   b += 2 * 64 * 4 + 2 * ((E + 15) & ~15);          // slot widths and tiers, expert widths and tiers
   return b;

@@ -300,6 +300,8 @@ class DeviceLayer:
     shared_layout: RecordLayout | None
     records: "object"         # torch.uint8 [E][stride]
     layout: RecordLayout
+    expert_bits: "object" = None  # mixed widths: numpy uint8 [E]
+    layouts: dict | None = None
 
 
 def _dev_fill_q(torch, gen, rec, q: QDesc, bits: int, scale_lo: float, scale_hi: float, bias_noise: float):
@@ -314,6 +316,28 @@ def _dev_fill_q(torch, gen, rec, q: QDesc, bits: int, scale_lo: float, scale_hi:
         b = b + torch.randn((n, ng), device=rec.device, generator=gen) * bias_noise
     rec[:, q.s:q.s + cs] = s.view(torch.int16).view(torch.uint8)
     rec[:, q.b:q.b + cs] = b.to(torch.bfloat16).view(torch.int16).view(torch.uint8)
+
+
+def make_device_mixed_layer(name: str, expert_bits, seed: int = 0, device="cuda") -> DeviceLayer:
+    """One layer of workload `name` whose routed records have the given
+    per-expert widths (4, 3 or 2; records stay the 4-bit stride apart), the
+    3- and 2-bit ones drawn with the low-bit scales, on the GPU."""
+    import torch
+    layer = make_device_layers(name, seed=seed, device=device, n_layers=1)[0]
+    eb = np.ascontiguousarray(expert_bits, dtype=np.uint8)
+    layouts = {b: record_layout(layer.hidden, layer.inter, b) for b in (4, 3, 2)}
+    gen = torch.Generator(device=device)
+    gen.manual_seed(seed + 77)
+    for b in (3, 2):
+        idx = torch.from_numpy(np.nonzero(eb == b)[0]).to(device)
+        if idx.numel() == 0:
+            continue
+        sub = torch.zeros((idx.numel(), layer.layout.stride), dtype=torch.uint8, device=device)
+        for q in (layouts[b].gate_up, layouts[b].down):
+            _dev_fill_q(torch, gen, sub, q, b, LOWBIT_SCALE[0], LOWBIT_SCALE[1], LOWBIT_BIAS_NOISE)
+        layer.records[idx] = sub
+    layer.expert_bits, layer.layouts = eb, layouts
+    return layer
 
 
 def make_device_layers(name: str, seed: int = 0, device="cuda", n_layers: int | None = None, **over):
