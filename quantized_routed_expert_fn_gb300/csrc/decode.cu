@@ -983,11 +983,13 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
   int *posof = reinterpret_cast<int *>(stg_host + kMaxStages);                   // [E] union scratch, INT_MAX between uses
   int *sbits = posof + E;                                                        // [64] slot -> code width (mixed)
   int *stier = sbits + 64;                                                       // [64] slot -> record in host memory
-  uint8_t *eb_s = reinterpret_cast<uint8_t *>(stier + 64);                       // [E] expert -> code width (mixed)
+  volatile int *absent = stier + 64;                                             // [4] [0]: some record of the layer not on this GPU
+  uint8_t *eb_s = reinterpret_cast<uint8_t *>(stier + 68);                       // [E] expert -> code width (mixed)
   uint8_t *et_s = eb_s + ((E + 15) & ~15);                                       // [E] expert -> record in host memory
 
   if (tid == 0) {
     for (int s = 0; s < S; s++) mbar_init(&bars[s], 1), stg_unit[s] = 0xffffffffu, stg_host[s] = 0u;
+    absent[0] = 0;
     fence_mbar_init();
     sflag[9] = 0;
   }
@@ -1049,7 +1051,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         wv[k] = ldg_stream4(wrow + ch * 256 + lane * 8);
       }
     }
-    for (int e = tid; e < E; e += NT) eaddr_s[e] = L.eaddr[e];
+    for (int e = tid; e < E; e += NT) {
+      const uint64_t a = L.eaddr[e];
+      eaddr_s[e] = a;
+      if (a == 0ull) absent[0] = 1;  // (cleared at the end of every layer)
+    }
     if (BITS == 0)
       for (int e = tid; e < E; e += NT) eb_s[e] = L.ebits[e];
     if (L.etier)
@@ -1059,89 +1065,103 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
       return;
     }
     MOE_STAMP(1)
+    const int n4 = nb * H / 4, h4 = H / 4;
+    const bool norm = (L.flags & kPrenorm) != 0;
     {
-      // one round trip: each thread loads up to 4 float4 of the nb rows
-      const int n4 = nb * H / 4, h4 = H / 4;
+      // the raw input to shared memory in one round trip (each thread up to
+      // 4 float4 of the nb rows); with the unit RMSNorm, the rows' sums of
+      // squares as warp partials (red[1024 + warp * 4 + b])
       const float4 *src4 = reinterpret_cast<const float4 *>(src);
+      float4 *xf4 = reinterpret_cast<float4 *>(xf);
       float4 v[4];
 #pragma unroll
       for (int k = 0; k < 4; k++) {
         const int i = tid + k * NT;
         v[k] = i < n4 ? __ldcg(src4 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (L.flags & kPrenorm) {
-        // per-row sums of squares: thread partials -> warp sums -> CTA sums (fixed order)
-        float ss[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const int i = tid + k * NT;
-          if (i < n4) {
-            const float q = v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
-            ss[i / h4] += q;
-          }
-        }
-#pragma unroll
-        for (int b = 0; b < 4; b++) ss[b] = warp_sum(ss[b]);
-        if (lane == 0)
-          for (int b = 0; b < 4; b++) red[warp * 4 + b] = ss[b];
-        __syncthreads();
-        if (tid < 4) {
-          float t = 0.f;
-          for (int w = 0; w < NW; w++) t += red[w * 4 + tid];
-          red[64 + tid] = 1.0f / sqrtf(t / (float)H + 1e-6f);
-        }
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < 4; k++) {
-          const int i = tid + k * NT;
-          if (i < n4) {
-            const float r = red[64 + i / h4];
-            v[k].x *= r, v[k].y *= r, v[k].z *= r, v[k].w *= r;
-          }
-        }
-      }
-      float4 *xf4 = reinterpret_cast<float4 *>(xf);
 #pragma unroll
       for (int k = 0; k < 4; k++) {
         const int i = tid + k * NT;
         if (i < n4) xf4[i] = v[k];
       }
+      if (norm) {
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 4; k++) {
+          const int i = tid + k * NT;
+          if (i < n4) ss[i / h4] += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+        }
+#pragma unroll
+        for (int b = 0; b < 4; b++) ss[b] = warp_sum(ss[b]);
+        if (lane == 0)
+          for (int b = 0; b < 4; b++) red[1024 + warp * 4 + b] = ss[b];
+      }
     }
     __syncthreads();
-    stage_frags<AB>(xf, H, nb, xa, xs, cs);
-    if (AB != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr, cs4);
-    __syncthreads();
-    MOE_STAMP(2)
-    {
+    // this CTA's router rows on the raw input: the norm is one scalar per
+    // row, applied to the sums as they are published, so the logits leave
+    // before the input's tensor-core fragments are staged
 #pragma unroll
-      for (int k = 0; k < 4; k++) {
-        const int it = warp + k * NW;
-        if (it < nitem) {
-          const int ch = it % nch;
-          const float wf[8] = {bf16lo(wv[k].x), bf16hi(wv[k].x), bf16lo(wv[k].y), bf16hi(wv[k].y),
-                               bf16lo(wv[k].z), bf16hi(wv[k].z), bf16lo(wv[k].w), bf16hi(wv[k].w)};
-          for (int b = 0; b < nb; b++) {
-            const float4 *xp = reinterpret_cast<const float4 *>(xf + b * H + ch * 256 + lane * 8);
-            const float4 x0 = xp[0], x1 = xp[1];
-            float acc = wf[0] * x0.x + wf[1] * x0.y + wf[2] * x0.z + wf[3] * x0.w + wf[4] * x1.x +
-                        wf[5] * x1.y + wf[6] * x1.z + wf[7] * x1.w;
-            acc = warp_sum(acc);
-            if (lane == 0) red[it * 4 + b] = acc;
-          }
+    for (int k = 0; k < 4; k++) {
+      const int it = warp + k * NW;
+      if (it < nitem) {
+        const int ch = it % nch;
+        const float wf[8] = {bf16lo(wv[k].x), bf16hi(wv[k].x), bf16lo(wv[k].y), bf16hi(wv[k].y),
+                             bf16lo(wv[k].z), bf16hi(wv[k].z), bf16lo(wv[k].w), bf16hi(wv[k].w)};
+        for (int b = 0; b < nb; b++) {
+          const float4 *xp = reinterpret_cast<const float4 *>(xf + b * H + ch * 256 + lane * 8);
+          const float4 x0 = xp[0], x1 = xp[1];
+          float acc = wf[0] * x0.x + wf[1] * x0.y + wf[2] * x0.z + wf[3] * x0.w + wf[4] * x1.x + wf[5] * x1.y +
+                      wf[6] * x1.z + wf[7] * x1.w;
+          acc = warp_sum(acc);
+          if (lane == 0) red[it * 4 + b] = acc;
         }
       }
     }
     __syncthreads();
+    // row scales 1 / sqrt(mean(x^2) + 1e-6), formed by every thread from the
+    // warp partials in a fixed order (the same value everywhere)
+    float rs[4] = {1.f, 1.f, 1.f, 1.f};
+    if (norm) {
+#pragma unroll
+      for (int b = 0; b < 4; b++) {
+        if (b < nb) {
+          float t = 0.f;
+          for (int w = 0; w < NW; w++) t += red[1024 + w * 4 + b];
+          rs[b] = 1.0f / sqrtf(t / (float)H + 1e-6f);
+        }
+      }
+    }
     for (int j = tid; j < (rr1 - rr0) * nb; j += NT) {
       const int r = j / nb, b = j % nb;
       float sum = 0.f;
       for (int ch = 0; ch < nch; ch++) sum += red[(r * nch + ch) * 4 + b];
+      sum *= rs[b];
       // value and layer tag in one 64-bit store: no release fence
       if (!(P.withhold && rr0 + r == 0))
         st_relaxed_u64(P.lgw + ((size_t)(l & 1) * kMaxGrid + cta) * kLogitWords + j,
                        ((unsigned long long)(l + 1) << 32) | __float_as_uint(sum));
     }
     MOE_STAMP(3)
+    // the normalised input and its fragments, while the other CTAs' logits
+    // arrive
+    if (norm) {
+      float4 *xf4 = reinterpret_cast<float4 *>(xf);
+#pragma unroll
+      for (int k = 0; k < 4; k++) {
+        const int i = tid + k * NT;
+        if (i < n4) {
+          const float r = rs[i / h4];
+          float4 q = xf4[i];
+          q.x *= r, q.y *= r, q.z *= r, q.w *= r;
+          xf4[i] = q;
+        }
+      }
+    }
+    __syncthreads();
+    stage_frags<AB>(xf, H, nb, xa, xs, cs);
+    if (AB != 4 && hs) stage_frags<4>(xf, H, nb, xa4, nullptr, cs4);
+    MOE_STAMP(2)
     // ---- lookahead: this CTA's rows of the next layer's router on this
     // layer's input, published for the prediction of the next layer's
     // experts (rows split over the CTAs as the exact ones are; one pass of
@@ -1162,8 +1182,14 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     MOE_STAMP(9)
     if (warp == 0) {
       union_warp(sidx, sw, nb, K, uni, wm, posof, reinterpret_cast<int *>(red), sflag + 1);
-      place_union(uni, wm, eaddr_s, L.etier ? et_s : nullptr, L.cut_w, sflag[1], stier + s.hsi, sflag + 2);
-      if (lane == 0 && s.hsi) stier[0] = 0;  // the shared expert's record is in device memory
+      if (absent[0] || L.etier || L.cut_w > 0.f) {
+        place_union(uni, wm, eaddr_s, L.etier ? et_s : nullptr, L.cut_w, sflag[1], stier + s.hsi, sflag + 2);
+        if (lane == 0 && s.hsi) stier[0] = 0;  // the shared expert's record is in device memory
+      } else {
+        // every record in device memory on this GPU, none cut: the union as it is
+        for (int j = lane; j < 64; j += 32) stier[j] = 0;
+        if (lane == 0) sflag[2] = sflag[1], sflag[3] = sflag[1];
+      }
     }
     __syncthreads();
     MOE_STAMP(10)
@@ -1199,6 +1225,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
         for (int j = tid; j < nb * E; j += NT) P.logits_out[j] = lg[(j / E) * E1 + j % E];
     }
     if (P.route_only) {
+      if (tid == 0) absent[0] = 0;
       __syncthreads();  // eaddr_s is rewritten at the top of the next layer
       continue;
     }
@@ -1402,7 +1429,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ F
     // done: the prefetches overlap the wait for the next layer's input and
     // its routing
     if (LA && lookahead_on(P, l, G)) lookahead_step(P, l, lg, E1, sidx, sw, posof, red);
-    if (tid == 0) sflag[9] = 0;  // the next layer's unit counter (read after several barriers)
+    if (tid == 0) sflag[9] = 0, absent[0] = 0;  // the next layer's unit counter and absent flag
     qbase += (unsigned)n;
     MOE_STAMP(7)
 #undef MOE_STAMP
@@ -1427,7 +1454,7 @@ static int fixed_smem(int H, int E, int I, int nb, int bits) {
   b += ((E + 1) & ~1) * 8;                         // expert addresses
   b += 2 * kMaxStages * 4;                         // last unit issued per stage, stage last filled by cp.async
   b += E * 4;                                      // union scratch
-  b += 2 * 64 * 4 + 2 * ((E + 15) & ~15);          // slot widths and tiers, expert widths and tiers
+  b += 2 * 64 * 4 + 16 + 2 * ((E + 15) & ~15);     // slot widths and tiers, layer flags, expert widths and tiers
   return b;
 }
 
