@@ -129,8 +129,9 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 // Persistent, warp-specialised: one CTA per SM walks tiles blockIdx.x,
 // blockIdx.x + gridDim.x, ... of a 128 x N output tile list (N <= 256 for
 // the router, <= kPfTileN for the expert GEMMs); K goes in stages of 64.
-// B (token rows) passes through a ring of kSB 128B-swizzled shared-memory
-// stages.  The expert GEMMs' A (dequantized weight rows) passes through a
+// B (token rows) passes through a ring of 128B-swizzled shared-memory
+// stages (router: six of 128 rows; expert GEMMs: three of up to 384 rows,
+// so that a full-width tile takes two k-panels per stage and handshake).  The expert GEMMs' A (dequantized weight rows) passes through a
 // ring of kSA stages in tensor memory, kPA k-panels of 32 columns each (row r in TMEM lane
 // r, bf16 pairs along k), and feeds tcgen05.mma from there; the router's A
 // (bf16 rows of R) comes by TMA into shared memory beside its B.
@@ -151,7 +152,8 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 // MOE_ETIMEOUT in *status and its role stops, so the CTA ends.
 
 constexpr int kWsThreads = 448;
-constexpr int kSB = 6;                     // B stages (shared memory)
+constexpr int kSB = 6;                     // B stages (shared memory), at most
+constexpr int kStageRows = 2 * kPfTileN;   // token rows of one expert-GEMM B stage (k-panels of 128 bytes)
 constexpr int kSA = 2;                     // A stages (tensor memory; expert GEMMs)
 constexpr int kPA = 2;                     // k-panels per A stage (one handshake per two panels)
 constexpr int kAccCols = 192;              // TMEM columns of one accumulator (expert GEMMs; N <= 192)
@@ -165,14 +167,16 @@ constexpr int kNStg = 3;                   // staged chunks: one being read, two
 constexpr int kEpiBytes = 16384;           // down: 4 warps x 32 x 32 fp32; gate_up: h rows
 
 // Shared-memory layout of one pf_gemm instantiation (offsets 1024-aligned
-// where the 128B swizzle needs it).  Router: kSB stages of A (128 router
-// rows) and B (128 token rows).  Expert GEMMs: kSB stages of B (up to
-// kPfTileN token rows) and the staged code chunks; A lives in TMEM.
+// where the 128B swizzle needs it).  Router: six stages of A (128 router
+// rows) and B (128 token rows).  Expert GEMMs: three stages of B (up to
+// kStageRows token rows: one or more k-panels of a tile) and the staged
+// code chunks; A lives in TMEM.
 template <int MODE>
 struct Lay {
-  static constexpr int stageB = MODE == MODE_ROUTER ? 128 * 128 : kPfTileN * 128;
-  static constexpr int offA = kSB * stageB;
-  static constexpr int offStg = offA + (MODE == MODE_ROUTER ? kSB * 128 * 128 : 0);
+  static constexpr int nSB = MODE == MODE_ROUTER ? kSB : 3;
+  static constexpr int stageB = MODE == MODE_ROUTER ? 128 * 128 : kStageRows * 128;
+  static constexpr int offA = nSB * stageB;
+  static constexpr int offStg = offA + (MODE == MODE_ROUTER ? nSB * 128 * 128 : 0);
   static constexpr int offEpi = offStg + (MODE == MODE_ROUTER ? 0 : kNStg * kStgBuf);
   static constexpr int offTile = offEpi + kEpiBytes;
   static constexpr int offBars = offTile + 2 * kPfTileN * 4;
@@ -228,7 +232,7 @@ __device__ __forceinline__ int panel_rows(int N) { return (N & ~127) + (((N & 12
 __device__ __forceinline__ int panels_per_stage(int N, int nk) {
   const int r = panel_rows(N);
   for (int p = 4; p > 1; p >>= 1)
-    if (p * r <= kPfTileN && nk % p == 0) return p;
+    if (p * r <= kStageRows && nk % p == 0) return p;
   return 1;
 }
 
@@ -408,7 +412,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
   auto tile_of = [&](int lt) { return (int)blockIdx.x + lt * (int)gridDim.x; };
 
   if (tid == 0) {
-    for (int s = 0; s < kSB; s++) {
+    for (int s = 0; s < LY::nSB; s++) {
       mbar_init(&B.full_b[s], 1);
       mbar_init(&B.empty_b[s], 1);
     }
@@ -498,7 +502,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
             if (tc05::elect_one()) tc05::commit(&B.empty_b[sb]);
             __syncwarp();
             pp = 0;
-            if (++sb == kSB) sb = 0, pb ^= 1;
+            if (++sb == LY::nSB) sb = 0, pb ^= 1;
           }
         }
         if (ok) {
@@ -530,8 +534,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       const CUtensorMap *m32 = MODE == MODE_GATE_UP ? &P.tm_xc32 : &P.tm_h32;
       const int ent = P.t * (P.K + 1);  // rows of one k-panel of xc / h
       for (int kk = 0; kk < nk; kk += ppb, f++) {
-        const int s = f % kSB;
-        if (!warp_wait(&B.empty_b[s], (uint32_t)(((f / kSB) & 1) ^ 1), P)) {
+        const int s = f % LY::nSB;
+        if (!warp_wait(&B.empty_b[s], (uint32_t)(((f / LY::nSB) & 1) ^ 1), P)) {
           ok = false;
           break;
         }
@@ -563,7 +567,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
     // every stage (after a timeout the consumer may have stopped early, so
     // the earlier stages' copies need not have been waited for)
     if (lane == 0)
-      for (int g = f > kSB ? f - kSB : 0; g < f; g++) pf_wait(&B.full_b[g % kSB], (uint32_t)((g / kSB) & 1), P);
+      for (int g = f > LY::nSB ? f - LY::nSB : 0; g < f; g++)
+        pf_wait(&B.full_b[g % LY::nSB], (uint32_t)((g / LY::nSB) & 1), P);
     __syncwarp();
   } else if (warp < 10) {
     // ---------------------------------------------------------------- A producers
