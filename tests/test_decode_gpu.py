@@ -213,6 +213,40 @@ def test_c1_teacher_forced_layer(moe, c1, layer):
     print(f"[parity] c1 teacher-forced layer {layer}: max err = {r:.4f} of the bound")
 
 
+def test_traced_call_matches_and_stamps(moe):
+    """moe_forward_traced computes what moe_forward computes, bit for bit,
+    and stamps every CTA's phases of every layer in program order: the layer
+    start, the input available, the logits read and the layer's end; CTAs
+    past the grid leave their rows zero."""
+    rng = np.random.default_rng(760)
+    nl, H, E, k, I, nb = 3, 512, 16, 4, 256, 2
+    layers = [synth.make_layer(rng, H, E, k, I, 4, shared=True, flags=synth.RESIDUAL | synth.PRENORM)
+              for _ in range(nl)]
+    dl = moe.DeviceLayers(layers)
+    x = synth.make_x(np.random.default_rng(761), nb, H)
+    base = run_forward(moe, dl, x)
+    xt = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).cuda()
+    out = torch.empty_like(xt)
+    ws = moe.alloc_workspace(moe.forward_workspace(dl.c, nb, nl))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    trace = torch.zeros((nl, 1024, 16), dtype=torch.int64, device="cuda")
+    moe.forward_traced(dl, xt, out, ws, status, trace)
+    torch.cuda.synchronize()
+    assert status.item() == 0, moe.STATUS_NAMES.get(status.item())
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), base["out"].view(np.uint32))
+    t = trace.cpu().numpy()
+    G = int((t[0, :, 0] > 0).sum())
+    assert 1 <= G <= 160
+    assert (t[:, :G, 0] > 0).all() and (t[:, G:, :] == 0).all()
+    for l in range(nl):
+        start, avail, lgt, done = (t[l, :G, ph] for ph in (0, 1, 4, 7))
+        assert (avail >= start).all() and (lgt >= avail).all() and (done >= lgt).all(), f"layer {l}"
+        if l + 1 < nl:
+            # no CTA has the next layer's input before some CTA finished this layer
+            assert t[l + 1, :G, 1].min() >= done.min(), f"layer {l + 1}"
+    print(f"[trace] {nl} layers x {G} CTAs stamped; outputs equal the untraced call")
+
+
 def test_bounded_wait_reports_timeout(moe):
     """A wait that can never be satisfied gives up within the limit and the
     kernel reports MOE_ETIMEOUT; the context stays usable afterwards."""

@@ -322,3 +322,36 @@ def test_prefill_c4_group(moe, c4):
     assert np.array_equal(g["rows"], ref["rows"])
     assert np.allclose(g["wts"][:-x.shape[0]], ref["wts"][:-x.shape[0]], rtol=0, atol=0), "routed weights placed"
     assert np.allclose(g["wts"][-x.shape[0]:], r["gamma"], rtol=0, atol=1e-6), "shared gate"
+
+
+def test_prefill_timed_matches_prefill(moe):
+    """moe_prefill_timed runs the same kernels as moe_prefill (the same ids;
+    the same bf16 output up to one ulp, since the down GEMM's scatter adds in
+    fp32 in whatever order its tiles finish) and records its events around
+    each of them, in order: the per-kernel times add up to the whole call."""
+    rng = np.random.default_rng(880)
+    H, E, k, I, t = 512, 16, 4, 256, 300
+    layer = synth.make_layer(rng, H, E, k, I, 4, shared=True, flags=synth.RESIDUAL)
+    dl = moe.DeviceLayers([layer])
+    x = rng.normal(size=(t, H)).astype(np.float32)
+    o_ref, idx_ref = run_prefill(moe, dl, x)
+    xt = torch.from_numpy(x).cuda()
+    out = torch.empty((t, H), dtype=torch.int16, device="cuda")
+    idx = torch.zeros((t, k), dtype=torch.int32, device="cuda")
+    ws = moe.alloc_workspace(moe.prefill_workspace(dl, t))
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(moe.PREFILL_KERNELS + 1)]
+    for e in evs:
+        e.record(stream)
+    torch.cuda.synchronize()
+    moe.prefill_timed(dl, xt, out, ws, status, evs, idx, stream=stream)
+    torch.cuda.synchronize()
+    assert status.item() == 0, moe.STATUS_NAMES.get(status.item())
+    o = synth.bf16_bits_to_f32(out.cpu().numpy().view(np.uint16)).astype(np.float64)
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
+    assert (np.abs(o - o_ref) <= bf16_ulp(o_ref)).all()
+    parts = [evs[j].elapsed_time(evs[j + 1]) for j in range(moe.PREFILL_KERNELS)]
+    total = evs[0].elapsed_time(evs[-1])
+    assert all(p >= 0 for p in parts) and abs(sum(parts) - total) <= 1e-3 * max(total, 1.0)
+    print(f"[prefill] timed call: {moe.PREFILL_KERNELS} kernels, {total * 1e3:.1f} us, outputs equal the plain call")
