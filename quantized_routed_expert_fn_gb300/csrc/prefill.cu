@@ -130,19 +130,24 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 // blockIdx.x + gridDim.x, ... of a 128 x N output tile list (N <= 256 for
 // the router, <= kPfTileN for the expert GEMMs); K goes in stages of 64.
 // B (token rows) passes through a ring of 128B-swizzled shared-memory
-// stages (router: six of 128 rows; expert GEMMs: three of up to 384 rows,
-// so that a full-width tile takes two k-panels per stage and handshake).  The expert GEMMs' A (dequantized weight rows) passes through a
-// ring of kSA stages in tensor memory, kPA k-panels of 32 columns each (row r in TMEM lane
-// r, bf16 pairs along k), and feeds tcgen05.mma from there; the router's A
-// (bf16 rows of R) comes by TMA into shared memory beside its B.
+// stages (router: six of 128 rows; expert GEMMs: three of up to 320 rows,
+// so that a full-width tile takes two k-panels per stage and handshake).
+// The expert GEMMs' A (dequantized weight rows) passes through a ring of
+// kSA = 3 stages in tensor memory, kPA = 2 k-panels of 32 columns each (row
+// r in TMEM lane r, bf16 pairs along k), and feeds tcgen05.mma from there;
+// tensor memory holds three such stages beside the two accumulators when a
+// tile is at most 160 tokens wide.  The router's A (bf16 rows of R) comes by
+// TMA into shared memory beside its B.
 //   warp 0      lane 0 issues the tcgen05 MMAs of a stage once its operands
 //               have landed and commits them (stage free / accumulator full)
 //   warp 1      TMA: B rows (and the router's A rows) of each stage
 //   warps 2-9   A producers: all 256 threads stage the codes of four
 //               k-panels (128 rows x 128 bytes, plus scale / bias words)
 //               into shared memory with coalesced cp.async, three chunks in
-//               the air; an A stage holds kPA = 2 panels, and a chunk's two
-//               A stages go to the two groups of four warps (w - 2) / 4:
+//               the air (two for 2- and 3-bit codes); a chunk's two A
+//               stages go to the two groups of four warps (w - 2) / 4, and
+//               with three stages in the ring a group's next stage was read
+//               by the MMAs three stages back, not two:
 //               warp w fills rows 32 (w % 4) .. +31 -- the TMEM lanes it may
 //               write -- 64 codes a panel, stored as 32 bf16 pairs per panel
 //               with tcgen05.st
@@ -154,16 +159,16 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 constexpr int kWsThreads = 448;
 constexpr int kSB = 6;                     // B stages (shared memory), at most
 constexpr int kStageRows = 2 * kPfTileN;   // token rows of one expert-GEMM B stage (k-panels of 128 bytes)
-constexpr int kSA = 2;                     // A stages (tensor memory; expert GEMMs)
+constexpr int kSA = 3;                     // A stages (tensor memory; expert GEMMs)
 constexpr int kPA = 2;                     // k-panels per A stage (one handshake per two panels)
-constexpr int kAccCols = 192;              // TMEM columns of one accumulator (expert GEMMs; N <= 192)
+constexpr int kAccCols = 160;              // TMEM columns of one accumulator (expert GEMMs; N <= 160)
 constexpr int kTmemA = 2 * kAccCols;       // first TMEM column of the A ring: kSA x kPA x 32 columns
 static_assert(kTmemA + 32 * kPA * kSA <= 512, "tensor memory");
 constexpr int kChunk = 4;                  // k-stages per staged chunk of codes
 constexpr int kStgCodes = 128 * 128;       // 128 rows x 128 bytes of codes (4 stages)
 constexpr int kStgSB = 128 * kChunk * 8;   // per row and stage: scale word, bias word
 constexpr int kStgBuf = kStgCodes + kStgSB;
-constexpr int kNStg = 3;                   // staged chunks: one being read, two in flight
+constexpr int kNStg = 4;                   // staged chunks at most: one being read, the rest in flight
 constexpr int kEpiBytes = 16384;           // down: 4 warps x 32 x 32 fp32; gate_up: h rows
 
 // Shared-memory layout of one pf_gemm instantiation (offsets 1024-aligned
@@ -577,6 +582,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       // r = 32 * (warp % 4) + lane (the TMEM lanes its warp may write); warp
       // group hf fills the chunk's A stage hf (k-panels 2hf, 2hf + 1)
       const int t = tid - 64, r = 32 * (warp & 3) + lane, hf = (warp - 2) >> 2;
+      // staging depth: four chunks for 4-bit records; the funnel-shift
+      // dequant of narrower ones ran slower with the fourth (measured)
+      constexpr int NStg = LB ? 3 : kNStg;
       const int nct = (nk + kChunk - 1) / kChunk;  // chunks per tile
       const int total = my_tiles * nct;
       const int inp = MODE == MODE_GATE_UP ? P.H : P.I;
@@ -598,20 +606,19 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
           slt = lt;
           if (lt + 1 < my_tiles) snext = ws_item<MODE>(P, tile_of(lt + 1));
         }
-        stage_chunk(srow, c - lt * nct, nk, t, stg + (c % kNStg) * kStgBuf);
+        stage_chunk(srow, c - lt * nct, nk, t, stg + (c % NStg) * kStgBuf);
       };
-      issue(0);
-      issue(1);
+      for (int c = 0; c < NStg - 1; c++) issue(c);
       // parity of the weight row = parity of r (tile row bases are even)
       const uint32_t rodd = (uint32_t)(r & (inp / 64) & 1);
       int qlt = -1, qbits = 4;  // the tile being dequantized and its code width
       bool ok = true;
       for (int c = 0; c < total && ok; c++) {
-        tc05::cp_wait_group<1>();  // this thread's copies of chunk c are done
+        tc05::cp_wait_group<NStg - 2>();  // this thread's copies of chunk c are done
         tc05::named_sync(3, 256);  // everyone's are; everyone is done reading chunk c - 1
-        issue(c + 2);
+        issue(c + NStg - 1);
         const int lt = c / nct, kc = c - lt * nct;
-        const uint8_t *buf = stg + (c % kNStg) * kStgBuf;
+        const uint8_t *buf = stg + (c % NStg) * kStgBuf;
         const int ns = min(kChunk, nk - kc * kChunk);
         if (LB && lt != qlt) qbits = item_bits<LB>(P, ws_item<MODE>(P, tile_of(lt))), qlt = lt;
         const int u0 = kPA * hf;  // this group's A stage of the chunk, if the chunk has it

@@ -14,7 +14,7 @@ struct PfItem {
   uint64_t rec;         // the group's record address
 };
 
-constexpr int kPfTileN = 192;  // token columns per tensor-core tile
+constexpr int kPfTileN = 160;  // token columns per tensor-core tile
 constexpr int kPfChunk = 32;   // tokens per chunk of the stable grouping
 
 struct PfParams {
