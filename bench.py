@@ -547,12 +547,17 @@ def run_prefill(args, rank, world, device):
     torch.cuda.synchronize()
     ev0.record(stream)
     for i in range(args.steps):
-        moe.prefill_timed(dl, x, out, ws, status, sets[i], idx, stream=stream)
+        moe.prefill(dl, x, out, ws, status, idx, stream=stream)
     ev1.record(stream)
     torch.cuda.synchronize()
     if dist:
         td.barrier()
     ms = ev0.elapsed_time(ev1) / args.steps
+    # per-kernel device times: the same steps again, an event before each kernel
+    # (the events' own gaps stay out of the step time above)
+    for i in range(args.steps):
+        moe.prefill_timed(dl, x, out, ws, status, sets[i], idx, stream=stream)
+    torch.cuda.synchronize()
     clocks = sampler.stop() if sampler else None
     if status.item() != 0:
         raise RuntimeError(f"device status {moe.STATUS_NAMES.get(status.item())}")

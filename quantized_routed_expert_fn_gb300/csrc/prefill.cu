@@ -782,56 +782,73 @@ __device__ __forceinline__ uint32_t orderable_f(float f) {
   const uint32_t u = __float_as_uint(f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// its inverse: the float a key was made from (bit for bit)
+__device__ __forceinline__ float from_orderable(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
 
-// Warp per token: top-k (ties to the lower id) of E <= 1024 logits, softmax
-// over the k chosen, per-(chunk, expert) counts.  Lane l holds experts
-// l, l + 32, ... (coalesced loads); each round takes the largest key, and
-// among equal keys the lowest expert id.
-__global__ void pf_topk(const __grid_constant__ PfParams P) {
-  const int lane = threadIdx.x & 31;
-  const int tok = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (tok >= P.t) return;
-  const int E = P.E, K = P.K;
-  const float *lg = P.logits + (size_t)tok * E;
-  uint32_t key[32];
+// One block per chunk of kPfChunk tokens, 16 warps of two tokens each:
+// top-k (ties to the lower id) of E <= 1024 logits and softmax over the k
+// chosen, per token; then the chunk's per-expert counts, gathered in a
+// shared-memory histogram and stored once per expert (chist[e][chunk]), so
+// that a popular expert's counter is not a global atomic every token hits.
+// Lane l holds experts l, l + 32, ... (coalesced loads); each round takes
+// the largest key, and among equal keys the lowest expert id.
+// PM: keys per lane (E <= 32 PM).
+constexpr int kTopkThreads = 512;
+template <int PM>
+__global__ void __launch_bounds__(kTopkThreads) pf_topk(const __grid_constant__ PfParams P) {
+  extern __shared__ int hist[];  // [E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, c = blockIdx.x;
+  const int E = P.E, K = P.K, nch = (P.t + kPfChunk - 1) / kPfChunk;
+  for (int e = threadIdx.x; e < E; e += kTopkThreads) hist[e] = 0;
+  __syncthreads();
+  for (int j = 0; j < kPfChunk * 32 / kTopkThreads; j++) {
+    const int tok = c * kPfChunk + j * (kTopkThreads / 32) + warp;
+    if (tok >= P.t) break;  // warp-uniform
+    const float *lg = P.logits + (size_t)tok * E;
+    uint32_t key[PM];
 #pragma unroll
-  for (int i = 0; i < 32; i++) {
-    const int e = i * 32 + lane;
-    key[i] = e < E ? orderable_f(lg[e]) : 0u;
-  }
-  uint32_t bk = 0;
-  int bi = 0;
+    for (int i = 0; i < PM; i++) {
+      const int e = i * 32 + lane;
+      key[i] = e < E ? orderable_f(lg[e]) : 0u;
+    }
+    uint32_t bk = 0;
+    int bi = 0;
 #pragma unroll
-  for (int i = 0; i < 32; i++)
-    if (key[i] > bk) bk = key[i], bi = i;
-  float myl = 0.f;
-  int myid = 0;
-  for (int r = 0; r < K; r++) {
-    const uint32_t m = __reduce_max_sync(FULLM, bk);
-    const uint32_t id = __reduce_min_sync(FULLM, bk == m ? (uint32_t)(bi * 32 + lane) : 0xffffffffu);
-    if (lane == r) myid = (int)id, myl = lg[id];
-    if (lane == (int)(id & 31)) {
-      uint32_t nbk = 0;
-      int nbi = 0;
+    for (int i = 0; i < PM; i++)
+      if (key[i] > bk) bk = key[i], bi = i;
+    float myl = 0.f;
+    int myid = 0;
+    for (int r = 0; r < K; r++) {
+      const uint32_t m = __reduce_max_sync(FULLM, bk);
+      const uint32_t id = __reduce_min_sync(FULLM, bk == m ? (uint32_t)(bi * 32 + lane) : 0xffffffffu);
+      if (lane == r) myid = (int)id, myl = from_orderable(m);  // the logit, from its key (no load)
+      if (lane == (int)(id & 31)) {
+        uint32_t nbk = 0;
+        int nbi = 0;
 #pragma unroll
-      for (int i = 0; i < 32; i++) {
-        if (i == bi) key[i] = 0u;
-        if (key[i] > nbk) nbk = key[i], nbi = i;
+        for (int i = 0; i < PM; i++) {
+          if (i == bi) key[i] = 0u;
+          if (key[i] > nbk) nbk = key[i], nbi = i;
+        }
+        bk = nbk, bi = nbi;
       }
-      bk = nbk, bi = nbi;
+    }
+    const float mx = __shfl_sync(FULLM, myl, 0);
+    const float ev = lane < K ? expf(myl - mx) : 0.f;
+    const float z = warp_sum_f(ev);
+    if (lane < K) {
+      const float w = ev / z;
+      P.tk_idx[(size_t)tok * K + lane] = myid;
+      P.tk_w[(size_t)tok * K + lane] = w;
+      if (P.topk_out) P.topk_out[(size_t)tok * K + lane] = (uint32_t)myid;
+      if (P.topkw_out) P.topkw_out[(size_t)tok * K + lane] = w;
+      atomicAdd(&hist[myid], 1);
     }
   }
-  const float mx = __shfl_sync(FULLM, myl, 0);
-  const float ev = lane < K ? expf(myl - mx) : 0.f;
-  const float z = warp_sum_f(ev);
-  if (lane < K) {
-    const float w = ev / z;
-    P.tk_idx[(size_t)tok * K + lane] = myid;
-    P.tk_w[(size_t)tok * K + lane] = w;
-    if (P.topk_out) P.topk_out[(size_t)tok * K + lane] = (uint32_t)myid;
-    if (P.topkw_out) P.topkw_out[(size_t)tok * K + lane] = w;
-    atomicAdd(&P.chist[(size_t)myid * ((P.t + kPfChunk - 1) / kPfChunk) + tok / kPfChunk], 1);
-  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kTopkThreads) P.chist[(size_t)e * nch + c] = hist[e];
 }
 
 // Block-wide exclusive scan (blockDim.x == 1024) of one int per thread.
@@ -943,20 +960,34 @@ __global__ void pf_fill(const __grid_constant__ PfParams P) {
   for (int e = lane; e < E; e += 32) cnt[e] = P.offs[e] + P.chist[(size_t)e * nch + c];
   __syncwarp();
   const int t0 = c * kPfChunk, t1 = min(P.t, t0 + kPfChunk);
-  for (int i0 = t0 * K; i0 < t1 * K; i0 += 32) {
-    const int i = i0 + lane;
-    const bool v = i < t1 * K;
-    const int e = v ? P.tk_idx[i] : -1;
-    const unsigned peers = __match_any_sync(FULLM, e);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const int base = v ? cnt[e] : 0;
-    __syncwarp();
-    if (v) {
-      P.rows[base + rank] = i / K;
-      P.wts[base + rank] = P.tk_w[i];
-      if (rank == 0) cnt[e] = base + __popc(peers);
+  // the chunk's (token, expert) pairs, eight rounds of 32 loaded at once
+  for (int b0 = t0 * K; b0 < t1 * K; b0 += 8 * 32) {
+    int ev[8];
+    float wv[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const int i = b0 + j * 32 + lane;
+      const bool v = i < t1 * K;
+      ev[j] = v ? P.tk_idx[i] : -1;
+      wv[j] = v ? P.tk_w[i] : 0.f;
     }
-    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      if (b0 + j * 32 >= t1 * K) break;  // warp-uniform
+      const int i = b0 + j * 32 + lane;
+      const bool v = i < t1 * K;
+      const int e = ev[j];
+      const unsigned peers = __match_any_sync(FULLM, e);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int base = v ? cnt[e] : 0;
+      __syncwarp();
+      if (v) {
+        P.rows[base + rank] = i / K;
+        P.wts[base + rank] = wv[j];
+        if (rank == 0) cnt[e] = base + __popc(peers);
+      }
+      __syncwarp();
+    }
   }
   if (P.sgate) {
     const int o = P.offs[E];
@@ -1102,7 +1133,6 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   const size_t ent_cap = (size_t)t * (p.K + 1);
   cudaError_t e;
   auto mark = [&](int i) { return events ? cudaEventRecord(events[i], st) : cudaSuccess; };
-  if ((e = cudaMemsetAsync(p.chist, 0, (size_t)nch * p.E * 4, st))) return e;
   if ((e = cudaMemsetAsync(p.status, 0, 4, st))) return e;
   if (!p.route_only && (e = cudaMemsetAsync(p.Y, 0, (size_t)t * p.H * 4, st))) return e;
   if ((e = cudaFuncSetAttribute(pf_gemm<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1126,7 +1156,14 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if ((e = mark(1))) return e;
   pf_gemm<MODE_ROUTER><<<g_router, kWsThreads, Lay<MODE_ROUTER>::smem, st>>>(p);
   if ((e = mark(2))) return e;
-  pf_topk<<<(t + 7) / 8, 256, 0, st>>>(p);
+  if (p.E <= 128)
+    pf_topk<4><<<nch, kTopkThreads, (size_t)p.E * 4, st>>>(p);
+  else if (p.E <= 256)
+    pf_topk<8><<<nch, kTopkThreads, (size_t)p.E * 4, st>>>(p);
+  else if (p.E <= 512)
+    pf_topk<16><<<nch, kTopkThreads, (size_t)p.E * 4, st>>>(p);
+  else
+    pf_topk<32><<<nch, kTopkThreads, (size_t)p.E * 4, st>>>(p);
   if ((e = mark(3))) return e;
   pf_group_count<<<(p.E + 7) / 8, 256, 0, st>>>(p);
   if ((e = mark(4))) return e;
