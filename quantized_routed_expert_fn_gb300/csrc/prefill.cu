@@ -904,15 +904,12 @@ __global__ void pf_group_count(const __grid_constant__ PfParams P) {
 
 // One block of 1024 threads.  Groups: the experts, then the shared expert
 // with every token.  Exclusive scans of the group sizes and of their
-// kPfTileN-token chunk counts give the group offsets and the tile work lists
-// (one item per thread).
+// kPfTileN-token chunk counts give the group offsets and the chunk offsets
+// (the tile work lists are written from them by pf_fill's blocks).
 __global__ void __launch_bounds__(1024) pf_group(const __grid_constant__ PfParams P) {
   __shared__ int s_off[1027], s_ch[1027], sh[32];
-  __shared__ uint64_t s_rec[1025];
   const int E = P.E, G = E + (P.sgate ? 1 : 0);
   const int nmt1 = P.I / 64, nmt2 = P.H / 128;
-  for (int g = threadIdx.x; g < G; g += blockDim.x)
-    s_rec[g] = g < E ? P.eaddr[g] : reinterpret_cast<uint64_t>(P.srec);
   int m2[2], c2[2];
 #pragma unroll
   for (int u = 0; u < 2; u++) {
@@ -937,24 +934,20 @@ __global__ void __launch_bounds__(1024) pf_group(const __grid_constant__ PfParam
   }
   __syncthreads();
   for (int g = threadIdx.x; g <= G; g += blockDim.x) P.offs[g] = s_off[g];
-  auto item = [&](int cc, int mt) {  // cc: global chunk index
-    int lo = 0, hi = G;              // the last group g with s_ch[g] <= cc (it holds chunk cc)
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_ch[mid] <= cc) lo = mid; else hi = mid;
-    }
-    const int g = lo, c = cc - s_ch[g], m = s_off[g + 1] - s_off[g];
-    return PfItem{g, mt, s_off[g] + c * kPfTileN, min(kPfTileN, m - c * kPfTileN), s_rec[g]};
-  };
-  for (int i = threadIdx.x; i < tot_ch * nmt1; i += blockDim.x) P.items1[i] = item(i / nmt1, i % nmt1);
-  for (int i = threadIdx.x; i < tot_ch * nmt2; i += blockDim.x) P.items2[i] = item(i / nmt2, i % nmt2);
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) P.choff[g] = s_ch[g];
 }
 
 // One warp per chunk of kPfChunk tokens: the chunk's (token, expert) pairs in
 // token order get consecutive places in their experts' lists, so every list
 // is in ascending token order.  Shared group: every token, weight = gate.
+// Then block c writes its share of the two GEMMs' tile work lists (item
+// cc * nmt + mt: chunk cc of its group, row tile mt), each chunk's group
+// found by a binary search over the chunk offsets.
 __global__ void pf_fill(const __grid_constant__ PfParams P) {
-  extern __shared__ int cnt[];  // [E] next place of each expert for this chunk
+  extern __shared__ uint64_t fsm[];  // [G + 1] group records, then int [E] cnt, [G + 1] chunk and row offsets
+  const int G = P.E + (P.sgate ? 1 : 0);
+  uint64_t *srec = fsm;
+  int *cnt = reinterpret_cast<int *>(srec + G + 1);  // [E] next place of each expert for this chunk
   const int E = P.E, K = P.K, c = blockIdx.x, lane = threadIdx.x;
   const int nch = (P.t + kPfChunk - 1) / kPfChunk;
   for (int e = lane; e < E; e += 32) cnt[e] = P.offs[e] + P.chist[(size_t)e * nch + c];
@@ -996,14 +989,53 @@ __global__ void pf_fill(const __grid_constant__ PfParams P) {
       P.wts[o + tok] = P.gam[tok];
     }
   }
+  int *sch = cnt + E, *soff = sch + G + 1;
+  for (int g = lane; g <= G; g += 32) {
+    srec[g] = g < E ? P.eaddr[g] : (g == E ? reinterpret_cast<uint64_t>(P.srec) : 0ull);
+    sch[g] = P.choff[g];
+    soff[g] = P.offs[g];
+  }
+  __syncwarp();
+  const int nmt1 = P.I / 64, nmt2 = P.H / 128, n1 = P.nitems[0], total = n1 + P.nitems[1];
+  const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x, j1 = min(total, (c + 1) * per);
+  for (int j = c * per + lane; j < j1; j += 32) {
+    const bool first = j < n1;
+    const int i = first ? j : j - n1, nmt = first ? nmt1 : nmt2;
+    const int cc = i / nmt, mt = i - cc * nmt;
+    int lo = 0, hi = G;  // the last group g with sch[g] <= cc holds chunk cc
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (sch[mid] <= cc) lo = mid; else hi = mid;
+    }
+    const int g = lo, ch = cc - sch[g], m = soff[g + 1] - soff[g];
+    (first ? P.items1 : P.items2)[i] =
+        PfItem{g, mt, soff[g] + ch * kPfTileN, min(kPfTileN, m - ch * kPfTileN), srec[g]};
+  }
 }
 
+// out = bf16(Y (+ x)): four elements a thread per step when out is 8-byte
+// aligned (x and Y always are; H is a multiple of 128), else one.
 __global__ void pf_final(const __grid_constant__ PfParams P) {
-  const size_t n = (size_t)P.t * P.H;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-    float y = P.Y[i];
-    if (P.flags & kResidualF) y += P.x[i];
-    P.out[i] = (uint16_t)f2bf_rn(y);
+  const size_t n = (size_t)P.t * P.H, stride = (size_t)gridDim.x * blockDim.x;
+  const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool res = (P.flags & kResidualF) != 0;
+  if ((reinterpret_cast<uintptr_t>(P.out) & 7u) == 0) {
+    const float4 *y4 = reinterpret_cast<const float4 *>(P.Y), *x4 = reinterpret_cast<const float4 *>(P.x);
+    uint2 *o2 = reinterpret_cast<uint2 *>(P.out);
+    for (size_t i = i0; i < n / 4; i += stride) {
+      float4 y = y4[i];
+      if (res) {
+        const float4 r = x4[i];
+        y.x += r.x, y.y += r.y, y.z += r.z, y.w += r.w;
+      }
+      o2[i] = make_uint2(f2bf_rn(y.x) | f2bf_rn(y.y) << 16, f2bf_rn(y.z) | f2bf_rn(y.w) << 16);
+    }
+  } else {
+    for (size_t i = i0; i < n; i += stride) {
+      float y = P.Y[i];
+      if (res) y += P.x[i];
+      P.out[i] = (uint16_t)f2bf_rn(y);
+    }
   }
 }
 
@@ -1038,6 +1070,7 @@ void carve(int H, int E, int K, int I, int t, F &&take) {
   take(14, ent * I * 2);         // hbuf
   take(15, (size_t)t * H * 4);   // Y
   take(16, ent * H * 2);         // xc
+  take(18, (size_t)(E + 3) * 4); // choff
 }
 
 }  // namespace
@@ -1051,7 +1084,7 @@ size_t pf_workspace_bytes(int H, int E, int K, int I, int t) {
 void pf_carve(PfParams &p, void *work) {
   char *base = reinterpret_cast<char *>(work);
   size_t o = 0;
-  void *ptr[18];
+  void *ptr[19];
   carve(p.H, p.E, p.K, p.I, p.t, [&](int k, size_t n) {
     ptr[k] = base + o;
     o += al(n);
@@ -1074,6 +1107,7 @@ void pf_carve(PfParams &p, void *work) {
   p.Y = (float *)ptr[15];
   p.xc = (uint16_t *)ptr[16];
   p.counts = (int *)ptr[17];
+  p.choff = (int *)ptr[18];
 }
 
 namespace {
@@ -1169,7 +1203,7 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if ((e = mark(4))) return e;
   pf_group<<<1, 1024, 0, st>>>(p);
   if ((e = mark(5))) return e;
-  pf_fill<<<nch, 32, (size_t)p.E * 4, st>>>(p);
+  pf_fill<<<nch, 32, (size_t)(p.E + 2) * 8 + (size_t)(3 * p.E + 6) * 4, st>>>(p);
   if ((e = mark(6))) return e;
   if (!p.route_only) {
     pf_gather<<<(int)((ent_cap + 7) / 8), 256, 0, st>>>(p);

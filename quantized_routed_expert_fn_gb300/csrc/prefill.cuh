@@ -53,6 +53,7 @@ struct PfParams {
   float *tk_w;              // [t][K]
   int *chist;               // [E][nch] per-(expert, token chunk) counts, then their places in the list
   int *counts;              // [E] entries per expert
+  int *choff;               // [E+2] first chunk (kPfTileN tokens) of each group; choff[G] = chunks
   int *offs;                // [E+2] first grouped entry of each group; offs[G] = total
   int *rows;                // [t*(K+1)] token of each grouped entry
   float *wts;               // [t*(K+1)] its weight
