@@ -937,68 +937,75 @@ __global__ void __launch_bounds__(1024) pf_group(const __grid_constant__ PfParam
   for (int g = threadIdx.x; g <= G; g += blockDim.x) P.choff[g] = s_ch[g];
 }
 
-// One warp per chunk of kPfChunk tokens: the chunk's (token, expert) pairs in
-// token order get consecutive places in their experts' lists, so every list
-// is in ascending token order.  Shared group: every token, weight = gate.
-// Then block c writes its share of the two GEMMs' tile work lists (item
+// One block per chunk of kPfChunk tokens; its first warp gives the chunk's
+// (token, expert) pairs, in token order, consecutive places in their
+// experts' lists, so every list is in ascending token order (shared group:
+// every token, weight = gate).  Then block c writes its share of the two
+// GEMMs' tile work lists (item
 // cc * nmt + mt: chunk cc of its group, row tile mt), each chunk's group
 // found by a binary search over the chunk offsets.
-__global__ void pf_fill(const __grid_constant__ PfParams P) {
+constexpr int kFillThreads = 128;
+__global__ void __launch_bounds__(kFillThreads) pf_fill(const __grid_constant__ PfParams P) {
   extern __shared__ uint64_t fsm[];  // [G + 1] group records, then int [E] cnt, [G + 1] chunk and row offsets
   const int G = P.E + (P.sgate ? 1 : 0);
   uint64_t *srec = fsm;
   int *cnt = reinterpret_cast<int *>(srec + G + 1);  // [E] next place of each expert for this chunk
-  const int E = P.E, K = P.K, c = blockIdx.x, lane = threadIdx.x;
-  const int nch = (P.t + kPfChunk - 1) / kPfChunk;
-  for (int e = lane; e < E; e += 32) cnt[e] = P.offs[e] + P.chist[(size_t)e * nch + c];
-  __syncwarp();
-  const int t0 = c * kPfChunk, t1 = min(P.t, t0 + kPfChunk);
-  // the chunk's (token, expert) pairs, eight rounds of 32 loaded at once
-  for (int b0 = t0 * K; b0 < t1 * K; b0 += 8 * 32) {
-    int ev[8];
-    float wv[8];
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-      const int i = b0 + j * 32 + lane;
-      const bool v = i < t1 * K;
-      ev[j] = v ? P.tk_idx[i] : -1;
-      wv[j] = v ? P.tk_w[i] : 0.f;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; j++) {
-      if (b0 + j * 32 >= t1 * K) break;  // warp-uniform
-      const int i = b0 + j * 32 + lane;
-      const bool v = i < t1 * K;
-      const int e = ev[j];
-      const unsigned peers = __match_any_sync(FULLM, e);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      const int base = v ? cnt[e] : 0;
-      __syncwarp();
-      if (v) {
-        P.rows[base + rank] = i / K;
-        P.wts[base + rank] = wv[j];
-        if (rank == 0) cnt[e] = base + __popc(peers);
-      }
-      __syncwarp();
-    }
-  }
-  if (P.sgate) {
-    const int o = P.offs[E];
-    for (int tok = t0 + lane; tok < t1; tok += 32) {
-      P.rows[o + tok] = tok;
-      P.wts[o + tok] = P.gam[tok];
-    }
-  }
-  int *sch = cnt + E, *soff = sch + G + 1;
-  for (int g = lane; g <= G; g += 32) {
+  int *sch = cnt + P.E, *soff = sch + G + 1;
+  const int E = P.E, K = P.K, c = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  // the work-list tables, by every thread (read after the barrier below)
+  for (int g = tid; g <= G; g += kFillThreads) {
     srec[g] = g < E ? P.eaddr[g] : (g == E ? reinterpret_cast<uint64_t>(P.srec) : 0ull);
     sch[g] = P.choff[g];
     soff[g] = P.offs[g];
   }
-  __syncwarp();
+  if (tid < 32) {
+    // warp 0: the chunk's row lists
+    const int nch = (P.t + kPfChunk - 1) / kPfChunk;
+    for (int e = lane; e < E; e += 32) cnt[e] = P.offs[e] + P.chist[(size_t)e * nch + c];
+    __syncwarp();
+    const int t0 = c * kPfChunk, t1 = min(P.t, t0 + kPfChunk);
+    // the chunk's (token, expert) pairs, eight rounds of 32 loaded at once
+    for (int b0 = t0 * K; b0 < t1 * K; b0 += 8 * 32) {
+      int ev[8];
+      float wv[8];
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        const int i = b0 + j * 32 + lane;
+        const bool v = i < t1 * K;
+        ev[j] = v ? P.tk_idx[i] : -1;
+        wv[j] = v ? P.tk_w[i] : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; j++) {
+        if (b0 + j * 32 >= t1 * K) break;  // warp-uniform
+        const int i = b0 + j * 32 + lane;
+        const bool v = i < t1 * K;
+        const int e = ev[j];
+        const unsigned peers = __match_any_sync(FULLM, e);
+        const int rank = __popc(peers & ((1u << lane) - 1u));
+        const int base = v ? cnt[e] : 0;
+        __syncwarp();
+        if (v) {
+          P.rows[base + rank] = i / K;
+          P.wts[base + rank] = wv[j];
+          if (rank == 0) cnt[e] = base + __popc(peers);
+        }
+        __syncwarp();
+      }
+    }
+    if (P.sgate) {
+      const int o = P.offs[E];
+      for (int tok = t0 + lane; tok < t1; tok += 32) {
+        P.rows[o + tok] = tok;
+        P.wts[o + tok] = P.gam[tok];
+      }
+    }
+  }
+  __syncthreads();
+  // every thread: this block's share of the two work lists
   const int nmt1 = P.I / 64, nmt2 = P.H / 128, n1 = P.nitems[0], total = n1 + P.nitems[1];
   const int per = (total + (int)gridDim.x - 1) / (int)gridDim.x, j1 = min(total, (c + 1) * per);
-  for (int j = c * per + lane; j < j1; j += 32) {
+  for (int j = c * per + tid; j < j1; j += kFillThreads) {
     const bool first = j < n1;
     const int i = first ? j : j - n1, nmt = first ? nmt1 : nmt2;
     const int cc = i / nmt, mt = i - cc * nmt;
@@ -1203,7 +1210,7 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if ((e = mark(4))) return e;
   pf_group<<<1, 1024, 0, st>>>(p);
   if ((e = mark(5))) return e;
-  pf_fill<<<nch, 32, (size_t)(p.E + 2) * 8 + (size_t)(3 * p.E + 6) * 4, st>>>(p);
+  pf_fill<<<nch, kFillThreads, (size_t)(p.E + 2) * 8 + (size_t)(3 * p.E + 6) * 4, st>>>(p);
   if ((e = mark(6))) return e;
   if (!p.route_only) {
     pf_gather<<<(int)((ent_cap + 7) / 8), 256, 0, st>>>(p);
