@@ -771,9 +771,21 @@ __global__ void pf_gather(const __grid_constant__ PfParams P) {
   if (e >= P.offs[G]) return;
   const uint4 *src = reinterpret_cast<const uint4 *>(P.xg + (size_t)P.rows[e] * P.H);
   const size_t ent = (size_t)P.t * (P.K + 1);
-  // piece i (8 elements) of the row goes to k-panel i / 8
-  for (int i = lane; i < P.H / 8; i += 32)
-    reinterpret_cast<uint4 *>(P.xc + ((size_t)(i >> 3) * ent + e) * 64)[i & 7] = src[i];
+  // piece i (8 elements) of the row goes to k-panel i / 8; a lane's loads
+  // of up to eight pieces are all in flight before its stores
+  for (int i0 = 0; i0 < P.H / 8; i0 += 8 * 32) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int i = i0 + u * 32 + lane;
+      if (i < P.H / 8) v[u] = src[i];
+    }
+#pragma unroll
+    for (int u = 0; u < 8; u++) {
+      const int i = i0 + u * 32 + lane;
+      if (i < P.H / 8) reinterpret_cast<uint4 *>(P.xc + ((size_t)(i >> 3) * ent + e) * 64)[i & 7] = v[u];
+    }
+  }
 }
 
 // ------------------------------------------------------------ routing
