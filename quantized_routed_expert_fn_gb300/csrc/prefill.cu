@@ -8,8 +8,10 @@
 //   router  logits = R [x^_hi | x^_lo] on tcgen05 (R bf16 exact, fp32 TMEM)
 //   top-k   per token, softmax over the k chosen; per-(chunk, expert) counts
 //   group   scan -> offsets of the groups (experts, then the shared expert
-//           with all t tokens); per-chunk bases; tile work lists
-//   fill    token lists in ascending token order (stable), routing weights
+//           with all t tokens) and of their kPfTileN-token chunks; per-chunk
+//           bases
+//   fill    token lists in ascending token order (stable), routing weights;
+//           the tile work lists
 //   gate_up per (group, 64 gate + 64 up rows, <= kPfTileN tokens): weights
 //           dequantized to bf16 into tensor memory (A), token rows in group
 //           order through TMA (B), tcgen05 MMA into TMEM; epilogue
