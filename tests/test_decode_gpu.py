@@ -213,6 +213,29 @@ def test_c1_teacher_forced_layer(moe, c1, layer):
     print(f"[parity] c1 teacher-forced layer {layer}: max err = {r:.4f} of the bound")
 
 
+EXTREMES = [
+    # H, E, k, I, nb
+    (256, 8, 1, 128, 1),     # one expert per row
+    (256, 8, 1, 128, 4),
+    (256, 8, 8, 128, 1),     # every expert chosen
+    (256, 8, 8, 128, 4),
+    (512, 1024, 4, 128, 2),  # the most experts
+    (256, 64, 32, 128, 1),   # the largest top_k
+    (2048, 16, 2, 1024, 4),  # the largest hidden and inter sizes (two ring stages)
+]
+
+
+@pytest.mark.parametrize("H,E,k,I,nb", EXTREMES)
+def test_routing_and_size_extremes(moe, H, E, k, I, nb):
+    """The limits of the routing and of the layer shapes the decode kernel
+    accepts: ids exact, the union and its weights, outputs within 2e-3 x row
+    RMS of the oracle."""
+    rng = np.random.default_rng(3000 + H + E + k + nb)
+    layers = [synth.make_layer(rng, H, E, k, I, 4, shared=True, flags=synth.RESIDUAL | synth.PRENORM)]
+    x, _ = find_x(oracle.Layer(layers[0]), nb, seed=11)
+    check_layer(moe, layers, x, f"extremes H{H} E{E} k{k} I{I} nb{nb}")
+
+
 def test_traced_call_matches_and_stamps(moe):
     """moe_forward_traced computes what moe_forward computes, bit for bit,
     and stamps every CTA's phases of every layer in program order: the layer

@@ -116,13 +116,17 @@ SMALL = [
     (768, 40, 5, 384, 300, True, synth.RESIDUAL | synth.PRENORM),
     (512, 130, 4, 192, 129, True, synth.PRENORM),
     (256, 4, 4, 64, 600, False, synth.RESIDUAL),
+    (256, 16, 1, 128, 70, True, synth.PRENORM),  # top_k = 1
+    (256, 1024, 4, 64, 50, True, 0),  # the most experts: most groups empty
+    (256, 64, 32, 64, 40, False, 0),  # the largest top_k
 ]
 
 
 @pytest.mark.parametrize("H,E,k,I,t,shared,flags", SMALL)
 def test_prefill_small(moe, H, E, k, I, t, shared, flags):
     """Several token tiles with a ragged tail, expert groups above the 256-token
-    tile, a router tile with padded experts, k == E, t == 1."""
+    tile, a router tile with padded experts, k == E, t == 1, k == 1, the most
+    experts (1024) and the largest k (32)."""
     rng = np.random.default_rng(1000 + H + E + t)
     layer = synth.make_layer(rng, H, E, k, I, 4, shared=shared, flags=flags)
     ol = oracle.Layer(layer)
