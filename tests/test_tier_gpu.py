@@ -60,6 +60,19 @@ def run(m, dl, x, nl, offset=0):
     return out.cpu().numpy(), slot.cpu().numpy().view(np.uint64), wmap.cpu().numpy()
 
 
+def cut_between(w):
+    """A cut threshold at the median of the routed weights w, but midway
+    between two neighbouring weights at least 1e-4 apart, so that no weight
+    sits on it (the kernel's fp32 weights and the oracle's fp64 ones then
+    fall on the same side)."""
+    v = np.unique(np.asarray(w, dtype=np.float64).ravel())
+    i = len(v) // 2
+    while i + 1 < len(v) and v[i + 1] - v[i] < 1e-4:
+        i += 1
+    assert i + 1 < len(v), "no gap in the routed weights"
+    return float((v[i] + v[i + 1]) / 2)
+
+
 def experts_of(slot_row, addr_row, n):
     a2e = {int(a): e for e, a in enumerate(addr_row)}
     return [a2e[int(a)] for a in slot_row[:n]]
@@ -125,7 +138,7 @@ def test_tiered_steps_match_untiered_and_promote(m):
 
 
 def test_cut_of_weak_host_experts_matches_oracle(m):
-    """Half the records in host memory, the cut at the median routed weight:
+    """Half the records in host memory, the cut near the median routed weight:
     ids exact, the listed slots = the union minus the oracle's cut (device
     records first), output within 2e-3 x row RMS of the oracle with the
     same tiers and threshold."""
@@ -138,8 +151,7 @@ def test_cut_of_weak_host_experts_matches_oracle(m):
         r0 = oracle.route(oracle.Layer(layer), x)
         if all(topk_gap(r0["logits"][b], k) >= GAP for b in range(nb)):
             break
-    w = np.sort(r0["w"].ravel())
-    cut_w = float(w[len(w) // 2])
+    cut_w = cut_between(r0["w"])
     layer.expert_tier, layer.cut_w = tier_np, cut_w
     ol = oracle.Layer(layer)
     ref = oracle.moe_layer(ol, x)
@@ -180,4 +192,40 @@ def test_host_memory_records_read_over_c2c(m):
     assert int(slot[0, 62]) == 0 and int(slot[0, 63]) == len(ref["union"])
     r = assert_close_rows(got, ref["out"], ref["moe"], what="host-memory records")
     print(f"[parity] all routed records in host memory: max err = {r:.4f} of the bound")
+    t.close()
+
+
+def test_mixed_widths_in_host_memory_with_cut(m):
+    """4-, 3- and 2-bit records, every routed record in pinned host memory
+    (read over the link by the mixed-width kernel, each at its own width),
+    and the cut near the median routed weight: the listed slots are the union
+    minus the oracle's cut, in union order; the output is within 2e-3 x row
+    RMS of the oracle with the same widths, tiers and threshold."""
+    rng = np.random.default_rng(1010)
+    H, E, k, I, nb = 1024, 30, 6, 256, 4
+    eb = np.array([4, 3, 2] * (E // 3), dtype=np.uint8)
+    np.random.default_rng(1011).shuffle(eb)
+    layer = synth.make_mixed_layer(rng, H, E, k, I, eb, shared=True, flags=synth.PRENORM)
+    for s_ in range(200):
+        x = synth.make_x(np.random.default_rng(1020 + s_), nb, H)
+        r0 = oracle.route(oracle.Layer(layer), x)
+        if all(topk_gap(r0["logits"][b], k) >= GAP for b in range(nb)) and set(eb[r0["union"]].tolist()) == {2, 3, 4}:
+            break
+    else:
+        pytest.fail("no seed with the top-k gap and every width in the union")
+    cut_w = cut_between(r0["w"])
+    layer.expert_tier, layer.cut_w = np.ones(E, dtype=np.uint8), cut_w
+    ol = oracle.Layer(layer)
+    ref = oracle.moe_layer(ol, x)
+    cut = oracle.cut(ol, ref["idx"], ref["w"])
+    assert cut.any() and not cut[ref["union"]].all()
+    t, dl, keep = tiered(m, [layer], n_slots=0, cut_weak=cut_w)
+    addr = keep[2]
+    got, slot, _ = run(m, dl, x, 1)
+    kept = [int(e) for e in ref["union"] if not cut[e]]
+    assert int(slot[0, 62]) == 0 and int(slot[0, 63]) == len(ref["union"])
+    assert experts_of(slot[0], addr[0].cpu().numpy().view(np.uint64), len(kept)) == kept
+    r = assert_close_rows(got, ref["out"], ref["moe"], what="mixed widths in host memory, cut")
+    print(f"[parity] mixed 4/3/2-bit records in host memory, {int(cut.sum())} cut (w = {cut_w:.3f}): "
+          f"max err = {r:.4f} of the bound")
     t.close()
