@@ -52,8 +52,8 @@ METRIC = "MoE-layer rows/sec and achieved HBM GB/s (% of roofline) at nb=1/4 on 
 NCU_TRAFFIC = {
     "c1": dict(bytes=1206.2e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],
                sha="ed238ad4d041d957"),
-    "c4": dict(bytes=640.6e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
-               sha="fc28667a5453707e"),
+    "c4": dict(bytes=640.7e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
+               sha="52f70263c7b75366"),
 }
 
 
@@ -444,7 +444,7 @@ def extras(args, device):
     """The other decode and prefill workloads of the metric, timed on this GPU
     after the headline: verify batches, low-bit records, mixed widths,
     records in host memory (with and without the cut), the lookahead, the
-    prefill chunk."""
+    prefill chunk with 4-bit and with 3-bit routed records."""
     import argparse as _ap
     import torch
     res = {}
@@ -475,17 +475,21 @@ def extras(args, device):
                                                                 "its device-memory records into L2"})
     del setup, dl
     torch.cuda.empty_cache()
-    a = _ap.Namespace(**vars(args))
-    a.workload, a.nb = "c4", 0
-    r = run_prefill(a, 0, 1, device)
-    gu = r["flops"]["gate_up_gemm"] / (r["kernel_ms"]["gate_up_gemm"] * 1e-3) / 1e12
-    dn = r["flops"]["down_gemm"] / (r["kernel_ms"]["down_gemm"] * 1e-3) / 1e12
-    res["c4"] = {"workload": WORKLOADS["c4"], "ms_per_step": r["ms"], "rows_per_s": r["t"] / (r["ms"] * 1e-3),
-                 "roofline": {"bound": "tensor", "kernel": "gate_up_gemm", "achieved": gu, "peak": r["peak"],
-                              "unit": "TFLOP/s", "frac": gu / r["peak"], "peak_source": r["peak_kind"] + " bf16 burst",
-                              "algorithmic_flops_per_launch": r["flops"]["gate_up_gemm"]},
-                 "down_gemm": {"achieved": dn, "frac": dn / r["peak"]},
-                 "kernel_ms": r["kernel_ms"], "clocks": r["clocks"]}
+    # the prefill chunk with 4-bit records, then with 3-bit routed records
+    for name in ("c4", "c4b3"):
+        a = _ap.Namespace(**vars(args))
+        a.workload, a.nb = name, 0
+        r = run_prefill(a, 0, 1, device)
+        gu = r["flops"]["gate_up_gemm"] / (r["kernel_ms"]["gate_up_gemm"] * 1e-3) / 1e12
+        dn = r["flops"]["down_gemm"] / (r["kernel_ms"]["down_gemm"] * 1e-3) / 1e12
+        res[name] = {"workload": WORKLOADS[name], "ms_per_step": r["ms"], "rows_per_s": r["t"] / (r["ms"] * 1e-3),
+                     "roofline": {"bound": "tensor", "kernel": "gate_up_gemm", "achieved": gu, "peak": r["peak"],
+                                  "unit": "TFLOP/s", "frac": gu / r["peak"],
+                                  "peak_source": r["peak_kind"] + " bf16 burst",
+                                  "algorithmic_flops_per_launch": r["flops"]["gate_up_gemm"]},
+                     "down_gemm": {"achieved": dn, "frac": dn / r["peak"]},
+                     "kernel_ms": r["kernel_ms"], "clocks": r["clocks"]}
+        torch.cuda.empty_cache()
     return res
 
 

@@ -271,12 +271,16 @@ __device__ __forceinline__ int ws_weight_row(const PfParams &P, int mt, int r) {
 // Global sources of one staging thread t for a tile, formed once per tile:
 // its four 16-byte code segments (row (i * 256 + t) / 8, piece t % 8, at
 // k-panel 0; a chunk's row segment is 32 * bits bytes, so pieces past
-// 2 * bits are not copied) and the scale / bias words of row t % 128.
+// 2 * bits are not copied) and the scale / bias entries of row t % 128.
+// w16 (input width a multiple of 256): every row's scale and bias tables
+// start on an 8-byte boundary, so a chunk's four entries of a table (8
+// bytes) lie in one aligned 16-byte window; thread t then copies that
+// window of table t / 128 (s: its row's table at k-panel 0).
 struct StgRows {
   const uint8_t *c[4];
   const uint8_t *s, *b;
   int seg;  // bytes of a row per chunk of four k-panels
-  bool ok;
+  bool ok, w16;
 };
 
 // code width of a tile's record: the shared expert's is 4-bit; LB: the
@@ -304,7 +308,8 @@ __device__ __forceinline__ StgRows stage_rows(const PfParams &P, const PfItem &i
                     : nullptr;
     }
     const size_t g2 = (size_t)ws_weight_row<MODE>(P, it.mt, t & 127) * (inp / 64) * 2;
-    sr.s = rec + q.s + g2;
+    sr.w16 = (inp & 255) == 0;
+    sr.s = rec + (sr.w16 && t >= 128 ? q.b : q.s) + g2;
     sr.b = rec + q.b + g2;
   }
   return sr;
@@ -314,10 +319,13 @@ __device__ __forceinline__ StgRows stage_rows(const PfParams &P, const PfItem &i
 // memory, by the 256 producer threads (t): 128 rows x 128 bytes, copied by 8
 // threads per row segment so that each warp instruction reads four whole
 // 128-byte lines (16-byte pieces placed at piece ^ (row & 7) against bank
-// conflicts); plus, per row and panel, the 4-byte words holding its scale
-// and bias.  A segment may run past the end of a row, into bytes of the same
-// record (codes are followed by the scale and bias tables); those bytes are
-// never used.
+// conflicts); plus the scale and bias entries: w16, per row and table the
+// 16-byte window holding the chunk's four entries (scales at row * 16,
+// biases 2048 bytes further); otherwise, per row and panel, the 4-byte words
+// holding its scale and bias.  A segment or window may run past the end of
+// a row, into bytes of the same record (codes are followed by the scale and
+// bias tables, and a table's end is 16-byte aligned); those bytes are never
+// used.
 __device__ __forceinline__ void stage_chunk(const StgRows &sr, int kc, int nk, int t, uint8_t *buf) {
   if (sr.ok) {
 #pragma unroll
@@ -326,6 +334,12 @@ __device__ __forceinline__ void stage_chunk(const StgRows &sr, int kc, int nk, i
       if (sr.c[i]) tc05::cp16(buf + row * 128 + ((part ^ (row & 7)) << 4), sr.c[i] + kc * sr.seg);
     }
     const int r = t & 127;
+    if (sr.w16) {
+      tc05::cp16(buf + kStgCodes + (t >> 7) * 2048 + r * 16,
+                 reinterpret_cast<const uint8_t *>(((uintptr_t)sr.s + 8 * kc) & ~(uintptr_t)15));
+      tc05::cp_commit();
+      return;
+    }
 #pragma unroll
     for (int v = 0; v < 2; v++) {
       const int u = 2 * (t >> 7) + v;
@@ -339,14 +353,24 @@ __device__ __forceinline__ void stage_chunk(const StgRows &sr, int kc, int nk, i
   tc05::cp_commit();
 }
 
+// Scale and bias (bf16 bits, in .x and .y) of row r, k-panel u of a staged
+// chunk.  w16: the chunk's entries sit at byte sel (0 or 8) of the row's
+// 16-byte windows; otherwise in half sel of the panel's 4-byte words.
+__device__ __forceinline__ uint2 staged_sb(const uint8_t *buf, int r, int u, uint32_t sel, bool w16) {
+  if (w16) {
+    const uint8_t *p = buf + kStgCodes + r * 16 + sel + 2 * u;
+    return make_uint2(*reinterpret_cast<const uint16_t *>(p), *reinterpret_cast<const uint16_t *>(p + 2048));
+  }
+  const uint2 w = *reinterpret_cast<const uint2 *>(buf + kStgCodes + (r * kChunk + u) * 8);
+  return make_uint2((w.x >> (16 * sel)) & 0xffffu, (w.y >> (16 * sel)) & 0xffffu);
+}
+
 // Row r's 64 codes of k-panel u of a staged chunk -> bf16(scale * code +
 // bias), k permuted within 8-blocks, as 32 words of two bf16 each (the row's
 // 32 A columns of the panel).  4-bit records; ws_dequant_row_lb below takes
-// 2- and 3-bit ones into the same layout.
-__device__ __forceinline__ void ws_dequant_row(const uint8_t *buf, int r, int u, uint32_t half, uint32_t (&a)[32]) {
-  const uint2 sbw = *reinterpret_cast<const uint2 *>(buf + kStgCodes + (r * kChunk + u) * 8);
-  const uint32_t s = (sbw.x >> (16 * half)) & 0xffffu, b = (sbw.y >> (16 * half)) & 0xffffu;
-  const uint32_t s2 = s * 0x10001u, b2 = b * 0x10001u;
+// 2- and 3-bit ones into the same layout.  sb: the panel's scale and bias.
+__device__ __forceinline__ void ws_dequant_row(const uint8_t *buf, int r, int u, uint2 sb, uint32_t (&a)[32]) {
+  const uint32_t s2 = sb.x * 0x10001u, b2 = sb.y * 0x10001u;
 #pragma unroll
   for (int hf = 0; hf < 2; hf++) {
     const uint4 c = *reinterpret_cast<const uint4 *>(buf + r * 128 + (((2 * u + hf) ^ (r & 7)) << 4));
@@ -375,10 +399,8 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[2 * B], int i) {
 // the row's staged segment (8-byte loads never straddle a 16-byte piece);
 // word 4ch + j of the output pairs codes 8ch + j and 8ch + j + 4, as for 4 bits.
 template <int B>
-__device__ __forceinline__ void ws_dequant_row_lb(const uint8_t *buf, int r, int u, uint32_t half, uint32_t (&a)[32]) {
-  const uint2 sbw = *reinterpret_cast<const uint2 *>(buf + kStgCodes + (r * kChunk + u) * 8);
-  const uint32_t s = (sbw.x >> (16 * half)) & 0xffffu, b = (sbw.y >> (16 * half)) & 0xffffu;
-  const uint32_t s2 = s * 0x10001u, b2 = b * 0x10001u;
+__device__ __forceinline__ void ws_dequant_row_lb(const uint8_t *buf, int r, int u, uint2 sb, uint32_t (&a)[32]) {
+  const uint32_t s2 = sb.x * 0x10001u, b2 = sb.y * 0x10001u;
   uint32_t w[2 * B];
 #pragma unroll
   for (int k = 0; k < B; k++) {
@@ -396,14 +418,14 @@ __device__ __forceinline__ void ws_dequant_row_lb(const uint8_t *buf, int r, int
     }
 }
 
-__device__ __forceinline__ void dequant_row_bits(int bits, const uint8_t *buf, int r, int u, uint32_t half,
+__device__ __forceinline__ void dequant_row_bits(int bits, const uint8_t *buf, int r, int u, uint2 sb,
                                                  uint32_t (&a)[32]) {
   if (bits == 4)
-    ws_dequant_row(buf, r, u, half, a);
+    ws_dequant_row(buf, r, u, sb, a);
   else if (bits == 3)
-    ws_dequant_row_lb<3>(buf, r, u, half, a);
+    ws_dequant_row_lb<3>(buf, r, u, sb, a);
   else
-    ws_dequant_row_lb<2>(buf, r, u, half, a);
+    ws_dequant_row_lb<2>(buf, r, u, sb, a);
 }
 
 template <int MODE, bool LB = false>
@@ -611,8 +633,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         stage_chunk(srow, c - lt * nct, nk, t, stg + (c % NStg) * kStgBuf);
       };
       for (int c = 0; c < NStg - 1; c++) issue(c);
-      // parity of the weight row = parity of r (tile row bases are even)
-      const uint32_t rodd = (uint32_t)(r & (inp / 64) & 1);
+      // parity of the weight row = parity of r (tile row bases are even):
+      // rodd tells whether the row's tables start in the second half of a
+      // 4-byte word, rodd8 (w16) in the second half of a 16-byte window
+      const bool w16 = (inp & 255) == 0;
+      const uint32_t rodd = (uint32_t)(r & (inp / 64) & 1), rodd8 = (uint32_t)(r & (inp / 256) & 1);
       int qlt = -1, qbits = 4;  // the tile being dequantized and its code width
       bool ok = true;
       for (int c = 0; c < total && ok; c++) {
@@ -630,15 +655,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
           if (warp_wait(&B.empty_a[sa], (uint32_t)(((ga / kSA) & 1) ^ 1), P)) {
             tc05::fence_after();  // after the MMAs that read this A stage
             const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTmemA + 32 * kPA * sa);
-            // scale / bias: the half of the staged 4-byte word holding entry row * G + kk
+            // scale / bias of entry row * G + kk: its place in the staged windows or words
             const int kk0 = kc * kChunk + u0;
             uint32_t av0[32], av1[32];
-            if (LB) dequant_row_bits(qbits, buf, r, u0, (rodd + (uint32_t)kk0) & 1u, av0);
-            else ws_dequant_row(buf, r, u0, (rodd + (uint32_t)kk0) & 1u, av0);
+            const uint32_t sel8 = 8u * ((rodd8 + (uint32_t)kc) & 1u);
+            const uint2 sb0 = staged_sb(buf, r, u0, w16 ? sel8 : (rodd + (uint32_t)kk0) & 1u, w16);
+            if (LB) dequant_row_bits(qbits, buf, r, u0, sb0, av0);
+            else ws_dequant_row(buf, r, u0, sb0, av0);
             tc05::st32(ta, av0);
             if (u0 + 1 < ns) {
-              if (LB) dequant_row_bits(qbits, buf, r, u0 + 1, (rodd + (uint32_t)kk0 + 1u) & 1u, av1);
-              else ws_dequant_row(buf, r, u0 + 1, (rodd + (uint32_t)kk0 + 1u) & 1u, av1);
+              const uint2 sb1 = staged_sb(buf, r, u0 + 1, w16 ? sel8 : (rodd + (uint32_t)kk0 + 1u) & 1u, w16);
+              if (LB) dequant_row_bits(qbits, buf, r, u0 + 1, sb1, av1);
+              else ws_dequant_row(buf, r, u0 + 1, sb1, av1);
               tc05::st32(ta + 32, av1);
             }
             tc05::wait_st();
