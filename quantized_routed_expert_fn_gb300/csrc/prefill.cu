@@ -24,6 +24,7 @@
 // pair (nibbles j and j+4 of a code word share a register).
 #include <cuda_runtime.h>
 
+#include "codec.cuh"
 #include "prefill.cuh"
 #include "tc05.cuh"
 
@@ -386,18 +387,13 @@ __device__ __forceinline__ void ws_dequant_row(const uint8_t *buf, int r, int u,
   }
 }
 
-// Code i (0..63) of a panel's little-endian bitstream w of B-bit codes.
-template <int B>
-__device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[2 * B], int i) {
-  const int bit = B * i, wi = bit >> 5, off = bit & 31;
-  uint32_t v = w[wi] >> off;
-  if (off + B > 32) v |= w[wi + 1] << (32 - off);
-  return v & ((1u << B) - 1u);
-}
-
 // ws_dequant_row for B = 2 or 3: the panel's 8B code bytes sit at byte 8Bu of
 // the row's staged segment (8-byte loads never straddle a 16-byte piece);
-// word 4ch + j of the output pairs codes 8ch + j and 8ch + j + 4, as for 4 bits.
+// word 4ch + j of the output pairs codes 8ch + j and 8ch + j + 4, as for 4
+// bits.  Each half of the panel (32 codes, B words) goes through the decode
+// codec's CodecO4<B>, which puts every such pair at shift 0 on 128.0 (a byte
+// permute per 16 codes for 2 bits, a funnel shift and a bit select per 24-bit
+// window for 3), so a pair costs one shift and one mask-or.
 template <int B>
 __device__ __forceinline__ void ws_dequant_row_lb(const uint8_t *buf, int r, int u, uint2 sb, uint32_t (&a)[32]) {
   const uint32_t s2 = sb.x * 0x10001u, b2 = sb.y * 0x10001u;
@@ -409,13 +405,17 @@ __device__ __forceinline__ void ws_dequant_row_lb(const uint8_t *buf, int r, int
     w[2 * k] = q.x, w[2 * k + 1] = q.y;
   }
 #pragma unroll
-  for (int ch = 0; ch < 8; ch++)
+  for (int h = 0; h < 2; h++) {
+    uint32_t hw[B], v[16];
 #pragma unroll
-    for (int j = 0; j < 4; j++) {
-      const uint32_t v = code_at<B>(w, 8 * ch + j) | (code_at<B>(w, 8 * ch + j + 4) << 16) | 0x43004300u;
-      const uint32_t qv = bfma2(v, 0x3f803f80u, 0xc300c300u);  // the codes, exact
-      a[4 * ch + j] = bfma2(qv, s2, b2);                      // bf16(s*q + b)
+    for (int k = 0; k < B; k++) hw[k] = w[B * h + k];
+    CodecO4<B>::unpack(hw, v);  // v[4g + j] = (128 + code 8g + j, 128 + code 8g + j + 4) of the half
+#pragma unroll
+    for (int i = 0; i < 16; i++) {
+      const uint32_t qv = bfma2(v[i], 0x3f803f80u, 0xc300c300u);  // the codes, exact
+      a[16 * h + i] = bfma2(qv, s2, b2);                         // bf16(s*q + b)
     }
+  }
 }
 
 __device__ __forceinline__ void dequant_row_bits(int bits, const uint8_t *buf, int r, int u, uint2 sb,
