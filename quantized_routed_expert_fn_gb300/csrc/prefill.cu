@@ -52,11 +52,25 @@ __device__ __forceinline__ float warp_sum_f(float v) {
   return v;
 }
 
-// bounded wait on an mbarrier phase; false (status set) once the limit passes
+// mbar_try_wait, but a thread whose phase is not complete sleeps until it
+// completes or about ns nanoseconds pass (instead of a system-set limit)
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+// bounded wait on an mbarrier phase; false (status set) once the limit passes.
+// The waiting thread sleeps on the barrier (up to 1 ms a try) rather than
+// polling, so the waiting roles leave the issue slots to the dequant warps.
 __device__ bool pf_wait(uint64_t *bar, uint32_t par, const PfParams &P) {
   if (mbar_try_wait(bar, par)) return true;
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, par)) {
+  while (!mbar_try_wait_sleep(bar, par, 1000000u)) {
     if (globaltimer() - t0 > P.timeout_ns) {
       atomicCAS(P.status, 0, kStatusTimeout);
       return false;
@@ -643,7 +657,6 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       for (int c = 0; c < total && ok; c++) {
         tc05::cp_wait_group<NStg - 2>();  // this thread's copies of chunk c are done
         tc05::named_sync(3, 256);  // everyone's are; everyone is done reading chunk c - 1
-        issue(c + NStg - 1);
         const int lt = c / nct, kc = c - lt * nct;
         const uint8_t *buf = stg + (c % NStg) * kStgBuf;
         const int ns = min(kChunk, nk - kc * kChunk);
@@ -681,6 +694,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
             ok = false;
           }
         }
+        // chunk c + NStg - 1 into chunk c - 1's buffer (free since the barrier
+        // above), after this chunk's dequantization: its copies land chunks
+        // before they are read, and their issue waits on the load queue
+        issue(c + NStg - 1);
         // the eight producer warps stop together (they share a named barrier)
         ok = tc05::named_and(4, 256, ok);
       }
