@@ -323,6 +323,13 @@ int check_prefill(const moe_layer *L, int t) {
   if (I == 0 || I % 64 || I > 16384) return fail(MOE_ESHAPE, "inter %u must be a multiple of 64 in 64..16384", I);
   if (E < 1 || E > 1024) return fail(MOE_ESHAPE, "n_experts %u outside 1..1024", E);
   if (K < 1 || K > E || K > 32) return fail(MOE_ESHAPE, "top_k %u outside 1..min(n_experts, 32)", K);
+  // the GEMMs reach a row of the grouped operands (x^ rows, h), stored as
+  // k-panels of t * (top_k + 1) rows, with a signed 32-bit tensor-map
+  // coordinate: panel * t * (top_k + 1) + row
+  const uint64_t ent = (uint64_t)t * (K + 1);
+  if ((uint64_t)(H / 64) * ent > (uint64_t)INT32_MAX || (uint64_t)(I / 64) * ent > (uint64_t)INT32_MAX)
+    return fail(MOE_ESHAPE, "t %d x (top_k + 1) rows in %u k-panels exceed the 2^31 rows a tensor-map coordinate reaches",
+                t, (H > I ? H : I) / 64);
   if (L->expert_bits) return fail(MOE_EINVAL, "mixed record widths (expert_bits) are supported by decode only");
   if (L->expert_tier || L->cut_weak != 0.f)
     return fail(MOE_EINVAL, "host-memory records (expert_tier, cut_weak) are supported by decode only");

@@ -132,6 +132,26 @@ def test_prefill_rejects_bad_calls(m):
     assert lib.moe_prefill_workspace(_struct(m, L, top_k=33), 16) == 0
 
 
+def test_prefill_rejects_chunks_past_the_tma_coordinate_range(m):
+    """The expert GEMMs reach a row of the grouped operands with a signed
+    32-bit tensor-map coordinate: (hidden / 64) * t * (top_k + 1) must stay
+    below 2^31, and a larger chunk is refused on the host."""
+    H, I, E = 16384, 256, 64
+    lay = synth.record_layout(H, I, 4)
+
+    def workspace(k, t):
+        arr = (m.MoeLayer * 1)()
+        c = arr[0]
+        c.hidden, c.n_experts, c.top_k, c.inter, c.bits, c.group, c.flags = H, E, k, I, 4, 64, 0
+        c.router, c.expert_addr = 0x10000, 0x20000
+        c.gate_up, c.down = m._q(lay.gate_up), m._q(lay.down)
+        return m.lib().moe_prefill_workspace(arr, t)
+
+    assert workspace(6, 1 << 20) > 0  # 256 k-panels x 7 x 2^20 rows < 2^31
+    assert workspace(7, 1 << 20) == 0  # = 2^31
+    assert workspace(7, (1 << 20) - 1) > 0
+
+
 def _mixed_struct(m, L, n_layers=1):
     arr = (m.MoeLayer * n_layers)()
     for i in range(n_layers):
