@@ -659,6 +659,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
       for (int c = 0; c < total && ok; c++) {
         tc05::cp_wait_group<NStg - 2>();  // this thread's copies of chunk c are done
         tc05::named_sync(3, 256);  // everyone's are; everyone is done reading chunk c - 1
+        // the second group, which waits longer for its A stage, issues chunk
+        // c + NStg - 1 (into chunk c - 1's buffer) before that wait; the first
+        // group after its dequantization
+        if (hf) issue(c + NStg - 1);
         const int lt = c / nct, kc = c - lt * nct;
         const uint8_t *buf = stg + (c % NStg) * kStgBuf;
         const int ns = min(kChunk, nk - kc * kChunk);
@@ -699,7 +703,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
         // chunk c + NStg - 1 into chunk c - 1's buffer (free since the barrier
         // above), after this chunk's dequantization: its copies land chunks
         // before they are read, and their issue waits on the load queue
-        issue(c + NStg - 1);
+        if (!hf) issue(c + NStg - 1);
         // the eight producer warps stop together (they share a named barrier)
         ok = tc05::named_and(4, 256, ok);
       }
