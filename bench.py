@@ -53,7 +53,7 @@ NCU_TRAFFIC = {
     "c1": dict(bytes=1206.2e6, sources=["decode.cu", "decode.cuh", "codec.cuh", "common.cuh"],
                sha="ed238ad4d041d957"),
     "c4": dict(bytes=640.7e6, sources=["prefill.cu", "prefill.cuh", "tc05.cuh", "common.cuh"],
-               sha="6c763b6a41b787fb"),
+               sha="eb12363a6b8ea9ee"),
 }
 
 

@@ -146,7 +146,7 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 // ------------------------------------------------------------ tensor-core GEMM
 //
 // Persistent, warp-specialised: one CTA per SM walks tiles blockIdx.x,
-// blockIdx.x + gridDim.x, ... of a 128 x N output tile list (N <= 256 for
+// blockIdx.x + gridDim.x, ... of a 128 x N output tile list (N <= 128 for
 // the router, <= kPfTileN for the expert GEMMs); K goes in stages of 64.
 // B (token rows) passes through a ring of 128B-swizzled shared-memory
 // stages (router: six of 128 rows; expert GEMMs: three of up to 320 rows,
@@ -169,11 +169,15 @@ __global__ void pf_prep(const __grid_constant__ PfParams P) {
 //               by the MMAs three stages back, not two:
 //               warp w fills rows 32 (w % 4) .. +31 -- the TMEM lanes it may
 //               write -- 64 codes a panel, stored as 32 bf16 pairs per panel
-//               with tcgen05.st
+//               with tcgen05.st.  Issuing cp.async copies stalls a warp, so
+//               the first group issues a chunk's copies after its dequant
+//               and the second, which waits longer for its A stage, before
+//               that wait.
 //   warps 10-13 epilogue: TMEM -> registers -> global, from one of two
 //               accumulators while the MMAs fill the other
-// Every mbarrier wait is bounded; a wait that gives up records
-// MOE_ETIMEOUT in *status and its role stops, so the CTA ends.
+// Every mbarrier wait is bounded and sleeps on the barrier between tries; a
+// wait that gives up records MOE_ETIMEOUT in *status and its role stops, so
+// the CTA ends.
 
 constexpr int kWsThreads = 448;
 constexpr int kSB = 6;                     // B stages (shared memory), at most
