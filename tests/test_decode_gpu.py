@@ -222,6 +222,7 @@ EXTREMES = [
     (512, 1024, 4, 128, 2),  # the most experts
     (256, 64, 32, 128, 1),   # the largest top_k
     (2048, 16, 2, 1024, 4),  # the largest hidden and inter sizes (two ring stages)
+    (256, 1, 1, 128, 3),     # a single expert: every row routes to it, weight 1
 ]
 
 

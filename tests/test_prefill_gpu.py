@@ -119,6 +119,7 @@ SMALL = [
     (256, 16, 1, 128, 70, True, synth.PRENORM),  # top_k = 1
     (256, 1024, 4, 64, 50, True, 0),  # the most experts: most groups empty
     (256, 64, 32, 64, 40, False, 0),  # the largest top_k
+    (256, 1, 1, 64, 33, True, 0),  # a single expert: every row routes to it, weight 1
 ]
 
 
