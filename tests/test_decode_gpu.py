@@ -387,17 +387,26 @@ def test_mixed_width_stack(moe):
 
 # ---------------------------------------------------------------- lookahead
 
-def test_lookahead_predicts_and_changes_nothing(moe):
+@pytest.mark.parametrize("width", ["4", "3", "mixed"])
+def test_lookahead_predicts_and_changes_nothing(moe, width):
     """With MOE_LOOKAHEAD on every layer, each layer's experts are predicted
     during the previous layer from its router on the previous layer's
     input, and the predicted records prefetched into L2.  The predicted ids
     equal the oracle's routing of that input by that router (as sets per
     row, where the top-k gap holds), the first layer reports no prediction,
-    and the outputs are bitwise those of the call without the lookahead."""
+    and the outputs are bitwise those of the call without the lookahead.
+    Layers of 4-bit records, of 3-bit routed records, and of mixed widths
+    (the kernel's lookahead instances for each)."""
     rng = np.random.default_rng(730)
     nl, H, E, k, I, nb = 5, 1024, 64, 6, 256, 2
-    layers = [synth.make_layer(rng, H, E, k, I, 4, shared=True, flags=synth.RESIDUAL | synth.PRENORM)
-              for _ in range(nl)]
+    flags = synth.RESIDUAL | synth.PRENORM
+
+    def make(l):
+        if width == "mixed":
+            return synth.make_mixed_layer(rng, H, E, k, I, mixed_widths(E, 740 + l), shared=True, flags=flags)
+        return synth.make_layer(rng, H, E, k, I, int(width), shared=True, flags=flags)
+
+    layers = [make(l) for l in range(nl)]
     ols = [oracle.Layer(L) for L in layers]
     x = synth.make_x(np.random.default_rng(731), nb, H)
     dl = moe.DeviceLayers(layers)
@@ -427,4 +436,5 @@ def test_lookahead_predicts_and_changes_nothing(moe):
             hits += len(set(pred[l][b].tolist()) & set(exact[b].tolist()))
             total += k
     assert checked >= nb * (nl - 1) // 2
-    print(f"[lookahead] predictions checked {checked}; hit rate {hits / total:.2f} of the exact experts")
+    print(f"[lookahead, {width}-bit records] predictions checked {checked}; "
+          f"hit rate {hits / total:.2f} of the exact experts")
