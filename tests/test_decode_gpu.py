@@ -387,7 +387,7 @@ def test_mixed_width_stack(moe):
 
 # ---------------------------------------------------------------- lookahead
 
-@pytest.mark.parametrize("width", ["4", "3", "mixed"])
+@pytest.mark.parametrize("width", ["4", "3", "2", "mixed"])
 def test_lookahead_predicts_and_changes_nothing(moe, width):
     """With MOE_LOOKAHEAD on every layer, each layer's experts are predicted
     during the previous layer from its router on the previous layer's

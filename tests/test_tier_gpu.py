@@ -229,3 +229,33 @@ def test_mixed_widths_in_host_memory_with_cut(m):
     print(f"[parity] mixed 4/3/2-bit records in host memory, {int(cut.sum())} cut (w = {cut_w:.3f}): "
           f"max err = {r:.4f} of the bound")
     t.close()
+
+
+def test_lookahead_with_host_memory_records_changes_nothing(m):
+    """A three-layer stack whose records sit partly in device slots and
+    partly in pinned host memory (after one promoting step).  With the
+    one-layer lookahead on every layer (predicted device records prefetched
+    into L2, host ones left to the kernel's own reads), the outputs, slot
+    tables and weight maps are bitwise those of the same call without it."""
+    rng = np.random.default_rng(1010)
+    nl, H, E, k, I, nb = 3, 512, 16, 4, 256, 2
+    flags = synth.RESIDUAL | synth.PRENORM
+    layers = [synth.make_layer(rng, H, E, k, I, 4, shared=True, flags=flags) for _ in range(nl)]
+    t, dl, keep = tiered(m, layers, n_slots=10)
+    _, slot0, _ = run(m, dl, synth.make_x(np.random.default_rng(1011), nb, H), nl)
+    t.update(slot0)
+    torch.cuda.synchronize()
+    x = synth.make_x(np.random.default_rng(1012), nb, H)
+    base, bslot, bw = run(m, dl, x, nl)
+    la = torch.zeros((nl, nb, k), dtype=torch.int32, device="cuda")
+    dl.set_flags(flags | m.LOOKAHEAD)
+    for l in range(nl):
+        dl.c[l].lookahead_idx = la[l].data_ptr()
+    got, gslot, gw = run(m, dl, x, nl)
+    assert np.array_equal(got.view(np.uint32), base.view(np.uint32)), "lookahead changed the result"
+    assert np.array_equal(gslot, bslot) and np.array_equal(gw.view(np.uint32), bw.view(np.uint32))
+    ndev = [int(bslot[l, 62]) for l in range(nl)]
+    nun = [int(bslot[l, 63]) for l in range(nl)]
+    assert any(0 < d < u for d, u in zip(ndev, nun)), "no union mixes the tiers"
+    print(f"[tier + lookahead] device / union records per layer: {list(zip(ndev, nun))}; bitwise equal")
+    t.close()
