@@ -847,11 +847,14 @@ __global__ void pf_gather(const __grid_constant__ PfParams P) {
 
 // ------------------------------------------------------------ routing
 
+// Unsigned key in the order of f; -0 is keyed as +0, so that a logit of -0
+// ties with +0 (to the lower id) as the comparison of the two floats does
+// (the tensor-core sum of an all-zero row's products may come out as -0).
 __device__ __forceinline__ uint32_t orderable_f(float f) {
-  const uint32_t u = __float_as_uint(f);
+  const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-// its inverse: the float a key was made from (bit for bit)
+// its inverse: the float a key was made from (bit for bit, but for -0)
 __device__ __forceinline__ float from_orderable(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }

@@ -438,3 +438,28 @@ def test_lookahead_predicts_and_changes_nothing(moe, width):
     assert checked >= nb * (nl - 1) // 2
     print(f"[lookahead, {width}-bit records] predictions checked {checked}; "
           f"hit rate {hits / total:.2f} of the exact experts")
+
+
+# ---------------------------------------------------------------- zero rows
+
+def test_zero_rows_route_by_the_tie_rule(moe):
+    """Rows of zeros: every logit is 0, so the k experts are the k lowest ids
+    (ties go to the lower id), each weighted 1/k, and the row's output is
+    exactly zero; an ordinary row in the same batch still matches the
+    oracle."""
+    rng = np.random.default_rng(1200)
+    H, E, k, I, nb = 512, 16, 4, 256, 3
+    layer = synth.make_layer(rng, H, E, k, I, 4, shared=True, flags=synth.RESIDUAL | synth.PRENORM)
+    ol = oracle.Layer(layer)
+    xr, _ = find_x(ol, 1, seed=1201)
+    x = np.zeros((nb, H), dtype=np.float32)
+    x[1] = xr[0]
+    ref = oracle.moe_layer(ol, x.astype(np.float64))
+    assert ref["idx"][0].tolist() == list(range(k)) and ref["idx"][2].tolist() == list(range(k))
+    g = run_forward(moe, moe.DeviceLayers([layer]), x)
+    for b in (0, 2):
+        assert g["idx"][0][b].tolist() == list(range(k)), g["idx"][0][b]
+        assert np.all(g["out"][b] == 0.0)
+    assert int(g["slot"][0, 63]) == len(ref["union"])
+    check_routing(g["idx"][0][1:2], None, {"idx": ref["idx"][1:2]}, ref["logits"][1:2], k, "ordinary row")
+    assert_close_rows(g["out"][1:2], ref["out"][1:2], ref["moe"][1:2], what="ordinary row beside zero rows")

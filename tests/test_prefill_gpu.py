@@ -379,3 +379,23 @@ def test_prefill_timed_matches_prefill(moe):
     total = evs[0].elapsed_time(evs[-1])
     assert all(p >= 0 for p in parts) and abs(sum(parts) - total) <= 1e-3 * max(total, 1.0)
     print(f"[prefill] timed call: {moe.PREFILL_KERNELS} kernels, {total * 1e3:.1f} us, outputs equal the plain call")
+
+
+def test_prefill_zero_rows_route_by_the_tie_rule(moe):
+    """Rows of zeros in a chunk: every logit is 0, so the k experts are the k
+    lowest ids (ties go to the lower id) and the row's output is exactly
+    zero; the other rows still match the oracle."""
+    rng = np.random.default_rng(1210)
+    H, E, k, I, t = 256, 16, 4, 128, 40
+    layer = synth.make_layer(rng, H, E, k, I, 4, shared=True, flags=synth.RESIDUAL | synth.PRENORM)
+    ol = oracle.Layer(layer)
+    x = rows_with_gap(ol, rng, t, H)
+    zero = np.arange(0, t, 3)
+    x[zero] = 0.0
+    got, idx = run_prefill(moe, moe.DeviceLayers([layer]), x)
+    assert (idx[zero] == np.arange(k)).all(), idx[zero]
+    assert np.all(got[zero] == 0.0)
+    rest = np.setdiff1d(np.arange(t), zero)
+    ref = oracle.prefill_rows(ol, x, rest, mirror=True)
+    assert np.array_equal(np.sort(idx[rest], axis=1), np.sort(ref["idx"], axis=1))
+    assert_prefill_close(got[rest], ref, x, layer.flags, rest, "rows beside zero rows")
