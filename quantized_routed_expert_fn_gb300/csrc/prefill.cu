@@ -44,6 +44,19 @@ __device__ __forceinline__ uint32_t f2bf_rn(float f) {
   return h;
 }
 
+// Programmatic dependent launch: every kernel of the chain lets the next one
+// launch at once (it then waits, resident, for this grid's completion),
+// and waits for the previous kernel's completion and memory before it
+// reads that kernel's results.  The next grid launches only when every
+// block of this one has started, so a waiting grid never holds resources
+// this one still needs.
+__device__ __forceinline__ void pdl_launch_next() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prev() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_begin() {
+  pdl_launch_next();
+  pdl_wait_prev();
+}
+
 // position of natural index j inside its 8-block under the operand
 // permutation: pairs (0,4),(1,5),(2,6),(3,7) are adjacent
 __device__ __forceinline__ int perm8(int j) { return (j & 3) * 2 + (j >> 2); }
@@ -86,6 +99,7 @@ __device__ bool pf_wait(uint64_t *bar, uint32_t par, const PfParams &P) {
 // (hi/lo, natural order), the expert operand (bf16 of x^, k permuted within
 // the block), the shared gate sigmoid(sg . x^).  16-byte loads and stores.
 __global__ void pf_prep(const __grid_constant__ PfParams P) {
+  pdl_launch_next();  // (launched after the call's memsets, in plain stream order)
   __shared__ float red[32];
   const int tok = blockIdx.x, H = P.H, nw = blockDim.x >> 5, nb8 = H / 8;
   const float4 *xr = reinterpret_cast<const float4 *>(P.x + (size_t)tok * H);
@@ -450,15 +464,12 @@ __device__ __forceinline__ void dequant_row_bits(int bits, const uint8_t *buf, i
 
 template <int MODE, bool LB = false>
 __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__ PfParams P) {
+  pdl_launch_next();
   extern __shared__ __align__(1024) uint8_t smraw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~(uintptr_t)1023);
   using LY = Lay<MODE>;
   WsBars &B = *reinterpret_cast<WsBars *>(sm + LY::offBars);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ntiles = ws_num_tiles<MODE>(P);
-  const int nk = ws_nk<MODE>(P);
-  const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  auto tile_of = [&](int lt) { return (int)blockIdx.x + lt * (int)gridDim.x; };
 
   if (tid == 0) {
     for (int s = 0; s < LY::nSB; s++) {
@@ -481,6 +492,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
   __syncthreads();
   tc05::fence_after();
   const uint32_t tmem = B.tmem;
+  // the setup above overlaps the previous kernel's end; everything below may
+  // read earlier kernels' results (the work-list sizes among them)
+  pdl_wait_prev();
+  const int ntiles = ws_num_tiles<MODE>(P);
+  const int nk = ws_nk<MODE>(P);
+  const int my_tiles = (int)blockIdx.x < ntiles ? (ntiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  auto tile_of = [&](int lt) { return (int)blockIdx.x + lt * (int)gridDim.x; };
 
   if (warp == 0) {
     // ---------------------------------------------------------------- MMA issue
@@ -823,6 +841,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) pf_gemm(const __grid_constant__
 // 16-byte copies).  One k-stage of a gate_up tile's B is then one contiguous
 // block of its rows x 128 bytes.  (h uses the same layout for the down GEMM.)
 __global__ void pf_gather(const __grid_constant__ PfParams P) {
+  pdl_begin();
   const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   const int G = P.E + (P.sgate ? 1 : 0);
   if (e >= P.offs[G]) return;
@@ -870,6 +889,7 @@ __device__ __forceinline__ float from_orderable(uint32_t k) {
 constexpr int kTopkThreads = 512;
 template <int PM>
 __global__ void __launch_bounds__(kTopkThreads) pf_topk(const __grid_constant__ PfParams P) {
+  pdl_begin();
   extern __shared__ int hist[];  // [E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, c = blockIdx.x;
   const int E = P.E, K = P.K, nch = (P.t + kPfChunk - 1) / kPfChunk;
@@ -954,6 +974,7 @@ __device__ int block_exscan(int v, int *sh, int *total) {
 // in place the exclusive prefix of its chunk counts -- the place, within
 // the expert's list, of each chunk's first entry.
 __global__ void pf_group_count(const __grid_constant__ PfParams P) {
+  pdl_begin();
   const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (e >= P.E) return;
   const int nch = (P.t + kPfChunk - 1) / kPfChunk;
@@ -979,6 +1000,7 @@ __global__ void pf_group_count(const __grid_constant__ PfParams P) {
 // kPfTileN-token chunk counts give the group offsets and the chunk offsets
 // (the tile work lists are written from them by pf_fill's blocks).
 __global__ void __launch_bounds__(1024) pf_group(const __grid_constant__ PfParams P) {
+  pdl_begin();
   __shared__ int s_off[1027], s_ch[1027], sh[32];
   const int E = P.E, G = E + (P.sgate ? 1 : 0);
   const int nmt1 = P.I / 64, nmt2 = P.H / 128;
@@ -1018,6 +1040,7 @@ __global__ void __launch_bounds__(1024) pf_group(const __grid_constant__ PfParam
 // found by a binary search over the chunk offsets.
 constexpr int kFillThreads = 128;
 __global__ void __launch_bounds__(kFillThreads) pf_fill(const __grid_constant__ PfParams P) {
+  pdl_begin();
   extern __shared__ uint64_t fsm[];  // [G + 1] group records, then int [E] cnt, [G + 1] chunk and row offsets
   const int G = P.E + (P.sgate ? 1 : 0);
   uint64_t *srec = fsm;
@@ -1095,6 +1118,7 @@ __global__ void __launch_bounds__(kFillThreads) pf_fill(const __grid_constant__ 
 // out = bf16(Y (+ x)): four elements a thread per step when out is 8-byte
 // aligned (x and Y always are; H is a multiple of 128), else one.
 __global__ void pf_final(const __grid_constant__ PfParams P) {
+  pdl_begin();
   const size_t n = (size_t)P.t * P.H, stride = (size_t)gridDim.x * blockDim.x;
   const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const bool res = (P.flags & kResidualF) != 0;
@@ -1241,6 +1265,24 @@ int pf_tensor_maps(PfParams &p, const char **why) {
   return 0;
 }
 
+// A kernel of the chain after the first: it may launch while the previous
+// one ends (programmatic dependent launch; the kernel waits for it with
+// griddepcontrol.wait before reading its results).
+template <class K>
+cudaError_t launch_after(K kernel, int grid, int block, size_t smem, cudaStream_t st, const PfParams &p) {
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   const int t = p.t, nch = (t + kPfChunk - 1) / kPfChunk;
   const size_t ent_cap = (size_t)t * (p.K + 1);
@@ -1267,38 +1309,32 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if ((e = mark(0))) return e;
   pf_prep<<<t, 256, 0, st>>>(p);
   if ((e = mark(1))) return e;
-  pf_gemm<MODE_ROUTER><<<g_router, kWsThreads, Lay<MODE_ROUTER>::smem, st>>>(p);
+  if ((e = launch_after(pf_gemm<MODE_ROUTER>, g_router, kWsThreads, Lay<MODE_ROUTER>::smem, st, p))) return e;
   if ((e = mark(2))) return e;
+  const size_t hs = (size_t)p.E * 4;
   if (p.E <= 128)
-    pf_topk<4><<<nch, kTopkThreads, (size_t)p.E * 4, st>>>(p);
+    e = launch_after(pf_topk<4>, nch, kTopkThreads, hs, st, p);
   else if (p.E <= 256)
-    pf_topk<8><<<nch, kTopkThreads, (size_t)p.E * 4, st>>>(p);
+    e = launch_after(pf_topk<8>, nch, kTopkThreads, hs, st, p);
   else if (p.E <= 512)
-    pf_topk<16><<<nch, kTopkThreads, (size_t)p.E * 4, st>>>(p);
+    e = launch_after(pf_topk<16>, nch, kTopkThreads, hs, st, p);
   else
-    pf_topk<32><<<nch, kTopkThreads, (size_t)p.E * 4, st>>>(p);
-  if ((e = mark(3))) return e;
-  pf_group_count<<<(p.E + 7) / 8, 256, 0, st>>>(p);
-  if ((e = mark(4))) return e;
-  pf_group<<<1, 1024, 0, st>>>(p);
-  if ((e = mark(5))) return e;
-  pf_fill<<<nch, kFillThreads, (size_t)(p.E + 2) * 8 + (size_t)(3 * p.E + 6) * 4, st>>>(p);
-  if ((e = mark(6))) return e;
+    e = launch_after(pf_topk<32>, nch, kTopkThreads, hs, st, p);
+  if (e || (e = mark(3))) return e;
+  if ((e = launch_after(pf_group_count, (p.E + 7) / 8, 256, 0, st, p)) || (e = mark(4))) return e;
+  if ((e = launch_after(pf_group, 1, 1024, 0, st, p)) || (e = mark(5))) return e;
+  if ((e = launch_after(pf_fill, nch, kFillThreads, (size_t)(p.E + 2) * 8 + (size_t)(3 * p.E + 6) * 4, st, p)) ||
+      (e = mark(6)))
+    return e;
   if (!p.route_only) {
-    pf_gather<<<(int)((ent_cap + 7) / 8), 256, 0, st>>>(p);
-    if ((e = mark(7))) return e;
-    if (p.bits == 4)
-      pf_gemm<MODE_GATE_UP><<<p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st>>>(p);
-    else
-      pf_gemm<MODE_GATE_UP, true><<<p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st>>>(p);
-    if ((e = mark(8))) return e;
-    if (p.bits == 4)
-      pf_gemm<MODE_DOWN><<<p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st>>>(p);
-    else
-      pf_gemm<MODE_DOWN, true><<<p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st>>>(p);
-    if ((e = mark(9))) return e;
-    pf_final<<<1024, 256, 0, st>>>(p);
-    if ((e = mark(10))) return e;
+    if ((e = launch_after(pf_gather, (int)((ent_cap + 7) / 8), 256, 0, st, p)) || (e = mark(7))) return e;
+    e = p.bits == 4 ? launch_after(pf_gemm<MODE_GATE_UP>, p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st, p)
+                    : launch_after(pf_gemm<MODE_GATE_UP, true>, p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st, p);
+    if (e || (e = mark(8))) return e;
+    e = p.bits == 4 ? launch_after(pf_gemm<MODE_DOWN>, p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st, p)
+                    : launch_after(pf_gemm<MODE_DOWN, true>, p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st, p);
+    if (e || (e = mark(9))) return e;
+    if ((e = launch_after(pf_final, 1024, 256, 0, st, p)) || (e = mark(10))) return e;
   }
   return cudaGetLastError();
 }
