@@ -1265,11 +1265,13 @@ int pf_tensor_maps(PfParams &p, const char **why) {
   return 0;
 }
 
-// A kernel of the chain after the first: it may launch while the previous
-// one ends (programmatic dependent launch; the kernel waits for it with
-// griddepcontrol.wait before reading its results).
+// A kernel of the chain after the first.  pdl: it may launch while the
+// previous one ends (programmatic dependent launch; the kernel waits for it
+// with griddepcontrol.wait before reading its results).  Only between two
+// kernels: with an event recorded between them (the timed call) the launch
+// keeps plain stream order, and griddepcontrol.wait has nothing to wait for.
 template <class K>
-cudaError_t launch_after(K kernel, int grid, int block, size_t smem, cudaStream_t st, const PfParams &p) {
+cudaError_t launch_after(K kernel, int grid, int block, size_t smem, cudaStream_t st, bool pdl, const PfParams &p) {
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
@@ -1279,7 +1281,7 @@ cudaError_t launch_after(K kernel, int grid, int block, size_t smem, cudaStream_
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 
@@ -1288,6 +1290,7 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   const size_t ent_cap = (size_t)t * (p.K + 1);
   cudaError_t e;
   auto mark = [&](int i) { return events ? cudaEventRecord(events[i], st) : cudaSuccess; };
+  const bool pdl = events == nullptr;
   if ((e = cudaMemsetAsync(p.status, 0, 4, st))) return e;
   if (!p.route_only && (e = cudaMemsetAsync(p.Y, 0, (size_t)t * p.H * 4, st))) return e;
   if ((e = cudaFuncSetAttribute(pf_gemm<MODE_ROUTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1309,32 +1312,32 @@ cudaError_t pf_launch(PfParams &p, cudaStream_t st, cudaEvent_t const *events) {
   if ((e = mark(0))) return e;
   pf_prep<<<t, 256, 0, st>>>(p);
   if ((e = mark(1))) return e;
-  if ((e = launch_after(pf_gemm<MODE_ROUTER>, g_router, kWsThreads, Lay<MODE_ROUTER>::smem, st, p))) return e;
+  if ((e = launch_after(pf_gemm<MODE_ROUTER>, g_router, kWsThreads, Lay<MODE_ROUTER>::smem, st, pdl, p))) return e;
   if ((e = mark(2))) return e;
   const size_t hs = (size_t)p.E * 4;
   if (p.E <= 128)
-    e = launch_after(pf_topk<4>, nch, kTopkThreads, hs, st, p);
+    e = launch_after(pf_topk<4>, nch, kTopkThreads, hs, st, pdl, p);
   else if (p.E <= 256)
-    e = launch_after(pf_topk<8>, nch, kTopkThreads, hs, st, p);
+    e = launch_after(pf_topk<8>, nch, kTopkThreads, hs, st, pdl, p);
   else if (p.E <= 512)
-    e = launch_after(pf_topk<16>, nch, kTopkThreads, hs, st, p);
+    e = launch_after(pf_topk<16>, nch, kTopkThreads, hs, st, pdl, p);
   else
-    e = launch_after(pf_topk<32>, nch, kTopkThreads, hs, st, p);
+    e = launch_after(pf_topk<32>, nch, kTopkThreads, hs, st, pdl, p);
   if (e || (e = mark(3))) return e;
-  if ((e = launch_after(pf_group_count, (p.E + 7) / 8, 256, 0, st, p)) || (e = mark(4))) return e;
-  if ((e = launch_after(pf_group, 1, 1024, 0, st, p)) || (e = mark(5))) return e;
-  if ((e = launch_after(pf_fill, nch, kFillThreads, (size_t)(p.E + 2) * 8 + (size_t)(3 * p.E + 6) * 4, st, p)) ||
+  if ((e = launch_after(pf_group_count, (p.E + 7) / 8, 256, 0, st, pdl, p)) || (e = mark(4))) return e;
+  if ((e = launch_after(pf_group, 1, 1024, 0, st, pdl, p)) || (e = mark(5))) return e;
+  if ((e = launch_after(pf_fill, nch, kFillThreads, (size_t)(p.E + 2) * 8 + (size_t)(3 * p.E + 6) * 4, st, pdl, p)) ||
       (e = mark(6)))
     return e;
   if (!p.route_only) {
-    if ((e = launch_after(pf_gather, (int)((ent_cap + 7) / 8), 256, 0, st, p)) || (e = mark(7))) return e;
-    e = p.bits == 4 ? launch_after(pf_gemm<MODE_GATE_UP>, p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st, p)
-                    : launch_after(pf_gemm<MODE_GATE_UP, true>, p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st, p);
+    if ((e = launch_after(pf_gather, (int)((ent_cap + 7) / 8), 256, 0, st, pdl, p)) || (e = mark(7))) return e;
+    e = p.bits == 4 ? launch_after(pf_gemm<MODE_GATE_UP>, p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st, pdl, p)
+                    : launch_after(pf_gemm<MODE_GATE_UP, true>, p.n_sms, kWsThreads, Lay<MODE_GATE_UP>::smem, st, pdl, p);
     if (e || (e = mark(8))) return e;
-    e = p.bits == 4 ? launch_after(pf_gemm<MODE_DOWN>, p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st, p)
-                    : launch_after(pf_gemm<MODE_DOWN, true>, p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st, p);
+    e = p.bits == 4 ? launch_after(pf_gemm<MODE_DOWN>, p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st, pdl, p)
+                    : launch_after(pf_gemm<MODE_DOWN, true>, p.n_sms, kWsThreads, Lay<MODE_DOWN>::smem, st, pdl, p);
     if (e || (e = mark(9))) return e;
-    if ((e = launch_after(pf_final, 1024, 256, 0, st, p)) || (e = mark(10))) return e;
+    if ((e = launch_after(pf_final, 1024, 256, 0, st, pdl, p)) || (e = mark(10))) return e;
   }
   return cudaGetLastError();
 }
