@@ -210,10 +210,9 @@ int run(const moe_layer *layers, int nl, const float *x, int nb, float *out, voi
   if (moe::decode_plan(dev, p, &grid, &smem) != 0)
     return fail(MOE_ECUDA, "decode kernel cannot be resident on this device (hidden %d, experts %d)", H, E);
   cudaStream_t st = (cudaStream_t)stream;
-  // counters and the logit exchange words start at zero every call (they are adjacent)
-  cudaError_t e = cudaMemsetAsync(p.cnt, 0, w.xbuf - w.cnt, st);
-  if (e == cudaSuccess) e = cudaMemsetAsync(status, 0, sizeof(int), st);
-  if (e == cudaSuccess) e = moe::launch_decode(p, grid, smem, st);
+  // counters and the logit exchange words (adjacent) and the status start at
+  // zero every call: a small kernel clears them, the decode kernel follows it
+  cudaError_t e = moe::launch_decode(p, grid, smem, st, (size_t)(w.xbuf - w.cnt));
   if (e != cudaSuccess) return fail(MOE_ECUDA, "launch failed: %s", cudaGetErrorString(e));
   return MOE_OK;
 }

@@ -945,6 +945,9 @@ __device__ __forceinline__ bool lookahead_on(const FwdParams &P, int l, int G) {
 // it carries none of the lookahead's code).
 template <int BITS, bool LA>
 __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ FwdParams P) {
+  // launched as a programmatic dependent of zero_call: wait for the zeroed
+  // counters and status before anything else
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   extern __shared__ __align__(128) unsigned char sm[];
   const int H = P.H, E = P.E, K = P.K, I = P.I, nb = P.nb;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1505,6 +1508,16 @@ int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes) {
   return 0;
 }
 
+// Start of a call: the counters and logit exchange words (n16 16-byte
+// units) and the status word to zero.  The decode kernel that follows may
+// launch at once and waits for this one with griddepcontrol.wait.
+__global__ void zero_call(uint4 *cnt, size_t n16, int *status) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x)
+    cnt[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (blockIdx.x == 0 && threadIdx.x == 0) *status = 0;
+}
+
 template <int BITS, bool LA>
 static cudaError_t launch_t(const FwdParams &p, int grid, int smem, cudaStream_t st) {
   cudaLaunchConfig_t cfg = {};
@@ -1512,11 +1525,13 @@ static cudaError_t launch_t(const FwdParams &p, int grid, int smem, cudaStream_t
   cfg.blockDim = dim3(NT);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, decode_kernel<BITS, LA>, p);
 }
 
@@ -1531,7 +1546,12 @@ static cudaError_t launch_b(const FwdParams &p, int grid, int smem, cudaStream_t
   }
 }
 
-cudaError_t launch_decode(const FwdParams &p, int grid, int smem, cudaStream_t st) {
+cudaError_t launch_decode(const FwdParams &p, int grid, int smem, cudaStream_t st, size_t zero_bytes) {
+  const size_t n16 = zero_bytes / 16, blocks = (n16 + 255) / 256;
+  zero_call<<<(int)(blocks < 1 ? 1 : blocks > 1024 ? 1024 : blocks), 256, 0, st>>>(reinterpret_cast<uint4 *>(p.cnt), n16,
+                                                                                   p.status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
   return p.lookahead ? launch_b<true>(p, grid, smem, st) : launch_b<false>(p, grid, smem, st);
 }
 

@@ -72,6 +72,7 @@ constexpr int kTracePhases = 16;
 // Fills p.stages / p.stage_bytes and the grid for this device; returns 0 or -1.
 // The grid is one CTA per SM, at most kMaxGrid.
 int decode_plan(int device, FwdParams &p, int *grid, int *smem_bytes);
-cudaError_t launch_decode(const FwdParams &p, int grid, int smem_bytes, cudaStream_t st);
+// zero_bytes: the counters and logit exchange words from p.cnt (a multiple of 16), zeroed first with *p.status
+cudaError_t launch_decode(const FwdParams &p, int grid, int smem_bytes, cudaStream_t st, size_t zero_bytes);
 
 }  // namespace moe
